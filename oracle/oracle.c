@@ -1,0 +1,497 @@
+/*
+ * ORACLE -- test infrastructure, not the product.
+ *
+ * A plain, slow CPU statement of what the quantised-linear hot path computes.
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline /
+ * reference arm may load this library.  It shares no code with the CUDA
+ * library; both sides only receive the same seeded inputs from `synth`.
+ *
+ * Sources (web pages; section names as printed on them):
+ *   [gemma.cpp tour]  pyshine.com "gemma.cpp" -- "Weights, Blobs, and the .sbs
+ *                     Format", "The Forward Pass, Layer by Layer".
+ *   [cpp20gemma]      README -- "Architecture & implementation", "Tests".
+ *   [llama2.c]        "llama2.c -- Llama-2 Inference in One C File" -- "The
+ *                     forward pass -- one token, one position" (Steps 0-6),
+ *                     "matmul", "Sampling", "The generation loop".
+ *   [citric]          "Gemma 3 1B at 114 tokens per second on a laptop CPU" --
+ *                     "On a CPU, speed is bytes", "Step 1: a kernel for 1.6-bit
+ *                     weights", "Step 2: making a ternary Gemma".
+ *
+ * Precision: integer work is exact (int64 accumulators).  Plain linear maps
+ * with no quantiser downstream (W8 linear, lm_head logits) accumulate in
+ * fp64 and round once.  Everything that feeds an activation quantiser in the
+ * decode step is defined in fp32 with a fixed operation order (pairwise sums,
+ * a Cody-Waite exponential), because a one-ulp change in front of an int8
+ * rounding changes a code and then every later token; see the readings in
+ * the design notes.  Compile with -ffp-contract=off.
+ *
+ * Parity pins: every function here is pinned by tests under tests/ against
+ * closed forms, hand-worked vectors, brute force or fp64 references.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_OK 0
+#define OR_EINVAL 1
+#define OR_EBADBYTE 3
+
+static const int32_t POW3[5] = {1, 3, 9, 27, 81};
+
+/* ------------------------------------------------------------------ S1 / S3
+ * Symmetric absmax int8 quantisation, [cpp20gemma] "Architecture &
+ * implementation": scale = max(|w|, 1e-9)/127, w8 = clip(round(w/scale)).
+ * Readings: division in fp32, round half to even (NumPy's round, which the
+ * converter script uses), clip to +-127 (the -128 end of the page's clip is
+ * unreachable because |w/scale| <= 127).  The same rule quantises activations
+ * per row ([citric] "Step 2": inputs to each layer rounded to int8;
+ * [llama2.c] "Key ideas": activations quantised dynamically, range +-127).
+ */
+static float absmax_scale(const float *v, int64_t n) {
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; i++) {
+        float a = fabsf(v[i]);
+        if (a > m) m = a;
+    }
+    if (m < 1e-9f) m = 1e-9f;
+    return m / 127.0f;
+}
+
+static int8_t quant_one(float v, float scale) {
+    float r = rintf(v / scale); /* default rounding mode: nearest, ties to even */
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    return (int8_t)r;
+}
+
+int or_w8_quantize(const float *w, int64_t n, int8_t *q, float *scale) {
+    if (!w || !q || !scale || n < 1) return OR_EINVAL;
+    float s = absmax_scale(w, n);
+    for (int64_t i = 0; i < n; i++) q[i] = quant_one(w[i], s);
+    *scale = s;
+    return OR_OK;
+}
+
+int or_quant_i8(const float *x, int64_t M, int64_t K, int8_t *xq, float *xs) {
+    if (!x || !xq || !xs || M < 1 || K < 1) return OR_EINVAL;
+    for (int64_t m = 0; m < M; m++) {
+        float s = absmax_scale(x + m * K, K);
+        for (int64_t k = 0; k < K; k++) xq[m * K + k] = quant_one(x[m * K + k], s);
+        xs[m] = s;
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ S5
+ * W8 linear: y = (x . w8) * scale, the scale applied once after the dot
+ * product ([cpp20gemma] "Architecture & implementation"); rows of w8 are
+ * [out][in] row-major; [llama2.c] "matmul" is the same loop over output rows.
+ * Accumulated in fp64, rounded once to fp32.
+ */
+int or_w8_linear(const float *x, const int8_t *q, int64_t q_pitch, float s, int64_t M, int64_t N,
+                 int64_t K, float *y) {
+    if (!x || !q || !y || M < 1 || N < 1 || K < 1 || q_pitch < K) return OR_EINVAL;
+    for (int64_t m = 0; m < M; m++) {
+#pragma omp parallel for schedule(static)
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; k++) acc += (double)x[m * K + k] * (double)q[n * q_pitch + k];
+            y[m * N + n] = (float)(acc * (double)s);
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ S2
+ * T158 packing, [citric] "Step 1": five ternary weights per byte in base 3
+ * (3^5 = 243 <= 256).  Digit order and row layout are not on the page; the
+ * adopted reading: digit d_i = trit_{5j+i} + 1, byte j = sum_i d_i * 3^i
+ * (least significant digit first), each row of a [N][K] matrix packed on its
+ * own into `pitch` bytes; trits past K are zero trits (digit 1), so every byte
+ * past ceil(K/5) is 121.
+ */
+int or_t158_pack(const int8_t *t, int64_t N, int64_t K, uint8_t *packed, int64_t pitch) {
+    if (!t || !packed || N < 1 || K < 1 || pitch < (K + 4) / 5) return OR_EINVAL;
+    for (int64_t i = 0; i < N * K; i++)
+        if (t[i] < -1 || t[i] > 1) return OR_EINVAL;
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t j = 0; j < pitch; j++) {
+            int32_t byte = 0;
+            for (int i = 0; i < 5; i++) {
+                int64_t k = 5 * j + i;
+                int32_t digit = (k < K) ? (int32_t)t[n * K + k] + 1 : 1;
+                byte += digit * POW3[i];
+            }
+            packed[n * pitch + j] = (uint8_t)byte;
+        }
+    }
+    return OR_OK;
+}
+
+/* Digit i (0..4) of a packed byte, as the trit it encodes. */
+static int32_t trit_of(uint8_t byte, int i) { return ((int32_t)byte / POW3[i]) % 3 - 1; }
+
+int or_t158_unpack(const uint8_t *packed, int64_t N, int64_t K, int64_t pitch, int8_t *t) {
+    if (!packed || !t || N < 1 || K < 1 || pitch < (K + 4) / 5) return OR_EINVAL;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t j = 0; j < pitch; j++)
+            if (packed[n * pitch + j] > 242) return OR_EBADBYTE;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++) t[n * K + k] = (int8_t)trit_of(packed[n * pitch + k / 5], (int)(k % 5));
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ S4 / S6
+ * T158 linear: acc[m][n] = sum_k trit[n][k] * xq[m][k], exact integer
+ * arithmetic ([citric] "Step 1": results do not depend on thread count or
+ * batch), then y = ((float)acc * w_scale) * x_scale in fp32, left to right
+ * (one scale per matrix, [citric] "Step 2"; scale applied after the dot
+ * product, [cpp20gemma]).  (float)acc is exact because |acc| < 2^24 for the
+ * shapes in use; the function reports EINVAL otherwise.
+ */
+int or_t158_linear(const int8_t *xq, const float *xs, const uint8_t *packed, int64_t pitch, float ws,
+                   int64_t M, int64_t N, int64_t K, int32_t *acc_out, float *y) {
+    if (!xq || !xs || !packed || M < 1 || N < 1 || K < 1 || pitch < (K + 4) / 5) return OR_EINVAL;
+    if (127 * K >= (1 << 24)) return OR_EINVAL;
+    for (int64_t m = 0; m < M; m++) {
+#pragma omp parallel for schedule(static)
+        for (int64_t n = 0; n < N; n++) {
+            int64_t acc = 0;
+            for (int64_t k = 0; k < K; k++)
+                acc += (int64_t)trit_of(packed[n * pitch + k / 5], (int)(k % 5)) * (int64_t)xq[m * K + k];
+            if (acc_out) acc_out[m * N + n] = (int32_t)acc;
+            if (y) y[m * N + n] = ((float)acc * ws) * xs[m];
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ fp32 building blocks
+ * Pairwise summation (Higham, "The accuracy of floating point summation",
+ * SIAM J. Sci. Comput. 1993): the n terms are padded with zeros to the next
+ * power of two P and summed as a balanced binary tree, sum(a[0:P]) =
+ * sum(a[0:P/2]) + sum(a[P/2:P]).  This fixes the fp32 rounding of every sum
+ * that feeds a quantiser.
+ */
+static int64_t next_pow2(int64_t n) {
+    int64_t p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+
+float or_psum_f32(const float *a, int64_t n) {
+    if (n <= 0) return 0.0f;
+    int64_t P = next_pow2(n);
+    float *b = (float *)malloc((size_t)P * sizeof(float));
+    for (int64_t i = 0; i < P; i++) b[i] = (i < n) ? a[i] : 0.0f;
+    for (int64_t len = P; len > 1; len >>= 1)
+        for (int64_t i = 0; i < len / 2; i++) b[i] = b[2 * i] + b[2 * i + 1];
+    float r = b[0];
+    free(b);
+    return r;
+}
+
+/* exp in fp32: Cody-Waite argument reduction (Cody & Waite, "Software Manual
+ * for the Elementary Functions", 1980) x = n ln2 + r with ln2 split into a
+ * short high part and a low part, then the degree-7 Taylor polynomial of e^r
+ * in Horner form with fused multiply-adds, then an exact scaling by 2^n
+ * (two power-of-two multiplies below the normal range, so the one rounding
+ * into subnormals is the IEEE one).  |r| <= 0.35, so the truncation error is
+ * below 6e-9 relative. */
+static float pow2i(int e) { /* 2^e for -126 <= e <= 127 */
+    uint32_t u = (uint32_t)(e + 127) << 23;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+float or_exp_f32(float x) {
+    if (x != x) return x;
+    if (x > 88.72283935546875f) return INFINITY;
+    if (x < -103.972084045410156f) return 0.0f;
+    const float LOG2E = 1.44269502162933349609375f; /* log2(e) rounded to fp32 */
+    const float LN2_HI = 0.693145751953125f;          /* 0x3F317200: ln2 with 9 low zero bits */
+    const float LN2_LO = 1.4286068203094172321e-06f;  /* ln2 - LN2_HI */
+    float n = rintf(x * LOG2E);
+    float r = fmaf(-n, LN2_HI, x);
+    r = fmaf(-n, LN2_LO, r);
+    float p = 1.0f / 5040.0f;
+    p = fmaf(p, r, 1.0f / 720.0f);
+    p = fmaf(p, r, 1.0f / 120.0f);
+    p = fmaf(p, r, 1.0f / 24.0f);
+    p = fmaf(p, r, 1.0f / 6.0f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    int e = (int)n;
+    if (e > 127) return (p * pow2i(127)) * 2.0f;
+    if (e < -126) return (p * pow2i(e + 64)) * pow2i(-64);
+    return p * pow2i(e);
+}
+
+/* tanh(z) = 1 - 2 / (e^{2z} + 1), with the exp above. */
+float or_tanh_f32(float z) {
+    float e = or_exp_f32(2.0f * z);
+    return 1.0f - 2.0f / (e + 1.0f);
+}
+
+/* GELU, tanh form (the form Gemma uses; the pages only say "GeLU"/"GeGLU"):
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), fp32, in this order. */
+float or_gelu_f32(float x) {
+    float x3 = (x * x) * x;
+    float inner = x + 0.044715f * x3;
+    float z = 0.7978845608028654f * inner;
+    float t = or_tanh_f32(z);
+    return (0.5f * x) * (1.0f + t);
+}
+
+/* ------------------------------------------------------------------ S9
+ * RMSNorm, [llama2.c] Step 1: o = w * (x / sqrt(mean(x^2) + eps)), computed
+ * as ss = sum x^2 (pairwise); ss = ss/n + eps; r = 1/sqrtf(ss); o = g*(r*x).
+ */
+void or_rmsnorm(const float *x, const float *g, int64_t n, float eps, float *o) {
+    float *sq = (float *)malloc((size_t)n * sizeof(float));
+    for (int64_t i = 0; i < n; i++) sq[i] = x[i] * x[i];
+    float ss = or_psum_f32(sq, n);
+    free(sq);
+    ss = ss / (float)n;
+    ss = ss + eps;
+    float r = 1.0f / sqrtf(ss);
+    for (int64_t i = 0; i < n; i++) o[i] = g[i] * (r * x[i]);
+}
+
+/* ------------------------------------------------------------------ S11
+ * RoPE.  Frequencies as in [llama2.c] Step 2: theta_i = base^(-2i/head_dim),
+ * angle = pos * theta_i, in double, cos/sin rounded to fp32.  Pairing (i,
+ * i + head_dim/2), the Gemma convention of [gemma.cpp tour] "The Forward
+ * Pass"; k is rotated before it is cached ([cpp20gemma]).  Rotation in fp32,
+ * each product rounded, then added:  x' = x c - y s,  y' = x s + y c.
+ */
+void or_rope_table(int64_t n_pos, int64_t head_dim, double base, float *cos_t, float *sin_t) {
+    int64_t half = head_dim / 2;
+    for (int64_t p = 0; p < n_pos; p++)
+        for (int64_t i = 0; i < half; i++) {
+            double theta = pow(base, -(double)(2 * i) / (double)head_dim);
+            double ang = (double)p * theta;
+            cos_t[p * half + i] = (float)cos(ang);
+            sin_t[p * half + i] = (float)sin(ang);
+        }
+}
+
+void or_rope_apply(float *x, int64_t n_heads, int64_t head_dim, const float *c, const float *s) {
+    int64_t half = head_dim / 2;
+    for (int64_t h = 0; h < n_heads; h++) {
+        float *v = x + h * head_dim;
+        for (int64_t i = 0; i < half; i++) {
+            float a = v[i], b = v[i + half];
+            float ac = a * c[i], bs = b * s[i], as = a * s[i], bc = b * c[i];
+            v[i] = ac - bs;
+            v[i + half] = as + bc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ S12
+ * Decode attention, [llama2.c] Step 4: for each query head h (KV head
+ * h / (n_heads/n_kv), the GQA rule), score_t = q.k_t / sqrt(head_dim) for
+ * t <= pos, softmax with the maximum subtracted, out = sum_t p_t v_t.
+ * Reading (fp32 order): dot products are pairwise sums of the rounded
+ * products; positions are taken in chunks of ATT_CHUNK and the softmax is
+ * assembled from per-chunk maxima and sums (the online-softmax identity
+ * e^{s-m} = e^{s-m_c} e^{m_c-m}), all sums pairwise; out = U / S.
+ * Mathematically this is the page's softmax; the fixed grouping fixes the
+ * rounding.
+ */
+#define ATT_CHUNK 32
+
+void or_attention(const float *q, const float *kc, const float *vc, int64_t pos, int64_t n_heads,
+                  int64_t n_kv, int64_t head_dim, float *out) {
+    int64_t kv_dim = n_kv * head_dim;
+    int64_t kv_mul = n_heads / n_kv;
+    int64_t T = pos + 1;
+    int64_t nc = (T + ATT_CHUNK - 1) / ATT_CHUNK;
+    float scale_div = sqrtf((float)head_dim);
+    float *prod = (float *)malloc((size_t)head_dim * sizeof(float));
+    float *s = (float *)malloc((size_t)(nc * ATT_CHUNK) * sizeof(float));
+    float *mc = (float *)malloc((size_t)nc * sizeof(float));
+    float *Sc = (float *)malloc((size_t)nc * sizeof(float));
+    float *Uc = (float *)malloc((size_t)(nc * head_dim) * sizeof(float));
+    float *tmp = (float *)malloc((size_t)(nc > ATT_CHUNK ? nc : ATT_CHUNK) * sizeof(float));
+    for (int64_t h = 0; h < n_heads; h++) {
+        const float *qh = q + h * head_dim;
+        int64_t kvh = h / kv_mul;
+        for (int64_t t = 0; t < T; t++) {
+            const float *k = kc + t * kv_dim + kvh * head_dim;
+            for (int64_t i = 0; i < head_dim; i++) prod[i] = qh[i] * k[i];
+            s[t] = or_psum_f32(prod, head_dim) / scale_div;
+        }
+        for (int64_t c = 0; c < nc; c++) {
+            int64_t t0 = c * ATT_CHUNK, t1 = t0 + ATT_CHUNK < T ? t0 + ATT_CHUNK : T;
+            float m = s[t0];
+            for (int64_t t = t0 + 1; t < t1; t++)
+                if (s[t] > m) m = s[t];
+            mc[c] = m;
+            float e[ATT_CHUNK];
+            for (int64_t t = t0; t < t1; t++) e[t - t0] = or_exp_f32(s[t] - m);
+            Sc[c] = or_psum_f32(e, t1 - t0);
+            for (int64_t i = 0; i < head_dim; i++) {
+                for (int64_t t = t0; t < t1; t++) tmp[t - t0] = e[t - t0] * vc[t * kv_dim + kvh * head_dim + i];
+                Uc[c * head_dim + i] = or_psum_f32(tmp, t1 - t0);
+            }
+        }
+        float m = mc[0];
+        for (int64_t c = 1; c < nc; c++)
+            if (mc[c] > m) m = mc[c];
+        float *w = (float *)malloc((size_t)nc * sizeof(float));
+        for (int64_t c = 0; c < nc; c++) w[c] = or_exp_f32(mc[c] - m);
+        for (int64_t c = 0; c < nc; c++) tmp[c] = Sc[c] * w[c];
+        float S = or_psum_f32(tmp, nc);
+        for (int64_t i = 0; i < head_dim; i++) {
+            for (int64_t c = 0; c < nc; c++) tmp[c] = Uc[c * head_dim + i] * w[c];
+            out[h * head_dim + i] = or_psum_f32(tmp, nc) / S;
+        }
+        free(w);
+    }
+    free(prod);
+    free(s);
+    free(mc);
+    free(Sc);
+    free(Uc);
+    free(tmp);
+}
+
+/* ------------------------------------------------------------------ S8 .. S16: decode step
+ * Pre-norm residual block of [cpp20gemma] "Architecture & implementation"
+ * (h += attn(rmsnorm(h)); h += mlp(rmsnorm(h)); logits = lm_head(rmsnorm(h)))
+ * in the order of [llama2.c] "The forward pass", with every linear layer a
+ * T158 linear on int8-quantised inputs ([citric] "Step 2") and a GeGLU MLP
+ * (down(gelu(gate x) * (up x)), [gemma.cpp tour], [cpp20gemma]).  No position
+ * bias (zeros per [cpp20gemma] "Real Gemma weights"), embedding kept in bf16
+ * and tied to the lm_head ([citric] "Step 2"; [llama2.c] "four structs").
+ */
+typedef struct {
+    int64_t n_layers, dim, n_heads, n_kv_heads, head_dim, ffn, vocab, max_pos;
+    float eps;
+    double rope_base;
+    const uint8_t *w[7]; /* wq wk wv wo wg wu wd, each [L][N][pitch] */
+    int64_t pitch[7];
+    const float *scales; /* [L][7] */
+    const float *g_attn, *g_ffn, *g_final; /* [L][dim], [L][dim], [dim] */
+    const uint16_t *emb;                   /* bf16 bits [vocab][dim] */
+} or_model;
+
+static float bf16f(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+static void mat_dims(const or_model *m, int j, int64_t *N, int64_t *K) {
+    int64_t d = m->dim, q = m->n_heads * m->head_dim, kv = m->n_kv_heads * m->head_dim, f = m->ffn;
+    static const int rows_sel[7] = {0, 1, 1, 2, 3, 3, 2}; /* 0:q 1:kv 2:d 3:f */
+    static const int cols_sel[7] = {2, 2, 2, 0, 2, 2, 3};
+    int64_t v[4] = {q, kv, d, f};
+    *N = v[rows_sel[j]];
+    *K = v[cols_sel[j]];
+}
+
+static void t158_layer(const or_model *m, int l, int j, const float *x, int8_t *xq, float *y) {
+    int64_t N, K;
+    mat_dims(m, j, &N, &K);
+    float xs;
+    or_quant_i8(x, 1, K, xq, &xs);
+    const uint8_t *w = m->w[j] + (int64_t)l * N * m->pitch[j];
+    or_t158_linear(xq, &xs, w, m->pitch[j], m->scales[l * 7 + j], 1, N, K, NULL, y);
+}
+
+/* One forward step at position pos: writes rotated k and v into the cache
+ * [L][2][max_pos][kv_dim], fp32 logits [vocab] (may be NULL) and the greedy
+ * token ([llama2.c] "Sampling": first maximum wins).  logits are fp64 sums
+ * rounded to fp32. */
+int or_decode_step(const or_model *m, float *kv, int32_t token, int64_t pos, float *logits, int32_t *next) {
+    if (!m || !kv || pos < 0 || pos >= m->max_pos || token < 0 || token >= m->vocab) return OR_EINVAL;
+    int64_t d = m->dim, qd = m->n_heads * m->head_dim, kvd = m->n_kv_heads * m->head_dim, f = m->ffn;
+    int64_t half = m->head_dim / 2;
+    int64_t big = f > qd ? f : qd;
+    if (d > big) big = d;
+    float *h = (float *)malloc((size_t)d * 4), *xn = (float *)malloc((size_t)d * 4);
+    float *q = (float *)malloc((size_t)qd * 4), *k = (float *)malloc((size_t)kvd * 4);
+    float *v = (float *)malloc((size_t)kvd * 4), *att = (float *)malloc((size_t)qd * 4);
+    float *y = (float *)malloc((size_t)big * 4), *g = (float *)malloc((size_t)f * 4);
+    float *u = (float *)malloc((size_t)f * 4);
+    int8_t *xq = (int8_t *)malloc((size_t)big);
+    float *rc = (float *)malloc((size_t)half * 4), *rs = (float *)malloc((size_t)half * 4);
+    float *lg = logits ? logits : (float *)malloc((size_t)m->vocab * 4);
+
+    /* Step 0: embed */
+    for (int64_t i = 0; i < d; i++) h[i] = bf16f(m->emb[(int64_t)token * d + i]);
+    /* RoPE table row for this position */
+    for (int64_t i = 0; i < half; i++) {
+        double theta = pow(m->rope_base, -(double)(2 * i) / (double)m->head_dim);
+        double ang = (double)pos * theta;
+        rc[i] = (float)cos(ang);
+        rs[i] = (float)sin(ang);
+    }
+    for (int64_t l = 0; l < m->n_layers; l++) {
+        float *kc = kv + ((l * 2 + 0) * m->max_pos) * kvd;
+        float *vc = kv + ((l * 2 + 1) * m->max_pos) * kvd;
+        /* Step 1: RMSNorm, quantise, Q K V */
+        or_rmsnorm(h, m->g_attn + l * d, d, m->eps, xn);
+        t158_layer(m, (int)l, 0, xn, xq, q);
+        t158_layer(m, (int)l, 1, xn, xq, k);
+        t158_layer(m, (int)l, 2, xn, xq, v);
+        /* Step 2: RoPE on q and k;  Step 3: cache write */
+        or_rope_apply(q, m->n_heads, m->head_dim, rc, rs);
+        or_rope_apply(k, m->n_kv_heads, m->head_dim, rc, rs);
+        memcpy(kc + pos * kvd, k, (size_t)kvd * 4);
+        memcpy(vc + pos * kvd, v, (size_t)kvd * 4);
+        /* Step 4: attention, then output projection and residual */
+        or_attention(q, kc, vc, pos, m->n_heads, m->n_kv_heads, m->head_dim, att);
+        t158_layer(m, (int)l, 3, att, xq, y);
+        for (int64_t i = 0; i < d; i++) h[i] = h[i] + y[i];
+        /* Step 5: FFN (GeGLU) and residual */
+        or_rmsnorm(h, m->g_ffn + l * d, d, m->eps, xn);
+        t158_layer(m, (int)l, 4, xn, xq, g);
+        t158_layer(m, (int)l, 5, xn, xq, u);
+        for (int64_t i = 0; i < f; i++) g[i] = or_gelu_f32(g[i]) * u[i];
+        t158_layer(m, (int)l, 6, g, xq, y);
+        for (int64_t i = 0; i < d; i++) h[i] = h[i] + y[i];
+    }
+    /* Step 6: final norm and classifier (tied bf16 table) */
+    or_rmsnorm(h, m->g_final, d, m->eps, xn);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < m->vocab; r++) {
+        double acc = 0.0;
+        const uint16_t *e = m->emb + r * d;
+        for (int64_t i = 0; i < d; i++) acc += (double)bf16f(e[i]) * (double)xn[i];
+        lg[r] = (float)acc;
+    }
+    int32_t best = 0;
+    for (int64_t r = 1; r < m->vocab; r++)
+        if (lg[r] > lg[best]) best = (int32_t)r;
+    if (next) *next = best;
+
+    if (!logits) free(lg);
+    free(h); free(xn); free(q); free(k); free(v); free(att); free(y); free(g); free(u); free(xq);
+    free(rc); free(rs);
+    return OR_OK;
+}
+
+/* [llama2.c] "The generation loop": force-feed the prompt, then feed back
+ * the greedy token.  Runs n_steps forwards at positions start_pos ...; out
+ * receives the argmax of every forward (for prompt positions too). */
+int or_decode_generate(const or_model *m, float *kv, const int32_t *prompt, int64_t n_prompt,
+                       int64_t start_pos, int64_t n_steps, int32_t *out) {
+    if (!prompt || n_prompt < 1 || !out) return OR_EINVAL;
+    int32_t token = prompt[0];
+    for (int64_t s = 0; s < n_steps; s++) {
+        int32_t nx;
+        int rc = or_decode_step(m, kv, token, start_pos + s, NULL, &nx);
+        if (rc) return rc;
+        out[s] = nx;
+        token = (s + 1 < n_prompt) ? prompt[s + 1] : nx;
+    }
+    return OR_OK;
+}
