@@ -1,0 +1,413 @@
+"""Benchmark: ternary (T158) Gemma-3-1B-shaped decode step on GB300, plus M=1 GEMV weight GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qlin|reference] [--workload ...]
+
+Default workload ("decode"): 26 blocks, hidden 1152, 4 query heads / 1 KV head
+of 256, GeGLU 6912, vocab 262144 tied bf16 embedding, ternary weights packed
+five per byte, seeded random weights (seed 4); the KV cache is filled to
+position 1024 with seeded N(0,1) values and every step decodes one token at a
+position cycling through 1024..1087, feeding the greedy token back on the
+device.  Weights (744 MB) exceed L2 (126 MB), so every step streams from HBM.
+
+value = tokens/s over all ranks (replicas: one independent decoder per GPU).
+Also on the line: M=1 GEMV weight GB/s (T158 K=1152 N=6912 and W8 K=4096
+N=11008, rotating weight copies >= 4x L2), the roofline of the dominant
+kernel (lm_head), e2e through the C ABI with host buffers, clocks sampled
+during the timed region, and the oracle timed on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "M=1 weight GB/s (% of 8 TB/s HBM) and decode tokens/s, Gemma-3-1B-shaped"
+NOMINAL_HBM_GBS = 8000.0
+POS0, POS_SPAN = 1024, 64
+SEED = 4
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
+    p.add_argument("--workload", choices=["decode"], default="decode")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if os.environ.get("BENCH_BACKEND", "nccl") == "nccl" else "gloo")
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def allmax(v, world):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+def decode_cfg(steps, warmup):
+    import synth
+
+    return synth.DecoderConfig(max_pos=POS0 + POS_SPAN + 1, **synth.GEMMA3_1B)
+
+
+def decode_bytes(cfg, pos):
+    """Algorithmic HBM bytes of one decode step at `pos`: packed trits at the canonical
+    ceil(K/5) pitch, the bf16 lm_head table, the KV cache read (pos+1 positions, k and v), the
+    new k/v written, and the small vectors (norm gains, scales, embedding row)."""
+    w = sum(cfg.n_layers * n * ((k + 4) // 5) for _, n, k in cfg.matrices())
+    lm = cfg.vocab * cfg.dim * 2
+    kv_read = cfg.n_layers * 2 * (pos + 1) * cfg.kv_dim * 4
+    small = cfg.n_layers * (2 * cfg.dim * 4 + 7 * 4) + cfg.dim * 4 + cfg.dim * 2
+    return w + lm + kv_read + small, lm
+
+
+def run_decode(args, rank, local, world):
+    import torch
+
+    import synth
+    from weight_streaming_gemv_gb300 import qlin
+    from weight_streaming_gemv_gb300.decoder import T158Decoder
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = decode_cfg(args.steps, args.warmup)
+    weights = synth.decoder_weights(cfg, seed=SEED)
+    gpu = T158Decoder(cfg, weights, device=dev)
+    gpu.kv.copy_(torch.from_numpy(synth.kv_fill(cfg, SEED, POS0)))
+    prompt0 = int(synth.prompt_ids(SEED, 1, cfg.vocab)[0])
+    gpu.token.fill_(prompt0)
+    stream = torch.cuda.current_stream()
+    for i in range(max(args.warmup, 3)):
+        gpu.step(POS0 + i % POS_SPAN, logits=False)
+    gpu.check_status()
+
+    # ---- device-resident timed region
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        gpu.step(POS0 + i % POS_SPAN, logits=False)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    gpu.check_status()
+    ms = e0.elapsed_time(e1)
+    ms = allmax(ms, world)
+    tok_s = world * args.steps / (ms / 1e3)
+    mean_pos = POS0 + (POS_SPAN - 1) / 2.0
+    step_bytes, lm_bytes = decode_bytes(cfg, int(mean_pos))
+
+    # ---- e2e: host token in, host token out, every step through the C ABI
+    pin_in = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    pin_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    pin_in.fill_(prompt0)
+    n_e2e = max(1, min(args.steps, 500))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        gpu.token.copy_(pin_in, non_blocking=True)
+        gpu.step(POS0 + i % POS_SPAN, logits=False)
+        pin_out.copy_(gpu.token, non_blocking=True)
+        stream.synchronize()
+        pin_in.copy_(pin_out)
+    e2e_s = time.perf_counter() - t0
+    e2e_s = allmax(e2e_s, world)
+    barrier(world)
+
+    # ---- dominant kernel: lm_head (bf16 table GEMV + argmax), timed alone
+    x = torch.randn(cfg.dim, dtype=torch.float32, device=dev)
+    nxt = torch.zeros(1, dtype=torch.int32, device=dev)
+    wsb = qlin.qlin_lm_head_workspace_size(cfg.vocab)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    for _ in range(5):
+        qlin.qlin_lm_head_argmax(gpu.emb, x, cfg.vocab, cfg.dim, None, nxt, ws, wsb)
+    n_lm = 50
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(n_lm):
+        qlin.qlin_lm_head_argmax(gpu.emb, x, cfg.vocab, cfg.dim, None, nxt, ws, wsb)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    lm_ms = a0.elapsed_time(a1) / n_lm
+    lm_alg = lm_bytes + cfg.dim * 4 + 8
+    peak, peak_kind = peaks()
+    lm_gbs = lm_alg / (lm_ms / 1e3) / 1e9
+    gemv = gemv_m1(dev, stream)
+    launches_per_step = qlin.decode_step_t158_launches(gpu.model)
+    del gpu
+    torch.cuda.empty_cache()
+
+    out = {
+        "metric": METRIC,
+        "value": round(tok_s, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8 x ternary -> int32, fp32 (bf16 lm_head)",
+        "data": "synthetic (seeded random ternary weights, N(0,1) KV cache filled to 1024)",
+        "config": {
+            "workload": "decode_step_t158, Gemma-3-1B-shaped ternary decoder, context 1024-1087",
+            "n_layers": cfg.n_layers, "dim": cfg.dim, "n_heads": cfg.n_heads, "n_kv_heads": cfg.n_kv_heads,
+            "head_dim": cfg.head_dim, "ffn": cfg.ffn, "vocab": cfg.vocab, "pos": [POS0, POS0 + POS_SPAN - 1],
+            "global_batch": world, "seq_len": 1, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (744 MB of weights per step)",
+            "hbm_bytes_per_step": step_bytes,
+        },
+        "step_hbm": {
+            "achieved_gbs": round(step_bytes * args.steps / (ms / 1e3) / 1e9, 1),
+            "frac_of_8tbs": round(step_bytes * args.steps / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
+            "frac_of_peak": round(step_bytes * args.steps / (ms / 1e3) / 1e9 / peak, 4),
+        },
+        "gemv_m1": gemv,
+        "roofline": {
+            "kernel": "lm_head_kernel (+argmax_final_kernel)",
+            "bound": "hbm", "achieved": round(lm_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(lm_gbs / peak, 4), "traffic": None, "algorithmic_bytes": lm_alg,
+            "ms_per_launch": round(lm_ms, 5),
+        },
+        "e2e": {"value": round(world * n_e2e / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
+                "d2h_bytes_per_step": 4, "steps": n_e2e},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clk,
+    }
+    return out, cfg, weights
+
+
+def gemv_m1(dev, stream):
+    """M=1 GEMV weight GB/s over rotating weight copies (>= 4x L2), launched back to back."""
+    import torch
+
+    import synth
+    from weight_streaming_gemv_gb300 import qlin
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    res = {}
+    # T158, K=1152, N=6912
+    K, N = 1152, 6912
+    d = synth.t158_gemv(1, 1, K, N)
+    pitch = qlin.t158_pitch(K)
+    w1 = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+    R = int(np.ceil(4 * l2 / w1.numel()))
+    ws = w1.repeat(R, 1)  # R copies back to back
+    x = torch.from_numpy(d["x"]).to(dev)
+    xq = torch.empty((1, K), dtype=torch.int8, device=dev)
+    xs = torch.empty(1, dtype=torch.float32, device=dev)
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    qlin.qlin_quant_i8(x, xq, xs, 1, K)
+    alg = N * ((K + 4) // 5) + K + 4 + N * 4
+
+    def t158(r):
+        qlin.qlin_t158_i8(xq, xs, ws[r * N], pitch, d["w_scale"], y, None, 1, N, K)
+
+    res["t158_k1152_n6912"] = _time_rotating(t158, R, alg, stream)
+    del ws
+    # W8, K=4096, N=11008
+    K, N = 4096, 11008
+    wq = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev)
+    R = int(np.ceil(4 * l2 / wq.numel()))
+    ws = wq.repeat(R, 1)
+    x = torch.randn((1, K), dtype=torch.float32, device=dev)
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    alg = N * K + 4 * K + 4 * N
+
+    def w8(r):
+        qlin.qlin_w8_f32(x, ws[r * N], K, 0.01, y, 1, N, K)
+
+    res["w8_k4096_n11008"] = _time_rotating(w8, R, alg, stream)
+    del ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def _time_rotating(fn, R, alg_bytes, stream):
+    import torch
+
+    for r in range(min(R, 8)):
+        fn(r)
+    torch.cuda.synchronize()
+    reps = max(1, 400 // R)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        for r in range(R):
+            fn(r)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    n = reps * R
+    us = e0.elapsed_time(e1) * 1e3 / n
+    gbs = alg_bytes / (us * 1e-6) / 1e9
+    return {"us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+            "copies": R, "calls": n, "algorithmic_bytes": alg_bytes}
+
+
+# ---------------------------------------------------------------- oracle on the host cores
+def oracle_decode(cfg, weights, steps, warmup, budget_s):
+    """The oracle's decode step at the same positions, until `steps` are done or `budget_s` passes."""
+    import oracle
+    import synth
+
+    orc = oracle.Decoder(cfg, weights)
+    kv = synth.kv_fill(cfg, SEED, POS0)
+    token = int(synth.prompt_ids(SEED, 1, cfg.vocab)[0])
+    for i in range(warmup):
+        token, _ = orc.step(kv, token, POS0 + i % POS_SPAN, want_logits=False)
+    done = 0
+    t0 = time.perf_counter()
+    while done < steps and time.perf_counter() - t0 < budget_s:
+        token, _ = orc.step(kv, token, POS0 + done % POS_SPAN, want_logits=False)
+        done += 1
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    threads = int(os.environ.get("OMP_NUM_THREADS", cores))
+    return done, dt, threads
+
+
+def main():
+    args = parse()
+    rank, local, world = dist_init(args.gpus)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import synth
+
+        cfg = decode_cfg(args.steps, args.warmup)
+        weights = synth.decoder_weights(cfg, seed=SEED)
+        done, dt, threads = oracle_decode(cfg, weights, args.steps, min(args.warmup, 2), budget_s=120.0)
+        v = done / dt
+        line = {
+            "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": done, "steps_requested": args.steps, "warmup": min(args.warmup, 2),
+            "ms_per_step": round(dt / done * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int64 exact / fp32 / fp64 (oracle)", "data": "synthetic",
+            "config": {"workload": "decode step, Gemma-3-1B-shaped ternary decoder, context 1024-1087 (CPU oracle)"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{done} decode steps (time-capped at 120 s)"},
+            "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
+        return 0
+
+    out, cfg, weights = run_decode(args, rank, local, world)
+    if rank == 0 and not args.no_cpu_baseline:
+        done, dt, threads = oracle_decode(cfg, weights, 40, 1, budget_s=20.0)
+        out["cpu_baseline"] = {"value": round(done / dt, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                               "sample": f"{done} oracle decode steps at context 1024+ on the host cores (~20 s cap)"}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

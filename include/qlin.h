@@ -1,0 +1,234 @@
+/*
+ * qlin -- quantised-weight linear layers and a ternary decode step for GB300
+ * (sm_103a).  C ABI, no C++ or torch types.
+ *
+ * What is computed comes from four web pages, cited by title and section:
+ *   [gemma.cpp tour]  "gemma.cpp" (pyshine.com)
+ *   [cpp20gemma]      cpp20gemma README
+ *   [llama2.c]        "llama2.c -- Llama-2 Inference in One C File"
+ *   [citric]          "Gemma 3 1B at 114 tokens per second on a laptop CPU"
+ *
+ * Conventions for every call:
+ *  - Matrices are row-major [out][in] ([cpp20gemma] "Architecture &
+ *    implementation": each output row is contiguous).  A "pitch" is the byte
+ *    distance between rows.
+ *  - "device" pointers are CUDA global-memory addresses of the current
+ *    device; "host" pointers are ordinary CPU memory.  The caller owns every
+ *    buffer; no call allocates or frees device memory, and none keeps a
+ *    pointer after it returns.
+ *  - Device calls are asynchronous on `stream` (NULL = the legacy default
+ *    stream).  Arguments are validated on the host before anything is
+ *    launched; a rejected call launches nothing and returns a status != 0.
+ *    Launch failures return QLIN_ERR_CUDA.  Faults inside a kernel surface at
+ *    the caller's next synchronisation, like any CUDA work.
+ *  - qlin_last_error() gives a thread-local message for the last failure.
+ *  - Device pointers must be 16-byte aligned unless stated otherwise.
+ */
+#ifndef QLIN_H
+#define QLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qlin_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+    QLIN_OK = 0,
+    QLIN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer or pitch */
+    QLIN_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement */
+    QLIN_ERR_BAD_PACKED = 3,  /* t158_unpack: a byte above 242 */
+    QLIN_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+    QLIN_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see decode_step_t158) */
+} qlin_status;
+
+/* Name of a status code; never NULL. */
+const char *qlin_status_str(int status);
+/* Detail of the calling thread's last failed call ("" if none); valid until its next call. */
+const char *qlin_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int qlin_version(void);
+
+/* ========================================================================
+ * S2  T158 packing  ([citric] "Step 1: a kernel for 1.6-bit weights": five
+ * ternary weights per byte, 3^5 = 243 <= 256).  Byte j of a row holds trits
+ * 5j..5j+4 as base-3 digits d_i = trit + 1, least significant first:
+ * byte = sum_i d_i 3^i.  Trits past K are zero trits, so filler bytes past
+ * ceil(K/5) are 121.  Host, synchronous.
+ * ====================================================================== */
+
+/* Row pitch the GPU kernels take for K trits: ceil(ceil(K/5) / 16) * 16 bytes. */
+int64_t t158_pitch(int64_t K);
+
+/* trits: host int8 [N][K] in {-1,0,+1}; packed: host uint8 [N][pitch], pitch >= ceil(K/5).
+ * INVALID_ARG on a null pointer, N/K < 1, short pitch or a trit outside {-1,0,1}. */
+qlin_status t158_pack(const int8_t *trits, int64_t N, int64_t K, uint8_t *packed, int64_t pitch);
+
+/* Inverse of t158_pack; every byte of every row (filler included) is checked first:
+ * BAD_PACKED if any is above 242, and then nothing is written. */
+qlin_status t158_unpack(const uint8_t *packed, int64_t N, int64_t K, int64_t pitch, int8_t *trits);
+
+/* ========================================================================
+ * S1  W8 weight quantisation ([cpp20gemma] "Architecture & implementation":
+ * scale = max(|w|, 1e-9)/127, w8 = clip(round(w/scale)); round half to even,
+ * clip +-127).  One scale for the whole tensor.  Device, asynchronous.
+ * w: device fp32 [N][K] (row stride K, 4-byte aligned); w8: device int8
+ * [N][w_pitch], w_pitch >= K and a multiple of 16 (bytes past K are zeroed);
+ * scale: device fp32 [1] (written last).
+ * ====================================================================== */
+qlin_status qlin_w8_quantize(const float *w, int64_t N, int64_t K, int8_t *w8, int64_t w_pitch,
+                             float *scale, qlin_stream_t stream);
+
+/* ========================================================================
+ * S3  Activation quantisation ([citric] "Step 2": the inputs to each layer
+ * are rounded to int8; [llama2.c] "Key ideas": dynamic symmetric +-127).
+ * Per row m: x_scale[m] = max(max_k |x[m][k]|, 1e-9)/127, xq = clip(
+ * rint(x / x_scale), +-127), fp32 division, ties to even.
+ * x: device fp32 [M][K] (4-byte aligned); xq: device int8 [M][K] (any
+ * alignment); x_scale: device fp32 [M] (4-byte aligned).
+ * ====================================================================== */
+qlin_status qlin_quant_i8(const float *x, int8_t *xq, float *x_scale, int M, int K, qlin_stream_t stream);
+
+/* ========================================================================
+ * S4 + S6 (+ S7 for large M)  T158 linear.
+ *   acc[m][n] = sum_{k<K} trit[n][k] * xq[m][k]          (exact int32)
+ *   y[m][n]   = ((float)acc[m][n] * w_scale) * x_scale[m] (fp32, in this order)
+ * ([citric] "Step 1": exact integer arithmetic; "Step 2": one scale per
+ * matrix, int8 inputs; [cpp20gemma]: scale applied once after the dot.)
+ * xq: device int8 [M][K] (any alignment); x_scale: device fp32 [M];
+ * w_packed: device uint8 [N][w_pitch] as written by t158_pack, w_pitch a
+ * multiple of 16 and >= ceil(K/5), base 16-byte aligned; y: device fp32
+ * [M][N] or NULL; acc: device int32 [M][N] or NULL (at least one non-NULL).
+ * Bytes above 242 in w_packed give unspecified but memory-safe results.
+ * M: 1..4096.  K: 1..131071 (so that |acc| stays below 2^24 and the fp32
+ * epilogue is exact).  UNSUPPORTED outside these ranges.
+ * ====================================================================== */
+qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *w_packed, int64_t w_pitch,
+                         float w_scale, float *y, int32_t *acc, int M, int N, int K, qlin_stream_t stream);
+
+/* ========================================================================
+ * S5  W8 linear: y[m][n] = (sum_k x[m][k] * w8[n][k]) * w_scale, fp32
+ * activations, the scale applied once after the dot product
+ * ([cpp20gemma] "Architecture & implementation"; [llama2.c] "matmul").
+ * x: device fp32 [M][K]; w8: device int8 [N][w_pitch], w_pitch >= K,
+ * multiple of 16; y: device fp32 [M][N].  M: 1..64.
+ * ====================================================================== */
+qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float w_scale, float *y, int M, int N,
+                        int K, qlin_stream_t stream);
+
+/* ========================================================================
+ * Decode-step building blocks (each also runs fused inside decode_step_t158).
+ * ====================================================================== */
+
+/* S8  Embedding lookup ([llama2.c] Step 0; no position bias, [cpp20gemma]
+ * "Real Gemma weights"): h[i] = (float)emb[token][i].  emb: device bf16 bits
+ * [vocab][dim]; token: device int32 [1]; h: device fp32 [dim].  An
+ * out-of-range token writes zeros and sets *status_word (device int32, may be
+ * NULL) to 1. */
+qlin_status qlin_embed_bf16(const uint16_t *emb, int vocab, int dim, const int32_t *token, float *h,
+                            int32_t *status_word, qlin_stream_t stream);
+
+/* S9  RMSNorm ([llama2.c] Step 1): o = g * (r * x), r = 1/sqrtf(ss/n + eps),
+ * ss = sum x^2 as a balanced pairwise sum (zero-padded to a power of two).
+ * x, g, out: device fp32 [M][n] / [n] / [M][n]; out may alias x. */
+qlin_status qlin_rmsnorm(const float *x, const float *gamma, float *out, int M, int n, float eps,
+                         qlin_stream_t stream);
+
+/* S11 (table)  RoPE tables: cos/sin[p][i] = (float)cos|sin(p * base^(-2i/head_dim)),
+ * angle in double ([llama2.c] Step 2).  cos_t, sin_t: device fp32 [max_pos][head_dim/2]. */
+qlin_status t158_rope_table(float *cos_t, float *sin_t, int max_pos, int head_dim, double base,
+                            qlin_stream_t stream);
+
+/* S11  RoPE with (i, i + head_dim/2) pairs ([gemma.cpp tour] "The Forward
+ * Pass"), rotate-then-cache ([cpp20gemma]): q [n_heads][head_dim] is rotated
+ * in place; k [n_kv][head_dim] is rotated and written with v to
+ * k_cache[pos], v_cache[pos] (device fp32 [max_pos][n_kv*head_dim]).
+ * Rotation in fp32, products rounded then added. */
+qlin_status qlin_rope_kv_append(float *q, const float *k, const float *v, float *k_cache, float *v_cache,
+                                const float *cos_t, const float *sin_t, int pos, int n_heads, int n_kv,
+                                int head_dim, qlin_stream_t stream);
+
+/* S12  Decode attention ([llama2.c] Step 4): for query head h (KV head
+ * h/(n_heads/n_kv)), softmax over t <= pos of q.k_t/sqrt(head_dim), then
+ * sum_t p_t v_t.  fp32 with a fixed order: dot products and every sum are
+ * pairwise; positions go in chunks of 32 whose maxima and sums are merged
+ * with the online-softmax identity.  q: device fp32 [n_heads][head_dim]
+ * (rotated); caches as in qlin_rope_kv_append; out: device fp32
+ * [n_heads][head_dim]; workspace: device scratch of
+ * qlin_attention_workspace_size() bytes.  head_dim: 16..256, power of two. */
+size_t qlin_attention_workspace_size(int max_pos, int n_heads, int head_dim);
+qlin_status qlin_attention_decode(const float *q, const float *k_cache, const float *v_cache, int pos,
+                                  int n_heads, int n_kv, int head_dim, float *out, void *workspace,
+                                  size_t workspace_bytes, qlin_stream_t stream);
+
+/* S14 (activation)  GeGLU: a = gelu(g) * u with the tanh form of GELU
+ * (0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))), [gemma.cpp tour],
+ * [cpp20gemma]); tanh(z) = 1 - 2/(e^{2z} + 1) with a Cody-Waite fp32 exp.
+ * g, u, a: device fp32 [n]; a may alias g or u. */
+qlin_status qlin_geglu(const float *g, const float *u, float *a, int n, qlin_stream_t stream);
+
+/* S16  lm_head + greedy pick ([llama2.c] Step 6 and "Sampling"):
+ * logits[v] = sum_i emb[v][i] * x[i] (bf16 table, fp32 x, fp32 accumulate),
+ * next = the first index of the maximum.  emb: device bf16 [vocab][dim];
+ * x: device fp32 [dim]; logits: device fp32 [vocab] or NULL; next: device
+ * int32 [1]; workspace: qlin_lm_head_workspace_size() bytes. */
+size_t qlin_lm_head_workspace_size(int vocab);
+qlin_status qlin_lm_head_argmax(const uint16_t *emb, const float *x, int vocab, int dim, float *logits,
+                                int32_t *next, void *workspace, size_t workspace_bytes, qlin_stream_t stream);
+
+/* ========================================================================
+ * S8-S16 composed: one decode step of a ternary Gemma-style decoder
+ * ([cpp20gemma] "Architecture & implementation": h += attn(rmsnorm(h));
+ * h += mlp(rmsnorm(h)); logits = lm_head(rmsnorm(h)); layer order of
+ * [llama2.c] "The forward pass"; every linear layer T158 on int8-quantised
+ * inputs, [citric] "Step 2"; GeGLU MLP; bf16 embedding tied to the lm_head).
+ * ====================================================================== */
+#define T158_NMAT 7 /* per layer, in this order: wq wk wv wo wg wu wd */
+
+typedef struct {
+    int32_t n_layers, dim, n_heads, n_kv_heads, head_dim, ffn, vocab, max_pos;
+    float eps;
+    float reserved0;
+    const uint8_t *w[T158_NMAT]; /* device, each [n_layers][rows][pitch[j]] packed by t158_pack */
+    int64_t pitch[T158_NMAT];    /* multiples of 16, >= ceil(in/5) */
+    const float *scales;         /* device fp32 [n_layers][7], one per matrix */
+    const float *g_attn;         /* device fp32 [n_layers][dim] */
+    const float *g_ffn;          /* device fp32 [n_layers][dim] */
+    const float *g_final;        /* device fp32 [dim] */
+    const uint16_t *emb;         /* device bf16 bits [vocab][dim], also the lm_head */
+    const float *rope_cos;       /* device fp32 [max_pos][head_dim/2] from t158_rope_table */
+    const float *rope_sin;
+} t158_model;
+
+/* Bytes of device scratch decode_step_t158 needs for this model. */
+qlin_status decode_step_t158_workspace_size(const t158_model *m, size_t *bytes);
+
+/* One forward step at position pos (0 <= pos < max_pos) for the token in
+ * device memory *token: writes rotated k and v of every layer at pos into
+ * kv_cache (device fp32 [n_layers][2][max_pos][n_kv_heads*head_dim], k then
+ * v), logits (device fp32 [vocab], or NULL) and the greedy next token to
+ * device *next_token (which may be the same address as token, so steps
+ * chain on the device).  Shapes supported: dim % 16 == 0, head_dim in
+ * {16,...,256} a power of two, n_heads % n_kv_heads == 0.  The workspace
+ * holds a status word: after the stream has finished the step,
+ * decode_step_t158_status() returns QLIN_ERR_TIMEOUT if a bounded device wait
+ * gave up and QLIN_ERR_INVALID_ARG if *token was out of range. */
+qlin_status decode_step_t158(const t158_model *m, float *kv_cache, void *workspace, size_t workspace_bytes,
+                             const int32_t *token, int32_t pos, float *logits, int32_t *next_token,
+                             qlin_stream_t stream);
+
+/* Number of kernel launches one decode_step_t158 call makes for this model
+ * (for launch accounting); -1 if the model is invalid. */
+int decode_step_t158_launches(const t158_model *m);
+
+/* Reads (synchronously, after synchronising `stream`) and clears the status
+ * word of a decode workspace. */
+qlin_status decode_step_t158_status(void *workspace, qlin_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QLIN_H */

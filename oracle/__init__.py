@@ -73,6 +73,7 @@ def _L():
                 "or_rope_table": ([i64, i64, f64, p, p], None),
                 "or_rope_apply": ([p, i64, i64, p, p], None),
                 "or_attention": ([p, p, p, i64, i64, i64, i64, p], None),
+                "or_lm_head_argmax": ([p, p, i64, i64, p, p], None),
                 "or_decode_step": ([ctypes.POINTER(OrModel), p, i32, i64, p, p], ctypes.c_int),
                 "or_decode_generate": ([ctypes.POINTER(OrModel), p, p, i64, i64, i64, p], ctypes.c_int),
             }
@@ -216,6 +217,17 @@ def attention(q: np.ndarray, kc: np.ndarray, vc: np.ndarray, pos: int, n_heads: 
     out = np.empty(n_heads * head_dim, np.float32)
     _L().or_attention(_p(q), _p(kc), _p(vc), pos, n_heads, n_kv, head_dim, _p(out))
     return out
+
+
+def lm_head_argmax(emb_bits: np.ndarray, x: np.ndarray):
+    """fp64 logits of the bf16 table against x, rounded to fp32, and the first argmax."""
+    e = np.ascontiguousarray(emb_bits, np.uint16)
+    x = np.ascontiguousarray(x, np.float32)
+    V, D = e.shape
+    logits = np.empty(V, np.float32)
+    nxt = ctypes.c_int32()
+    _L().or_lm_head_argmax(_p(e), _p(x), V, D, _p(logits), ctypes.byref(nxt))
+    return nxt.value, logits
 
 
 # ------------------------------------------------------------------ decode step

@@ -406,6 +406,23 @@ static void t158_layer(const or_model *m, int l, int j, const float *x, int8_t *
     or_t158_linear(xq, &xs, w, m->pitch[j], m->scales[l * 7 + j], 1, N, K, NULL, y);
 }
 
+/* S16: logits[r] = sum_i bf16(emb[r][i]) * x[i] in fp64, rounded to fp32
+ * ([llama2.c] Step 6), and the greedy token: the first maximum wins
+ * ([llama2.c] "Sampling", strict > in the argmax loop). */
+void or_lm_head_argmax(const uint16_t *emb, const float *x, int64_t vocab, int64_t dim, float *logits, int32_t *next) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < vocab; r++) {
+        double acc = 0.0;
+        const uint16_t *e = emb + r * dim;
+        for (int64_t i = 0; i < dim; i++) acc += (double)bf16f(e[i]) * (double)x[i];
+        logits[r] = (float)acc;
+    }
+    int32_t best = 0;
+    for (int64_t r = 1; r < vocab; r++)
+        if (logits[r] > logits[best]) best = (int32_t)r;
+    if (next) *next = best;
+}
+
 /* One forward step at position pos: writes rotated k and v into the cache
  * [L][2][max_pos][kv_dim], fp32 logits [vocab] (may be NULL) and the greedy
  * token ([llama2.c] "Sampling": first maximum wins).  logits are fp64 sums
@@ -461,17 +478,7 @@ int or_decode_step(const or_model *m, float *kv, int32_t token, int64_t pos, flo
     }
     /* Step 6: final norm and classifier (tied bf16 table) */
     or_rmsnorm(h, m->g_final, d, m->eps, xn);
-#pragma omp parallel for schedule(static)
-    for (int64_t r = 0; r < m->vocab; r++) {
-        double acc = 0.0;
-        const uint16_t *e = m->emb + r * d;
-        for (int64_t i = 0; i < d; i++) acc += (double)bf16f(e[i]) * (double)xn[i];
-        lg[r] = (float)acc;
-    }
-    int32_t best = 0;
-    for (int64_t r = 1; r < m->vocab; r++)
-        if (lg[r] > lg[best]) best = (int32_t)r;
-    if (next) *next = best;
+    or_lm_head_argmax(m->emb, xn, m->vocab, d, lg, next);
 
     if (!logits) free(lg);
     free(h); free(xn); free(q); free(k); free(v); free(att); free(y); free(g); free(u); free(xq);

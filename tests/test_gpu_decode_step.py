@@ -1,0 +1,119 @@
+"""GPU parity of the composed decode step (S8-S16) against the oracle.
+
+* tiny decoder: 79 forwards (16-token prompt + 64 greedy tokens), every
+  argmax equal, logits within max-abs-rel 2e-3, KV cache bit-exact;
+* Gemma-3-1B-shaped decoder (26 blocks, hidden 1152, 4/1 heads of 256, GeGLU
+  6912, vocab 262144, seed 4): the same 16 + 64 greedy run from an empty cache,
+  and steps on a cache filled to position 1024 (the throughput state);
+* the status word reports an out-of-range token.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import device, host, max_abs_rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return device()
+
+
+def _pair(cfg, seed, dev, emb_std=0.02):
+    from weight_streaming_gemv_gb300.decoder import T158Decoder
+
+    w = synth.decoder_weights(cfg, seed=seed, emb_std=emb_std)
+    return T158Decoder(cfg, w, device=dev), oracle.Decoder(cfg, w)
+
+
+def _run_and_compare(gpu, orc, kv_o, prompt, start_pos, n_steps, logit_checks=None):
+    import torch
+
+    token = int(prompt[0])
+    gpu.token.fill_(token)
+    ids_g, ids_o = [], []
+    for s in range(n_steps):
+        pos = start_pos + s
+        want = logit_checks is None or s in logit_checks
+        nx_o, lg_o = orc.step(kv_o, token, pos, want_logits=True)
+        gpu.step(pos, logits=want)
+        torch.cuda.synchronize()
+        nx_g = int(gpu.token.item())
+        if want:
+            err = max_abs_rel(gpu.logits.cpu().numpy(), lg_o)
+            assert err <= 2e-3, f"step {s} (pos {pos}): logits max-abs-rel {err}"
+        if nx_g != nx_o:
+            top = np.sort(lg_o)[-2:]
+            raise AssertionError(f"step {s} (pos {pos}): token {nx_g} != oracle {nx_o}; oracle top-2 gap {top[1]-top[0]}")
+        ids_g.append(nx_g)
+        ids_o.append(nx_o)
+        token = int(prompt[s + 1]) if s + 1 < len(prompt) else nx_o
+        gpu.token.fill_(token)
+    gpu.check_status()
+    return np.array(ids_g), np.array(ids_o)
+
+
+def test_tiny_decoder_79_steps(dev):
+    cfg = synth.DecoderConfig(max_pos=96, **synth.TINY)
+    for emb_std in (0.02, 0.002):
+        gpu, orc = _pair(cfg, 5, dev, emb_std)
+        kv_o = orc.new_cache()
+        prompt = synth.prompt_ids(5, 16, cfg.vocab)
+        _run_and_compare(gpu, orc, kv_o, prompt, 0, 79)
+        np.testing.assert_array_equal(host(gpu.kv), kv_o)
+
+
+@pytest.fixture(scope="module")
+def gemma(dev):
+    cfg = synth.DecoderConfig(max_pos=1152, **synth.GEMMA3_1B)
+    return (cfg,) + _pair(cfg, 4, dev)
+
+
+def test_gemma_shape_greedy_64_from_prompt(gemma):
+    cfg, gpu, orc = gemma
+    gpu.kv.zero_()
+    kv_o = orc.new_cache()
+    prompt = synth.prompt_ids(4, 16, cfg.vocab)
+    ids, _ = _run_and_compare(gpu, orc, kv_o, prompt, 0, 16 + 64 - 1, logit_checks={0, 15, 40, 78})
+    np.testing.assert_array_equal(host(gpu.kv)[:, :, :79], kv_o[:, :, :79])
+    print("generated:", ids[15:].tolist())
+
+
+def test_gemma_shape_steps_at_pos_1024(gemma):
+    import torch
+
+    cfg, gpu, orc = gemma
+    kv0 = synth.kv_fill(cfg, 4, 1024)
+    gpu.kv.copy_(torch.from_numpy(kv0))
+    kv_o = kv0.copy()
+    prompt = np.array([int(synth.prompt_ids(4, 1, cfg.vocab)[0])], np.int32)
+    _run_and_compare(gpu, orc, kv_o, prompt, 1024, 4)
+    np.testing.assert_array_equal(host(gpu.kv)[:, :, 1024:1028], kv_o[:, :, 1024:1028])
+
+
+def test_out_of_range_token_sets_status(dev):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    cfg = synth.DecoderConfig(max_pos=8, **synth.TINY)
+    gpu, _ = _pair(cfg, 5, dev)
+    gpu.step(0, token=torch.tensor([cfg.vocab + 5], dtype=torch.int32, device=dev))
+    with pytest.raises(qlin.QlinError) as e:
+        gpu.check_status()
+    assert e.value.status == 1
+    gpu.check_status()  # the word was cleared
+
+
+def test_decode_step_rejects_bad_arguments(dev):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    cfg = synth.DecoderConfig(max_pos=8, **synth.TINY)
+    gpu, _ = _pair(cfg, 5, dev)
+    with pytest.raises(qlin.QlinError):
+        gpu.step(8)  # pos == max_pos
+    with pytest.raises(qlin.QlinError):
+        qlin.decode_step_t158(gpu.model, gpu.kv, gpu.workspace, gpu.ws_bytes - 1, gpu.token, 0, None, gpu.token)

@@ -1,0 +1,162 @@
+"""GPU parity of the linear-layer rows (S1, S3, S4+S6, S5, S7) against the oracle.
+
+Integer results (codes, accumulators) and the exact T158 epilogue must match
+bit for bit; the W8 outputs within max-abs-rel 1e-5.  Full sizes of the
+benchmark workloads plus ragged and edge shapes.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import device, host, max_abs_rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return device()
+
+
+def _empty(shape, dtype, dev):
+    import torch
+
+    return torch.empty(shape, dtype=dtype, device=dev)
+
+
+# ---------------------------------------------------------------- S3 activation quantiser
+@pytest.mark.parametrize("M,K", [(1, 1), (1, 1152), (3, 1157), (16, 6912), (512, 1152)])
+def test_quant_i8_bit_exact(dev, M, K):
+    import torch
+
+    x = synth.normal_f32(40, K, (M, K))
+    x[0, 0] = 0.0
+    xq_o, xs_o = oracle.quant_i8(x)
+    xq = _empty((M, K), torch.int8, dev)
+    xs = _empty((M,), torch.float32, dev)
+    from weight_streaming_gemv_gb300 import qlin
+
+    qlin.qlin_quant_i8(to_dev(x, dev), xq, xs, M, K)
+    np.testing.assert_array_equal(host(xq), xq_o)
+    np.testing.assert_array_equal(host(xs), xs_o)
+
+
+def test_quant_i8_zero_row_and_ties(dev):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    x = np.zeros((2, 8), np.float32)
+    x[1] = [127.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5]
+    xq_o, xs_o = oracle.quant_i8(x)
+    xq = _empty((2, 8), torch.int8, dev)
+    xs = _empty((2,), torch.float32, dev)
+    qlin.qlin_quant_i8(to_dev(x, dev), xq, xs, 2, 8)
+    np.testing.assert_array_equal(host(xq), xq_o)
+    np.testing.assert_array_equal(host(xs), xs_o)
+
+
+# ---------------------------------------------------------------- S1 W8 quantisation
+@pytest.mark.parametrize("N,K", [(768, 288), (4096, 4096), (1, 1), (3, 17)])
+def test_w8_quantize_bit_exact(dev, N, K):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    w = synth.normal_f32(41, K, (N, K), 0.0, 0.02)
+    q_o, s_o = oracle.w8_quantize(w)
+    pitch = (K + 15) // 16 * 16
+    w8 = _empty((N, pitch), torch.int8, dev)
+    s = _empty((1,), torch.float32, dev)
+    qlin.qlin_w8_quantize(to_dev(w, dev), N, K, w8, pitch, s)
+    w8h = host(w8)
+    np.testing.assert_array_equal(w8h[:, :K], q_o)
+    assert (w8h[:, K:] == 0).all()
+    assert host(s)[0] == s_o
+
+
+# ---------------------------------------------------------------- S4 + S6 T158 linear
+def _t158_case(dev, M, K, N, seed, trits=None, xq=None):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    d = synth.t158_gemv(seed, M, K, N)
+    t = d["trits"] if trits is None else trits
+    if xq is None:
+        xq, xs = oracle.quant_i8(d["x"])
+    else:
+        xs = np.full(M, 0.01, np.float32)
+    acc_o, y_o = oracle.t158_linear(xq, xs, oracle.t158_pack(t), d["w_scale"], K)
+    pitch = qlin.t158_pitch(K)
+    w = to_dev(qlin.t158_pack(t, pitch), dev)
+    y = _empty((M, N), torch.float32, dev)
+    acc = _empty((M, N), torch.int32, dev)
+    qlin.qlin_t158_i8(to_dev(xq, dev), to_dev(xs, dev), w, pitch, d["w_scale"], y, acc, M, N, K)
+    np.testing.assert_array_equal(host(acc), acc_o)
+    np.testing.assert_array_equal(host(y), y_o)
+
+
+def test_t158_gemv_gate_up_shape_full_size(dev):
+    # M=1, K=1152, N=6912: the Gemma-3-1B GeGLU gate/up shape (rows zero-padded to 1155 trits)
+    _t158_case(dev, 1, 1152, 6912, seed=1)
+
+
+def test_t158_gemv_down_shape_full_size(dev):
+    _t158_case(dev, 1, 6912, 1152, seed=2)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1, 1), (1, 5, 3), (1, 31, 33), (1, 81, 700), (1, 1024, 1152),
+                                   (2, 1157, 333), (3, 640, 65), (4, 1152, 1536), (7, 77, 129),
+                                   (16, 6912, 1152), (17, 333, 100)])
+def test_t158_ragged_shapes(dev, M, K, N):
+    _t158_case(dev, M, K, N, seed=M * 1000 + K)
+
+
+def test_t158_adversarial_extremes(dev):
+    # all +1 trits against all +127 activations: acc = 127 K at K = 6912, the largest in use
+    K, N = 6912, 64
+    t = np.ones((N, K), np.int8)
+    t[1] = -1
+    t[2] = 0
+    t[3, ::2] = -1
+    xq = np.full((2, K), 127, np.int8)
+    xq[1, ::3] = -127
+    _t158_case(dev, 2, K, N, seed=9, trits=t, xq=xq)
+
+
+@pytest.mark.parametrize("K,N", [(1152, 6912), (6912, 1152)])
+def test_t158_prefill_m512_full_size(dev, K, N):
+    # the two prefill layers: 512 tokens through 1152->6912 and 6912->1152
+    _t158_case(dev, 512, K, N, seed=2)
+
+
+def test_t158_bad_bytes_are_memory_safe(dev):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    K, N = 100, 50
+    pitch = qlin.t158_pitch(K)
+    w = torch.full((N, pitch), 255, dtype=torch.uint8, device=dev)
+    xq = torch.ones((1, K), dtype=torch.int8, device=dev)
+    xs = torch.ones(1, dtype=torch.float32, device=dev)
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    qlin.qlin_t158_i8(xq, xs, w, pitch, 1.0, y, None, 1, N, K)
+    torch.cuda.synchronize()  # unspecified values, but no fault
+
+
+# ---------------------------------------------------------------- S5 W8 linear
+@pytest.mark.parametrize("M,K,N", [(1, 288, 768), (1, 4096, 11008), (1, 11008, 4096), (1, 4096, 4096),
+                                   (4, 4096, 11008), (4, 11008, 4096), (16, 4096, 4096), (16, 11008, 4096),
+                                   (16, 4096, 11008), (3, 17, 5), (1, 1, 1), (64, 300, 70)])
+def test_w8_linear(dev, M, K, N):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    d = synth.w8_gemv(3 if K >= 4096 else 0, M, K, N)
+    q_o, s_o = oracle.w8_quantize(d["w"])
+    y_o = oracle.w8_linear(d["x"], q_o, s_o)
+    pitch = (K + 15) // 16 * 16
+    w8 = np.zeros((N, pitch), np.int8)
+    w8[:, :K] = q_o
+    y = _empty((M, N), torch.float32, dev)
+    qlin.qlin_w8_f32(to_dev(d["x"], dev), to_dev(w8, dev), pitch, float(s_o), y, M, N, K)
+    assert max_abs_rel(host(y), y_o) <= 1e-5

@@ -1,0 +1,529 @@
+// Decode-step kernels: embedding lookup, RMSNorm, RoPE table and KV append,
+// split-position decode attention, GeGLU, lm_head + greedy argmax, and the
+// composed ternary decode step.
+//
+// Sources: llama2.c "The forward pass -- one token, one position" (Steps 0-6)
+// and "Sampling"; cpp20gemma README "Architecture & implementation"; gemma.cpp
+// tour "The Forward Pass, Layer by Layer"; "Gemma 3 1B at 114 tokens per
+// second on a laptop CPU", "Step 2".
+#include <algorithm>
+#include <vector>
+
+#include "decode_ops.cuh"
+
+namespace qlin {
+
+qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
+                                   const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st);
+
+// ---------------------------------------------------------------- S8
+__global__ void embed_kernel(const uint16_t *__restrict__ emb, int vocab, int dim, const int32_t *__restrict__ token,
+                             float *__restrict__ h, int32_t *status) {
+    const int tok = *token;
+    const bool ok = tok >= 0 && tok < vocab;
+    for (int i = threadIdx.x; i < dim; i += blockDim.x)
+        h[i] = ok ? __uint_as_float((uint32_t)emb[(int64_t)tok * dim + i] << 16) : 0.0f;
+    if (!ok && threadIdx.x == 0 && status) atomicOr(status, 1);
+}
+
+// ---------------------------------------------------------------- S9
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float *x, const float *__restrict__ g, float *out, int n,
+                                                      float eps) {
+    extern __shared__ float buf[];
+    __shared__ float red[32];
+    const int64_t row = blockIdx.x;
+    rmsnorm_row(x + row * n, g, out + row * n, n, eps, buf, red);
+}
+
+// ---------------------------------------------------------------- S11
+__global__ void rope_table_kernel(float *cos_t, float *sin_t, int max_pos, int head_dim, double base) {
+    const int half = head_dim / 2;
+    const int64_t total = (int64_t)max_pos * half;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (int64_t)gridDim.x * blockDim.x) {
+        const int p = (int)(idx / half), i = (int)(idx % half);
+        const double theta = pow(base, -(double)(2 * i) / (double)head_dim);
+        const double ang = (double)p * theta;
+        cos_t[idx] = (float)cos(ang);
+        sin_t[idx] = (float)sin(ang);
+    }
+}
+
+__global__ void rope_kv_kernel(float *q, const float *k, const float *v, float *kc, float *vc,
+                               const float *__restrict__ cos_t, const float *__restrict__ sin_t, int pos, int nh,
+                               int nkv, int hd) {
+    extern __shared__ float kr[];  // [nkv*hd]
+    const int half = hd / 2;
+    const float *c = cos_t + (int64_t)pos * half;
+    const float *s = sin_t + (int64_t)pos * half;
+    rope_rotate(q, nh, hd, c, s);
+    for (int i = threadIdx.x; i < nkv * hd; i += blockDim.x) kr[i] = k[i];
+    __syncthreads();
+    rope_rotate(kr, nkv, hd, c, s);
+    __syncthreads();
+    const int64_t off = (int64_t)pos * nkv * hd;
+    for (int i = threadIdx.x; i < nkv * hd; i += blockDim.x) {
+        kc[off + i] = kr[i];
+        vc[off + i] = v[i];
+    }
+}
+
+// ---------------------------------------------------------------- S12
+struct AttnWs {
+    float *m, *S, *U;  // [nh][ncmax], [nh][ncmax], [nh][ncmax][hd]
+};
+
+__host__ __device__ inline int att_chunks(int max_pos) { return (max_pos + 31) / 32; }
+
+__host__ __device__ inline size_t attn_ws_floats(int max_pos, int nh, int hd) {
+    const size_t nc = (size_t)att_chunks(max_pos);
+    return (size_t)nh * nc * (2 + (size_t)hd);
+}
+
+__device__ __forceinline__ AttnWs attn_ws(float *base, int ncmax, int nh, int hd) {
+    AttnWs w;
+    w.m = base;
+    w.S = base + (size_t)nh * ncmax;
+    w.U = base + (size_t)2 * nh * ncmax;
+    return w;
+}
+
+// grid (nchunks, nh): chunk c of head h
+__global__ void __launch_bounds__(256) attn_chunk_kernel(const float *__restrict__ q, const float *__restrict__ kc,
+                                                         const float *__restrict__ vc, int pos, int nh, int nkv, int hd,
+                                                         float *ws, int ncmax) {
+    __shared__ float qs[256];
+    __shared__ float sc[32];
+    const int c = blockIdx.x, h = blockIdx.y;
+    const int kvh = h / (nh / nkv);
+    for (int i = threadIdx.x; i < hd; i += blockDim.x) qs[i] = q[h * hd + i];
+    __syncthreads();
+    const int t0 = c * 32;
+    const int nt = min(32, pos + 1 - t0);
+    const int ld = nkv * hd;
+    AttnWs w = attn_ws(ws, ncmax, nh, hd);
+    attention_chunk(qs, kc + (int64_t)t0 * ld + kvh * hd, vc + (int64_t)t0 * ld + kvh * hd, ld, nt, hd,
+                    w.m + h * ncmax + c, w.S + h * ncmax + c, w.U + ((int64_t)h * ncmax + c) * hd, sc);
+}
+
+__global__ void __launch_bounds__(256) attn_merge_kernel(const float *ws, int ncmax, int nc, int nh, int hd, float *out) {
+    extern __shared__ float wbuf[];
+    __shared__ float red[32];
+    const int h = blockIdx.x;
+    AttnWs w = attn_ws(const_cast<float *>(ws), ncmax, nh, hd);
+    attention_merge(w.m + h * ncmax, w.S + h * ncmax, w.U + (int64_t)h * ncmax * hd, nc, hd, out + h * hd, wbuf, red);
+}
+
+// ---------------------------------------------------------------- S14 / residual
+__global__ void geglu_kernel(const float *g, const float *u, float *a, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        a[i] = __fmul_rn(gelu32(g[i]), u[i]);
+}
+
+__global__ void add_kernel(float *h, const float *y, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) h[i] = __fadd_rn(h[i], y[i]);
+}
+
+// ---------------------------------------------------------------- S16
+// Row r of the bf16 table against fp32 x.  16 lanes per row (16-byte chunks
+// c = lane%16 + 16 j), 2 rows per slot, 2 slots per warp pass.  Each block
+// leaves its best (value, index) in part[blockIdx.x]; ties go to the lower
+// index, so the result does not depend on the schedule.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
+
+__global__ void __launch_bounds__(256) lm_head_kernel(const uint16_t *__restrict__ emb, const float *__restrict__ x,
+                                                      int vocab, int dim, float *__restrict__ logits,
+                                                      float2 *__restrict__ part) {
+    extern __shared__ float4 xs4[];
+    __shared__ float bv_s[8];
+    __shared__ int bi_s[8];
+    float *xsf = reinterpret_cast<float *>(xs4);
+    const int C = dim / 8;  // 16-byte chunks of a bf16 row
+    for (int i = threadIdx.x; i < dim; i += blockDim.x) xsf[i] = x[i];
+    __syncthreads();
+    const int lane = threadIdx.x & 31, sub = lane & 15, rsub = lane >> 4;
+    const int warps = blockDim.x >> 5;
+    const int64_t gwarp = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * warps;
+    float best_v = -__int_as_float(0x7f800000);
+    int best_i = 0x7fffffff;
+    for (int64_t r0 = gwarp * 4; r0 < vocab; r0 += nwarps * 4) {
+        float acc[2] = {0.0f, 0.0f};
+#pragma unroll 3
+        for (int c = sub; c < C; c += 16) {
+            uint4 wv[2];
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                const int64_t row = r0 + 2 * r + rsub;
+                wv[r] = row < vocab ? ld_stream_v4(emb + row * dim + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
+            }
+            const float4 xa = xs4[2 * c], xb = xs4[2 * c + 1];
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                float a = acc[r];
+                a = fmaf(__uint_as_float(wv[r].x << 16), xa.x, a);
+                a = fmaf(__uint_as_float(wv[r].x & 0xffff0000u), xa.y, a);
+                a = fmaf(__uint_as_float(wv[r].y << 16), xa.z, a);
+                a = fmaf(__uint_as_float(wv[r].y & 0xffff0000u), xa.w, a);
+                a = fmaf(__uint_as_float(wv[r].z << 16), xb.x, a);
+                a = fmaf(__uint_as_float(wv[r].z & 0xffff0000u), xb.y, a);
+                a = fmaf(__uint_as_float(wv[r].w << 16), xb.z, a);
+                a = fmaf(__uint_as_float(wv[r].w & 0xffff0000u), xb.w, a);
+                acc[r] = a;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            float v = acc[r];
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            const int64_t row = r0 + 2 * r + rsub;
+            if (sub == 0 && row < vocab) {
+                if (logits) logits[row] = v;
+                if (better(v, (int)row, best_v, best_i)) {
+                    best_v = v;
+                    best_i = (int)row;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best_v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, best_i, off);
+        if (better(ov, oi, best_v, best_i)) {
+            best_v = ov;
+            best_i = oi;
+        }
+    }
+    if (lane == 0) {
+        bv_s[threadIdx.x >> 5] = best_v;
+        bi_s[threadIdx.x >> 5] = best_i;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float v = bv_s[0];
+        int i = bi_s[0];
+        for (int w = 1; w < warps; w++)
+            if (better(bv_s[w], bi_s[w], v, i)) {
+                v = bv_s[w];
+                i = bi_s[w];
+            }
+        part[blockIdx.x] = make_float2(v, __int_as_float(i));
+    }
+}
+
+__global__ void argmax_final_kernel(const float2 *__restrict__ part, int n, int32_t *next) {
+    float v = -__int_as_float(0x7f800000);
+    int i = 0x7fffffff;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        const float2 p = part[j];
+        if (better(p.x, __float_as_int(p.y), v, i)) {
+            v = p.x;
+            i = __float_as_int(p.y);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+        if (better(ov, oi, v, i)) {
+            v = ov;
+            i = oi;
+        }
+    }
+    __shared__ float sv[32];
+    __shared__ int si[32];
+    if ((threadIdx.x & 31) == 0) {
+        sv[threadIdx.x >> 5] = v;
+        si[threadIdx.x >> 5] = i;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); w++)
+            if (better(sv[w], si[w], v, i)) {
+                v = sv[w];
+                i = si[w];
+            }
+        *next = i;
+    }
+}
+
+static int lm_head_blocks() { return sm_count() * 4; }
+
+// ---------------------------------------------------------------- host wrappers
+static qlin_status launch_rmsnorm(const float *x, const float *g, float *out, int M, int n, float eps, cudaStream_t st) {
+    const size_t smem = (size_t)next_pow2(n) * sizeof(float);
+    QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "rmsnorm: n=%d too large", n);
+    if (smem > 48 * 1024) QLIN_CUDA(cudaFuncSetAttribute(rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    rmsnorm_kernel<<<M, 256, smem, st>>>(x, g, out, n, eps);
+    QLIN_LAUNCHED("rmsnorm_kernel");
+    return QLIN_OK;
+}
+
+static qlin_status launch_attention(const float *q, const float *kc, const float *vc, int pos, int nh, int nkv, int hd,
+                                    float *out, float *ws, int ncmax, cudaStream_t st) {
+    const int nc = pos / 32 + 1;
+    attn_chunk_kernel<<<dim3(nc, nh), 256, 0, st>>>(q, kc, vc, pos, nh, nkv, hd, ws, ncmax);
+    QLIN_LAUNCHED("attn_chunk_kernel");
+    const size_t smem = (size_t)next_pow2(nc) * sizeof(float);
+    attn_merge_kernel<<<nh, 256, smem, st>>>(ws, ncmax, nc, nh, hd, out);
+    QLIN_LAUNCHED("attn_merge_kernel");
+    return QLIN_OK;
+}
+
+static qlin_status launch_lm_head(const uint16_t *emb, const float *x, int vocab, int dim, float *logits, int32_t *next,
+                                  float2 *part, cudaStream_t st) {
+    const int blocks = lm_head_blocks();
+    lm_head_kernel<<<blocks, 256, (size_t)dim * sizeof(float), st>>>(emb, x, vocab, dim, logits, part);
+    QLIN_LAUNCHED("lm_head_kernel");
+    argmax_final_kernel<<<1, 256, 0, st>>>(part, blocks, next);
+    QLIN_LAUNCHED("argmax_final_kernel");
+    return QLIN_OK;
+}
+
+// ---------------------------------------------------------------- composed decode step
+struct DecodeWs {
+    float *h, *xn, *q, *k, *v, *att, *y, *g, *u, *xs, *attn;
+    int8_t *xq;
+    float2 *part;
+    int32_t *status;
+    size_t bytes;
+};
+
+static size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+static DecodeWs carve(const t158_model *m, char *base) {
+    DecodeWs w{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *p = base ? base + off : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    const int d = m->dim, qd = m->n_heads * m->head_dim, kvd = m->n_kv_heads * m->head_dim, f = m->ffn;
+    const int big = std::max(std::max(d, qd), f);
+    w.status = (int32_t *)take(sizeof(int32_t) * 4);
+    w.h = (float *)take(sizeof(float) * d);
+    w.xn = (float *)take(sizeof(float) * big);
+    w.q = (float *)take(sizeof(float) * qd);
+    w.k = (float *)take(sizeof(float) * kvd);
+    w.v = (float *)take(sizeof(float) * kvd);
+    w.att = (float *)take(sizeof(float) * qd);
+    w.y = (float *)take(sizeof(float) * big);
+    w.g = (float *)take(sizeof(float) * f);
+    w.u = (float *)take(sizeof(float) * f);
+    w.xs = (float *)take(sizeof(float) * 4);
+    w.xq = (int8_t *)take((size_t)big);
+    w.attn = (float *)take(sizeof(float) * attn_ws_floats(m->max_pos, m->n_heads, m->head_dim));
+    w.part = (float2 *)take(sizeof(float2) * (size_t)lm_head_blocks());
+    w.bytes = off;
+    return w;
+}
+
+static qlin_status check_model(const t158_model *m) {
+    QLIN_REQUIRE(m, QLIN_ERR_INVALID_ARG, "decode_step_t158: null model");
+    QLIN_REQUIRE(m->n_layers >= 1 && m->dim >= 16 && m->dim % 16 == 0 && m->n_heads >= 1 && m->n_kv_heads >= 1 &&
+                     m->n_heads % m->n_kv_heads == 0 && m->ffn >= 1 && m->vocab >= 1 && m->max_pos >= 1,
+                 QLIN_ERR_INVALID_ARG, "decode_step_t158: bad model dimensions");
+    QLIN_REQUIRE(m->head_dim >= 16 && m->head_dim <= 256 && (m->head_dim & (m->head_dim - 1)) == 0,
+                 QLIN_ERR_UNSUPPORTED, "decode_step_t158: head_dim %d not a power of two in 16..256", m->head_dim);
+    const int d = m->dim, qd = m->n_heads * m->head_dim, kvd = m->n_kv_heads * m->head_dim, f = m->ffn;
+    const int ins[T158_NMAT] = {d, d, d, qd, d, d, f};
+    for (int j = 0; j < T158_NMAT; j++) {
+        QLIN_REQUIRE(m->w[j] && aligned16(m->w[j]), QLIN_ERR_INVALID_ARG, "decode_step_t158: weight %d null/misaligned", j);
+        QLIN_REQUIRE(m->pitch[j] % 16 == 0 && m->pitch[j] >= (ins[j] + 4) / 5, QLIN_ERR_INVALID_ARG,
+                     "decode_step_t158: pitch[%d]=%lld", j, (long long)m->pitch[j]);
+    }
+    (void)kvd;
+    QLIN_REQUIRE(m->scales && m->g_attn && m->g_ffn && m->g_final && m->emb && m->rope_cos && m->rope_sin,
+                 QLIN_ERR_INVALID_ARG, "decode_step_t158: null model tensor");
+    QLIN_REQUIRE(aligned16(m->emb), QLIN_ERR_INVALID_ARG, "decode_step_t158: emb not 16-byte aligned");
+    return QLIN_OK;
+}
+
+qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
+                                   const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st);
+
+qlin_status launch_quant_i8(const float *x, int8_t *xq, float *xs, int M, int K, cudaStream_t st);
+
+// One forward step as a sequence of kernels on `st`.
+static qlin_status decode_sequence(const t158_model *m, float *kv, const DecodeWs &w, const int32_t *token, int pos,
+                                   float *logits, int32_t *next, cudaStream_t st) {
+    const int d = m->dim, nh = m->n_heads, nkv = m->n_kv_heads, hd = m->head_dim, f = m->ffn;
+    const int qd = nh * hd, kvd = nkv * hd;
+    const int ncmax = att_chunks(m->max_pos);
+    const int rows[T158_NMAT] = {qd, kvd, kvd, d, f, f, d};
+    const int ins[T158_NMAT] = {d, d, d, qd, d, d, f};
+    embed_kernel<<<1, 256, 0, st>>>(m->emb, m->vocab, d, token, w.h, w.status);
+    QLIN_LAUNCHED("embed_kernel");
+    auto lin = [&](int l, int j, const float *x, float *out) -> qlin_status {
+        qlin_status qs = launch_quant_i8(x, w.xq, w.xs, 1, ins[j], st);
+        if (qs) return qs;
+        const uint8_t *wt = m->w[j] + (int64_t)l * rows[j] * m->pitch[j];
+        return t158_linear_cuda_cores(w.xq, w.xs, wt, m->pitch[j], 0.0f, m->scales + l * T158_NMAT + j, out, nullptr, 1,
+                                      rows[j], ins[j], st);
+    };
+    qlin_status s;
+    for (int l = 0; l < m->n_layers; l++) {
+        float *kc = kv + (int64_t)(2 * l) * m->max_pos * kvd;
+        float *vc = kv + (int64_t)(2 * l + 1) * m->max_pos * kvd;
+        if ((s = launch_rmsnorm(w.h, m->g_attn + (int64_t)l * d, w.xn, 1, d, m->eps, st))) return s;
+        if ((s = lin(l, 0, w.xn, w.q))) return s;
+        if ((s = lin(l, 1, w.xn, w.k))) return s;
+        if ((s = lin(l, 2, w.xn, w.v))) return s;
+        rope_kv_kernel<<<1, 256, kvd * sizeof(float), st>>>(w.q, w.k, w.v, kc, vc, m->rope_cos, m->rope_sin, pos, nh,
+                                                            nkv, hd);
+        QLIN_LAUNCHED("rope_kv_kernel");
+        if ((s = launch_attention(w.q, kc, vc, pos, nh, nkv, hd, w.att, w.attn, ncmax, st))) return s;
+        if ((s = lin(l, 3, w.att, w.y))) return s;
+        add_kernel<<<ceil_div(d, 256), 256, 0, st>>>(w.h, w.y, d);
+        QLIN_LAUNCHED("add_kernel");
+        if ((s = launch_rmsnorm(w.h, m->g_ffn + (int64_t)l * d, w.xn, 1, d, m->eps, st))) return s;
+        if ((s = lin(l, 4, w.xn, w.g))) return s;
+        if ((s = lin(l, 5, w.xn, w.u))) return s;
+        geglu_kernel<<<ceil_div(f, 256), 256, 0, st>>>(w.g, w.u, w.g, f);
+        QLIN_LAUNCHED("geglu_kernel");
+        if ((s = lin(l, 6, w.g, w.y))) return s;
+        add_kernel<<<ceil_div(d, 256), 256, 0, st>>>(w.h, w.y, d);
+        QLIN_LAUNCHED("add_kernel");
+    }
+    if ((s = launch_rmsnorm(w.h, m->g_final, w.xn, 1, d, m->eps, st))) return s;
+    return launch_lm_head(m->emb, w.xn, m->vocab, d, logits, next, w.part, st);
+}
+
+}  // namespace qlin
+
+extern "C" {
+
+qlin_status qlin_embed_bf16(const uint16_t *emb, int vocab, int dim, const int32_t *token, float *h,
+                            int32_t *status_word, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(emb && token && h, QLIN_ERR_INVALID_ARG, "qlin_embed_bf16: null pointer");
+    QLIN_REQUIRE(vocab >= 1 && dim >= 1, QLIN_ERR_INVALID_ARG, "qlin_embed_bf16: vocab=%d dim=%d", vocab, dim);
+    qlin::embed_kernel<<<1, 256, 0, (cudaStream_t)stream>>>(emb, vocab, dim, token, h, status_word);
+    QLIN_LAUNCHED("embed_kernel");
+    return QLIN_OK;
+}
+
+qlin_status qlin_rmsnorm(const float *x, const float *gamma, float *out, int M, int n, float eps, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(x && gamma && out, QLIN_ERR_INVALID_ARG, "qlin_rmsnorm: null pointer");
+    QLIN_REQUIRE(M >= 1 && n >= 1, QLIN_ERR_INVALID_ARG, "qlin_rmsnorm: M=%d n=%d", M, n);
+    return qlin::launch_rmsnorm(x, gamma, out, M, n, eps, (cudaStream_t)stream);
+}
+
+qlin_status t158_rope_table(float *cos_t, float *sin_t, int max_pos, int head_dim, double base, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(cos_t && sin_t, QLIN_ERR_INVALID_ARG, "t158_rope_table: null pointer");
+    QLIN_REQUIRE(max_pos >= 1 && head_dim >= 2 && head_dim % 2 == 0 && base > 0, QLIN_ERR_INVALID_ARG,
+                 "t158_rope_table: max_pos=%d head_dim=%d", max_pos, head_dim);
+    qlin::rope_table_kernel<<<qlin::sm_count() * 4, 256, 0, (cudaStream_t)stream>>>(cos_t, sin_t, max_pos, head_dim, base);
+    QLIN_LAUNCHED("rope_table_kernel");
+    return QLIN_OK;
+}
+
+qlin_status qlin_rope_kv_append(float *q, const float *k, const float *v, float *k_cache, float *v_cache,
+                                const float *cos_t, const float *sin_t, int pos, int n_heads, int n_kv, int head_dim,
+                                qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(q && k && v && k_cache && v_cache && cos_t && sin_t, QLIN_ERR_INVALID_ARG, "qlin_rope_kv_append: null");
+    QLIN_REQUIRE(pos >= 0 && n_heads >= 1 && n_kv >= 1 && head_dim >= 2 && head_dim % 2 == 0, QLIN_ERR_INVALID_ARG,
+                 "qlin_rope_kv_append: pos=%d n_heads=%d n_kv=%d head_dim=%d", pos, n_heads, n_kv, head_dim);
+    QLIN_REQUIRE((size_t)n_kv * head_dim * sizeof(float) <= 48 * 1024, QLIN_ERR_UNSUPPORTED, "qlin_rope_kv_append: kv too wide");
+    qlin::rope_kv_kernel<<<1, 256, n_kv * head_dim * sizeof(float), (cudaStream_t)stream>>>(
+        q, k, v, k_cache, v_cache, cos_t, sin_t, pos, n_heads, n_kv, head_dim);
+    QLIN_LAUNCHED("rope_kv_kernel");
+    return QLIN_OK;
+}
+
+size_t qlin_attention_workspace_size(int max_pos, int n_heads, int head_dim) {
+    if (max_pos < 1 || n_heads < 1 || head_dim < 1) return 0;
+    return qlin::attn_ws_floats(max_pos, n_heads, head_dim) * sizeof(float);
+}
+
+qlin_status qlin_attention_decode(const float *q, const float *k_cache, const float *v_cache, int pos, int n_heads,
+                                  int n_kv, int head_dim, float *out, void *workspace, size_t workspace_bytes,
+                                  qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(q && k_cache && v_cache && out && workspace, QLIN_ERR_INVALID_ARG, "qlin_attention_decode: null");
+    QLIN_REQUIRE(pos >= 0 && n_heads >= 1 && n_kv >= 1 && n_heads % n_kv == 0, QLIN_ERR_INVALID_ARG,
+                 "qlin_attention_decode: pos=%d n_heads=%d n_kv=%d", pos, n_heads, n_kv);
+    QLIN_REQUIRE(head_dim >= 16 && head_dim <= 256 && (head_dim & (head_dim - 1)) == 0, QLIN_ERR_UNSUPPORTED,
+                 "qlin_attention_decode: head_dim %d", head_dim);
+    QLIN_REQUIRE(pos < (1 << 20), QLIN_ERR_UNSUPPORTED, "qlin_attention_decode: pos %d", pos);
+    const size_t need = qlin_attention_workspace_size(pos + 1, n_heads, head_dim);
+    QLIN_REQUIRE(workspace_bytes >= need, QLIN_ERR_INVALID_ARG, "qlin_attention_decode: workspace %zu < %zu",
+                 workspace_bytes, need);
+    return qlin::launch_attention(q, k_cache, v_cache, pos, n_heads, n_kv, head_dim, out, (float *)workspace,
+                                  qlin::att_chunks(pos + 1), (cudaStream_t)stream);
+}
+
+qlin_status qlin_geglu(const float *g, const float *u, float *a, int n, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(g && u && a && n >= 1, QLIN_ERR_INVALID_ARG, "qlin_geglu: bad arguments");
+    qlin::geglu_kernel<<<qlin::ceil_div(n, 256), 256, 0, (cudaStream_t)stream>>>(g, u, a, n);
+    QLIN_LAUNCHED("geglu_kernel");
+    return QLIN_OK;
+}
+
+size_t qlin_lm_head_workspace_size(int vocab) {
+    (void)vocab;
+    return sizeof(float2) * (size_t)qlin::lm_head_blocks();
+}
+
+qlin_status qlin_lm_head_argmax(const uint16_t *emb, const float *x, int vocab, int dim, float *logits, int32_t *next,
+                                void *workspace, size_t workspace_bytes, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(emb && x && next && workspace, QLIN_ERR_INVALID_ARG, "qlin_lm_head_argmax: null pointer");
+    QLIN_REQUIRE(vocab >= 1 && dim >= 8 && dim % 8 == 0, QLIN_ERR_INVALID_ARG, "qlin_lm_head_argmax: vocab=%d dim=%d",
+                 vocab, dim);
+    QLIN_REQUIRE(qlin::aligned16(emb) && qlin::aligned16(x), QLIN_ERR_INVALID_ARG, "qlin_lm_head_argmax: misaligned");
+    QLIN_REQUIRE(workspace_bytes >= qlin_lm_head_workspace_size(vocab), QLIN_ERR_INVALID_ARG,
+                 "qlin_lm_head_argmax: workspace too small");
+    return qlin::launch_lm_head(emb, x, vocab, dim, logits, next, (float2 *)workspace, (cudaStream_t)stream);
+}
+
+qlin_status decode_step_t158_workspace_size(const t158_model *m, size_t *bytes) {
+    qlin::clear_error();
+    qlin_status s = qlin::check_model(m);
+    if (s) return s;
+    QLIN_REQUIRE(bytes, QLIN_ERR_INVALID_ARG, "decode_step_t158_workspace_size: null bytes");
+    *bytes = qlin::carve(m, nullptr).bytes;
+    return QLIN_OK;
+}
+
+qlin_status decode_step_t158(const t158_model *m, float *kv_cache, void *workspace, size_t workspace_bytes,
+                             const int32_t *token, int32_t pos, float *logits, int32_t *next_token, qlin_stream_t stream) {
+    qlin::clear_error();
+    qlin_status s = qlin::check_model(m);
+    if (s) return s;
+    QLIN_REQUIRE(kv_cache && workspace && token && next_token, QLIN_ERR_INVALID_ARG, "decode_step_t158: null pointer");
+    QLIN_REQUIRE(pos >= 0 && pos < m->max_pos, QLIN_ERR_INVALID_ARG, "decode_step_t158: pos %d outside [0, %d)", pos,
+                 m->max_pos);
+    QLIN_REQUIRE(qlin::aligned16(workspace), QLIN_ERR_INVALID_ARG, "decode_step_t158: workspace not 16-byte aligned");
+    const qlin::DecodeWs w = qlin::carve(m, (char *)workspace);
+    QLIN_REQUIRE(workspace_bytes >= w.bytes, QLIN_ERR_INVALID_ARG, "decode_step_t158: workspace %zu < %zu bytes",
+                 workspace_bytes, w.bytes);
+    return qlin::decode_sequence(m, kv_cache, w, token, pos, logits, next_token, (cudaStream_t)stream);
+}
+
+int decode_step_t158_launches(const t158_model *m) {
+    qlin::clear_error();
+    if (qlin::check_model(m)) return -1;
+    // embed; per layer 22 (norm, 7 x [quantise + GEMV], RoPE/append, 2 attention, 2 adds, norm, GeGLU); norm + lm_head 2
+    return 1 + 22 * m->n_layers + 3;
+}
+
+qlin_status decode_step_t158_status(void *workspace, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(workspace, QLIN_ERR_INVALID_ARG, "decode_step_t158_status: null workspace");
+    int32_t st[4] = {0, 0, 0, 0};
+    QLIN_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    QLIN_CUDA(cudaMemcpy(st, workspace, sizeof st, cudaMemcpyDeviceToHost));
+    QLIN_CUDA(cudaMemset(workspace, 0, sizeof st));
+    QLIN_REQUIRE(!(st[0] & 2), QLIN_ERR_TIMEOUT, "decode_step_t158: a device-side wait gave up");
+    QLIN_REQUIRE(!(st[0] & 1), QLIN_ERR_INVALID_ARG, "decode_step_t158: token out of range");
+    return QLIN_OK;
+}
+
+}  // extern "C"
