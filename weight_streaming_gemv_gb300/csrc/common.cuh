@@ -49,6 +49,12 @@ inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3
 int sm_count();
 int max_smem_optin();
 
+// Resident blocks per SM of `kern` (blockDim 256) for `smem` dynamic bytes on
+// the current device, with the kernel's dynamic shared-memory limit raised to
+// the opt-in maximum on first use.  Cached per (kernel, device, smem): the
+// CUDA occupancy queries run once, not on every launch.
+int blocks_per_sm(const void *kern, size_t smem);
+
 // ----------------------------------------------------------------- device helpers
 // 16-byte streaming load: read-only path, no L1 allocation (weights are read once).
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {

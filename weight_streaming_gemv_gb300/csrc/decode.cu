@@ -254,7 +254,7 @@ static int lm_head_blocks() { return sm_count() * 4; }
 static qlin_status launch_rmsnorm(const float *x, const float *g, float *out, int M, int n, float eps, cudaStream_t st) {
     const size_t smem = (size_t)next_pow2(n) * sizeof(float);
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "rmsnorm: n=%d too large", n);
-    if (smem > 48 * 1024) QLIN_CUDA(cudaFuncSetAttribute(rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    if (smem > 48 * 1024) blocks_per_sm((const void *)rmsnorm_kernel, smem);
     rmsnorm_kernel<<<M, 256, smem, st>>>(x, g, out, n, eps);
     QLIN_LAUNCHED("rmsnorm_kernel");
     return QLIN_OK;

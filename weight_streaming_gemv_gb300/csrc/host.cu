@@ -2,7 +2,10 @@
 // device attributes and the T158 packing of "Gemma 3 1B at 114 tokens per
 // second on a laptop CPU", "Step 1: a kernel for 1.6-bit weights".
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <set>
+#include <tuple>
 #include <vector>
 
 #include "common.cuh"
@@ -49,6 +52,30 @@ int sm_count() {
 }
 
 int max_smem_optin() { return attr_of_current().smem_optin; }
+
+namespace {
+std::mutex g_occ_mu;
+std::map<std::tuple<const void *, int, size_t>, int> g_occ;
+std::set<std::pair<const void *, int>> g_attr_set;
+}  // namespace
+
+int blocks_per_sm(const void *kern, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    auto key = std::make_tuple(kern, dev, smem);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+    if (!g_attr_set.count({kern, dev})) {
+        const int optin = attr_of_current().smem_optin;
+        if (optin > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        g_attr_set.insert({kern, dev});
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 256, smem) != cudaSuccess || n < 1) n = 1;
+    g_occ[key] = n;
+    return n;
+}
 
 }  // namespace qlin
 

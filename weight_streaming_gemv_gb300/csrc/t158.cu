@@ -186,10 +186,7 @@ static qlin_status launch_t158(const int8_t *xq, const float *xs, const uint8_t 
     const size_t smem = (size_t)MT * C * 5 * sizeof(uint4) + (MT + 32) * sizeof(int);
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "qlin_t158_i8: K=%d needs %zu B of shared memory",
                  K, smem);
-    if (smem > 48 * 1024) QLIN_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    int per_sm = 0;
-    QLIN_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
-    if (per_sm < 1) per_sm = 1;
+    const int per_sm = blocks_per_sm((const void *)kern, smem);
     constexpr int ROWS = (32 / LPR) * R;
     const int64_t warps_needed = (N + ROWS - 1) / ROWS;
     int64_t blocks = (warps_needed + 7) / 8;

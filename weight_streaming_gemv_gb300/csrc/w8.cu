@@ -129,10 +129,7 @@ static qlin_status launch_w8(const float *x, const int8_t *w, int64_t pitch, flo
     const size_t smem = (size_t)MT * C * 16 * sizeof(float);
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "qlin_w8_f32: M tile x K=%d needs %zu B smem", K,
                  smem);
-    if (smem > 48 * 1024) QLIN_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    int per_sm = 0;
-    QLIN_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
-    if (per_sm < 1) per_sm = 1;
+    const int per_sm = blocks_per_sm((const void *)kern, smem);
     const int64_t warps_needed = (N + R - 1) / R;
     int64_t blocks = (warps_needed + 7) / 8;
     const int64_t cap = (int64_t)sm_count() * per_sm;
