@@ -164,6 +164,29 @@ qlin_status qlin_attention_decode(const float *q, const float *k_cache, const fl
                                   int n_heads, int n_kv, int head_dim, float *out, void *workspace,
                                   size_t workspace_bytes, qlin_stream_t stream);
 
+/* Decode attention with no workspace argument, for callers that cannot
+ * allocate device memory (a plugin inside an application that owns all device
+ * memory and gives it no allocator, a real-time loop that cannot risk an
+ * allocation's latency or failure, a process that reserved its memory up
+ * front).  The pages have no counterpart: this is the same computation as
+ * qlin_attention_decode, whose chunk partials here go to a fixed array of
+ * QLIN_ATTENTION_NOALLOC_SCRATCH_BYTES inside the library instead of a
+ * caller workspace.  Every GPU that loads the library holds that array until
+ * the process exits.  The call allocates nothing.
+ *  - Size limit: n_heads * ceil((pos+1)/32) * (head_dim + 2) * 4 bytes must fit
+ *    in the array (e.g. 4 heads of 256 up to pos 2015); larger calls return
+ *    QLIN_ERR_UNSUPPORTED and launch nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents
+ *    (nothing in it needs to start at zero): calls whose kernels overlap on
+ *    the GPU, e.g. on two streams, race on it and give wrong results.
+ * Other arguments as in qlin_attention_decode. */
+#define QLIN_ATTENTION_NOALLOC_SCRATCH_BYTES 262144
+qlin_status qlin_attention_decode_noalloc(const float *q, const float *k_cache, const float *v_cache, int pos,
+                                          int n_heads, int n_kv, int head_dim, float *out, qlin_stream_t stream);
+
 /* S14 (activation)  GeGLU: a = gelu(g) * u with the tanh form of GELU
  * (0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))), [gemma.cpp tour],
  * [cpp20gemma]); tanh(z) = 1 - 2/(e^{2z} + 1) with a Cody-Waite fp32 exp.

@@ -260,8 +260,8 @@ static qlin_status launch_rmsnorm(const float *x, const float *g, float *out, in
     return QLIN_OK;
 }
 
-static qlin_status launch_attention(const float *q, const float *kc, const float *vc, int pos, int nh, int nkv, int hd,
-                                    float *out, float *ws, int ncmax, cudaStream_t st) {
+qlin_status launch_attention(const float *q, const float *kc, const float *vc, int pos, int nh, int nkv, int hd,
+                             float *out, float *ws, int ncmax, cudaStream_t st) {
     const int nc = pos / 32 + 1;
     attn_chunk_kernel<<<dim3(nc, nh), 256, 0, st>>>(q, kc, vc, pos, nh, nkv, hd, ws, ncmax);
     QLIN_LAUNCHED("attn_chunk_kernel");

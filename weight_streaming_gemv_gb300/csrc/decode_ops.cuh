@@ -182,4 +182,9 @@ __device__ __forceinline__ void attention_merge(const float *pm, const float *pS
     __syncthreads();
 }
 
+// Launches the chunk and merge kernels of the decode attention on `st`; `ws`
+// holds n_heads * ncmax * (head_dim + 2) floats, ncmax >= pos/32 + 1.
+qlin_status launch_attention(const float *q, const float *kc, const float *vc, int pos, int nh, int nkv, int hd,
+                             float *out, float *ws, int ncmax, cudaStream_t st);
+
 }  // namespace qlin

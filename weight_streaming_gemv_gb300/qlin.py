@@ -63,6 +63,7 @@ SIGNATURES = {
     "qlin_rope_kv_append": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _ST),
     "qlin_attention_workspace_size": ([_I, _I, _I], _SZ),
     "qlin_attention_decode": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _ST),
+    "qlin_attention_decode_noalloc": ([_P, _P, _P, _I, _I, _I, _I, _P, _P], _ST),
     "qlin_geglu": ([_P, _P, _P, _I, _P], _ST),
     "qlin_lm_head_workspace_size": ([_I], _SZ),
     "qlin_lm_head_argmax": ([_P, _P, _I, _I, _P, _P, _P, _SZ, _P], _ST),
@@ -189,6 +190,18 @@ def qlin_attention_decode(q, k_cache, v_cache, pos, n_heads, n_kv, head_dim, out
     _check("qlin_attention_decode", lib().qlin_attention_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), pos, n_heads,
                                                                 n_kv, head_dim, _ptr(out), _ptr(workspace),
                                                                 workspace_bytes, _stream(stream)))
+
+
+ATTENTION_NOALLOC_SCRATCH_BYTES = 262144
+
+
+def qlin_attention_decode_noalloc(q, k_cache, v_cache, pos, n_heads, n_kv, head_dim, out, stream=None):
+    """Decode attention without a workspace argument, for callers that cannot allocate
+    device memory: the partials go to a fixed 256 KiB array inside the library.  Calls
+    that overlap on the GPU share that array and race."""
+    _check("qlin_attention_decode_noalloc",
+           lib().qlin_attention_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), pos, n_heads, n_kv, head_dim,
+                                               _ptr(out), _stream(stream)))
 
 
 def qlin_geglu(g, u, a, n, stream=None):
