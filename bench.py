@@ -267,7 +267,7 @@ def run_decode(args, rank, local, world):
         },
         "gemv_m1": gemv,
         "roofline": {
-            "kernel": "lm_head_kernel (+argmax_final_kernel)",
+            "kernel": "lm_head_kernel",
             "bound": "hbm", "achieved": round(lm_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(lm_gbs / peak, 4), "traffic": None, "algorithmic_bytes": lm_alg,
             "ms_per_launch": round(lm_ms, 5),

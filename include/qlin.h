@@ -197,7 +197,9 @@ qlin_status qlin_geglu(const float *g, const float *u, float *a, int n, qlin_str
  * logits[v] = sum_i emb[v][i] * x[i] (bf16 table, fp32 x, fp32 accumulate),
  * next = the first index of the maximum.  emb: device bf16 [vocab][dim];
  * x: device fp32 [dim]; logits: device fp32 [vocab] or NULL; next: device
- * int32 [1]; workspace: qlin_lm_head_workspace_size() bytes. */
+ * int32 [1]; workspace: qlin_lm_head_workspace_size() bytes of device memory,
+ * zero-filled before its first use (each call leaves it zero-filled again);
+ * calls sharing a workspace must not overlap on the GPU. */
 size_t qlin_lm_head_workspace_size(int vocab);
 qlin_status qlin_lm_head_argmax(const uint16_t *emb, const float *x, int vocab, int dim, float *logits,
                                 int32_t *next, void *workspace, size_t workspace_bytes, qlin_stream_t stream);
@@ -226,7 +228,9 @@ typedef struct {
     const float *rope_sin;
 } t158_model;
 
-/* Bytes of device scratch decode_step_t158 needs for this model. */
+/* Bytes of device scratch decode_step_t158 needs for this model.  The
+ * workspace must be zero-filled before its first use; steps leave it ready
+ * for the next one.  Steps sharing a workspace must not overlap on the GPU. */
 qlin_status decode_step_t158_workspace_size(const t158_model *m, size_t *bytes);
 
 /* One forward step at position pos (0 <= pos < max_pos) for the token in

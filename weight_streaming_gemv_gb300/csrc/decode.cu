@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "decode_ops.cuh"
+#include "stream.cuh"
 
 namespace qlin {
 
@@ -124,99 +125,154 @@ __global__ void add_kernel(float *h, const float *y, int n) {
 }
 
 // ---------------------------------------------------------------- S16
-// Row r of the bf16 table against fp32 x.  16 lanes per row (16-byte chunks
-// c = lane%16 + 16 j), 2 rows per slot, 2 slots per warp pass.  Each block
-// leaves its best (value, index) in part[blockIdx.x]; ties go to the lower
+// lm_head: logits[r] = emb[r] . x for every row of the bf16 table, and the
+// greedy token.  One persistent CTA per SM owns a contiguous slice of rows
+// and streams it through a ring of shared-memory tiles with TMA bulk copies
+// (warp 0, lane 0 is the producer); eight consumer warps take two rows of a
+// tile each (16 lanes per row, 16-byte chunks) against x in shared memory.
+// Each CTA leaves its best (value, index) in part[]; the last CTA to finish
+// (atomic ticket) reduces them and resets the ticket.  Ties go to the lower
 // index, so the result does not depend on the schedule.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
-__global__ void __launch_bounds__(256) lm_head_kernel(const uint16_t *__restrict__ emb, const float *__restrict__ x,
-                                                      int vocab, int dim, float *__restrict__ logits,
-                                                      float2 *__restrict__ part) {
-    extern __shared__ float4 xs4[];
-    __shared__ float bv_s[8];
-    __shared__ int bi_s[8];
-    float *xsf = reinterpret_cast<float *>(xs4);
-    const int C = dim / 8;  // 16-byte chunks of a bf16 row
-    for (int i = threadIdx.x; i < dim; i += blockDim.x) xsf[i] = x[i];
+constexpr int kLmStages = 4;
+constexpr int kLmConsumers = 8;
+
+struct LmWs {
+    float2 *part;
+    unsigned *ticket;
+    int32_t *status;
+};
+
+__host__ __device__ inline int lm_tile_rows(int dim) {
+    int r = 40960 / (2 * dim);
+    r = r > 16 ? 16 : r;
+    return r < 1 ? 1 : r;
+}
+
+__global__ void __launch_bounds__(288, 1) lm_head_kernel(const uint16_t *__restrict__ emb, const float *__restrict__ x,
+                                                         int vocab, int dim, float *__restrict__ logits, LmWs ws,
+                                                         int32_t *__restrict__ next) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int TR = lm_tile_rows(dim);
+    const int tile_bytes = TR * dim * 2;
+    uint8_t *slots = smem;
+    float4 *xs4 = reinterpret_cast<float4 *>(smem + (size_t)kLmStages * tile_bytes);
+    Ring<kLmStages> *ring = reinterpret_cast<Ring<kLmStages> *>(smem + (size_t)kLmStages * tile_bytes + (size_t)dim * 4);
+    __shared__ float bv_s[kLmConsumers];
+    __shared__ int bi_s[kLmConsumers];
+    __shared__ int last_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r0 = (int64_t)vocab * blockIdx.x / gridDim.x;
+    const int64_t r1 = (int64_t)vocab * (blockIdx.x + 1) / gridDim.x;
+    const int ntiles = (int)((r1 - r0 + TR - 1) / TR);
+    if (threadIdx.x == 0) ring->init(kLmConsumers);
+    // x as two float4 planes: xs4[c] = x[8c..8c+3], xs4[C + c] = x[8c+4..8c+7]
+    const int C = dim / 8;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        xs4[c] = make_float4(x[8 * c], x[8 * c + 1], x[8 * c + 2], x[8 * c + 3]);
+        xs4[C + c] = make_float4(x[8 * c + 4], x[8 * c + 5], x[8 * c + 6], x[8 * c + 7]);
+    }
     __syncthreads();
-    const int lane = threadIdx.x & 31, sub = lane & 15, rsub = lane >> 4;
-    const int warps = blockDim.x >> 5;
-    const int64_t gwarp = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * warps;
+
     float best_v = -__int_as_float(0x7f800000);
     int best_i = 0x7fffffff;
-    for (int64_t r0 = gwarp * 4; r0 < vocab; r0 += nwarps * 4) {
-        float acc[2] = {0.0f, 0.0f};
-#pragma unroll 3
-        for (int c = sub; c < C; c += 16) {
-            uint4 wv[2];
-#pragma unroll
-            for (int r = 0; r < 2; r++) {
-                const int64_t row = r0 + 2 * r + rsub;
-                wv[r] = row < vocab ? ld_stream_v4(emb + row * dim + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first();
+            int t = 0;
+            for (; t < ntiles; t++) {
+                const int s = t % kLmStages;
+                if (t >= kLmStages && !mbar_wait(&ring->empty[s], ((t / kLmStages) - 1) & 1)) {
+                    raise_status(ws.status, kStatusTimeout);
+                    break;
+                }
+                const int64_t row = r0 + (int64_t)t * TR;
+                const int rows = (int)min((int64_t)TR, r1 - row);
+                const uint32_t bytes = (uint32_t)rows * dim * 2;
+                mbar_arrive_expect_tx(&ring->full[s], bytes);
+                bulk_g2s(slots + (size_t)s * tile_bytes, emb + row * dim, bytes, &ring->full[s], pol);
             }
-            const float4 xa = xs4[2 * c], xb = xs4[2 * c + 1];
-#pragma unroll
-            for (int r = 0; r < 2; r++) {
-                float a = acc[r];
-                a = fmaf(__uint_as_float(wv[r].x << 16), xa.x, a);
-                a = fmaf(__uint_as_float(wv[r].x & 0xffff0000u), xa.y, a);
-                a = fmaf(__uint_as_float(wv[r].y << 16), xa.z, a);
-                a = fmaf(__uint_as_float(wv[r].y & 0xffff0000u), xa.w, a);
-                a = fmaf(__uint_as_float(wv[r].z << 16), xb.x, a);
-                a = fmaf(__uint_as_float(wv[r].z & 0xffff0000u), xb.y, a);
-                a = fmaf(__uint_as_float(wv[r].w << 16), xb.z, a);
-                a = fmaf(__uint_as_float(wv[r].w & 0xffff0000u), xb.w, a);
-                acc[r] = a;
-            }
+            // drain: every copy issued must have landed before the CTA leaves
+            for (int u = max(0, t - kLmStages); u < t; u++)
+                if (!mbar_wait(&ring->full[u % kLmStages], (u / kLmStages) & 1)) raise_status(ws.status, kStatusTimeout);
         }
+    } else {
+        const int cw = warp - 1, sub = lane & 15, rsub = lane >> 4;
+        const int rit = 2 * cw + rsub;  // row within a tile
+        for (int t = 0; t < ntiles; t++) {
+            const int s = t % kLmStages;
+            if (!mbar_wait(&ring->full[s], (t / kLmStages) & 1)) {
+                raise_status(ws.status, kStatusTimeout);
+                break;
+            }
+            const int64_t row = r0 + (int64_t)t * TR + rit;
+            const bool valid = rit < TR && row < r1;
+            float acc = 0.0f;
+            if (valid) {
+                const uint8_t *wrow = slots + (size_t)s * tile_bytes + (size_t)rit * dim * 2;
+#pragma unroll 4
+                for (int c = sub; c < C; c += 16) {
+                    const uint4 w = lds128(wrow + (size_t)c * 16);
+                    const float4 xa = xs4[c], xb = xs4[C + c];
+                    acc = fmaf(__uint_as_float(w.x << 16), xa.x, acc);
+                    acc = fmaf(__uint_as_float(w.x & 0xffff0000u), xa.y, acc);
+                    acc = fmaf(__uint_as_float(w.y << 16), xa.z, acc);
+                    acc = fmaf(__uint_as_float(w.y & 0xffff0000u), xa.w, acc);
+                    acc = fmaf(__uint_as_float(w.z << 16), xb.x, acc);
+                    acc = fmaf(__uint_as_float(w.z & 0xffff0000u), xb.y, acc);
+                    acc = fmaf(__uint_as_float(w.w << 16), xb.z, acc);
+                    acc = fmaf(__uint_as_float(w.w & 0xffff0000u), xb.w, acc);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ring->empty[s]);
 #pragma unroll
-        for (int r = 0; r < 2; r++) {
-            float v = acc[r];
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            const int64_t row = r0 + 2 * r + rsub;
-            if (sub == 0 && row < vocab) {
-                if (logits) logits[row] = v;
-                if (better(v, (int)row, best_v, best_i)) {
-                    best_v = v;
+            for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (sub == 0 && valid) {
+                if (logits) logits[row] = acc;
+                if (better(acc, (int)row, best_v, best_i)) {
+                    best_v = acc;
                     best_i = (int)row;
                 }
             }
         }
-    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best_v, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, best_i, off);
-        if (better(ov, oi, best_v, best_i)) {
-            best_v = ov;
-            best_i = oi;
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best_v, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, best_i, off);
+            if (better(ov, oi, best_v, best_i)) {
+                best_v = ov;
+                best_i = oi;
+            }
         }
-    }
-    if (lane == 0) {
-        bv_s[threadIdx.x >> 5] = best_v;
-        bi_s[threadIdx.x >> 5] = best_i;
+        if (lane == 0) {
+            bv_s[cw] = best_v;
+            bi_s[cw] = best_i;
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         float v = bv_s[0];
         int i = bi_s[0];
-        for (int w = 1; w < warps; w++)
+        for (int w = 1; w < kLmConsumers; w++)
             if (better(bv_s[w], bi_s[w], v, i)) {
                 v = bv_s[w];
                 i = bi_s[w];
             }
-        part[blockIdx.x] = make_float2(v, __int_as_float(i));
+        ws.part[blockIdx.x] = make_float2(v, __int_as_float(i));
+        __threadfence();
+        last_s = (atomicAdd(ws.ticket, 1u) == gridDim.x - 1);
     }
-}
-
-__global__ void argmax_final_kernel(const float2 *__restrict__ part, int n, int32_t *next) {
+    __syncthreads();
+    if (!last_s) return;
+    // the last CTA: reduce every CTA's candidate
+    __threadfence();
     float v = -__int_as_float(0x7f800000);
     int i = 0x7fffffff;
-    for (int j = threadIdx.x; j < n; j += blockDim.x) {
-        const float2 p = part[j];
+    for (int j = threadIdx.x; j < (int)gridDim.x; j += blockDim.x) {
+        const float2 p = __ldcg(&ws.part[j]);
         if (better(p.x, __float_as_int(p.y), v, i)) {
             v = p.x;
             i = __float_as_int(p.y);
@@ -231,24 +287,35 @@ __global__ void argmax_final_kernel(const float2 *__restrict__ part, int n, int3
             i = oi;
         }
     }
-    __shared__ float sv[32];
-    __shared__ int si[32];
-    if ((threadIdx.x & 31) == 0) {
-        sv[threadIdx.x >> 5] = v;
-        si[threadIdx.x >> 5] = i;
+    __shared__ float fv[9];
+    __shared__ int fi[9];
+    if (lane == 0) {
+        fv[warp] = v;
+        fi[warp] = i;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         for (int w = 1; w < (int)(blockDim.x >> 5); w++)
-            if (better(sv[w], si[w], v, i)) {
-                v = sv[w];
-                i = si[w];
+            if (better(fv[w], fi[w], v, i)) {
+                v = fv[w];
+                i = fi[w];
             }
         *next = i;
+        *ws.ticket = 0u;
     }
 }
 
-static int lm_head_blocks() { return sm_count() * 4; }
+static int lm_head_blocks() { return sm_count(); }
+
+static size_t lm_ws_bytes() { return 256 + sizeof(float2) * (size_t)lm_head_blocks(); }
+
+static LmWs lm_ws(void *base, int32_t *status) {
+    LmWs w;
+    w.ticket = reinterpret_cast<unsigned *>(base);
+    w.part = reinterpret_cast<float2 *>(reinterpret_cast<char *>(base) + 256);
+    w.status = status;
+    return w;
+}
 
 // ---------------------------------------------------------------- host wrappers
 static qlin_status launch_rmsnorm(const float *x, const float *g, float *out, int M, int n, float eps, cudaStream_t st) {
@@ -272,12 +339,12 @@ qlin_status launch_attention(const float *q, const float *kc, const float *vc, i
 }
 
 static qlin_status launch_lm_head(const uint16_t *emb, const float *x, int vocab, int dim, float *logits, int32_t *next,
-                                  float2 *part, cudaStream_t st) {
-    const int blocks = lm_head_blocks();
-    lm_head_kernel<<<blocks, 256, (size_t)dim * sizeof(float), st>>>(emb, x, vocab, dim, logits, part);
+                                  void *ws, int32_t *status, cudaStream_t st) {
+    const size_t smem = (size_t)kLmStages * lm_tile_rows(dim) * dim * 2 + (size_t)dim * 4 + sizeof(Ring<kLmStages>);
+    QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "lm_head: dim %d too large", dim);
+    blocks_per_sm((const void *)lm_head_kernel, smem);  // raises the dynamic shared-memory limit once
+    lm_head_kernel<<<lm_head_blocks(), 288, smem, st>>>(emb, x, vocab, dim, logits, lm_ws(ws, status), next);
     QLIN_LAUNCHED("lm_head_kernel");
-    argmax_final_kernel<<<1, 256, 0, st>>>(part, blocks, next);
-    QLIN_LAUNCHED("argmax_final_kernel");
     return QLIN_OK;
 }
 
@@ -285,7 +352,7 @@ static qlin_status launch_lm_head(const uint16_t *emb, const float *x, int vocab
 struct DecodeWs {
     float *h, *xn, *q, *k, *v, *att, *y, *g, *u, *xs, *attn;
     int8_t *xq;
-    float2 *part;
+    void *lm;
     int32_t *status;
     size_t bytes;
 };
@@ -315,7 +382,7 @@ static DecodeWs carve(const t158_model *m, char *base) {
     w.xs = (float *)take(sizeof(float) * 4);
     w.xq = (int8_t *)take((size_t)big);
     w.attn = (float *)take(sizeof(float) * attn_ws_floats(m->max_pos, m->n_heads, m->head_dim));
-    w.part = (float2 *)take(sizeof(float2) * (size_t)lm_head_blocks());
+    w.lm = take(lm_ws_bytes());
     w.bytes = off;
     return w;
 }
@@ -388,7 +455,7 @@ static qlin_status decode_sequence(const t158_model *m, float *kv, const DecodeW
         QLIN_LAUNCHED("add_kernel");
     }
     if ((s = launch_rmsnorm(w.h, m->g_final, w.xn, 1, d, m->eps, st))) return s;
-    return launch_lm_head(m->emb, w.xn, m->vocab, d, logits, next, w.part, st);
+    return launch_lm_head(m->emb, w.xn, m->vocab, d, logits, next, w.lm, w.status, st);
 }
 
 }  // namespace qlin
@@ -468,7 +535,7 @@ qlin_status qlin_geglu(const float *g, const float *u, float *a, int n, qlin_str
 
 size_t qlin_lm_head_workspace_size(int vocab) {
     (void)vocab;
-    return sizeof(float2) * (size_t)qlin::lm_head_blocks();
+    return qlin::lm_ws_bytes();
 }
 
 qlin_status qlin_lm_head_argmax(const uint16_t *emb, const float *x, int vocab, int dim, float *logits, int32_t *next,
@@ -480,7 +547,7 @@ qlin_status qlin_lm_head_argmax(const uint16_t *emb, const float *x, int vocab, 
     QLIN_REQUIRE(qlin::aligned16(emb) && qlin::aligned16(x), QLIN_ERR_INVALID_ARG, "qlin_lm_head_argmax: misaligned");
     QLIN_REQUIRE(workspace_bytes >= qlin_lm_head_workspace_size(vocab), QLIN_ERR_INVALID_ARG,
                  "qlin_lm_head_argmax: workspace too small");
-    return qlin::launch_lm_head(emb, x, vocab, dim, logits, next, (float2 *)workspace, (cudaStream_t)stream);
+    return qlin::launch_lm_head(emb, x, vocab, dim, logits, next, workspace, nullptr, (cudaStream_t)stream);
 }
 
 qlin_status decode_step_t158_workspace_size(const t158_model *m, size_t *bytes) {
@@ -510,8 +577,8 @@ qlin_status decode_step_t158(const t158_model *m, float *kv_cache, void *workspa
 int decode_step_t158_launches(const t158_model *m) {
     qlin::clear_error();
     if (qlin::check_model(m)) return -1;
-    // embed; per layer 22 (norm, 7 x [quantise + GEMV], RoPE/append, 2 attention, 2 adds, norm, GeGLU); norm + lm_head 2
-    return 1 + 22 * m->n_layers + 3;
+    // embed; per layer 22 (norm, 7 x [quantise + GEMV], RoPE/append, 2 attention, 2 adds, norm, GeGLU); norm + lm_head
+    return 1 + 22 * m->n_layers + 2;
 }
 
 qlin_status decode_step_t158_status(void *workspace, qlin_stream_t stream) {

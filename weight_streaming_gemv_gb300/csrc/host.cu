@@ -67,8 +67,11 @@ int blocks_per_sm(const void *kern, size_t smem) {
     auto it = g_occ.find(key);
     if (it != g_occ.end()) return it->second;
     if (!g_attr_set.count({kern, dev})) {
+        // dynamic + static shared memory may not exceed the opt-in limit
+        cudaFuncAttributes fa{};
         const int optin = attr_of_current().smem_optin;
-        if (optin > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (cudaFuncGetAttributes(&fa, kern) == cudaSuccess && optin > 48 * 1024)
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
         g_attr_set.insert({kern, dev});
     }
     int n = 0;
