@@ -9,8 +9,7 @@
 #include <algorithm>
 #include <vector>
 
-#include "decode_ops.cuh"
-#include "stream.cuh"
+#include "decode_fused.cuh"
 
 namespace qlin {
 
@@ -33,7 +32,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *x, const floa
     extern __shared__ float buf[];
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
-    rmsnorm_row(x + row * n, g, out + row * n, n, eps, buf, red);
+    rmsnorm_row(x + row * n, g, out + row * n, n, eps, buf, red, whole_block());
 }
 
 // ---------------------------------------------------------------- S11
@@ -56,10 +55,10 @@ __global__ void rope_kv_kernel(float *q, const float *k, const float *v, float *
     const int half = hd / 2;
     const float *c = cos_t + (int64_t)pos * half;
     const float *s = sin_t + (int64_t)pos * half;
-    rope_rotate(q, nh, hd, c, s);
+    rope_rotate(q, nh, hd, c, s, whole_block());
     for (int i = threadIdx.x; i < nkv * hd; i += blockDim.x) kr[i] = k[i];
     __syncthreads();
-    rope_rotate(kr, nkv, hd, c, s);
+    rope_rotate(kr, nkv, hd, c, s, whole_block());
     __syncthreads();
     const int64_t off = (int64_t)pos * nkv * hd;
     for (int i = threadIdx.x; i < nkv * hd; i += blockDim.x) {
@@ -103,7 +102,7 @@ __global__ void __launch_bounds__(256) attn_chunk_kernel(const float *__restrict
     const int ld = nkv * hd;
     AttnWs w = attn_ws(ws, ncmax, nh, hd);
     attention_chunk(qs, kc + (int64_t)t0 * ld + kvh * hd, vc + (int64_t)t0 * ld + kvh * hd, ld, nt, hd,
-                    w.m + h * ncmax + c, w.S + h * ncmax + c, w.U + ((int64_t)h * ncmax + c) * hd, sc);
+                    w.m + h * ncmax + c, w.S + h * ncmax + c, w.U + ((int64_t)h * ncmax + c) * hd, sc, whole_block());
 }
 
 __global__ void __launch_bounds__(256) attn_merge_kernel(const float *ws, int ncmax, int nc, int nh, int hd, float *out) {
@@ -111,7 +110,8 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float *ws, int nc
     __shared__ float red[32];
     const int h = blockIdx.x;
     AttnWs w = attn_ws(const_cast<float *>(ws), ncmax, nh, hd);
-    attention_merge(w.m + h * ncmax, w.S + h * ncmax, w.U + (int64_t)h * ncmax * hd, nc, hd, out + h * hd, wbuf, red);
+    attention_merge(w.m + h * ncmax, w.S + h * ncmax, w.U + (int64_t)h * ncmax * hd, nc, hd, out + h * hd, wbuf, red,
+                    whole_block());
 }
 
 // ---------------------------------------------------------------- S14 / residual
@@ -349,15 +349,21 @@ static qlin_status launch_lm_head(const uint16_t *emb, const float *x, int vocab
 }
 
 // ---------------------------------------------------------------- composed decode step
-struct DecodeWs {
-    float *h, *xn, *q, *k, *v, *att, *y, *g, *u, *xs, *attn;
-    int8_t *xq;
-    void *lm;
-    int32_t *status;
-    size_t bytes;
-};
+// The step runs as one persistent kernel (decode_fused.cu).
+qlin_status launch_decode_fused(const FusedArgs &args, cudaStream_t st);
+size_t fused_smem_bytes(const t158_model *m, int G);
 
 static size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+struct DecodeWs {
+    int32_t *status;
+    unsigned long long *bar_ctr;
+    unsigned *lm_ticket;
+    float2 *lm_part;
+    float *h, *q, *k, *v, *a, *att, *pm, *pS, *pU;
+    int ncmax;
+    size_t bytes;
+};
 
 static DecodeWs carve(const t158_model *m, char *base) {
     DecodeWs w{};
@@ -368,21 +374,20 @@ static DecodeWs carve(const t158_model *m, char *base) {
         return p;
     };
     const int d = m->dim, qd = m->n_heads * m->head_dim, kvd = m->n_kv_heads * m->head_dim, f = m->ffn;
-    const int big = std::max(std::max(d, qd), f);
-    w.status = (int32_t *)take(sizeof(int32_t) * 4);
+    w.ncmax = att_chunks(m->max_pos);
+    w.status = (int32_t *)take(16);  // must stay first: decode_step_t158_status reads offset 0
+    w.bar_ctr = (unsigned long long *)take(8);
+    w.lm_ticket = (unsigned *)take(4);
+    w.lm_part = (float2 *)take(sizeof(float2) * (size_t)sm_count());
     w.h = (float *)take(sizeof(float) * d);
-    w.xn = (float *)take(sizeof(float) * big);
     w.q = (float *)take(sizeof(float) * qd);
     w.k = (float *)take(sizeof(float) * kvd);
     w.v = (float *)take(sizeof(float) * kvd);
+    w.a = (float *)take(sizeof(float) * f);
     w.att = (float *)take(sizeof(float) * qd);
-    w.y = (float *)take(sizeof(float) * big);
-    w.g = (float *)take(sizeof(float) * f);
-    w.u = (float *)take(sizeof(float) * f);
-    w.xs = (float *)take(sizeof(float) * 4);
-    w.xq = (int8_t *)take((size_t)big);
-    w.attn = (float *)take(sizeof(float) * attn_ws_floats(m->max_pos, m->n_heads, m->head_dim));
-    w.lm = take(lm_ws_bytes());
+    w.pm = (float *)take(sizeof(float) * (size_t)m->n_heads * w.ncmax);
+    w.pS = (float *)take(sizeof(float) * (size_t)m->n_heads * w.ncmax);
+    w.pU = (float *)take(sizeof(float) * (size_t)m->n_heads * w.ncmax * m->head_dim);
     w.bytes = off;
     return w;
 }
@@ -400,62 +405,18 @@ static qlin_status check_model(const t158_model *m) {
         QLIN_REQUIRE(m->w[j] && aligned16(m->w[j]), QLIN_ERR_INVALID_ARG, "decode_step_t158: weight %d null/misaligned", j);
         QLIN_REQUIRE(m->pitch[j] % 16 == 0 && m->pitch[j] >= (ins[j] + 4) / 5, QLIN_ERR_INVALID_ARG,
                      "decode_step_t158: pitch[%d]=%lld", j, (long long)m->pitch[j]);
+        QLIN_REQUIRE(m->pitch[j] <= kFSlot, QLIN_ERR_UNSUPPORTED, "decode_step_t158: pitch[%d]=%lld above %d", j,
+                     (long long)m->pitch[j], kFSlot);
     }
-    (void)kvd;
+    QLIN_REQUIRE(32 * kvd * 4 <= kFSlot && d * 2 <= kFSlot, QLIN_ERR_UNSUPPORTED,
+                 "decode_step_t158: kv width %d or dim %d too large for the weight ring", kvd, d);
+    QLIN_REQUIRE(m->max_pos <= 4096, QLIN_ERR_UNSUPPORTED, "decode_step_t158: max_pos %d above 4096", m->max_pos);
+    QLIN_REQUIRE(m->ffn % 4 == 0, QLIN_ERR_UNSUPPORTED, "decode_step_t158: ffn %d not a multiple of 4", m->ffn);
+    QLIN_REQUIRE(next_pow2(m->dim) <= 32 * 128, QLIN_ERR_UNSUPPORTED, "decode_step_t158: dim %d above 4096", m->dim);
     QLIN_REQUIRE(m->scales && m->g_attn && m->g_ffn && m->g_final && m->emb && m->rope_cos && m->rope_sin,
                  QLIN_ERR_INVALID_ARG, "decode_step_t158: null model tensor");
     QLIN_REQUIRE(aligned16(m->emb), QLIN_ERR_INVALID_ARG, "decode_step_t158: emb not 16-byte aligned");
     return QLIN_OK;
-}
-
-qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
-                                   const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st);
-
-qlin_status launch_quant_i8(const float *x, int8_t *xq, float *xs, int M, int K, cudaStream_t st);
-
-// One forward step as a sequence of kernels on `st`.
-static qlin_status decode_sequence(const t158_model *m, float *kv, const DecodeWs &w, const int32_t *token, int pos,
-                                   float *logits, int32_t *next, cudaStream_t st) {
-    const int d = m->dim, nh = m->n_heads, nkv = m->n_kv_heads, hd = m->head_dim, f = m->ffn;
-    const int qd = nh * hd, kvd = nkv * hd;
-    const int ncmax = att_chunks(m->max_pos);
-    const int rows[T158_NMAT] = {qd, kvd, kvd, d, f, f, d};
-    const int ins[T158_NMAT] = {d, d, d, qd, d, d, f};
-    embed_kernel<<<1, 256, 0, st>>>(m->emb, m->vocab, d, token, w.h, w.status);
-    QLIN_LAUNCHED("embed_kernel");
-    auto lin = [&](int l, int j, const float *x, float *out) -> qlin_status {
-        qlin_status qs = launch_quant_i8(x, w.xq, w.xs, 1, ins[j], st);
-        if (qs) return qs;
-        const uint8_t *wt = m->w[j] + (int64_t)l * rows[j] * m->pitch[j];
-        return t158_linear_cuda_cores(w.xq, w.xs, wt, m->pitch[j], 0.0f, m->scales + l * T158_NMAT + j, out, nullptr, 1,
-                                      rows[j], ins[j], st);
-    };
-    qlin_status s;
-    for (int l = 0; l < m->n_layers; l++) {
-        float *kc = kv + (int64_t)(2 * l) * m->max_pos * kvd;
-        float *vc = kv + (int64_t)(2 * l + 1) * m->max_pos * kvd;
-        if ((s = launch_rmsnorm(w.h, m->g_attn + (int64_t)l * d, w.xn, 1, d, m->eps, st))) return s;
-        if ((s = lin(l, 0, w.xn, w.q))) return s;
-        if ((s = lin(l, 1, w.xn, w.k))) return s;
-        if ((s = lin(l, 2, w.xn, w.v))) return s;
-        rope_kv_kernel<<<1, 256, kvd * sizeof(float), st>>>(w.q, w.k, w.v, kc, vc, m->rope_cos, m->rope_sin, pos, nh,
-                                                            nkv, hd);
-        QLIN_LAUNCHED("rope_kv_kernel");
-        if ((s = launch_attention(w.q, kc, vc, pos, nh, nkv, hd, w.att, w.attn, ncmax, st))) return s;
-        if ((s = lin(l, 3, w.att, w.y))) return s;
-        add_kernel<<<ceil_div(d, 256), 256, 0, st>>>(w.h, w.y, d);
-        QLIN_LAUNCHED("add_kernel");
-        if ((s = launch_rmsnorm(w.h, m->g_ffn + (int64_t)l * d, w.xn, 1, d, m->eps, st))) return s;
-        if ((s = lin(l, 4, w.xn, w.g))) return s;
-        if ((s = lin(l, 5, w.xn, w.u))) return s;
-        geglu_kernel<<<ceil_div(f, 256), 256, 0, st>>>(w.g, w.u, w.g, f);
-        QLIN_LAUNCHED("geglu_kernel");
-        if ((s = lin(l, 6, w.g, w.y))) return s;
-        add_kernel<<<ceil_div(d, 256), 256, 0, st>>>(w.h, w.y, d);
-        QLIN_LAUNCHED("add_kernel");
-    }
-    if ((s = launch_rmsnorm(w.h, m->g_final, w.xn, 1, d, m->eps, st))) return s;
-    return launch_lm_head(m->emb, w.xn, m->vocab, d, logits, next, w.lm, w.status, st);
 }
 
 }  // namespace qlin
@@ -567,18 +528,39 @@ qlin_status decode_step_t158(const t158_model *m, float *kv_cache, void *workspa
     QLIN_REQUIRE(kv_cache && workspace && token && next_token, QLIN_ERR_INVALID_ARG, "decode_step_t158: null pointer");
     QLIN_REQUIRE(pos >= 0 && pos < m->max_pos, QLIN_ERR_INVALID_ARG, "decode_step_t158: pos %d outside [0, %d)", pos,
                  m->max_pos);
-    QLIN_REQUIRE(qlin::aligned16(workspace), QLIN_ERR_INVALID_ARG, "decode_step_t158: workspace not 16-byte aligned");
+    QLIN_REQUIRE(qlin::aligned16(workspace) && qlin::aligned16(kv_cache), QLIN_ERR_INVALID_ARG,
+                 "decode_step_t158: workspace or kv_cache not 16-byte aligned");
     const qlin::DecodeWs w = qlin::carve(m, (char *)workspace);
     QLIN_REQUIRE(workspace_bytes >= w.bytes, QLIN_ERR_INVALID_ARG, "decode_step_t158: workspace %zu < %zu bytes",
                  workspace_bytes, w.bytes);
-    return qlin::decode_sequence(m, kv_cache, w, token, pos, logits, next_token, (cudaStream_t)stream);
+    qlin::FusedArgs a{};
+    a.m = *m;
+    a.kv = kv_cache;
+    a.token = token;
+    a.pos = pos;
+    a.logits = logits;
+    a.next = next_token;
+    a.h = w.h;
+    a.q = w.q;
+    a.k = w.k;
+    a.v = w.v;
+    a.a = w.a;
+    a.att = w.att;
+    a.pm = w.pm;
+    a.pS = w.pS;
+    a.pU = w.pU;
+    a.ncmax = w.ncmax;
+    a.lm_part = w.lm_part;
+    a.lm_ticket = w.lm_ticket;
+    a.bar_ctr = w.bar_ctr;
+    a.status = w.status;
+    return qlin::launch_decode_fused(a, (cudaStream_t)stream);
 }
 
 int decode_step_t158_launches(const t158_model *m) {
     qlin::clear_error();
     if (qlin::check_model(m)) return -1;
-    // embed; per layer 22 (norm, 7 x [quantise + GEMV], RoPE/append, 2 attention, 2 adds, norm, GeGLU); norm + lm_head
-    return 1 + 22 * m->n_layers + 2;
+    return 1;  // one persistent kernel per step
 }
 
 qlin_status decode_step_t158_status(void *workspace, qlin_stream_t stream) {

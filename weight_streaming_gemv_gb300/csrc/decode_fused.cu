@@ -1,0 +1,492 @@
+// One decode step of the ternary decoder as a single persistent kernel.
+//
+// The forward pass of llama2.c "The forward pass -- one token, one position"
+// (Steps 0-6), with the block structure of the cpp20gemma README
+// ("Architecture & implementation": h += attn(rmsnorm(h)); h += mlp(rmsnorm(h));
+// logits = lm_head(rmsnorm(h))), every linear layer ternary on int8-quantised
+// inputs ("Gemma 3 1B at 114 tokens per second on a laptop CPU", "Step 2").
+//
+// Grid: one CTA per SM, launched cooperatively so all CTAs are resident.
+// Warp 0 (lane 0) is a TMA producer that streams, in order, this CTA's slice
+// of every weight matrix of every layer, the cached K/V rows of its attention
+// chunks and its rows of the bf16 lm_head table through a ring of shared
+// memory slots; it runs ahead of the computation across phase boundaries, so
+// the weights of a phase are usually on chip before the phase starts.  Warps
+// 1..8 compute.  Per layer there are five phases separated by grid barriers:
+//   P1 RMSNorm + quantise (every CTA, redundantly) -> Q/K/V rows
+//   P2 RoPE, cache append, attention partials per chunk of 32 positions
+//   P3 merge of all chunks (every CTA) -> quantise -> Wo rows -> h += y
+//   P4 RMSNorm + quantise -> gate and up rows -> GeGLU
+//   P5 quantise GeGLU output -> down rows -> h += y
+// then the final RMSNorm and the lm_head with a last-CTA argmax.  Every fp32
+// operation that feeds a quantiser is the same device code, in the same
+// order, as the standalone kernels, so results are bit-identical to them.
+#include "decode_fused.cuh"
+
+namespace qlin {
+
+struct FusedSmem {
+    // offsets in bytes into dynamic shared memory
+    int slots, xr, normbuf, hvec, xv, lmx, qs, ks, vs, wbuf, abuf, gbuf, gam, scl, misc, ring, total;
+};
+
+__host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline FusedSmem fused_smem(const t158_model &m, int G) {
+    FusedSmem s;
+    const int d = m.dim, qd = m.n_heads * m.head_dim, kvd = m.n_kv_heads * m.head_dim;
+    int maxC = 0;
+    for (int j = 0; j < T158_NMAT; j++) maxC = maxC > (int)(m.pitch[j] / 16) ? maxC : (int)(m.pitch[j] / 16);
+    const int ncmax = (m.max_pos + 31) / 32;
+    int o = 0;
+    s.slots = o;
+    o += kFStages * kFSlot;
+    s.xr = o;
+    o = align_up(o + maxC * 80, 128);
+    s.normbuf = o;
+    o = align_up(o + next_pow2(d) * 4, 128);
+    s.hvec = o;
+    o = align_up(o + d * 4, 128);
+    s.xv = o;
+    o = align_up(o + (d > qd ? d : qd) * 4, 128);
+    s.lmx = o;
+    o = align_up(o + d * 4, 128);
+    s.qs = o;
+    o = align_up(o + qd * 4, 128);
+    s.ks = o;
+    o = align_up(o + kvd * 4, 128);
+    s.vs = o;
+    o = align_up(o + kvd * 4, 128);
+    s.wbuf = o;
+    o = align_up(o + m.n_heads * next_pow2(ncmax) * 4, 128);
+    s.abuf = o;
+    o = align_up(o + m.ffn * 4, 128);
+    s.gbuf = o;
+    o = align_up(o + (m.ffn / G + 2) * 4, 128);
+    s.gam = o;  // RMSNorm gains of the next norm (prefetched with cp.async)
+    o = align_up(o + d * 4, 128);
+    s.scl = o;  // every matrix scale of the model
+    o = align_up(o + m.n_layers * T158_NMAT * 4, 128);
+    s.misc = o;  // red[32] f32, ired[32] i32, sc[32] f32, flags
+    o = align_up(o + 512, 128);
+    s.ring = o;
+    o = align_up(o + (int)sizeof(Ring<kFStages>), 128);
+    s.total = o;
+    return s;
+}
+
+__global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedArgs A) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const t158_model &m = A.m;
+    const int G = gridDim.x, b = blockIdx.x;
+    const FusedSmem L = fused_smem(m, G);
+    uint8_t *slots = smem + L.slots;
+    Ring<kFStages> *ring = reinterpret_cast<Ring<kFStages> *>(smem + L.ring);
+    float *red = reinterpret_cast<float *>(smem + L.misc);
+    int *ired = reinterpret_cast<int *>(smem + L.misc + 128);
+    float *sc = reinterpret_cast<float *>(smem + L.misc + 256);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + L.misc + 384);
+    int *last_flag = reinterpret_cast<int *>(smem + L.misc + 388);
+
+    if (threadIdx.x == 0) {
+        ring->init(kFConsumerWarps);
+        *abort = 0;
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        const uint64_t pol = l2_evict_first();
+        int t = 0;
+        bool ok = true;
+        auto push = [&](const Piece &p) {
+            if (!ok) return;
+            const int s = t % kFStages;
+            if (t >= kFStages && !mbar_wait(&ring->empty[s], ((t / kFStages) - 1) & 1)) {
+                raise_status(A.status, kStatusTimeout);
+                ok = false;
+                return;
+            }
+            const uint32_t bytes = (uint32_t)p.rows * (uint32_t)p.pitch;
+            mbar_arrive_expect_tx(&ring->full[s], bytes);
+            bulk_g2s(slots + (size_t)s * kFSlot, p.src, bytes, &ring->full[s], pol);
+            t++;
+        };
+        for (int l = 0; l < m.n_layers && ok; l++) layer_items(A, l, b, G, push);
+        lm_items(A, b, G, push);
+        for (int u = max(0, t - kFStages); u < t; u++)
+            if (!mbar_wait(&ring->full[u % kFStages], (u / kFStages) & 1)) raise_status(A.status, kStatusTimeout);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const Grp g{(int)threadIdx.x - 32, 32 * kFConsumerWarps, 1};
+    const int d = m.dim, nh = m.n_heads, nkv = m.n_kv_heads, hd = m.head_dim, ff = m.ffn;
+    const int qd = nh * hd, kvd = nkv * hd, half = hd / 2;
+    uint4 *xr = reinterpret_cast<uint4 *>(smem + L.xr);
+    float *normbuf = reinterpret_cast<float *>(smem + L.normbuf);
+    float *hvec = reinterpret_cast<float *>(smem + L.hvec);
+    float *xv = reinterpret_cast<float *>(smem + L.xv);
+    float4 *lmx = reinterpret_cast<float4 *>(smem + L.lmx);
+    float *qs = reinterpret_cast<float *>(smem + L.qs);
+    float *ks = reinterpret_cast<float *>(smem + L.ks);
+    float *vs = reinterpret_cast<float *>(smem + L.vs);
+    float *wbuf = reinterpret_cast<float *>(smem + L.wbuf);
+    float *gbuf = reinterpret_cast<float *>(smem + L.gbuf);
+    float *abuf = reinterpret_cast<float *>(smem + L.abuf);
+    float *gam = reinterpret_cast<float *>(smem + L.gam);
+    float *scl = reinterpret_cast<float *>(smem + L.scl);
+
+    int t = 0;  // ring item counter, mirrors the producer
+    unsigned long long nbar = 0;
+    // One thread waits for a slot, then the named barrier releases the group, so
+    // every consumer thread sees the same abort flag.  After an abort nothing
+    // waits any more: the remaining items are skipped.
+    auto wait_full = [&](int item) {
+        if (g.tid == 0 && !*abort && !mbar_wait(&ring->full[item % kFStages], (item / kFStages) & 1)) {
+            raise_status(A.status, kStatusTimeout);
+            *abort = 1;
+        }
+        g.sync();
+    };
+    auto take = [&](Piece &) -> const uint8_t * {
+        wait_full(t);
+        return slots + (size_t)(t % kFStages) * kFSlot;
+    };
+    auto give = [&]() {
+        g.sync();  // every consumer thread is done with the slot
+        if (g.lane() == 0 && !*abort) mbar_arrive(&ring->empty[t % kFStages]);
+        t++;
+    };
+    auto barrier = [&]() -> bool {
+        nbar++;
+        return grid_barrier(A.bar_ctr, nbar * (unsigned long long)G, A.status, abort, g);
+    };
+
+    int H0, H1;  // residual rows owned by this CTA (Wo and down outputs)
+    share(d, b, G, H0, H1);
+    int J0, J1;
+    share(ff, b, G, J0, J1);
+
+    for (int i = g.tid; i < m.n_layers * T158_NMAT; i += g.n) scl[i] = m.scales[i];
+    cp_async_f4(gam, m.g_attn, d, g);  // gains of the first norm
+
+    // Step 0: h = emb[token] (every CTA for its norm; owners seed the global h)
+    int tok = *A.token;
+    if (tok < 0 || tok >= m.vocab) {
+        if (g.tid == 0) raise_status(A.status, kStatusBadToken);
+        tok = -1;
+    }
+    for (int i = g.tid; i < d; i += g.n) {
+        const float e = tok >= 0 ? __uint_as_float((uint32_t)m.emb[(int64_t)tok * d + i] << 16) : 0.0f;
+        hvec[i] = e;
+        if (i >= H0 && i < H1) A.h[i] = e;
+    }
+    g.sync();
+
+    const float *cos_p = m.rope_cos + (int64_t)A.pos * half;
+    const float *sin_p = m.rope_sin + (int64_t)A.pos * half;
+    const int nc = A.pos / 32 + 1;
+
+    for (int l = 0; l < m.n_layers; l++) {
+        const float *sc_l = scl + l * T158_NMAT;
+        float *kc = A.kv + (int64_t)(2 * l) * m.max_pos * kvd;
+        float *vc = A.kv + (int64_t)(2 * l + 1) * m.max_pos * kvd;
+        // ---------------- P1: norm, quantise, Q K V
+        cp_async_wait(g);
+        if (l > 0) {
+            rmsnorm_from_l2(A.h, gam, hvec, xv, d, m.eps, red, g);
+        } else {
+            rmsnorm_row(hvec, gam, xv, d, m.eps, normbuf, red, g);
+            g.sync();
+        }
+        float xs = quant_scale(group_absmax(xv, d, red, g));
+        int sumx = quant_planes(xv, d, xs, (int)(m.pitch[0] / 16), xr, ired, g);
+        cp_async_f4(gam, m.g_ffn + (int64_t)l * d, d, g);  // for P4 (gam was consumed by the norm)
+        {
+            int lo, hi;
+            share(qd + 2 * kvd, b, G, lo, hi);
+            int base = 0;
+            const int rows3[3] = {qd, kvd, kvd};
+            float *outs[3] = {A.q, A.k, A.v};
+#pragma unroll
+            for (int j = 0; j < 3; j++) {
+                const int a0 = max(lo, base), a1 = min(hi, base + rows3[j]);
+                if (a1 > a0) {
+                    const float ws = sc_l[j];
+                    float *out = outs[j];
+                    pieces(m.w[j], m.pitch[j], a0 - base, a1 - base, j, [&](const Piece &p) {
+                        const uint8_t *slot = take(const_cast<Piece &>(p));
+                        if (!*abort)
+                            slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
+                                out[p.row0 + r] = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
+                            });
+                        give();
+                    });
+                }
+                base += rows3[j];
+            }
+        }
+        if (!barrier()) break;
+
+        // ---------------- P2: RoPE, cache append, attention partials
+        load_l2_f4(qs, A.q, qd, g);
+        load_l2_f4(ks, A.k, kvd, g);
+        load_l2_f4(vs, A.v, kvd, g);
+        g.sync();
+        rope_rotate(qs, nh, hd, cos_p, sin_p, g);
+        rope_rotate(ks, nkv, hd, cos_p, sin_p, g);
+        g.sync();
+        if (b == ((A.pos / 32) * nh) % G) {  // owner of item (chunk of pos, head 0) appends k, v
+            for (int i = g.tid; i < kvd; i += g.n) {
+                kc[(int64_t)A.pos * kvd + i] = ks[i];
+                vc[(int64_t)A.pos * kvd + i] = vs[i];
+            }
+        }
+        for (int e = b; e < nc * nh; e += G) {
+            const int c = e / nh, hh = e % nh;
+            const int t0 = 32 * c, npre = min(t0 + 32, A.pos) - t0;
+            const int nt = min(32, A.pos + 1 - t0);
+            const float *Kc = ks, *Vc = vs;
+            uint8_t *kslot = nullptr, *vslot = nullptr;
+            if (npre > 0) {
+                // K rows are item t, V rows item t+1; both are held until the chunk is done
+                wait_full(t);
+                wait_full(t + 1);
+                kslot = slots + (size_t)(t % kFStages) * kFSlot;
+                vslot = slots + (size_t)((t + 1) % kFStages) * kFSlot;
+                if (nt > npre && !*abort) {  // the current position goes after the cached rows
+                    for (int i = g.tid; i < kvd; i += g.n) {
+                        reinterpret_cast<float *>(kslot)[npre * kvd + i] = ks[i];
+                        reinterpret_cast<float *>(vslot)[npre * kvd + i] = vs[i];
+                    }
+                    // these generic-proxy writes must be ordered before the next TMA write of the slots
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                g.sync();
+                Kc = reinterpret_cast<const float *>(kslot);
+                Vc = reinterpret_cast<const float *>(vslot);
+            }
+            if (!*abort) {
+                const int kvh = hh / (nh / nkv);
+                attention_chunk(qs + hh * hd, Kc + kvh * hd, Vc + kvh * hd, kvd, nt, hd,
+                                A.pm + (int64_t)hh * A.ncmax + c, A.pS + (int64_t)hh * A.ncmax + c,
+                                A.pU + ((int64_t)hh * A.ncmax + c) * hd, sc, g);
+            }
+            if (npre > 0) {
+                give();
+                give();
+            }
+        }
+        if (!barrier()) break;
+
+        // ---------------- P3a: merge, one output element per warp, spread over the CTAs
+        {
+            int o0, o1;
+            share(qd, b, G, o0, o1);
+            for (int e = o0 + g.warp(); e < o1; e += kFConsumerWarps) {
+                const int hh = e / hd, i = e % hd;
+                const float o = attention_merge_one(A.pm + (int64_t)hh * A.ncmax, A.pS + (int64_t)hh * A.ncmax,
+                                                    A.pU + (int64_t)hh * A.ncmax * hd, nc, hd, i, g.lane());
+                if (g.lane() == 0) A.att[e] = o;
+            }
+        }
+        if (!barrier()) break;
+        // ---------------- P3b: quantise, Wo, residual
+        load_l2_f4(xv, A.att, qd, g);
+        g.sync();
+        xs = quant_scale(group_absmax(xv, qd, red, g));
+        sumx = quant_planes(xv, qd, xs, (int)(m.pitch[3] / 16), xr, ired, g);
+        {
+            const float ws = sc_l[3];
+            pieces(m.w[3], m.pitch[3], H0, H1, 3, [&](const Piece &p) {
+                const uint8_t *slot = take(const_cast<Piece &>(p));
+                if (!*abort)
+                    slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
+                        const int row = p.row0 + r;
+                        const float y = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
+                        A.h[row] = __fadd_rn(A.h[row], y);
+                    });
+                give();
+            });
+        }
+        if (!barrier()) break;
+
+        // ---------------- P4: norm, quantise, gate and up, GeGLU
+        cp_async_wait(g);
+        rmsnorm_from_l2(A.h, gam, hvec, xv, d, m.eps, red, g);
+        xs = quant_scale(group_absmax(xv, d, red, g));
+        sumx = quant_planes(xv, d, xs, (int)(m.pitch[4] / 16), xr, ired, g);
+        cp_async_f4(gam, l + 1 < m.n_layers ? m.g_attn + (int64_t)(l + 1) * d : m.g_final, d, g);
+        {
+            const float wsg = sc_l[4], wsu = sc_l[5];
+            pieces(m.w[4], m.pitch[4], J0, J1, 4, [&](const Piece &p) {
+                const uint8_t *slot = take(const_cast<Piece &>(p));
+                if (!*abort)
+                    slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
+                        gbuf[p.row0 + r - J0] = __fmul_rn(__fmul_rn((float)(acc - sumx), wsg), xs);
+                    });
+                give();
+            });
+            pieces(m.w[5], m.pitch[5], J0, J1, 5, [&](const Piece &p) {
+                const uint8_t *slot = take(const_cast<Piece &>(p));
+                if (!*abort)
+                    slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
+                        const int row = p.row0 + r;
+                        const float u = __fmul_rn(__fmul_rn((float)(acc - sumx), wsu), xs);
+                        A.a[row] = __fmul_rn(gelu32(gbuf[row - J0]), u);
+                    });
+                give();
+            });
+        }
+        if (!barrier()) break;
+
+        // ---------------- P5: quantise GeGLU output, down, residual
+        load_l2_f4(abuf, A.a, ff, g);
+        g.sync();
+        xs = quant_scale(group_absmax(abuf, ff, red, g));
+        sumx = quant_planes(abuf, ff, xs, (int)(m.pitch[6] / 16), xr, ired, g);
+        {
+            const float ws = sc_l[6];
+            pieces(m.w[6], m.pitch[6], H0, H1, 6, [&](const Piece &p) {
+                const uint8_t *slot = take(const_cast<Piece &>(p));
+                if (!*abort)
+                    slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
+                        const int row = p.row0 + r;
+                        const float y = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
+                        A.h[row] = __fadd_rn(A.h[row], y);
+                    });
+                give();
+            });
+        }
+        if (!barrier()) break;
+    }
+
+    // ---------------- final norm, lm_head, argmax
+    float best_v = -__int_as_float(0x7f800000);
+    int best_i = 0x7fffffff;
+    if (!*abort) {
+        cp_async_wait(g);
+        rmsnorm_from_l2(A.h, gam, hvec, xv, d, m.eps, red, g);
+        const int C = d / 8;
+        for (int c = g.tid; c < C; c += g.n) {
+            lmx[c] = make_float4(xv[8 * c], xv[8 * c + 1], xv[8 * c + 2], xv[8 * c + 3]);
+            lmx[C + c] = make_float4(xv[8 * c + 4], xv[8 * c + 5], xv[8 * c + 6], xv[8 * c + 7]);
+        }
+        g.sync();
+        const int sub = lane & 15, rsub = lane >> 4, cw = g.warp();
+        lm_items(A, b, G, [&](const Piece &p) {
+            const uint8_t *slot = take(const_cast<Piece &>(p));
+            if (!*abort) {
+                for (int r0 = 2 * cw; r0 < p.rows; r0 += 2 * kFConsumerWarps) {
+                    const int rit = r0 + rsub;
+                    float acc = 0.0f;
+                    if (rit < p.rows) {
+                        const uint8_t *wrow = slot + (size_t)rit * p.pitch;
+#pragma unroll 4
+                        for (int c = sub; c < C; c += 16) {
+                            const uint4 w = lds128(wrow + (size_t)c * 16);
+                            const float4 xa = lmx[c], xb = lmx[C + c];
+                            acc = fmaf(__uint_as_float(w.x << 16), xa.x, acc);
+                            acc = fmaf(__uint_as_float(w.x & 0xffff0000u), xa.y, acc);
+                            acc = fmaf(__uint_as_float(w.y << 16), xa.z, acc);
+                            acc = fmaf(__uint_as_float(w.y & 0xffff0000u), xa.w, acc);
+                            acc = fmaf(__uint_as_float(w.z << 16), xb.x, acc);
+                            acc = fmaf(__uint_as_float(w.z & 0xffff0000u), xb.y, acc);
+                            acc = fmaf(__uint_as_float(w.w << 16), xb.z, acc);
+                            acc = fmaf(__uint_as_float(w.w & 0xffff0000u), xb.w, acc);
+                        }
+                    }
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                    const int row = p.row0 + rit;
+                    if (sub == 0 && rit < p.rows) {
+                        if (A.logits) A.logits[row] = acc;
+                        if (acc > best_v || (acc == best_v && row < best_i)) {
+                            best_v = acc;
+                            best_i = row;
+                        }
+                    }
+                }
+            }
+            give();
+        });
+    }
+    // CTA argmax -> part[b]; the last CTA reduces and resets the shared counters
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best_v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, best_i, off);
+        if (ov > best_v || (ov == best_v && oi < best_i)) {
+            best_v = ov;
+            best_i = oi;
+        }
+    }
+    if (lane == 0) {
+        red[g.warp()] = best_v;
+        ired[g.warp()] = best_i;
+    }
+    g.sync();
+    if (g.tid == 0) {
+        float v = red[0];
+        int i = ired[0];
+        for (int w = 1; w < kFConsumerWarps; w++)
+            if (red[w] > v || (red[w] == v && ired[w] < i)) {
+                v = red[w];
+                i = ired[w];
+            }
+        A.lm_part[b] = make_float2(v, __int_as_float(i));
+        __threadfence();
+        *last_flag = (atomicAdd(A.lm_ticket, 1u) == (unsigned)G - 1);
+    }
+    g.sync();
+    if (!*last_flag) return;
+    __threadfence();
+    if (g.tid < 32) {
+        float v = -__int_as_float(0x7f800000);
+        int i = 0x7fffffff;
+        for (int j = g.tid; j < G; j += 32) {
+            const float2 pp = __ldcg(&A.lm_part[j]);
+            const int pi = __float_as_int(pp.y);
+            if (pp.x > v || (pp.x == v && pi < i)) {
+                v = pp.x;
+                i = pi;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+            if (ov > v || (ov == v && oi < i)) {
+                v = ov;
+                i = oi;
+            }
+        }
+        if (g.tid == 0) {
+            *A.next = i;
+            *A.lm_ticket = 0u;
+            *A.bar_ctr = 0ull;
+        }
+    }
+}
+
+size_t fused_smem_bytes(const t158_model *m, int G) { return (size_t)fused_smem(*m, G).total; }
+
+qlin_status launch_decode_fused(const FusedArgs &args, cudaStream_t st) {
+    const int G = sm_count();
+    const size_t smem = fused_smem_bytes(&args.m, G);
+    QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED,
+                 "decode_step_t158: the model needs %zu B of shared memory per CTA", smem);
+    blocks_per_sm((const void *)decode_fused_kernel, smem);  // raises the dynamic shared-memory limit
+    int per_sm = 0;
+    QLIN_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel, kFThreads, smem));
+    QLIN_REQUIRE(per_sm >= 1, QLIN_ERR_UNSUPPORTED, "decode_step_t158: fused kernel cannot be resident");
+    FusedArgs a = args;
+    void *params[] = {&a};
+    QLIN_CUDA(cudaLaunchCooperativeKernel((const void *)decode_fused_kernel, dim3(G), dim3(kFThreads), params, smem, st));
+    return QLIN_OK;
+}
+
+}  // namespace qlin
