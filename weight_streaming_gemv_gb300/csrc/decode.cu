@@ -412,7 +412,9 @@ static qlin_status check_model(const t158_model *m) {
                  "decode_step_t158: kv width %d or dim %d too large for the weight ring", kvd, d);
     QLIN_REQUIRE(m->max_pos <= 4096, QLIN_ERR_UNSUPPORTED, "decode_step_t158: max_pos %d above 4096", m->max_pos);
     QLIN_REQUIRE(m->ffn % 4 == 0, QLIN_ERR_UNSUPPORTED, "decode_step_t158: ffn %d not a multiple of 4", m->ffn);
-    QLIN_REQUIRE(next_pow2(m->dim) <= 32 * 128, QLIN_ERR_UNSUPPORTED, "decode_step_t158: dim %d above 4096", m->dim);
+    QLIN_REQUIRE(m->dim <= 4096, QLIN_ERR_UNSUPPORTED, "decode_step_t158: dim %d above 4096", m->dim);
+    QLIN_REQUIRE(t158_pitch(m->dim) <= 4 * 32 * kFConsumerWarps, QLIN_ERR_UNSUPPORTED,
+                 "decode_step_t158: dim %d needs more than four packed bytes per thread", m->dim);
     QLIN_REQUIRE(m->scales && m->g_attn && m->g_ffn && m->g_final && m->emb && m->rope_cos && m->rope_sin,
                  QLIN_ERR_INVALID_ARG, "decode_step_t158: null model tensor");
     QLIN_REQUIRE(aligned16(m->emb), QLIN_ERR_INVALID_ARG, "decode_step_t158: emb not 16-byte aligned");

@@ -63,8 +63,8 @@ __host__ __device__ inline FusedSmem fused_smem(const t158_model &m, int G) {
     o = align_up(o + m.ffn * 4, 128);
     s.gbuf = o;
     o = align_up(o + (m.ffn / G + 2) * 4, 128);
-    s.gam = o;  // RMSNorm gains of the next norm (prefetched with cp.async)
-    o = align_up(o + d * 4, 128);
+    s.gam = o;  // RMSNorm gains of the next norm (cp.async; the transposed layout spans next_pow2(d) floats)
+    o = align_up(o + next_pow2(d) * 4, 128);
     s.scl = o;  // every matrix scale of the model
     o = align_up(o + m.n_layers * T158_NMAT * 4, 128);
     s.misc = o;  // red[32] f32, ired[32] i32, sc[32] f32, flags
@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     float *sc = reinterpret_cast<float *>(smem + L.misc + 256);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L.misc + 384);
     int *last_flag = reinterpret_cast<int *>(smem + L.misc + 388);
+    int *isum = reinterpret_cast<int *>(smem + L.misc + 392);
 
     if (threadIdx.x == 0) {
         ring->init(kFConsumerWarps);
@@ -196,14 +197,14 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
         float *vc = A.kv + (int64_t)(2 * l + 1) * m.max_pos * kvd;
         // ---------------- P1: norm, quantise, Q K V
         cp_async_wait(g);
-        if (l > 0) {
-            rmsnorm_from_l2(A.h, gam, hvec, xv, d, m.eps, red, g);
-        } else {
-            rmsnorm_row(hvec, gam, xv, d, m.eps, normbuf, red, g);
-            g.sync();
-        }
-        float xs = quant_scale(group_absmax(xv, d, red, g));
-        int sumx = quant_planes(xv, d, xs, (int)(m.pitch[0] / 16), xr, ired, g);
+        int sumx;
+        float xs;
+        if (l > 0)
+            xs = norm_quant([&](int u) { return __ldcg(reinterpret_cast<const float4 *>(A.h) + u); }, gam, d, m.eps,
+                            hvec, xv, xr, (int)(m.pitch[0] / 16), red, isum, &sumx, g);
+        else
+            xs = norm_quant([&](int u) { return reinterpret_cast<const float4 *>(hvec)[u]; }, gam, d, m.eps, normbuf,
+                            xv, xr, (int)(m.pitch[0] / 16), red, isum, &sumx, g);
         cp_async_f4(gam, m.g_ffn + (int64_t)l * d, d, g);  // for P4 (gam was consumed by the norm)
         {
             int lo, hi;
@@ -295,10 +296,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
         }
         if (!barrier()) break;
         // ---------------- P3b: quantise, Wo, residual
-        load_l2_f4(xv, A.att, qd, g);
-        g.sync();
-        xs = quant_scale(group_absmax(xv, qd, red, g));
-        sumx = quant_planes(xv, qd, xs, (int)(m.pitch[3] / 16), xr, ired, g);
+        xs = quant_from_l2(A.att, qd, xv, xr, (int)(m.pitch[3] / 16), red, isum, &sumx, g);
         {
             const float ws = sc_l[3];
             pieces(m.w[3], m.pitch[3], H0, H1, 3, [&](const Piece &p) {
@@ -316,9 +314,8 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
 
         // ---------------- P4: norm, quantise, gate and up, GeGLU
         cp_async_wait(g);
-        rmsnorm_from_l2(A.h, gam, hvec, xv, d, m.eps, red, g);
-        xs = quant_scale(group_absmax(xv, d, red, g));
-        sumx = quant_planes(xv, d, xs, (int)(m.pitch[4] / 16), xr, ired, g);
+        xs = norm_quant([&](int u) { return __ldcg(reinterpret_cast<const float4 *>(A.h) + u); }, gam, d, m.eps, hvec,
+                        xv, xr, (int)(m.pitch[4] / 16), red, isum, &sumx, g);
         cp_async_f4(gam, l + 1 < m.n_layers ? m.g_attn + (int64_t)(l + 1) * d : m.g_final, d, g);
         {
             const float wsg = sc_l[4], wsu = sc_l[5];
@@ -344,10 +341,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
         if (!barrier()) break;
 
         // ---------------- P5: quantise GeGLU output, down, residual
-        load_l2_f4(abuf, A.a, ff, g);
-        g.sync();
-        xs = quant_scale(group_absmax(abuf, ff, red, g));
-        sumx = quant_planes(abuf, ff, xs, (int)(m.pitch[6] / 16), xr, ired, g);
+        xs = quant_from_l2(A.a, ff, abuf, xr, (int)(m.pitch[6] / 16), red, isum, &sumx, g);
         {
             const float ws = sc_l[6];
             pieces(m.w[6], m.pitch[6], H0, H1, 6, [&](const Piece &p) {

@@ -175,6 +175,215 @@ __device__ __forceinline__ int quant_planes(const float *v, int K, float scale, 
     return t;
 }
 
+// Codes of v (shared memory, K elements) for step `scale` into the plane
+// layout, one packed byte per thread (as quant_planes), with the sum of the
+// codes accumulated into *isum (shared memory, zeroed by the caller before the
+// last group barrier).  No group barrier inside: the caller syncs once after.
+__device__ __forceinline__ void planes_from_smem(const float *v, int K, float scale, int C, uint4 *xr, int *isum,
+                                                 Grp g) {
+    uint32_t *xw = reinterpret_cast<uint32_t *>(xr);
+    const int nbytes = C * 16;
+    const int lane = g.lane();
+    int s = 0;
+    for (int j0 = 0; j0 < nbytes; j0 += g.n) {
+        const int j = j0 + g.tid;
+        uint32_t code[5];
+#pragma unroll
+        for (int i = 0; i < 5; i++) {
+            const int k = 5 * j + i;
+            const int q = (j < nbytes && k < K) ? quant_code(v[k], scale) : 0;
+            s += q;
+            code[i] = (uint32_t)(q & 0xff);
+        }
+#pragma unroll
+        for (int i = 0; i < 5; i++) {
+            uint32_t w = code[i] << (8 * (lane & 3));
+            w |= __shfl_xor_sync(0xffffffffu, w, 1);
+            w |= __shfl_xor_sync(0xffffffffu, w, 2);
+            if ((lane & 3) == 0 && j < nbytes) xw[(j >> 4) * 20 + i * 4 + ((j >> 2) & 3)] = w;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) atomicAdd(isum, s);
+}
+
+// RMSNorm + absmax quantisation of a d-vector (d <= 4096, d % 4 == 0) into
+// the planes, with three group barriers.  load4(u) gives elements 4u..4u+3
+// (from L2 or shared memory).  The first T threads (T = the largest power of
+// two not above the group) load the S = next_pow2(d)/T consecutive leaves of
+// their segment of the pairwise tree (S <= 32, in float4 units when S >= 4),
+// square and sum them as a balanced tree, then lanes, then warps; every
+// thread then finishes the tree itself from the warp sums.  Each thread
+// normalises the five elements of its own packed byte(s), takes the absmax
+// over the group and writes its codes into the planes.  gam and the staged x
+// (xs) are in natural order in shared memory; xn receives the normalised
+// vector.  Returns the step; *sumx gets the sum of the codes.  The arithmetic
+// is that of rmsnorm_row and the absmax quantiser.
+template <class Load4>
+__device__ __forceinline__ float norm_quant(Load4 load4, const float *gam, int d, float eps, float *xs, float *xn,
+                                            uint4 *xr, int C, float *red, int *isum, int *sumx, Grp g) {
+    int T = 32;
+    while (2 * T <= g.n) T *= 2;
+    const int P = next_pow2(d);
+    const int S = P >= T ? P / T : 1;
+    const int t = g.tid;
+    float part = 0.0f;
+    if (t < T) {
+        float v[32];
+        if (S >= 4) {
+            float4 w[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) w[j] = load4(min(t * S / 4 + j, d / 4 - 1));  // clamped: all in flight
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const bool ok = 4 * j < S && t * S + 4 * j < d;
+                v[4 * j] = ok ? w[j].x : 0.0f;
+                v[4 * j + 1] = ok ? w[j].y : 0.0f;
+                v[4 * j + 2] = ok ? w[j].z : 0.0f;
+                v[4 * j + 3] = ok ? w[j].w : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                if (4 * j < S && t * S + 4 * j < d)
+                    reinterpret_cast<float4 *>(xs)[t * S / 4 + j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                                                                v[4 * j + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; i++) v[i] = 0.0f;
+            for (int i = 0; i < S; i++) {
+                const int e = t * S + i;
+                if (e < d) {
+                    const float4 q = load4(e / 4);
+                    const int c = e % 4;
+                    const float xe = c == 0 ? q.x : c == 1 ? q.y : c == 2 ? q.z : q.w;
+                    xs[e] = xe;
+                    if (i == 0) v[0] = xe; else if (i == 1) v[1] = xe; else v[2 + (i & 1)] = xe;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i++) v[i] = __fmul_rn(v[i], v[i]);
+#pragma unroll
+        for (int st = 1; st < 32; st <<= 1)
+#pragma unroll
+            for (int i = 0; i < 32; i += 2 * st)
+                if (st < S) v[i] = __fadd_rn(v[i], v[i + st]);
+        part = v[0];
+    }
+    part = warp_psum(part);
+    if ((t & 31) == 0 && t < T) red[t >> 5] = part;
+    g.sync();  // 1: warp sums and the staged vector are visible
+    float ss;
+    {
+        const int W = T >> 5;  // a power of two <= 8
+        float w8[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) w8[i] = i < W ? red[i] : 0.0f;
+#pragma unroll
+        for (int st = 1; st < 8; st <<= 1)
+#pragma unroll
+            for (int i = 0; i < 8; i += 2 * st)
+                if (st < W) w8[i] = __fadd_rn(w8[i], w8[i + st]);
+        ss = w8[0];
+    }
+    ss = __fdiv_rn(ss, (float)d);
+    ss = __fadd_rn(ss, eps);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(ss));
+    // normalised values of this thread's packed bytes j = t, t + n, ...
+    const int nbytes = C * 16;
+    constexpr int MAXB = 4;  // bytes per thread (nbytes <= 4 * group size)
+    float o[MAXB][5];
+    float amax = 0.0f;
+#pragma unroll
+    for (int bi = 0; bi < MAXB; bi++) {
+        const int j = t + bi * g.n;
+#pragma unroll
+        for (int i = 0; i < 5; i++) {
+            const int k = 5 * j + i;
+            float val = 0.0f;
+            if (j < nbytes && k < d) {
+                val = __fmul_rn(gam[k], __fmul_rn(r, xs[k]));
+                xn[k] = val;
+                amax = fmaxf(amax, fabsf(val));
+            }
+            o[bi][i] = val;
+        }
+    }
+    amax = warp_max(amax);
+    if (g.lane() == 0) red[8 + g.warp()] = amax;
+    if (t == 0) *isum = 0;
+    g.sync();  // 2: absmax parts
+    float m = red[8];
+    for (int w = 1; w < (g.n >> 5); w++) m = fmaxf(m, red[8 + w]);
+    const float scale = quant_scale(m);
+    uint32_t *xw = reinterpret_cast<uint32_t *>(xr);
+    const int lane = g.lane();
+    int sacc = 0;
+#pragma unroll
+    for (int bi = 0; bi < MAXB; bi++) {
+        const int j0 = bi * g.n;
+        if (j0 >= nbytes) break;  // uniform across the group
+        const int j = t + j0;
+        uint32_t code[5];
+#pragma unroll
+        for (int i = 0; i < 5; i++) {
+            const int k = 5 * j + i;
+            const int q = (j < nbytes && k < d) ? quant_code(o[bi][i], scale) : 0;
+            sacc += q;
+            code[i] = (uint32_t)(q & 0xff);
+        }
+#pragma unroll
+        for (int i = 0; i < 5; i++) {
+            uint32_t w = code[i] << (8 * (lane & 3));
+            w |= __shfl_xor_sync(0xffffffffu, w, 1);
+            w |= __shfl_xor_sync(0xffffffffu, w, 2);
+            if ((lane & 3) == 0 && j < nbytes) xw[(j >> 4) * 20 + i * 4 + ((j >> 2) & 3)] = w;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, off);
+    if (lane == 0) atomicAdd(isum, sacc);
+    g.sync();  // 3: planes and the code sum
+    *sumx = *isum;
+    return scale;
+}
+
+// Absmax quantisation of a K-vector written by other CTAs (global, read
+// through L2) into the planes, with two group barriers: the vector is staged
+// in v (shared memory) while each thread tracks its maximum.
+__device__ __forceinline__ float quant_from_l2(const float *src, int K, float *v, uint4 *xr, int C, float *red,
+                                               int *isum, int *sumx, Grp g) {
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+    float4 *d4 = reinterpret_cast<float4 *>(v);
+    float amax = 0.0f;
+    const int n4 = K / 4;
+    for (int i0 = 0; i0 < n4; i0 += 8 * g.n) {
+        float4 t[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) t[j] = __ldcg(s4 + min(i0 + g.tid + j * g.n, n4 - 1));  // clamped: all in flight
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int i = i0 + g.tid + j * g.n;
+            if (i < n4) {
+                d4[i] = t[j];
+                amax = fmaxf(fmaxf(fmaxf(amax, fabsf(t[j].x)), fmaxf(fabsf(t[j].y), fabsf(t[j].z))), fabsf(t[j].w));
+            }
+        }
+    }
+    amax = warp_max(amax);
+    if (g.lane() == 0) red[g.warp()] = amax;
+    if (g.tid == 0) *isum = 0;
+    g.sync();
+    float m = red[0];
+    for (int w = 1; w < (g.n >> 5); w++) m = fmaxf(m, red[w]);
+    const float scale = quant_scale(m);
+    planes_from_smem(v, K, scale, C, xr, isum, g);
+    g.sync();
+    *sumx = *isum;
+    return scale;
+}
+
 // RMSNorm of the d-vector x in global memory (written by other CTAs: read
 // through L2) into xn (shared memory), also leaving x itself in xs_out
 // (shared memory).  Same tree as rmsnorm_row: the first T threads (T = the

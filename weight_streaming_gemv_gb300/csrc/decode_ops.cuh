@@ -266,10 +266,7 @@ __device__ __forceinline__ void load_l2_f4(float *dst, const float *src, int n, 
     for (int i0 = 0; i0 < n4; i0 += 4 * g.n) {
         float4 v[4];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int i = i0 + g.tid + j * g.n;
-            if (i < n4) v[j] = __ldcg(s4 + i);
-        }
+        for (int j = 0; j < 4; j++) v[j] = __ldcg(s4 + min(i0 + g.tid + j * g.n, n4 - 1));  // clamped: all in flight
 #pragma unroll
         for (int j = 0; j < 4; j++) {
             const int i = i0 + g.tid + j * g.n;
