@@ -357,14 +357,16 @@ static size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct DecodeWs {
     int32_t *status;
-    unsigned long long *bar_ctr;
+    unsigned *seq;
     unsigned *lm_ticket;
     float2 *lm_part;
-    float *h, *q, *k, *v, *a, *att, *pm, *pS, *pU;
+    uint64_t *hT, *qkvT, *attT, *aT, *pmT, *pST, *pUT;
     int ncmax;
     size_t bytes;
 };
 
+// Workspace layout; every word is zero in a fresh (zero-filled) workspace,
+// and a zero tagged word never matches the tag of any phase.
 static DecodeWs carve(const t158_model *m, char *base) {
     DecodeWs w{};
     size_t off = 0;
@@ -376,18 +378,16 @@ static DecodeWs carve(const t158_model *m, char *base) {
     const int d = m->dim, qd = m->n_heads * m->head_dim, kvd = m->n_kv_heads * m->head_dim, f = m->ffn;
     w.ncmax = att_chunks(m->max_pos);
     w.status = (int32_t *)take(16);  // must stay first: decode_step_t158_status reads offset 0
-    w.bar_ctr = (unsigned long long *)take(8);
+    w.seq = (unsigned *)take(8);
     w.lm_ticket = (unsigned *)take(4);
     w.lm_part = (float2 *)take(sizeof(float2) * (size_t)sm_count());
-    w.h = (float *)take(sizeof(float) * d);
-    w.q = (float *)take(sizeof(float) * qd);
-    w.k = (float *)take(sizeof(float) * kvd);
-    w.v = (float *)take(sizeof(float) * kvd);
-    w.a = (float *)take(sizeof(float) * f);
-    w.att = (float *)take(sizeof(float) * qd);
-    w.pm = (float *)take(sizeof(float) * (size_t)m->n_heads * w.ncmax);
-    w.pS = (float *)take(sizeof(float) * (size_t)m->n_heads * w.ncmax);
-    w.pU = (float *)take(sizeof(float) * (size_t)m->n_heads * w.ncmax * m->head_dim);
+    w.hT = (uint64_t *)take(8 * (size_t)d);
+    w.qkvT = (uint64_t *)take(8 * (size_t)(qd + 2 * kvd));
+    w.attT = (uint64_t *)take(8 * (size_t)qd);
+    w.aT = (uint64_t *)take(8 * (size_t)f);
+    w.pmT = (uint64_t *)take(8 * (size_t)m->n_heads * w.ncmax);
+    w.pST = (uint64_t *)take(8 * (size_t)m->n_heads * w.ncmax);
+    w.pUT = (uint64_t *)take(8 * (size_t)m->n_heads * w.ncmax * m->head_dim);
     w.bytes = off;
     return w;
 }
@@ -412,6 +412,7 @@ static qlin_status check_model(const t158_model *m) {
                  "decode_step_t158: kv width %d or dim %d too large for the weight ring", kvd, d);
     QLIN_REQUIRE(m->max_pos <= 4096, QLIN_ERR_UNSUPPORTED, "decode_step_t158: max_pos %d above 4096", m->max_pos);
     QLIN_REQUIRE(m->ffn % 4 == 0, QLIN_ERR_UNSUPPORTED, "decode_step_t158: ffn %d not a multiple of 4", m->ffn);
+    QLIN_REQUIRE(m->n_layers <= 127, QLIN_ERR_UNSUPPORTED, "decode_step_t158: %d layers above 127", m->n_layers);
     QLIN_REQUIRE(m->dim <= 4096, QLIN_ERR_UNSUPPORTED, "decode_step_t158: dim %d above 4096", m->dim);
     QLIN_REQUIRE(t158_pitch(m->dim) <= 4 * 32 * kFConsumerWarps, QLIN_ERR_UNSUPPORTED,
                  "decode_step_t158: dim %d needs more than four packed bytes per thread", m->dim);
@@ -542,19 +543,17 @@ qlin_status decode_step_t158(const t158_model *m, float *kv_cache, void *workspa
     a.pos = pos;
     a.logits = logits;
     a.next = next_token;
-    a.h = w.h;
-    a.q = w.q;
-    a.k = w.k;
-    a.v = w.v;
-    a.a = w.a;
-    a.att = w.att;
-    a.pm = w.pm;
-    a.pS = w.pS;
-    a.pU = w.pU;
+    a.hT = w.hT;
+    a.qkvT = w.qkvT;
+    a.attT = w.attT;
+    a.aT = w.aT;
+    a.pmT = w.pmT;
+    a.pST = w.pST;
+    a.pUT = w.pUT;
     a.ncmax = w.ncmax;
     a.lm_part = w.lm_part;
     a.lm_ticket = w.lm_ticket;
-    a.bar_ctr = w.bar_ctr;
+    a.seq = w.seq;
     a.status = w.status;
     return qlin::launch_decode_fused(a, (cudaStream_t)stream);
 }

@@ -27,7 +27,7 @@ namespace qlin {
 
 struct FusedSmem {
     // offsets in bytes into dynamic shared memory
-    int slots, xr, normbuf, hvec, xv, lmx, qs, ks, vs, wbuf, abuf, gbuf, gam, scl, misc, ring, total;
+    int slots, xr, seg, rope, hvec, xv, lmx, qs, ks, vs, wbuf, abuf, gbuf, gam, scl, misc, ring, total;
 };
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -43,8 +43,10 @@ __host__ __device__ inline FusedSmem fused_smem(const t158_model &m, int G) {
     o += kFStages * kFSlot;
     s.xr = o;
     o = align_up(o + maxC * 80, 128);
-    s.normbuf = o;
-    o = align_up(o + next_pow2(d) * 4, 128);
+    s.seg = o;  // 32-element segment sums of a norm (d <= 4096)
+    o = align_up(o + 128 * 4, 128);
+    s.rope = o;  // cos then sin of this position, head_dim/2 each
+    o = align_up(o + m.head_dim * 4, 128);
     s.hvec = o;
     o = align_up(o + d * 4, 128);
     s.xv = o;
@@ -127,7 +129,8 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     const int d = m.dim, nh = m.n_heads, nkv = m.n_kv_heads, hd = m.head_dim, ff = m.ffn;
     const int qd = nh * hd, kvd = nkv * hd, half = hd / 2;
     uint4 *xr = reinterpret_cast<uint4 *>(smem + L.xr);
-    float *normbuf = reinterpret_cast<float *>(smem + L.normbuf);
+    float *seg = reinterpret_cast<float *>(smem + L.seg);
+    float *rc = reinterpret_cast<float *>(smem + L.rope);
     float *hvec = reinterpret_cast<float *>(smem + L.hvec);
     float *xv = reinterpret_cast<float *>(smem + L.xv);
     float4 *lmx = reinterpret_cast<float4 *>(smem + L.lmx);
@@ -141,7 +144,6 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     float *scl = reinterpret_cast<float *>(smem + L.scl);
 
     int t = 0;  // ring item counter, mirrors the producer
-    unsigned long long nbar = 0;
     // One thread waits for a slot, then the named barrier releases the group, so
     // every consumer thread sees the same abort flag.  After an abort nothing
     // waits any more: the remaining items are skipped.
@@ -161,68 +163,62 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
         if (g.lane() == 0 && !*abort) mbar_arrive(&ring->empty[t % kFStages]);
         t++;
     };
-    auto barrier = [&]() -> bool {
-        nbar++;
-        return grid_barrier(A.bar_ctr, nbar * (unsigned long long)G, A.status, abort, g);
-    };
 
     int H0, H1;  // residual rows owned by this CTA (Wo and down outputs)
     share(d, b, G, H0, H1);
     int J0, J1;
     share(ff, b, G, J0, J1);
+    const uint32_t seq = *reinterpret_cast<volatile const unsigned *>(A.seq) & 0x3fffffu;
 
     for (int i = g.tid; i < m.n_layers * T158_NMAT; i += g.n) scl[i] = m.scales[i];
     cp_async_f4(gam, m.g_attn, d, g);  // gains of the first norm
 
-    // Step 0: h = emb[token] (every CTA for its norm; owners seed the global h)
+    // Step 0: h = emb[token], kept in hvec (owners of residual rows read their rows from it)
     int tok = *A.token;
     if (tok < 0 || tok >= m.vocab) {
         if (g.tid == 0) raise_status(A.status, kStatusBadToken);
         tok = -1;
     }
-    for (int i = g.tid; i < d; i += g.n) {
-        const float e = tok >= 0 ? __uint_as_float((uint32_t)m.emb[(int64_t)tok * d + i] << 16) : 0.0f;
-        hvec[i] = e;
-        if (i >= H0 && i < H1) A.h[i] = e;
+    for (int i = g.tid; i < d; i += g.n)
+        hvec[i] = tok >= 0 ? __uint_as_float((uint32_t)m.emb[(int64_t)tok * d + i] << 16) : 0.0f;
+    float *rs = rc + half;
+    for (int i = g.tid; i < half; i += g.n) {
+        rc[i] = m.rope_cos[(int64_t)A.pos * half + i];
+        rs[i] = m.rope_sin[(int64_t)A.pos * half + i];
     }
     g.sync();
 
-    const float *cos_p = m.rope_cos + (int64_t)A.pos * half;
-    const float *sin_p = m.rope_sin + (int64_t)A.pos * half;
     const int nc = A.pos / 32 + 1;
+    const int cpos = A.pos / 32;
 
-    for (int l = 0; l < m.n_layers; l++) {
+    for (int l = 0; l < m.n_layers && !*abort; l++) {
         const float *sc_l = scl + l * T158_NMAT;
         float *kc = A.kv + (int64_t)(2 * l) * m.max_pos * kvd;
         float *vc = A.kv + (int64_t)(2 * l + 1) * m.max_pos * kvd;
-        // ---------------- P1: norm, quantise, Q K V
+        // ---------------- P1: norm, quantise, Q K V (h of layer l-1 phase 5)
         cp_async_wait(g);
         int sumx;
         float xs;
-        if (l > 0)
-            xs = norm_quant([&](int u) { return __ldcg(reinterpret_cast<const float4 *>(A.h) + u); }, gam, d, m.eps,
-                            hvec, xv, xr, (int)(m.pitch[0] / 16), red, isum, &sumx, g);
-        else
-            xs = norm_quant([&](int u) { return reinterpret_cast<const float4 *>(hvec)[u]; }, gam, d, m.eps, normbuf,
-                            xv, xr, (int)(m.pitch[0] / 16), red, isum, &sumx, g);
+        xs = norm_quant(l > 0 ? A.hT : nullptr, l > 0 ? make_tag(seq, l - 1, 5) : 0u, hvec, gam, d, m.eps, xv, xr,
+                        (int)(m.pitch[0] / 16), red, seg, isum, &sumx, g, abort, A.status);
         cp_async_f4(gam, m.g_ffn + (int64_t)l * d, d, g);  // for P4 (gam was consumed by the norm)
         {
+            const uint32_t tg = make_tag(seq, l, 1);
             int lo, hi;
             share(qd + 2 * kvd, b, G, lo, hi);
             int base = 0;
             const int rows3[3] = {qd, kvd, kvd};
-            float *outs[3] = {A.q, A.k, A.v};
 #pragma unroll
             for (int j = 0; j < 3; j++) {
                 const int a0 = max(lo, base), a1 = min(hi, base + rows3[j]);
                 if (a1 > a0) {
                     const float ws = sc_l[j];
-                    float *out = outs[j];
+                    uint64_t *out = A.qkvT + base;
                     pieces(m.w[j], m.pitch[j], a0 - base, a1 - base, j, [&](const Piece &p) {
                         const uint8_t *slot = take(const_cast<Piece &>(p));
                         if (!*abort)
                             slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
-                                out[p.row0 + r] = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
+                                st_tagged(out + p.row0 + r, __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs), tg);
                             });
                         give();
                     });
@@ -230,95 +226,141 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
                 base += rows3[j];
             }
         }
-        if (!barrier()) break;
 
-        // ---------------- P2: RoPE, cache append, attention partials
-        load_l2_f4(qs, A.q, qd, g);
-        load_l2_f4(ks, A.k, kvd, g);
-        load_l2_f4(vs, A.v, kvd, g);
-        g.sync();
-        rope_rotate(qs, nh, hd, cos_p, sin_p, g);
-        rope_rotate(ks, nkv, hd, cos_p, sin_p, g);
-        g.sync();
-        if (b == ((A.pos / 32) * nh) % G) {  // owner of item (chunk of pos, head 0) appends k, v
-            for (int i = g.tid; i < kvd; i += g.n) {
-                kc[(int64_t)A.pos * kvd + i] = ks[i];
-                vc[(int64_t)A.pos * kvd + i] = vs[i];
-            }
-        }
-        for (int e = b; e < nc * nh; e += G) {
-            const int c = e / nh, hh = e % nh;
-            const int t0 = 32 * c, npre = min(t0 + 32, A.pos) - t0;
-            const int nt = min(32, A.pos + 1 - t0);
-            const float *Kc = ks, *Vc = vs;
-            uint8_t *kslot = nullptr, *vslot = nullptr;
-            if (npre > 0) {
-                // K rows are item t, V rows item t+1; both are held until the chunk is done
-                wait_full(t);
-                wait_full(t + 1);
-                kslot = slots + (size_t)(t % kFStages) * kFSlot;
-                vslot = slots + (size_t)((t + 1) % kFStages) * kFSlot;
-                if (nt > npre && !*abort) {  // the current position goes after the cached rows
-                    for (int i = g.tid; i < kvd; i += g.n) {
-                        reinterpret_cast<float *>(kslot)[npre * kvd + i] = ks[i];
-                        reinterpret_cast<float *>(vslot)[npre * kvd + i] = vs[i];
+        // ---------------- P2: per (chunk, head) item: RoPE, cache append, attention partials
+        {
+            const uint32_t tq = make_tag(seq, l, 1), tp = make_tag(seq, l, 2);
+            for (int e = b; e < nc * nh; e += G) {
+                const int c = e / nh, hh = e % nh;
+                const int t0 = 32 * c, npre = min(t0 + 32, A.pos) - t0;
+                const int nt = min(32, A.pos + 1 - t0);
+                const bool has_pos = c == cpos;
+                // q of this head (and k, v of the current position when the chunk holds it),
+                // RoPE applied as the words arrive.  Unit u < half: the q pair (u, u + half);
+                // then the k pairs of every kv head; then consecutive v pairs.
+                {
+                    const int nq = half, nk = has_pos ? nkv * half : 0, nvp = has_pos ? kvd / 2 : 0;
+                    const int U = nq + nk + nvp;
+                    auto word = [&](int u, int which) -> const uint64_t * {
+                        if (u < nq) return A.qkvT + hh * hd + u + which * half;
+                        u -= nq;
+                        if (u < nk) return A.qkvT + qd + (u / half) * hd + (u % half) + which * half;
+                        u -= nk;
+                        return A.qkvT + qd + kvd + 2 * u + which;
+                    };
+                    for (int u0 = 0; u0 < U; u0 += 2 * g.n) {
+                        const int ua = u0 + g.tid, ub = ua + g.n;
+                        const uint32_t mask = (ua < U ? 3u : 0u) | (ub < U ? 12u : 0u);
+                        float v4[4];
+                        fetch_tagged_at<4>([&](int j) { return word(j < 2 ? ua : ub, j & 1); }, mask, tq, v4, abort,
+                                           A.status);
+#pragma unroll
+                        for (int r = 0; r < 2; r++) {
+                            int u = r ? ub : ua;
+                            if (u >= U) continue;
+                            const float x0 = v4[2 * r], x1 = v4[2 * r + 1];
+                            if (u < nq + nk) {
+                                float *dst = u < nq ? qs : ks + ((u - nq) / half) * hd;
+                                const int i = u < nq ? u : (u - nq) % half;
+                                dst[i] = __fsub_rn(__fmul_rn(x0, rc[i]), __fmul_rn(x1, rs[i]));
+                                dst[i + half] = __fadd_rn(__fmul_rn(x0, rs[i]), __fmul_rn(x1, rc[i]));
+                            } else {
+                                u -= nq + nk;
+                                vs[2 * u] = x0;
+                                vs[2 * u + 1] = x1;
+                            }
+                        }
                     }
-                    // these generic-proxy writes must be ordered before the next TMA write of the slots
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
                 g.sync();
-                Kc = reinterpret_cast<const float *>(kslot);
-                Vc = reinterpret_cast<const float *>(vslot);
-            }
-            if (!*abort) {
-                const int kvh = hh / (nh / nkv);
-                attention_chunk(qs + hh * hd, Kc + kvh * hd, Vc + kvh * hd, kvd, nt, hd,
-                                A.pm + (int64_t)hh * A.ncmax + c, A.pS + (int64_t)hh * A.ncmax + c,
-                                A.pU + ((int64_t)hh * A.ncmax + c) * hd, sc, g);
-            }
-            if (npre > 0) {
-                give();
-                give();
+                if (has_pos && hh == 0) {  // one CTA appends the rotated k and v at pos
+                    for (int i = g.tid; i < kvd; i += g.n) {
+                        kc[(int64_t)A.pos * kvd + i] = ks[i];
+                        vc[(int64_t)A.pos * kvd + i] = vs[i];
+                    }
+                }
+                const float *Kc = ks, *Vc = vs;
+                if (npre > 0) {
+                    // K rows are item t, V rows item t+1; both are held until the chunk is done
+                    if (g.tid == 0 && !*abort &&
+                        (!mbar_wait(&ring->full[t % kFStages], (t / kFStages) & 1) ||
+                         !mbar_wait(&ring->full[(t + 1) % kFStages], ((t + 1) / kFStages) & 1))) {
+                        raise_status(A.status, kStatusTimeout);
+                        *abort = 1;
+                    }
+                    g.sync();
+                    uint8_t *kslot = slots + (size_t)(t % kFStages) * kFSlot;
+                    uint8_t *vslot = slots + (size_t)((t + 1) % kFStages) * kFSlot;
+                    if (nt > npre && !*abort) {  // the current position goes after the cached rows
+                        for (int i = g.tid; i < kvd; i += g.n) {
+                            reinterpret_cast<float *>(kslot)[npre * kvd + i] = ks[i];
+                            reinterpret_cast<float *>(vslot)[npre * kvd + i] = vs[i];
+                        }
+                        // generic-proxy writes ordered before the next TMA write of the slots
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    g.sync();
+                    Kc = reinterpret_cast<const float *>(kslot);
+                    Vc = reinterpret_cast<const float *>(vslot);
+                }
+                if (!*abort) {
+                    const int kvh = hh / (nh / nkv);
+                    attention_chunk(qs, Kc + kvh * hd, Vc + kvh * hd, kvd, nt, hd, &red[16], &red[17], xv, sc, g);
+                    const int64_t pi = (int64_t)hh * A.ncmax + c;
+                    if (g.tid == 0) {
+                        st_tagged(A.pmT + pi, red[16], tp);
+                        st_tagged(A.pST + pi, red[17], tp);
+                    }
+                    for (int i = g.tid; i < hd; i += g.n) st_tagged(A.pUT + pi * hd + i, xv[i], tp);
+                    g.sync();
+                }
+                if (npre > 0) {
+                    give();
+                    give();
+                }
             }
         }
-        if (!barrier()) break;
 
         // ---------------- P3a: merge, one output element per warp, spread over the CTAs
         {
+            const uint32_t tp = make_tag(seq, l, 2), ta = make_tag(seq, l, 6);
             int o0, o1;
             share(qd, b, G, o0, o1);
             for (int e = o0 + g.warp(); e < o1; e += kFConsumerWarps) {
                 const int hh = e / hd, i = e % hd;
-                const float o = attention_merge_one(A.pm + (int64_t)hh * A.ncmax, A.pS + (int64_t)hh * A.ncmax,
-                                                    A.pU + (int64_t)hh * A.ncmax * hd, nc, hd, i, g.lane());
-                if (g.lane() == 0) A.att[e] = o;
+                const float o = attention_merge_tagged(A.pmT + (int64_t)hh * A.ncmax, A.pST + (int64_t)hh * A.ncmax,
+                                                       A.pUT + (int64_t)hh * A.ncmax * hd, nc, hd, i, g.lane(), tp,
+                                                       abort, A.status);
+                if (g.lane() == 0) st_tagged(A.attT + e, o, ta);
             }
         }
-        if (!barrier()) break;
-        // ---------------- P3b: quantise, Wo, residual
-        xs = quant_from_l2(A.att, qd, xv, xr, (int)(m.pitch[3] / 16), red, isum, &sumx, g);
+
+        // ---------------- P3b: quantise attention output, Wo, residual (h of layer l phase 3)
+        xs = quant_from_tagged(A.attT, make_tag(seq, l, 6), qd, xv, xr, (int)(m.pitch[3] / 16), red, isum, &sumx, g,
+                               abort, A.status);
         {
             const float ws = sc_l[3];
+            const uint32_t th = make_tag(seq, l, 3);
             pieces(m.w[3], m.pitch[3], H0, H1, 3, [&](const Piece &p) {
                 const uint8_t *slot = take(const_cast<Piece &>(p));
                 if (!*abort)
                     slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
                         const int row = p.row0 + r;
                         const float y = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
-                        A.h[row] = __fadd_rn(A.h[row], y);
+                        st_tagged(A.hT + row, __fadd_rn(hvec[row], y), th);
                     });
                 give();
             });
         }
-        if (!barrier()) break;
 
-        // ---------------- P4: norm, quantise, gate and up, GeGLU
+        // ---------------- P4: norm, quantise, gate and up, GeGLU (a of layer l phase 4)
         cp_async_wait(g);
-        xs = norm_quant([&](int u) { return __ldcg(reinterpret_cast<const float4 *>(A.h) + u); }, gam, d, m.eps, hvec,
-                        xv, xr, (int)(m.pitch[4] / 16), red, isum, &sumx, g);
+        xs = norm_quant(A.hT, make_tag(seq, l, 3), hvec, gam, d, m.eps, xv, xr, (int)(m.pitch[4] / 16), red, seg,
+                        isum, &sumx, g, abort, A.status);
         cp_async_f4(gam, l + 1 < m.n_layers ? m.g_attn + (int64_t)(l + 1) * d : m.g_final, d, g);
         {
             const float wsg = sc_l[4], wsu = sc_l[5];
+            const uint32_t ta = make_tag(seq, l, 4);
             pieces(m.w[4], m.pitch[4], J0, J1, 4, [&](const Piece &p) {
                 const uint8_t *slot = take(const_cast<Piece &>(p));
                 if (!*abort)
@@ -333,29 +375,29 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
                     slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
                         const int row = p.row0 + r;
                         const float u = __fmul_rn(__fmul_rn((float)(acc - sumx), wsu), xs);
-                        A.a[row] = __fmul_rn(gelu32(gbuf[row - J0]), u);
+                        st_tagged(A.aT + row, __fmul_rn(gelu32(gbuf[row - J0]), u), ta);
                     });
                 give();
             });
         }
-        if (!barrier()) break;
 
-        // ---------------- P5: quantise GeGLU output, down, residual
-        xs = quant_from_l2(A.a, ff, abuf, xr, (int)(m.pitch[6] / 16), red, isum, &sumx, g);
+        // ---------------- P5: quantise GeGLU output, down, residual (h of layer l phase 5)
+        xs = quant_from_tagged(A.aT, make_tag(seq, l, 4), ff, abuf, xr, (int)(m.pitch[6] / 16), red, isum, &sumx, g,
+                               abort, A.status);
         {
             const float ws = sc_l[6];
+            const uint32_t th = make_tag(seq, l, 5);
             pieces(m.w[6], m.pitch[6], H0, H1, 6, [&](const Piece &p) {
                 const uint8_t *slot = take(const_cast<Piece &>(p));
                 if (!*abort)
                     slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
                         const int row = p.row0 + r;
                         const float y = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
-                        A.h[row] = __fadd_rn(A.h[row], y);
+                        st_tagged(A.hT + row, __fadd_rn(hvec[row], y), th);
                     });
                 give();
             });
         }
-        if (!barrier()) break;
     }
 
     // ---------------- final norm, lm_head, argmax
@@ -363,7 +405,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     int best_i = 0x7fffffff;
     if (!*abort) {
         cp_async_wait(g);
-        rmsnorm_from_l2(A.h, gam, hvec, xv, d, m.eps, red, g);
+        rmsnorm_from_tagged(A.hT, make_tag(seq, m.n_layers - 1, 5), gam, hvec, xv, d, m.eps, seg, g, abort, A.status);
         const int C = d / 8;
         for (int c = g.tid; c < C; c += g.n) {
             lmx[c] = make_float4(xv[8 * c], xv[8 * c + 1], xv[8 * c + 2], xv[8 * c + 3]);
@@ -461,7 +503,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
         if (g.tid == 0) {
             *A.next = i;
             *A.lm_ticket = 0u;
-            *A.bar_ctr = 0ull;
+            *reinterpret_cast<volatile unsigned *>(A.seq) = (seq + 1u) & 0x3fffffu;  // tags of the next launch
         }
     }
 }

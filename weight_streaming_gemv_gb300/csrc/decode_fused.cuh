@@ -21,14 +21,80 @@ struct FusedArgs {
     int pos;
     float *logits;
     int32_t *next;
-    // workspace
-    float *h, *q, *k, *v, *a, *att, *pm, *pS, *pU;
+    // workspace: vectors passed between CTAs as tagged words (value | tag << 32)
+    uint64_t *hT, *qkvT, *attT, *aT, *pmT, *pST, *pUT;
     int ncmax;
     float2 *lm_part;
     unsigned *lm_ticket;
-    unsigned long long *bar_ctr;
+    unsigned *seq;  // launch sequence number, advanced by the last CTA of every launch
     int32_t *status;
 };
+
+// ---------------------------------------------------------------- tagged words
+// A float handed from one CTA to others is stored together with a tag in one
+// 8-byte word (relaxed, gpu scope: single-copy atomic), so a reader that sees
+// the tag of the current launch, layer and phase also sees the value.  This
+// replaces grid-wide barriers: every CTA waits only for the words it reads.
+__device__ __forceinline__ uint32_t make_tag(uint32_t seq, int layer, int phase) {
+    return (seq << 10) | ((uint32_t)layer << 3) | (uint32_t)phase;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t tag) {
+    const uint64_t w = (uint64_t)__float_as_uint(v) | ((uint64_t)tag << 32);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+// out[j] = value of the tagged word at ptr(j) for every j whose bit is set in
+// `mask`, 0 for the others; waits (bounded) until every one of those words
+// carries `tag`.  All loads of a round are in flight together; only words
+// still stale are reloaded.  On timeout: status gets kStatusTimeout, *abort
+// is set.
+template <int N, class Ptr>
+__device__ __forceinline__ void fetch_tagged_at(Ptr &&ptr, uint32_t mask, uint32_t tag, float (&out)[N],
+                                                volatile int *abort, int32_t *status) {
+    uint64_t w[N];
+    uint32_t pending = 0;
+#pragma unroll
+    for (int j = 0; j < N; j++) {
+        w[j] = 0;
+        if (mask & (1u << j)) {
+            w[j] = ld_relaxed_u64(ptr(j));
+            if ((uint32_t)(w[j] >> 32) != tag) pending |= 1u << j;
+        }
+    }
+    if (pending) {
+        const uint64_t t0 = global_ns();
+        while (pending && !*abort) {
+            __nanosleep(32);
+#pragma unroll
+            for (int j = 0; j < N; j++)
+                if (pending & (1u << j)) w[j] = ld_relaxed_u64(ptr(j));
+#pragma unroll
+            for (int j = 0; j < N; j++)
+                if ((pending & (1u << j)) && (uint32_t)(w[j] >> 32) == tag) pending &= ~(1u << j);
+            if (pending && global_ns() - t0 > kWaitLimitNs) {
+                raise_status(status, kStatusTimeout);
+                *abort = 1;
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < N; j++) out[j] = (mask & (1u << j)) ? __uint_as_float((uint32_t)w[j]) : 0.0f;
+}
+
+// src[first + j * stride] for j < count (count <= N)
+template <int N>
+__device__ __forceinline__ void fetch_tagged(const uint64_t *src, int first, int stride, int count, uint32_t tag,
+                                             float (&out)[N], volatile int *abort, int32_t *status) {
+    const uint32_t mask = count >= 32 ? 0xffffffffu : (1u << (count > 0 ? count : 0)) - 1u;
+    fetch_tagged_at<N>([&](int j) { return src + first + j * stride; }, mask, tag, out, abort, status);
+}
 
 // rows [lo, hi) of n rows owned by CTA b of G
 __device__ __forceinline__ void share(int n, int b, int G, int &lo, int &hi) {
@@ -208,85 +274,83 @@ __device__ __forceinline__ void planes_from_smem(const float *v, int K, float sc
     if (lane == 0) atomicAdd(isum, s);
 }
 
-// RMSNorm + absmax quantisation of a d-vector (d <= 4096, d % 4 == 0) into
-// the planes, with three group barriers.  load4(u) gives elements 4u..4u+3
-// (from L2 or shared memory).  The first T threads (T = the largest power of
-// two not above the group) load the S = next_pow2(d)/T consecutive leaves of
-// their segment of the pairwise tree (S <= 32, in float4 units when S >= 4),
-// square and sum them as a balanced tree, then lanes, then warps; every
-// thread then finishes the tree itself from the warp sums.  Each thread
-// normalises the five elements of its own packed byte(s), takes the absmax
-// over the group and writes its codes into the planes.  gam and the staged x
-// (xs) are in natural order in shared memory; xn receives the normalised
-// vector.  Returns the step; *sumx gets the sum of the codes.  The arithmetic
-// is that of rmsnorm_row and the absmax quantiser.
-template <class Load4>
-__device__ __forceinline__ float norm_quant(Load4 load4, const float *gam, int d, float eps, float *xs, float *xn,
-                                            uint4 *xr, int C, float *red, int *isum, int *sumx, Grp g) {
-    int T = 32;
-    while (2 * T <= g.n) T *= 2;
-    const int P = next_pow2(d);
-    const int S = P >= T ? P / T : 1;
-    const int t = g.tid;
-    float part = 0.0f;
-    if (t < T) {
-        float v[32];
-        if (S >= 4) {
-            float4 w[8];
+// Sum of squares of x[0..d) (d <= 4096) as the pairwise tree over
+// next_pow2(d) zero-padded leaves.  The 32-leaf segment s of x (elements
+// 32s .. 32s+31) is held by warp s mod nw, one element per lane, so the loads
+// are coalesced; the warp sums the squares of a segment with the adjacent-lane
+// tree (its lower five levels) and seg[s] keeps the result.  With srcT the
+// vector comes from tagged words (waited for by tag) and is staged into xs;
+// without, xs already holds it.  The caller syncs the group, then calls
+// seg_total.
+__device__ __forceinline__ void stage_segments(const uint64_t *srcT, uint32_t tag, float *xs, int d, float *seg,
+                                               Grp g, volatile int *abort, int32_t *status) {
+    constexpr int N = 8;
+    const int nw = g.n >> 5, lane = g.lane(), w = g.warp();
+    const int nseg = (d + 31) >> 5;
+    for (int s0 = 0; s0 < nseg; s0 += N * nw) {
+        uint32_t mask = 0;
 #pragma unroll
-            for (int j = 0; j < 8; j++) w[j] = load4(min(t * S / 4 + j, d / 4 - 1));  // clamped: all in flight
+        for (int j = 0; j < N; j++) {
+            const int k = 32 * (s0 + w + j * nw) + lane;
+            if (k < d) mask |= 1u << j;
+        }
+        float v[N];
+        if (srcT) {
+            fetch_tagged_at<N>([&](int j) { return srcT + 32 * (s0 + w + j * nw) + lane; }, mask, tag, v, abort,
+                               status);
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const bool ok = 4 * j < S && t * S + 4 * j < d;
-                v[4 * j] = ok ? w[j].x : 0.0f;
-                v[4 * j + 1] = ok ? w[j].y : 0.0f;
-                v[4 * j + 2] = ok ? w[j].z : 0.0f;
-                v[4 * j + 3] = ok ? w[j].w : 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; j++)
-                if (4 * j < S && t * S + 4 * j < d)
-                    reinterpret_cast<float4 *>(xs)[t * S / 4 + j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                                                                                v[4 * j + 3]);
+            for (int j = 0; j < N; j++)
+                if (mask & (1u << j)) xs[32 * (s0 + w + j * nw) + lane] = v[j];
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; i++) v[i] = 0.0f;
-            for (int i = 0; i < S; i++) {
-                const int e = t * S + i;
-                if (e < d) {
-                    const float4 q = load4(e / 4);
-                    const int c = e % 4;
-                    const float xe = c == 0 ? q.x : c == 1 ? q.y : c == 2 ? q.z : q.w;
-                    xs[e] = xe;
-                    if (i == 0) v[0] = xe; else if (i == 1) v[1] = xe; else v[2 + (i & 1)] = xe;
-                }
-            }
+            for (int j = 0; j < N; j++) v[j] = (mask & (1u << j)) ? xs[32 * (s0 + w + j * nw) + lane] : 0.0f;
         }
 #pragma unroll
-        for (int i = 0; i < 32; i++) v[i] = __fmul_rn(v[i], v[i]);
-#pragma unroll
-        for (int st = 1; st < 32; st <<= 1)
-#pragma unroll
-            for (int i = 0; i < 32; i += 2 * st)
-                if (st < S) v[i] = __fadd_rn(v[i], v[i + st]);
-        part = v[0];
+        for (int j = 0; j < N; j++) {
+            const int sg = s0 + w + j * nw;  // uniform across the warp
+            if (sg < nseg) {
+                const float sq = warp_psum(__fmul_rn(v[j], v[j]));
+                if (lane == 0) seg[sg] = sq;
+            }
+        }
     }
-    part = warp_psum(part);
-    if ((t & 31) == 0 && t < T) red[t >> 5] = part;
-    g.sync();  // 1: warp sums and the staged vector are visible
-    float ss;
-    {
-        const int W = T >> 5;  // a power of two <= 8
-        float w8[8];
+}
+
+// The upper levels of the tree of stage_segments: every warp sums the
+// segment sums (zero past the last segment of x) and returns the total.
+__device__ __forceinline__ float seg_total(const float *seg, int d, Grp g) {
+    const int nseg = (d + 31) >> 5;
+    const int ns = next_pow2(d) >> 5;  // segments of the padded tree (>= 1)
+    const int L = ns > 32 ? ns / 32 : 1;  // 1, 2 or 4 per lane
+    const int lane = g.lane();
+    float a[4];
 #pragma unroll
-        for (int i = 0; i < 8; i++) w8[i] = i < W ? red[i] : 0.0f;
-#pragma unroll
-        for (int st = 1; st < 8; st <<= 1)
-#pragma unroll
-            for (int i = 0; i < 8; i += 2 * st)
-                if (st < W) w8[i] = __fadd_rn(w8[i], w8[i + st]);
-        ss = w8[0];
+    for (int i = 0; i < 4; i++) {
+        const int idx = lane * L + i;
+        a[i] = (i < L && idx < nseg) ? seg[idx] : 0.0f;
     }
+    float t = a[0];
+    if (L == 2) t = __fadd_rn(a[0], a[1]);
+    if (L == 4) t = __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
+    return warp_psum(t);
+}
+
+// RMSNorm + absmax quantisation of a d-vector (d <= 4096) into the planes,
+// with three group barriers.  The vector comes from tagged words srcT (other
+// CTAs' output, waited for by tag, staged into xs) or, when srcT is null, is
+// already in xs (shared memory).  Sum of squares as stage_segments/seg_total;
+// each thread normalises the five elements of its own packed byte(s), takes
+// the absmax over the group and writes its codes into the planes.  gam is in
+// shared memory; xn receives the normalised vector.  Returns the step; *sumx
+// gets the sum of the codes.  The arithmetic is that of rmsnorm_row and the
+// absmax quantiser.
+__device__ __forceinline__ float norm_quant(const uint64_t *srcT, uint32_t tag, float *xs, const float *gam, int d,
+                                            float eps, float *xn, uint4 *xr, int C, float *red, float *seg, int *isum,
+                                            int *sumx, Grp g, volatile int *abort, int32_t *status) {
+    const int t = g.tid;
+    stage_segments(srcT, tag, xs, d, seg, g, abort, status);
+    g.sync();  // 1: segment sums and the staged vector are visible
+    float ss = seg_total(seg, d, g);
     ss = __fdiv_rn(ss, (float)d);
     ss = __fadd_rn(ss, eps);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(ss));
@@ -349,27 +413,24 @@ __device__ __forceinline__ float norm_quant(Load4 load4, const float *gam, int d
     return scale;
 }
 
-// Absmax quantisation of a K-vector written by other CTAs (global, read
-// through L2) into the planes, with two group barriers: the vector is staged
+// Absmax quantisation of a K-vector of tagged words (other CTAs' output, waited
+// for by tag) into the planes, with two group barriers: the vector is staged
 // in v (shared memory) while each thread tracks its maximum.
-__device__ __forceinline__ float quant_from_l2(const float *src, int K, float *v, uint4 *xr, int C, float *red,
-                                               int *isum, int *sumx, Grp g) {
-    const float4 *s4 = reinterpret_cast<const float4 *>(src);
-    float4 *d4 = reinterpret_cast<float4 *>(v);
+__device__ __forceinline__ float quant_from_tagged(const uint64_t *srcT, uint32_t tag, int K, float *v, uint4 *xr, int C,
+                                                   float *red, int *isum, int *sumx, Grp g, volatile int *abort,
+                                                   int32_t *status) {
     float amax = 0.0f;
-    const int n4 = K / 4;
-    for (int i0 = 0; i0 < n4; i0 += 8 * g.n) {
-        float4 t[8];
+    for (int k0 = 0; k0 < K; k0 += 32 * g.n) {
+        const int first = k0 + g.tid;
+        const int cnt = first < K ? min(32, (K - first + g.n - 1) / g.n) : 0;
+        float val[32];
+        fetch_tagged<32>(srcT, first < K ? first : 0, g.n, cnt, tag, val, abort, status);
 #pragma unroll
-        for (int j = 0; j < 8; j++) t[j] = __ldcg(s4 + min(i0 + g.tid + j * g.n, n4 - 1));  // clamped: all in flight
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const int i = i0 + g.tid + j * g.n;
-            if (i < n4) {
-                d4[i] = t[j];
-                amax = fmaxf(fmaxf(fmaxf(amax, fabsf(t[j].x)), fmaxf(fabsf(t[j].y), fabsf(t[j].z))), fabsf(t[j].w));
+        for (int j = 0; j < 32; j++)
+            if (j < cnt) {
+                v[first + j * g.n] = val[j];
+                amax = fmaxf(amax, fabsf(val[j]));
             }
-        }
     }
     amax = warp_max(amax);
     if (g.lane() == 0) red[g.warp()] = amax;
@@ -384,54 +445,69 @@ __device__ __forceinline__ float quant_from_l2(const float *src, int K, float *v
     return scale;
 }
 
-// RMSNorm of the d-vector x in global memory (written by other CTAs: read
-// through L2) into xn (shared memory), also leaving x itself in xs_out
-// (shared memory).  Same tree as rmsnorm_row: the first T threads (T = the
-// largest power of two not above the group) hold the P/T consecutive squares
-// of their segment in registers (P = next_pow2(d) <= 32 T), sum them as a
-// balanced tree, then lanes, then warps.
-__device__ __forceinline__ void rmsnorm_from_l2(const float *x, const float *gam, float *xs_out, float *xn, int d,
-                                                float eps, float *red, Grp g) {
-    int T = 32;
-    while (2 * T <= g.n) T *= 2;
-    const int P = next_pow2(d);
-    const int S = P >= T ? P / T : 1;
-    const int t = g.tid;
-    float v[32];
-    float part = 0.0f;
-    if (t < T) {
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-            const int k = t * S + i;
-            v[i] = (i < S && k < d) ? __ldcg(x + k) : 0.0f;
-        }
-#pragma unroll
-        for (int i = 0; i < 32; i++)
-            if (i < S && t * S + i < d) xs_out[t * S + i] = v[i];
-#pragma unroll
-        for (int i = 0; i < 32; i++) v[i] = __fmul_rn(v[i], v[i]);
-#pragma unroll
-        for (int st = 1; st < 32; st <<= 1)
-#pragma unroll
-            for (int i = 0; i < 32; i += 2 * st)
-                if (st < S) v[i] = __fadd_rn(v[i], v[i + st]);
-        part = (P >= T || t < P) ? v[0] : 0.0f;
-    }
-    part = warp_psum(part);
-    if ((t & 31) == 0 && t < T) red[t >> 5] = part;
+// RMSNorm of the d-vector of tagged words srcT (waited for by tag) into xn
+// (shared memory), staging x in xs.  Same tree as rmsnorm_row.
+__device__ __forceinline__ void rmsnorm_from_tagged(const uint64_t *srcT, uint32_t tag, const float *gam, float *xs,
+                                                    float *xn, int d, float eps, float *seg, Grp g,
+                                                    volatile int *abort, int32_t *status) {
+    stage_segments(srcT, tag, xs, d, seg, g, abort, status);
     g.sync();
-    if (t == 0) {
-        const int W = T >> 5;
-        for (int st = 1; st < W; st <<= 1)
-            for (int i = 0; i < W; i += 2 * st) red[i] = __fadd_rn(red[i], red[i + st]);
-    }
-    g.sync();
-    float ss = red[0];
+    float ss = seg_total(seg, d, g);
     ss = __fdiv_rn(ss, (float)d);
     ss = __fadd_rn(ss, eps);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(ss));
-    for (int i = t; i < d; i += g.n) xn[i] = __fmul_rn(gam[i], __fmul_rn(r, xs_out[i]));
+    for (int i = g.tid; i < d; i += g.n) xn[i] = __fmul_rn(gam[i], __fmul_rn(r, xs[i]));
     g.sync();
+}
+
+// attention_merge_one on tagged partials (pm/pS [chunk], pU [chunk][hd] of
+// one head), waiting for each word's tag: one output element per warp.
+__device__ __forceinline__ float attention_merge_tagged(const uint64_t *pm, const uint64_t *pS, const uint64_t *pU,
+                                                        int nc, int hd, int i, int lane, uint32_t tag,
+                                                        volatile int *abort, int32_t *status) {
+    const int P = next_pow2(nc);
+    const int Lf = P > 32 ? P / 32 : 1;  // leaves per lane: 1, 2 or 4 (nc <= 128)
+    const int c0 = lane * Lf;
+    const int cnt = c0 < nc ? min(Lf, nc - c0) : 0;
+    float all[12];
+    const uint32_t m4 = (1u << cnt) - 1u;
+    fetch_tagged_at<12>(
+        [&](int j) {
+            const int c = c0 + (j & 3);
+            return j < 4 ? pm + c : j < 8 ? pS + c : pU + (int64_t)c * hd + i;
+        },
+        m4 | (m4 << 4) | (m4 << 8), tag, all, abort, status);
+    float mv[4], sv[4], uv[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        mv[j] = all[j];
+        sv[j] = all[4 + j];
+        uv[j] = all[8 + j];
+    }
+    float m = -__int_as_float(0x7f800000);
+#pragma unroll
+    for (int j = 0; j < 4; j++)
+        if (j < cnt) m = fmaxf(m, mv[j]);
+    m = warp_max(m);
+    float ws[4], wu[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const bool ok = j < cnt;
+        const float w = ok ? exp32(__fsub_rn(mv[j], m)) : 0.0f;
+        ws[j] = ok ? __fmul_rn(sv[j], w) : 0.0f;
+        wu[j] = ok ? __fmul_rn(uv[j], w) : 0.0f;
+    }
+    float s_l = ws[0], u_l = wu[0];
+    if (Lf == 2) {
+        s_l = __fadd_rn(ws[0], ws[1]);
+        u_l = __fadd_rn(wu[0], wu[1]);
+    } else if (Lf == 4) {
+        s_l = __fadd_rn(__fadd_rn(ws[0], ws[1]), __fadd_rn(ws[2], ws[3]));
+        u_l = __fadd_rn(__fadd_rn(wu[0], wu[1]), __fadd_rn(wu[2], wu[3]));
+    }
+    const float S = warp_psum(s_l);
+    const float U = warp_psum(u_l);
+    return __fdiv_rn(U, S);
 }
 
 // ---------------------------------------------------------------- T158 rows from a slot
@@ -496,35 +572,6 @@ __device__ __forceinline__ void cp_async_f4(float *dst, const float *src, int n,
 __device__ __forceinline__ void cp_async_wait(Grp g) {
     asm volatile("cp.async.wait_all;" ::: "memory");
     g.sync();
-}
-
-// ---------------------------------------------------------------- grid barrier
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// All CTAs of the (co-resident) grid meet here.  The counter only grows
-// within a launch; barrier number k completes at k * gridDim.x arrivals.
-// Bounded: on timeout the status word gets kStatusTimeout and *abort is set.
-__device__ __forceinline__ bool grid_barrier(unsigned long long *ctr, unsigned long long target, int32_t *status,
-                                             volatile int *abort, Grp g) {
-    g.sync();  // the CTA's writes happen-before thread 0's release below (bar.sync is cumulative)
-    if (g.tid == 0 && !*abort) {
-        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
-        const uint64_t t0 = global_ns();
-        uint32_t it = 0;
-        while (ld_acquire_u64(ctr) < target) {  // acquire: other CTAs' writes are visible after the loop
-            if ((++it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) {
-                raise_status(status, kStatusTimeout);
-                *abort = 1;
-                break;
-            }
-        }
-    }
-    g.sync();
-    return !*abort;
 }
 
 }  // namespace qlin
