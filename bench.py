@@ -18,6 +18,7 @@ during the timed region, and the oracle timed on the host cores.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -46,6 +47,21 @@ def parse():
     p.add_argument("--workload", choices=["decode"], default="decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
+
+
+# DRAM traffic of one launch of the fused decode kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture at context `pos`), valid only for
+# the kernel sources it was taken on: any change to them reports null.
+FUSED_SOURCES = ['decode_fused.cu', 'decode_fused.cuh', 'decode_ops.cuh', 'stream.cuh', 'common.cuh']
+FUSED_TRAFFIC = {"sha256": "8ff9a95fe2bb55bb114705c5fae60ae398c6ea33eb41b9587d5cb77fbd32f0c4", "bytes": 806220800, "pos": 1027}
+
+
+def fused_traffic():
+    h = hashlib.sha256()
+    for f in FUSED_SOURCES:
+        with open(os.path.join(ROOT, "weight_streaming_gemv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return FUSED_TRAFFIC if h.hexdigest() == FUSED_TRAFFIC["sha256"] else None
 
 
 def peaks():
@@ -235,6 +251,8 @@ def run_decode(args, rank, local, world):
     peak, peak_kind = peaks()
     lm_gbs = lm_alg / (lm_ms / 1e3) / 1e9
     gemv = gemv_m1(dev, stream)
+    step_gbs = step_bytes * args.steps / (ms / 1e3) / 1e9
+    traffic = fused_traffic()
     launches_per_step = qlin.decode_step_t158_launches(gpu.model)
     del gpu
     torch.cuda.empty_cache()
@@ -266,11 +284,20 @@ def run_decode(args, rank, local, world):
             "frac_of_peak": round(step_bytes * args.steps / (ms / 1e3) / 1e9 / peak, 4),
         },
         "gemv_m1": gemv,
+        # the step is one launch of the fused kernel: its algorithmic bytes over
+        # its CUDA-event time on the launching stream
         "roofline": {
-            "kernel": "lm_head_kernel",
-            "bound": "hbm", "achieved": round(lm_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-            "frac": round(lm_gbs / peak, 4), "traffic": None, "algorithmic_bytes": lm_alg,
-            "ms_per_launch": round(lm_ms, 5),
+            "kernel": "decode_fused_kernel",
+            "bound": "hbm", "achieved": round(step_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(step_gbs / peak, 4),
+            "traffic": traffic["bytes"] if traffic else None,
+            "traffic_pos": traffic["pos"] if traffic else None,
+            "algorithmic_bytes": step_bytes, "ms_per_launch": round(ms / args.steps, 5),
+        },
+        "lm_head": {
+            "kernel": "lm_head_kernel (standalone, timed alone)",
+            "bound": "hbm", "achieved": round(lm_gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(lm_gbs / peak, 4), "algorithmic_bytes": lm_alg, "ms_per_launch": round(lm_ms, 5),
         },
         "e2e": {"value": round(world * n_e2e / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 4, "steps": n_e2e},
