@@ -56,6 +56,39 @@ def test_quant_i8_zero_row_and_ties(dev):
     np.testing.assert_array_equal(host(xs), xs_o)
 
 
+def test_quant_i8_half_integer_boundaries(dev):
+    """Inputs exactly at (k + 1/2) times the step and a few ulps either side,
+    for every code k and for steps of several magnitudes: the codes must be
+    those of the IEEE quotient (the kernel decides far-from-boundary cases with
+    a product by the rounded reciprocal and these by the quotient itself)."""
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    absmax = [1.0, 3.7, 127.0, 0.1, 1e-3, 12345.678, 2.0**20 - 1, 0.9999999, 1.0000001, 5e-10]
+    rows = []
+    for a in absmax:
+        a = np.float32(a)
+        s = np.float32(max(a, np.float32(1e-9)) / np.float32(127.0))
+        vals = [a]
+        for k in range(-127, 127):
+            x0 = np.float32(np.float32(k + 0.5) * s)
+            for d in (-2, -1, 0, 1, 2):
+                x = x0
+                for _ in range(abs(d)):
+                    x = np.nextafter(x, np.float32(np.inf if d > 0 else -np.inf), dtype=np.float32)
+                vals.append(x if abs(x) <= a else np.float32(0.0))
+        rows.append(np.array(vals, np.float32))
+    K = len(rows[0])
+    x = np.stack(rows)
+    M = x.shape[0]
+    xq_o, xs_o = oracle.quant_i8(x)
+    xq = _empty((M, K), torch.int8, dev)
+    xs = _empty((M,), torch.float32, dev)
+    qlin.qlin_quant_i8(to_dev(x, dev), xq, xs, M, K)
+    np.testing.assert_array_equal(host(xs), xs_o)
+    np.testing.assert_array_equal(host(xq), xq_o)
+
+
 # ---------------------------------------------------------------- S1 W8 quantisation
 @pytest.mark.parametrize("N,K", [(768, 288), (4096, 4096), (1, 1), (3, 17)])
 def test_w8_quantize_bit_exact(dev, N, K):

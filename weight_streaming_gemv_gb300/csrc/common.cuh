@@ -150,6 +150,22 @@ __device__ __forceinline__ int quant_code(float v, float scale) {
     return static_cast<int>(r);
 }
 
+// quant_code with the division replaced by a product with rinv = RN(1/scale),
+// the same code for every v whose quotient is at most 127(1+2^-23) in
+// magnitude (every element of the vector the scale was taken from).  With
+// r = RN(1/s), y = RN(v r) = (v/s)(1+d1)(1+d2), |d1|,|d2| <= 2^-24, so
+// |y - v/s| < 2^-15.9 for |v/s| <= 128, and f = RN(v/s) is within 2^-18 of
+// v/s: |y - f| < 2^-15.  When y lies farther than 0.5 - 2^-14 from its
+// nearest integer k, f is strictly within 0.5 of k and rint(f) = k; otherwise
+// (and for NaN) the IEEE quotient decides.
+__device__ __forceinline__ int quant_code_r(float v, float scale, float rinv) {
+    const float y = __fmul_rn(v, rinv);
+    float r = rintf(y);
+    if (!(fabsf(__fsub_rn(y, r)) < 0.49993896484375f)) r = rintf(__fdiv_rn(v, scale));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
 // Step of the absmax quantiser: max(absmax, 1e-9)/127.
 __device__ __forceinline__ float quant_scale(float absmax) {
     return __fdiv_rn(fmaxf(absmax, 1e-9f), 127.0f);

@@ -27,7 +27,7 @@ namespace qlin {
 
 struct FusedSmem {
     // offsets in bytes into dynamic shared memory
-    int slots, xr, seg, rope, hvec, xv, lmx, qs, ks, vs, wbuf, abuf, gbuf, gam, scl, misc, ring, total;
+    int slots, xr, seg, rope, hvec, xv, lmx, qs, ks, vs, wbuf, abuf, gbuf, scl, misc, ring, total;
 };
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -65,8 +65,6 @@ __host__ __device__ inline FusedSmem fused_smem(const t158_model &m, int G) {
     o = align_up(o + m.ffn * 4, 128);
     s.gbuf = o;
     o = align_up(o + (m.ffn / G + 2) * 4, 128);
-    s.gam = o;  // RMSNorm gains of the next norm (cp.async; the transposed layout spans next_pow2(d) floats)
-    o = align_up(o + next_pow2(d) * 4, 128);
     s.scl = o;  // every matrix scale of the model
     o = align_up(o + m.n_layers * T158_NMAT * 4, 128);
     s.misc = o;  // red[32] f32, ired[32] i32, sc[32] f32, flags
@@ -140,7 +138,6 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     float *wbuf = reinterpret_cast<float *>(smem + L.wbuf);
     float *gbuf = reinterpret_cast<float *>(smem + L.gbuf);
     float *abuf = reinterpret_cast<float *>(smem + L.abuf);
-    float *gam = reinterpret_cast<float *>(smem + L.gam);
     float *scl = reinterpret_cast<float *>(smem + L.scl);
 
     int t = 0;  // ring item counter, mirrors the producer
@@ -171,7 +168,6 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     const uint32_t seq = *reinterpret_cast<volatile const unsigned *>(A.seq) & 0x3fffffu;
 
     for (int i = g.tid; i < m.n_layers * T158_NMAT; i += g.n) scl[i] = m.scales[i];
-    cp_async_f4(gam, m.g_attn, d, g);  // gains of the first norm
 
     // Step 0: h = emb[token], kept in hvec (owners of residual rows read their rows from it)
     int tok = *A.token;
@@ -190,213 +186,184 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
 
     const int nc = A.pos / 32 + 1;
     const int cpos = A.pos / 32;
+    const int qkv_rows = qd + 2 * kvd;
+    int Q0, Q1;  // rows of the concatenation q | k | v owned by this CTA
+    share(qkv_rows, b, G, Q0, Q1);
 
+    // The ops of a layer, in order.  Every kind of work has one code site in
+    // the loop body (the loop is not unrolled), so the instructions a layer
+    // executes stay few enough to be served from the SM's instruction cache.
+    enum : int { kOpQKV = 0, kOpAttn = 1, kOpMerge = 2, kOpWo = 3, kOpGate = 4, kOpUp = 5, kOpDown = 6, kNumOps = 7 };
+    int sumx = 0;
+    float xs = 0.0f;
     for (int l = 0; l < m.n_layers && !*abort; l++) {
         const float *sc_l = scl + l * T158_NMAT;
         float *kc = A.kv + (int64_t)(2 * l) * m.max_pos * kvd;
         float *vc = A.kv + (int64_t)(2 * l + 1) * m.max_pos * kvd;
-        // ---------------- P1: norm, quantise, Q K V (h of layer l-1 phase 5)
-        cp_async_wait(g);
-        int sumx;
-        float xs;
-        xs = norm_quant(l > 0 ? A.hT : nullptr, l > 0 ? make_tag(seq, l - 1, 5) : 0u, hvec, gam, d, m.eps, xv, xr,
-                        (int)(m.pitch[0] / 16), red, seg, isum, &sumx, g, abort, A.status);
-        cp_async_f4(gam, m.g_ffn + (int64_t)l * d, d, g);  // for P4 (gam was consumed by the norm)
-        {
-            const uint32_t tg = make_tag(seq, l, 1);
-            int lo, hi;
-            share(qd + 2 * kvd, b, G, lo, hi);
-            int base = 0;
-            const int rows3[3] = {qd, kvd, kvd};
+#pragma unroll 1
+        for (int op = 0; op < kNumOps && !*abort; op++) {
+            // ---- input of the op's matrices: RMSNorm + quantise, or quantise
+            if (op == kOpQKV || op == kOpGate) {
+                const bool qkv = op == kOpQKV;
+                // h after layer l-1 (phase 5) for Q K V, h after attention (phase 3) for gate/up
+                xs = norm_quant(qkv && l == 0 ? nullptr : A.hT, qkv ? make_tag(seq, l - 1, 5) : make_tag(seq, l, 3),
+                                hvec, (qkv ? m.g_attn : m.g_ffn) + (int64_t)l * d, d, m.eps, xv, xr,
+                                (int)(m.pitch[qkv ? 0 : 4] / 16), red, seg, isum, &sumx, g, abort, A.status);
+            } else if (op == kOpWo || op == kOpDown) {
+                const bool wo = op == kOpWo;
+                xs = quant_from_tagged(wo ? A.attT : A.aT, wo ? make_tag(seq, l, 6) : make_tag(seq, l, 4),
+                                       wo ? qd : ff, wo ? xv : abuf, xr, (int)(m.pitch[wo ? 3 : 6] / 16), red, isum,
+                                       &sumx, g, abort, A.status);
+            }
+
+            if (op == kOpAttn) {
+                // ---- per (chunk, head) item: RoPE, cache append, attention partials
+                const uint32_t tq = make_tag(seq, l, 1), tp = make_tag(seq, l, 2);
+                for (int e = b; e < nc * nh; e += G) {
+                    const int c = e / nh, hh = e % nh;
+                    const int t0 = 32 * c, npre = min(t0 + 32, A.pos) - t0;
+                    const int nt = min(32, A.pos + 1 - t0);
+                    const bool has_pos = c == cpos;
+                    // q of this head (and k, v of the current position when the chunk holds
+                    // it), RoPE applied as the words arrive.  Unit u < half: the q pair
+                    // (u, u + half); then the k pairs of every kv head; then consecutive v pairs.
+                    {
+                        const int nq = half, nk = has_pos ? nkv * half : 0, nvp = has_pos ? kvd / 2 : 0;
+                        const int U = nq + nk + nvp;
+                        auto word = [&](int u, int which) -> const uint64_t * {
+                            if (u < nq) return A.qkvT + hh * hd + u + which * half;
+                            u -= nq;
+                            if (u < nk) return A.qkvT + qd + (u / half) * hd + (u % half) + which * half;
+                            u -= nk;
+                            return A.qkvT + qd + kvd + 2 * u + which;
+                        };
+                        for (int u0 = 0; u0 < U; u0 += 2 * g.n) {
+                            const int ua = u0 + g.tid, ub = ua + g.n;
+                            const uint32_t mask = (ua < U ? 3u : 0u) | (ub < U ? 12u : 0u);
+                            float v4[4];
+                            fetch_tagged_at<4>([&](int j) { return word(j < 2 ? ua : ub, j & 1); }, mask, tq, v4,
+                                               abort, A.status);
 #pragma unroll
-            for (int j = 0; j < 3; j++) {
-                const int a0 = max(lo, base), a1 = min(hi, base + rows3[j]);
-                if (a1 > a0) {
-                    const float ws = sc_l[j];
-                    uint64_t *out = A.qkvT + base;
-                    pieces(m.w[j], m.pitch[j], a0 - base, a1 - base, j, [&](const Piece &p) {
+                            for (int r = 0; r < 2; r++) {
+                                int u = r ? ub : ua;
+                                if (u >= U) continue;
+                                const float x0 = v4[2 * r], x1 = v4[2 * r + 1];
+                                if (u < nq + nk) {
+                                    float *dst = u < nq ? qs : ks + ((u - nq) / half) * hd;
+                                    const int i = u < nq ? u : (u - nq) % half;
+                                    dst[i] = __fsub_rn(__fmul_rn(x0, rc[i]), __fmul_rn(x1, rs[i]));
+                                    dst[i + half] = __fadd_rn(__fmul_rn(x0, rs[i]), __fmul_rn(x1, rc[i]));
+                                } else {
+                                    u -= nq + nk;
+                                    vs[2 * u] = x0;
+                                    vs[2 * u + 1] = x1;
+                                }
+                            }
+                        }
+                    }
+                    g.sync();
+                    if (has_pos && hh == 0) {  // one CTA appends the rotated k and v at pos
+                        for (int i = g.tid; i < kvd; i += g.n) {
+                            kc[(int64_t)A.pos * kvd + i] = ks[i];
+                            vc[(int64_t)A.pos * kvd + i] = vs[i];
+                        }
+                    }
+                    const float *Kc = ks, *Vc = vs;
+                    if (npre > 0) {
+                        // K rows are item t, V rows item t+1; both are held until the chunk is done
+                        if (g.tid == 0 && !*abort &&
+                            (!mbar_wait(&ring->full[t % kFStages], (t / kFStages) & 1) ||
+                             !mbar_wait(&ring->full[(t + 1) % kFStages], ((t + 1) / kFStages) & 1))) {
+                            raise_status(A.status, kStatusTimeout);
+                            *abort = 1;
+                        }
+                        g.sync();
+                        uint8_t *kslot = slots + (size_t)(t % kFStages) * kFSlot;
+                        uint8_t *vslot = slots + (size_t)((t + 1) % kFStages) * kFSlot;
+                        if (nt > npre && !*abort) {  // the current position goes after the cached rows
+                            for (int i = g.tid; i < kvd; i += g.n) {
+                                reinterpret_cast<float *>(kslot)[npre * kvd + i] = ks[i];
+                                reinterpret_cast<float *>(vslot)[npre * kvd + i] = vs[i];
+                            }
+                            // generic-proxy writes ordered before the next TMA write of the slots
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        }
+                        g.sync();
+                        Kc = reinterpret_cast<const float *>(kslot);
+                        Vc = reinterpret_cast<const float *>(vslot);
+                    }
+                    if (!*abort) {
+                        const int kvh = hh / (nh / nkv);
+                        attention_chunk(qs, Kc + kvh * hd, Vc + kvh * hd, kvd, nt, hd, &red[16], &red[17], xv, sc, g);
+                        const int64_t pi = (int64_t)hh * A.ncmax + c;
+                        if (g.tid == 0) {
+                            st_tagged(A.pmT + pi, red[16], tp);
+                            st_tagged(A.pST + pi, red[17], tp);
+                        }
+                        for (int i = g.tid; i < hd; i += g.n) st_tagged(A.pUT + pi * hd + i, xv[i], tp);
+                        g.sync();
+                    }
+                    if (npre > 0) {
+                        give();
+                        give();
+                    }
+                }
+            } else if (op == kOpMerge) {
+                // ---- merge, one output element per warp, spread over the CTAs
+                const uint32_t tp = make_tag(seq, l, 2), ta = make_tag(seq, l, 6);
+                int o0, o1;
+                share(qd, b, G, o0, o1);
+                for (int e = o0 + g.warp(); e < o1; e += kFConsumerWarps) {
+                    const int hh = e / hd, i = e % hd;
+                    const float o = attention_merge_tagged(A.pmT + (int64_t)hh * A.ncmax,
+                                                           A.pST + (int64_t)hh * A.ncmax,
+                                                           A.pUT + (int64_t)hh * A.ncmax * hd, nc, hd, i, g.lane(), tp,
+                                                           abort, A.status);
+                    if (g.lane() == 0) st_tagged(A.attT + e, o, ta);
+                }
+            } else {
+                // ---- T158 rows of this CTA and their epilogue.  Q K V is the
+                // concatenation q | k | v (three matrices); the others are one matrix.
+                int lo, hi;
+                if (op == kOpQKV) {
+                    lo = Q0;
+                    hi = Q1;
+                } else if (op == kOpWo || op == kOpDown) {
+                    lo = H0;
+                    hi = H1;
+                } else {
+                    lo = J0;
+                    hi = J1;
+                }
+                const uint32_t tg = make_tag(seq, l, op == kOpQKV ? 1 : op == kOpWo ? 3 : op == kOpUp ? 4 : 5);
+                const int nmat = op == kOpQKV ? 3 : 1;
+#pragma unroll 1
+                for (int jm = 0; jm < nmat; jm++) {
+                    const int mat = op == kOpQKV ? jm : op == kOpWo ? 3 : op == kOpGate ? 4 : op == kOpUp ? 5 : 6;
+                    const int base = op == kOpQKV ? (jm == 0 ? 0 : jm == 1 ? qd : qd + kvd) : 0;
+                    const int nrows = op == kOpQKV ? (jm == 0 ? qd : kvd) : (op == kOpWo || op == kOpDown ? d : ff);
+                    const int a0 = max(lo, base), a1 = min(hi, base + nrows);
+                    if (a1 <= a0) continue;
+                    const float ws = sc_l[mat];
+                    pieces(m.w[mat], m.pitch[mat], a0 - base, a1 - base, mat, [&](const Piece &p) {
                         const uint8_t *slot = take(const_cast<Piece &>(p));
                         if (!*abort)
                             slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
-                                st_tagged(out + p.row0 + r, __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs), tg);
+                                const int row = base + p.row0 + r;
+                                const float y = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
+                                if (op == kOpQKV)
+                                    st_tagged(A.qkvT + row, y, tg);
+                                else if (op == kOpGate)
+                                    gbuf[row - J0] = y;
+                                else if (op == kOpUp)
+                                    st_tagged(A.aT + row, __fmul_rn(gelu32(gbuf[row - J0]), y), tg);
+                                else  // Wo, down: residual
+                                    st_tagged(A.hT + row, __fadd_rn(hvec[row], y), tg);
                             });
                         give();
                     });
                 }
-                base += rows3[j];
             }
-        }
-
-        // ---------------- P2: per (chunk, head) item: RoPE, cache append, attention partials
-        {
-            const uint32_t tq = make_tag(seq, l, 1), tp = make_tag(seq, l, 2);
-            for (int e = b; e < nc * nh; e += G) {
-                const int c = e / nh, hh = e % nh;
-                const int t0 = 32 * c, npre = min(t0 + 32, A.pos) - t0;
-                const int nt = min(32, A.pos + 1 - t0);
-                const bool has_pos = c == cpos;
-                // q of this head (and k, v of the current position when the chunk holds it),
-                // RoPE applied as the words arrive.  Unit u < half: the q pair (u, u + half);
-                // then the k pairs of every kv head; then consecutive v pairs.
-                {
-                    const int nq = half, nk = has_pos ? nkv * half : 0, nvp = has_pos ? kvd / 2 : 0;
-                    const int U = nq + nk + nvp;
-                    auto word = [&](int u, int which) -> const uint64_t * {
-                        if (u < nq) return A.qkvT + hh * hd + u + which * half;
-                        u -= nq;
-                        if (u < nk) return A.qkvT + qd + (u / half) * hd + (u % half) + which * half;
-                        u -= nk;
-                        return A.qkvT + qd + kvd + 2 * u + which;
-                    };
-                    for (int u0 = 0; u0 < U; u0 += 2 * g.n) {
-                        const int ua = u0 + g.tid, ub = ua + g.n;
-                        const uint32_t mask = (ua < U ? 3u : 0u) | (ub < U ? 12u : 0u);
-                        float v4[4];
-                        fetch_tagged_at<4>([&](int j) { return word(j < 2 ? ua : ub, j & 1); }, mask, tq, v4, abort,
-                                           A.status);
-#pragma unroll
-                        for (int r = 0; r < 2; r++) {
-                            int u = r ? ub : ua;
-                            if (u >= U) continue;
-                            const float x0 = v4[2 * r], x1 = v4[2 * r + 1];
-                            if (u < nq + nk) {
-                                float *dst = u < nq ? qs : ks + ((u - nq) / half) * hd;
-                                const int i = u < nq ? u : (u - nq) % half;
-                                dst[i] = __fsub_rn(__fmul_rn(x0, rc[i]), __fmul_rn(x1, rs[i]));
-                                dst[i + half] = __fadd_rn(__fmul_rn(x0, rs[i]), __fmul_rn(x1, rc[i]));
-                            } else {
-                                u -= nq + nk;
-                                vs[2 * u] = x0;
-                                vs[2 * u + 1] = x1;
-                            }
-                        }
-                    }
-                }
-                g.sync();
-                if (has_pos && hh == 0) {  // one CTA appends the rotated k and v at pos
-                    for (int i = g.tid; i < kvd; i += g.n) {
-                        kc[(int64_t)A.pos * kvd + i] = ks[i];
-                        vc[(int64_t)A.pos * kvd + i] = vs[i];
-                    }
-                }
-                const float *Kc = ks, *Vc = vs;
-                if (npre > 0) {
-                    // K rows are item t, V rows item t+1; both are held until the chunk is done
-                    if (g.tid == 0 && !*abort &&
-                        (!mbar_wait(&ring->full[t % kFStages], (t / kFStages) & 1) ||
-                         !mbar_wait(&ring->full[(t + 1) % kFStages], ((t + 1) / kFStages) & 1))) {
-                        raise_status(A.status, kStatusTimeout);
-                        *abort = 1;
-                    }
-                    g.sync();
-                    uint8_t *kslot = slots + (size_t)(t % kFStages) * kFSlot;
-                    uint8_t *vslot = slots + (size_t)((t + 1) % kFStages) * kFSlot;
-                    if (nt > npre && !*abort) {  // the current position goes after the cached rows
-                        for (int i = g.tid; i < kvd; i += g.n) {
-                            reinterpret_cast<float *>(kslot)[npre * kvd + i] = ks[i];
-                            reinterpret_cast<float *>(vslot)[npre * kvd + i] = vs[i];
-                        }
-                        // generic-proxy writes ordered before the next TMA write of the slots
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    }
-                    g.sync();
-                    Kc = reinterpret_cast<const float *>(kslot);
-                    Vc = reinterpret_cast<const float *>(vslot);
-                }
-                if (!*abort) {
-                    const int kvh = hh / (nh / nkv);
-                    attention_chunk(qs, Kc + kvh * hd, Vc + kvh * hd, kvd, nt, hd, &red[16], &red[17], xv, sc, g);
-                    const int64_t pi = (int64_t)hh * A.ncmax + c;
-                    if (g.tid == 0) {
-                        st_tagged(A.pmT + pi, red[16], tp);
-                        st_tagged(A.pST + pi, red[17], tp);
-                    }
-                    for (int i = g.tid; i < hd; i += g.n) st_tagged(A.pUT + pi * hd + i, xv[i], tp);
-                    g.sync();
-                }
-                if (npre > 0) {
-                    give();
-                    give();
-                }
-            }
-        }
-
-        // ---------------- P3a: merge, one output element per warp, spread over the CTAs
-        {
-            const uint32_t tp = make_tag(seq, l, 2), ta = make_tag(seq, l, 6);
-            int o0, o1;
-            share(qd, b, G, o0, o1);
-            for (int e = o0 + g.warp(); e < o1; e += kFConsumerWarps) {
-                const int hh = e / hd, i = e % hd;
-                const float o = attention_merge_tagged(A.pmT + (int64_t)hh * A.ncmax, A.pST + (int64_t)hh * A.ncmax,
-                                                       A.pUT + (int64_t)hh * A.ncmax * hd, nc, hd, i, g.lane(), tp,
-                                                       abort, A.status);
-                if (g.lane() == 0) st_tagged(A.attT + e, o, ta);
-            }
-        }
-
-        // ---------------- P3b: quantise attention output, Wo, residual (h of layer l phase 3)
-        xs = quant_from_tagged(A.attT, make_tag(seq, l, 6), qd, xv, xr, (int)(m.pitch[3] / 16), red, isum, &sumx, g,
-                               abort, A.status);
-        {
-            const float ws = sc_l[3];
-            const uint32_t th = make_tag(seq, l, 3);
-            pieces(m.w[3], m.pitch[3], H0, H1, 3, [&](const Piece &p) {
-                const uint8_t *slot = take(const_cast<Piece &>(p));
-                if (!*abort)
-                    slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
-                        const int row = p.row0 + r;
-                        const float y = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
-                        st_tagged(A.hT + row, __fadd_rn(hvec[row], y), th);
-                    });
-                give();
-            });
-        }
-
-        // ---------------- P4: norm, quantise, gate and up, GeGLU (a of layer l phase 4)
-        cp_async_wait(g);
-        xs = norm_quant(A.hT, make_tag(seq, l, 3), hvec, gam, d, m.eps, xv, xr, (int)(m.pitch[4] / 16), red, seg,
-                        isum, &sumx, g, abort, A.status);
-        cp_async_f4(gam, l + 1 < m.n_layers ? m.g_attn + (int64_t)(l + 1) * d : m.g_final, d, g);
-        {
-            const float wsg = sc_l[4], wsu = sc_l[5];
-            const uint32_t ta = make_tag(seq, l, 4);
-            pieces(m.w[4], m.pitch[4], J0, J1, 4, [&](const Piece &p) {
-                const uint8_t *slot = take(const_cast<Piece &>(p));
-                if (!*abort)
-                    slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
-                        gbuf[p.row0 + r - J0] = __fmul_rn(__fmul_rn((float)(acc - sumx), wsg), xs);
-                    });
-                give();
-            });
-            pieces(m.w[5], m.pitch[5], J0, J1, 5, [&](const Piece &p) {
-                const uint8_t *slot = take(const_cast<Piece &>(p));
-                if (!*abort)
-                    slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
-                        const int row = p.row0 + r;
-                        const float u = __fmul_rn(__fmul_rn((float)(acc - sumx), wsu), xs);
-                        st_tagged(A.aT + row, __fmul_rn(gelu32(gbuf[row - J0]), u), ta);
-                    });
-                give();
-            });
-        }
-
-        // ---------------- P5: quantise GeGLU output, down, residual (h of layer l phase 5)
-        xs = quant_from_tagged(A.aT, make_tag(seq, l, 4), ff, abuf, xr, (int)(m.pitch[6] / 16), red, isum, &sumx, g,
-                               abort, A.status);
-        {
-            const float ws = sc_l[6];
-            const uint32_t th = make_tag(seq, l, 5);
-            pieces(m.w[6], m.pitch[6], H0, H1, 6, [&](const Piece &p) {
-                const uint8_t *slot = take(const_cast<Piece &>(p));
-                if (!*abort)
-                    slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
-                        const int row = p.row0 + r;
-                        const float y = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
-                        st_tagged(A.hT + row, __fadd_rn(hvec[row], y), th);
-                    });
-                give();
-            });
         }
     }
 
@@ -404,8 +371,8 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     float best_v = -__int_as_float(0x7f800000);
     int best_i = 0x7fffffff;
     if (!*abort) {
-        cp_async_wait(g);
-        rmsnorm_from_tagged(A.hT, make_tag(seq, m.n_layers - 1, 5), gam, hvec, xv, d, m.eps, seg, g, abort, A.status);
+        rmsnorm_from_tagged(A.hT, make_tag(seq, m.n_layers - 1, 5), m.g_final, hvec, xv, d, m.eps, seg, g, abort,
+                            A.status);
         const int C = d / 8;
         for (int c = g.tid; c < C; c += g.n) {
             lmx[c] = make_float4(xv[8 * c], xv[8 * c + 1], xv[8 * c + 2], xv[8 * c + 3]);

@@ -186,92 +186,32 @@ __device__ __forceinline__ void lm_items(const FusedArgs &A, int b, int G, F &&f
 }
 
 // ---------------------------------------------------------------- quantise into digit-plane order
-// Absmax step of v[0..K) by the group.
-__device__ __forceinline__ float group_absmax(const float *v, int K, float *red, Grp g) {
-    float a = 0.0f;
-    for (int i = g.tid; i < K; i += g.n) a = fmaxf(a, fabsf(v[i]));
-    a = warp_max(a);
-    if (g.lane() == 0) red[g.warp()] = a;
-    g.sync();
-    float m = red[0];
-    for (int w = 1; w < (g.n >> 5); w++) m = fmaxf(m, red[w]);
-    g.sync();
-    return m;
-}
-
-// int8 codes of v/scale placed in the plane order of the T158 kernels
-// (xr[c*5+i] word w byte b = code of element 5*(16c+4w+b)+i, 0 past K);
-// returns the exact sum of the codes.  One thread per packed byte j (five
-// consecutive elements); the four bytes of a word come from four consecutive
-// lanes and are joined with shuffles.  The group size must be a multiple of 4.
-__device__ __forceinline__ int quant_planes(const float *v, int K, float scale, int C, uint4 *xr, int *ired, Grp g) {
-    uint32_t *xw = reinterpret_cast<uint32_t *>(xr);
-    const int nbytes = C * 16;
-    int s = 0;
-    const int lane = g.lane();
-    for (int j0 = 0; j0 < nbytes; j0 += g.n) {
-        const int j = j0 + g.tid;  // lanes of a warp take consecutive bytes
-        uint32_t code[5];
-#pragma unroll
-        for (int i = 0; i < 5; i++) {
-            const int k = 5 * j + i;
-            const int q = (j < nbytes && k < K) ? quant_code(v[k], scale) : 0;
-            s += q;
-            code[i] = (uint32_t)(q & 0xff);
-        }
-        // word of plane i for bytes 4(j/4) .. 4(j/4)+3: gather from the four lanes
-#pragma unroll
-        for (int i = 0; i < 5; i++) {
-            uint32_t w = code[i] << (8 * (lane & 3));
-            w |= __shfl_xor_sync(0xffffffffu, w, 1);
-            w |= __shfl_xor_sync(0xffffffffu, w, 2);
-            if ((lane & 3) == 0 && j < nbytes) {
-                const int c = j >> 4, wd = (j >> 2) & 3;
-                xw[c * 20 + i * 4 + wd] = w;
-            }
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (g.lane() == 0) ired[g.warp()] = s;
-    g.sync();
-    int t = 0;
-    for (int w = 0; w < (g.n >> 5); w++) t += ired[w];
-    g.sync();
-    return t;
-}
-
 // Codes of v (shared memory, K elements) for step `scale` into the plane
-// layout, one packed byte per thread (as quant_planes), with the sum of the
-// codes accumulated into *isum (shared memory, zeroed by the caller before the
+// layout, one plane word per thread and round: word c*20 + 4i + w holds, in
+// byte b, the code of element 5(16c + 4w + b) + i (0 past K).  The sum of the
+// codes is added into *isum (shared memory, zeroed by the caller before the
 // last group barrier).  No group barrier inside: the caller syncs once after.
-__device__ __forceinline__ void planes_from_smem(const float *v, int K, float scale, int C, uint4 *xr, int *isum,
-                                                 Grp g) {
+__device__ __forceinline__ void planes_words(const float *v, int K, float scale, int C, uint4 *xr, int *isum, Grp g) {
     uint32_t *xw = reinterpret_cast<uint32_t *>(xr);
-    const int nbytes = C * 16;
-    const int lane = g.lane();
+    const float rinv = __fdiv_rn(1.0f, scale);
+    const int nwords = C * 20;
     int s = 0;
-    for (int j0 = 0; j0 < nbytes; j0 += g.n) {
-        const int j = j0 + g.tid;
-        uint32_t code[5];
+    for (int wi = g.tid; wi < nwords; wi += g.n) {
+        const int c = wi / 20, r = wi - 20 * c;
+        const int base = 5 * (16 * c + 4 * (r & 3)) + (r >> 2);
+        uint32_t word = 0;
 #pragma unroll
-        for (int i = 0; i < 5; i++) {
-            const int k = 5 * j + i;
-            const int q = (j < nbytes && k < K) ? quant_code(v[k], scale) : 0;
+        for (int bb = 0; bb < 4; bb++) {
+            const int k = base + 5 * bb;
+            const int q = k < K ? quant_code_r(v[k], scale, rinv) : 0;
             s += q;
-            code[i] = (uint32_t)(q & 0xff);
+            word |= (uint32_t)(q & 0xff) << (8 * bb);
         }
-#pragma unroll
-        for (int i = 0; i < 5; i++) {
-            uint32_t w = code[i] << (8 * (lane & 3));
-            w |= __shfl_xor_sync(0xffffffffu, w, 1);
-            w |= __shfl_xor_sync(0xffffffffu, w, 2);
-            if ((lane & 3) == 0 && j < nbytes) xw[(j >> 4) * 20 + i * 4 + ((j >> 2) & 3)] = w;
-        }
+        xw[wi] = word;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) atomicAdd(isum, s);
+    if (g.lane() == 0) atomicAdd(isum, s);
 }
 
 // Sum of squares of x[0..d) (d <= 4096) as the pairwise tree over
@@ -339,75 +279,47 @@ __device__ __forceinline__ float seg_total(const float *seg, int d, Grp g) {
 // with three group barriers.  The vector comes from tagged words srcT (other
 // CTAs' output, waited for by tag, staged into xs) or, when srcT is null, is
 // already in xs (shared memory).  Sum of squares as stage_segments/seg_total;
-// each thread normalises the five elements of its own packed byte(s), takes
-// the absmax over the group and writes its codes into the planes.  gam is in
-// shared memory; xn receives the normalised vector.  Returns the step; *sumx
-// gets the sum of the codes.  The arithmetic is that of rmsnorm_row and the
+// each thread normalises the elements k = t, t + n, ... into xn, with its
+// gains (global memory, read-only) read into registers before the vector
+// arrives; the group takes the absmax, and the codes are written one plane
+// word per thread (planes_words).  Returns the step; *sumx gets the sum of
+// the codes.  The arithmetic is that of rmsnorm_row and the
 // absmax quantiser.
 __device__ __forceinline__ float norm_quant(const uint64_t *srcT, uint32_t tag, float *xs, const float *gam, int d,
                                             float eps, float *xn, uint4 *xr, int C, float *red, float *seg, int *isum,
                                             int *sumx, Grp g, volatile int *abort, int32_t *status) {
     const int t = g.tid;
+    constexpr int MAXE = 20;  // elements per thread (d <= 20 * group size)
+    float gv[MAXE];
+#pragma unroll
+    for (int e = 0; e < MAXE; e++) {
+        const int k = t + e * g.n;
+        gv[e] = k < d ? __ldg(gam + k) : 0.0f;
+    }
     stage_segments(srcT, tag, xs, d, seg, g, abort, status);
     g.sync();  // 1: segment sums and the staged vector are visible
     float ss = seg_total(seg, d, g);
     ss = __fdiv_rn(ss, (float)d);
     ss = __fadd_rn(ss, eps);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(ss));
-    // normalised values of this thread's packed bytes j = t, t + n, ...
-    const int nbytes = C * 16;
-    constexpr int MAXB = 4;  // bytes per thread (nbytes <= 4 * group size)
-    float o[MAXB][5];
     float amax = 0.0f;
 #pragma unroll
-    for (int bi = 0; bi < MAXB; bi++) {
-        const int j = t + bi * g.n;
-#pragma unroll
-        for (int i = 0; i < 5; i++) {
-            const int k = 5 * j + i;
-            float val = 0.0f;
-            if (j < nbytes && k < d) {
-                val = __fmul_rn(gam[k], __fmul_rn(r, xs[k]));
-                xn[k] = val;
-                amax = fmaxf(amax, fabsf(val));
-            }
-            o[bi][i] = val;
+    for (int e = 0; e < MAXE; e++) {
+        const int k = t + e * g.n;
+        if (k < d) {
+            const float val = __fmul_rn(gv[e], __fmul_rn(r, xs[k]));
+            xn[k] = val;
+            amax = fmaxf(amax, fabsf(val));
         }
     }
     amax = warp_max(amax);
     if (g.lane() == 0) red[8 + g.warp()] = amax;
     if (t == 0) *isum = 0;
-    g.sync();  // 2: absmax parts
+    g.sync();  // 2: the normalised vector and the absmax parts
     float m = red[8];
     for (int w = 1; w < (g.n >> 5); w++) m = fmaxf(m, red[8 + w]);
     const float scale = quant_scale(m);
-    uint32_t *xw = reinterpret_cast<uint32_t *>(xr);
-    const int lane = g.lane();
-    int sacc = 0;
-#pragma unroll
-    for (int bi = 0; bi < MAXB; bi++) {
-        const int j0 = bi * g.n;
-        if (j0 >= nbytes) break;  // uniform across the group
-        const int j = t + j0;
-        uint32_t code[5];
-#pragma unroll
-        for (int i = 0; i < 5; i++) {
-            const int k = 5 * j + i;
-            const int q = (j < nbytes && k < d) ? quant_code(o[bi][i], scale) : 0;
-            sacc += q;
-            code[i] = (uint32_t)(q & 0xff);
-        }
-#pragma unroll
-        for (int i = 0; i < 5; i++) {
-            uint32_t w = code[i] << (8 * (lane & 3));
-            w |= __shfl_xor_sync(0xffffffffu, w, 1);
-            w |= __shfl_xor_sync(0xffffffffu, w, 2);
-            if ((lane & 3) == 0 && j < nbytes) xw[(j >> 4) * 20 + i * 4 + ((j >> 2) & 3)] = w;
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, off);
-    if (lane == 0) atomicAdd(isum, sacc);
+    planes_words(xn, d, scale, C, xr, isum, g);
     g.sync();  // 3: planes and the code sum
     *sumx = *isum;
     return scale;
@@ -439,14 +351,15 @@ __device__ __forceinline__ float quant_from_tagged(const uint64_t *srcT, uint32_
     float m = red[0];
     for (int w = 1; w < (g.n >> 5); w++) m = fmaxf(m, red[w]);
     const float scale = quant_scale(m);
-    planes_from_smem(v, K, scale, C, xr, isum, g);
+    planes_words(v, K, scale, C, xr, isum, g);
     g.sync();
     *sumx = *isum;
     return scale;
 }
 
 // RMSNorm of the d-vector of tagged words srcT (waited for by tag) into xn
-// (shared memory), staging x in xs.  Same tree as rmsnorm_row.
+// (shared memory), staging x in xs; gains gam in global memory.  Same tree as
+// rmsnorm_row.
 __device__ __forceinline__ void rmsnorm_from_tagged(const uint64_t *srcT, uint32_t tag, const float *gam, float *xs,
                                                     float *xn, int d, float eps, float *seg, Grp g,
                                                     volatile int *abort, int32_t *status) {
@@ -456,7 +369,7 @@ __device__ __forceinline__ void rmsnorm_from_tagged(const uint64_t *srcT, uint32
     ss = __fdiv_rn(ss, (float)d);
     ss = __fadd_rn(ss, eps);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(ss));
-    for (int i = g.tid; i < d; i += g.n) xn[i] = __fmul_rn(gam[i], __fmul_rn(r, xs[i]));
+    for (int i = g.tid; i < d; i += g.n) xn[i] = __fmul_rn(__ldg(gam + i), __fmul_rn(r, xs[i]));
     g.sync();
 }
 
@@ -511,8 +424,29 @@ __device__ __forceinline__ float attention_merge_tagged(const uint64_t *pm, cons
 }
 
 // ---------------------------------------------------------------- T158 rows from a slot
+// acc + the dot product of one 16-byte chunk of packed trits (digits 0..2)
+// with its 80 activation codes in plane order X[0..5).
+__device__ __forceinline__ int chunk_dot(const uint4 wv, const uint4 *X, int acc) {
+    uint32_t D[4][5];
+    t158_planes(wv.x, D[0]);
+    t158_planes(wv.y, D[1]);
+    t158_planes(wv.z, D[2]);
+    t158_planes(wv.w, D[3]);
+#pragma unroll
+    for (int i = 0; i < 5; i++) {
+        const uint4 xv = X[i];
+        acc = dp4a(D[0][i], xv.x, acc);
+        acc = dp4a(D[1][i], xv.y, acc);
+        acc = dp4a(D[2][i], xv.z, acc);
+        acc = dp4a(D[3][i], xv.w, acc);
+    }
+    return acc;
+}
+
 // rows x pitch packed bytes at `slot` (shared memory) against the planes xr;
-// f(row, acc) with the exact integer sum of d * x (digits 0..2) per row.
+// f(row, acc) with the exact integer sum of d * x (digits 0..2) per row.  LPR
+// lanes share a row; a lane takes chunks sub, sub + LPR, ... two at a time
+// into two accumulators (two independent dp4a chains).
 template <int LPR, class F>
 __device__ __forceinline__ void slot_rows(const uint8_t *slot, int rows, int pitch, const uint4 *xr, Grp g, F &&f) {
     constexpr int RPS = 32 / LPR;
@@ -521,57 +455,51 @@ __device__ __forceinline__ void slot_rows(const uint8_t *slot, int rows, int pit
     const int nw = g.n >> 5;
     for (int r0 = g.warp() * RPS; r0 < rows; r0 += nw * RPS) {
         const int row = r0 + rsub;
-        int acc = 0;
+        int acc0 = 0, acc1 = 0;
         if (row < rows) {
             const uint8_t *wr = slot + (size_t)row * pitch;
-            for (int c = sub; c < C; c += LPR) {
-                const uint4 wv = lds128(wr + (size_t)c * 16);
-                uint32_t D[4][5];
-                t158_planes(wv.x, D[0]);
-                t158_planes(wv.y, D[1]);
-                t158_planes(wv.z, D[2]);
-                t158_planes(wv.w, D[3]);
-                const uint4 *X = xr + (size_t)c * 5;
-#pragma unroll
-                for (int i = 0; i < 5; i++) {
-                    const uint4 xv = X[i];
-                    acc = dp4a(D[0][i], xv.x, acc);
-                    acc = dp4a(D[1][i], xv.y, acc);
-                    acc = dp4a(D[2][i], xv.z, acc);
-                    acc = dp4a(D[3][i], xv.w, acc);
-                }
+            int c = sub;
+            for (; c + LPR < C; c += 2 * LPR) {
+                const uint4 wa = lds128(wr + (size_t)c * 16), wb = lds128(wr + (size_t)(c + LPR) * 16);
+                acc0 = chunk_dot(wa, xr + (size_t)c * 5, acc0);
+                acc1 = chunk_dot(wb, xr + (size_t)(c + LPR) * 5, acc1);
             }
+            if (c < C) acc0 = chunk_dot(lds128(wr + (size_t)c * 16), xr + (size_t)c * 5, acc0);
         }
+        int acc = acc0 + acc1;
 #pragma unroll
         for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (sub == 0 && row < rows) f(row, acc);
     }
 }
 
+// Lanes per row for `rows` rows of C chunks over nw warps: the fewest passes
+// times (chunks per lane + reduction steps), in rough cycle units (a chunk
+// about 55 with two in flight, a shuffle step about 30).
+__device__ __forceinline__ int rows_lpr(int rows, int C, int nw) {
+    int best = 32, best_cost = 1 << 30;
+#pragma unroll
+    for (int lg = 2; lg <= 5; lg++) {
+        const int lpr = 1 << lg;
+        const int per_pass = nw * (32 / lpr);
+        const int passes = (rows + per_pass - 1) / per_pass;
+        const int cost = passes * (((C + lpr - 1) / lpr) * 55 + lg * 30);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = lpr;
+        }
+    }
+    return best;
+}
+
 template <class F>
 __device__ __forceinline__ void slot_rows_any(const uint8_t *slot, int rows, int pitch, const uint4 *xr, Grp g, F &&f) {
-    const int C = pitch / 16;
-    if (C <= 8)
-        slot_rows<8>(slot, rows, pitch, xr, g, f);
-    else if (C <= 16)
-        slot_rows<16>(slot, rows, pitch, xr, g, f);
-    else
-        slot_rows<32>(slot, rows, pitch, xr, g, f);
-}
-
-// ---------------------------------------------------------------- async copies of small constants
-// n floats (n % 4 == 0, both pointers 16-byte aligned) global -> shared with
-// cp.async; completes at cp_async_wait().
-__device__ __forceinline__ void cp_async_f4(float *dst, const float *src, int n, Grp g) {
-    for (int i = g.tid; i < n / 4; i += g.n)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst + 4 * i)), "l"(src + 4 * i)
-                     : "memory");
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait(Grp g) {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    g.sync();
+    switch (rows_lpr(rows, pitch / 16, g.n >> 5)) {
+        case 4: slot_rows<4>(slot, rows, pitch, xr, g, f); break;
+        case 8: slot_rows<8>(slot, rows, pitch, xr, g, f); break;
+        case 16: slot_rows<16>(slot, rows, pitch, xr, g, f); break;
+        default: slot_rows<32>(slot, rows, pitch, xr, g, f); break;
+    }
 }
 
 }  // namespace qlin

@@ -33,7 +33,9 @@ __global__ void __launch_bounds__(256) quant_i8_kernel(const float *__restrict__
     }
     __syncthreads();
     const float s = quant_scale(red[0]);
-    for (int k = threadIdx.x; k < K; k += blockDim.x) xq[(int64_t)m * K + k] = (int8_t)quant_code(row[k], s);
+    const float rinv = __fdiv_rn(1.0f, s);
+    for (int k = threadIdx.x; k < K; k += blockDim.x)
+        xq[(int64_t)m * K + k] = (int8_t)quant_code_r(row[k], s, rinv);
     if (threadIdx.x == 0) xs[m] = s;
 }
 
