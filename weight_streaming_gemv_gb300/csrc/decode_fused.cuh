@@ -11,7 +11,7 @@ namespace qlin {
 
 constexpr int kFStages = 4;
 constexpr int kFSlot = 36864;  // bytes per ring slot (16 bf16 rows of 1152)
-constexpr int kFConsumerWarps = 7;  // + 1 producer warp = 8 warps: 2 per SM sub-partition, up to 255 registers
+constexpr int kFConsumerWarps = 11;  // + 1 producer warp = 12 warps: 3 per SM sub-partition, up to 168 registers
 constexpr int kFThreads = 32 * (kFConsumerWarps + 1);
 
 struct FusedArgs {
