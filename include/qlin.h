@@ -113,8 +113,18 @@ qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *
  * S5  W8 linear: y[m][n] = (sum_k x[m][k] * w8[n][k]) * w_scale, fp32
  * activations, the scale applied once after the dot product
  * ([cpp20gemma] "Architecture & implementation"; [llama2.c] "matmul").
- * x: device fp32 [M][K]; w8: device int8 [N][w_pitch], w_pitch >= K,
- * multiple of 16; y: device fp32 [M][N].  M: 1..64.
+ * x: device fp32 [M][K] (4-byte aligned); w8: device int8 [N][w_pitch],
+ * w_pitch >= K, multiple of 16, base 16-byte aligned; y: device fp32 [M][N].
+ * M: 1..64.  Accuracy: within 1e-5 of max|y| (max-abs-rel against the exact
+ * dot product) on the parity inputs.
+ * One token (M = 1, K <= 16384): the weights stream through shared memory by
+ * bulk copies and the dot products are integer: each 16-element slice of x a
+ * lane owns is held as 22-bit fixed point on a power-of-two scale from that
+ * slice's largest |x| (three int8 limbs, dp4a), i.e. x is rounded to within
+ * 2^-23 of the slice maximum.  A NaN or an infinity in x makes every y NaN.
+ * The kernel is launched with programmatic stream serialisation: it may start
+ * while the previous kernel on the stream finishes, and waits for that
+ * kernel's completion before it reads x or w8 or writes y.
  * ====================================================================== */
 qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float w_scale, float *y, int M, int N,
                         int K, qlin_stream_t stream);

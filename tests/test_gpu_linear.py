@@ -89,6 +89,38 @@ def test_quant_i8_half_integer_boundaries(dev):
     np.testing.assert_array_equal(host(xq), xq_o)
 
 
+def test_w8_m1_unaligned_x_tiny_values_and_nonfinite(dev):
+    """The one-token W8 path: x that is not 16-byte aligned (element loads), x
+    of tiny magnitude (scaled by two powers of two), and a non-finite x (every
+    row reads NaN)."""
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    K, N = 4099, 333
+    d = synth.w8_gemv(3, 1, K, N)
+    q_o, s_o = oracle.w8_quantize(d["w"])
+    pitch = (K + 15) // 16 * 16
+    w8 = np.zeros((N, pitch), np.int8)
+    w8[:, :K] = q_o
+    w8d = to_dev(w8, dev)
+    y = _empty((1, N), torch.float32, dev)
+    # x at an odd float offset inside a larger buffer
+    buf = torch.zeros(K + 1, dtype=torch.float32, device=dev)
+    buf[1:] = to_dev(d["x"][0], dev)
+    qlin.qlin_w8_f32(buf[1:], w8d, pitch, float(s_o), y, 1, N, K)
+    assert max_abs_rel(host(y), oracle.w8_linear(d["x"], q_o, s_o)) <= 1e-5
+    # tiny magnitudes (below 2^-100)
+    xt = (d["x"] * np.float32(2.0**-110)).astype(np.float32)
+    qlin.qlin_w8_f32(to_dev(xt, dev), w8d, pitch, float(s_o), y, 1, N, K)
+    assert max_abs_rel(host(y), oracle.w8_linear(xt, q_o, s_o)) <= 1e-5
+    # a NaN and an infinity
+    for bad in (np.nan, np.inf):
+        xb = d["x"].copy()
+        xb[0, 77] = bad
+        qlin.qlin_w8_f32(to_dev(xb, dev), w8d, pitch, float(s_o), y, 1, N, K)
+        assert np.isnan(host(y)).all()
+
+
 # ---------------------------------------------------------------- S1 W8 quantisation
 @pytest.mark.parametrize("N,K", [(768, 288), (4096, 4096), (1, 1), (3, 17)])
 def test_w8_quantize_bit_exact(dev, N, K):
@@ -179,7 +211,8 @@ def test_t158_bad_bytes_are_memory_safe(dev):
 # ---------------------------------------------------------------- S5 W8 linear
 @pytest.mark.parametrize("M,K,N", [(1, 288, 768), (1, 4096, 11008), (1, 11008, 4096), (1, 4096, 4096),
                                    (4, 4096, 11008), (4, 11008, 4096), (16, 4096, 4096), (16, 11008, 4096),
-                                   (16, 4096, 11008), (3, 17, 5), (1, 1, 1), (64, 300, 70)])
+                                   (16, 4096, 11008), (3, 17, 5), (1, 1, 1), (64, 300, 70),
+                                   (1, 5000, 2437), (1, 2047, 9), (1, 300, 7)])
 def test_w8_linear(dev, M, K, N):
     import torch
     from weight_streaming_gemv_gb300 import qlin

@@ -5,6 +5,7 @@
 // fp32 exactly with the 2^23 magic-number trick (one byte permute and one
 // subtraction) and accumulated with fp32 FMA.
 #include "common.cuh"
+#include "stream.cuh"
 
 namespace qlin {
 
@@ -121,6 +122,251 @@ __global__ void __launch_bounds__(256) w8_gemv_kernel(const float *__restrict__ 
     }
 }
 
+// ---------------------------------------------------------------- S5 GEMV, one token, TMA streaming
+// One CTA per SM over a contiguous run of rows.  Lane 0 of warp 0 streams the
+// run as tiles of TR whole rows (one bulk copy each: rows are contiguous)
+// through a ring of kW8Stages shared-memory slots; an mbarrier per slot counts
+// the bytes in, another counts the consumer warps out.
+//
+// The consumers never widen a weight.  Each lane holds its slice of x (at most
+// kW8JMax chunks of 16 elements) as 22-bit fixed point on a power-of-two
+// scale taken from the slice's largest |x|, X = rint(x 2^(22-E)), split into
+// three signed 8-bit limbs X = 2^16 a + 2^8 b + c; a row's dot product is then
+// three dp4a per 4 weights into exact int32 sums A, B, C, and the lane's
+// partial is (2^16 A + 2^8 B + C) 2^(E-22) in fp32.  x is thereby rounded to
+// within 2^-23 of the slice's largest |x| (an fp32 value carries 2^-24 of
+// itself).  A slice holding a NaN or an infinity makes its partial, and so
+// the row, NaN.
+//
+// The eight consumer warps are KS K-parts x (8 / KS) row groups: warp w owns
+// chunks [C p / KS, C (p+1) / KS) of the rows of group g (p = w % KS,
+// g = w / KS; C = pitch / 16), two rows at a time.  After every tile the
+// consumers meet at a named barrier and one warp adds the KS partials of each
+// row in a fixed order, so the result does not depend on timing.
+constexpr int kW8Warps = 8;    // consumer warps
+constexpr int kW8Stages = 3;  // 3 slots of <= 32 KB: two CTAs fit on an SM, so the next call's can wait there
+constexpr int kW8JMax = 4;     // chunks per lane: C <= 32 * 8 * 4 (K <= 16384)
+constexpr int kW8MaxTR = 32;   // rows per tile
+
+struct W8Smem {
+    int slot, tr, ks, xoff, total;  // slots at 0, then (at xoff) the ring and the partials
+};
+
+__host__ __device__ inline W8Smem w8_stream_layout(int64_t pitch, int smem_optin) {
+    W8Smem L;
+    const int C = (int)(pitch / 16);
+    L.ks = 1;  // the fewest K parts that leave at most kW8JMax chunks per lane
+    while (L.ks < kW8Warps && (C + L.ks * 32 - 1) / (L.ks * 32) > kW8JMax) L.ks *= 2;
+    const int rstep = 2 * (kW8Warps / L.ks);  // a tile holds whole row pairs of every group
+    const int fixed = (int)(sizeof(Ring<kW8Stages>) + 2 * kW8MaxTR * kW8Warps * sizeof(float)) + 256;
+    int slot = (smem_optin / 2 - 1024 - fixed) / kW8Stages;
+    slot = slot > 32768 ? 32768 : slot;
+    slot = slot / 128 * 128;  // so that the rounded-up tile below stays within it
+    int tr = (int)(slot / pitch);
+    tr = tr > kW8MaxTR ? kW8MaxTR : tr;
+    tr = tr / rstep * rstep;
+    L.tr = tr;
+    L.slot = (int)((tr * pitch + 127) / 128 * 128);
+    L.xoff = kW8Stages * L.slot;
+    L.total = kW8Stages * L.slot + fixed;
+    if ((C + L.ks * 32 - 1) / (L.ks * 32) > kW8JMax) L.tr = 0;  // K too large for this kernel
+    return L;
+}
+
+// 2^e for -126 <= e <= 127
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+__global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const float *__restrict__ x,
+                                                                         const int8_t *__restrict__ w, int64_t pitch,
+                                                                         float s, float *__restrict__ y, int N, int K,
+                                                                         W8Smem L) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *slots = smem;
+    Ring<kW8Stages> *ring = reinterpret_cast<Ring<kW8Stages> *>(smem + L.xoff);
+    float *part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ring) + sizeof(Ring<kW8Stages>));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = (int)(pitch / 16), TR = L.tr, KS = L.ks;
+    const int64_t r0 = (int64_t)N * blockIdx.x / gridDim.x, r1 = (int64_t)N * (blockIdx.x + 1) / gridDim.x;
+    const int ntiles = (int)((r1 - r0 + TR - 1) / TR);
+    // Programmatic dependent launch: the next kernel on the stream may start its
+    // own set-up now; this one waits for the previous kernel to complete (and its
+    // writes to be visible) before it reads x or the weights or writes y.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) ring->init(kW8Warps);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the first tile of the weight stream goes out at once, the other stages after
+    // the x loads below (so that those few loads do not queue behind the stream)
+    const uint64_t pol = l2_evict_first();
+    auto issue = [&](int t) {
+        const int st = t % kW8Stages;
+        const int64_t row = r0 + (int64_t)t * TR;
+        const uint32_t bytes = (uint32_t)(min((int64_t)TR, r1 - row) * pitch);
+        mbar_arrive_expect_tx(&ring->full[st], bytes);
+        bulk_g2s(slots + (size_t)st * L.slot, w + row * pitch, bytes, &ring->full[st], pol);
+    };
+    if (threadIdx.x == 0 && ntiles > 0) issue(0);
+    // consumers: load this lane's x slice first, so that these few loads do not
+    // queue behind the weight stream
+    const int cw = warp - 1, p = cw % KS, grp = cw / KS;
+    const int ca = C * p / KS, cb = C * (p + 1) / KS;
+    // the slice straight from global memory, every load in flight at once (16-byte
+    // loads when x is 16-byte aligned; a 16-byte group that crosses K element by element)
+    float xv[kW8JMax][16];
+    if (warp > 0) {
+        const bool x16 = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+#pragma unroll
+        for (int j = 0; j < kW8JMax; j++) {
+            const int c = ca + lane + 32 * j;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int k0 = 16 * c + 4 * q;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c < cb) {
+                    if (x16 && k0 + 3 < K) {
+                        v = __ldg(reinterpret_cast<const float4 *>(x + k0));
+                    } else {
+                        if (k0 < K) v.x = __ldg(x + k0);
+                        if (k0 + 1 < K) v.y = __ldg(x + k0 + 1);
+                        if (k0 + 2 < K) v.z = __ldg(x + k0 + 2);
+                        if (k0 + 3 < K) v.w = __ldg(x + k0 + 3);
+                    }
+                }
+                xv[j][4 * q] = v.x;
+                xv[j][4 * q + 1] = v.y;
+                xv[j][4 * q + 2] = v.z;
+                xv[j][4 * q + 3] = v.w;
+            }
+        }
+    }
+    // the loads are in flight; one barrier, then the weight stream starts
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int t = 1; t < min(ntiles, kW8Stages); t++) issue(t);
+
+    if (warp == 0) {
+        if (lane != 0) return;
+        int t = min(ntiles, kW8Stages);
+        for (; t < ntiles; t++) {
+            if (!mbar_wait(&ring->empty[t % kW8Stages], ((t / kW8Stages) - 1) & 1)) break;
+            issue(t);
+        }
+        // every copy issued must have landed before the CTA leaves
+        for (int u = max(0, t - kW8Stages); u < t; u++) mbar_wait(&ring->full[u % kW8Stages], (u / kW8Stages) & 1);
+        return;
+    }
+
+    // consumers: this lane's x chunks as three limbs of 22-bit fixed point
+    // largest |x| of the slice and finiteness from one integer maximum of the magnitude bits
+    uint32_t mbits = 0;
+#pragma unroll
+    for (int j = 0; j < kW8JMax; j++)
+#pragma unroll
+        for (int e = 0; e < 16; e++) mbits = max(mbits, (uint32_t)__float_as_int(xv[j][e]) & 0x7fffffffu);
+    const bool finite = mbits < 0x7f800000u;
+    // amax < 2^E (E from the exponent bits; frexp for a subnormal amax)
+    int E = 0;
+    if (mbits != 0 && finite) {
+        const int eb = (int)(mbits >> 23);
+        if (eb != 0)
+            E = eb - 126;
+        else
+            frexpf(__int_as_float((int)mbits), &E);
+    }
+    // X = rint(v 2^(22-E)) with two exact power-of-two factors (the second
+    // one only matters for slices below 2^-78); |X| <= 2^22, so adding
+    // 1.5 * 2^23 rounds to the integer (ties to even) and leaves it in the
+    // low mantissa bits.  Y = X + 0x808080 has bytes c_i + 128 for the
+    // balanced base-256 digits X = 2^16 c2 + 2^8 c1 + c0 (c_i in -128..127),
+    // so each limb word is four bytes of Y with the top bit flipped.
+    const int sh = 22 - E;
+    const float p1 = pow2f(sh > 100 ? 100 : sh), p2 = pow2f(sh > 100 ? sh - 100 : 0);
+    uint32_t la[kW8JMax][4], lb[kW8JMax][4], lc[kW8JMax][4];
+#pragma unroll
+    for (int j = 0; j < kW8JMax; j++) {
+        const int c = ca + lane + 32 * j;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            uint32_t Y[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const float v = (finite && c < cb) ? xv[j][4 * q + e] : 0.0f;
+                const float r = __fadd_rn(__fmul_rn(__fmul_rn(v, p1), p2), 12582912.0f);
+                Y[e] = (uint32_t)__float_as_int(r) - (0x4B400000u - 0x808080u);
+            }
+            const uint32_t lo = __byte_perm(Y[0], Y[1], 0x5140u), hi = __byte_perm(Y[2], Y[3], 0x5140u);
+            // lo = [Y0.b0, Y1.b0, Y0.b1, Y1.b1], hi likewise for Y2, Y3
+            lc[j][q] = __byte_perm(lo, hi, 0x5410u) ^ 0x80808080u;
+            lb[j][q] = __byte_perm(lo, hi, 0x7632u) ^ 0x80808080u;
+            la[j][q] = __byte_perm(__byte_perm(Y[0], Y[1], 0x0062u), __byte_perm(Y[2], Y[3], 0x0062u), 0x5410u) ^
+                       0x80808080u;
+        }
+    }
+    if (!finite) E = 0;
+    const int ush = E - 22;  // partial = (2^16 A + 2^8 B + C) 2^(E-22), in two exact steps
+    const float s1 = pow2f(ush < -100 ? -100 : ush), s2 = pow2f(ush < -100 ? ush + 100 : 0);
+    const float nanv = finite ? 0.0f : __int_as_float(0x7fc00000);  // a non-finite slice poisons its partials
+    const int gsz = TR / (kW8Warps / KS);  // rows of a group in a full tile (even)
+
+    bool ok = true;
+    for (int t = 0; t < ntiles; t++) {
+        const int st = t % kW8Stages;
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(&ring->full[st], (t / kW8Stages) & 1))) ok = false;
+        const int64_t row0 = r0 + (int64_t)t * TR;
+        const int rows = (int)min((int64_t)TR, r1 - row0);
+        float *pt = part + (size_t)(t & 1) * kW8MaxTR * kW8Warps;
+        if (ok) {
+            const uint8_t *tile = slots + (size_t)st * L.slot;
+            const int g0 = grp * gsz, g1 = min(rows, g0 + gsz);
+            for (int r = g0; r < g1; r += 2) {
+                const bool two = r + 1 < g1;
+                const uint8_t *ra = tile + (size_t)r * pitch, *rb = ra + pitch;
+                int Aa = 0, Ba = 0, Ca = 0, Ab = 0, Bb = 0, Cb = 0;
+#pragma unroll
+                for (int j = 0; j < kW8JMax; j++) {
+                    const int c = ca + lane + 32 * j;
+                    if (c < cb) {
+                        const uint4 wa = lds128(ra + (size_t)c * 16);
+                        const uint4 wb = two ? lds128(rb + (size_t)c * 16) : make_uint4(0u, 0u, 0u, 0u);
+                        const uint32_t ua[4] = {wa.x, wa.y, wa.z, wa.w}, ub[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            Aa = dp4a(ua[q], la[j][q], Aa);
+                            Ba = dp4a(ua[q], lb[j][q], Ba);
+                            Ca = dp4a(ua[q], lc[j][q], Ca);
+                            Ab = dp4a(ub[q], la[j][q], Ab);
+                            Bb = dp4a(ub[q], lb[j][q], Bb);
+                            Cb = dp4a(ub[q], lc[j][q], Cb);
+                        }
+                    }
+                }
+                float fa = __fmul_rn(__fmul_rn(fmaf((float)Aa, 65536.0f, fmaf((float)Ba, 256.0f, (float)Ca)), s1), s2);
+                float fb = __fmul_rn(__fmul_rn(fmaf((float)Ab, 65536.0f, fmaf((float)Bb, 256.0f, (float)Cb)), s1), s2);
+                fa = __fadd_rn(fa, nanv);
+                fb = __fadd_rn(fb, nanv);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    fa += __shfl_xor_sync(0xffffffffu, fa, o);
+                    fb += __shfl_xor_sync(0xffffffffu, fb, o);
+                }
+                if (lane == 0) {
+                    pt[r * kW8Warps + p] = fa;
+                    if (two) pt[(r + 1) * kW8Warps + p] = fb;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(&ring->empty[st]);
+        // all partials of tile t are in: one warp adds them (the other buffer
+        // takes tile t+1 meanwhile)
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * kW8Warps) : "memory");
+        if (cw == t % kW8Warps && lane < rows) {
+            float v = pt[lane * kW8Warps];
+            for (int q = 1; q < KS; q++) v += pt[lane * kW8Warps + q];
+            y[row0 + lane] = ok ? v * s : __int_as_float(0x7fc00000);
+        }
+    }
+}
+
 template <int R, int MT>
 static qlin_status launch_w8(const float *x, const int8_t *w, int64_t pitch, float s, float *y, int M, int N, int K,
                              cudaStream_t st) {
@@ -176,6 +422,25 @@ qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float
     QLIN_REQUIRE(M <= 64, QLIN_ERR_UNSUPPORTED, "qlin_w8_f32: M=%d > 64", M);
     cudaStream_t st = (cudaStream_t)stream;
     const size_t tile8_smem = (size_t)8 * ((K + 15) / 16) * 16 * sizeof(float);
+    if (M == 1 && w_pitch <= 16 * 32 * qlin::kW8Warps * qlin::kW8JMax) {
+        const qlin::W8Smem L = qlin::w8_stream_layout(w_pitch, qlin::max_smem_optin());
+        if (L.tr >= 1) {
+            qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel, L.total);  // raises the dynamic smem limit
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)qlin::sm_count());
+            cfg.blockDim = dim3(32 * (qlin::kW8Warps + 1));
+            cfg.dynamicSmemBytes = (size_t)L.total;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            QLIN_CUDA(cudaLaunchKernelEx(&cfg, qlin::w8_stream_kernel, x, w8, w_pitch, w_scale, y, N, K, L));
+            QLIN_LAUNCHED("w8_stream_kernel");
+            return QLIN_OK;
+        }
+    }
     if (M == 1) return qlin::launch_w8<4, 1>(x, w8, w_pitch, w_scale, y, M, N, K, st);
     if (M <= 4 || (int)tile8_smem > qlin::max_smem_optin())
         return qlin::launch_w8<2, 4>(x, w8, w_pitch, w_scale, y, M, N, K, st);
