@@ -194,6 +194,30 @@ def test_t158_prefill_m512_full_size(dev, K, N):
     _t158_case(dev, 512, K, N, seed=2)
 
 
+@pytest.mark.parametrize("M,K,N", [(64, 80, 128), (128, 80, 128), (100, 100, 200), (300, 1155, 130), (129, 161, 257),
+                                   (512, 6912, 100)])
+def test_t158_tensor_core_tiles(dev, M, K, N):
+    # the tensor-core path (M >= 64): ragged token, row and K tiles against the oracle, bit for bit
+    _t158_case(dev, M, K, N, seed=11)
+
+
+def test_t158_tensor_core_unaligned_x_acc_only(dev):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    M, K, N = 96, 333, 140
+    d = synth.t158_gemv(12, M, K, N)
+    xq_o, xs_o = oracle.quant_i8(d["x"])
+    acc_o, _ = oracle.t158_linear(xq_o, xs_o, oracle.t158_pack(d["trits"]), d["w_scale"], K)
+    pitch = qlin.t158_pitch(K)
+    w = to_dev(qlin.t158_pack(d["trits"], pitch), dev)
+    buf = torch.zeros(M * K + 1, dtype=torch.int8, device=dev)
+    buf[1:] = to_dev(xq_o.reshape(-1), dev)
+    acc = _empty((M, N), torch.int32, dev)
+    qlin.qlin_t158_i8(buf[1:], to_dev(xs_o, dev), w, pitch, d["w_scale"], None, acc, M, N, K)
+    np.testing.assert_array_equal(host(acc), acc_o)
+
+
 def test_t158_bad_bytes_are_memory_safe(dev):
     import torch
     from weight_streaming_gemv_gb300 import qlin

@@ -210,6 +210,11 @@ static qlin_status dispatch_mt(const int8_t *xq, const float *xs, const uint8_t 
     return launch_t158<LPR, 2, 16>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
 }
 
+// Tokens from which the tensor-core kernel (a 128-token tile) takes over.
+constexpr int kTensorCoreMinM = 64;
+qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
+                                     float *y, int32_t *acc, int M, int N, int K, cudaStream_t st);
+
 qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
                                    const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st) {
     const int C = (int)(pitch / 16);
@@ -242,6 +247,9 @@ qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *
                  QLIN_ERR_INVALID_ARG, "qlin_t158_i8: misaligned x_scale/y/acc");
     QLIN_REQUIRE(M <= 4096 && K <= 131071, QLIN_ERR_UNSUPPORTED, "qlin_t158_i8: M=%d K=%d outside 1..4096 x 1..131071",
                  M, K);
+    if (M >= qlin::kTensorCoreMinM)
+        return qlin::t158_linear_tensor_cores(xq, x_scale, w_packed, w_pitch, w_scale, y, acc, M, N, K,
+                                              (cudaStream_t)stream);
     return qlin::t158_linear_cuda_cores(xq, x_scale, w_packed, w_pitch, w_scale, nullptr, y, acc, M, N, K,
                                         (cudaStream_t)stream);
 }
