@@ -23,28 +23,44 @@
 // (warp w reads lanes 32 (w % 4) .. + 31, columns 64 (w / 4) .. + 63).
 #include <cuda_fp16.h>
 
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 #include "stream.cuh"
 
 namespace qlin {
 
 constexpr int kTcBM = 128;                      // tokens per CTA (MMA M)
-constexpr int kTcBN = 128;                      // weight rows per CTA (MMA N)
+constexpr int kTcBN = 256;                      // weight rows per CTA (MMA N)
 constexpr int kTcKS = 80;                       // K elements per step (16 packed bytes)
-constexpr int kTcThreads = 256;
+constexpr int kTcConv = kTcBM + kTcBN;          // converter threads: one per activation row and per weight row
+constexpr int kTcThreads = kTcConv + 32;        // + one warp that issues the MMAs
 constexpr int kTcChunks = kTcKS / 8;            // 16-byte core-matrix columns per row and step
 constexpr int kTcSBO = kTcChunks * 128;         // bytes between 8-row groups
-constexpr int kTcTile = (kTcBM / 8) * kTcSBO;   // bytes of one operand tile of one step
-constexpr int kTcStages = 2;
-constexpr uint32_t kTcCols = 128;               // tensor-memory columns: the 128 x 128 fp32 accumulator
-
-static_assert(kTcBM == kTcBN, "both operand tiles share one layout");
+constexpr int kTcTileA = (kTcBM / 8) * kTcSBO;  // bytes of the A tile of one step
+constexpr int kTcTileB = (kTcBN / 8) * kTcSBO;  // bytes of the B tile of one step
+constexpr int kTcStages = 2;                    // fp16 operand stages
+constexpr int kTcRaw = 6;                       // raw (int8 / packed) stages copied ahead
+constexpr uint32_t kTcCols = kTcBN;             // tensor-memory columns: the 128 x 256 fp32 accumulator
+constexpr int kTcPStride = kTcBN + 4;           // floats per row of a partial tile in shared memory
+constexpr int kTcMaxSplit = 8;                  // CTAs of a cluster that split K
 
 struct TcSmem {
-    uint8_t a[kTcStages][kTcTile];
-    uint8_t b[kTcStages][kTcTile];
-    uint64_t mma_done[kTcStages];
+    union {
+        struct {
+            uint8_t a[kTcStages][kTcTileA];
+            uint8_t b[kTcStages][kTcTileB];
+            uint8_t raw_a[kTcRaw][kTcBM][kTcKS];  // each thread's own activation row, step by step
+            uint8_t raw_b[kTcRaw][kTcBN][16];     // each thread's own packed weight row
+        } in;
+        float part[kTcBM][kTcPStride];  // after the K loop: this CTA's partial tile (split K)
+    };
+    uint64_t full[kTcStages];      // the converters have written the stage (kTcConv arrivals)
+    uint64_t mma_done[kTcStages];  // the MMAs reading the stage are done (tcgen05.commit)
+    float xs[kTcBM];               // activation scales of the tile's tokens
     uint32_t tmem;
+    int abort;
 };
 
 // Shared-memory matrix descriptor of the MMA: K-major, no swizzle, leading
@@ -59,7 +75,8 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
-// K-major, N = kTcBN, M = kTcBM.
+// K-major, N = kTcBN, M = kTcBM.  Both tiles use the descriptor above (the same
+// K step, so the same stride between 8-row groups).
 constexpr uint32_t kTcIdesc =
     (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kTcBN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
 
@@ -110,7 +127,55 @@ __device__ __forceinline__ uint32_t h2sub(uint32_t bits, uint32_t cbits) {
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// Activation row m (token) of step s into the A tile, K' order, fp16.
+// 80 activation bytes of one row (words in[], byte v + 128 of each value v,
+// i.e. already xor 0x80) into row r of the A tile, K' order, fp16.
+__device__ __forceinline__ void tc_put_a(uint8_t *tile, const uint32_t (&in)[20], int r) {
+#pragma unroll
+    for (int kc = 0; kc < kTcChunks; kc++) {
+        uint32_t h[4];
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            const int kp = 8 * kc + 2 * p;           // K' of the low half
+            const int i = kp >> 4, j = kp & 15;      // digit, packed byte
+            const int e0 = 5 * j + i, e1 = e0 + 5;   // element offsets within the step
+            h[p] = h2sub(i8pair_bits(in[e0 >> 2], in[e1 >> 2], e0 & 3, e1 & 3), 0x64806480u);
+        }
+        *reinterpret_cast<uint4 *>(tile + tc_off(r, kc)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
+// 16 packed bytes of one weight row into row r of the B tile, K' order, fp16 trits.
+__device__ __forceinline__ void tc_put_b(uint8_t *tile, const uint4 v, int r) {
+    uint32_t D[4][5];
+    t158_planes(v.x, D[0]);
+    t158_planes(v.y, D[1]);
+    t158_planes(v.z, D[2]);
+    t158_planes(v.w, D[3]);
+#pragma unroll
+    for (int kc = 0; kc < kTcChunks; kc++) {
+        const int i = kc >> 1, wa = 2 * (kc & 1);
+        // digits d in 0..2: fp16 (1024 + d) - 1025 = d - 1
+        const uint32_t h0 = h2sub(__byte_perm(D[wa][i], 0x6464u, 0x5140u), 0x64016401u);
+        const uint32_t h1 = h2sub(__byte_perm(D[wa][i], 0x6464u, 0x5342u), 0x64016401u);
+        const uint32_t h2 = h2sub(__byte_perm(D[wa + 1][i], 0x6464u, 0x5140u), 0x64016401u);
+        const uint32_t h3 = h2sub(__byte_perm(D[wa + 1][i], 0x6464u, 0x5342u), 0x64016401u);
+        *reinterpret_cast<uint4 *>(tile + tc_off(r, kc)) = make_uint4(h0, h1, h2, h3);
+    }
+}
+
+// 16 bytes global -> shared, the bytes past src_bytes (0..16) zero.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pending() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Activation row m (token) of step s into the A tile, K' order, fp16, loaded
+// directly (any alignment).
 __device__ __forceinline__ void tc_fill_a(uint8_t *tile, const int8_t *__restrict__ xq, int M, int K, int m, int r,
                                           int s, bool vec) {
     const int k0 = s * kTcKS;
@@ -142,53 +207,78 @@ __device__ __forceinline__ void tc_fill_a(uint8_t *tile, const int8_t *__restric
             in[i] = v ^ 0x80808080u;
         }
     }
-#pragma unroll
-    for (int kc = 0; kc < kTcChunks; kc++) {
-        uint32_t h[4];
-#pragma unroll
-        for (int p = 0; p < 4; p++) {
-            const int kp = 8 * kc + 2 * p;           // K' of the low half
-            const int i = kp >> 4, j = kp & 15;      // digit, packed byte
-            const int e0 = 5 * j + i, e1 = e0 + 5;   // element offsets within the step
-            h[p] = h2sub(i8pair_bits(in[e0 >> 2], in[e1 >> 2], e0 & 3, e1 & 3), 0x64806480u);
-        }
-        *reinterpret_cast<uint4 *>(tile + tc_off(r, kc)) = make_uint4(h[0], h[1], h[2], h[3]);
-    }
+    tc_put_a(tile, in, r);
 }
 
-// Weight row n of step s into the B tile, K' order, fp16 trits.
-__device__ __forceinline__ void tc_fill_b(uint8_t *tile, const uint8_t *__restrict__ w, int64_t pitch, int N, int n,
-                                          int r, int s) {
-    uint4 v = make_uint4(0x79797979u, 0x79797979u, 0x79797979u, 0x79797979u);  // byte 121: five zero trits
-    if (n < N) v = __ldg(reinterpret_cast<const uint4 *>(w + (int64_t)n * pitch + (int64_t)s * 16));
-    uint32_t D[4][5];
-    t158_planes(v.x, D[0]);
-    t158_planes(v.y, D[1]);
-    t158_planes(v.z, D[2]);
-    t158_planes(v.w, D[3]);
-#pragma unroll
-    for (int kc = 0; kc < kTcChunks; kc++) {
-        const int i = kc >> 1, wa = 2 * (kc & 1);
-        // digits d in 0..2: fp16 (1024 + d) - 1025 = d - 1
-        const uint32_t h0 = h2sub(__byte_perm(D[wa][i], 0x6464u, 0x5140u), 0x64016401u);
-        const uint32_t h1 = h2sub(__byte_perm(D[wa][i], 0x6464u, 0x5342u), 0x64016401u);
-        const uint32_t h2 = h2sub(__byte_perm(D[wa + 1][i], 0x6464u, 0x5140u), 0x64016401u);
-        const uint32_t h3 = h2sub(__byte_perm(D[wa + 1][i], 0x6464u, 0x5342u), 0x64016401u);
-        *reinterpret_cast<uint4 *>(tile + tc_off(r, kc)) = make_uint4(h0, h1, h2, h3);
-    }
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// float4 at a shared address of CTA `rank` of this cluster
+__device__ __forceinline__ float4 ld_peer_f4(const void *local, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(local)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a)
+                 : "memory");
+    return v;
 }
 
+// Grid: (N tiles, M tiles, split); a cluster is the `split` CTAs of one tile,
+// each over its own range of K steps.  split == 1: no cluster reduction.
 __global__ void __launch_bounds__(kTcThreads, 1) t158_tc_kernel(const int8_t *__restrict__ xq,
                                                                const float *__restrict__ xs,
                                                                const uint8_t *__restrict__ w, int64_t pitch, float ws,
                                                                float *__restrict__ y, int32_t *__restrict__ acc_out,
-                                                               int M, int N, int K) {
+                                                               int M, int N, int K, int split) {
     extern __shared__ __align__(128) uint8_t tc_smem_raw[];
     TcSmem &S = *reinterpret_cast<TcSmem *>(tc_smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * kTcBN, m0 = blockIdx.y * kTcBM;
     const int nsteps = (K + kTcKS - 1) / kTcKS;
+    const int z = split > 1 ? (int)cluster_rank() : 0;
+    const int s_lo = (int)((int64_t)nsteps * z / split), s_hi = (int)((int64_t)nsteps * (z + 1) / split);
 
+    // Converters.  Raw bytes of each thread's own row run kTcRaw - 1
+    // steps ahead through cp.async (16-byte copies, zero-filled past K, M
+    // and N: such products are zero or land outside the output); a thread
+    // reads back only what it copied, so its own wait_group is enough.
+    // Activations that are not 16-byte aligned are loaded directly.
+    const bool a_async = (reinterpret_cast<uintptr_t>(xq) & 15) == 0 && K % 16 == 0;
+    const bool is_a = tid < kTcBM;
+    const int r_own = is_a ? tid : tid - kTcBM;
+    auto fetch = [&](int s) {
+        if (s < s_hi) {
+            const int rs = (s - s_lo) % kTcRaw;
+            if (is_a) {
+                if (a_async) {
+                    const int m = m0 + r_own, k0 = s * kTcKS;
+                    const int8_t *row = xq + (int64_t)(m < M ? m : 0) * K;
+#pragma unroll
+                    for (int c = 0; c < kTcKS / 16; c++) {
+                        const int kb = k0 + 16 * c;
+                        const int nb = m < M ? max(0, min(16, K - kb)) : 0;
+                        cp_async16(S.in.raw_a[rs][r_own] + 16 * c, nb > 0 ? row + kb : row, nb);
+                    }
+                }
+            } else {
+                const int n = n0 + r_own;
+                cp_async16(S.in.raw_b[rs][r_own], w + (int64_t)(n < N ? n : 0) * pitch + (int64_t)s * 16,
+                           n < N ? 16 : 0);
+            }
+        }
+        cp_async_commit();
+    };
+    // the first copies go out before anything else
+    if (tid < kTcConv) {
+#pragma unroll
+        for (int s = 0; s < kTcRaw - 1; s++) fetch(s_lo + s);
+    }
+    for (int i = tid; i < kTcBM; i += kTcThreads) S.xs[i] = m0 + i < M ? xs[m0 + i] : 0.0f;
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&S.tmem)),
                      "r"(kTcCols)
@@ -196,91 +286,190 @@ __global__ void __launch_bounds__(kTcThreads, 1) t158_tc_kernel(const int8_t *__
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 32) {
-        for (int i = 0; i < kTcStages; i++) mbar_init(&S.mma_done[i], 1);
+        for (int i = 0; i < kTcStages; i++) {
+            mbar_init(&S.full[i], kTcConv);
+            mbar_init(&S.mma_done[i], 1);
+        }
+        S.abort = 0;
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = S.tmem;
-    const bool a_vec = (reinterpret_cast<uintptr_t>(xq) & 15) == 0 && K % 16 == 0;
+    volatile int *abort = &S.abort;
+    const int nst = s_hi - s_lo;  // steps of this CTA
 
-    bool ok = true;
-    int issued = 0;  // steps whose MMAs were issued
-    for (int s = 0; s < nsteps; s++) {
-        const int st = s & 1;
-        // the MMAs of step s-2 read this stage: wait until they are done
-        const bool waited = s < 2 || mbar_wait(&S.mma_done[st], ((s >> 1) - 1) & 1);
-        if (!__syncthreads_and(waited)) {
-            ok = false;
-            break;
-        }
-        if (tid < 128)
-            tc_fill_a(S.a[st], xq, M, K, m0 + tid, tid, s, a_vec);
-        else
-            tc_fill_b(S.b[st], w, pitch, N, n0 + tid - 128, tid - 128, s);
-        // the generic-proxy writes above, visible to the tensor core (async proxy)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t a0 = smem_addr(S.a[st]), b0 = smem_addr(S.b[st]);
-#pragma unroll
-            for (int u = 0; u < kTcKS / 16; u++)  // K = 16: two core-matrix columns (256 bytes)
-                tc_mma(tmem, tc_desc(a0 + 256u * u), tc_desc(b0 + 256u * u), (s > 0 || u > 0) ? 1u : 0u);
-            tc_commit(&S.mma_done[st]);
-        }
-        issued = s + 1;
-    }
-    // the last commit covers every MMA issued before it
-    if (issued > 0) {
-        const int s = issued - 1;
-        if (!mbar_wait(&S.mma_done[s & 1], (s >> 1) & 1)) ok = false;
-    }
-    ok = __syncthreads_and(ok) != 0;
-    tc_fence_after();
-
-    if (ok && issued == nsteps) {
-        const int q = warp & 3, hf = warp >> 2;
-        const int m = m0 + 32 * q + lane;
-        const float xsm = m < M ? xs[m] : 0.0f;
-        const bool vec_out = y && (reinterpret_cast<uintptr_t>(y) & 15) == 0 && N % 4 == 0;
-#pragma unroll
-        for (int c = 0; c < 2; c++) {
-            const int col = 64 * hf + 32 * c;
-            uint32_t r[32];
-            tc_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
-            if (m < M) {
-                const int nb = n0 + col;
-                if (acc_out)
-                    for (int j = 0; j < 32; j++)
-                        if (nb + j < N) acc_out[(int64_t)m * N + nb + j] = __float2int_rz(__uint_as_float(r[j]));
-                if (y) {
-                    if (vec_out && nb + 32 <= N) {
-                        float4 *dst = reinterpret_cast<float4 *>(y + (int64_t)m * N + nb);
-#pragma unroll
-                        for (int j = 0; j < 8; j++)
-                            dst[j] = make_float4(__fmul_rn(__fmul_rn(__uint_as_float(r[4 * j]), ws), xsm),
-                                                 __fmul_rn(__fmul_rn(__uint_as_float(r[4 * j + 1]), ws), xsm),
-                                                 __fmul_rn(__fmul_rn(__uint_as_float(r[4 * j + 2]), ws), xsm),
-                                                 __fmul_rn(__fmul_rn(__uint_as_float(r[4 * j + 3]), ws), xsm));
-                    } else {
-                        for (int j = 0; j < 32; j++)
-                            if (nb + j < N)
-                                y[(int64_t)m * N + nb + j] = __fmul_rn(__fmul_rn(__uint_as_float(r[j]), ws), xsm);
-                    }
+    if (warp == kTcConv / 32) {
+        // ---- MMA warp: lane 0 issues each step's five MMAs once the converters
+        // have filled the stage, and commits them to the stage's mma_done
+        if (lane == 0) {
+            for (int i = 0; i < nst && !*abort; i++) {
+                const int st = i & 1;
+                if (!mbar_wait(&S.full[st], (i >> 1) & 1)) {
+                    *abort = 1;
+                    break;
                 }
+                tc_fence_after();
+                const uint32_t a0 = smem_addr(S.in.a[st]), b0 = smem_addr(S.in.b[st]);
+#pragma unroll
+                for (int u = 0; u < kTcKS / 16; u++)  // K = 16: two core-matrix columns (256 bytes)
+                    tc_mma(tmem, tc_desc(a0 + 256u * u), tc_desc(b0 + 256u * u), (i > 0 || u > 0) ? 1u : 0u);
+                tc_commit(&S.mma_done[st]);
             }
         }
-    } else if (!ok && tid == 0) {
-        // a wait gave up (never in a correct build): the tile reads NaN
-        for (int mm = 0; mm < kTcBM && m0 + mm < M; mm++)
-            for (int j = 0; j < kTcBN && n0 + j < N; j++)
-                if (y) y[(int64_t)(m0 + mm) * N + n0 + j] = __int_as_float(0x7fc00000);
+    } else {
+        // ---- converters
+        for (int i = 0; i < nst && !*abort; i++) {
+            const int s = s_lo + i, st = i & 1;
+            fetch(s + kTcRaw - 1);
+            cp_async_wait_pending<kTcRaw - 1>();  // this thread's copies of step s have landed
+            // the MMAs of step i-2 read this stage: wait until they are done
+            if (i >= 2 && !mbar_wait(&S.mma_done[st], ((i >> 1) - 1) & 1)) {
+                *abort = 1;
+                break;
+            }
+            if (is_a) {
+                if (a_async) {
+                    uint32_t in[20];
+                    const uint4 *src = reinterpret_cast<const uint4 *>(S.in.raw_a[i % kTcRaw][r_own]);
+#pragma unroll
+                    for (int q = 0; q < 5; q++) {
+                        const uint4 v = src[q];
+                        in[4 * q] = v.x ^ 0x80808080u;
+                        in[4 * q + 1] = v.y ^ 0x80808080u;
+                        in[4 * q + 2] = v.z ^ 0x80808080u;
+                        in[4 * q + 3] = v.w ^ 0x80808080u;
+                    }
+                    tc_put_a(S.in.a[st], in, r_own);
+                } else {
+                    tc_fill_a(S.in.a[st], xq, M, K, m0 + r_own, r_own, s, false);
+                }
+            } else {
+                tc_put_b(S.in.b[st], *reinterpret_cast<const uint4 *>(S.in.raw_b[i % kTcRaw][r_own]), r_own);
+            }
+            // the generic-proxy writes above, visible to the tensor core (async proxy)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&S.full[st]);
+        }
+        cp_async_wait_pending<0>();
     }
+    // the last commit covers every MMA issued before it
+    bool ok = true;
+    if (nst > 0 && !*abort) {
+        const int i = nst - 1;
+        if (!mbar_wait(&S.mma_done[i & 1], (i >> 1) & 1)) *abort = 1;
+    }
+    __syncthreads();
+    ok = !*abort;
+    tc_fence_after();
+
+    const float nanv = ok ? 0.0f : __int_as_float(0x7fc00000);  // a wait that gave up: the tile reads NaN
+    const bool vec_out = y && (reinterpret_cast<uintptr_t>(y) & 15) == 0 && N % 4 == 0;
+    // the accumulator into shared memory (warps 0..7: lanes 32 (w % 4) .. + 31,
+    // columns 128 (w / 4) .. + 127), so that the output rows are written coalesced
+    if (warp < 8) {
+        const int q = warp & 3, cg = warp >> 2;
+        const int row = 32 * q + lane;
+#pragma unroll 1
+        for (int c = 0; c < 4; c++) {
+            const int col = 128 * cg + 32 * c;
+            uint32_t r[32];
+            tc_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
+            float4 *dst = reinterpret_cast<float4 *>(&S.part[row][col]);
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+    }
+    // split K: CTA z adds rows [128 z / split, 128 (z+1) / split) over the
+    // cluster in rank order (integers below 2^24: exact); split 1: all rows
+    if (split > 1)
+        cluster_sync();
+    else
+        __syncthreads();
+    const int r0 = kTcBM * z / split, r1 = kTcBM * (z + 1) / split;
+#pragma unroll 4
+    for (int e = tid; e < (r1 - r0) * (kTcBN / 4); e += kTcThreads) {
+        const int row = r0 + e / (kTcBN / 4), c4 = e % (kTcBN / 4);
+        float4 v;
+        if (split == 1) {
+            v = *reinterpret_cast<const float4 *>(&S.part[row][4 * c4]);
+        } else {
+            float4 u[kTcMaxSplit];
+#pragma unroll
+            for (int qq = 0; qq < kTcMaxSplit; qq++)
+                if (qq < split) u[qq] = ld_peer_f4(&S.part[row][4 * c4], (uint32_t)qq);
+            v = u[0];
+#pragma unroll
+            for (int qq = 1; qq < kTcMaxSplit; qq++)
+                if (qq < split) {
+                    v.x = __fadd_rn(v.x, u[qq].x);
+                    v.y = __fadd_rn(v.y, u[qq].y);
+                    v.z = __fadd_rn(v.z, u[qq].z);
+                    v.w = __fadd_rn(v.w, u[qq].w);
+                }
+        }
+        const int m = m0 + row, nb = n0 + 4 * c4;
+        if (m >= M || nb >= N) continue;
+        const float xsm = S.xs[row];
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+        if (acc_out) {
+            if ((reinterpret_cast<uintptr_t>(acc_out) & 15) == 0 && N % 4 == 0 && nb + 4 <= N) {
+                *reinterpret_cast<int4 *>(acc_out + (int64_t)m * N + nb) =
+                    make_int4(__float2int_rz(vv[0]), __float2int_rz(vv[1]), __float2int_rz(vv[2]), __float2int_rz(vv[3]));
+            } else {
+                for (int j = 0; j < 4; j++)
+                    if (nb + j < N) acc_out[(int64_t)m * N + nb + j] = __float2int_rz(vv[j]);
+            }
+        }
+        if (y) {
+            if (vec_out && nb + 4 <= N) {
+                *reinterpret_cast<float4 *>(y + (int64_t)m * N + nb) =
+                    make_float4(__fadd_rn(__fmul_rn(__fmul_rn(vv[0], ws), xsm), nanv),
+                                __fadd_rn(__fmul_rn(__fmul_rn(vv[1], ws), xsm), nanv),
+                                __fadd_rn(__fmul_rn(__fmul_rn(vv[2], ws), xsm), nanv),
+                                __fadd_rn(__fmul_rn(__fmul_rn(vv[3], ws), xsm), nanv));
+            } else {
+                for (int j = 0; j < 4; j++)
+                    if (nb + j < N) y[(int64_t)m * N + nb + j] = __fadd_rn(__fmul_rn(__fmul_rn(vv[j], ws), xsm), nanv);
+            }
+        }
+    }
+    if (split > 1) cluster_sync();  // no CTA leaves while another still reads its shared memory
     tc_fence_before();
     __syncthreads();
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols) : "memory");
+}
+
+// Clusters of `c` CTAs of this kernel that can be resident at once (cached).
+static int tc_resident_clusters(int c, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find({dev, c});
+    if (it != cache.end()) return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, (unsigned)c);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)c;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, t158_tc_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    cache[{dev, c}] = n;
+    return n;
 }
 
 qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
@@ -288,8 +477,32 @@ qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const ui
     const size_t smem = sizeof(TcSmem);
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "qlin_t158_i8: tensor-core tile does not fit");
     blocks_per_sm((const void *)t158_tc_kernel, smem);  // raises the dynamic shared-memory limit
-    dim3 grid((unsigned)((N + kTcBN - 1) / kTcBN), (unsigned)((M + kTcBM - 1) / kTcBM));
-    t158_tc_kernel<<<grid, kTcThreads, smem, st>>>(xq, xs, w, pitch, ws, y, acc, M, N, K);
+    const int tiles_n = (N + kTcBN - 1) / kTcBN, tiles_m = (M + kTcBM - 1) / kTcBM;
+    const int nsteps = (K + kTcKS - 1) / kTcKS;
+    // split K over a cluster when the tiles alone leave SMs idle: the largest
+    // split whose clusters (they must fit within a GPC) are all resident at once
+    const int tiles = tiles_n * tiles_m;
+    int split = 1;
+    for (int c = kTcMaxSplit; c >= 2; c--) {
+        if (c > nsteps || tiles * c > 2 * sm_count()) continue;
+        if (tc_resident_clusters(c, smem) >= tiles) {
+            split = c;
+            break;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)tiles_n, (unsigned)tiles_m, (unsigned)split);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)split;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tc_kernel, xq, xs, w, pitch, ws, y, acc, M, N, K, split));
     QLIN_LAUNCHED("t158_tc_kernel");
     return QLIN_OK;
 }
