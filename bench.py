@@ -251,6 +251,7 @@ def run_decode(args, rank, local, world):
     peak, peak_kind = peaks()
     lm_gbs = lm_alg / (lm_ms / 1e3) / 1e9
     gemv = gemv_m1(dev, stream)
+    prefill = prefill_m512(dev, stream)
     step_gbs = step_bytes * args.steps / (ms / 1e3) / 1e9
     traffic = fused_traffic()
     launches_per_step = qlin.decode_step_t158_launches(gpu.model)
@@ -284,6 +285,7 @@ def run_decode(args, rank, local, world):
             "frac_of_peak": round(step_bytes * args.steps / (ms / 1e3) / 1e9 / peak, 4),
         },
         "gemv_m1": gemv,
+        "prefill_m512": prefill,
         # the step is one launch of the fused kernel: its algorithmic bytes over
         # its CUDA-event time on the launching stream
         "roofline": {
@@ -385,6 +387,57 @@ def _time_rotating(fn, R, alg_bytes, stream):
     del g
     return {"us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
             "copies": R, "calls": n, "algorithmic_bytes": alg_bytes, "timing": "CUDA graph of the rotating calls"}
+
+
+def prefill_m512(dev, stream):
+    """The two 512-token T158 layers of the prompt (1152->6912, 6912->1152) on the tensor
+    cores: each call timed alone with CUDA events after an L2 flush; dense fp16 rate
+    (2 M N K flops per call) against the measured bf16 tensor peak (fp16 and bf16 share
+    one rate)."""
+    import torch
+
+    import synth
+    from weight_streaming_gemv_gb300 import qlin
+
+    tflops_peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            tflops_peak = float(json.load(fh)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        tflops_peak = 1900.0
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    res = {}
+    M = 512
+    for K, N in [(1152, 6912), (6912, 1152)]:
+        d = synth.t158_gemv(2, M, K, N)
+        pitch = qlin.t158_pitch(K)
+        w = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+        x = torch.from_numpy(d["x"]).to(dev)
+        xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+        xs = torch.empty(M, dtype=torch.float32, device=dev)
+        qlin.qlin_quant_i8(x, xq, xs, M, K)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, M, N, K)
+        times = []
+        for _ in range(20):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, M, N, K)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(times)
+        tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        res[f"t158_m{M}_k{K}_n{N}"] = {
+            "us_per_call": round(us, 2), "bound": "tensor", "tflops": round(tf, 1), "peak_tflops": tflops_peak,
+            "frac": round(tf / tflops_peak, 4), "int_ops": 2 * M * N * K,
+            "timing": "median of 20 calls, each after an L2 flush"}
+        del w, x, xq, xs, y
+    del flush
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------- oracle on the host cores
