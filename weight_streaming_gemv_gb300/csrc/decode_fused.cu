@@ -27,7 +27,7 @@ namespace qlin {
 
 struct FusedSmem {
     // offsets in bytes into dynamic shared memory
-    int slots, xr, seg, rope, hvec, xv, lmx, qs, ks, vs, wbuf, abuf, gbuf, scl, misc, ring, total;
+    int slots, xr, seg, rope, racc, hvec, xv, lmx, qs, ks, vs, abuf, gbuf, scl, misc, ring, total;
 };
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -47,6 +47,8 @@ __host__ __device__ inline FusedSmem fused_smem(const t158_model &m, int G) {
     o = align_up(o + 128 * 4, 128);
     s.rope = o;  // cos then sin of this position, head_dim/2 each
     o = align_up(o + m.head_dim * 4, 128);
+    s.racc = o;  // integer sums of the rows of one T158 piece
+    o = align_up(o + kFMaxRows * 4, 128);
     s.hvec = o;
     o = align_up(o + d * 4, 128);
     s.xv = o;
@@ -59,8 +61,6 @@ __host__ __device__ inline FusedSmem fused_smem(const t158_model &m, int G) {
     o = align_up(o + kvd * 4, 128);
     s.vs = o;
     o = align_up(o + kvd * 4, 128);
-    s.wbuf = o;
-    o = align_up(o + m.n_heads * next_pow2(ncmax) * 4, 128);
     s.abuf = o;
     o = align_up(o + m.ffn * 4, 128);
     s.gbuf = o;
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     float *qs = reinterpret_cast<float *>(smem + L.qs);
     float *ks = reinterpret_cast<float *>(smem + L.ks);
     float *vs = reinterpret_cast<float *>(smem + L.vs);
-    float *wbuf = reinterpret_cast<float *>(smem + L.wbuf);
+    int *racc = reinterpret_cast<int *>(smem + L.racc);
     float *gbuf = reinterpret_cast<float *>(smem + L.gbuf);
     float *abuf = reinterpret_cast<float *>(smem + L.abuf);
     float *scl = reinterpret_cast<float *>(smem + L.scl);
@@ -345,23 +345,31 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
                     const int a0 = max(lo, base), a1 = min(hi, base + nrows);
                     if (a1 <= a0) continue;
                     const float ws = sc_l[mat];
-                    pieces(m.w[mat], m.pitch[mat], a0 - base, a1 - base, mat, [&](const Piece &p) {
-                        const uint8_t *slot = take(const_cast<Piece &>(p));
-                        if (!*abort)
-                            slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) {
-                                const int row = base + p.row0 + r;
-                                const float y = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
-                                if (op == kOpQKV)
-                                    st_tagged(A.qkvT + row, y, tg);
-                                else if (op == kOpGate)
-                                    gbuf[row - J0] = y;
-                                else if (op == kOpUp)
-                                    st_tagged(A.aT + row, __fmul_rn(gelu32(gbuf[row - J0]), y), tg);
-                                else  // Wo, down: residual
-                                    st_tagged(A.hT + row, __fadd_rn(hvec[row], y), tg);
-                            });
-                        give();
-                    });
+                    pieces(
+                        m.w[mat], m.pitch[mat], a0 - base, a1 - base, mat,
+                        [&](const Piece &p) {
+                            const uint8_t *slot = take(const_cast<Piece &>(p));
+                            if (!*abort) {
+                                // integer row sums to shared memory, then one epilogue
+                                // loop (a single copy of the scale / GeGLU / residual code)
+                                slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) { racc[r] = acc; });
+                                g.sync();
+                                for (int r = g.tid; r < p.rows; r += g.n) {
+                                    const int row = base + p.row0 + r;
+                                    const float y = __fmul_rn(__fmul_rn((float)(racc[r] - sumx), ws), xs);
+                                    if (op == kOpQKV)
+                                        st_tagged(A.qkvT + row, y, tg);
+                                    else if (op == kOpGate)
+                                        gbuf[row - J0] = y;
+                                    else if (op == kOpUp)
+                                        st_tagged(A.aT + row, __fmul_rn(gelu32(gbuf[row - J0]), y), tg);
+                                    else  // Wo, down: residual
+                                        st_tagged(A.hT + row, __fadd_rn(hvec[row], y), tg);
+                                }
+                            }
+                            give();
+                        },
+                        kFMaxRows);
                 }
             }
         }

@@ -13,6 +13,7 @@ constexpr int kFStages = 4;
 constexpr int kFSlot = 36864;  // bytes per ring slot (16 bf16 rows of 1152)
 constexpr int kFConsumerWarps = 11;  // + 1 producer warp = 12 warps: 3 per SM sub-partition, up to 168 registers
 constexpr int kFThreads = 32 * (kFConsumerWarps + 1);
+constexpr int kFMaxRows = 512;  // rows of a T158 piece (their integer sums wait in shared memory)
 
 struct FusedArgs {
     t158_model m;
@@ -59,30 +60,27 @@ template <int N, class Ptr>
 __device__ __forceinline__ void fetch_tagged_at(Ptr &&ptr, uint32_t mask, uint32_t tag, float (&out)[N],
                                                 volatile int *abort, int32_t *status) {
     uint64_t w[N];
-    uint32_t pending = 0;
 #pragma unroll
-    for (int j = 0; j < N; j++) {
-        w[j] = 0;
-        if (mask & (1u << j)) {
-            w[j] = ld_relaxed_u64(ptr(j));
-            if ((uint32_t)(w[j] >> 32) != tag) pending |= 1u << j;
+    for (int j = 0; j < N; j++) w[j] = 0;
+    uint32_t pending = mask;
+    uint64_t t0 = 0;
+    // one block of loads serves the first pass and every retry (a small loop
+    // body keeps the instruction cache free for the rest of the layer)
+    for (int pass = 0;; pass++) {
+#pragma unroll
+        for (int j = 0; j < N; j++)
+            if (pending & (1u << j)) w[j] = ld_relaxed_u64(ptr(j));
+#pragma unroll
+        for (int j = 0; j < N; j++)
+            if ((pending & (1u << j)) && (uint32_t)(w[j] >> 32) == tag) pending &= ~(1u << j);
+        if (!pending || *abort) break;
+        if (pass == 0) t0 = global_ns();
+        if (global_ns() - t0 > kWaitLimitNs) {
+            raise_status(status, kStatusTimeout);
+            *abort = 1;
+            break;
         }
-    }
-    if (pending) {
-        const uint64_t t0 = global_ns();
-        while (pending && !*abort) {
-            __nanosleep(32);
-#pragma unroll
-            for (int j = 0; j < N; j++)
-                if (pending & (1u << j)) w[j] = ld_relaxed_u64(ptr(j));
-#pragma unroll
-            for (int j = 0; j < N; j++)
-                if ((pending & (1u << j)) && (uint32_t)(w[j] >> 32) == tag) pending &= ~(1u << j);
-            if (pending && global_ns() - t0 > kWaitLimitNs) {
-                raise_status(status, kStatusTimeout);
-                *abort = 1;
-            }
-        }
+        __nanosleep(32);
     }
 #pragma unroll
     for (int j = 0; j < N; j++) out[j] = (mask & (1u << j)) ? __uint_as_float((uint32_t)w[j]) : 0.0f;
@@ -143,7 +141,7 @@ __device__ __forceinline__ void layer_items(const FusedArgs &A, int l, int b, in
     for (int j = 0; j < 3; j++) {
         const int a0 = max(lo, base), a1 = min(hi, base + rows[j]);
         if (a1 > a0)
-            pieces(m.w[j] + (int64_t)l * rows[j] * m.pitch[j], m.pitch[j], a0 - base, a1 - base, j, f);
+            pieces(m.w[j] + (int64_t)l * rows[j] * m.pitch[j], m.pitch[j], a0 - base, a1 - base, j, f, kFMaxRows);
         base += rows[j];
     }
     // attention K/V prefetch (rows strictly below pos) for this CTA's (chunk, head) items
@@ -167,12 +165,12 @@ __device__ __forceinline__ void layer_items(const FusedArgs &A, int l, int b, in
         }
     }
     share(d, b, G, lo, hi);
-    pieces(m.w[3] + (int64_t)l * rows[3] * m.pitch[3], m.pitch[3], lo, hi, 3, f);
+    pieces(m.w[3] + (int64_t)l * rows[3] * m.pitch[3], m.pitch[3], lo, hi, 3, f, kFMaxRows);
     int g0, g1;
     share(ff, b, G, g0, g1);
-    pieces(m.w[4] + (int64_t)l * rows[4] * m.pitch[4], m.pitch[4], g0, g1, 4, f);
-    pieces(m.w[5] + (int64_t)l * rows[5] * m.pitch[5], m.pitch[5], g0, g1, 5, f);
-    pieces(m.w[6] + (int64_t)l * rows[6] * m.pitch[6], m.pitch[6], lo, hi, 6, f);
+    pieces(m.w[4] + (int64_t)l * rows[4] * m.pitch[4], m.pitch[4], g0, g1, 4, f, kFMaxRows);
+    pieces(m.w[5] + (int64_t)l * rows[5] * m.pitch[5], m.pitch[5], g0, g1, 5, f, kFMaxRows);
+    pieces(m.w[6] + (int64_t)l * rows[6] * m.pitch[6], m.pitch[6], lo, hi, 6, f, kFMaxRows);
 }
 
 // lm_head tiles of CTA b
@@ -473,33 +471,22 @@ __device__ __forceinline__ void slot_rows(const uint8_t *slot, int rows, int pit
     }
 }
 
-// Lanes per row for `rows` rows of C chunks over nw warps: the fewest passes
-// times (chunks per lane + reduction steps), in rough cycle units (a chunk
-// about 55 with two in flight, a shuffle step about 30).
+// Lanes per row for `rows` rows of C chunks over nw warps, 4 or 16: the
+// fewer passes times (chunks per lane + reduction steps), in rough cycle units
+// (a chunk about 55 with two in flight, a shuffle step about 30).  16 lanes
+// take rows of any length.
 __device__ __forceinline__ int rows_lpr(int rows, int C, int nw) {
-    int best = 32, best_cost = 1 << 30;
-#pragma unroll
-    for (int lg = 2; lg <= 5; lg++) {
-        const int lpr = 1 << lg;
-        const int per_pass = nw * (32 / lpr);
-        const int passes = (rows + per_pass - 1) / per_pass;
-        const int cost = passes * (((C + lpr - 1) / lpr) * 55 + lg * 30);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = lpr;
-        }
-    }
-    return best;
+    const int pass4 = (rows + nw * 8 - 1) / (nw * 8), pass16 = (rows + nw * 2 - 1) / (nw * 2);
+    const int c4 = pass4 * (((C + 3) / 4) * 55 + 2 * 30), c16 = pass16 * (((C + 15) / 16) * 55 + 4 * 30);
+    return c4 < c16 ? 4 : 16;
 }
 
 template <class F>
 __device__ __forceinline__ void slot_rows_any(const uint8_t *slot, int rows, int pitch, const uint4 *xr, Grp g, F &&f) {
-    switch (rows_lpr(rows, pitch / 16, g.n >> 5)) {
-        case 4: slot_rows<4>(slot, rows, pitch, xr, g, f); break;
-        case 8: slot_rows<8>(slot, rows, pitch, xr, g, f); break;
-        case 16: slot_rows<16>(slot, rows, pitch, xr, g, f); break;
-        default: slot_rows<32>(slot, rows, pitch, xr, g, f); break;
-    }
+    if (rows_lpr(rows, pitch / 16, g.n >> 5) == 4)
+        slot_rows<4>(slot, rows, pitch, xr, g, f);
+    else
+        slot_rows<16>(slot, rows, pitch, xr, g, f);
 }
 
 }  // namespace qlin
