@@ -408,6 +408,9 @@ static qlin_status check_model(const t158_model *m) {
         QLIN_REQUIRE(m->pitch[j] <= kFSlot, QLIN_ERR_UNSUPPORTED, "decode_step_t158: pitch[%d]=%lld above %d", j,
                      (long long)m->pitch[j], kFSlot);
     }
+    QLIN_REQUIRE(m->pitch[4] == m->pitch[5], QLIN_ERR_UNSUPPORTED,
+                 "decode_step_t158: gate and up rows must have the same pitch (%lld, %lld)", (long long)m->pitch[4],
+                 (long long)m->pitch[5]);
     QLIN_REQUIRE(32 * kvd * 4 <= kFSlot && d * 2 <= kFSlot, QLIN_ERR_UNSUPPORTED,
                  "decode_step_t158: kv width %d or dim %d too large for the weight ring", kvd, d);
     QLIN_REQUIRE(m->max_pos <= 4096, QLIN_ERR_UNSUPPORTED, "decode_step_t158: max_pos %d above 4096", m->max_pos);

@@ -27,7 +27,7 @@ namespace qlin {
 
 struct FusedSmem {
     // offsets in bytes into dynamic shared memory
-    int slots, xr, seg, rope, racc, hvec, xv, lmx, qs, ks, vs, abuf, gbuf, scl, misc, ring, total;
+    int slots, xr, seg, rope, racc, hvec, xv, lmx, qs, ks, vs, abuf, scl, misc, ring, total;
 };
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -47,8 +47,8 @@ __host__ __device__ inline FusedSmem fused_smem(const t158_model &m, int G) {
     o = align_up(o + 128 * 4, 128);
     s.rope = o;  // cos then sin of this position, head_dim/2 each
     o = align_up(o + m.head_dim * 4, 128);
-    s.racc = o;  // integer sums of the rows of one T158 piece
-    o = align_up(o + kFMaxRows * 4, 128);
+    s.racc = o;  // integer sums of the rows of one T158 piece (of a gate piece and its up piece)
+    o = align_up(o + 2 * kFMaxRows * 4, 128);
     s.hvec = o;
     o = align_up(o + d * 4, 128);
     s.xv = o;
@@ -63,8 +63,6 @@ __host__ __device__ inline FusedSmem fused_smem(const t158_model &m, int G) {
     o = align_up(o + kvd * 4, 128);
     s.abuf = o;
     o = align_up(o + m.ffn * 4, 128);
-    s.gbuf = o;
-    o = align_up(o + (m.ffn / G + 2) * 4, 128);
     s.scl = o;  // every matrix scale of the model
     o = align_up(o + m.n_layers * T158_NMAT * 4, 128);
     s.misc = o;  // red[32] f32, ired[32] i32, sc[32] f32, flags
@@ -136,7 +134,6 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     float *ks = reinterpret_cast<float *>(smem + L.ks);
     float *vs = reinterpret_cast<float *>(smem + L.vs);
     int *racc = reinterpret_cast<int *>(smem + L.racc);
-    float *gbuf = reinterpret_cast<float *>(smem + L.gbuf);
     float *abuf = reinterpret_cast<float *>(smem + L.abuf);
     float *scl = reinterpret_cast<float *>(smem + L.scl);
 
@@ -168,6 +165,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     const uint32_t seq = *reinterpret_cast<volatile const unsigned *>(A.seq) & 0x3fffffu;
 
     for (int i = g.tid; i < m.n_layers * T158_NMAT; i += g.n) scl[i] = m.scales[i];
+    for (int i = g.tid; i < 2 * kFMaxRows; i += g.n) racc[i] = 0;
 
     // Step 0: h = emb[token], kept in hvec (owners of residual rows read their rows from it)
     int tok = *A.token;
@@ -216,7 +214,9 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
                                        &sumx, g, abort, A.status);
             }
 
-            if (op == kOpAttn) {
+            if (op == kOpUp) {
+                // up runs together with gate
+            } else if (op == kOpAttn) {
                 // ---- per (chunk, head) item: RoPE, cache append, attention partials
                 const uint32_t tq = make_tag(seq, l, 1), tp = make_tag(seq, l, 2);
                 for (int e = b; e < nc * nh; e += G) {
@@ -335,39 +335,57 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
                     lo = J0;
                     hi = J1;
                 }
-                const uint32_t tg = make_tag(seq, l, op == kOpQKV ? 1 : op == kOpWo ? 3 : op == kOpUp ? 4 : 5);
+                const uint32_t tg = make_tag(seq, l, op == kOpQKV ? 1 : op == kOpWo ? 3 : op == kOpGate ? 4 : 5);
                 const int nmat = op == kOpQKV ? 3 : 1;
 #pragma unroll 1
                 for (int jm = 0; jm < nmat; jm++) {
-                    const int mat = op == kOpQKV ? jm : op == kOpWo ? 3 : op == kOpGate ? 4 : op == kOpUp ? 5 : 6;
+                    const int mat = op == kOpQKV ? jm : op == kOpWo ? 3 : op == kOpGate ? 4 : 6;
                     const int base = op == kOpQKV ? (jm == 0 ? 0 : jm == 1 ? qd : qd + kvd) : 0;
                     const int nrows = op == kOpQKV ? (jm == 0 ? qd : kvd) : (op == kOpWo || op == kOpDown ? d : ff);
                     const int a0 = max(lo, base), a1 = min(hi, base + nrows);
                     if (a1 <= a0) continue;
-                    const float ws = sc_l[mat];
+                    const float ws = sc_l[mat], wsu = sc_l[5];
+                    const bool gu = op == kOpGate;  // gate piece t, its up piece t + 1
                     pieces(
                         m.w[mat], m.pitch[mat], a0 - base, a1 - base, mat,
                         [&](const Piece &p) {
-                            const uint8_t *slot = take(const_cast<Piece &>(p));
+                            if (gu) {
+                                if (g.tid == 0 && !*abort &&
+                                    (!mbar_wait(&ring->full[t % kFStages], (t / kFStages) & 1) ||
+                                     !mbar_wait(&ring->full[(t + 1) % kFStages], ((t + 1) / kFStages) & 1))) {
+                                    raise_status(A.status, kStatusTimeout);
+                                    *abort = 1;
+                                }
+                                g.sync();
+                            } else {
+                                wait_full(t);
+                            }
+                            const uint8_t *slot = slots + (size_t)(t % kFStages) * kFSlot;
+                            const uint8_t *slot_u = slots + (size_t)((t + 1) % kFStages) * kFSlot;
                             if (!*abort) {
                                 // integer row sums to shared memory, then one epilogue
                                 // loop (a single copy of the scale / GeGLU / residual code)
-                                slot_rows_any(slot, p.rows, p.pitch, xr, g, [&](int r, int acc) { racc[r] = acc; });
+                                t158_rows(slot, gu ? 2 * p.rows : p.rows, p.pitch, xr, racc, g, slot_u, p.rows);
                                 g.sync();
                                 for (int r = g.tid; r < p.rows; r += g.n) {
                                     const int row = base + p.row0 + r;
-                                    const float y = __fmul_rn(__fmul_rn((float)(racc[r] - sumx), ws), xs);
-                                    if (op == kOpQKV)
+                                    const int acc = racc[r];
+                                    racc[r] = 0;  // zero again for the next piece
+                                    const float y = __fmul_rn(__fmul_rn((float)(acc - sumx), ws), xs);
+                                    if (op == kOpQKV) {
                                         st_tagged(A.qkvT + row, y, tg);
-                                    else if (op == kOpGate)
-                                        gbuf[row - J0] = y;
-                                    else if (op == kOpUp)
-                                        st_tagged(A.aT + row, __fmul_rn(gelu32(gbuf[row - J0]), y), tg);
-                                    else  // Wo, down: residual
+                                    } else if (gu) {
+                                        const int accu = racc[p.rows + r];
+                                        racc[p.rows + r] = 0;
+                                        const float u = __fmul_rn(__fmul_rn((float)(accu - sumx), wsu), xs);
+                                        st_tagged(A.aT + row, __fmul_rn(gelu32(y), u), tg);
+                                    } else {  // Wo, down: residual
                                         st_tagged(A.hT + row, __fadd_rn(hvec[row], y), tg);
+                                    }
                                 }
                             }
                             give();
+                            if (gu) give();
                         },
                         kFMaxRows);
                 }

@@ -168,8 +168,14 @@ __device__ __forceinline__ void layer_items(const FusedArgs &A, int l, int b, in
     pieces(m.w[3] + (int64_t)l * rows[3] * m.pitch[3], m.pitch[3], lo, hi, 3, f, kFMaxRows);
     int g0, g1;
     share(ff, b, G, g0, g1);
-    pieces(m.w[4] + (int64_t)l * rows[4] * m.pitch[4], m.pitch[4], g0, g1, 4, f, kFMaxRows);
-    pieces(m.w[5] + (int64_t)l * rows[5] * m.pitch[5], m.pitch[5], g0, g1, 5, f, kFMaxRows);
+    // gate and up in pairs over the same rows (one pass computes both)
+    pieces(m.w[4] + (int64_t)l * rows[4] * m.pitch[4], m.pitch[4], g0, g1, 4, [&](const Piece &p) {
+        f(p);
+        Piece u = p;
+        u.mat = 5;
+        u.src = m.w[5] + (int64_t)l * rows[5] * m.pitch[5] + (int64_t)p.row0 * m.pitch[5];
+        f(u);
+    }, kFMaxRows);
     pieces(m.w[6] + (int64_t)l * rows[6] * m.pitch[6], m.pitch[6], lo, hi, 6, f, kFMaxRows);
 }
 
@@ -441,52 +447,38 @@ __device__ __forceinline__ int chunk_dot(const uint4 wv, const uint4 *X, int acc
     return acc;
 }
 
-// rows x pitch packed bytes at `slot` (shared memory) against the planes xr;
-// f(row, acc) with the exact integer sum of d * x (digits 0..2) per row.  LPR
-// lanes share a row; a lane takes chunks sub, sub + LPR, ... two at a time
-// into two accumulators (two independent dp4a chains).
-template <int LPR, class F>
-__device__ __forceinline__ void slot_rows(const uint8_t *slot, int rows, int pitch, const uint4 *xr, Grp g, F &&f) {
-    constexpr int RPS = 32 / LPR;
-    const int lane = g.lane(), sub = lane % LPR, rsub = lane / LPR;
+// Integer row sums of `rows` packed rows (pitch bytes each) at `slot` against
+// the planes xr, added into racc[row] (shared memory, zero on entry); with
+// slot2, rows rows1.. come from slot2 (two matrices of one input in one pass).  The
+// rows x C chunk dot products are spread over the whole group in units of U
+// chunks of one row (U <= 4, so that nearly every thread has work and keeps
+// several independent chunks in flight); unit k of a row takes chunks k,
+// k + upr, ... so consecutive lanes read consecutive chunks.  Partial sums
+// meet through shared-memory atomics: integer addition, exact in any order.
+__device__ __forceinline__ void t158_rows(const uint8_t *slot, int rows, int pitch, const uint4 *xr, int *racc, Grp g,
+                                          const uint8_t *slot2 = nullptr, int rows1 = 1 << 30) {
     const int C = pitch / 16;
-    const int nw = g.n >> 5;
-    for (int r0 = g.warp() * RPS; r0 < rows; r0 += nw * RPS) {
-        const int row = r0 + rsub;
-        int acc0 = 0, acc1 = 0;
-        if (row < rows) {
-            const uint8_t *wr = slot + (size_t)row * pitch;
-            int c = sub;
-            for (; c + LPR < C; c += 2 * LPR) {
-                const uint4 wa = lds128(wr + (size_t)c * 16), wb = lds128(wr + (size_t)(c + LPR) * 16);
-                acc0 = chunk_dot(wa, xr + (size_t)c * 5, acc0);
-                acc1 = chunk_dot(wb, xr + (size_t)(c + LPR) * 5, acc1);
-            }
-            if (c < C) acc0 = chunk_dot(lds128(wr + (size_t)c * 16), xr + (size_t)c * 5, acc0);
-        }
-        int acc = acc0 + acc1;
+    int U = (rows * C + g.n - 1) / g.n;
+    U = U < 1 ? 1 : U > 4 ? 4 : U;
+    const int upr = (C + U - 1) / U;
+    const int units = rows * upr;
+    for (int u = g.tid; u < units; u += g.n) {
+        const int r = u / upr, k = u - r * upr;
+        const uint8_t *wr = r < rows1 ? slot + (size_t)r * pitch : slot2 + (size_t)(r - rows1) * pitch;
+        int a0 = 0, a1 = 0;
 #pragma unroll
-        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (sub == 0 && row < rows) f(row, acc);
+        for (int j = 0; j < 4; j++) {
+            const int c = k + j * upr;
+            if (j < U && c < C) {
+                const int t = chunk_dot(lds128(wr + (size_t)c * 16), xr + (size_t)c * 5, 0);
+                if (j & 1)
+                    a1 += t;
+                else
+                    a0 += t;
+            }
+        }
+        atomicAdd(&racc[r], a0 + a1);
     }
-}
-
-// Lanes per row for `rows` rows of C chunks over nw warps, 4 or 16: the
-// fewer passes times (chunks per lane + reduction steps), in rough cycle units
-// (a chunk about 55 with two in flight, a shuffle step about 30).  16 lanes
-// take rows of any length.
-__device__ __forceinline__ int rows_lpr(int rows, int C, int nw) {
-    const int pass4 = (rows + nw * 8 - 1) / (nw * 8), pass16 = (rows + nw * 2 - 1) / (nw * 2);
-    const int c4 = pass4 * (((C + 3) / 4) * 55 + 2 * 30), c16 = pass16 * (((C + 15) / 16) * 55 + 4 * 30);
-    return c4 < c16 ? 4 : 16;
-}
-
-template <class F>
-__device__ __forceinline__ void slot_rows_any(const uint8_t *slot, int rows, int pitch, const uint4 *xr, Grp g, F &&f) {
-    if (rows_lpr(rows, pitch / 16, g.n >> 5) == 4)
-        slot_rows<4>(slot, rows, pitch, xr, g, f);
-    else
-        slot_rows<16>(slot, rows, pitch, xr, g, f);
 }
 
 }  // namespace qlin
