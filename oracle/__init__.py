@@ -62,6 +62,8 @@ def _L():
                 "or_w8_quantize": ([p, i64, p, p], ctypes.c_int),
                 "or_quant_i8": ([p, i64, i64, p, p], ctypes.c_int),
                 "or_w8_linear": ([p, p, i64, f32, i64, i64, i64, p], ctypes.c_int),
+                "or_w8g_quantize": ([p, i64, i64, i64, p, p], ctypes.c_int),
+                "or_w8g_linear": ([p, p, i64, p, i64, i64, i64, i64, i64, p], ctypes.c_int),
                 "or_t158_pack": ([p, i64, i64, p, i64], ctypes.c_int),
                 "or_t158_unpack": ([p, i64, i64, i64, p], ctypes.c_int),
                 "or_t158_linear": ([p, p, p, i64, f32, i64, i64, i64, p, p], ctypes.c_int),
@@ -122,6 +124,29 @@ def w8_linear(x: np.ndarray, q: np.ndarray, s: float, K: int | None = None):
     N, pitch = q.shape
     y = np.empty((M, N), np.float32)
     _check(_L().or_w8_linear(_p(x), _p(q), pitch, np.float32(s), M, N, K, _p(y)), "w8_linear")
+    return y
+
+
+# ------------------------------------------------------------------ W8 with group scales
+def w8g_quantize(w: np.ndarray, G: int = 128):
+    """int8 codes [N][K] and fp32 scales [N][ceil(K/G)] (one scale per G weights of a row)."""
+    w = np.ascontiguousarray(np.atleast_2d(w), np.float32)
+    N, K = w.shape
+    q = np.empty((N, K), np.int8)
+    s = np.empty((N, (K + G - 1) // G), np.float32)
+    _check(_L().or_w8g_quantize(_p(w), N, K, G, _p(q), _p(s)), "w8g_quantize")
+    return q, s
+
+
+def w8g_linear(x: np.ndarray, q: np.ndarray, scales: np.ndarray, G: int = 128, K: int | None = None):
+    x = np.ascontiguousarray(np.atleast_2d(x), np.float32)
+    q = np.ascontiguousarray(q, np.int8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    M = x.shape[0]
+    K = x.shape[1] if K is None else K
+    N, pitch = q.shape
+    y = np.empty((M, N), np.float32)
+    _check(_L().or_w8g_linear(_p(x), _p(q), pitch, _p(scales), scales.shape[1], G, M, N, K, _p(y)), "w8g_linear")
     return y
 
 

@@ -103,6 +103,51 @@ int or_w8_linear(const float *x, const int8_t *q, int64_t q_pitch, float s, int6
     return OR_OK;
 }
 
+/* ------------------------------------------------------------------ W8 with group scales
+ * gemma.cpp's I8Stream ([gemma.cpp tour] "The compression formats"): int8 in
+ * groups of 128 with a shared scale; runq.c's Q8_0 ([llama2.c] "Key ideas &
+ * tradeoffs"): symmetric, range +-127, weights only.  Reading: the groups
+ * are G consecutive weights of a row along K (the last group of a row is
+ * shorter when G does not divide K), each quantised with the W8 rule above
+ * (its own absmax, the 1e-9 floor, fp32 division, round half to even).
+ * q: int8 [N][K]; scales: fp32 [N][ceil(K/G)].
+ */
+int or_w8g_quantize(const float *w, int64_t N, int64_t K, int64_t G, int8_t *q, float *scales) {
+    if (!w || !q || !scales || N < 1 || K < 1 || G < 1) return OR_EINVAL;
+    const int64_t ng = (K + G - 1) / G;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t g = 0; g < ng; g++) {
+            const int64_t k0 = g * G, len = (k0 + G <= K) ? G : K - k0;
+            const float s = absmax_scale(w + n * K + k0, len);
+            for (int64_t k = k0; k < k0 + len; k++) q[n * K + k] = quant_one(w[n * K + k], s);
+            scales[n * ng + g] = s;
+        }
+    return OR_OK;
+}
+
+/* y[m][n] = sum_g scale[n][g] * (sum_{k in g} x[m][k] * q[n][k]): each
+ * group's dot product takes its own scale, in fp64, rounded once to fp32. */
+int or_w8g_linear(const float *x, const int8_t *q, int64_t q_pitch, const float *scales, int64_t s_pitch, int64_t G,
+                  int64_t M, int64_t N, int64_t K, float *y) {
+    if (!x || !q || !scales || !y || M < 1 || N < 1 || K < 1 || G < 1 || q_pitch < K || s_pitch < (K + G - 1) / G)
+        return OR_EINVAL;
+    const int64_t ng = (K + G - 1) / G;
+    for (int64_t m = 0; m < M; m++) {
+#pragma omp parallel for schedule(static)
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int64_t g = 0; g < ng; g++) {
+                double part = 0.0;
+                for (int64_t k = g * G; k < K && k < (g + 1) * G; k++)
+                    part += (double)x[m * K + k] * (double)q[n * q_pitch + k];
+                acc += part * (double)scales[n * s_pitch + g];
+            }
+            y[m * N + n] = (float)acc;
+        }
+    }
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------ S2
  * T158 packing, [citric] "Step 1": five ternary weights per byte in base 3
  * (3^5 = 243 <= 256).  Digit order and row layout are not on the page; the
