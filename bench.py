@@ -352,6 +352,19 @@ def gemv_m1(dev, stream):
 
     res["w8_k4096_n11008"] = _time_rotating(w8, R, alg, stream)
     del ws
+    # W8 with one scale per 128 weights, same shape
+    G = 128
+    s_pitch = (K // G + 3) // 4 * 4
+    sc1 = torch.rand((N, s_pitch), dtype=torch.float32, device=dev) * 0.01 + 0.001
+    ws = wq.repeat(R, 1)
+    scs = sc1.repeat(R, 1)
+    alg = N * K + 4 * N * (K // G) + 4 * K + 4 * N
+
+    def w8g(r):
+        qlin.qlin_w8g_f32(x, ws[r * N], K, scs[r * N], s_pitch, G, y, 1, N, K)
+
+    res["w8g128_k4096_n11008"] = _time_rotating(w8g, R, alg, stream)
+    del ws, scs
     torch.cuda.empty_cache()
     return res
 

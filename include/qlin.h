@@ -135,6 +135,30 @@ qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float
                         int K, qlin_stream_t stream);
 
 /* ========================================================================
+ * W8 with one scale per group of G weights ([gemma.cpp tour] "The compression
+ * formats": I8Stream, int8 groups of 128 with a shared scale; [llama2.c] "Key
+ * ideas & tradeoffs": runq.c's Q8_0, symmetric +-127, weights only).  The
+ * groups are G consecutive weights of a row along K (the last group of a row
+ * is shorter when G does not divide K); each is quantised with the W8 rule:
+ * scale = max(|w|, 1e-9) / 127 (fp32 division), codes rint(w / scale)
+ * (half to even), clip +-127.
+ * qlin_w8g_quantize: w device fp32 [N][K] (4-byte aligned); w8 device int8
+ * [N][w_pitch] (16-byte aligned, w_pitch >= K, multiple of 16; bytes past K
+ * written 0); scales device fp32 [N][s_pitch] (16-byte aligned, s_pitch >=
+ * ceil(K/G), multiple of 4; slots past ceil(K/G) written 0).  G: a multiple
+ * of 16, >= 16 (128 in the cited formats).
+ * qlin_w8g_f32: y[m][n] = sum_g scales[n][g] * sum_{k in g} x[m][k] w8[n][k],
+ * fp32 activations as qlin_w8_f32 (the same one-token kernel, each 16-weight
+ * chunk's dot product taking its group's scale); x device fp32 [M][K]; y
+ * device fp32 [M][N]; M: 1..64.  Accuracy as qlin_w8_f32.
+ * Both asynchronous on `stream`; INVALID_ARG for bad sizes or alignment.
+ * ====================================================================== */
+qlin_status qlin_w8g_quantize(const float *w, int64_t N, int64_t K, int G, int8_t *w8, int64_t w_pitch, float *scales,
+                              int64_t s_pitch, qlin_stream_t stream);
+qlin_status qlin_w8g_f32(const float *x, const int8_t *w8, int64_t w_pitch, const float *scales, int64_t s_pitch, int G,
+                         float *y, int M, int N, int K, qlin_stream_t stream);
+
+/* ========================================================================
  * Decode-step building blocks (each also runs fused inside decode_step_t158).
  * ====================================================================== */
 

@@ -250,3 +250,40 @@ def test_w8_linear(dev, M, K, N):
     y = _empty((M, N), torch.float32, dev)
     qlin.qlin_w8_f32(to_dev(d["x"], dev), to_dev(w8, dev), pitch, float(s_o), y, M, N, K)
     assert max_abs_rel(host(y), y_o) <= 1e-5
+
+
+# ---------------------------------------------------------------- W8 with group scales
+def _w8g_case(dev, M, K, N, G, seed, x_offset=0, w_pitch=None):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    d = synth.w8_gemv(seed, M, K, N)
+    q_o, s_o = oracle.w8g_quantize(d["w"], G)
+    y_o = oracle.w8g_linear(d["x"], q_o, s_o, G)
+    pitch = w_pitch or (K + 15) // 16 * 16
+    ng = (K + G - 1) // G
+    s_pitch = (ng + 3) // 4 * 4
+    w8 = _empty((N, pitch), torch.int8, dev)
+    sc = _empty((N, s_pitch), torch.float32, dev)
+    qlin.qlin_w8g_quantize(to_dev(d["w"], dev), N, K, G, w8, pitch, sc, s_pitch)
+    w8h, sch = host(w8), host(sc)
+    np.testing.assert_array_equal(w8h[:, :K], q_o)
+    assert (w8h[:, K:] == 0).all()
+    np.testing.assert_array_equal(sch[:, :ng], s_o)
+    assert (sch[:, ng:] == 0).all()
+    buf = torch.zeros(M * K + x_offset, dtype=torch.float32, device=dev)
+    buf[x_offset:] = to_dev(d["x"].reshape(-1), dev)
+    y = _empty((M, N), torch.float32, dev)
+    qlin.qlin_w8g_f32(buf[x_offset:], w8, pitch, sc, s_pitch, G, y, M, N, K)
+    assert max_abs_rel(host(y), y_o) <= 1e-5
+
+
+@pytest.mark.parametrize("M,K,N,G", [(1, 4096, 11008, 128), (1, 11008, 4096, 128), (1, 300, 70, 128), (1, 1000, 33, 64),
+                                     (4, 4096, 1000, 128), (16, 1000, 300, 128), (3, 130, 7, 16)])
+def test_w8g_quantize_bit_exact_and_linear(dev, M, K, N, G):
+    _w8g_case(dev, M, K, N, G, seed=21)
+
+
+def test_w8g_unaligned_x_and_wide_pitch(dev):
+    # x at an odd float offset; row pitch far past K (chunks past K take no scale)
+    _w8g_case(dev, 1, 100, 40, 16, seed=22, x_offset=1, w_pitch=512)

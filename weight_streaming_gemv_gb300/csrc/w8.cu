@@ -32,6 +32,31 @@ __global__ void w8_scale_kernel(float *scale) {
     *scale = quant_scale(__uint_as_float(*reinterpret_cast<unsigned int *>(scale)));
 }
 
+// Group quantisation: one warp per (row n, group g) of G weights; the group's
+// absmax, its step (the W8 rule) and codes; the row's bytes past K and the
+// scale slots past ceil(K/G) are written zero.
+__global__ void w8g_quant_kernel(const float *__restrict__ w, int64_t N, int64_t K, int G, int8_t *__restrict__ q,
+                                 int64_t pitch, float *__restrict__ scales, int64_t s_pitch) {
+    const int64_t ng = (K + G - 1) / G;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= N * s_pitch) return;
+    const int64_t n = gw / s_pitch, g = gw % s_pitch;
+    if (g >= ng) {
+        if (lane == 0) scales[n * s_pitch + g] = 0.0f;
+        return;
+    }
+    const int64_t k0 = g * G, k1 = min(K, k0 + G);
+    float a = 0.0f;
+    for (int64_t k = k0 + lane; k < k1; k += 32) a = fmaxf(a, fabsf(w[n * K + k]));
+    a = warp_max(a);
+    const float sc = quant_scale(a);
+    for (int64_t k = k0 + lane; k < k1; k += 32) q[n * pitch + k] = (int8_t)quant_code(w[n * K + k], sc);
+    if (g == ng - 1)
+        for (int64_t k = K + lane; k < pitch; k += 32) q[n * pitch + k] = 0;
+    if (lane == 0) scales[n * s_pitch + g] = sc;
+}
+
 // ---------------------------------------------------------------- S5 GEMV
 // int8 byte j of a (bias-flipped) word -> exact fp32 value
 __device__ __forceinline__ float i8_to_f32(uint32_t flipped, uint32_t sel) {
@@ -41,10 +66,13 @@ __device__ __forceinline__ float i8_to_f32(uint32_t flipped, uint32_t sel) {
 // One warp handles R rows; lanes take 16-byte chunks c = lane + 32 j; the
 // fp32 activations of a chunk are read from shared memory once and used for
 // all R rows.  MT tokens per block.
+// scales: null for one scale s of the whole tensor, else group scales
+// [N][s_pitch], one per G weights of a row (G a multiple of 16, so a chunk of
+// 16 weights lies in one group): each chunk's dot product takes its scale.
 template <int R, int MT>
 __global__ void __launch_bounds__(256) w8_gemv_kernel(const float *__restrict__ x, const int8_t *__restrict__ w,
                                                       int64_t pitch, float s, float *__restrict__ y, int M, int N,
-                                                      int K) {
+                                                      int K, const float *__restrict__ scales, int64_t s_pitch, int G) {
     extern __shared__ float4 xs4[];  // [MT][C*4] float4
     const int C = (K + 15) / 16;
     const int m0 = blockIdx.y * MT;
@@ -85,22 +113,33 @@ __global__ void __launch_bounds__(256) w8_gemv_kernel(const float *__restrict__ 
                     wf[r][4 * q + 3] = i8_to_f32(u[q], 0x7653u);
                 }
             }
+            float gs[R];  // the chunk's group scale per row (1 without groups)
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                const int64_t row = r0 + r;
+                gs[r] = (scales && row < N) ? __ldg(scales + row * s_pitch + (16 * c) / G) : 1.0f;
+            }
 #pragma unroll
             for (int mm = 0; mm < MT; mm++) {
                 const float4 *X = xs4 + ((size_t)mm * C + c) * 4;
+                float cs[R];
+#pragma unroll
+                for (int r = 0; r < R; r++) cs[r] = scales ? 0.0f : acc[r][mm];
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     const float4 xv = X[q];
 #pragma unroll
                     for (int r = 0; r < R; r++) {
-                        float a = acc[r][mm];
+                        float a = cs[r];
                         a = fmaf(xv.x, wf[r][4 * q + 0], a);
                         a = fmaf(xv.y, wf[r][4 * q + 1], a);
                         a = fmaf(xv.z, wf[r][4 * q + 2], a);
                         a = fmaf(xv.w, wf[r][4 * q + 3], a);
-                        acc[r][mm] = a;
+                        cs[r] = a;
                     }
                 }
+#pragma unroll
+                for (int r = 0; r < R; r++) acc[r][mm] = scales ? fmaf(cs[r], gs[r], acc[r][mm]) : cs[r];
             }
         }
 #pragma unroll
@@ -150,25 +189,34 @@ constexpr int kW8MaxTR = 32;   // rows per tile
 
 struct W8Smem {
     int slot, tr, ks, xoff, total;  // slots at 0, then (at xoff) the ring and the partials
+    int sslot, soff;                // group scales: a slot of sslot bytes per stage at soff (0 without groups)
 };
 
-__host__ __device__ inline W8Smem w8_stream_layout(int64_t pitch, int smem_optin) {
+// s_pitch: floats per row of group scales (0: one scale for the tensor)
+__host__ __device__ inline W8Smem w8_stream_layout(int64_t pitch, int smem_optin, int64_t s_pitch = 0) {
     W8Smem L;
     const int C = (int)(pitch / 16);
     L.ks = 1;  // the fewest K parts that leave at most kW8JMax chunks per lane
     while (L.ks < kW8Warps && (C + L.ks * 32 - 1) / (L.ks * 32) > kW8JMax) L.ks *= 2;
     const int rstep = 2 * (kW8Warps / L.ks);  // a tile holds whole row pairs of every group
     const int fixed = (int)(sizeof(Ring<kW8Stages>) + 2 * kW8MaxTR * kW8Warps * sizeof(float)) + 256;
-    int slot = (smem_optin / 2 - 1024 - fixed) / kW8Stages;
+    // weight tiles of up to 32 KB, group scales (4 s_pitch bytes a row) beside
+    // them, all within half the shared memory so that two CTAs fit on an SM
+    const int budget = smem_optin / 2 - 1024 - fixed;
+    int slot = budget / kW8Stages;
     slot = slot > 32768 ? 32768 : slot;
     slot = slot / 128 * 128;  // so that the rounded-up tile below stays within it
     int tr = (int)(slot / pitch);
     tr = tr > kW8MaxTR ? kW8MaxTR : tr;
     tr = tr / rstep * rstep;
+    while (tr > 0 && kW8Stages * (((tr * pitch + 127) / 128 + (tr * 4 * s_pitch + 127) / 128) * 128) > budget)
+        tr -= rstep;
     L.tr = tr;
     L.slot = (int)((tr * pitch + 127) / 128 * 128);
-    L.xoff = kW8Stages * L.slot;
-    L.total = kW8Stages * L.slot + fixed;
+    L.sslot = (int)((tr * 4 * s_pitch + 127) / 128 * 128);
+    L.soff = kW8Stages * L.slot;
+    L.xoff = kW8Stages * (L.slot + L.sslot);
+    L.total = L.xoff + fixed;
     if ((C + L.ks * 32 - 1) / (L.ks * 32) > kW8JMax) L.tr = 0;  // K too large for this kernel
     return L;
 }
@@ -176,10 +224,14 @@ __host__ __device__ inline W8Smem w8_stream_layout(int64_t pitch, int smem_optin
 // 2^e for -126 <= e <= 127
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
 
+// GROUPED: group scales `scales` [N][s_pitch], one per G weights of a row;
+// otherwise one scale s of the whole tensor (scales unused)
+template <bool GROUPED>
 __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const float *__restrict__ x,
                                                                          const int8_t *__restrict__ w, int64_t pitch,
                                                                          float s, float *__restrict__ y, int N, int K,
-                                                                         W8Smem L) {
+                                                                         W8Smem L, const float *__restrict__ scales,
+                                                                         int64_t s_pitch, int G) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *slots = smem;
     Ring<kW8Stages> *ring = reinterpret_cast<Ring<kW8Stages> *>(smem + L.xoff);
@@ -200,9 +252,11 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
     auto issue = [&](int t) {
         const int st = t % kW8Stages;
         const int64_t row = r0 + (int64_t)t * TR;
-        const uint32_t bytes = (uint32_t)(min((int64_t)TR, r1 - row) * pitch);
-        mbar_arrive_expect_tx(&ring->full[st], bytes);
+        const int64_t nr = min((int64_t)TR, r1 - row);
+        const uint32_t bytes = (uint32_t)(nr * pitch), sbytes = GROUPED ? (uint32_t)(nr * 4 * s_pitch) : 0u;
+        mbar_arrive_expect_tx(&ring->full[st], bytes + sbytes);
         bulk_g2s(slots + (size_t)st * L.slot, w + row * pitch, bytes, &ring->full[st], pol);
+        if (GROUPED) bulk_g2s(slots + L.soff + (size_t)st * L.sslot, scales + row * s_pitch, sbytes, &ring->full[st], pol);
     };
     if (threadIdx.x == 0 && ntiles > 0) issue(0);
     // consumers: load this lane's x slice first, so that these few loads do not
@@ -316,15 +370,18 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
         float *pt = part + (size_t)(t & 1) * kW8MaxTR * kW8Warps;
         if (ok) {
             const uint8_t *tile = slots + (size_t)st * L.slot;
+            const float *stile = reinterpret_cast<const float *>(slots + L.soff + (size_t)st * L.sslot);
             const int g0 = grp * gsz, g1 = min(rows, g0 + gsz);
             for (int r = g0; r < g1; r += 2) {
                 const bool two = r + 1 < g1;
                 const uint8_t *ra = tile + (size_t)r * pitch, *rb = ra + pitch;
                 int Aa = 0, Ba = 0, Ca = 0, Ab = 0, Bb = 0, Cb = 0;
+                float ga = 0.0f, gb = 0.0f;  // with group scales: sum of the chunks' scaled sums
 #pragma unroll
                 for (int j = 0; j < kW8JMax; j++) {
                     const int c = ca + lane + 32 * j;
                     if (c < cb) {
+                        if (GROUPED) Aa = Ba = Ca = Ab = Bb = Cb = 0;
                         const uint4 wa = lds128(ra + (size_t)c * 16);
                         const uint4 wb = two ? lds128(rb + (size_t)c * 16) : make_uint4(0u, 0u, 0u, 0u);
                         const uint32_t ua[4] = {wa.x, wa.y, wa.z, wa.w}, ub[4] = {wb.x, wb.y, wb.z, wb.w};
@@ -337,10 +394,22 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
                             Bb = dp4a(ub[q], lb[j][q], Bb);
                             Cb = dp4a(ub[q], lc[j][q], Cb);
                         }
+                        if (GROUPED && 16 * c < K) {  // the chunk lies in group 16 c / G (G a multiple of 16)
+                            const int gi = (16 * c) / G;
+                            ga = fmaf(fmaf((float)Aa, 65536.0f, fmaf((float)Ba, 256.0f, (float)Ca)),
+                                      stile[(size_t)r * s_pitch + gi], ga);
+                            if (two)
+                                gb = fmaf(fmaf((float)Ab, 65536.0f, fmaf((float)Bb, 256.0f, (float)Cb)),
+                                          stile[(size_t)(r + 1) * s_pitch + gi], gb);
+                        }
                     }
                 }
-                float fa = __fmul_rn(__fmul_rn(fmaf((float)Aa, 65536.0f, fmaf((float)Ba, 256.0f, (float)Ca)), s1), s2);
-                float fb = __fmul_rn(__fmul_rn(fmaf((float)Ab, 65536.0f, fmaf((float)Bb, 256.0f, (float)Cb)), s1), s2);
+                if (!GROUPED) {
+                    ga = fmaf((float)Aa, 65536.0f, fmaf((float)Ba, 256.0f, (float)Ca));
+                    gb = fmaf((float)Ab, 65536.0f, fmaf((float)Bb, 256.0f, (float)Cb));
+                }
+                float fa = __fmul_rn(__fmul_rn(ga, s1), s2);
+                float fb = __fmul_rn(__fmul_rn(gb, s1), s2);
                 fa = __fadd_rn(fa, nanv);
                 fb = __fadd_rn(fb, nanv);
 #pragma unroll
@@ -369,7 +438,7 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
 
 template <int R, int MT>
 static qlin_status launch_w8(const float *x, const int8_t *w, int64_t pitch, float s, float *y, int M, int N, int K,
-                             cudaStream_t st) {
+                             cudaStream_t st, const float *scales = nullptr, int64_t s_pitch = 0, int G = 0) {
     auto kern = w8_gemv_kernel<R, MT>;
     const int C = (K + 15) / 16;
     const size_t smem = (size_t)MT * C * 16 * sizeof(float);
@@ -381,7 +450,7 @@ static qlin_status launch_w8(const float *x, const int8_t *w, int64_t pitch, flo
     const int64_t cap = (int64_t)sm_count() * per_sm;
     if (blocks > cap) blocks = cap;
     dim3 grid((unsigned)blocks, (unsigned)((M + MT - 1) / MT));
-    kern<<<grid, 256, smem, st>>>(x, w, pitch, s, y, M, N, K);
+    kern<<<grid, 256, smem, st>>>(x, w, pitch, s, y, M, N, K, scales, s_pitch, G);
     QLIN_LAUNCHED("w8_gemv_kernel");
     return QLIN_OK;
 }
@@ -425,7 +494,7 @@ qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float
     if (M == 1 && w_pitch <= 16 * 32 * qlin::kW8Warps * qlin::kW8JMax) {
         const qlin::W8Smem L = qlin::w8_stream_layout(w_pitch, qlin::max_smem_optin());
         if (L.tr >= 1) {
-            qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel, L.total);  // raises the dynamic smem limit
+            qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel<false>, L.total);  // raises the dynamic smem limit
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)qlin::sm_count());
             cfg.blockDim = dim3(32 * (qlin::kW8Warps + 1));
@@ -436,7 +505,8 @@ qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            QLIN_CUDA(cudaLaunchKernelEx(&cfg, qlin::w8_stream_kernel, x, w8, w_pitch, w_scale, y, N, K, L));
+            QLIN_CUDA(cudaLaunchKernelEx(&cfg, qlin::w8_stream_kernel<false>, x, w8, w_pitch, w_scale, y, N, K, L,
+                                         (const float *)nullptr, (int64_t)0, 0));
             QLIN_LAUNCHED("w8_stream_kernel");
             return QLIN_OK;
         }
@@ -445,6 +515,65 @@ qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float
     if (M <= 4 || (int)tile8_smem > qlin::max_smem_optin())
         return qlin::launch_w8<2, 4>(x, w8, w_pitch, w_scale, y, M, N, K, st);
     return qlin::launch_w8<2, 8>(x, w8, w_pitch, w_scale, y, M, N, K, st);
+}
+
+qlin_status qlin_w8g_quantize(const float *w, int64_t N, int64_t K, int G, int8_t *w8, int64_t w_pitch, float *scales,
+                              int64_t s_pitch, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(w && w8 && scales, QLIN_ERR_INVALID_ARG, "qlin_w8g_quantize: null pointer");
+    QLIN_REQUIRE(N >= 1 && K >= 1 && G >= 16 && G % 16 == 0 && w_pitch >= K && w_pitch % 16 == 0 &&
+                     s_pitch >= (K + G - 1) / G && s_pitch % 4 == 0,
+                 QLIN_ERR_INVALID_ARG, "qlin_w8g_quantize: N=%lld K=%lld G=%d w_pitch=%lld s_pitch=%lld", (long long)N,
+                 (long long)K, G, (long long)w_pitch, (long long)s_pitch);
+    QLIN_REQUIRE(qlin::aligned4(w) && qlin::aligned16(w8) && qlin::aligned16(scales), QLIN_ERR_INVALID_ARG,
+                 "qlin_w8g_quantize: misaligned pointer");
+    const int64_t warps = N * s_pitch;
+    const int64_t blocks = (warps * 32 + 255) / 256;
+    QLIN_REQUIRE(blocks < ((int64_t)1 << 31), QLIN_ERR_UNSUPPORTED, "qlin_w8g_quantize: too many groups");
+    qlin::w8g_quant_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(w, N, K, G, w8, w_pitch, scales,
+                                                                               s_pitch);
+    QLIN_LAUNCHED("w8g_quant_kernel");
+    return QLIN_OK;
+}
+
+qlin_status qlin_w8g_f32(const float *x, const int8_t *w8, int64_t w_pitch, const float *scales, int64_t s_pitch, int G,
+                         float *y, int M, int N, int K, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(x && w8 && scales && y, QLIN_ERR_INVALID_ARG, "qlin_w8g_f32: null pointer");
+    QLIN_REQUIRE(M >= 1 && N >= 1 && K >= 1, QLIN_ERR_INVALID_ARG, "qlin_w8g_f32: M=%d N=%d K=%d", M, N, K);
+    QLIN_REQUIRE(G >= 16 && G % 16 == 0 && w_pitch >= K && w_pitch % 16 == 0 && s_pitch >= (K + G - 1) / G &&
+                     s_pitch % 4 == 0,
+                 QLIN_ERR_INVALID_ARG, "qlin_w8g_f32: G=%d w_pitch=%lld s_pitch=%lld", G, (long long)w_pitch,
+                 (long long)s_pitch);
+    QLIN_REQUIRE(qlin::aligned16(w8) && qlin::aligned16(scales) && qlin::aligned4(x) && qlin::aligned4(y),
+                 QLIN_ERR_INVALID_ARG, "qlin_w8g_f32: misaligned pointer");
+    QLIN_REQUIRE(M <= 64, QLIN_ERR_UNSUPPORTED, "qlin_w8g_f32: M=%d > 64", M);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (M == 1 && w_pitch <= 16 * 32 * qlin::kW8Warps * qlin::kW8JMax) {
+        const qlin::W8Smem L = qlin::w8_stream_layout(w_pitch, qlin::max_smem_optin(), s_pitch);
+        if (L.tr >= 1) {
+            qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel<true>, L.total);  // raises the dynamic smem limit
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)qlin::sm_count());
+            cfg.blockDim = dim3(32 * (qlin::kW8Warps + 1));
+            cfg.dynamicSmemBytes = (size_t)L.total;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            QLIN_CUDA(cudaLaunchKernelEx(&cfg, qlin::w8_stream_kernel<true>, x, w8, w_pitch, 1.0f, y, N, K, L, scales,
+                                         s_pitch, G));
+            QLIN_LAUNCHED("w8_stream_kernel");
+            return QLIN_OK;
+        }
+    }
+    const size_t tile8_smem = (size_t)8 * ((K + 15) / 16) * 16 * sizeof(float);
+    if (M == 1) return qlin::launch_w8<4, 1>(x, w8, w_pitch, 1.0f, y, M, N, K, st, scales, s_pitch, G);
+    if (M <= 4 || (int)tile8_smem > qlin::max_smem_optin())
+        return qlin::launch_w8<2, 4>(x, w8, w_pitch, 1.0f, y, M, N, K, st, scales, s_pitch, G);
+    return qlin::launch_w8<2, 8>(x, w8, w_pitch, 1.0f, y, M, N, K, st, scales, s_pitch, G);
 }
 
 }  // extern "C"

@@ -57,6 +57,8 @@ SIGNATURES = {
     "qlin_quant_i8": ([_P, _P, _P, _I, _I, _P], _ST),
     "qlin_t158_i8": ([_P, _P, _P, _I64, _F, _P, _P, _I, _I, _I, _P], _ST),
     "qlin_w8_f32": ([_P, _P, _I64, _F, _P, _I, _I, _I, _P], _ST),
+    "qlin_w8g_quantize": ([_P, _I64, _I64, _I, _P, _I64, _P, _I64, _P], _ST),
+    "qlin_w8g_f32": ([_P, _P, _I64, _P, _I64, _I, _P, _I, _I, _I, _P], _ST),
     "qlin_embed_bf16": ([_P, _I, _I, _P, _P, _P, _P], _ST),
     "qlin_rmsnorm": ([_P, _P, _P, _I, _I, _F, _P], _ST),
     "t158_rope_table": ([_P, _P, _I, _I, _D, _P], _ST),
@@ -159,6 +161,16 @@ def qlin_t158_i8(xq, x_scale, w_packed, w_pitch, w_scale, y, acc, M, N, K, strea
 def qlin_w8_f32(x, w8, w_pitch, w_scale, y, M, N, K, stream=None):
     _check("qlin_w8_f32", lib().qlin_w8_f32(_ptr(x), _ptr(w8), w_pitch, float(w_scale), _ptr(y), M, N, K,
                                             _stream(stream)))
+
+
+def qlin_w8g_quantize(w, N, K, G, w8, w_pitch, scales, s_pitch, stream=None):
+    _check("qlin_w8g_quantize", lib().qlin_w8g_quantize(_ptr(w), N, K, G, _ptr(w8), w_pitch, _ptr(scales), s_pitch,
+                                                        _stream(stream)))
+
+
+def qlin_w8g_f32(x, w8, w_pitch, scales, s_pitch, G, y, M, N, K, stream=None):
+    _check("qlin_w8g_f32", lib().qlin_w8g_f32(_ptr(x), _ptr(w8), w_pitch, _ptr(scales), s_pitch, G, _ptr(y), M, N, K,
+                                              _stream(stream)))
 
 
 def qlin_embed_bf16(emb, vocab, dim, token, h, status_word=None, stream=None):
