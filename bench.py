@@ -252,6 +252,7 @@ def run_decode(args, rank, local, world):
     lm_gbs = lm_alg / (lm_ms / 1e3) / 1e9
     gemv = gemv_m1(dev, stream)
     prefill = prefill_m512(dev, stream)
+    lanes = lanes_t158(dev, stream)
     step_gbs = step_bytes * args.steps / (ms / 1e3) / 1e9
     traffic = fused_traffic()
     launches_per_step = qlin.decode_step_t158_launches(gpu.model)
@@ -286,6 +287,7 @@ def run_decode(args, rank, local, world):
         },
         "gemv_m1": gemv,
         "prefill_m512": prefill,
+        "lanes_t158": lanes,
         # the step is one launch of the fused kernel: its algorithmic bytes over
         # its CUDA-event time on the launching stream
         "roofline": {
@@ -448,6 +450,50 @@ def prefill_m512(dev, stream):
             "frac": round(tf / tflops_peak, 4), "int_ops": 2 * M * N * K,
             "timing": "median of 20 calls, each after an L2 flush"}
         del w, x, xq, xs, y
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def lanes_t158(dev, stream):
+    """Many tokens through one weight pass ([citric] "Many users at once"): the T158
+    layers of the decoder at M = 1..64 tokens, each call after an L2 flush; token-rows
+    per microsecond = M / time."""
+    import torch
+
+    import synth
+    from weight_streaming_gemv_gb300 import qlin
+
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    res = {}
+    for K, N in [(1152, 6912), (6912, 1152)]:
+        d = synth.t158_gemv(2, 64, K, N)
+        pitch = qlin.t158_pitch(K)
+        w = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+        x = torch.from_numpy(d["x"]).to(dev)
+        row = {"M": [], "us_per_call": [], "token_rows_per_us": []}
+        for M in [1, 2, 4, 8, 16, 32, 64]:
+            xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+            xs = torch.empty(M, dtype=torch.float32, device=dev)
+            qlin.qlin_quant_i8(x[:M].contiguous(), xq, xs, M, K)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            for _ in range(3):
+                qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, M, N, K)
+            times = []
+            for _ in range(15):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, M, N, K)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) * 1e3)
+            us = statistics.median(times)
+            row["M"].append(M)
+            row["us_per_call"].append(round(us, 2))
+            row["token_rows_per_us"].append(round(M / us, 3))
+        res[f"t158_k{K}_n{N}"] = row
+        del w, x
     del flush
     torch.cuda.empty_cache()
     return res

@@ -105,7 +105,7 @@ qlin_status qlin_quant_i8(const float *x, int8_t *xq, float *x_scale, int M, int
  * Bytes above 242 in w_packed give unspecified but memory-safe results.
  * M: 1..4096.  K: 1..131071 (so that |acc| stays below 2^24 and the fp32
  * epilogue is exact).  UNSUPPORTED outside these ranges.
- * From M = 64 tokens (prefill, [citric] "Step 4": all prompt tokens through
+ * From M = 8 tokens (prefill and batched decode, [citric] "Step 4": all prompt tokens through
  * each matrix in one pass) the products run on the tensor cores as an fp16
  * matrix product with fp32 accumulation, exact for these operands (int8
  * codes and trits are fp16 integers and every partial sum stays below

@@ -195,7 +195,7 @@ def test_t158_prefill_m512_full_size(dev, K, N):
 
 
 @pytest.mark.parametrize("M,K,N", [(64, 80, 128), (128, 80, 128), (100, 100, 200), (300, 1155, 130), (129, 161, 257),
-                                   (512, 6912, 100)])
+                                   (512, 6912, 100), (8, 1152, 6912), (16, 6912, 1152), (32, 1152, 300), (9, 77, 33)])
 def test_t158_tensor_core_tiles(dev, M, K, N):
     # the tensor-core path (M >= 64): ragged token, row and K tiles against the oracle, bit for bit
     _t158_case(dev, M, K, N, seed=11)

@@ -210,8 +210,10 @@ static qlin_status dispatch_mt(const int8_t *xq, const float *xs, const uint8_t 
     return launch_t158<LPR, 2, 16>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
 }
 
-// Tokens from which the tensor-core kernel (a 128-token tile) takes over.
-constexpr int kTensorCoreMinM = 64;
+// Tokens from which the tensor-core kernel (a 128-token tile) takes over: its
+// time hardly depends on M, and from about 8 tokens it beats the CUDA-core
+// kernel on the Gemma-3-1B shapes (1152 -> 6912 and 6912 -> 1152).
+constexpr int kTensorCoreMinM = 8;
 qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
                                      float *y, int32_t *acc, int M, int N, int K, cudaStream_t st);
 
