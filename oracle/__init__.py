@@ -76,6 +76,8 @@ def _L():
                 "or_rope_apply": ([p, i64, i64, p, p], None),
                 "or_attention": ([p, p, p, i64, i64, i64, i64, p], None),
                 "or_lm_head_argmax": ([p, p, i64, i64, p, p], None),
+                "or_sketch_ce": ([p, i64, i64, p], ctypes.c_int),
+                "or_sketch_head": ([p, i64, i64, p, i64, i64, i64, f32, p, p, p, p], ctypes.c_int),
                 "or_decode_step": ([ctypes.POINTER(OrModel), p, i32, i64, p, p], ctypes.c_int),
                 "or_decode_generate": ([ctypes.POINTER(OrModel), p, p, i64, i64, i64, p], ctypes.c_int),
             }
@@ -253,6 +255,38 @@ def lm_head_argmax(emb_bits: np.ndarray, x: np.ndarray):
     nxt = ctypes.c_int32()
     _L().or_lm_head_argmax(_p(e), _p(x), V, D, _p(logits), ctypes.byref(nxt))
     return nxt.value, logits
+
+
+# ------------------------------------------------------------------ sketch head
+def sketch_ce(emb_bits: np.ndarray) -> float:
+    """Mean |E| of a bf16 table (fp64 sum, rounded to fp32): the sketch's scale."""
+    e = np.ascontiguousarray(emb_bits, np.uint16)
+    V, D = e.shape
+    out = ctypes.c_float()
+    _check(_L().or_sketch_ce(_p(e), V, D, ctypes.byref(out)), "sketch_ce")
+    return out.value
+
+
+def sketch_head(emb_bits: np.ndarray, x: np.ndarray, k: int = 32, G: int = 8, n_cand: int = 1024,
+                cE: float | None = None):
+    """Candidates first, exact scores for them only.
+
+    Returns ``(next, cand, cand_logits, approx)``: the chosen word, the n_cand
+    candidate words in ascending order, their exact logits (fp64 dot rounded
+    to fp32) and every word's approximate score.
+    """
+    e = np.ascontiguousarray(emb_bits, np.uint16)
+    x = np.ascontiguousarray(x, np.float32).reshape(-1)
+    V, D = e.shape
+    if cE is None:
+        cE = sketch_ce(e)
+    approx = np.empty(V, np.float32)
+    cand = np.empty(n_cand, np.int32)
+    cl = np.empty(n_cand, np.float32)
+    nxt = ctypes.c_int32()
+    _check(_L().or_sketch_head(_p(e), V, D, _p(x), k, G, n_cand, cE, _p(approx), _p(cand), _p(cl),
+                               ctypes.byref(nxt)), "sketch_head")
+    return nxt.value, cand, cl, approx
 
 
 # ------------------------------------------------------------------ decode step

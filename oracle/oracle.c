@@ -15,7 +15,8 @@
  *                     "matmul", "Sampling", "The generation loop".
  *   [citric]          "Gemma 3 1B at 114 tokens per second on a laptop CPU" --
  *                     "On a CPU, speed is bytes", "Step 1: a kernel for 1.6-bit
- *                     weights", "Step 2: making a ternary Gemma".
+ *                     weights", "Step 2: making a ternary Gemma", "Step 3: the
+ *                     output layer became the bottleneck".
  *
  * Precision: integer work is exact (int64 accumulators).  Plain linear maps
  * with no quantiser downstream (W8 linear, lm_head logits) accumulate in
@@ -449,6 +450,139 @@ static void t158_layer(const or_model *m, int l, int j, const float *x, int8_t *
     or_quant_i8(x, 1, K, xq, &xs);
     const uint8_t *w = m->w[j] + (int64_t)l * N * m->pitch[j];
     or_t158_linear(xq, &xs, w, m->pitch[j], m->scales[l * 7 + j], 1, N, K, NULL, y);
+}
+
+/* ------------------------------------------------------------------ sketch head
+ * [citric] "Step 3: the output layer became the bottleneck": candidates first,
+ * exact scores only for them.  (1) the k dimensions of x with the largest
+ * values are scored exactly for every word; (2) the other dimensions are
+ * scored from the signs of the table only, grouped by size with a weight per
+ * group; (3) the n_cand words with the best approximate scores are scored
+ * exactly, every other word scores minus infinity.
+ * Readings (the page gives the steps, not their arithmetic):
+ * - "largest values" = largest |x_d|, ties to the lower index;
+ * - the other D - k dimensions, ranked by |x_d| (ties to the lower index),
+ *   form G groups of consecutive ranks (group g: ranks [g R / G, (g+1) R / G),
+ *   R = D - k); group g's weight w_g = (mean of |x_d| over the group) * cE,
+ *   cE = the mean |E| of the table, so that w_g * (agreeing signs - disagreeing
+ *   signs) estimates the group's part of the dot product;
+ * - the sign of E is the sign bit of its bf16 value, the sign of x its sign bit;
+ * - ties among approximate scores go to the lower index.
+ * The fp32 arithmetic is fixed so that two implementations select the same
+ * candidates: the exact part is the pairwise sum (zero-padded to a power of
+ * two) of the products bf16(E[v][d]) * x[d], d ascending over the k dims; a
+ * group mean is the pairwise sum of |x_d| (d ascending) divided by the group
+ * size, times cE; the sketch is sum over g ascending of w_g * (n_g - 2 m_g),
+ * each product rounded, then added; approx = exact part + sketch.
+ */
+typedef struct {
+    float key;
+    int64_t idx;
+} or_keyidx;
+
+static int or_cmp_desc(const void *a, const void *b) {
+    const or_keyidx *p = (const or_keyidx *)a, *q = (const or_keyidx *)b;
+    if (p->key > q->key) return -1;
+    if (p->key < q->key) return 1;
+    return p->idx < q->idx ? -1 : p->idx > q->idx ? 1 : 0;
+}
+
+static int or_cmp_i64(const void *a, const void *b) {
+    const int64_t p = *(const int64_t *)a, q = *(const int64_t *)b;
+    return p < q ? -1 : p > q ? 1 : 0;
+}
+
+int or_sketch_ce(const uint16_t *emb, int64_t V, int64_t D, float *cE) {
+    if (!emb || !cE || V < 1 || D < 1) return OR_EINVAL;
+    double acc = 0.0;
+    for (int64_t i = 0; i < V * D; i++) acc += fabs((double)bf16f(emb[i]));
+    *cE = (float)(acc / (double)(V * D));
+    return OR_OK;
+}
+
+int or_sketch_head(const uint16_t *emb, int64_t V, int64_t D, const float *x, int64_t k, int64_t G, int64_t n_cand,
+                   float cE, float *approx, int32_t *cand, float *cand_logits, int32_t *next) {
+    if (!emb || !x || !approx || !cand || !cand_logits || !next || V < 1 || D < 1 || k < 0 || k > D || G < 1 ||
+        n_cand < 1 || n_cand > V)
+        return OR_EINVAL;
+    const int64_t R = D - k;
+    if (R > 0 && G > R) return OR_EINVAL;
+    or_keyidx *ord = (or_keyidx *)malloc((size_t)D * sizeof(or_keyidx));
+    for (int64_t d = 0; d < D; d++) {
+        ord[d].key = fabsf(x[d]);
+        ord[d].idx = d;
+    }
+    qsort(ord, (size_t)D, sizeof(or_keyidx), or_cmp_desc);
+    int64_t *top = (int64_t *)malloc((size_t)(k > 0 ? k : 1) * sizeof(int64_t));
+    for (int64_t j = 0; j < k; j++) top[j] = ord[j].idx;
+    qsort(top, (size_t)k, sizeof(int64_t), or_cmp_i64);
+    /* groups: dims (ascending) and weights */
+    int64_t *gdims = (int64_t *)malloc((size_t)(R > 0 ? R : 1) * sizeof(int64_t));
+    int64_t *gstart = (int64_t *)malloc((size_t)(G + 1) * sizeof(int64_t));
+    float *wg = (float *)malloc((size_t)G * sizeof(float));
+    float *tmp = (float *)malloc((size_t)(D + 1) * sizeof(float));
+    for (int64_t g = 0; g <= G; g++) gstart[g] = R > 0 ? g * R / G : 0;
+    for (int64_t g = 0; g < G; g++) {
+        const int64_t a = gstart[g], b = gstart[g + 1];
+        for (int64_t r = a; r < b; r++) gdims[r] = ord[k + r].idx;
+        qsort(gdims + a, (size_t)(b - a), sizeof(int64_t), or_cmp_i64);
+        for (int64_t r = a; r < b; r++) tmp[r - a] = fabsf(x[gdims[r]]);
+        wg[g] = b > a ? (or_psum_f32(tmp, b - a) / (float)(b - a)) * cE : 0.0f;
+    }
+#pragma omp parallel
+    {
+        float *prod = (float *)malloc((size_t)(k > 0 ? k : 1) * sizeof(float));
+#pragma omp for schedule(static)
+        for (int64_t v = 0; v < V; v++) {
+            const uint16_t *e = emb + v * D;
+            for (int64_t j = 0; j < k; j++) prod[j] = bf16f(e[top[j]]) * x[top[j]];
+            const float exact = k > 0 ? or_psum_f32(prod, k) : 0.0f;
+            float sk = 0.0f;
+            for (int64_t g = 0; g < G; g++) {
+                int64_t mism = 0;
+                for (int64_t r = gstart[g]; r < gstart[g + 1]; r++) {
+                    const int64_t d = gdims[r];
+                    mism += (int64_t)((e[d] >> 15) != (uint16_t)(signbit(x[d]) ? 1 : 0));
+                }
+                const float t = (float)(gstart[g + 1] - gstart[g] - 2 * mism);
+                sk = sk + wg[g] * t;
+            }
+            approx[v] = exact + sk;
+        }
+        free(prod);
+    }
+    or_keyidx *all = (or_keyidx *)malloc((size_t)V * sizeof(or_keyidx));
+    for (int64_t v = 0; v < V; v++) {
+        all[v].key = approx[v];
+        all[v].idx = v;
+    }
+    qsort(all, (size_t)V, sizeof(or_keyidx), or_cmp_desc);
+    int64_t *cv = (int64_t *)malloc((size_t)n_cand * sizeof(int64_t));
+    for (int64_t i = 0; i < n_cand; i++) cv[i] = all[i].idx;
+    qsort(cv, (size_t)n_cand, sizeof(int64_t), or_cmp_i64);
+    int32_t best = -1;
+    float bv = 0.0f;
+    for (int64_t i = 0; i < n_cand; i++) {
+        const uint16_t *e = emb + cv[i] * D;
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; d++) acc += (double)bf16f(e[d]) * (double)x[d];
+        cand[i] = (int32_t)cv[i];
+        cand_logits[i] = (float)acc;
+        if (best < 0 || cand_logits[i] > bv) {
+            best = (int32_t)cv[i];
+            bv = cand_logits[i];
+        }
+    }
+    *next = best;
+    free(ord);
+    free(top);
+    free(gdims);
+    free(gstart);
+    free(wg);
+    free(tmp);
+    free(all);
+    free(cv);
+    return OR_OK;
 }
 
 /* S16: logits[r] = sum_i bf16(emb[r][i]) * x[i] in fp64, rounded to fp32

@@ -118,6 +118,15 @@ def t158_gemv(seed: int, M: int, K: int, N: int):
     }
 
 
+def sketch_head(seed: int, V: int, D: int):
+    """Output-layer inputs: bf16 table ~N(0, 0.02) [V][D] and a final hidden state whose
+    dimensions have uneven sizes, x_d = N(0,1) * U(0.5, 2)."""
+    return {
+        "emb": normal_bf16(seed, 1, (V, D), 0.0, 0.02),
+        "x": (normal_f32(seed, 2, (D,), 0.0, 1.0) * uniform_f32(seed, 3, (D,), 0.5, 2.0)).astype(np.float32),
+    }
+
+
 class DecoderConfig:
     """Shape of a Gemma-3-1B-like ternary decoder."""
 
