@@ -77,7 +77,8 @@ def _L():
                 "or_attention": ([p, p, p, i64, i64, i64, i64, p], None),
                 "or_lm_head_argmax": ([p, p, i64, i64, p, p], None),
                 "or_sketch_ce": ([p, i64, i64, p], ctypes.c_int),
-                "or_sketch_head": ([p, i64, i64, p, i64, i64, i64, f32, p, p, p, p], ctypes.c_int),
+                "or_sketch_perm": ([p, i64, p], ctypes.c_int),
+                "or_sketch_head": ([p, i64, i64, p, i64, p, i64, i64, f32, p, p, p, p], ctypes.c_int),
                 "or_decode_step": ([ctypes.POINTER(OrModel), p, i32, i64, p, p], ctypes.c_int),
                 "or_decode_generate": ([ctypes.POINTER(OrModel), p, p, i64, i64, i64, p], ctypes.c_int),
             }
@@ -267,24 +268,39 @@ def sketch_ce(emb_bits: np.ndarray) -> float:
     return out.value
 
 
-def sketch_head(emb_bits: np.ndarray, x: np.ndarray, k: int = 32, G: int = 8, n_cand: int = 1024,
+def sketch_perm(scale, D: int | None = None) -> np.ndarray:
+    """Dimensions by size: largest |scale| first, ties to the lower index (identity if scale is None)."""
+    if scale is None:
+        sc, D = None, int(D)
+    else:
+        sc = np.ascontiguousarray(scale, np.float32).reshape(-1)
+        D = sc.size
+    perm = np.empty(D, np.int64)
+    _check(_L().or_sketch_perm(None if sc is None else _p(sc), D, _p(perm)), "sketch_perm")
+    return perm
+
+
+def sketch_head(emb_bits: np.ndarray, x: np.ndarray, perm=None, B: int = 64, k: int = 32, n_cand: int = 1024,
                 cE: float | None = None):
     """Candidates first, exact scores for them only.
 
-    Returns ``(next, cand, cand_logits, approx)``: the chosen word, the n_cand
-    candidate words in ascending order, their exact logits (fp64 dot rounded
-    to fp32) and every word's approximate score.
+    perm: the dimension order of the sign blocks (``sketch_perm``; identity if
+    None); B: dimensions per block.  Returns ``(next, cand, cand_logits,
+    approx)``: the chosen word, the n_cand candidate words in ascending order,
+    their exact logits (fp64 dot rounded to fp32) and every word's approximate
+    score.
     """
     e = np.ascontiguousarray(emb_bits, np.uint16)
     x = np.ascontiguousarray(x, np.float32).reshape(-1)
     V, D = e.shape
+    perm = np.arange(D, dtype=np.int64) if perm is None else np.ascontiguousarray(perm, np.int64)
     if cE is None:
         cE = sketch_ce(e)
     approx = np.empty(V, np.float32)
     cand = np.empty(n_cand, np.int32)
     cl = np.empty(n_cand, np.float32)
     nxt = ctypes.c_int32()
-    _check(_L().or_sketch_head(_p(e), V, D, _p(x), k, G, n_cand, cE, _p(approx), _p(cand), _p(cl),
+    _check(_L().or_sketch_head(_p(e), V, D, _p(perm), B, _p(x), k, n_cand, cE, _p(approx), _p(cand), _p(cl),
                                ctypes.byref(nxt)), "sketch_head")
     return nxt.value, cand, cl, approx
 

@@ -456,24 +456,31 @@ static void t158_layer(const or_model *m, int l, int j, const float *x, int8_t *
  * [citric] "Step 3: the output layer became the bottleneck": candidates first,
  * exact scores only for them.  (1) the k dimensions of x with the largest
  * values are scored exactly for every word; (2) the other dimensions are
- * scored from the signs of the table only, grouped by size with a weight per
- * group; (3) the n_cand words with the best approximate scores are scored
+ * scored from the signs of the table only -- one XOR and one bit count per 64
+ * dimensions of a word -- with the dimensions grouped by size and one weight
+ * per group; (3) the n_cand words with the best approximate scores are scored
  * exactly, every other word scores minus infinity.
  * Readings (the page gives the steps, not their arithmetic):
  * - "largest values" = largest |x_d|, ties to the lower index;
- * - the other D - k dimensions, ranked by |x_d| (ties to the lower index),
- *   form G groups of consecutive ranks (group g: ranks [g R / G, (g+1) R / G),
- *   R = D - k); group g's weight w_g = (mean of |x_d| over the group) * cE,
- *   cE = the mean |E| of the table, so that w_g * (agreeing signs - disagreeing
- *   signs) estimates the group's part of the dot product;
+ * - a group is one B-dimension block of the stored sign table (B = 64 on the
+ *   page: one XOR and one bit count per block), so grouping by size is a fixed
+ *   order of the dimensions chosen when the table is prepared: perm lists the
+ *   dimensions by a per-dimension size s_d (largest |s_d| first, ties to the
+ *   lower index; the identity without sizes), block b holds positions
+ *   bB .. bB+B-1 of that order;
+ * - block b's weight is w_b = (mean |x_d| over its sketched dims) * cE, cE =
+ *   the mean |E| of the table, so that w_b * (agreeing - differing signs)
+ *   estimates the block's part of the dot product; the exact dims are left
+ *   out of every block;
  * - the sign of E is the sign bit of its bf16 value, the sign of x its sign bit;
  * - ties among approximate scores go to the lower index.
  * The fp32 arithmetic is fixed so that two implementations select the same
  * candidates: the exact part is the pairwise sum (zero-padded to a power of
  * two) of the products bf16(E[v][d]) * x[d], d ascending over the k dims; a
- * group mean is the pairwise sum of |x_d| (d ascending) divided by the group
- * size, times cE; the sketch is sum over g ascending of w_g * (n_g - 2 m_g),
- * each product rounded, then added; approx = exact part + sketch.
+ * block's |x| sum is the pairwise sum over its B positions in order, exact
+ * dims and positions past D counting +0; the sketch is the sum over blocks in
+ * order of w_b * (n_b - 2 m_b), each product rounded, then added; approx =
+ * exact part + sketch.
  */
 typedef struct {
     float key;
@@ -492,6 +499,19 @@ static int or_cmp_i64(const void *a, const void *b) {
     return p < q ? -1 : p > q ? 1 : 0;
 }
 
+int or_sketch_perm(const float *scale, int64_t D, int64_t *perm) {
+    if (!perm || D < 1) return OR_EINVAL;
+    or_keyidx *ord = (or_keyidx *)malloc((size_t)D * sizeof(or_keyidx));
+    for (int64_t d = 0; d < D; d++) {
+        ord[d].key = scale ? fabsf(scale[d]) : 0.0f;
+        ord[d].idx = d;
+    }
+    qsort(ord, (size_t)D, sizeof(or_keyidx), or_cmp_desc);
+    for (int64_t i = 0; i < D; i++) perm[i] = ord[i].idx;
+    free(ord);
+    return OR_OK;
+}
+
 int or_sketch_ce(const uint16_t *emb, int64_t V, int64_t D, float *cE) {
     if (!emb || !cE || V < 1 || D < 1) return OR_EINVAL;
     double acc = 0.0;
@@ -500,34 +520,49 @@ int or_sketch_ce(const uint16_t *emb, int64_t V, int64_t D, float *cE) {
     return OR_OK;
 }
 
-int or_sketch_head(const uint16_t *emb, int64_t V, int64_t D, const float *x, int64_t k, int64_t G, int64_t n_cand,
-                   float cE, float *approx, int32_t *cand, float *cand_logits, int32_t *next) {
-    if (!emb || !x || !approx || !cand || !cand_logits || !next || V < 1 || D < 1 || k < 0 || k > D || G < 1 ||
-        n_cand < 1 || n_cand > V)
+int or_sketch_head(const uint16_t *emb, int64_t V, int64_t D, const int64_t *perm, int64_t B, const float *x,
+                   int64_t k, int64_t n_cand, float cE, float *approx, int32_t *cand, float *cand_logits,
+                   int32_t *next) {
+    if (!emb || !perm || !x || !approx || !cand || !cand_logits || !next || V < 1 || D < 1 || B < 1 || k < 0 ||
+        k > D || n_cand < 1 || n_cand > V)
         return OR_EINVAL;
-    const int64_t R = D - k;
-    if (R > 0 && G > R) return OR_EINVAL;
+    char *seen = (char *)calloc((size_t)D, 1);
+    for (int64_t i = 0; i < D; i++) {
+        if (perm[i] < 0 || perm[i] >= D || seen[perm[i]]) {
+            free(seen);
+            return OR_EINVAL;
+        }
+        seen[perm[i]] = 1;
+    }
+    free(seen);
+    /* (1) the exact dims */
     or_keyidx *ord = (or_keyidx *)malloc((size_t)D * sizeof(or_keyidx));
     for (int64_t d = 0; d < D; d++) {
         ord[d].key = fabsf(x[d]);
         ord[d].idx = d;
     }
     qsort(ord, (size_t)D, sizeof(or_keyidx), or_cmp_desc);
+    char *exact_dim = (char *)calloc((size_t)D, 1);
     int64_t *top = (int64_t *)malloc((size_t)(k > 0 ? k : 1) * sizeof(int64_t));
-    for (int64_t j = 0; j < k; j++) top[j] = ord[j].idx;
+    for (int64_t j = 0; j < k; j++) {
+        top[j] = ord[j].idx;
+        exact_dim[top[j]] = 1;
+    }
     qsort(top, (size_t)k, sizeof(int64_t), or_cmp_i64);
-    /* groups: dims (ascending) and weights */
-    int64_t *gdims = (int64_t *)malloc((size_t)(R > 0 ? R : 1) * sizeof(int64_t));
-    int64_t *gstart = (int64_t *)malloc((size_t)(G + 1) * sizeof(int64_t));
+    /* (2) the blocks: sketched dims, counts and weights */
+    const int64_t G = (D + B - 1) / B;
     float *wg = (float *)malloc((size_t)G * sizeof(float));
-    float *tmp = (float *)malloc((size_t)(D + 1) * sizeof(float));
-    for (int64_t g = 0; g <= G; g++) gstart[g] = R > 0 ? g * R / G : 0;
+    int64_t *ng = (int64_t *)malloc((size_t)G * sizeof(int64_t));
+    float *tmp = (float *)malloc((size_t)B * sizeof(float));
     for (int64_t g = 0; g < G; g++) {
-        const int64_t a = gstart[g], b = gstart[g + 1];
-        for (int64_t r = a; r < b; r++) gdims[r] = ord[k + r].idx;
-        qsort(gdims + a, (size_t)(b - a), sizeof(int64_t), or_cmp_i64);
-        for (int64_t r = a; r < b; r++) tmp[r - a] = fabsf(x[gdims[r]]);
-        wg[g] = b > a ? (or_psum_f32(tmp, b - a) / (float)(b - a)) * cE : 0.0f;
+        ng[g] = 0;
+        for (int64_t p = 0; p < B; p++) {
+            const int64_t i = g * B + p;
+            const int in = i < D && !exact_dim[perm[i]];
+            tmp[p] = in ? fabsf(x[perm[i]]) : 0.0f;
+            ng[g] += in;
+        }
+        wg[g] = ng[g] > 0 ? (or_psum_f32(tmp, B) / (float)ng[g]) * cE : 0.0f;
     }
 #pragma omp parallel
     {
@@ -540,17 +575,19 @@ int or_sketch_head(const uint16_t *emb, int64_t V, int64_t D, const float *x, in
             float sk = 0.0f;
             for (int64_t g = 0; g < G; g++) {
                 int64_t mism = 0;
-                for (int64_t r = gstart[g]; r < gstart[g + 1]; r++) {
-                    const int64_t d = gdims[r];
+                for (int64_t p = 0; p < B && g * B + p < D; p++) {
+                    const int64_t d = perm[g * B + p];
+                    if (exact_dim[d]) continue;
                     mism += (int64_t)((e[d] >> 15) != (uint16_t)(signbit(x[d]) ? 1 : 0));
                 }
-                const float t = (float)(gstart[g + 1] - gstart[g] - 2 * mism);
+                const float t = (float)(ng[g] - 2 * mism);
                 sk = sk + wg[g] * t;
             }
             approx[v] = exact + sk;
         }
         free(prod);
     }
+    /* (3) candidates and their exact scores */
     or_keyidx *all = (or_keyidx *)malloc((size_t)V * sizeof(or_keyidx));
     for (int64_t v = 0; v < V; v++) {
         all[v].key = approx[v];
@@ -575,10 +612,10 @@ int or_sketch_head(const uint16_t *emb, int64_t V, int64_t D, const float *x, in
     }
     *next = best;
     free(ord);
+    free(exact_dim);
     free(top);
-    free(gdims);
-    free(gstart);
     free(wg);
+    free(ng);
     free(tmp);
     free(all);
     free(cv);

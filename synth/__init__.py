@@ -119,12 +119,18 @@ def t158_gemv(seed: int, M: int, K: int, N: int):
 
 
 def sketch_head(seed: int, V: int, D: int):
-    """Output-layer inputs: bf16 table ~N(0, 0.02) [V][D] and a final hidden state whose
-    dimensions have uneven sizes, x_d = N(0,1) * U(0.5, 2)."""
+    """Output-layer inputs: bf16 table ~N(0, 0.02) [V][D] and a per-dimension size
+    s_d ~ U(0.5, 2) (the fixed scale of each hidden dimension, as a final norm
+    gain gives it); hidden states come from ``sketch_x``."""
     return {
         "emb": normal_bf16(seed, 1, (V, D), 0.0, 0.02),
-        "x": (normal_f32(seed, 2, (D,), 0.0, 1.0) * uniform_f32(seed, 3, (D,), 0.5, 2.0)).astype(np.float32),
+        "scale": uniform_f32(seed, 3, (D,), 0.5, 2.0),
     }
+
+
+def sketch_x(seed: int, token: int, scale: np.ndarray) -> np.ndarray:
+    """A final hidden state: x_d = N(0,1) * s_d, one draw per token."""
+    return (normal_f32(seed, 100 + token, (scale.size,), 0.0, 1.0) * scale).astype(np.float32)
 
 
 class DecoderConfig:
