@@ -243,6 +243,53 @@ size_t qlin_lm_head_workspace_size(int vocab);
 qlin_status qlin_lm_head_argmax(const uint16_t *emb, const float *x, int vocab, int dim, float *logits,
                                 int32_t *next, void *workspace, size_t workspace_bytes, qlin_stream_t stream);
 
+/* Sketch head: candidates first, exact scores for them only ([citric] "Step 3:
+ * the output layer became the bottleneck").  For the final hidden state x:
+ *   1. the k dims with the largest |x_d| (ties: lower d) are scored exactly,
+ *      exact[v] = pairwise fp32 sum over them, ascending d, of bf16(E[v][d])*x_d;
+ *   2. the other dims are scored from the sign bits of the table, one 64-bit
+ *      XOR and bit count per block of 64 dims: block b holds positions
+ *      64b .. 64b+63 of the size order perm (fixed at preparation) minus the
+ *      exact dims; n_b = its sketched dims, m_b[v] = how many of their sign
+ *      bits differ between E[v] and x, w_b = (pairwise fp32 sum of |x| over
+ *      the block's 64 positions, exact dims and positions past dim counting
+ *      +0) / n_b * c_E; sketch[v] = sum over b in order (each product rounded)
+ *      of w_b * (n_b - 2 m_b[v]); approx[v] = exact[v] + sketch[v];
+ *   3. the n_cand words with the largest approx (ties: lower index) are the
+ *      candidates, in ascending order in cand[]; cand_logits[i] = their exact
+ *      logits with the lm_head's arithmetic (qlin_lm_head_argmax); every other
+ *      word scores minus infinity; *next = the first maximum among them.
+ * qlin_sketch_prepare makes, once per table (device memory, caller-owned):
+ *   perm   int32 [dim]: the dims by size, largest |dim_scale[d]| first, ties
+ *          to the lower index (dim_scale: device fp32 [dim], finite, or NULL
+ *          for the identity order; the final norm gain of a decoder);
+ *   emb_t  bf16 [dim][qlin_sketch_emb_t_pitch(vocab)]: the table by dimension,
+ *          zeros past vocab;
+ *   signs  qlin_sketch_signs_bytes(vocab, dim) bytes: uint64
+ *          [ceil(dim/64)][qlin_sketch_emb_t_pitch(vocab)], bit p of [b][v] =
+ *          sign bit of E[v][perm[64b + p]], zero past dim or vocab;
+ *   c_e    device float: the mean |E| over the table (fp64 sum, rounded once).
+ * qlin_sketch_prepare uses a static device buffer for the c_E partial sums:
+ * calls must not overlap.  Limits: 8 <= dim <= 2048, dim % 8 == 0, 0 <= k <=
+ * min(32, dim), 1 <= n_cand <= vocab; emb, emb_t, signs, x and workspace
+ * 16-byte aligned.  approx (device fp32 [vocab]) may be NULL.  x must be
+ * finite.  The workspace (qlin_sketch_workspace_size bytes) must be
+ * zero-filled before its first use; calls leave it ready for the next; calls
+ * sharing it must not overlap.  The kernel is one cooperative launch whose
+ * grid barriers wait at most 2 s; qlin_sketch_head_status() (which
+ * synchronises `stream`) returns QLIN_ERR_TIMEOUT if one gave up, after which
+ * the workspace must be zero-filled again. */
+int64_t qlin_sketch_emb_t_pitch(int vocab);
+size_t qlin_sketch_signs_bytes(int vocab, int dim);
+qlin_status qlin_sketch_prepare(const uint16_t *emb, int vocab, int dim, const float *dim_scale, uint16_t *emb_t,
+                                uint64_t *signs, int32_t *perm, float *c_e, qlin_stream_t stream);
+size_t qlin_sketch_workspace_size(int vocab);
+qlin_status qlin_sketch_head(const uint16_t *emb, const uint16_t *emb_t, const uint64_t *signs, const int32_t *perm,
+                             const float *c_e, int vocab, int dim, const float *x, int k, int n_cand, float *approx,
+                             int32_t *cand, float *cand_logits, int32_t *next, void *workspace,
+                             size_t workspace_bytes, qlin_stream_t stream);
+qlin_status qlin_sketch_head_status(void *workspace, qlin_stream_t stream);
+
 /* ========================================================================
  * S8-S16 composed: one decode step of a ternary Gemma-style decoder
  * ([cpp20gemma] "Architecture & implementation": h += attn(rmsnorm(h));

@@ -93,6 +93,21 @@ def test_device_calls_validate_before_launch():
     assert L.qlin_quant_i8(None, 16, 16, 1, 1, None) == 1
     assert L.qlin_attention_decode(16, 16, 16, 0, 4, 1, 24, 16, 16, 1 << 20, None) == 2  # head_dim not pow2
     assert "head_dim" in qlin.lib().qlin_last_error().decode()
+    # sketch head: emb, emb_t, signs, perm, c_e, vocab, dim, x, k, n_cand, approx, cand, logits, next, ws, bytes
+    ok = (16, 32, 48, 64, 80, 1000, 128, 96, 32, 100, None, 112, 128, 144, 160, 1 << 20, None)
+    def sk(**kw):
+        names = ("emb", "emb_t", "signs", "perm", "c_e", "V", "D", "x", "k", "n", "approx", "cand", "cl", "nx",
+                 "ws", "wsb", "st")
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return L.qlin_sketch_head(*[a[n] for n in names])
+    assert sk(k=33) == 1 and sk(k=-1) == 1 and sk(n=0) == 1 and sk(n=1001) == 1
+    assert sk(D=132) == 1 and sk(D=4096) == 1 and sk(emb=8) == 1 and sk(x=None) == 1 and sk(perm=None) == 1
+    assert sk(D=16, k=20) == 1
+    assert "k = 20" in qlin.lib().qlin_last_error().decode()
+    assert L.qlin_sketch_prepare(16, 1000, 12, None, 32, 48, 64, 80, None) == 1  # dim % 8
+    assert L.qlin_sketch_signs_bytes(1000, 1152) == 18 * 1000 * 8
+    assert L.qlin_sketch_emb_t_pitch(1001) == 1008
     m = qlin.T158ModelC()
     import ctypes
     n = ctypes.c_size_t()

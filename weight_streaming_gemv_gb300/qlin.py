@@ -69,6 +69,12 @@ SIGNATURES = {
     "qlin_geglu": ([_P, _P, _P, _I, _P], _ST),
     "qlin_lm_head_workspace_size": ([_I], _SZ),
     "qlin_lm_head_argmax": ([_P, _P, _I, _I, _P, _P, _P, _SZ, _P], _ST),
+    "qlin_sketch_emb_t_pitch": ([_I], ctypes.c_int64),
+    "qlin_sketch_signs_bytes": ([_I, _I], _SZ),
+    "qlin_sketch_prepare": ([_P, _I, _I, _P, _P, _P, _P, _P, _P], _ST),
+    "qlin_sketch_workspace_size": ([_I], _SZ),
+    "qlin_sketch_head": ([_P, _P, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _SZ, _P], _ST),
+    "qlin_sketch_head_status": ([_P, _P], _ST),
     "decode_step_t158_workspace_size": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(_SZ)], _ST),
     "decode_step_t158": ([ctypes.POINTER(T158ModelC), _P, _P, _SZ, _P, ctypes.c_int32, _P, _P, _P], _ST),
     "decode_step_t158_launches": ([ctypes.POINTER(T158ModelC)], _I),
@@ -228,6 +234,34 @@ def qlin_lm_head_argmax(emb, x, vocab, dim, logits, next_token, workspace, works
     _check("qlin_lm_head_argmax", lib().qlin_lm_head_argmax(_ptr(emb), _ptr(x), vocab, dim, _ptr(logits),
                                                             _ptr(next_token), _ptr(workspace), workspace_bytes,
                                                             _stream(stream)))
+
+
+def qlin_sketch_emb_t_pitch(vocab) -> int:
+    return int(lib().qlin_sketch_emb_t_pitch(vocab))
+
+
+def qlin_sketch_signs_bytes(vocab, dim) -> int:
+    return int(lib().qlin_sketch_signs_bytes(vocab, dim))
+
+
+def qlin_sketch_prepare(emb, vocab, dim, dim_scale, emb_t, signs, perm, c_e, stream=None):
+    _check("qlin_sketch_prepare", lib().qlin_sketch_prepare(_ptr(emb), vocab, dim, _ptr(dim_scale), _ptr(emb_t),
+                                                            _ptr(signs), _ptr(perm), _ptr(c_e), _stream(stream)))
+
+
+def qlin_sketch_workspace_size(vocab) -> int:
+    return int(lib().qlin_sketch_workspace_size(vocab))
+
+
+def qlin_sketch_head(emb, emb_t, signs, perm, c_e, vocab, dim, x, k, n_cand, approx, cand, cand_logits,
+                     next_token, workspace, workspace_bytes, stream=None):
+    _check("qlin_sketch_head", lib().qlin_sketch_head(
+        _ptr(emb), _ptr(emb_t), _ptr(signs), _ptr(perm), _ptr(c_e), vocab, dim, _ptr(x), k, n_cand, _ptr(approx),
+        _ptr(cand), _ptr(cand_logits), _ptr(next_token), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def qlin_sketch_head_status(workspace, stream=None):
+    _check("qlin_sketch_head_status", lib().qlin_sketch_head_status(_ptr(workspace), _stream(stream)))
 
 
 def decode_step_t158_workspace_size(model: T158ModelC) -> int:
