@@ -54,7 +54,7 @@ namespace {
 constexpr int kSkConsumerWarps = 16;
 constexpr int kSkWarps = kSkConsumerWarps + 1;  // + the producer warp
 constexpr int kSkThreads = 32 * kSkWarps;
-constexpr int kSkStages = 3;
+constexpr int kSkStages = 4;  // consumer groups divide it (see the scoring loop)
 constexpr int kSkRingBudget = 180 * 1024;  // bytes of shared memory for the stages
 constexpr int kSkMaxDim = 2048;
 constexpr int kSkMaxK = 32;
@@ -64,7 +64,8 @@ constexpr int kSkBins1 = 4096;  // key bits 31..20
 constexpr int kSkBins2 = 1024;  // key bits 19..10
 constexpr int kSkBins3 = 1024;  // key bits 9..0
 constexpr int kSkHistWords = kSkBins1 + kSkBins2 + kSkBins3;
-constexpr int kSkTile = 32;        // words per warp pass (one per lane)
+constexpr int kSkTile = 32;        // words per range unit
+constexpr int kSkSub = 64;         // words per warp pass (two per lane)
 constexpr int kSkCap = 4096;       // superset words one CTA resolves
 constexpr int kSkMemberCap = kSkThreads;  // dims of the boundary magnitude bin ranked pairwise
 
@@ -74,6 +75,7 @@ struct SketchWs {
     unsigned *bar;     // [2]: arrivals (zero between calls), generation
     unsigned *ticket;  // CTAs done (zero between calls)
     unsigned *tcount;  // superset words written (zero between calls)
+    unsigned *info;    // [4] the boundary bin, words above it, superset size (written each call)
     unsigned *hist;    // [kSkHistWords] (zero between calls)
     uint2 *counts;     // [blocks] words above / equal to the threshold per CTA
     float2 *part;      // [blocks] best (logit, index) per CTA
@@ -99,6 +101,7 @@ SketchWs carve(char *base, size_t *bytes) {
     w.bar = (unsigned *)take(8);
     w.ticket = (unsigned *)take(4);
     w.tcount = (unsigned *)take(4);
+    w.info = (unsigned *)take(16);
     w.hist = (unsigned *)take(4 * (size_t)kSkHistWords);
     w.counts = (uint2 *)take(sizeof(uint2) * (size_t)max_blocks());
     w.part = (float2 *)take(sizeof(float2) * (size_t)max_blocks());
@@ -221,45 +224,36 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Pairwise (balanced-tree) sum of a[0..k) zero-padded to the next power of
-// two P <= 32: the value of the tree over a[0..P) is taken at level log2 P.
-__device__ __forceinline__ float pairwise32(float (&a)[kSkMaxK], int k) {
-    if (k <= 0) return 0.0f;
-    const int lv = 32 - __clz(k - 1);
-    float r = a[0];
-#pragma unroll
-    for (int L = 1; L <= 5; L++) {
-#pragma unroll
-        for (int i = 0; i < (kSkMaxK >> L); i++) a[i] = __fadd_rn(a[2 * i], a[2 * i + 1]);
-        if (L == lv) r = a[0];
-    }
-    return r;
-}
-
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
 // Exact logit of one row with the lm_head's arithmetic: 16 lanes per row,
 // lane s takes 8-dim chunks s, s+16, ... with fused multiply-adds in
-// dimension order, then a butterfly over the 16 lanes.  Called by whole
-// warps; rows of the two half-warps may differ; invalid rows give 0.
+// dimension order, then a butterfly over the 16 lanes.  NCH >= the chunks of
+// a lane (all its loads are issued first).  Called by whole warps; rows of the
+// two half-warps may differ; invalid rows give 0.
+template <int NCH>
 __device__ __forceinline__ float row_logit(const uint16_t *emb, int D, int word, bool valid, const float *xv) {
     const int sub = threadIdx.x & 15, C = D / 8;
     const uint4 *row = reinterpret_cast<const uint4 *>(emb + (int64_t)word * D);
+    uint4 w[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; i++)
+        if (valid && sub + 16 * i < C) w[i] = ld_stream_v4(row + sub + 16 * i);
     float acc = 0.0f;
-    if (valid) {
-#pragma unroll 4
-        for (int c = sub; c < C; c += 16) {
-            const uint4 w = ld_stream_v4(row + c);
+#pragma unroll
+    for (int i = 0; i < NCH; i++) {
+        const int c = sub + 16 * i;
+        if (valid && c < C) {
             const float4 xa = *reinterpret_cast<const float4 *>(xv + 8 * c);
             const float4 xb = *reinterpret_cast<const float4 *>(xv + 8 * c + 4);
-            acc = fmaf(__uint_as_float(w.x << 16), xa.x, acc);
-            acc = fmaf(__uint_as_float(w.x & 0xffff0000u), xa.y, acc);
-            acc = fmaf(__uint_as_float(w.y << 16), xa.z, acc);
-            acc = fmaf(__uint_as_float(w.y & 0xffff0000u), xa.w, acc);
-            acc = fmaf(__uint_as_float(w.z << 16), xb.x, acc);
-            acc = fmaf(__uint_as_float(w.z & 0xffff0000u), xb.y, acc);
-            acc = fmaf(__uint_as_float(w.w << 16), xb.z, acc);
-            acc = fmaf(__uint_as_float(w.w & 0xffff0000u), xb.w, acc);
+            acc = fmaf(__uint_as_float(w[i].x << 16), xa.x, acc);
+            acc = fmaf(__uint_as_float(w[i].x & 0xffff0000u), xa.y, acc);
+            acc = fmaf(__uint_as_float(w[i].y << 16), xa.z, acc);
+            acc = fmaf(__uint_as_float(w[i].y & 0xffff0000u), xa.w, acc);
+            acc = fmaf(__uint_as_float(w[i].z << 16), xb.x, acc);
+            acc = fmaf(__uint_as_float(w[i].z & 0xffff0000u), xb.y, acc);
+            acc = fmaf(__uint_as_float(w[i].w << 16), xb.z, acc);
+            acc = fmaf(__uint_as_float(w[i].w & 0xffff0000u), xb.w, acc);
         }
     }
 #pragma unroll
@@ -307,7 +301,7 @@ __device__ void block_best(float &v, int &i, float *wbv, int *wbi) {
 }
 
 struct SkSmem {
-    int ring, bars, hist, xv, pv, isx, mem, topd, xt, bne, bxs, bw, bn, tmp, misc, wbv, wk, sel, total;
+    int ring, bars, hist, xv, pv, isx, mem, topd, xt, bmx, bwn, tmp, misc, wbv, wk, sel, total;
 };
 
 // Shared-memory carve: ring_bytes of stages (the ring region is at least
@@ -331,10 +325,8 @@ __host__ __device__ inline SkSmem sk_layout(int ring_bytes, int range_words) {
     s.mem = take(4 * kSkMemberCap);
     s.topd = take(4 * kSkMaxK);
     s.xt = take(4 * kSkMaxK);
-    s.bne = take(8 * kSkMaxBlocks);
-    s.bxs = take(8 * kSkMaxBlocks);
-    s.bw = take(4 * kSkMaxBlocks);
-    s.bn = take(4 * kSkMaxBlocks);
+    s.bmx = take(16 * kSkMaxBlocks);  // per block: sketched-dim mask, x's sign bits (64 bits each)
+    s.bwn = take(8 * kSkMaxBlocks);   // per block: weight, sketched-dim count
     s.tmp = take(4 * 40);
     s.misc = take(4 * 16);
     s.wbv = take(8 * kSkWarps);
@@ -375,10 +367,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) sketch_head_kernel(SketchArgs a
     int *mem = reinterpret_cast<int *>(smem + L.mem);
     int *topd = reinterpret_cast<int *>(smem + L.topd);
     float *xt = reinterpret_cast<float *>(smem + L.xt);
-    uint64_t *bne = reinterpret_cast<uint64_t *>(smem + L.bne);
-    uint64_t *bxs = reinterpret_cast<uint64_t *>(smem + L.bxs);
-    float *bw = reinterpret_cast<float *>(smem + L.bw);
-    int *bn = reinterpret_cast<int *>(smem + L.bn);
+    uint4 *bmx = reinterpret_cast<uint4 *>(smem + L.bmx);
+    float2 *bwn = reinterpret_cast<float2 *>(smem + L.bwn);
     unsigned *tmp = reinterpret_cast<unsigned *>(smem + L.tmp);
     int *misc = reinterpret_cast<int *>(smem + L.misc);
     float *wbv = reinterpret_cast<float *>(smem + L.wbv);
@@ -393,14 +383,21 @@ __global__ void __launch_bounds__(kSkThreads, 1) sketch_head_kernel(SketchArgs a
     const int w0 = kSkTile * t0;
     const int nw = max(0, min(kSkTile * t1, V) - w0);  // words of this CTA
     const int nchunks = (nw + W - 1) / W;
-    const size_t stage_bytes = (size_t)W * (8 * nblk + 2 * k);
+    const size_t stage_bytes = (size_t)W * 8 * nblk;
     const bool producer = warp == kSkConsumerWarps;
+    // Consumer warps form `groups` groups of gsize warps; group g takes the
+    // chunks c = g (mod groups), one 64-word sub-tile per warp at a time.
+    // groups divides kSkStages, so chunk c - kSkStages (the previous fill of
+    // the stage chunk c waits on) belongs to the same group and has landed:
+    // a waiter is never two phases ahead of a stage's full barrier, where
+    // the parity would name an old phase.
+    const int gsize = min(kSkConsumerWarps, W / kSkSub);
+    const int groups = kSkConsumerWarps / gsize >= kSkStages ? kSkStages : kSkConsumerWarps / gsize >= 2 ? 2 : 1;
     // words, sign bytes and exact-row bytes of chunk c
     auto chunk_words = [&](int c) { return min(W, nw - c * W); };
     auto sign_bytes = [&](int c) { return (uint32_t)((chunk_words(c) + 1) / 2 * 16); };
-    auto exact_bytes = [&](int c) { return (uint32_t)((chunk_words(c) + 7) / 8 * 16); };
 
-    if (tid == 0) ring->init(kSkConsumerWarps);
+    if (tid == 0) ring->init(gsize);
     for (int d = tid; d < D; d += kSkThreads) {
         xv[d] = a.x[d];
         const int pd = a.perm[d];
@@ -409,11 +406,12 @@ __global__ void __launch_bounds__(kSkThreads, 1) sketch_head_kernel(SketchArgs a
     for (int i = tid; i < 2048; i += kSkThreads) hist_s[i] = 0u;
     __syncthreads();
     const uint64_t pol = l2_evict_first();
-    if (producer && lane == 0) {  // the sign words of the first stages need nothing from x
+    if (producer) {  // the sign words of the first stages need nothing from x
         for (int c = 0; c < min(kSkStages, nchunks); c++) {
             uint8_t *st = ringp + (size_t)c * stage_bytes;
-            mbar_arrive_expect_tx(&ring->full[c], (uint32_t)nblk * sign_bytes(c) + (uint32_t)k * exact_bytes(c));
-            for (int b = 0; b < nblk; b++)
+            if (lane == 0) mbar_arrive_expect_tx(&ring->full[c], (uint32_t)nblk * sign_bytes(c));
+            __syncwarp();
+            for (int b = lane; b < nblk; b += 32)
                 bulk_g2s(st + (size_t)b * W * 8, a.signs + (int64_t)b * a.Vt + w0 + c * W, sign_bytes(c),
                          &ring->full[c], pol);
         }
@@ -525,10 +523,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) sketch_head_kernel(SketchArgs a
             for (int o = 1; o < 32; o <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
             if (lane == 0) {
                 const int n = __popcll(ne);
-                bne[b] = ne;
-                bxs[b] = xs;
-                bn[b] = n;
-                bw[b] = n > 0 ? __fmul_rn(__fdiv_rn(s, (float)n), cE) : 0.0f;
+                bmx[b] = make_uint4((uint32_t)ne, (uint32_t)(ne >> 32), (uint32_t)xs, (uint32_t)(xs >> 32));
+                bwn[b] = make_float2(n > 0 ? __fmul_rn(__fdiv_rn(s, (float)n), cE) : 0.0f, __int_as_float(n));
             }
         }
     }
@@ -537,70 +533,119 @@ __global__ void __launch_bounds__(kSkThreads, 1) sketch_head_kernel(SketchArgs a
 
     // ---------------------------------------------------------------- approximate scores
     if (producer) {
+        int c = kSkStages;
+        for (; c < nchunks; c++) {
+            const int s = c % kSkStages;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&ring->empty[s], ((c / kSkStages) - 1) & 1);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) raise_status(a.ws.status, kStatusTimeout);
+                break;
+            }
+            uint8_t *st = ringp + (size_t)s * stage_bytes;
+            if (lane == 0) mbar_arrive_expect_tx(&ring->full[s], (uint32_t)nblk * sign_bytes(c));
+            __syncwarp();
+            for (int b = lane; b < nblk; b += 32)
+                bulk_g2s(st + (size_t)b * W * 8, a.signs + (int64_t)b * a.Vt + w0 + c * W, sign_bytes(c),
+                         &ring->full[s], pol);
+        }
+        // every copy issued must have landed before the CTA moves on
         if (lane == 0) {
-            for (int c = 0; c < min(kSkStages, nchunks); c++) {
-                uint8_t *st = ringp + (size_t)c * stage_bytes + (size_t)W * 8 * nblk;
-                for (int j = 0; j < k; j++)
-                    bulk_g2s(st + (size_t)j * W * 2, a.emb_t + (int64_t)topd[j] * a.Vt + w0 + c * W, exact_bytes(c),
-                             &ring->full[c], pol);
-            }
-            int c = kSkStages;
-            for (; c < nchunks; c++) {
-                const int s = c % kSkStages;
-                if (!mbar_wait(&ring->empty[s], ((c / kSkStages) - 1) & 1)) {
-                    raise_status(a.ws.status, kStatusTimeout);
-                    break;
-                }
-                uint8_t *st = ringp + (size_t)s * stage_bytes;
-                mbar_arrive_expect_tx(&ring->full[s], (uint32_t)nblk * sign_bytes(c) + (uint32_t)k * exact_bytes(c));
-                for (int b = 0; b < nblk; b++)
-                    bulk_g2s(st + (size_t)b * W * 8, a.signs + (int64_t)b * a.Vt + w0 + c * W, sign_bytes(c),
-                             &ring->full[s], pol);
-                for (int j = 0; j < k; j++)
-                    bulk_g2s(st + (size_t)W * 8 * nblk + (size_t)j * W * 2,
-                             a.emb_t + (int64_t)topd[j] * a.Vt + w0 + c * W, exact_bytes(c), &ring->full[s], pol);
-            }
-            // every copy issued must have landed before the CTA moves on
             const int issued = min(c, nchunks);
             for (int u = max(0, issued - kSkStages); u < issued; u++)
                 if (!mbar_wait(&ring->full[u % kSkStages], (u / kSkStages) & 1))
                     raise_status(a.ws.status, kStatusTimeout);
         }
-    } else {
+    } else if (warp < groups * gsize) {
+        const int grp = warp / gsize, wg = warp % gsize;
 #pragma unroll 1
-        for (int c = 0; c < nchunks; c++) {
+        for (int c = grp; c < nchunks; c += groups) {
             const int s = c % kSkStages;
+            const int ncw = chunk_words(c);
+            // the exact rows of this warp's first sub-tile: coalesced loads issued before the stage wait
+            uint32_t raw[kSkMaxK];
+            {
+                const int v = w0 + c * W + wg * kSkSub + 2 * lane;
+                const bool any = wg * kSkSub < ncw && v < V;
+#pragma unroll
+                for (int j = 0; j < kSkMaxK; j++)
+                    raw[j] = (any && j < k) ? __ldg(reinterpret_cast<const uint32_t *>(a.emb_t + (int64_t)topd[j] * a.Vt + v)) : 0u;
+            }
             if (!mbar_wait(&ring->full[s], (c / kSkStages) & 1)) {
                 raise_status(a.ws.status, kStatusTimeout);
                 break;
             }
-            const uint8_t *st = ringp + (size_t)s * stage_bytes;
-            const uint64_t *sg = reinterpret_cast<const uint64_t *>(st);
-            const uint16_t *ex = reinterpret_cast<const uint16_t *>(st + (size_t)W * 8 * nblk);
-            const int ncw = chunk_words(c);
+            const uint64_t *sg = reinterpret_cast<const uint64_t *>(ringp + (size_t)s * stage_bytes);
 #pragma unroll 1
-            for (int sub = warp; sub * kSkTile < ncw; sub += kSkConsumerWarps) {
-                const int vl = sub * kSkTile + lane;
-                float e[kSkMaxK];
+            for (int sub = wg; sub * kSkSub < ncw; sub += gsize) {
+                const int vl = sub * kSkSub + 2 * lane;  // this lane's two words: vl, vl + 1
+                if (sub != wg) {
+                    const int v = w0 + c * W + vl;
+#pragma unroll
+                    for (int j = 0; j < kSkMaxK; j++)
+                        raw[j] = (v < V && j < k) ? __ldg(reinterpret_cast<const uint32_t *>(a.emb_t + (int64_t)topd[j] * a.Vt + v)) : 0u;
+                }
+                // exact part: a streaming pairwise tree per word (slot l holds a
+                // finished subtree of 2^l products; element j merges with the
+                // slots of its trailing one bits), zero-padded up to P
+                float p0[6], p1[6];
+#pragma unroll
+                for (int l = 0; l < 6; l++) p0[l] = p1[l] = 0.0f;
+                const int P = k > 0 ? 1 << (32 - __clz(k - 1)) : 0;
 #pragma unroll
                 for (int j = 0; j < kSkMaxK; j++)
-                    e[j] = j < k ? __fmul_rn(__uint_as_float((uint32_t)ex[(size_t)j * W + vl] << 16), xt[j]) : 0.0f;
-                const float exact = pairwise32(e, k);
-                float sk = 0.0f;
+                    if (j < P) {
+                        float c0 = 0.0f, c1 = 0.0f;
+                        if (j < k) {
+                            const uint32_t pr = raw[j];
+                            const float xj = xt[j];
+                            c0 = __fmul_rn(__uint_as_float(pr << 16), xj);
+                            c1 = __fmul_rn(__uint_as_float(pr & 0xffff0000u), xj);
+                        }
+#pragma unroll
+                        for (int l = 0; l < 6; l++) {
+                            if (l < 5 && ((j >> l) & 1)) {
+                                c0 = __fadd_rn(p0[l], c0);
+                                c1 = __fadd_rn(p1[l], c1);
+                            } else {
+                                p0[l] = c0;
+                                p1[l] = c1;
+                                break;
+                            }
+                        }
+                    }
+                const int lv = k > 0 ? 32 - __clz(k - 1) : 0;  // the root of the P-tree sits in slot log2 P
+                float exact0 = 0.0f, exact1 = 0.0f;
+#pragma unroll
+                for (int l = 0; l < 6; l++)
+                    if (k > 0 && l == lv) {
+                        exact0 = p0[l];
+                        exact1 = p1[l];
+                    }
+                float sk0 = 0.0f, sk1 = 0.0f;
 #pragma unroll
                 for (int b = 0; b < MAXB; b++)
                     if (b < nblk) {
-                        const int m = __popcll((sg[(size_t)b * W + vl] ^ bxs[b]) & bne[b]);
-                        sk = __fadd_rn(sk, __fmul_rn(bw[b], (float)(bn[b] - 2 * m)));
+                        const uint4 sw = *reinterpret_cast<const uint4 *>(sg + (size_t)b * W + vl);
+                        const uint4 mx = bmx[b];
+                        const float2 wn = bwn[b];
+                        const int n = __float_as_int(wn.y);
+                        const int m0 = __popc((sw.x ^ mx.z) & mx.x) + __popc((sw.y ^ mx.w) & mx.y);
+                        const int m1 = __popc((sw.z ^ mx.z) & mx.x) + __popc((sw.w ^ mx.w) & mx.y);
+                        sk0 = __fadd_rn(sk0, __fmul_rn(wn.x, (float)(n - 2 * m0)));
+                        sk1 = __fadd_rn(sk1, __fmul_rn(wn.x, (float)(n - 2 * m1)));
                     }
-                if (vl < ncw) {
-                    const int v = w0 + c * W + vl;
-                    const float ap = __fadd_rn(exact, sk);
-                    if (a.approx) a.approx[v] = ap;
-                    const uint32_t key = order_key(ap);
-                    wkey[v - w0] = key;
-                    atomicAdd(&hist_s[key >> 20], 1u);
-                }
+#pragma unroll
+                for (int h = 0; h < 2; h++)
+                    if (vl + h < ncw) {
+                        const int v = w0 + c * W + vl + h;
+                        const float ap = __fadd_rn(h ? exact1 : exact0, h ? sk1 : sk0);
+                        if (a.approx) a.approx[v] = ap;
+                        const uint32_t key = order_key(ap);
+                        wkey[v - w0] = key;
+                        atomicAdd(&hist_s[key >> 20], 1u);
+                    }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ring->empty[s]);
@@ -609,13 +654,45 @@ __global__ void __launch_bounds__(kSkThreads, 1) sketch_head_kernel(SketchArgs a
     __syncthreads();
     for (int i = tid; i < kSkBins1; i += kSkThreads)
         if (hist_s[i]) atomicAdd(&a.ws.hist[i], hist_s[i]);
-    if (!grid_barrier(a.ws.bar, a.ws.status, misc + 8)) return;
-
     // ---------------------------------------------------------------- the boundary bin
-    find_bin<true>(a.ws.hist, kSkBins1, (unsigned)a.n_cand, tmp, misc + 0, (unsigned *)misc + 1);
-    const uint32_t b1 = (uint32_t)misc[0];
-    const unsigned above1 = (unsigned)misc[1];
-    const unsigned superset = above1 + __ldcg(a.ws.hist + b1);
+    // A grid barrier whose last arrival (every histogram is in) finds the bin
+    // of the n_cand-th largest key before it opens the barrier.
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned g = ld_acquire_u32(a.ws.bar + 1);
+        __threadfence();
+        misc[9] = atomicAdd(a.ws.bar, 1u) == gridDim.x - 1;
+        misc[10] = (int)g;
+    }
+    __syncthreads();
+    if (misc[9]) {
+        __threadfence();
+        find_bin<true>(a.ws.hist, kSkBins1, (unsigned)a.n_cand, tmp, misc + 0, (unsigned *)misc + 1);
+        if (tid == 0) {
+            a.ws.info[0] = (unsigned)misc[0];
+            a.ws.info[1] = (unsigned)misc[1];
+            a.ws.info[2] = (unsigned)misc[1] + __ldcg(a.ws.hist + misc[0]);
+            atomicExch(a.ws.bar, 0u);
+            __threadfence();
+            st_release_u32(a.ws.bar + 1, (unsigned)misc[10] + 1);
+        }
+    } else if (tid == 0) {
+        const uint64_t tw = global_ns();
+        while (ld_acquire_u32(a.ws.bar + 1) == (unsigned)misc[10]) {
+            if (global_ns() - tw > kWaitLimitNs) {
+                raise_status(a.ws.status, kStatusTimeout);
+                misc[9] = -1;
+                break;
+            }
+            __nanosleep(32);
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    if (misc[9] < 0) return;
+    const uint32_t b1 = __ldcg(a.ws.info + 0);
+    const unsigned above1 = __ldcg(a.ws.info + 1);
+    const unsigned superset = __ldcg(a.ws.info + 2);
     const int per = (nw + kSkThreads - 1) / kSkThreads;
     const int c0 = min(nw, per * tid), c1 = min(nw, c0 + per);
 
@@ -643,7 +720,7 @@ __global__ void __launch_bounds__(kSkThreads, 1) sketch_head_kernel(SketchArgs a
         for (int jw = 2 * warp; jw < (int)blk; jw += 2 * kSkWarps) {  // warp-uniform trip count
             const int j = jw + (lane >> 4);
             const bool valid = j < (int)blk;
-            const float lg = row_logit(a.emb, D, valid ? sel[j] : 0, valid, xv);
+            const float lg = row_logit<MAXB / 2>(a.emb, D, valid ? sel[j] : 0, valid, xv);
             if ((lane & 15) == 0 && valid) a.ws.tlogit[off + j] = lg;
         }
         __syncthreads();
@@ -673,18 +750,40 @@ __global__ void __launch_bounds__(kSkThreads, 1) sketch_head_kernel(SketchArgs a
         uint32_t *rk = reinterpret_cast<uint32_t *>(ringp);
         int *ri = reinterpret_cast<int *>(ringp + 4 * kSkCap);
         float *rl = reinterpret_cast<float *>(ringp + 8 * kSkCap);
-        for (int p = tid; p < (int)S; p += kSkThreads) {
-            int lo = 0, hi = nb - 1;  // the CTA whose segment holds walk position p
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (wst[mid] <= (unsigned)p) lo = mid;
-                else hi = mid - 1;
+        constexpr int kGather = (kSkCap + kSkThreads - 1) / kSkThreads;
+        unsigned srcs[kGather];
+#pragma unroll
+        for (int q = 0; q < kGather; q++) {
+            const int p = tid + q * kSkThreads;
+            srcs[q] = 0xffffffffu;
+            if (p < (int)S) {
+                int lo = 0, hi = nb - 1;  // the CTA whose segment holds walk position p
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (wst[mid] <= (unsigned)p) lo = mid;
+                    else hi = mid - 1;
+                }
+                srcs[q] = wst[nb + lo] + ((unsigned)p - wst[lo]);
             }
-            const unsigned src = wst[nb + lo] + ((unsigned)p - wst[lo]);
-            rk[p] = __ldcg(a.ws.tkey + src);
-            ri[p] = __ldcg(a.ws.tidx + src);
-            rl[p] = __ldcg(a.ws.tlogit + src);
         }
+        uint32_t gk[kGather];
+        int gi[kGather];
+        float gl[kGather];
+#pragma unroll
+        for (int q = 0; q < kGather; q++)
+            if (srcs[q] != 0xffffffffu) {
+                gk[q] = __ldcg(a.ws.tkey + srcs[q]);
+                gi[q] = __ldcg(a.ws.tidx + srcs[q]);
+                gl[q] = __ldcg(a.ws.tlogit + srcs[q]);
+            }
+#pragma unroll
+        for (int q = 0; q < kGather; q++)
+            if (srcs[q] != 0xffffffffu) {
+                const int p = tid + q * kSkThreads;
+                rk[p] = gk[q];
+                ri[p] = gi[q];
+                rl[p] = gl[q];
+            }
         __syncthreads();
         // the n_cand-th largest key: the rest of the radix select inside bin b1
         unsigned need = (unsigned)a.n_cand - above1;
@@ -805,7 +904,7 @@ __global__ void __launch_bounds__(kSkThreads, 1) sketch_head_kernel(SketchArgs a
         const int j = jw + (lane >> 4);
         const bool valid = j < (int)blk_sel;
         const int word = valid ? sel[j] : 0;
-        const float lg = row_logit(a.emb, D, word, valid, xv);
+        const float lg = row_logit<MAXB / 2>(a.emb, D, word, valid, xv);
         if ((lane & 15) == 0 && valid) {
             a.cand_logits[base + j] = lg;
             if (better(lg, word, best_v, best_i)) {
@@ -1003,12 +1102,12 @@ qlin_status qlin_sketch_head(const uint16_t *emb, const uint16_t *emb_t, const u
     // one CTA per SM; the stages take what the per-CTA tables leave
     const int nb = std::min(sm_count(), tiles);
     const int range_tiles = (tiles + nb - 1) / nb;
-    const int per_word = 8 * nblk + 2 * k;
+    const int per_word = 8 * nblk;
     // the stages get what the opt-in limit leaves after the fixed tables (at most kSkRingBudget)
     const int fixed = sk_layout(0, kSkTile * range_tiles).total - sk_layout(0, 0).ring - 12 * kSkCap;
     const int budget = std::min(kSkRingBudget, max_smem_optin() - fixed - 1024);
-    int chunk = budget / (kSkStages * per_word) / kSkTile * kSkTile;
-    chunk = std::max(kSkTile, std::min(chunk, range_tiles * kSkTile));
+    int chunk = budget / (kSkStages * per_word) / kSkSub * kSkSub;
+    chunk = std::max(kSkSub, std::min(chunk, (range_tiles * kSkTile + kSkSub - 1) / kSkSub * kSkSub));
     const int ring_bytes = kSkStages * chunk * per_word;
     const size_t smem = (size_t)sk_layout(ring_bytes, kSkTile * range_tiles).total;
     QLIN_REQUIRE(smem <= (size_t)max_smem_optin(), QLIN_ERR_UNSUPPORTED,
