@@ -341,6 +341,31 @@ int decode_step_t158_launches(const t158_model *m);
  * word of a decode workspace. */
 qlin_status decode_step_t158_status(void *workspace, qlin_stream_t stream);
 
+/* The decode step with the sketch head as its output layer ([citric] "Step 3:
+ * the output layer became the bottleneck"): decode_step_t158 up to the final
+ * norm, then qlin_sketch_head over the tied table (m->emb) picks the next
+ * token.  Two launches per step.  The tables come from qlin_sketch_prepare on
+ * m->emb, with the final norm gain m->g_final as the per-dimension size. */
+typedef struct {
+    const uint16_t *emb_t;  /* dimension-major copy of m->emb */
+    const uint64_t *signs;  /* sign words */
+    const int32_t *perm;    /* size order of the dims */
+    const float *c_e;       /* device float: mean |E| */
+    int k;                  /* exact dims, 0..32 */
+    int n_cand;             /* candidates, 1..vocab */
+} t158_sketch;
+
+/* Bytes of device scratch for decode_step_t158_sketch: the decode workspace,
+ * the final hidden state, the candidates and the sketch head's workspace.
+ * Zero-filled before first use; steps leave it ready for the next one. */
+qlin_status decode_step_t158_sketch_workspace_size(const t158_model *m, const t158_sketch *s, size_t *bytes);
+qlin_status decode_step_t158_sketch(const t158_model *m, const t158_sketch *s, float *kv_cache, void *workspace,
+                                    size_t workspace_bytes, const int32_t *token, int32_t pos, int32_t *next_token,
+                                    qlin_stream_t stream);
+/* Reads and clears both status words (synchronises `stream`). */
+qlin_status decode_step_t158_sketch_status(const t158_model *m, const t158_sketch *s, void *workspace,
+                                           qlin_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -80,6 +80,7 @@ def _L():
                 "or_sketch_perm": ([p, i64, p], ctypes.c_int),
                 "or_sketch_head": ([p, i64, i64, p, i64, p, i64, i64, f32, p, p, p, p], ctypes.c_int),
                 "or_decode_step": ([ctypes.POINTER(OrModel), p, i32, i64, p, p], ctypes.c_int),
+                "or_decode_hidden": ([ctypes.POINTER(OrModel), p, i32, i64, p], ctypes.c_int),
                 "or_decode_generate": ([ctypes.POINTER(OrModel), p, p, i64, i64, i64, p], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
@@ -352,6 +353,13 @@ class Decoder:
                                  _p(logits) if want_logits else None, ctypes.byref(nxt))
         _check(rc, "decode_step")
         return nxt.value, logits
+
+    def hidden(self, kv: np.ndarray, token: int, pos: int):
+        """The step up to the final norm: appends k and v at pos, returns the normalised hidden state."""
+        assert kv.flags.c_contiguous and kv.dtype == np.float32
+        xn = np.empty(self.cfg.dim, np.float32)
+        _check(_L().or_decode_hidden(ctypes.byref(self.model), _p(kv), int(token), int(pos), _p(xn)), "decode_hidden")
+        return xn
 
     def generate(self, kv: np.ndarray, prompt: np.ndarray, start_pos: int, n_steps: int):
         prompt = np.ascontiguousarray(prompt, np.int32)

@@ -643,7 +643,7 @@ void or_lm_head_argmax(const uint16_t *emb, const float *x, int64_t vocab, int64
  * [L][2][max_pos][kv_dim], fp32 logits [vocab] (may be NULL) and the greedy
  * token ([llama2.c] "Sampling": first maximum wins).  logits are fp64 sums
  * rounded to fp32. */
-int or_decode_step(const or_model *m, float *kv, int32_t token, int64_t pos, float *logits, int32_t *next) {
+static int decode_hidden(const or_model *m, float *kv, int32_t token, int64_t pos, float *xn_out) {
     if (!m || !kv || pos < 0 || pos >= m->max_pos || token < 0 || token >= m->vocab) return OR_EINVAL;
     int64_t d = m->dim, qd = m->n_heads * m->head_dim, kvd = m->n_kv_heads * m->head_dim, f = m->ffn;
     int64_t half = m->head_dim / 2;
@@ -656,7 +656,6 @@ int or_decode_step(const or_model *m, float *kv, int32_t token, int64_t pos, flo
     float *u = (float *)malloc((size_t)f * 4);
     int8_t *xq = (int8_t *)malloc((size_t)big);
     float *rc = (float *)malloc((size_t)half * 4), *rs = (float *)malloc((size_t)half * 4);
-    float *lg = logits ? logits : (float *)malloc((size_t)m->vocab * 4);
 
     /* Step 0: embed */
     for (int64_t i = 0; i < d; i++) h[i] = bf16f(m->emb[(int64_t)token * d + i]);
@@ -692,14 +691,33 @@ int or_decode_step(const or_model *m, float *kv, int32_t token, int64_t pos, flo
         t158_layer(m, (int)l, 6, g, xq, y);
         for (int64_t i = 0; i < d; i++) h[i] = h[i] + y[i];
     }
-    /* Step 6: final norm and classifier (tied bf16 table) */
-    or_rmsnorm(h, m->g_final, d, m->eps, xn);
-    or_lm_head_argmax(m->emb, xn, m->vocab, d, lg, next);
+    /* Step 6 (first half): final norm */
+    or_rmsnorm(h, m->g_final, d, m->eps, xn_out);
 
-    if (!logits) free(lg);
     free(h); free(xn); free(q); free(k); free(v); free(att); free(y); free(g); free(u); free(xq);
     free(rc); free(rs);
     return OR_OK;
+}
+
+int or_decode_step(const or_model *m, float *kv, int32_t token, int64_t pos, float *logits, int32_t *next) {
+    if (!m || !next) return OR_EINVAL;
+    float *xn = (float *)malloc((size_t)(m->dim > 0 ? m->dim : 1) * 4);
+    const int rc = decode_hidden(m, kv, token, pos, xn);
+    if (rc == OR_OK) {
+        /* Step 6 (second half): classifier (tied bf16 table) */
+        float *lg = logits ? logits : (float *)malloc((size_t)m->vocab * 4);
+        or_lm_head_argmax(m->emb, xn, m->vocab, m->dim, lg, next);
+        if (!logits) free(lg);
+    }
+    free(xn);
+    return rc;
+}
+
+/* The same forward step up to the final norm: the hidden state the output
+ * layer scores (for a sketch head in place of the full classifier). */
+int or_decode_hidden(const or_model *m, float *kv, int32_t token, int64_t pos, float *xn) {
+    if (!m || !xn) return OR_EINVAL;
+    return decode_hidden(m, kv, token, pos, xn);
 }
 
 /* [llama2.c] "The generation loop": force-feed the prompt, then feed back

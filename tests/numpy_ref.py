@@ -150,6 +150,12 @@ class NumpyDecoder:
         return out.ravel()
 
     def step(self, kv, token, pos):
+        hn = self.hidden(kv, token, pos)
+        logits = (self.emb.astype(np.float64) @ hn.astype(np.float64)).astype(f32)
+        return int(np.argmax(logits)), logits
+
+    def hidden(self, kv, token, pos):
+        """The step up to the final norm (appends k and v at pos)."""
         cfg = self.cfg
         h = self.emb[token].astype(f32).copy()
         for l in range(cfg.n_layers):
@@ -169,9 +175,7 @@ class NumpyDecoder:
             u = self._lin(W["wu"], xn)
             a = (gelu32(g) * u).astype(f32)
             h = (h + self._lin(W["wd"], a)).astype(f32)
-        hn = rmsnorm32(h, self.g_final, cfg.eps)
-        logits = (self.emb.astype(np.float64) @ hn.astype(np.float64)).astype(f32)
-        return int(np.argmax(logits)), logits
+        return rmsnorm32(h, self.g_final, cfg.eps)
 
     def generate(self, kv, prompt, start_pos, n_steps):
         out = []

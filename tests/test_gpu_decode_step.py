@@ -5,7 +5,11 @@
 * Gemma-3-1B-shaped decoder (26 blocks, hidden 1152, 4/1 heads of 256, GeGLU
   6912, vocab 262144, seed 4): the same 16 + 64 greedy run from an empty cache,
   and steps on a cache filled to position 1024 (the throughput state);
-* the status word reports an out-of-range token.
+* the status word reports an out-of-range token;
+* the decode step with the sketch head as its output layer: tokens equal to
+  the oracle's step cut at the final norm plus the oracle's sketch head, KV
+  cache bit-exact (tiny decoder, and four steps of the Gemma-shaped one at
+  position 1024).
 """
 import numpy as np
 import pytest
@@ -92,6 +96,59 @@ def test_gemma_shape_steps_at_pos_1024(gemma):
     prompt = np.array([int(synth.prompt_ids(4, 1, cfg.vocab)[0])], np.int32)
     _run_and_compare(gpu, orc, kv_o, prompt, 1024, 4)
     np.testing.assert_array_equal(host(gpu.kv)[:, :, 1024:1028], kv_o[:, :, 1024:1028])
+
+
+def _sketch_run(cfg, gpu, orc, kv_o, token, start_pos, n_steps, k, n_cand):
+    """Steps of decode_step_t158_sketch against the oracle's step cut at the
+    final norm followed by the oracle's sketch head (size order from the final
+    norm gain, the GPU's c_E); tokens fed back; returns the tokens and how many
+    agree with the exact output layer."""
+    import torch
+
+    perm = oracle.sketch_perm(host(gpu.g_final))
+    cE = float(host(gpu.sk_ce)[0])
+    gpu.token.fill_(token)
+    ids, agree = [], 0
+    for s in range(n_steps):
+        pos = start_pos + s
+        xn = orc.hidden(kv_o, token, pos)
+        nx_o, cand_o, cl_o, _ = oracle.sketch_head(orc.emb, xn, perm=perm, k=k, n_cand=n_cand, cE=cE)
+        gpu.step_sketch(pos)
+        torch.cuda.synchronize()
+        nx_g = int(gpu.token.item())
+        if nx_g != nx_o:  # only a near-tie among the candidates' exact logits may differ
+            tol = 1e-5 * float(np.abs(cl_o).max())
+            near = set(cand_o[cl_o >= cl_o.max() - 2 * tol].tolist())
+            assert nx_g in near, f"step {s} (pos {pos}): token {nx_g} != oracle {nx_o}"
+        agree += int(nx_o == oracle.lm_head_argmax(orc.emb, xn)[0])
+        ids.append(nx_g)
+        token = nx_o
+        gpu.token.fill_(token)
+    gpu.check_sketch_status()
+    return np.array(ids), agree
+
+
+def test_tiny_decoder_sketch_head_steps(dev):
+    cfg = synth.DecoderConfig(max_pos=96, **synth.TINY)
+    gpu, orc = _pair(cfg, 5, dev)
+    gpu.prepare_sketch(k=16, n_cand=48)
+    kv_o = orc.new_cache()
+    ids, _ = _sketch_run(cfg, gpu, orc, kv_o, 7, 0, 40, 16, 48)
+    np.testing.assert_array_equal(host(gpu.kv)[:, :, :40], kv_o[:, :, :40])
+
+
+def test_gemma_shape_sketch_head_steps_at_pos_1024(gemma):
+    import torch
+
+    cfg, gpu, orc = gemma
+    gpu.prepare_sketch(k=32, n_cand=1024)
+    kv0 = synth.kv_fill(cfg, 4, 1024)
+    gpu.kv.copy_(torch.from_numpy(kv0))
+    kv_o = kv0.copy()
+    token = int(synth.prompt_ids(4, 1, cfg.vocab)[0])
+    ids, agree = _sketch_run(cfg, gpu, orc, kv_o, token, 1024, 4, 32, 1024)
+    np.testing.assert_array_equal(host(gpu.kv)[:, :, 1024:1028], kv_o[:, :, 1024:1028])
+    print("sketch tokens:", ids.tolist(), "agree with the exact output layer:", agree, "of", len(ids))
 
 
 def test_out_of_range_token_sets_status(dev):

@@ -101,3 +101,21 @@ def test_argmax_first_maximum_wins():
     orc = oracle.Decoder(cfg, w)
     nx, logits = orc.step(orc.new_cache(), 9, 0)
     assert (logits == logits[0]).all() and nx == 0
+
+
+def test_hidden_state_is_the_step_before_the_classifier(tiny):
+    """The step cut before the classifier: the classifier of its hidden state
+    gives the full step's token and logits exactly, the caches are the same,
+    and the hidden state is the NumPy reference's final normalised residual."""
+    cfg, w, orc, ref = tiny
+    kv_a, kv_b, kv_c = orc.new_cache(), orc.new_cache(), orc.new_cache()
+    token = 11
+    for pos in range(24):
+        xn = orc.hidden(kv_a, token, pos)
+        nb, lb = orc.step(kv_b, token, pos)
+        na, la = oracle.lm_head_argmax(w["emb"], xn)
+        assert na == nb
+        np.testing.assert_array_equal(la, lb)
+        np.testing.assert_allclose(xn, ref.hidden(kv_c, token, pos), rtol=0, atol=1e-5 * np.abs(xn).max())
+        token = nb
+    np.testing.assert_array_equal(kv_a, kv_b)

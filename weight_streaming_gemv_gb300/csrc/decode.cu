@@ -561,6 +561,104 @@ qlin_status decode_step_t158(const t158_model *m, float *kv_cache, void *workspa
     return qlin::launch_decode_fused(a, (cudaStream_t)stream);
 }
 
+namespace {
+struct SketchStepWs {
+    float *final_x;
+    int32_t *cand;
+    float *cand_logits;
+    char *sketch;
+    size_t sketch_bytes, bytes;
+};
+
+SketchStepWs carve_sketch(const t158_model *m, const t158_sketch *s, char *base) {
+    SketchStepWs w{};
+    size_t off = qlin::align256(qlin::carve(m, nullptr).bytes);
+    auto take = [&](size_t b) {
+        char *p = base ? base + off : nullptr;
+        off += qlin::align256(b);
+        return p;
+    };
+    w.final_x = (float *)take(4 * (size_t)m->dim);
+    w.cand = (int32_t *)take(4 * (size_t)s->n_cand);
+    w.cand_logits = (float *)take(4 * (size_t)s->n_cand);
+    w.sketch_bytes = qlin_sketch_workspace_size(m->vocab);
+    w.sketch = take(w.sketch_bytes);
+    w.bytes = off;
+    return w;
+}
+
+qlin_status check_sketch(const t158_model *m, const t158_sketch *s) {
+    QLIN_REQUIRE(s && s->emb_t && s->signs && s->perm && s->c_e, QLIN_ERR_INVALID_ARG,
+                 "decode_step_t158_sketch: null sketch table");
+    QLIN_REQUIRE(s->k >= 0 && s->k <= 32 && s->k <= m->dim && s->n_cand >= 1 && s->n_cand <= m->vocab,
+                 QLIN_ERR_INVALID_ARG, "decode_step_t158_sketch: k = %d, n_cand = %d", s->k, s->n_cand);
+    return QLIN_OK;
+}
+}  // namespace
+
+qlin_status decode_step_t158_sketch_workspace_size(const t158_model *m, const t158_sketch *s, size_t *bytes) {
+    qlin::clear_error();
+    qlin_status st = qlin::check_model(m);
+    if (st) return st;
+    if ((st = check_sketch(m, s))) return st;
+    QLIN_REQUIRE(bytes, QLIN_ERR_INVALID_ARG, "decode_step_t158_sketch_workspace_size: null bytes");
+    *bytes = carve_sketch(m, s, nullptr).bytes;
+    return QLIN_OK;
+}
+
+qlin_status decode_step_t158_sketch(const t158_model *m, const t158_sketch *s, float *kv_cache, void *workspace,
+                                    size_t workspace_bytes, const int32_t *token, int32_t pos, int32_t *next_token,
+                                    qlin_stream_t stream) {
+    qlin::clear_error();
+    qlin_status st = qlin::check_model(m);
+    if (st) return st;
+    if ((st = check_sketch(m, s))) return st;
+    QLIN_REQUIRE(kv_cache && workspace && token && next_token, QLIN_ERR_INVALID_ARG,
+                 "decode_step_t158_sketch: null pointer");
+    QLIN_REQUIRE(pos >= 0 && pos < m->max_pos, QLIN_ERR_INVALID_ARG, "decode_step_t158_sketch: pos %d outside [0, %d)",
+                 pos, m->max_pos);
+    QLIN_REQUIRE(qlin::aligned16(workspace) && qlin::aligned16(kv_cache), QLIN_ERR_INVALID_ARG,
+                 "decode_step_t158_sketch: workspace or kv_cache not 16-byte aligned");
+    const SketchStepWs sw = carve_sketch(m, s, (char *)workspace);
+    QLIN_REQUIRE(workspace_bytes >= sw.bytes, QLIN_ERR_INVALID_ARG,
+                 "decode_step_t158_sketch: workspace %zu < %zu bytes", workspace_bytes, sw.bytes);
+    const qlin::DecodeWs w = qlin::carve(m, (char *)workspace);
+    qlin::FusedArgs a{};
+    a.m = *m;
+    a.kv = kv_cache;
+    a.token = token;
+    a.pos = pos;
+    a.logits = nullptr;
+    a.next = next_token;
+    a.final_x = sw.final_x;
+    a.hT = w.hT;
+    a.qkvT = w.qkvT;
+    a.attT = w.attT;
+    a.aT = w.aT;
+    a.pmT = w.pmT;
+    a.pST = w.pST;
+    a.pUT = w.pUT;
+    a.ncmax = w.ncmax;
+    a.lm_part = w.lm_part;
+    a.lm_ticket = w.lm_ticket;
+    a.seq = w.seq;
+    a.status = w.status;
+    if ((st = qlin::launch_decode_fused(a, (cudaStream_t)stream))) return st;
+    return qlin_sketch_head(m->emb, s->emb_t, s->signs, s->perm, s->c_e, m->vocab, m->dim, sw.final_x, s->k, s->n_cand,
+                            nullptr, sw.cand, sw.cand_logits, next_token, sw.sketch, sw.sketch_bytes, stream);
+}
+
+qlin_status decode_step_t158_sketch_status(const t158_model *m, const t158_sketch *s, void *workspace,
+                                           qlin_stream_t stream) {
+    qlin::clear_error();
+    qlin_status st = qlin::check_model(m);
+    if (st) return st;
+    if ((st = check_sketch(m, s))) return st;
+    QLIN_REQUIRE(workspace, QLIN_ERR_INVALID_ARG, "decode_step_t158_sketch_status: null workspace");
+    if ((st = decode_step_t158_status(workspace, stream))) return st;
+    return qlin_sketch_head_status(carve_sketch(m, s, (char *)workspace).sketch, stream);
+}
+
 int decode_step_t158_launches(const t158_model *m) {
     qlin::clear_error();
     if (qlin::check_model(m)) return -1;

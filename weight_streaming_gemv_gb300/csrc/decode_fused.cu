@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
             t++;
         };
         for (int l = 0; l < m.n_layers && ok; l++) layer_items(A, l, b, G, push);
-        lm_items(A, b, G, push);
+        if (!A.final_x) lm_items(A, b, G, push);
         for (int u = max(0, t - kFStages); u < t; u++)
             if (!mbar_wait(&ring->full[u % kFStages], (u / kFStages) & 1)) raise_status(A.status, kStatusTimeout);
         return;
@@ -396,7 +396,13 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     // ---------------- final norm, lm_head, argmax
     float best_v = -__int_as_float(0x7f800000);
     int best_i = 0x7fffffff;
-    if (!*abort) {
+    const bool go = !*abort;  // read once, as every stage of the step does
+    if (go && A.final_x) {  // the step ends at the final norm: its output goes to another head
+        rmsnorm_from_tagged(A.hT, make_tag(seq, m.n_layers - 1, 5), m.g_final, hvec, xv, d, m.eps, seg, g, abort,
+                            A.status);
+        if (b == 0)
+            for (int c = g.tid; c < d; c += g.n) A.final_x[c] = xv[c];
+    } else if (go) {
         rmsnorm_from_tagged(A.hT, make_tag(seq, m.n_layers - 1, 5), m.g_final, hvec, xv, d, m.eps, seg, g, abort,
                             A.status);
         const int C = d / 8;
@@ -494,7 +500,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
             }
         }
         if (g.tid == 0) {
-            *A.next = i;
+            if (!A.final_x) *A.next = i;
             *A.lm_ticket = 0u;
             *reinterpret_cast<volatile unsigned *>(A.seq) = (seq + 1u) & 0x3fffffu;  // tags of the next launch
         }

@@ -22,6 +22,7 @@ struct FusedArgs {
     int pos;
     float *logits;
     int32_t *next;
+    float *final_x;  // non-null: stop after the final norm and write it here (no lm_head, next untouched)
     // workspace: vectors passed between CTAs as tagged words (value | tag << 32)
     uint64_t *hT, *qkvT, *attT, *aT, *pmT, *pST, *pUT;
     int ncmax;

@@ -80,3 +80,33 @@ class T158Decoder:
 
     def check_status(self, stream=None):
         qlin.decode_step_t158_status(self.workspace, stream)
+
+    # ---------------------------------------------------------------- sketch head
+    def prepare_sketch(self, k: int = 32, n_cand: int = 1024, stream=None):
+        """Tables of the sketch head over the tied table, ordered by the final norm gain,
+        and the workspace of ``step_sketch``."""
+        cfg, dev = self.cfg, self.emb.device
+        self.sk_emb_t = torch.empty((cfg.dim, qlin.qlin_sketch_emb_t_pitch(cfg.vocab)), dtype=torch.int16,
+                                    device=dev)
+        self.sk_signs = torch.empty(qlin.qlin_sketch_signs_bytes(cfg.vocab, cfg.dim) // 8, dtype=torch.int64,
+                                    device=dev)
+        self.sk_perm = torch.empty(cfg.dim, dtype=torch.int32, device=dev)
+        self.sk_ce = torch.zeros(1, dtype=torch.float32, device=dev)
+        qlin.qlin_sketch_prepare(self.emb, cfg.vocab, cfg.dim, self.g_final, self.sk_emb_t, self.sk_signs,
+                                 self.sk_perm, self.sk_ce, stream)
+        sk = qlin.T158SketchC()
+        sk.emb_t, sk.signs = self.sk_emb_t.data_ptr(), self.sk_signs.data_ptr()
+        sk.perm, sk.c_e = self.sk_perm.data_ptr(), self.sk_ce.data_ptr()
+        sk.k, sk.n_cand = k, n_cand
+        self.sketch = sk
+        self.sk_ws_bytes = qlin.decode_step_t158_sketch_workspace_size(self.model, sk)
+        self.sk_workspace = torch.zeros(self.sk_ws_bytes, dtype=torch.uint8, device=dev)
+
+    def step_sketch(self, pos: int, token=None, stream=None):
+        """One forward step whose next token comes from the sketch head (two launches)."""
+        tok = self.token if token is None else token
+        qlin.decode_step_t158_sketch(self.model, self.sketch, self.kv, self.sk_workspace, self.sk_ws_bytes, tok, pos,
+                                     self.token, stream)
+
+    def check_sketch_status(self, stream=None):
+        qlin.decode_step_t158_sketch_status(self.model, self.sketch, self.sk_workspace, stream)

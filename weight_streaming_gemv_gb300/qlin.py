@@ -42,6 +42,15 @@ class T158ModelC(ctypes.Structure):
     ]
 
 
+class T158SketchC(ctypes.Structure):
+    """Mirror of ``t158_sketch``."""
+
+    _fields_ = [
+        ("emb_t", ctypes.c_void_p), ("signs", ctypes.c_void_p), ("perm", ctypes.c_void_p), ("c_e", ctypes.c_void_p),
+        ("k", ctypes.c_int32), ("n_cand", ctypes.c_int32),
+    ]
+
+
 _P, _I, _I64, _F, _D, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double,
                              ctypes.c_size_t)
 _ST = ctypes.c_int
@@ -79,6 +88,11 @@ SIGNATURES = {
     "decode_step_t158": ([ctypes.POINTER(T158ModelC), _P, _P, _SZ, _P, ctypes.c_int32, _P, _P, _P], _ST),
     "decode_step_t158_launches": ([ctypes.POINTER(T158ModelC)], _I),
     "decode_step_t158_status": ([_P, _P], _ST),
+    "decode_step_t158_sketch_workspace_size": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(T158SketchC),
+                                                ctypes.POINTER(_SZ)], _ST),
+    "decode_step_t158_sketch": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(T158SketchC), _P, _P, _SZ, _P,
+                                 ctypes.c_int32, _P, _P], _ST),
+    "decode_step_t158_sketch_status": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(T158SketchC), _P, _P], _ST),
 }
 
 
@@ -283,3 +297,22 @@ def decode_step_t158_launches(model: T158ModelC) -> int:
 
 def decode_step_t158_status(workspace, stream=None):
     _check("decode_step_t158_status", lib().decode_step_t158_status(_ptr(workspace), _stream(stream)))
+
+
+def decode_step_t158_sketch_workspace_size(model: T158ModelC, sk: T158SketchC) -> int:
+    n = ctypes.c_size_t()
+    _check("decode_step_t158_sketch_workspace_size",
+           lib().decode_step_t158_sketch_workspace_size(ctypes.byref(model), ctypes.byref(sk), ctypes.byref(n)))
+    return n.value
+
+
+def decode_step_t158_sketch(model: T158ModelC, sk: T158SketchC, kv_cache, workspace, workspace_bytes, token, pos,
+                            next_token, stream=None):
+    _check("decode_step_t158_sketch", lib().decode_step_t158_sketch(
+        ctypes.byref(model), ctypes.byref(sk), _ptr(kv_cache), _ptr(workspace), workspace_bytes, _ptr(token), pos,
+        _ptr(next_token), _stream(stream)))
+
+
+def decode_step_t158_sketch_status(model: T158ModelC, sk: T158SketchC, workspace, stream=None):
+    _check("decode_step_t158_sketch_status", lib().decode_step_t158_sketch_status(
+        ctypes.byref(model), ctypes.byref(sk), _ptr(workspace), _stream(stream)))
