@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
     p.add_argument("--workload", choices=["decode"], default="decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kernel", choices=["sketch_head", "decode_steps"], default=None,
+                   help="time one kernel alone on its full-size synthetic inputs (for profiling); no JSON bench line")
     return p.parse_args()
 
 
@@ -53,7 +55,7 @@ def parse():
 # dram__bytes_write.sum from one ncu capture at context `pos`), valid only for
 # the kernel sources it was taken on: any change to them reports null.
 FUSED_SOURCES = ['decode_fused.cu', 'decode_fused.cuh', 'decode_ops.cuh', 'stream.cuh', 'common.cuh']
-FUSED_TRAFFIC = {"sha256": "27cb45ac5ea64309aa9ec7e429e62882746af37f6e48af0e401e1187c4be9649", "bytes": 806239744, "pos": 1024}
+FUSED_TRAFFIC = {"sha256": "248ee7ad7fe4898346d1d39b679763eb616409db63fc3c48b6a1d0b684574d2d", "bytes": 806089216, "pos": 1024}
 
 
 def fused_traffic():
@@ -250,6 +252,7 @@ def run_decode(args, rank, local, world):
     lm_alg = lm_bytes + cfg.dim * 4 + 8
     peak, peak_kind = peaks()
     lm_gbs = lm_alg / (lm_ms / 1e3) / 1e9
+    sketch = sketch_decode(gpu, cfg, args, stream, lm_ms, peak)
     gemv = gemv_m1(dev, stream)
     prefill = prefill_m512(dev, stream)
     lanes = lanes_t158(dev, stream)
@@ -285,6 +288,7 @@ def run_decode(args, rank, local, world):
             "frac_of_8tbs": round(step_bytes * args.steps / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
             "frac_of_peak": round(step_bytes * args.steps / (ms / 1e3) / 1e9 / peak, 4),
         },
+        "sketch_head": sketch,
         "gemv_m1": gemv,
         "prefill_m512": prefill,
         "lanes_t158": lanes,
@@ -309,6 +313,67 @@ def run_decode(args, rank, local, world):
         "clocks": clk,
     }
     return out, cfg, weights
+
+
+def sketch_decode(gpu, cfg, args, stream, lm_ms, peak):
+    """The output layer as a sketch head: the decode step with it (two launches per
+    step, tokens fed back on the device) and the sketch head kernel timed alone after
+    an L2 flush, against the exact lm_head kernel's time."""
+    import torch
+
+    from weight_streaming_gemv_gb300 import qlin
+
+    K_EXACT, N_CAND = 32, 1024
+    gpu.prepare_sketch(k=K_EXACT, n_cand=N_CAND, stream=stream)
+    for i in range(max(args.warmup, 3)):
+        gpu.step_sketch(POS0 + i % POS_SPAN)
+    torch.cuda.synchronize()
+    gpu.check_sketch_status()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        gpu.step_sketch(POS0 + i % POS_SPAN)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    gpu.check_sketch_status()
+    ms = e0.elapsed_time(e1) / args.steps
+
+    # the kernel alone: a hidden state with the final norm's sizes, L2 flushed before each call
+    V, D = cfg.vocab, cfg.dim
+    x = (torch.randn(D, device=gpu.emb.device) * gpu.g_final.abs()).contiguous()
+    cand = torch.empty(N_CAND, dtype=torch.int32, device=x.device)
+    cl = torch.empty(N_CAND, dtype=torch.float32, device=x.device)
+    nx = torch.zeros(1, dtype=torch.int32, device=x.device)
+    wsb = qlin.qlin_sketch_workspace_size(V)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=x.device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=x.device)
+    call = lambda: qlin.qlin_sketch_head(gpu.emb, gpu.sk_emb_t, gpu.sk_signs, gpu.sk_perm, gpu.sk_ce, V, D, x,
+                                         K_EXACT, N_CAND, None, cand, cl, nx, ws, wsb, stream)
+    for _ in range(5):
+        call()
+    ts = []
+    for it in range(40):
+        flush.fill_(it & 255)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        call()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a0.elapsed_time(a1) * 1e3)
+    qlin.qlin_sketch_head_status(ws)
+    us = float(sorted(ts)[len(ts) // 2])
+    nblk = (D + 63) // 64
+    alg = V * nblk * 8 + K_EXACT * V * 2 + N_CAND * D * 2 + D * 4
+    gbs = alg / (us * 1e-6) / 1e9
+    return {
+        "decode_tokens_per_s": round(1e3 / ms, 2), "decode_ms_per_step": round(ms, 5), "launches_per_step": 2,
+        "k_exact": K_EXACT, "n_cand": N_CAND, "size_order": "|final norm gain|",
+        "kernel": "sketch_head_kernel (alone, L2 flushed, median of 40)",
+        "us_per_call": round(us, 2), "exact_lm_head_us": round(lm_ms * 1e3, 2),
+        "speedup_vs_exact_lm_head": round(lm_ms * 1e3 / us, 2),
+        "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+        "algorithmic_bytes": alg,
+    }
 
 
 def gemv_m1(dev, stream):
@@ -521,8 +586,70 @@ def oracle_decode(cfg, weights, steps, warmup, budget_s):
     return done, dt, threads
 
 
+def kernel_only(name):
+    """The sketch head alone on a synthetic 262144 x 1152 table: 5 warm-up calls, then 20 timed
+    calls with an L2 flush before each (prints one line of timings)."""
+    import numpy as np
+    import torch
+
+    import synth
+    from weight_streaming_gemv_gb300 import qlin
+
+    dev = torch.device("cuda", 0)
+    if name == "decode_steps":
+        # six exact steps and six sketch-head steps of the Gemma-shaped decoder at context 1024
+        from weight_streaming_gemv_gb300.decoder import T158Decoder
+
+        cfg = decode_cfg(6, 0)
+        gpu = T158Decoder(cfg, synth.decoder_weights(cfg, seed=SEED), device=dev)
+        gpu.kv.copy_(torch.from_numpy(synth.kv_fill(cfg, SEED, POS0)))
+        gpu.token.fill_(int(synth.prompt_ids(SEED, 1, cfg.vocab)[0]))
+        gpu.prepare_sketch(32, 1024)
+        for i in range(6):
+            gpu.step(POS0 + i, logits=False)
+        for i in range(6):
+            gpu.step_sketch(POS0 + i)
+        torch.cuda.synchronize()
+        gpu.check_status()
+        gpu.check_sketch_status()
+        print(json.dumps({"kernel": name, "next": int(gpu.token.item())}))
+        return 0
+    V, D, K_EXACT, N_CAND = 262144, 1152, 32, 1024
+    d = synth.sketch_head(SEED, V, D)
+    emb = torch.from_numpy(d["emb"].view(np.int16)).to(dev)
+    scale = torch.from_numpy(d["scale"]).to(dev)
+    emb_t = torch.empty((D, qlin.qlin_sketch_emb_t_pitch(V)), dtype=torch.int16, device=dev)
+    signs = torch.empty(qlin.qlin_sketch_signs_bytes(V, D) // 8, dtype=torch.int64, device=dev)
+    perm = torch.empty(D, dtype=torch.int32, device=dev)
+    c_e = torch.zeros(1, dtype=torch.float32, device=dev)
+    qlin.qlin_sketch_prepare(emb, V, D, scale, emb_t, signs, perm, c_e)
+    x = torch.from_numpy(synth.sketch_x(SEED, 0, d["scale"])).to(dev)
+    cand = torch.empty(N_CAND, dtype=torch.int32, device=dev)
+    cl = torch.empty(N_CAND, dtype=torch.float32, device=dev)
+    nx = torch.zeros(1, dtype=torch.int32, device=dev)
+    wsb = qlin.qlin_sketch_workspace_size(V)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ts = []
+    for it in range(25):
+        flush.fill_(it & 255)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        qlin.qlin_sketch_head(emb, emb_t, signs, perm, c_e, V, D, x, K_EXACT, N_CAND, None, cand, cl, nx, ws, wsb)
+        e1.record()
+        torch.cuda.synchronize()
+        if it >= 5:
+            ts.append(e0.elapsed_time(e1) * 1e3)
+    qlin.qlin_sketch_head_status(ws)
+    print(json.dumps({"kernel": name, "us_median": round(float(np.median(ts)), 2), "us_min": round(min(ts), 2),
+                      "next": int(nx.item())}))
+    return 0
+
+
 def main():
     args = parse()
+    if args.kernel:
+        return kernel_only(args.kernel)
     rank, local, world = dist_init(args.gpus)
     if args.impl == "reference":
         if rank != 0:
