@@ -81,6 +81,7 @@ def _L():
                 "or_sketch_head": ([p, i64, i64, p, i64, p, i64, i64, f32, p, p, p, p], ctypes.c_int),
                 "or_decode_step": ([ctypes.POINTER(OrModel), p, i32, i64, p, p], ctypes.c_int),
                 "or_decode_hidden": ([ctypes.POINTER(OrModel), p, i32, i64, p], ctypes.c_int),
+                "or_decode_lanes": ([ctypes.POINTER(OrModel), p, i64, i64, p, p, p, p, p], ctypes.c_int),
                 "or_decode_generate": ([ctypes.POINTER(OrModel), p, p, i64, i64, i64, p], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
@@ -360,6 +361,19 @@ class Decoder:
         xn = np.empty(self.cfg.dim, np.float32)
         _check(_L().or_decode_hidden(ctypes.byref(self.model), _p(kv), int(token), int(pos), _p(xn)), "decode_hidden")
         return xn
+
+    def lanes(self, kvs: np.ndarray, tokens, positions, seqs, want_logits: bool = False):
+        """One step over M lanes; kvs: [n_seqs][L][2][max_pos][kv_dim].  Returns (next [M], logits [M][V] or None)."""
+        assert kvs.flags.c_contiguous and kvs.dtype == np.float32
+        t = np.ascontiguousarray(tokens, np.int32)
+        p = np.ascontiguousarray(positions, np.int32)
+        sq = np.ascontiguousarray(seqs, np.int32)
+        M = t.size
+        nxt = np.empty(M, np.int32)
+        lg = np.empty((M, self.cfg.vocab), np.float32) if want_logits else None
+        _check(_L().or_decode_lanes(ctypes.byref(self.model), _p(kvs), kvs.shape[0], M, _p(t), _p(p), _p(sq),
+                                    _p(lg) if want_logits else None, _p(nxt)), "decode_lanes")
+        return nxt, lg
 
     def generate(self, kv: np.ndarray, prompt: np.ndarray, start_pos: int, n_steps: int):
         prompt = np.ascontiguousarray(prompt, np.int32)

@@ -720,6 +720,83 @@ int or_decode_hidden(const or_model *m, float *kv, int32_t token, int64_t pos, f
     return decode_hidden(m, kv, token, pos, xn);
 }
 
+/* A step over M lanes ([citric] "Many users at once": a lane is one token of
+ * one sequence at one position; batches of users and chunks of a prompt go
+ * through the same step).  Lane i takes token[i] at position pos[i] of
+ * sequence seq[i], whose KV cache is kv + seq[i] * (L * 2 * max_pos * kvd).
+ * Layer by layer: every lane's k and v are written to its cache before any
+ * lane attends, so a lane sees the positions <= its own that other lanes of
+ * its sequence write in the same step.  Each lane's arithmetic is the single
+ * token step's.  logits: fp32 [M][vocab] or NULL; next: [M]. */
+int or_decode_lanes(const or_model *m, float *kv, int64_t n_seqs, int64_t M, const int32_t *token, const int32_t *pos,
+                    const int32_t *seq, float *logits, int32_t *next) {
+    if (!m || !kv || !token || !pos || !seq || !next || M < 1 || n_seqs < 1) return OR_EINVAL;
+    for (int64_t i = 0; i < M; i++)
+        if (pos[i] < 0 || pos[i] >= m->max_pos || token[i] < 0 || token[i] >= m->vocab || seq[i] < 0 ||
+            seq[i] >= n_seqs)
+            return OR_EINVAL;
+    const int64_t d = m->dim, qd = m->n_heads * m->head_dim, kvd = m->n_kv_heads * m->head_dim, f = m->ffn;
+    const int64_t half = m->head_dim / 2, L = m->n_layers;
+    const int64_t per_seq = L * 2 * m->max_pos * kvd;
+    int64_t big = f > qd ? f : qd;
+    if (d > big) big = d;
+    float *h = (float *)malloc((size_t)(M * d) * 4), *xn = (float *)malloc((size_t)d * 4);
+    float *q = (float *)malloc((size_t)(M * qd) * 4), *k = (float *)malloc((size_t)kvd * 4);
+    float *v = (float *)malloc((size_t)kvd * 4), *att = (float *)malloc((size_t)qd * 4);
+    float *y = (float *)malloc((size_t)big * 4), *g = (float *)malloc((size_t)f * 4);
+    float *u = (float *)malloc((size_t)f * 4);
+    int8_t *xq = (int8_t *)malloc((size_t)big);
+    float *rc = (float *)malloc((size_t)(M * half) * 4), *rs = (float *)malloc((size_t)(M * half) * 4);
+    for (int64_t i = 0; i < M; i++) {
+        for (int64_t e = 0; e < d; e++) h[i * d + e] = bf16f(m->emb[(int64_t)token[i] * d + e]);
+        for (int64_t e = 0; e < half; e++) {
+            double theta = pow(m->rope_base, -(double)(2 * e) / (double)m->head_dim);
+            double ang = (double)pos[i] * theta;
+            rc[i * half + e] = (float)cos(ang);
+            rs[i * half + e] = (float)sin(ang);
+        }
+    }
+    for (int64_t l = 0; l < L; l++) {
+        /* every lane: norm, q k v, rotation, cache write */
+        for (int64_t i = 0; i < M; i++) {
+            float *kc = kv + seq[i] * per_seq + ((l * 2 + 0) * m->max_pos) * kvd;
+            float *vc = kv + seq[i] * per_seq + ((l * 2 + 1) * m->max_pos) * kvd;
+            or_rmsnorm(h + i * d, m->g_attn + l * d, d, m->eps, xn);
+            t158_layer(m, (int)l, 0, xn, xq, q + i * qd);
+            t158_layer(m, (int)l, 1, xn, xq, k);
+            t158_layer(m, (int)l, 2, xn, xq, v);
+            or_rope_apply(q + i * qd, m->n_heads, m->head_dim, rc + i * half, rs + i * half);
+            or_rope_apply(k, m->n_kv_heads, m->head_dim, rc + i * half, rs + i * half);
+            memcpy(kc + (int64_t)pos[i] * kvd, k, (size_t)kvd * 4);
+            memcpy(vc + (int64_t)pos[i] * kvd, v, (size_t)kvd * 4);
+        }
+        /* every lane: attention, output projection, FFN */
+        for (int64_t i = 0; i < M; i++) {
+            const float *kc = kv + seq[i] * per_seq + ((l * 2 + 0) * m->max_pos) * kvd;
+            const float *vc = kv + seq[i] * per_seq + ((l * 2 + 1) * m->max_pos) * kvd;
+            float *hi = h + i * d;
+            or_attention(q + i * qd, kc, vc, pos[i], m->n_heads, m->n_kv_heads, m->head_dim, att);
+            t158_layer(m, (int)l, 3, att, xq, y);
+            for (int64_t e = 0; e < d; e++) hi[e] = hi[e] + y[e];
+            or_rmsnorm(hi, m->g_ffn + l * d, d, m->eps, xn);
+            t158_layer(m, (int)l, 4, xn, xq, g);
+            t158_layer(m, (int)l, 5, xn, xq, u);
+            for (int64_t e = 0; e < f; e++) g[e] = or_gelu_f32(g[e]) * u[e];
+            t158_layer(m, (int)l, 6, g, xq, y);
+            for (int64_t e = 0; e < d; e++) hi[e] = hi[e] + y[e];
+        }
+    }
+    float *lg = (float *)malloc((size_t)m->vocab * 4);
+    for (int64_t i = 0; i < M; i++) {
+        or_rmsnorm(h + i * d, m->g_final, d, m->eps, xn);
+        or_lm_head_argmax(m->emb, xn, m->vocab, d, logits ? logits + i * m->vocab : lg, next + i);
+    }
+    free(lg);
+    free(h); free(xn); free(q); free(k); free(v); free(att); free(y); free(g); free(u); free(xq);
+    free(rc); free(rs);
+    return OR_OK;
+}
+
 /* [llama2.c] "The generation loop": force-feed the prompt, then feed back
  * the greedy token.  Runs n_steps forwards at positions start_pos ...; out
  * receives the argmax of every forward (for prompt positions too). */

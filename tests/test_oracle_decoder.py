@@ -119,3 +119,55 @@ def test_hidden_state_is_the_step_before_the_classifier(tiny):
         np.testing.assert_allclose(xn, ref.hidden(kv_c, token, pos), rtol=0, atol=1e-5 * np.abs(xn).max())
         token = nb
     np.testing.assert_array_equal(kv_a, kv_b)
+
+
+def _cache(cfg, n_seqs):
+    return np.zeros((n_seqs, cfg.n_layers, 2, cfg.max_pos, cfg.kv_dim), np.float32)
+
+
+def test_lanes_of_separate_sequences_are_separate_steps(tiny):
+    """Lanes of different sequences at different positions: each lane's token,
+    logits and cache rows are those of the single-token step on its own cache."""
+    cfg, w, orc, _ = tiny
+    kvs = _cache(cfg, 3)
+    rng_tok = synth.prompt_ids(6, 12, cfg.vocab)
+    for s in range(3):  # give every sequence some history
+        for p in range(4 + 2 * s):
+            orc.step(kvs[s], int(rng_tok[p]), p, want_logits=False)
+    ref = kvs.copy()
+    tokens, positions, seqs = [11, 22, 33], [4, 6, 8], [0, 1, 2]
+    nxt, lg = orc.lanes(kvs, tokens, positions, seqs, want_logits=True)
+    for i in range(3):
+        nx, l1 = orc.step(ref[seqs[i]], tokens[i], positions[i])
+        assert nxt[i] == nx
+        np.testing.assert_array_equal(lg[i], l1)
+    np.testing.assert_array_equal(kvs, ref)
+
+
+def test_lanes_of_one_sequence_are_a_prompt_chunk(tiny):
+    """Consecutive positions of one sequence in one step (a chunk of a prompt):
+    the same as feeding the tokens one step at a time, in whichever order the
+    lanes are listed -- every lane's k and v are in the cache before any lane
+    attends."""
+    cfg, w, orc, _ = tiny
+    prompt = synth.prompt_ids(7, 9, cfg.vocab)
+    ref = _cache(cfg, 1)
+    want = [orc.step(ref[0], int(prompt[p]), p)[0] for p in range(9)]
+    for order in (np.arange(9), np.array([8, 0, 7, 1, 6, 2, 5, 3, 4])):
+        kvs = _cache(cfg, 1)
+        nxt, _ = orc.lanes(kvs, prompt[order], order, np.zeros(9, np.int32))
+        np.testing.assert_array_equal(nxt, np.array(want)[order])
+        np.testing.assert_array_equal(kvs, ref)
+
+
+def test_lanes_mix_and_bad_lanes(tiny):
+    cfg, w, orc, _ = tiny
+    kvs = _cache(cfg, 2)
+    # one lane alone is the single-token step
+    ref = _cache(cfg, 2)
+    nxt, _ = orc.lanes(kvs, [5], [0], [1])
+    assert nxt[0] == orc.step(ref[1], 5, 0, want_logits=False)[0]
+    np.testing.assert_array_equal(kvs, ref)
+    for bad in (([5], [cfg.max_pos], [0]), ([5], [0], [2]), ([cfg.vocab], [0], [0]), ([5], [-1], [0])):
+        with pytest.raises(ValueError):
+            orc.lanes(kvs, *bad)
