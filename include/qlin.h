@@ -366,6 +366,31 @@ qlin_status decode_step_t158_sketch(const t158_model *m, const t158_sketch *s, f
 qlin_status decode_step_t158_sketch_status(const t158_model *m, const t158_sketch *s, void *workspace,
                                            qlin_stream_t stream);
 
+/* A decode step over lanes ([citric] "Many users at once": every step is a
+ * set of lanes, a lane being one token of one sequence at one position, so
+ * batches of users and chunks of a prompt share one path and each weight byte
+ * is read once for all lanes).  Lane i takes tokens[i] at positions[i] of
+ * sequence seqs[i] (device int32 [n_lanes] each); sequence s owns the KV cache
+ * kv_caches + s * n_layers * 2 * max_pos * n_kv_heads * head_dim (device fp32,
+ * the layout of decode_step_t158).  Layer by layer every lane's k and v are
+ * written before any lane attends: lanes of one sequence at distinct
+ * positions form a prompt chunk, in any order.  Each lane's results are those
+ * of decode_step_t158 for its token (k, v bit for bit; logits as there).
+ * logits: device fp32 [n_lanes][vocab] or NULL; next: device int32 [n_lanes].
+ * The workspace (decode_lanes_t158_workspace_size(m, max_lanes) bytes, the
+ * same max_lanes passed to every call) needs no set-up.  The call issues a
+ * fixed sequence of kernels (decode_lanes_t158_launches) and no host
+ * synchronisation, so it can be captured in a CUDA graph once the first call
+ * has run outside capture.  decode_lanes_t158_status() (synchronises
+ * `stream`) returns QLIN_ERR_INVALID_ARG if a lane's token, position or
+ * sequence slot was out of range (such a lane writes nothing to any cache). */
+qlin_status decode_lanes_t158_workspace_size(const t158_model *m, int max_lanes, size_t *bytes);
+qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs, int n_lanes, const int32_t *tokens,
+                              const int32_t *positions, const int32_t *seqs, float *logits, int32_t *next,
+                              void *workspace, size_t workspace_bytes, int max_lanes, qlin_stream_t stream);
+int decode_lanes_t158_launches(const t158_model *m, int n_lanes);
+qlin_status decode_lanes_t158_status(void *workspace, qlin_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

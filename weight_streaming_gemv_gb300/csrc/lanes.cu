@@ -1,0 +1,296 @@
+// A decode step over lanes ([citric] "Many users at once": every step is a set
+// of lanes, a lane being one token of one sequence at one position; batches of
+// users and chunks of a prompt go through the same step, and each weight byte
+// is read once for all lanes).
+//
+// Lane i takes tokens[i] at positions[i] of sequence seqs[i]; sequence s owns
+// the KV cache kv + s * L * 2 * max_pos * kv_dim (the single-token decode
+// step's layout).  Layer by layer, every lane's k and v are written before any
+// lane attends, so lanes of one sequence at consecutive positions form a
+// prompt chunk.  Each lane's arithmetic is the single-token step's, operation
+// for operation: RMSNorm, int8 absmax quantisation, T158 linear (exact integer
+// dot, fp32 epilogue), RoPE and cache write, chunked attention, GeGLU,
+// residual adds, final norm and the bf16 lm_head with a greedy pick.
+//
+// GB300 mapping: the step is a fixed sequence of kernels over all lanes at
+// once (19 per layer), so it can be captured in a CUDA graph; from 8 lanes
+// the T158 products run on the tensor cores (one pass over each matrix for all
+// lanes).  Positions and sequence slots live in device memory: attention
+// grids are sized for max_pos and chunks past a lane's position exit at once.
+#include <algorithm>
+
+#include "common.cuh"
+#include "decode_ops.cuh"
+
+namespace qlin {
+
+qlin_status t158_linear_dev_scale(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch,
+                                  const float *ws_ptr, float *y, int M, int N, int K, cudaStream_t st);
+
+namespace {
+
+constexpr int kLaneStatusBad = 1;  // a lane's token, position or sequence slot out of range
+
+__device__ __forceinline__ bool lane_ok(int pos, int seq, int max_pos, int n_seqs) {
+    return pos >= 0 && pos < max_pos && seq >= 0 && seq < n_seqs;
+}
+
+// per lane (blockIdx.x): h = emb[token]; a token out of range gives zeros
+__global__ void lanes_embed_kernel(const uint16_t *__restrict__ emb, int vocab, int dim,
+                                   const int32_t *__restrict__ tokens, float *__restrict__ h, int32_t *status) {
+    const int i = blockIdx.x;
+    const int tok = tokens[i];
+    const bool ok = tok >= 0 && tok < vocab;
+    for (int e = threadIdx.x; e < dim; e += blockDim.x)
+        h[(int64_t)i * dim + e] = ok ? __uint_as_float((uint32_t)emb[(int64_t)tok * dim + e] << 16) : 0.0f;
+    if (!ok && threadIdx.x == 0) atomicOr(status, kLaneStatusBad);
+}
+
+// per lane: rotate q and k at the lane's position, write k and v to its cache row
+__global__ void lanes_rope_kv_kernel(float *q, const float *k, const float *v, float *kv, const int32_t *pos,
+                                     const int32_t *seq, int n_seqs, int layer, int L, int max_pos,
+                                     const float *__restrict__ cos_t, const float *__restrict__ sin_t, int nh,
+                                     int nkv, int hd, int32_t *status) {
+    extern __shared__ float kr[];  // [nkv*hd]
+    const int i = blockIdx.x;
+    const int p = pos[i], s = seq[i];
+    if (!lane_ok(p, s, max_pos, n_seqs)) {
+        if (threadIdx.x == 0) atomicOr(status, kLaneStatusBad);
+        return;
+    }
+    const int half = hd / 2, kvd = nkv * hd;
+    const float *c = cos_t + (int64_t)p * half;
+    const float *sn = sin_t + (int64_t)p * half;
+    rope_rotate(q + (int64_t)i * nh * hd, nh, hd, c, sn, whole_block());
+    for (int e = threadIdx.x; e < kvd; e += blockDim.x) kr[e] = k[(int64_t)i * kvd + e];
+    __syncthreads();
+    rope_rotate(kr, nkv, hd, c, sn, whole_block());
+    __syncthreads();
+    float *kc = kv + (((int64_t)s * L + layer) * 2 + 0) * max_pos * kvd;
+    float *vc = kc + (int64_t)max_pos * kvd;
+    const int64_t off = (int64_t)p * kvd;
+    for (int e = threadIdx.x; e < kvd; e += blockDim.x) {
+        kc[off + e] = kr[e];
+        vc[off + e] = v[(int64_t)i * kvd + e];
+    }
+}
+
+// chunk partials of lane i (one workspace block of nh * ncmax * (2 + hd) floats per lane)
+struct LaneAttnWs {
+    float *m, *S, *U;
+};
+
+__device__ __forceinline__ LaneAttnWs lane_attn_ws(float *base, int lane, int ncmax, int nh, int hd) {
+    float *b = base + (size_t)lane * nh * ncmax * (2 + hd);
+    LaneAttnWs w;
+    w.m = b;
+    w.S = b + (size_t)nh * ncmax;
+    w.U = b + (size_t)2 * nh * ncmax;
+    return w;
+}
+
+// grid (ncmax, nh, lanes): chunk c of head h of lane i; chunks past the lane's position exit
+__global__ void __launch_bounds__(256) lanes_attn_chunk_kernel(const float *__restrict__ q, const float *__restrict__ kv,
+                                                               const int32_t *pos, const int32_t *seq, int n_seqs,
+                                                               int layer, int L, int max_pos, int nh, int nkv, int hd,
+                                                               float *ws, int ncmax) {
+    __shared__ float qs[256];
+    __shared__ float sc[32];
+    const int c = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
+    const int p = pos[i], s = seq[i];
+    if (!lane_ok(p, s, max_pos, n_seqs) || c * 32 > p) return;
+    const int kvh = h / (nh / nkv);
+    for (int e = threadIdx.x; e < hd; e += blockDim.x) qs[e] = q[((int64_t)i * nh + h) * hd + e];
+    __syncthreads();
+    const int t0 = c * 32;
+    const int nt = min(32, p + 1 - t0);
+    const int ld = nkv * hd;
+    const float *kc = kv + (((int64_t)s * L + layer) * 2 + 0) * max_pos * ld;
+    const float *vc = kc + (int64_t)max_pos * ld;
+    LaneAttnWs w = lane_attn_ws(ws, i, ncmax, nh, hd);
+    attention_chunk(qs, kc + (int64_t)t0 * ld + kvh * hd, vc + (int64_t)t0 * ld + kvh * hd, ld, nt, hd,
+                    w.m + h * ncmax + c, w.S + h * ncmax + c, w.U + ((int64_t)h * ncmax + c) * hd, sc, whole_block());
+}
+
+// grid (nh, lanes): merge the lane's chunks of head h
+__global__ void __launch_bounds__(256) lanes_attn_merge_kernel(const float *ws, int ncmax, const int32_t *pos,
+                                                               const int32_t *seq, int n_seqs, int max_pos, int nh,
+                                                               int hd, float *out) {
+    extern __shared__ float wbuf[];
+    __shared__ float red[32];
+    const int h = blockIdx.x, i = blockIdx.y;
+    const int p = pos[i];
+    if (!lane_ok(p, seq[i], max_pos, n_seqs)) return;
+    LaneAttnWs w = lane_attn_ws(const_cast<float *>(ws), i, ncmax, nh, hd);
+    attention_merge(w.m + h * ncmax, w.S + h * ncmax, w.U + (int64_t)h * ncmax * hd, p / 32 + 1, hd,
+                    out + ((int64_t)i * nh + h) * hd, wbuf, red, whole_block());
+}
+
+__global__ void lanes_add_kernel(float *h, const float *y, int64_t n) {
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x)
+        h[e] = __fadd_rn(h[e], y[e]);
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+int attn_chunks(int max_pos) { return (max_pos + 31) / 32; }
+
+struct LanesWs {
+    int32_t *status;
+    float *h, *xn, *xs, *q, *k, *v, *att, *y, *g, *u, *attn;
+    int8_t *xq;
+    void *lm;
+    size_t lm_bytes, bytes;
+};
+
+LanesWs carve_lanes(const t158_model *m, int max_lanes, char *base) {
+    LanesWs w{};
+    size_t off = 0;
+    auto take = [&](size_t b) {
+        char *p = base ? base + off : nullptr;
+        off += align256(b);
+        return p;
+    };
+    const size_t M = (size_t)max_lanes, d = m->dim, qd = (size_t)m->n_heads * m->head_dim;
+    const size_t kvd = (size_t)m->n_kv_heads * m->head_dim, f = m->ffn;
+    const size_t big = std::max(std::max(d, qd), f);
+    w.status = (int32_t *)take(16);  // must stay first: decode_lanes_t158_status reads offset 0
+    w.h = (float *)take(4 * M * d);
+    w.xn = (float *)take(4 * M * d);
+    w.xq = (int8_t *)take(M * big);
+    w.xs = (float *)take(4 * M);
+    w.q = (float *)take(4 * M * qd);
+    w.k = (float *)take(4 * M * kvd);
+    w.v = (float *)take(4 * M * kvd);
+    w.att = (float *)take(4 * M * qd);
+    w.y = (float *)take(4 * M * d);
+    w.g = (float *)take(4 * M * f);
+    w.u = (float *)take(4 * M * f);
+    w.attn = (float *)take(4 * M * m->n_heads * (size_t)attn_chunks(m->max_pos) * (2 + m->head_dim));
+    w.lm_bytes = qlin_lm_head_workspace_size(m->vocab);
+    w.lm = take(w.lm_bytes);
+    w.bytes = off;
+    return w;
+}
+
+qlin_status check_lanes_model(const t158_model *m) {
+    QLIN_REQUIRE(m, QLIN_ERR_INVALID_ARG, "decode_lanes_t158: null model");
+    QLIN_REQUIRE(m->n_layers >= 1 && m->dim >= 8 && m->dim % 8 == 0 && m->n_heads >= 1 && m->n_kv_heads >= 1 &&
+                     m->n_heads % m->n_kv_heads == 0 && m->ffn >= 1 && m->vocab >= 1 && m->max_pos >= 1,
+                 QLIN_ERR_INVALID_ARG, "decode_lanes_t158: bad model dimensions");
+    QLIN_REQUIRE(m->head_dim >= 16 && m->head_dim <= 256 && (m->head_dim & (m->head_dim - 1)) == 0,
+                 QLIN_ERR_UNSUPPORTED, "decode_lanes_t158: head_dim %d not a power of two in 16..256", m->head_dim);
+    for (int j = 0; j < T158_NMAT; j++)
+        QLIN_REQUIRE(m->w[j] && aligned16(m->w[j]) && m->pitch[j] % 16 == 0, QLIN_ERR_INVALID_ARG,
+                     "decode_lanes_t158: weight %d null, misaligned or pitch not a multiple of 16", j);
+    QLIN_REQUIRE(m->scales && m->g_attn && m->g_ffn && m->g_final && m->emb && m->rope_cos && m->rope_sin,
+                 QLIN_ERR_INVALID_ARG, "decode_lanes_t158: null model tensor");
+    QLIN_REQUIRE(aligned16(m->emb), QLIN_ERR_INVALID_ARG, "decode_lanes_t158: emb not 16-byte aligned");
+    return QLIN_OK;
+}
+
+}  // namespace
+}  // namespace qlin
+
+using namespace qlin;
+
+extern "C" {
+
+qlin_status decode_lanes_t158_workspace_size(const t158_model *m, int max_lanes, size_t *bytes) {
+    qlin::clear_error();
+    qlin_status st = check_lanes_model(m);
+    if (st) return st;
+    QLIN_REQUIRE(bytes && max_lanes >= 1 && max_lanes <= 4096, QLIN_ERR_INVALID_ARG,
+                 "decode_lanes_t158_workspace_size: max_lanes %d outside 1..4096", max_lanes);
+    *bytes = carve_lanes(m, max_lanes, nullptr).bytes;
+    return QLIN_OK;
+}
+
+qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs, int n_lanes, const int32_t *tokens,
+                              const int32_t *positions, const int32_t *seqs, float *logits, int32_t *next,
+                              void *workspace, size_t workspace_bytes, int max_lanes, qlin_stream_t stream) {
+    qlin::clear_error();
+    qlin_status st = check_lanes_model(m);
+    if (st) return st;
+    QLIN_REQUIRE(kv_caches && tokens && positions && seqs && next && workspace, QLIN_ERR_INVALID_ARG,
+                 "decode_lanes_t158: null pointer");
+    QLIN_REQUIRE(n_seqs >= 1 && n_lanes >= 1 && n_lanes <= max_lanes && max_lanes <= 4096, QLIN_ERR_INVALID_ARG,
+                 "decode_lanes_t158: n_seqs %d, n_lanes %d, max_lanes %d", n_seqs, n_lanes, max_lanes);
+    QLIN_REQUIRE(aligned16(workspace) && aligned16(kv_caches), QLIN_ERR_INVALID_ARG,
+                 "decode_lanes_t158: workspace or kv_caches not 16-byte aligned");
+    const LanesWs w = carve_lanes(m, max_lanes, (char *)workspace);
+    QLIN_REQUIRE(workspace_bytes >= w.bytes, QLIN_ERR_INVALID_ARG, "decode_lanes_t158: workspace %zu < %zu bytes",
+                 workspace_bytes, w.bytes);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int M = n_lanes, L = m->n_layers, d = m->dim, nh = m->n_heads, nkv = m->n_kv_heads, hd = m->head_dim;
+    const int qd = nh * hd, kvd = nkv * hd, f = m->ffn;
+    const int ncmax = attn_chunks(m->max_pos);
+    const uint8_t *W[T158_NMAT];
+    for (int j = 0; j < T158_NMAT; j++) W[j] = m->w[j];
+    const int rows[T158_NMAT] = {qd, kvd, kvd, d, f, f, d};
+    const int cols[T158_NMAT] = {d, d, d, qd, d, d, f};
+    // linear j of layer l on the quantised activations in w.xq / w.xs
+    auto lin = [&](int l, int j, float *out) -> qlin_status {
+        return t158_linear_dev_scale(w.xq, w.xs, W[j] + (int64_t)l * rows[j] * m->pitch[j], m->pitch[j],
+                                     m->scales + (int64_t)l * T158_NMAT + j, out, M, rows[j], cols[j], s);
+    };
+    auto quant = [&](const float *x, int K) { return qlin_quant_i8(x, w.xq, w.xs, M, K, stream); };
+    const int add_blocks = std::max(1, std::min(4 * sm_count(), (int)(((int64_t)M * d + 255) / 256)));
+
+    lanes_embed_kernel<<<M, 256, 0, s>>>(m->emb, m->vocab, d, tokens, w.h, w.status);
+    QLIN_LAUNCHED("lanes_embed_kernel");
+    for (int l = 0; l < L; l++) {
+        if ((st = qlin_rmsnorm(w.h, m->g_attn + (int64_t)l * d, w.xn, M, d, m->eps, stream))) return st;
+        if ((st = quant(w.xn, d))) return st;
+        if ((st = lin(l, 0, w.q)) || (st = lin(l, 1, w.k)) || (st = lin(l, 2, w.v))) return st;
+        lanes_rope_kv_kernel<<<M, 256, (size_t)kvd * sizeof(float), s>>>(
+            w.q, w.k, w.v, kv_caches, positions, seqs, n_seqs, l, L, m->max_pos, m->rope_cos, m->rope_sin, nh, nkv,
+            hd, w.status);
+        QLIN_LAUNCHED("lanes_rope_kv_kernel");
+        lanes_attn_chunk_kernel<<<dim3(ncmax, nh, M), 256, 0, s>>>(w.q, kv_caches, positions, seqs, n_seqs, l, L,
+                                                                   m->max_pos, nh, nkv, hd, w.attn, ncmax);
+        QLIN_LAUNCHED("lanes_attn_chunk_kernel");
+        lanes_attn_merge_kernel<<<dim3(nh, M), 256, (size_t)next_pow2(ncmax) * sizeof(float), s>>>(
+            w.attn, ncmax, positions, seqs, n_seqs, m->max_pos, nh, hd, w.att);
+        QLIN_LAUNCHED("lanes_attn_merge_kernel");
+        if ((st = quant(w.att, qd)) || (st = lin(l, 3, w.y))) return st;
+        lanes_add_kernel<<<add_blocks, 256, 0, s>>>(w.h, w.y, (int64_t)M * d);
+        QLIN_LAUNCHED("lanes_add_kernel");
+        if ((st = qlin_rmsnorm(w.h, m->g_ffn + (int64_t)l * d, w.xn, M, d, m->eps, stream))) return st;
+        if ((st = quant(w.xn, d))) return st;
+        if ((st = lin(l, 4, w.g)) || (st = lin(l, 5, w.u))) return st;
+        if ((st = qlin_geglu(w.g, w.u, w.g, M * f, stream))) return st;
+        if ((st = quant(w.g, f)) || (st = lin(l, 6, w.y))) return st;
+        lanes_add_kernel<<<add_blocks, 256, 0, s>>>(w.h, w.y, (int64_t)M * d);
+        QLIN_LAUNCHED("lanes_add_kernel");
+    }
+    if ((st = qlin_rmsnorm(w.h, m->g_final, w.xn, M, d, m->eps, stream))) return st;
+    for (int i = 0; i < M; i++)
+        if ((st = qlin_lm_head_argmax(m->emb, w.xn + (int64_t)i * d, m->vocab, d,
+                                      logits ? logits + (int64_t)i * m->vocab : nullptr, next + i, w.lm, w.lm_bytes,
+                                      stream)))
+            return st;
+    return QLIN_OK;
+}
+
+int decode_lanes_t158_launches(const t158_model *m, int n_lanes) {
+    qlin::clear_error();
+    if (check_lanes_model(m) || n_lanes < 1) return -1;
+    // embed; per layer 2 norms, 4 quantisations, 7 linears, rope/append, 2 attention, 2 adds, geglu;
+    // final norm; one lm_head per lane (two kernels each when it needs a separate argmax: counted as one)
+    return 1 + m->n_layers * 19 + 1 + n_lanes;
+}
+
+qlin_status decode_lanes_t158_status(void *workspace, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(workspace, QLIN_ERR_INVALID_ARG, "decode_lanes_t158_status: null workspace");
+    int32_t stw[4] = {0, 0, 0, 0};
+    QLIN_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    QLIN_CUDA(cudaMemcpy(stw, workspace, sizeof stw, cudaMemcpyDeviceToHost));
+    QLIN_CUDA(cudaMemset(workspace, 0, sizeof stw));
+    QLIN_REQUIRE(!(stw[0] & kLaneStatusBad), QLIN_ERR_INVALID_ARG,
+                 "decode_lanes_t158: a lane's token, position or sequence slot was out of range");
+    return QLIN_OK;
+}
+
+}  // extern "C"

@@ -215,7 +215,8 @@ static qlin_status dispatch_mt(const int8_t *xq, const float *xs, const uint8_t 
 // kernel on the Gemma-3-1B shapes (1152 -> 6912 and 6912 -> 1152).
 constexpr int kTensorCoreMinM = 8;
 qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
-                                     float *y, int32_t *acc, int M, int N, int K, cudaStream_t st);
+                                     const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K,
+                                     cudaStream_t st);
 
 qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
                                    const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st) {
@@ -223,6 +224,14 @@ qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint
     if (C <= 8) return dispatch_mt<8>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
     if (C <= 16) return dispatch_mt<16>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
     return dispatch_mt<32>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+}
+
+// T158 linear for M tokens with the weight scale in device memory (the decode
+// paths keep the model's scales on the device): the same dispatch as qlin_t158_i8.
+qlin_status t158_linear_dev_scale(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch,
+                                  const float *ws_ptr, float *y, int M, int N, int K, cudaStream_t st) {
+    if (M >= kTensorCoreMinM) return t158_linear_tensor_cores(xq, xs, w, pitch, 0.0f, ws_ptr, y, nullptr, M, N, K, st);
+    return t158_linear_cuda_cores(xq, xs, w, pitch, 0.0f, ws_ptr, y, nullptr, M, N, K, st);
 }
 
 }  // namespace qlin
@@ -250,7 +259,7 @@ qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *
     QLIN_REQUIRE(M <= 4096 && K <= 131071, QLIN_ERR_UNSUPPORTED, "qlin_t158_i8: M=%d K=%d outside 1..4096 x 1..131071",
                  M, K);
     if (M >= qlin::kTensorCoreMinM)
-        return qlin::t158_linear_tensor_cores(xq, x_scale, w_packed, w_pitch, w_scale, y, acc, M, N, K,
+        return qlin::t158_linear_tensor_cores(xq, x_scale, w_packed, w_pitch, w_scale, nullptr, y, acc, M, N, K,
                                               (cudaStream_t)stream);
     return qlin::t158_linear_cuda_cores(xq, x_scale, w_packed, w_pitch, w_scale, nullptr, y, acc, M, N, K,
                                         (cudaStream_t)stream);

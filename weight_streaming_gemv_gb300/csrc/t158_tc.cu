@@ -232,9 +232,11 @@ __device__ __forceinline__ float4 ld_peer_f4(const void *local, uint32_t rank) {
 // each over its own range of K steps.  split == 1: no cluster reduction.
 __global__ void __launch_bounds__(kTcThreads, 1) t158_tc_kernel(const int8_t *__restrict__ xq,
                                                                const float *__restrict__ xs,
-                                                               const uint8_t *__restrict__ w, int64_t pitch, float ws,
+                                                               const uint8_t *__restrict__ w, int64_t pitch, float ws_arg,
+                                                               const float *__restrict__ ws_ptr,
                                                                float *__restrict__ y, int32_t *__restrict__ acc_out,
                                                                int M, int N, int K, int split) {
+    const float ws = ws_ptr ? __ldg(ws_ptr) : ws_arg;  // the weight scale, from device memory when given
     extern __shared__ __align__(128) uint8_t tc_smem_raw[];
     TcSmem &S = *reinterpret_cast<TcSmem *>(tc_smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -473,7 +475,8 @@ static int tc_resident_clusters(int c, size_t smem) {
 }
 
 qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
-                                     float *y, int32_t *acc, int M, int N, int K, cudaStream_t st) {
+                                     const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K,
+                                     cudaStream_t st) {
     const size_t smem = sizeof(TcSmem);
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "qlin_t158_i8: tensor-core tile does not fit");
     blocks_per_sm((const void *)t158_tc_kernel, smem);  // raises the dynamic shared-memory limit
@@ -502,7 +505,7 @@ qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const ui
     attr[0].val.clusterDim.z = (unsigned)split;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tc_kernel, xq, xs, w, pitch, ws, y, acc, M, N, K, split));
+    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tc_kernel, xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, split));
     QLIN_LAUNCHED("t158_tc_kernel");
     return QLIN_OK;
 }

@@ -110,3 +110,27 @@ class T158Decoder:
 
     def check_sketch_status(self, stream=None):
         qlin.decode_step_t158_sketch_status(self.model, self.sketch, self.sk_workspace, stream)
+
+    # ---------------------------------------------------------------- lanes
+    def prepare_lanes(self, n_seqs: int, max_lanes: int):
+        """KV caches for n_seqs sequences and the workspace of ``step_lanes``."""
+        cfg, dev = self.cfg, self.emb.device
+        self.n_seqs, self.max_lanes = n_seqs, max_lanes
+        self.kv_lanes = torch.zeros((n_seqs, cfg.n_layers, 2, cfg.max_pos, cfg.kv_dim), dtype=torch.float32,
+                                    device=dev)
+        self.lanes_ws_bytes = qlin.decode_lanes_t158_workspace_size(self.model, max_lanes)
+        self.lanes_workspace = torch.zeros(self.lanes_ws_bytes, dtype=torch.uint8, device=dev)
+        self.lane_tokens = torch.zeros(max_lanes, dtype=torch.int32, device=dev)
+        self.lane_pos = torch.zeros(max_lanes, dtype=torch.int32, device=dev)
+        self.lane_seq = torch.zeros(max_lanes, dtype=torch.int32, device=dev)
+        self.lane_next = torch.zeros(max_lanes, dtype=torch.int32, device=dev)
+
+    def step_lanes(self, n_lanes: int, logits=None, stream=None):
+        """One step over lanes 0..n_lanes-1 of lane_tokens / lane_pos / lane_seq; the greedy tokens go to
+        lane_next (and the logits [n_lanes][vocab] to ``logits`` if given)."""
+        qlin.decode_lanes_t158(self.model, self.kv_lanes, self.n_seqs, n_lanes, self.lane_tokens, self.lane_pos,
+                               self.lane_seq, logits, self.lane_next, self.lanes_workspace, self.lanes_ws_bytes,
+                               self.max_lanes, stream)
+
+    def check_lanes_status(self, stream=None):
+        qlin.decode_lanes_t158_status(self.lanes_workspace, stream)

@@ -92,6 +92,10 @@ SIGNATURES = {
                                                 ctypes.POINTER(_SZ)], _ST),
     "decode_step_t158_sketch": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(T158SketchC), _P, _P, _SZ, _P,
                                  ctypes.c_int32, _P, _P], _ST),
+    "decode_lanes_t158_workspace_size": ([ctypes.POINTER(T158ModelC), _I, ctypes.POINTER(_SZ)], _ST),
+    "decode_lanes_t158": ([ctypes.POINTER(T158ModelC), _P, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _I, _P], _ST),
+    "decode_lanes_t158_launches": ([ctypes.POINTER(T158ModelC), _I], _I),
+    "decode_lanes_t158_status": ([_P, _P], _ST),
     "decode_step_t158_sketch_status": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(T158SketchC), _P, _P], _ST),
 }
 
@@ -316,3 +320,25 @@ def decode_step_t158_sketch(model: T158ModelC, sk: T158SketchC, kv_cache, worksp
 def decode_step_t158_sketch_status(model: T158ModelC, sk: T158SketchC, workspace, stream=None):
     _check("decode_step_t158_sketch_status", lib().decode_step_t158_sketch_status(
         ctypes.byref(model), ctypes.byref(sk), _ptr(workspace), _stream(stream)))
+
+
+def decode_lanes_t158_workspace_size(model: T158ModelC, max_lanes: int) -> int:
+    n = ctypes.c_size_t()
+    _check("decode_lanes_t158_workspace_size",
+           lib().decode_lanes_t158_workspace_size(ctypes.byref(model), max_lanes, ctypes.byref(n)))
+    return n.value
+
+
+def decode_lanes_t158(model: T158ModelC, kv_caches, n_seqs, n_lanes, tokens, positions, seqs, logits, next_tokens,
+                      workspace, workspace_bytes, max_lanes, stream=None):
+    _check("decode_lanes_t158", lib().decode_lanes_t158(
+        ctypes.byref(model), _ptr(kv_caches), n_seqs, n_lanes, _ptr(tokens), _ptr(positions), _ptr(seqs),
+        _ptr(logits), _ptr(next_tokens), _ptr(workspace), workspace_bytes, max_lanes, _stream(stream)))
+
+
+def decode_lanes_t158_launches(model: T158ModelC, n_lanes: int) -> int:
+    return int(lib().decode_lanes_t158_launches(ctypes.byref(model), n_lanes))
+
+
+def decode_lanes_t158_status(workspace, stream=None):
+    _check("decode_lanes_t158_status", lib().decode_lanes_t158_status(_ptr(workspace), _stream(stream)))
