@@ -290,6 +290,24 @@ qlin_status qlin_sketch_head(const uint16_t *emb, const uint16_t *emb_t, const u
                              size_t workspace_bytes, qlin_stream_t stream);
 qlin_status qlin_sketch_head_status(void *workspace, qlin_stream_t stream);
 
+/* S16 for many lanes ([citric] "Many users at once"): the output layer and
+ * greedy pick of n_lanes hidden states in one pass over the bf16 table.
+ * logits[u][r] = sum_i emb[r][i] * x[u][i], next[u] = the first index of the
+ * maximum.  On the tensor cores: x enters as three bf16 terms (hi, mid, lo;
+ * x to 24 bits) against the bf16 table with fp32 accumulation, so the logits
+ * are within fp32 rounding of the fp32 dot product but not in the order of
+ * qlin_lm_head_argmax.  emb: device bf16 [vocab][dim], 16-byte aligned;
+ * x: device fp32 [n_lanes][dim]; logits: device fp32 [n_lanes][vocab] or NULL;
+ * next: device int32 [n_lanes].  dim % 8 == 0.  Workspace:
+ * qlin_lm_head_lanes_workspace_size() bytes, zero-filled before its first
+ * use; calls leave it ready; calls sharing it must not overlap.  Up to 64
+ * lanes per pass over the table.  qlin_lm_head_lanes_status() (synchronises
+ * `stream`) returns QLIN_ERR_TIMEOUT if a bounded device wait gave up. */
+size_t qlin_lm_head_lanes_workspace_size(int vocab, int dim);
+qlin_status qlin_lm_head_lanes(const uint16_t *emb, const float *x, int vocab, int dim, int n_lanes, float *logits,
+                               int32_t *next, void *workspace, size_t workspace_bytes, qlin_stream_t stream);
+qlin_status qlin_lm_head_lanes_status(void *workspace, qlin_stream_t stream);
+
 /* ========================================================================
  * S8-S16 composed: one decode step of a ternary Gemma-style decoder
  * ([cpp20gemma] "Architecture & implementation": h += attn(rmsnorm(h));
@@ -375,10 +393,12 @@ qlin_status decode_step_t158_sketch_status(const t158_model *m, const t158_sketc
  * the layout of decode_step_t158).  Layer by layer every lane's k and v are
  * written before any lane attends: lanes of one sequence at distinct
  * positions form a prompt chunk, in any order.  Each lane's results are those
- * of decode_step_t158 for its token (k, v bit for bit; logits as there).
+ * of decode_step_t158 for its token (k, v bit for bit; logits and the
+ * greedy pick as qlin_lm_head_lanes gives them).
  * logits: device fp32 [n_lanes][vocab] or NULL; next: device int32 [n_lanes].
  * The workspace (decode_lanes_t158_workspace_size(m, max_lanes) bytes, the
- * same max_lanes passed to every call) needs no set-up.  The call issues a
+ * same max_lanes passed to every call) must be zero-filled before its first
+ * use; calls leave it ready for the next.  The call issues a
  * fixed sequence of kernels (decode_lanes_t158_launches) and no host
  * synchronisation, so it can be captured in a CUDA graph once the first call
  * has run outside capture.  decode_lanes_t158_status() (synchronises

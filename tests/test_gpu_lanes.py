@@ -110,3 +110,28 @@ def test_bad_lanes_set_status(dev):
         if tok == cfg.vocab:
             after[1, :, :, 1] = before[1, :, :, 1]  # a bad token still has a slot: its row comes from zeros
         np.testing.assert_array_equal(after, before)  # the bad lane wrote nothing anywhere else
+
+
+@pytest.mark.parametrize("V,D,U", [(1000, 64, 1), (5000, 136, 5), (129, 8, 17), (3000, 1152, 70), (262144, 1152, 64)])
+def test_lm_head_lanes_matches_oracle(dev, V, D, U):
+    """The output layer for many lanes on the tensor cores: every lane's logits
+    within max-abs-rel 1e-5 of the oracle's fp64 dot products, the greedy pick
+    the oracle's unless its best two are closer than that."""
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    emb = synth.normal_bf16(70, V % 97, (V, D), 0.0, 0.02)
+    x = synth.normal_f32(71, U, (U, D), 0.0, 1.0)
+    lg = torch.empty((U, V), dtype=torch.float32, device=dev)
+    nx = torch.full((U,), -1, dtype=torch.int32, device=dev)
+    wsb = qlin.qlin_lm_head_lanes_workspace_size(V, D)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    qlin.qlin_lm_head_lanes(to_dev(emb, dev), to_dev(x, dev), V, D, U, lg, nx, ws, wsb)
+    qlin.qlin_lm_head_lanes_status(ws)
+    lg_h, nx_h = host(lg), host(nx)
+    for u in range(U):
+        nx_o, lg_o = oracle.lm_head_argmax(emb, x[u])
+        assert max_abs_rel(lg_h[u], lg_o) <= 1e-5, u
+        if nx_h[u] != nx_o:
+            top = np.sort(lg_o)[-2:]
+            assert top[1] - top[0] <= 2e-5 * np.abs(lg_o).max(), (u, nx_h[u], nx_o)

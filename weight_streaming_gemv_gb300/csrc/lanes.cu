@@ -10,7 +10,9 @@
 // prompt chunk.  Each lane's arithmetic is the single-token step's, operation
 // for operation: RMSNorm, int8 absmax quantisation, T158 linear (exact integer
 // dot, fp32 epilogue), RoPE and cache write, chunked attention, GeGLU,
-// residual adds, final norm and the bf16 lm_head with a greedy pick.
+// residual adds, final norm and the bf16 output layer with a greedy pick
+// (here for all lanes in one pass over the table, on the tensor cores, with
+// fp32-accurate logits rather than the single step's exact fp32 order).
 //
 // GB300 mapping: the step is a fixed sequence of kernels over all lanes at
 // once (19 per layer), so it can be captured in a CUDA graph; from 8 lanes
@@ -89,27 +91,39 @@ __device__ __forceinline__ LaneAttnWs lane_attn_ws(float *base, int lane, int nc
     return w;
 }
 
-// grid (ncmax, nh, lanes): chunk c of head h of lane i; chunks past the lane's position exit
+// grid (ncmax, nkv, lanes): chunk c of KV head g of lane i, for every query head
+// of the group (the chunk's k and v rows are read once into shared memory and
+// serve all nh / nkv heads); chunks past the lane's position exit.
 __global__ void __launch_bounds__(256) lanes_attn_chunk_kernel(const float *__restrict__ q, const float *__restrict__ kv,
                                                                const int32_t *pos, const int32_t *seq, int n_seqs,
                                                                int layer, int L, int max_pos, int nh, int nkv, int hd,
                                                                float *ws, int ncmax) {
+    extern __shared__ __align__(16) float kvs[];  // [32][hd] k rows, then [32][hd] v rows
     __shared__ float qs[256];
     __shared__ float sc[32];
-    const int c = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
+    const int c = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
     const int p = pos[i], s = seq[i];
     if (!lane_ok(p, s, max_pos, n_seqs) || c * 32 > p) return;
-    const int kvh = h / (nh / nkv);
-    for (int e = threadIdx.x; e < hd; e += blockDim.x) qs[e] = q[((int64_t)i * nh + h) * hd + e];
-    __syncthreads();
     const int t0 = c * 32;
     const int nt = min(32, p + 1 - t0);
     const int ld = nkv * hd;
-    const float *kc = kv + (((int64_t)s * L + layer) * 2 + 0) * max_pos * ld;
+    const float *kc = kv + (((int64_t)s * L + layer) * 2 + 0) * max_pos * ld + (int64_t)t0 * ld + kvh * hd;
     const float *vc = kc + (int64_t)max_pos * ld;
+    float *Ks = kvs, *Vs = kvs + 32 * hd;
+    for (int e = threadIdx.x; e < nt * hd; e += blockDim.x) {
+        const int t = e / hd, dd = e - t * hd;
+        Ks[e] = kc[(int64_t)t * ld + dd];
+        Vs[e] = vc[(int64_t)t * ld + dd];
+    }
     LaneAttnWs w = lane_attn_ws(ws, i, ncmax, nh, hd);
-    attention_chunk(qs, kc + (int64_t)t0 * ld + kvh * hd, vc + (int64_t)t0 * ld + kvh * hd, ld, nt, hd,
-                    w.m + h * ncmax + c, w.S + h * ncmax + c, w.U + ((int64_t)h * ncmax + c) * hd, sc, whole_block());
+    const int grp = nh / nkv;
+    for (int h = kvh * grp; h < (kvh + 1) * grp; h++) {
+        __syncthreads();  // the k/v rows are in; the previous head is done with qs
+        for (int e = threadIdx.x; e < hd; e += blockDim.x) qs[e] = q[((int64_t)i * nh + h) * hd + e];
+        __syncthreads();
+        attention_chunk(qs, Ks, Vs, hd, nt, hd, w.m + h * ncmax + c, w.S + h * ncmax + c,
+                        w.U + ((int64_t)h * ncmax + c) * hd, sc, whole_block());
+    }
 }
 
 // grid (nh, lanes): merge the lane's chunks of head h
@@ -167,7 +181,7 @@ LanesWs carve_lanes(const t158_model *m, int max_lanes, char *base) {
     w.g = (float *)take(4 * M * f);
     w.u = (float *)take(4 * M * f);
     w.attn = (float *)take(4 * M * m->n_heads * (size_t)attn_chunks(m->max_pos) * (2 + m->head_dim));
-    w.lm_bytes = qlin_lm_head_workspace_size(m->vocab);
+    w.lm_bytes = qlin_lm_head_lanes_workspace_size(m->vocab, m->dim);
     w.lm = take(w.lm_bytes);
     w.bytes = off;
     return w;
@@ -236,6 +250,8 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     };
     auto quant = [&](const float *x, int K) { return qlin_quant_i8(x, w.xq, w.xs, M, K, stream); };
     const int add_blocks = std::max(1, std::min(4 * sm_count(), (int)(((int64_t)M * d + 255) / 256)));
+    const size_t attn_smem = (size_t)2 * 32 * hd * sizeof(float);
+    if (attn_smem > 48 * 1024) blocks_per_sm((const void *)lanes_attn_chunk_kernel, attn_smem);  // raises the limit once
 
     lanes_embed_kernel<<<M, 256, 0, s>>>(m->emb, m->vocab, d, tokens, w.h, w.status);
     QLIN_LAUNCHED("lanes_embed_kernel");
@@ -247,8 +263,9 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
             w.q, w.k, w.v, kv_caches, positions, seqs, n_seqs, l, L, m->max_pos, m->rope_cos, m->rope_sin, nh, nkv,
             hd, w.status);
         QLIN_LAUNCHED("lanes_rope_kv_kernel");
-        lanes_attn_chunk_kernel<<<dim3(ncmax, nh, M), 256, 0, s>>>(w.q, kv_caches, positions, seqs, n_seqs, l, L,
-                                                                   m->max_pos, nh, nkv, hd, w.attn, ncmax);
+        lanes_attn_chunk_kernel<<<dim3(ncmax, nkv, M), 256, attn_smem, s>>>(w.q, kv_caches, positions, seqs, n_seqs,
+                                                                             l, L, m->max_pos, nh, nkv, hd, w.attn,
+                                                                             ncmax);
         QLIN_LAUNCHED("lanes_attn_chunk_kernel");
         lanes_attn_merge_kernel<<<dim3(nh, M), 256, (size_t)next_pow2(ncmax) * sizeof(float), s>>>(
             w.attn, ncmax, positions, seqs, n_seqs, m->max_pos, nh, hd, w.att);
@@ -265,11 +282,8 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
         QLIN_LAUNCHED("lanes_add_kernel");
     }
     if ((st = qlin_rmsnorm(w.h, m->g_final, w.xn, M, d, m->eps, stream))) return st;
-    for (int i = 0; i < M; i++)
-        if ((st = qlin_lm_head_argmax(m->emb, w.xn + (int64_t)i * d, m->vocab, d,
-                                      logits ? logits + (int64_t)i * m->vocab : nullptr, next + i, w.lm, w.lm_bytes,
-                                      stream)))
-            return st;
+    // the output layer for all lanes in one pass over the table (tensor cores)
+    if ((st = qlin_lm_head_lanes(m->emb, w.xn, m->vocab, d, M, logits, next, w.lm, w.lm_bytes, stream))) return st;
     return QLIN_OK;
 }
 
@@ -277,8 +291,8 @@ int decode_lanes_t158_launches(const t158_model *m, int n_lanes) {
     qlin::clear_error();
     if (check_lanes_model(m) || n_lanes < 1) return -1;
     // embed; per layer 2 norms, 4 quantisations, 7 linears, rope/append, 2 attention, 2 adds, geglu;
-    // final norm; one lm_head per lane (two kernels each when it needs a separate argmax: counted as one)
-    return 1 + m->n_layers * 19 + 1 + n_lanes;
+    // final norm; the lanes' output layer (a split and a table pass per 64 lanes)
+    return 1 + m->n_layers * 19 + 1 + 2 * ((n_lanes + 63) / 64);
 }
 
 qlin_status decode_lanes_t158_status(void *workspace, qlin_stream_t stream) {

@@ -92,6 +92,9 @@ SIGNATURES = {
                                                 ctypes.POINTER(_SZ)], _ST),
     "decode_step_t158_sketch": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(T158SketchC), _P, _P, _SZ, _P,
                                  ctypes.c_int32, _P, _P], _ST),
+    "qlin_lm_head_lanes_workspace_size": ([_I, _I], _SZ),
+    "qlin_lm_head_lanes": ([_P, _P, _I, _I, _I, _P, _P, _P, _SZ, _P], _ST),
+    "qlin_lm_head_lanes_status": ([_P, _P], _ST),
     "decode_lanes_t158_workspace_size": ([ctypes.POINTER(T158ModelC), _I, ctypes.POINTER(_SZ)], _ST),
     "decode_lanes_t158": ([ctypes.POINTER(T158ModelC), _P, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _I, _P], _ST),
     "decode_lanes_t158_launches": ([ctypes.POINTER(T158ModelC), _I], _I),
@@ -342,3 +345,17 @@ def decode_lanes_t158_launches(model: T158ModelC, n_lanes: int) -> int:
 
 def decode_lanes_t158_status(workspace, stream=None):
     _check("decode_lanes_t158_status", lib().decode_lanes_t158_status(_ptr(workspace), _stream(stream)))
+
+
+def qlin_lm_head_lanes_workspace_size(vocab, dim) -> int:
+    return int(lib().qlin_lm_head_lanes_workspace_size(vocab, dim))
+
+
+def qlin_lm_head_lanes(emb, x, vocab, dim, n_lanes, logits, next_tokens, workspace, workspace_bytes, stream=None):
+    _check("qlin_lm_head_lanes", lib().qlin_lm_head_lanes(_ptr(emb), _ptr(x), vocab, dim, n_lanes, _ptr(logits),
+                                                          _ptr(next_tokens), _ptr(workspace), workspace_bytes,
+                                                          _stream(stream)))
+
+
+def qlin_lm_head_lanes_status(workspace, stream=None):
+    _check("qlin_lm_head_lanes_status", lib().qlin_lm_head_lanes_status(_ptr(workspace), _stream(stream)))
