@@ -91,16 +91,21 @@ __device__ __forceinline__ LaneAttnWs lane_attn_ws(float *base, int lane, int nc
     return w;
 }
 
-// grid (ncmax, nkv, lanes): chunk c of KV head g of lane i, for every query head
-// of the group (the chunk's k and v rows are read once into shared memory and
-// serve all nh / nkv heads); chunks past the lane's position exit.
-__global__ void __launch_bounds__(256) lanes_attn_chunk_kernel(const float *__restrict__ q, const float *__restrict__ kv,
-                                                               const int32_t *pos, const int32_t *seq, int n_seqs,
-                                                               int layer, int L, int max_pos, int nh, int nkv, int hd,
-                                                               float *ws, int ncmax) {
+constexpr int kAttnGroupThreads = 128;  // threads per query head in the chunk kernel
+constexpr int kAttnMaxGroups = 8;        // query heads served at once (1024 threads)
+
+// grid (ncmax, nkv, lanes), block hpar * 128 threads: chunk c of KV head g of
+// lane i for every query head of the group.  The chunk's k and v rows are
+// read once into shared memory (16-byte loads); hpar heads then run at once,
+// each on its own 128 threads and hardware barrier.  Chunks past the lane's
+// position exit.
+__global__ void __launch_bounds__(kAttnGroupThreads * kAttnMaxGroups)
+    lanes_attn_chunk_kernel(const float *__restrict__ q, const float *__restrict__ kv, const int32_t *pos,
+                            const int32_t *seq, int n_seqs, int layer, int L, int max_pos, int nh, int nkv, int hd,
+                            float *ws, int ncmax) {
     extern __shared__ __align__(16) float kvs[];  // [32][hd] k rows, then [32][hd] v rows
-    __shared__ float qs[256];
-    __shared__ float sc[32];
+    __shared__ float qs[kAttnMaxGroups][256];
+    __shared__ float sc[kAttnMaxGroups][32];
     const int c = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
     const int p = pos[i], s = seq[i];
     if (!lane_ok(p, s, max_pos, n_seqs) || c * 32 > p) return;
@@ -110,19 +115,26 @@ __global__ void __launch_bounds__(256) lanes_attn_chunk_kernel(const float *__re
     const float *kc = kv + (((int64_t)s * L + layer) * 2 + 0) * max_pos * ld + (int64_t)t0 * ld + kvh * hd;
     const float *vc = kc + (int64_t)max_pos * ld;
     float *Ks = kvs, *Vs = kvs + 32 * hd;
-    for (int e = threadIdx.x; e < nt * hd; e += blockDim.x) {
-        const int t = e / hd, dd = e - t * hd;
-        Ks[e] = kc[(int64_t)t * ld + dd];
-        Vs[e] = vc[(int64_t)t * ld + dd];
+    const int hd4 = hd / 4;
+    for (int e = threadIdx.x; e < nt * hd4; e += blockDim.x) {
+        const int t = e / hd4, dd = e - t * hd4;
+        reinterpret_cast<float4 *>(Ks)[e] = *reinterpret_cast<const float4 *>(kc + (int64_t)t * ld + 4 * dd);
+        reinterpret_cast<float4 *>(Vs)[e] = *reinterpret_cast<const float4 *>(vc + (int64_t)t * ld + 4 * dd);
     }
     LaneAttnWs w = lane_attn_ws(ws, i, ncmax, nh, hd);
-    const int grp = nh / nkv;
-    for (int h = kvh * grp; h < (kvh + 1) * grp; h++) {
-        __syncthreads();  // the k/v rows are in; the previous head is done with qs
-        for (int e = threadIdx.x; e < hd; e += blockDim.x) qs[e] = q[((int64_t)i * nh + h) * hd + e];
+    const int grp = nh / nkv, hpar = blockDim.x / kAttnGroupThreads;
+    const int gi = threadIdx.x / kAttnGroupThreads;
+    const Grp g{(int)threadIdx.x - gi * kAttnGroupThreads, kAttnGroupThreads, 1 + gi};
+    for (int h0 = 0; h0 < grp; h0 += hpar) {
+        __syncthreads();  // the k/v rows are in; the previous round is done with qs
+        const int h = kvh * grp + h0 + gi;
+        const bool active = h0 + gi < grp;
+        if (active)
+            for (int e = g.tid; e < hd; e += g.n) qs[gi][e] = q[((int64_t)i * nh + h) * hd + e];
         __syncthreads();
-        attention_chunk(qs, Ks, Vs, hd, nt, hd, w.m + h * ncmax + c, w.S + h * ncmax + c,
-                        w.U + ((int64_t)h * ncmax + c) * hd, sc, whole_block());
+        if (active)
+            attention_chunk(qs[gi], Ks, Vs, hd, nt, hd, w.m + h * ncmax + c, w.S + h * ncmax + c,
+                            w.U + ((int64_t)h * ncmax + c) * hd, sc[gi], g);
     }
 }
 
@@ -251,6 +263,7 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     auto quant = [&](const float *x, int K) { return qlin_quant_i8(x, w.xq, w.xs, M, K, stream); };
     const int add_blocks = std::max(1, std::min(4 * sm_count(), (int)(((int64_t)M * d + 255) / 256)));
     const size_t attn_smem = (size_t)2 * 32 * hd * sizeof(float);
+    const int attn_threads = kAttnGroupThreads * std::min(kAttnMaxGroups, nh / nkv);
     if (attn_smem > 48 * 1024) blocks_per_sm((const void *)lanes_attn_chunk_kernel, attn_smem);  // raises the limit once
 
     lanes_embed_kernel<<<M, 256, 0, s>>>(m->emb, m->vocab, d, tokens, w.h, w.status);
@@ -263,7 +276,7 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
             w.q, w.k, w.v, kv_caches, positions, seqs, n_seqs, l, L, m->max_pos, m->rope_cos, m->rope_sin, nh, nkv,
             hd, w.status);
         QLIN_LAUNCHED("lanes_rope_kv_kernel");
-        lanes_attn_chunk_kernel<<<dim3(ncmax, nkv, M), 256, attn_smem, s>>>(w.q, kv_caches, positions, seqs, n_seqs,
+        lanes_attn_chunk_kernel<<<dim3(ncmax, nkv, M), attn_threads, attn_smem, s>>>(w.q, kv_caches, positions, seqs, n_seqs,
                                                                              l, L, m->max_pos, nh, nkv, hd, w.attn,
                                                                              ncmax);
         QLIN_LAUNCHED("lanes_attn_chunk_kernel");
