@@ -46,7 +46,7 @@ def parse():
     p.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
     p.add_argument("--workload", choices=["decode"], default="decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--kernel", choices=["sketch_head", "decode_steps"], default=None,
+    p.add_argument("--kernel", choices=["sketch_head", "decode_steps", "lanes_steps"], default=None,
                    help="time one kernel alone on its full-size synthetic inputs (for profiling); no JSON bench line")
     return p.parse_args()
 
@@ -253,9 +253,10 @@ def run_decode(args, rank, local, world):
     peak, peak_kind = peaks()
     lm_gbs = lm_alg / (lm_ms / 1e3) / 1e9
     sketch = sketch_decode(gpu, cfg, args, stream, lm_ms, peak)
+    lanes = lanes_decode(gpu, cfg, stream, tok_s)
     gemv = gemv_m1(dev, stream)
     prefill = prefill_m512(dev, stream)
-    lanes = lanes_t158(dev, stream)
+    lanes_gemm = lanes_t158(dev, stream)
     step_gbs = step_bytes * args.steps / (ms / 1e3) / 1e9
     traffic = fused_traffic()
     launches_per_step = qlin.decode_step_t158_launches(gpu.model)
@@ -289,9 +290,10 @@ def run_decode(args, rank, local, world):
             "frac_of_peak": round(step_bytes * args.steps / (ms / 1e3) / 1e9 / peak, 4),
         },
         "sketch_head": sketch,
+        "lanes_decode": lanes,
         "gemv_m1": gemv,
         "prefill_m512": prefill,
-        "lanes_t158": lanes,
+        "lanes_t158": lanes_gemm,
         # the step is one launch of the fused kernel: its algorithmic bytes over
         # its CUDA-event time on the launching stream
         "roofline": {
@@ -374,6 +376,64 @@ def sketch_decode(gpu, cfg, args, stream, lm_ms, peak):
         "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
         "algorithmic_bytes": alg,
     }
+
+
+def lanes_decode(gpu, cfg, stream, single_tok_s):
+    """Many users at once: one decode step over U lanes (one token of each of U
+    sequences at context 1024), captured in a CUDA graph and replayed; tokens/s
+    = U / step time, against the single-user fused step."""
+    import torch
+
+    users = (1, 2, 4, 8, 16, 32, 64)
+    U_MAX = users[-1]
+    gpu.prepare_lanes(n_seqs=U_MAX, max_lanes=U_MAX)
+    kv0 = gpu.kv[:, :, :, :].clone()  # the bench's cache: filled to 1024 by the decode run
+    for s in range(U_MAX):
+        gpu.kv_lanes[s].copy_(kv0)
+    gpu.lane_seq.copy_(torch.arange(U_MAX, dtype=torch.int32))
+    gpu.lane_tokens.fill_(int(gpu.token.item()))
+    gpu.lane_pos.fill_(POS0)
+    rows = []
+    for U in users:
+        gpu.step_lanes(U, stream=stream)
+        torch.cuda.synchronize()
+        gpu.check_lanes_status()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                gpu.step_lanes(U, stream=cap)
+        torch.cuda.current_stream().wait_stream(cap)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        n = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        rows.append((U, ms))
+        del g
+    gpu.check_lanes_status()
+    del gpu.kv_lanes, gpu.lanes_workspace
+    torch.cuda.empty_cache()
+    return {
+        "users": [u for u, _ in rows], "ms_per_step": [round(ms, 4) for _, ms in rows],
+        "tokens_per_s": [round(u / ms * 1e3, 1) for u, ms in rows],
+        "vs_single_user_fused_step": [round(u / ms * 1e3 / single_tok_s, 2) for u, ms in rows],
+        "timing": "CUDA graph of one lanes step, 20 replays; every user at context 1024",
+        "launches_per_step": [qlin_launches(gpu, u) for u, _ in rows],
+    }
+
+
+def qlin_launches(gpu, U):
+    from weight_streaming_gemv_gb300 import qlin
+
+    return qlin.decode_lanes_t158_launches(gpu.model, U)
 
 
 def gemv_m1(dev, stream):
@@ -596,6 +656,27 @@ def kernel_only(name):
     from weight_streaming_gemv_gb300 import qlin
 
     dev = torch.device("cuda", 0)
+    if name == "lanes_steps":
+        # three steps of 64 lanes (64 users at context 1024) of the Gemma-shaped decoder
+        from weight_streaming_gemv_gb300.decoder import T158Decoder
+
+        cfg = decode_cfg(3, 0)
+        gpu = T158Decoder(cfg, synth.decoder_weights(cfg, seed=SEED), device=dev)
+        U = 64
+        gpu.prepare_lanes(n_seqs=U, max_lanes=U)
+        kv0 = torch.from_numpy(synth.kv_fill(cfg, SEED, POS0)).to(dev)
+        for s in range(U):
+            gpu.kv_lanes[s].copy_(kv0)
+        gpu.lane_seq.copy_(torch.arange(U, dtype=torch.int32))
+        gpu.lane_tokens.copy_(torch.from_numpy(synth.prompt_ids(SEED, U, cfg.vocab)))
+        for i in range(3):
+            gpu.lane_pos.fill_(POS0 + i)
+            gpu.step_lanes(U)
+            gpu.lane_tokens.copy_(gpu.lane_next)
+        torch.cuda.synchronize()
+        gpu.check_lanes_status()
+        print(json.dumps({"kernel": name, "next0": int(gpu.lane_next[0].item())}))
+        return 0
     if name == "decode_steps":
         # six exact steps and six sketch-head steps of the Gemma-shaped decoder at context 1024
         from weight_streaming_gemv_gb300.decoder import T158Decoder
