@@ -66,6 +66,8 @@ def _L():
                 "or_w8g_linear": ([p, p, i64, p, i64, i64, i64, i64, i64, p], ctypes.c_int),
                 "or_t158_pack": ([p, i64, i64, p, i64], ctypes.c_int),
                 "or_t158_unpack": ([p, i64, i64, i64, p], ctypes.c_int),
+                "or_t158_pack_groups": ([p, i64, i64, p, i64], ctypes.c_int),
+                "or_t158_unpack_groups": ([p, i64, i64, i64, p], ctypes.c_int),
                 "or_t158_linear": ([p, p, p, i64, f32, i64, i64, i64, p, p], ctypes.c_int),
                 "or_psum_f32": ([p, i64], f32),
                 "or_exp_f32": ([f32], f32),
@@ -167,6 +169,26 @@ def t158_pack(trits: np.ndarray, pitch: int | None = None):
     out = np.empty((N, pitch), np.uint8)
     _check(_L().or_t158_pack(_p(t), N, K, _p(out), pitch), "t158_pack")
     return out
+
+
+def t158_pack_groups(trits: np.ndarray, gpitch: int | None = None):
+    """Group-major packing for zero-group skipping: [ceil(K/4)][gpitch] bytes."""
+    t = np.ascontiguousarray(trits, np.int8)
+    N, K = t.shape
+    gpitch = N if gpitch is None else gpitch
+    out = np.empty(((K + 3) // 4, gpitch), np.uint8)
+    _check(_L().or_t158_pack_groups(_p(t), N, K, _p(out), gpitch), "t158_pack_groups")
+    return out
+
+
+def t158_unpack_groups(packed_g: np.ndarray, N: int, K: int):
+    pk = np.ascontiguousarray(packed_g, np.uint8)
+    t = np.empty((N, K), np.int8)
+    rc = _L().or_t158_unpack_groups(_p(pk), N, K, pk.shape[1], _p(t))
+    if rc == EBADBYTE:
+        raise ValueError("t158_unpack_groups: byte above 80")
+    _check(rc, "t158_unpack_groups")
+    return t
 
 
 def t158_unpack(packed: np.ndarray, K: int):

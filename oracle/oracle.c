@@ -188,6 +188,46 @@ int or_t158_unpack(const uint8_t *packed, int64_t N, int64_t K, int64_t pitch, i
     return OR_OK;
 }
 
+/* Zero-group skipping ([citric] "What is next": a kernel that skips groups of
+ * four zero inputs).  Its weights are stored by input group: group g holds
+ * inputs 4g .. 4g+3, and row n of the group is one byte, sum_i (t[n][4g+i]+1)
+ * * 3^i (least significant digit first, as the five-trit bytes; trits past K
+ * are zero trits, digit 1), so one input group's weights are the gpitch
+ * contiguous bytes [g][0 .. gpitch) and a zero group's bytes are never read.
+ * Bytes of rows gpitch > n >= N are 40 (four zero trits).  The page gives no
+ * layout; this is the plainest one in which skipping a group skips its bytes.
+ * The linear layer itself is the T158 linear below: leaving out zero inputs
+ * changes no sum.
+ */
+int or_t158_pack_groups(const int8_t *t, int64_t N, int64_t K, uint8_t *packed_g, int64_t gpitch) {
+    if (!t || !packed_g || N < 1 || K < 1 || gpitch < N) return OR_EINVAL;
+    for (int64_t i = 0; i < N * K; i++)
+        if (t[i] < -1 || t[i] > 1) return OR_EINVAL;
+    const int64_t G = (K + 3) / 4;
+    for (int64_t g = 0; g < G; g++)
+        for (int64_t n = 0; n < gpitch; n++) {
+            int32_t byte = 0;
+            for (int i = 0; i < 4; i++) {
+                const int64_t k = 4 * g + i;
+                const int32_t digit = (n < N && k < K) ? (int32_t)t[n * K + k] + 1 : 1;
+                byte += digit * POW3[i];
+            }
+            packed_g[g * gpitch + n] = (uint8_t)byte;
+        }
+    return OR_OK;
+}
+
+int or_t158_unpack_groups(const uint8_t *packed_g, int64_t N, int64_t K, int64_t gpitch, int8_t *t) {
+    if (!packed_g || !t || N < 1 || K < 1 || gpitch < N) return OR_EINVAL;
+    const int64_t G = (K + 3) / 4;
+    for (int64_t g = 0; g < G; g++)
+        for (int64_t n = 0; n < N; n++)
+            if (packed_g[g * gpitch + n] > 80) return OR_EBADBYTE;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++) t[n * K + k] = (int8_t)trit_of(packed_g[(k / 4) * gpitch + n], (int)(k % 4));
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------ S4 / S6
  * T158 linear: acc[m][n] = sum_k trit[n][k] * xq[m][k], exact integer
  * arithmetic ([citric] "Step 1": results do not depend on thread count or

@@ -200,3 +200,34 @@ def test_w8_linear_pitch():
     qp[:, :40] = q
     qp[:, 40:] = 99  # padding is never read
     np.testing.assert_array_equal(oracle.w8_linear(d["x"], qp, s, K=40), oracle.w8_linear(d["x"], q, s))
+
+
+# ---------------------------------------------------------------- zero-group skipping layout
+def test_group_pack_hand_worked():
+    # one row, K = 6: groups (-1, 0, 1, 1) and (1, -1, pad, pad)
+    t = np.array([[-1, 0, 1, 1, 1, -1]], np.int8)
+    g = oracle.t158_pack_groups(t, gpitch=3)
+    # digits (0, 1, 2, 2) -> 0 + 3 + 18 + 54 = 75; (2, 0, 1, 1) -> 2 + 0 + 9 + 27 = 38; rows past N: 40
+    np.testing.assert_array_equal(g, np.array([[75, 40, 40], [38, 40, 40]], np.uint8))
+
+
+def test_group_pack_all_81_patterns_round_trip():
+    pats = np.array([[((v // 3 ** i) % 3) - 1 for i in range(4)] for v in range(81)], np.int8)  # [81][4]
+    g = oracle.t158_pack_groups(pats)  # one group, 81 rows
+    np.testing.assert_array_equal(g[0], np.arange(81, dtype=np.uint8))
+    np.testing.assert_array_equal(oracle.t158_unpack_groups(g, 81, 4), pats)
+
+
+@pytest.mark.parametrize("N,K", [(7, 13), (64, 1152), (5, 4)])
+def test_group_pack_round_trip_and_five_trit_agreement(N, K):
+    t = synth.trits(40, 0, (N, K))
+    g = oracle.t158_pack_groups(t, gpitch=N + 9)
+    np.testing.assert_array_equal(oracle.t158_unpack_groups(g, N, K), t)
+    np.testing.assert_array_equal(oracle.t158_unpack(oracle.t158_pack(t), K), t)  # the same trits either way
+    assert (g[:, N:] == 40).all()
+
+
+def test_group_unpack_rejects_bytes_above_80():
+    g = np.full((1, 2), 81, np.uint8)
+    with pytest.raises(ValueError):
+        oracle.t158_unpack_groups(g, 2, 4)
