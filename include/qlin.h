@@ -114,6 +114,25 @@ qlin_status qlin_quant_i8(const float *x, int8_t *xq, float *x_scale, int M, int
 qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *w_packed, int64_t w_pitch,
                          float w_scale, float *y, int32_t *acc, int M, int N, int K, qlin_stream_t stream);
 
+/* T158 linear for one token that skips groups of four zero inputs ([citric]
+ * "What is next": a kernel that skips groups of 4 zero inputs).  Same acc and
+ * y as qlin_t158_i8 with M = 1, from weights stored by input group:
+ * t158_pack_groups writes w_groups uint8 [ceil(K/4)][gpitch], byte [g][n] =
+ * sum_i (trit[n][4g+i] + 1) * 3^i (trits past K zero; rows N .. gpitch-1 the
+ * byte 40), so the weights of one input group are gpitch contiguous bytes and
+ * a group of four zero codes costs no weight bytes.  gpitch >= N, a multiple
+ * of 16 (t158_group_pitch(N)); w_groups 16-byte aligned; xq device int8 [K]
+ * and x_scale device fp32 [1], 4-byte aligned.  K <= 65536.  Workspace:
+ * qlin_t158_skip_workspace_size(N) bytes, zero-filled before first use; calls
+ * leave it ready; calls sharing it must not overlap.  Bytes above 80 give
+ * unspecified but memory-safe results. */
+int64_t t158_group_pitch(int64_t N);
+qlin_status t158_pack_groups(const int8_t *trits, int64_t N, int64_t K, uint8_t *w_groups, int64_t gpitch);
+size_t qlin_t158_skip_workspace_size(int N);
+qlin_status qlin_t158_i8_skip(const int8_t *xq, const float *x_scale, const uint8_t *w_groups, int64_t gpitch,
+                              float w_scale, float *y, int32_t *acc, int N, int K, void *workspace,
+                              size_t workspace_bytes, qlin_stream_t stream);
+
 /* ========================================================================
  * S5  W8 linear: y[m][n] = (sum_k x[m][k] * w8[n][k]) * w_scale, fp32
  * activations, the scale applied once after the dot product

@@ -65,6 +65,14 @@ def test_pack_matches_oracle_bytes(K):
     np.testing.assert_array_equal(qlin.t158_unpack(qlin.t158_pack(t, pitch), K), t)
 
 
+@pytest.mark.parametrize("N,K", [(9, 13), (33, 1152), (6, 4)])
+def test_group_pack_matches_oracle_bytes(N, K):
+    t = synth.trits(31, K, (N, K))
+    gp = qlin.t158_group_pitch(N)
+    assert gp % 16 == 0 and gp >= N
+    np.testing.assert_array_equal(qlin.t158_pack_groups(t, gp), oracle.t158_pack_groups(t, gp))
+
+
 def test_unpack_rejects_bytes_above_242():
     pk = np.full((2, 16), 121, np.uint8)
     pk[1, 15] = 243  # in the filler

@@ -134,6 +134,31 @@ qlin_status t158_pack(const int8_t *trits, int64_t N, int64_t K, uint8_t *packed
     return QLIN_OK;
 }
 
+int64_t t158_group_pitch(int64_t N) { return N < 1 ? 0 : (N + 15) / 16 * 16; }
+
+qlin_status t158_pack_groups(const int8_t *trits, int64_t N, int64_t K, uint8_t *packed_g, int64_t gpitch) {
+    qlin::clear_error();
+    QLIN_REQUIRE(trits && packed_g, QLIN_ERR_INVALID_ARG, "t158_pack_groups: null pointer");
+    QLIN_REQUIRE(N >= 1 && K >= 1, QLIN_ERR_INVALID_ARG, "t158_pack_groups: N=%lld K=%lld", (long long)N,
+                 (long long)K);
+    QLIN_REQUIRE(gpitch >= N, QLIN_ERR_INVALID_ARG, "t158_pack_groups: gpitch %lld < N", (long long)gpitch);
+    for (int64_t i = 0; i < N * K; i++)
+        QLIN_REQUIRE(trits[i] >= -1 && trits[i] <= 1, QLIN_ERR_INVALID_ARG, "t158_pack_groups: trit %d at %lld",
+                     (int)trits[i], (long long)i);
+    const int64_t G = (K + 3) / 4;
+    for (int64_t g = 0; g < G; g++) {
+        uint8_t *dst = packed_g + g * gpitch;
+        for (int64_t n = 0; n < N; n++) {
+            const int8_t *t = trits + n * K + 4 * g;
+            int v = 0, p3 = 1;
+            for (int i = 0; i < 4; i++, p3 *= 3) v += p3 * (4 * g + i < K ? t[i] + 1 : 1);
+            dst[n] = (uint8_t)v;
+        }
+        for (int64_t n = N; n < gpitch; n++) dst[n] = 40;  // four zero trits
+    }
+    return QLIN_OK;
+}
+
 qlin_status t158_unpack(const uint8_t *packed, int64_t N, int64_t K, int64_t pitch, int8_t *trits) {
     qlin::clear_error();
     QLIN_REQUIRE(trits && packed, QLIN_ERR_INVALID_ARG, "t158_unpack: null pointer");

@@ -92,6 +92,10 @@ SIGNATURES = {
                                                 ctypes.POINTER(_SZ)], _ST),
     "decode_step_t158_sketch": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(T158SketchC), _P, _P, _SZ, _P,
                                  ctypes.c_int32, _P, _P], _ST),
+    "t158_group_pitch": ([_I64], _I64),
+    "t158_pack_groups": ([_P, _I64, _I64, _P, _I64], _ST),
+    "qlin_t158_skip_workspace_size": ([_I], _SZ),
+    "qlin_t158_i8_skip": ([_P, _P, _P, _I64, _F, _P, _P, _I, _I, _P, _SZ, _P], _ST),
     "qlin_lm_head_lanes_workspace_size": ([_I, _I], _SZ),
     "qlin_lm_head_lanes": ([_P, _P, _I, _I, _I, _P, _P, _P, _SZ, _P], _ST),
     "qlin_lm_head_lanes_status": ([_P, _P], _ST),
@@ -359,3 +363,27 @@ def qlin_lm_head_lanes(emb, x, vocab, dim, n_lanes, logits, next_tokens, workspa
 
 def qlin_lm_head_lanes_status(workspace, stream=None):
     _check("qlin_lm_head_lanes_status", lib().qlin_lm_head_lanes_status(_ptr(workspace), _stream(stream)))
+
+
+def t158_group_pitch(N: int) -> int:
+    return int(lib().t158_group_pitch(N))
+
+
+def t158_pack_groups(trits, gpitch=None):
+    """Host packing by input group (for qlin_t158_i8_skip): [ceil(K/4)][gpitch] uint8."""
+    t = np.ascontiguousarray(trits, np.int8)
+    N, K = t.shape
+    gpitch = t158_group_pitch(N) if gpitch is None else gpitch
+    out = np.empty(((K + 3) // 4, gpitch), np.uint8)
+    _check("t158_pack_groups", lib().t158_pack_groups(t.ctypes.data, N, K, out.ctypes.data, gpitch))
+    return out
+
+
+def qlin_t158_skip_workspace_size(N) -> int:
+    return int(lib().qlin_t158_skip_workspace_size(N))
+
+
+def qlin_t158_i8_skip(xq, x_scale, w_groups, gpitch, w_scale, y, acc, N, K, workspace, workspace_bytes, stream=None):
+    _check("qlin_t158_i8_skip", lib().qlin_t158_i8_skip(_ptr(xq), _ptr(x_scale), _ptr(w_groups), gpitch, w_scale,
+                                                        _ptr(y), _ptr(acc), N, K, _ptr(workspace), workspace_bytes,
+                                                        _stream(stream)))
