@@ -493,7 +493,56 @@ def gemv_m1(dev, stream):
     res["w8g128_k4096_n11008"] = _time_rotating(w8g, R, alg, stream)
     del ws, scs
     torch.cuda.empty_cache()
+    res["zero_skip"] = zero_skip(dev, stream, l2)
     return res
+
+
+def zero_skip(dev, stream, l2):
+    """T158 M = 1 with 80% of the input groups of four zero: the dense kernel on the
+    five-trit layout against the kernel that skips zero groups on the group-major
+    layout, both over rotating weight copies (>= 4x L2) in a CUDA graph."""
+    import torch
+
+    import synth
+    from weight_streaming_gemv_gb300 import qlin
+
+    out = {}
+    for K, N in ((1152, 6912), (6912, 1152), (16384, 16384)):
+        d = synth.t158_gemv(5, 1, K, N)
+        x = d["x"].copy()
+        G = (K + 3) // 4
+        keep = synth.uniform_f32(5, 9, (G,), 0.0, 1.0) >= 0.8
+        x[0, :] *= np.repeat(keep, 4)[:K]
+        xd = torch.from_numpy(x).to(dev)
+        xq = torch.empty((1, K), dtype=torch.int8, device=dev)
+        xs = torch.empty(1, dtype=torch.float32, device=dev)
+        qlin.qlin_quant_i8(xd, xq, xs, 1, K)
+        y = torch.empty((1, N), dtype=torch.float32, device=dev)
+        pitch = qlin.t158_pitch(K)
+        w1 = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+        R = int(np.ceil(4 * l2 / w1.numel()))
+        wd = w1.repeat(R, 1)
+        dense = _time_rotating(lambda r: qlin.qlin_t158_i8(xq, xs, wd[r * N], pitch, d["w_scale"], y, None, 1, N, K),
+                               R, N * ((K + 4) // 5) + K + 8 + 4 * N, stream)
+        del wd
+        gp = qlin.t158_group_pitch(N)
+        g1 = torch.from_numpy(qlin.t158_pack_groups(d["trits"], gp)).to(dev)
+        Rg = int(np.ceil(4 * l2 / g1.numel()))
+        wg = g1.repeat(Rg, 1)
+        wsb = qlin.qlin_t158_skip_workspace_size(N)
+        wsk = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+        nnz = int(keep.sum())
+        skip = _time_rotating(lambda r: qlin.qlin_t158_i8_skip(xq, xs, wg[r * G], gp, d["w_scale"], y, None, N, K,
+                                                                wsk, wsb), Rg, nnz * N + K + 8 + 4 * N, stream)
+        del wg
+        out[f"t158_k{K}_n{N}"] = {
+            "nonzero_groups": nnz, "groups": G,
+            "dense_us": dense["us_per_call"], "skip_us": skip["us_per_call"],
+            "speedup": round(dense["us_per_call"] / skip["us_per_call"], 2),
+            "skip_weight_bytes_read": nnz * N, "dense_weight_bytes_read": N * ((K + 4) // 5),
+        }
+    torch.cuda.empty_cache()
+    return out
 
 
 def _time_rotating(fn, R, alg_bytes, stream):

@@ -36,9 +36,8 @@ __global__ void __launch_bounds__(kSkThreads) t158_skip_kernel(const int8_t *__r
     uint32_t *xg = sk_dyn;                                        // [G] the listed groups' four codes
     uint16_t *list = reinterpret_cast<uint16_t *>(sk_dyn + G);  // [G] the nonzero groups
     __shared__ uint32_t tab[256];                                 // byte -> four trits (int8 x 4)
-    __shared__ unsigned wsum[kSkThreads / 32 + 1];
     __shared__ int last;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int rb = blockIdx.x, share = blockIdx.y, shares = gridDim.y;
     const int Np = (N + 3) / 4 * 4;  // row stride of the partial sums (16-byte rows of four)
     {
@@ -46,37 +45,55 @@ __global__ void __launch_bounds__(kSkThreads) t158_skip_kernel(const int8_t *__r
         const uint32_t d0 = v % 3, d1 = (v / 3) % 3, d2 = (v / 9) % 3, d3 = (v / 27) % 3;
         tab[tid] = ((d0 - 1) & 0xffu) | (((d1 - 1) & 0xffu) << 8) | (((d2 - 1) & 0xffu) << 16) | ((d3 - 1) << 24);
     }
-    // the nonzero groups, in order
+    // the nonzero groups, in the same order in every CTA (thread by thread, then
+    // the thread's groups in turn), so that the CTAs of a row block split one list
+    __shared__ unsigned wsum[kSkThreads / 32 + 1];
+    const int lane = tid & 31, warp = tid >> 5;
     unsigned base = 0;
-    for (int g0 = 0; g0 < G; g0 += kSkThreads) {
-        const int g = g0 + tid;
-        uint32_t x4 = 0;
-        if (g < G) {
-            if (4 * g + 4 <= K) {
-                x4 = *reinterpret_cast<const uint32_t *>(xq + 4 * g);
-            } else {
-                for (int i = 0; i < 4 && 4 * g + i < K; i++) x4 |= (uint32_t)(uint8_t)xq[4 * g + i] << (8 * i);
+    for (int g0 = 0; g0 < G; g0 += 8 * kSkThreads) {
+        uint32_t x4[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) {  // every load of the round in flight
+            const int g = g0 + u * kSkThreads + tid;
+            uint32_t v = 0u;
+            if (g < G) {
+                if (4 * g + 4 <= K) {
+                    v = __ldg(reinterpret_cast<const uint32_t *>(xq + 4 * g));
+                } else {
+                    for (int i = 0; i < 4 && 4 * g + i < K; i++) v |= (uint32_t)(uint8_t)xq[4 * g + i] << (8 * i);
+                }
             }
+            x4[u] = v;
         }
-        const bool nz = x4 != 0u;
-        const unsigned b = __ballot_sync(0xffffffffu, nz);
-        if (lane == 0) wsum[warp] = __popc(b);
+        unsigned c = 0;
+#pragma unroll
+        for (int u = 0; u < 8; u++) c += x4[u] != 0u;
+        unsigned inc = c;  // inclusive scan over the threads
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned t = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += t;
+        }
+        if (lane == 31) wsum[warp] = inc;
         __syncthreads();
         if (tid == 0) {
             unsigned run = 0;
             for (int w = 0; w < kSkThreads / 32; w++) {
-                const unsigned c = wsum[w];
+                const unsigned t = wsum[w];
                 wsum[w] = run;
-                run += c;
+                run += t;
             }
             wsum[kSkThreads / 32] = run;
         }
         __syncthreads();
-        if (nz) {
-            const unsigned p = base + wsum[warp] + __popc(b & ((1u << lane) - 1u));
-            list[p] = (uint16_t)g;
-            xg[p] = x4;
-        }
+        unsigned p = base + wsum[warp] + inc - c;
+#pragma unroll
+        for (int u = 0; u < 8; u++)
+            if (x4[u] != 0u) {
+                list[p] = (uint16_t)(g0 + u * kSkThreads + tid);
+                xg[p] = x4[u];
+                p++;
+            }
         base += wsum[kSkThreads / 32];
         __syncthreads();
     }
@@ -89,12 +106,12 @@ __global__ void __launch_bounds__(kSkThreads) t158_skip_kernel(const int8_t *__r
     if (rows_in) {
         const uint8_t *col = wg + n0;
         int j = j0;
-        for (; j + 4 <= j1; j += 4) {
-            uint32_t w[4];
+        for (; j + 8 <= j1; j += 8) {
+            uint32_t w[8];
 #pragma unroll
-            for (int u = 0; u < 4; u++) w[u] = __ldg(reinterpret_cast<const uint32_t *>(col + (int64_t)list[j + u] * gpitch));
+            for (int u = 0; u < 8; u++) w[u] = __ldg(reinterpret_cast<const uint32_t *>(col + (int64_t)list[j + u] * gpitch));
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
+            for (int u = 0; u < 8; u++) {
                 const uint32_t x4 = xg[j + u];
                 a0 = __dp4a((int)tab[w[u] & 0xffu], (int)x4, a0);
                 a1 = __dp4a((int)tab[(w[u] >> 8) & 0xffu], (int)x4, a1);
@@ -173,8 +190,8 @@ qlin_status qlin_t158_i8_skip(const int8_t *xq, const float *x_scale, const uint
     QLIN_REQUIRE(workspace_bytes >= qlin_t158_skip_workspace_size(N), QLIN_ERR_INVALID_ARG,
                  "qlin_t158_i8_skip: workspace %zu < %zu bytes", workspace_bytes, qlin_t158_skip_workspace_size(N));
     const int rbs = (N + kSkRows - 1) / kSkRows;
-    // enough CTAs to cover the SMs twice, the groups split between them
-    const int shares = std::max(1, std::min(kSkMaxShares, 2 * sm_count() / rbs));
+    // the groups split between CTAs of a row block, about 64 groups (16 nonzero at 75% zeros) each
+    const int shares = std::max(1, std::min(kSkMaxShares, std::min(2 * sm_count() / rbs, ((K + 3) / 4 + 63) / 64)));
     unsigned *tickets = (unsigned *)workspace;
     int32_t *part = (int32_t *)((char *)workspace + align256((size_t)rbs * sizeof(unsigned)));
     const size_t smem = (size_t)6 * ((K + 3) / 4) + 16;
