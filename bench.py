@@ -46,7 +46,8 @@ def parse():
     p.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
     p.add_argument("--workload", choices=["decode"], default="decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--kernel", choices=["sketch_head", "decode_steps", "lanes_steps"], default=None,
+    p.add_argument("--kernel", choices=["sketch_head", "decode_steps", "lanes_steps", "t158_linears", "t158_calls"],
+                   default=None,
                    help="time one kernel alone on its full-size synthetic inputs (for profiling); no JSON bench line")
     return p.parse_args()
 
@@ -580,9 +581,11 @@ def _time_rotating(fn, R, alg_bytes, stream):
 
 def prefill_m512(dev, stream):
     """The two 512-token T158 layers of the prompt (1152->6912, 6912->1152) on the tensor
-    cores: each call timed alone with CUDA events after an L2 flush; dense fp16 rate
-    (2 M N K flops per call) against the measured bf16 tensor peak (fp16 and bf16 share
-    one rate)."""
+    cores through qlin_t158_i8_ws (activation tiles converted once per call, inside the
+    timed call): a CUDA graph of back-to-back calls over rotating weight copies (>= 4x L2);
+    dense fp16 rate (2 M N K flops per call) against the measured bf16 tensor peak (fp16 and
+    bf16 share one rate).  `us_no_ws`: the same through qlin_t158_i8 (activations converted
+    inside the product for every 128 weight rows)."""
     import torch
 
     import synth
@@ -594,56 +597,61 @@ def prefill_m512(dev, stream):
             tflops_peak = float(json.load(fh)["bf16_tflops"])
     except (OSError, KeyError, ValueError):
         tflops_peak = 1900.0
-    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
     res = {}
     M = 512
     for K, N in [(1152, 6912), (6912, 1152)]:
         d = synth.t158_gemv(2, M, K, N)
         pitch = qlin.t158_pitch(K)
-        w = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+        w1 = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+        R = int(np.ceil(4 * l2 / w1.numel()))
+        wr = w1.repeat(R, 1)
         x = torch.from_numpy(d["x"]).to(dev)
         xq = torch.empty((M, K), dtype=torch.int8, device=dev)
         xs = torch.empty(M, dtype=torch.float32, device=dev)
         qlin.qlin_quant_i8(x, xq, xs, M, K)
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
-        for _ in range(3):
-            qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, M, N, K)
-        times = []
-        for _ in range(20):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, M, N, K)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1) * 1e3)
-        us = statistics.median(times)
+        nb = qlin.qlin_t158_i8_workspace_size(M, K)
+        work = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+        def call_ws(r):
+            qlin.qlin_t158_i8_ws(xq, xs, wr[r * N], pitch, d["w_scale"], y, None, M, N, K, work, nb)
+
+        def call_plain(r):
+            qlin.qlin_t158_i8(xq, xs, wr[r * N], pitch, d["w_scale"], y, None, M, N, K)
+
+        us = _time_rotating(call_ws, R, 0, stream)["us_per_call"]
+        us_plain = _time_rotating(call_plain, R, 0, stream)["us_per_call"]
         tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
         res[f"t158_m{M}_k{K}_n{N}"] = {
             "us_per_call": round(us, 2), "bound": "tensor", "tflops": round(tf, 1), "peak_tflops": tflops_peak,
-            "frac": round(tf / tflops_peak, 4), "int_ops": 2 * M * N * K,
-            "timing": "median of 20 calls, each after an L2 flush"}
-        del w, x, xq, xs, y
-    del flush
+            "frac": round(tf / tflops_peak, 4), "int_ops": 2 * M * N * K, "us_no_ws": round(us_plain, 2),
+            "timing": f"CUDA graph of {R} back-to-back calls over rotating weight copies (>= 4x L2)"}
+        del w1, wr, x, xq, xs, y, work
     torch.cuda.empty_cache()
     return res
 
 
 def lanes_t158(dev, stream):
     """Many tokens through one weight pass ([citric] "Many users at once"): the T158
-    layers of the decoder at M = 1..64 tokens, each call after an L2 flush; token-rows
-    per microsecond = M / time."""
+    layers of the decoder at M = 1..64 tokens through qlin_t158_i8_ws, a CUDA graph of
+    back-to-back calls over rotating weight copies (>= 4x L2); token-rows per microsecond
+    = M / time."""
     import torch
 
     import synth
     from weight_streaming_gemv_gb300 import qlin
 
-    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
     res = {}
     for K, N in [(1152, 6912), (6912, 1152)]:
         d = synth.t158_gemv(2, 64, K, N)
         pitch = qlin.t158_pitch(K)
-        w = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+        w1 = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+        R = int(np.ceil(4 * l2 / w1.numel()))
+        wr = w1.repeat(R, 1)
         x = torch.from_numpy(d["x"]).to(dev)
         row = {"M": [], "us_per_call": [], "token_rows_per_us": []}
         for M in [1, 2, 4, 8, 16, 32, 64]:
@@ -651,24 +659,19 @@ def lanes_t158(dev, stream):
             xs = torch.empty(M, dtype=torch.float32, device=dev)
             qlin.qlin_quant_i8(x[:M].contiguous(), xq, xs, M, K)
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            for _ in range(3):
-                qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, M, N, K)
-            times = []
-            for _ in range(15):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, M, N, K)
-                e1.record(stream)
-                torch.cuda.synchronize()
-                times.append(e0.elapsed_time(e1) * 1e3)
-            us = statistics.median(times)
+            nb = qlin.qlin_t158_i8_workspace_size(M, K)
+            work = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+
+            def call(r):
+                qlin.qlin_t158_i8_ws(xq, xs, wr[r * N], pitch, d["w_scale"], y, None, M, N, K, work, nb)
+
+            us = _time_rotating(call, R, 0, stream)["us_per_call"]
             row["M"].append(M)
             row["us_per_call"].append(round(us, 2))
             row["token_rows_per_us"].append(round(M / us, 3))
+        row["timing"] = f"CUDA graph of {R} back-to-back calls over rotating weight copies (>= 4x L2)"
         res[f"t158_k{K}_n{N}"] = row
-        del w, x
-    del flush
+        del w1, wr, x
     torch.cuda.empty_cache()
     return res
 
@@ -705,6 +708,31 @@ def kernel_only(name):
     from weight_streaming_gemv_gb300 import qlin
 
     dev = torch.device("cuda", 0)
+    if name == "t158_linears":
+        # the 512-token prompt layers and the 1..64-token layers of the tensor-core T158 linear
+        stream = torch.cuda.current_stream(dev)
+        print(json.dumps({"kernel": name, "prefill_m512": prefill_m512(dev, stream),
+                          "lanes_t158": lanes_t158(dev, stream)}))
+        return 0
+    if name == "t158_calls":
+        # five plain calls of qlin_t158_i8_ws per shape (512 and 64 tokens through 1152->6912 and
+        # 6912->1152, in that order): a short launch list for the profiler
+        for M in (512, 64):
+            for K, N in [(1152, 6912), (6912, 1152)]:
+                d = synth.t158_gemv(2, M, K, N)
+                pitch = qlin.t158_pitch(K)
+                w = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+                xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+                xs = torch.empty(M, dtype=torch.float32, device=dev)
+                qlin.qlin_quant_i8(torch.from_numpy(d["x"]).to(dev), xq, xs, M, K)
+                y = torch.empty((M, N), dtype=torch.float32, device=dev)
+                nb = qlin.qlin_t158_i8_workspace_size(M, K)
+                work = torch.empty(nb, dtype=torch.uint8, device=dev)
+                for _ in range(5):
+                    qlin.qlin_t158_i8_ws(xq, xs, w, pitch, d["w_scale"], y, None, M, N, K, work, nb)
+        torch.cuda.synchronize()
+        print(json.dumps({"kernel": name}))
+        return 0
     if name == "lanes_steps":
         # three steps of 64 lanes (64 users at context 1024) of the Gemma-shaped decoder
         from weight_streaming_gemv_gb300.decoder import T158Decoder

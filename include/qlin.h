@@ -114,6 +114,20 @@ qlin_status qlin_quant_i8(const float *x, int8_t *xq, float *x_scale, int M, int
 qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *w_packed, int64_t w_pitch,
                          float w_scale, float *y, int32_t *acc, int M, int N, int K, qlin_stream_t stream);
 
+/* qlin_t158_i8 with caller scratch for the tensor-core path: the int8 codes
+ * are converted once per call into fp16 activation tiles in the workspace
+ * (one launch), instead of once per 128 weight rows inside the product.  The
+ * same acc and y, bit for bit.  workspace: device, 16-byte aligned, at least
+ * qlin_t158_i8_workspace_size(M, K) bytes (0 below the tensor-core threshold
+ * of 8 tokens, where NULL is accepted), owned by the caller, overwritten; a
+ * smaller or misaligned workspace is QLIN_ERR_INVALID_ARG.  Other arguments
+ * and ranges as qlin_t158_i8.  qlin_t158_i8_workspace_size returns 0 for M or
+ * K out of range. */
+size_t qlin_t158_i8_workspace_size(int M, int K);
+qlin_status qlin_t158_i8_ws(const int8_t *xq, const float *x_scale, const uint8_t *w_packed, int64_t w_pitch,
+                            float w_scale, float *y, int32_t *acc, int M, int N, int K, void *workspace,
+                            size_t workspace_bytes, qlin_stream_t stream);
+
 /* T158 linear for one token that skips groups of four zero inputs ([citric]
  * "What is next": a kernel that skips groups of 4 zero inputs).  Same acc and
  * y as qlin_t158_i8 with M = 1, from weights stored by input group:

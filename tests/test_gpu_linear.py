@@ -140,7 +140,8 @@ def test_w8_quantize_bit_exact(dev, N, K):
 
 
 # ---------------------------------------------------------------- S4 + S6 T158 linear
-def _t158_case(dev, M, K, N, seed, trits=None, xq=None):
+def _t158_case(dev, M, K, N, seed, trits=None, xq=None, both=True):
+    # qlin_t158_i8 and (both) qlin_t158_i8_ws against the oracle, bit for bit
     import torch
     from weight_streaming_gemv_gb300 import qlin
 
@@ -153,11 +154,20 @@ def _t158_case(dev, M, K, N, seed, trits=None, xq=None):
     acc_o, y_o = oracle.t158_linear(xq, xs, oracle.t158_pack(t), d["w_scale"], K)
     pitch = qlin.t158_pitch(K)
     w = to_dev(qlin.t158_pack(t, pitch), dev)
+    xq_d, xs_d = to_dev(xq, dev), to_dev(xs, dev)
     y = _empty((M, N), torch.float32, dev)
     acc = _empty((M, N), torch.int32, dev)
-    qlin.qlin_t158_i8(to_dev(xq, dev), to_dev(xs, dev), w, pitch, d["w_scale"], y, acc, M, N, K)
+    qlin.qlin_t158_i8(xq_d, xs_d, w, pitch, d["w_scale"], y, acc, M, N, K)
     np.testing.assert_array_equal(host(acc), acc_o)
     np.testing.assert_array_equal(host(y), y_o)
+    if both:
+        nb = qlin.qlin_t158_i8_workspace_size(M, K)
+        work = torch.full((max(nb, 16),), 0x7f, dtype=torch.uint8, device=dev)  # stale bytes must not matter
+        y = _empty((M, N), torch.float32, dev)
+        acc = _empty((M, N), torch.int32, dev)
+        qlin.qlin_t158_i8_ws(xq_d, xs_d, w, pitch, d["w_scale"], y, acc, M, N, K, work, nb)
+        np.testing.assert_array_equal(host(acc), acc_o)
+        np.testing.assert_array_equal(host(y), y_o)
 
 
 def test_t158_gemv_gate_up_shape_full_size(dev):
@@ -201,6 +211,44 @@ def test_t158_tensor_core_tiles(dev, M, K, N):
     _t158_case(dev, M, K, N, seed=11)
 
 
+@pytest.mark.parametrize("M,K,N", [(257, 333, 200), (4096, 160, 129), (40, 6912, 1152), (200, 1152, 140),
+                                   (64, 1152, 6912), (480, 240, 384)])
+def test_t158_tensor_core_token_tiles(dev, M, K, N):
+    # token tiles of 32..256 (the MMA's N), one or several per call, with and
+    # without split K, against the oracle bit for bit
+    _t158_case(dev, M, K, N, seed=13)
+
+
+def test_t158_tensor_core_extreme_operands(dev):
+    # all codes -127 / +127 against all-minus / all-plus trits: the largest
+    # partial sums the fp32 accumulator must hold exactly (127 K)
+    M, K, N = 96, 6912, 256
+    xq = np.full((M, K), 127, np.int8)
+    xq[1::2] = -127
+    t = np.ones((N, K), np.int8)
+    t[::3] = -1
+    _t158_case(dev, M, K, N, seed=14, trits=t, xq=xq)
+
+
+def test_t158_ws_rejects_small_workspace(dev):
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    M, K, N = 64, 1152, 256
+    nb = qlin.qlin_t158_i8_workspace_size(M, K)
+    # 64 tokens (one 64-token tile) x 15 steps of 80 inputs, 2 bytes each
+    assert nb == 64 * 15 * 80 * 2
+    assert qlin.qlin_t158_i8_workspace_size(4, K) == 0  # CUDA-core path: no scratch
+    assert qlin.qlin_t158_i8_workspace_size(0, K) == 0 and qlin.qlin_t158_i8_workspace_size(M, 131072) == 0
+    xq = torch.zeros((M, K), dtype=torch.int8, device=dev)
+    xs = torch.ones(M, dtype=torch.float32, device=dev)
+    w = torch.zeros((N, qlin.t158_pitch(K)), dtype=torch.uint8, device=dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    work = torch.empty(nb, dtype=torch.uint8, device=dev)
+    with pytest.raises(qlin.QlinError):
+        qlin.qlin_t158_i8_ws(xq, xs, w, qlin.t158_pitch(K), 1.0, y, None, M, N, K, work, nb - 16)
+
+
 def test_t158_tensor_core_unaligned_x_acc_only(dev):
     import torch
     from weight_streaming_gemv_gb300 import qlin
@@ -215,6 +263,12 @@ def test_t158_tensor_core_unaligned_x_acc_only(dev):
     buf[1:] = to_dev(xq_o.reshape(-1), dev)
     acc = _empty((M, N), torch.int32, dev)
     qlin.qlin_t158_i8(buf[1:], to_dev(xs_o, dev), w, pitch, d["w_scale"], None, acc, M, N, K)
+    np.testing.assert_array_equal(host(acc), acc_o)
+    # the same through the activation-tile conversion (byte loads: neither aligned nor K % 16 == 0)
+    nb = qlin.qlin_t158_i8_workspace_size(M, K)
+    work = torch.empty(nb, dtype=torch.uint8, device=dev)
+    acc = _empty((M, N), torch.int32, dev)
+    qlin.qlin_t158_i8_ws(buf[1:], to_dev(xs_o, dev), w, pitch, d["w_scale"], None, acc, M, N, K, work, nb)
     np.testing.assert_array_equal(host(acc), acc_o)
 
 

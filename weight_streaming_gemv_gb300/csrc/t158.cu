@@ -214,9 +214,13 @@ static qlin_status dispatch_mt(const int8_t *xq, const float *xs, const uint8_t 
 // time hardly depends on M, and from about 8 tokens it beats the CUDA-core
 // kernel on the Gemma-3-1B shapes (1152 -> 6912 and 6912 -> 1152).
 constexpr int kTensorCoreMinM = 8;
+// work: null, or scratch of t158_tc_workspace_bytes(M, K) bytes for the
+// activation tiles; convert: write them from xq first (false: they already
+// hold this xq's tiles, written by an earlier call with the same M and K).
 qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
                                      const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K,
-                                     cudaStream_t st);
+                                     cudaStream_t st, void *work, bool convert);
+size_t t158_tc_workspace_bytes(int M, int K);
 
 qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
                                    const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st) {
@@ -227,12 +231,17 @@ qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint
 }
 
 // T158 linear for M tokens with the weight scale in device memory (the decode
-// paths keep the model's scales on the device): the same dispatch as qlin_t158_i8.
+// paths keep the model's scales on the device): the same dispatch as
+// qlin_t158_i8, with the activation-tile scratch of t158_linear_tensor_cores.
 qlin_status t158_linear_dev_scale(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch,
-                                  const float *ws_ptr, float *y, int M, int N, int K, cudaStream_t st) {
-    if (M >= kTensorCoreMinM) return t158_linear_tensor_cores(xq, xs, w, pitch, 0.0f, ws_ptr, y, nullptr, M, N, K, st);
+                                  const float *ws_ptr, float *y, int M, int N, int K, cudaStream_t st, void *work,
+                                  bool convert) {
+    if (M >= kTensorCoreMinM)
+        return t158_linear_tensor_cores(xq, xs, w, pitch, 0.0f, ws_ptr, y, nullptr, M, N, K, st, work, convert);
     return t158_linear_cuda_cores(xq, xs, w, pitch, 0.0f, ws_ptr, y, nullptr, M, N, K, st);
 }
+
+size_t t158_workspace_bytes(int M, int K) { return M >= kTensorCoreMinM ? t158_tc_workspace_bytes(M, K) : 0; }
 
 }  // namespace qlin
 
@@ -260,7 +269,36 @@ qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *
                  M, K);
     if (M >= qlin::kTensorCoreMinM)
         return qlin::t158_linear_tensor_cores(xq, x_scale, w_packed, w_pitch, w_scale, nullptr, y, acc, M, N, K,
-                                              (cudaStream_t)stream);
+                                              (cudaStream_t)stream, nullptr, false);
+    return qlin::t158_linear_cuda_cores(xq, x_scale, w_packed, w_pitch, w_scale, nullptr, y, acc, M, N, K,
+                                        (cudaStream_t)stream);
+}
+
+size_t qlin_t158_i8_workspace_size(int M, int K) {
+    if (M < 1 || K < 1 || M > 4096 || K > 131071) return 0;
+    return qlin::t158_workspace_bytes(M, K);
+}
+
+qlin_status qlin_t158_i8_ws(const int8_t *xq, const float *x_scale, const uint8_t *w_packed, int64_t w_pitch,
+                            float w_scale, float *y, int32_t *acc, int M, int N, int K, void *workspace,
+                            size_t workspace_bytes, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(xq && x_scale && w_packed && (y || acc), QLIN_ERR_INVALID_ARG, "qlin_t158_i8_ws: null pointer");
+    QLIN_REQUIRE(M >= 1 && N >= 1 && K >= 1, QLIN_ERR_INVALID_ARG, "qlin_t158_i8_ws: M=%d N=%d K=%d", M, N, K);
+    QLIN_REQUIRE(w_pitch % 16 == 0 && w_pitch >= (K + 4) / 5, QLIN_ERR_INVALID_ARG,
+                 "qlin_t158_i8_ws: w_pitch %lld must be a multiple of 16 and >= ceil(K/5)", (long long)w_pitch);
+    QLIN_REQUIRE(qlin::aligned16(w_packed), QLIN_ERR_INVALID_ARG, "qlin_t158_i8_ws: w_packed not 16-byte aligned");
+    QLIN_REQUIRE(qlin::aligned4(x_scale) && (!y || qlin::aligned4(y)) && (!acc || qlin::aligned4(acc)),
+                 QLIN_ERR_INVALID_ARG, "qlin_t158_i8_ws: misaligned x_scale/y/acc");
+    QLIN_REQUIRE(M <= 4096 && K <= 131071, QLIN_ERR_UNSUPPORTED,
+                 "qlin_t158_i8_ws: M=%d K=%d outside 1..4096 x 1..131071", M, K);
+    const size_t need = qlin::t158_workspace_bytes(M, K);
+    QLIN_REQUIRE(workspace_bytes >= need && (need == 0 || (workspace && qlin::aligned16(workspace))),
+                 QLIN_ERR_INVALID_ARG, "qlin_t158_i8_ws: workspace %zu < %zu bytes, null or not 16-byte aligned",
+                 workspace_bytes, need);
+    if (M >= qlin::kTensorCoreMinM)
+        return qlin::t158_linear_tensor_cores(xq, x_scale, w_packed, w_pitch, w_scale, nullptr, y, acc, M, N, K,
+                                              (cudaStream_t)stream, workspace, true);
     return qlin::t158_linear_cuda_cores(xq, x_scale, w_packed, w_pitch, w_scale, nullptr, y, acc, M, N, K,
                                         (cudaStream_t)stream);
 }

@@ -1,67 +1,109 @@
-// T158 linear for many tokens (prefill) on the fifth-generation tensor cores.
+// T158 linear for many tokens (prefill, batched decode) on the fifth-generation
+// tensor cores.
 //
-// All prompt tokens go through each weight matrix in one pass (citric, "Step 4":
+// All tokens go through each weight matrix in one pass (citric, "Step 4":
 // batched prompt processing).  The integer dot products of "Step 1" run as an
 // fp16 matrix product with fp32 accumulation, which is exact here: int8 codes
 // (|x| <= 127) and trits are fp16 integers, every product is an integer of
 // magnitude <= 127 and every partial sum stays below 127 K < 2^24, so each fp32
 // addition is exact and the accumulator equals the int32 sum.
 //
-// One CTA computes a 128-token x 128-row tile with tcgen05.mma (M = 128,
-// N = 128, K = 16 per instruction) into a 128-column fp32 accumulator in tensor
-// memory.  K advances in steps of 80 elements: 16 packed bytes of every weight
-// row.  Within a step both operands use the same permuted K order, K' = 16 i + j
-// for element 5 j + i (digit i of packed byte j), which leaves the dot product
-// unchanged and lets the trits come straight out of the digit-plane decode.
-// Threads 0..127 convert the step's activation rows (int8 -> fp16, gathered into
-// K' order), threads 128..255 decode the weight rows (5 trits per byte ->
-// fp16), both into shared memory in the no-swizzle K-major layout of the MMA
-// (8-row x 16-byte core matrices, 128 bytes apart along K, kTcSBO bytes
-// between 8-row groups); one thread issues the step's five MMAs and commits
-// them to an mbarrier; two stages let the conversion of step s+1 overlap the
-// MMAs of step s.  The epilogue reads the accumulator back with tcgen05.ld
-// (warp w reads lanes 32 (w % 4) .. + 31, columns 64 (w / 4) .. + 63).
+// One CTA computes 128 weight rows x T tokens (T a multiple of 32, at most
+// 256) with tcgen05.mma (M = 128 weight rows, N = T tokens, K = 16 per
+// instruction) into T fp32 accumulator columns of tensor memory.  K advances in
+// steps of 80 elements: 16 packed bytes of every weight row.  Within a step
+// both operands use the same permuted K order, K' = 16 i + j for element
+// 5 j + i (digit i of packed byte j), which leaves the dot product unchanged
+// and lets the trits come straight out of the digit-plane decode.
+//
+// The weight tile is the MMA's A operand and sits in tensor memory: eight
+// converter warps decode the packed bytes (warp w: rows 32 (w % 4) .. + 31,
+// half w / 4 of the step's 16 bytes) and write the fp16 trits with tcgen05.st
+// into the lanes of their own rows, so decoded weights never pass through
+// shared memory.  The activation tile is the B operand, in shared memory in
+// the no-swizzle K-major layout of the MMA (8-row x 16-byte core matrices, 128
+// bytes apart along K, kTcSBO bytes between 8-row groups), reached one of two
+// ways:
+//  - with a workspace, t158_act_tiles_kernel converts every token row once per
+//    call into the exact image of each step's tile, and a copy warp brings a
+//    step's tile in with one bulk copy (the conversion is not repeated for
+//    every 128 weight rows);
+//  - without one, the converter warps also convert the step's int8 rows, two
+//    units of work per row (bytes 0..47 and 32..79 of the step: the first and
+//    second eight packed-byte columns).
+// Raw bytes run a few steps ahead through cp.async; several operand stages let
+// the conversion of later steps overlap the MMAs of earlier ones; one thread
+// issues each step's five MMAs and commits them to the stage's mbarrier.  The
+// epilogue reads the accumulator back with tcgen05.ld: a thread holds one
+// weight row for 16 tokens at a time and its warp writes 32 consecutive
+// outputs of each token.  Split K: a cluster of CTAs over one tile, each over
+// its own K steps, adds the partial tiles through distributed shared memory in
+// rank order.
 #include <cuda_fp16.h>
 
 #include <map>
 #include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "stream.cuh"
 
 namespace qlin {
 
-constexpr int kTcBM = 128;                      // tokens per CTA (MMA M)
-constexpr int kTcBN = 256;                      // weight rows per CTA (MMA N)
-constexpr int kTcKS = 80;                       // K elements per step (16 packed bytes)
-constexpr int kTcConv = kTcBM + kTcBN;          // converter threads: one per activation row and per weight row
-constexpr int kTcThreads = kTcConv + 32;        // + one warp that issues the MMAs
-constexpr int kTcChunks = kTcKS / 8;            // 16-byte core-matrix columns per row and step
-constexpr int kTcSBO = kTcChunks * 128;         // bytes between 8-row groups
-constexpr int kTcTileA = (kTcBM / 8) * kTcSBO;  // bytes of the A tile of one step
-constexpr int kTcTileB = (kTcBN / 8) * kTcSBO;  // bytes of the B tile of one step
-constexpr int kTcStages = 2;                    // fp16 operand stages
-constexpr int kTcRaw = 6;                       // raw (int8 / packed) stages copied ahead
-constexpr uint32_t kTcCols = kTcBN;             // tensor-memory columns: the 128 x 256 fp32 accumulator
-constexpr int kTcPStride = kTcBN + 4;           // floats per row of a partial tile in shared memory
-constexpr int kTcMaxSplit = 8;                  // CTAs of a cluster that split K
+constexpr int kTmRows = 128;              // weight rows per CTA (MMA M, tensor-memory lanes)
+constexpr int kTmMaxTok = 256;            // tokens per CTA at most (MMA N)
+constexpr int kTcKS = 80;                 // K elements per step (16 packed bytes)
+constexpr int kTcChunks = kTcKS / 8;      // 16-byte core-matrix columns per row and step
+constexpr int kTcSBO = kTcChunks * 128;   // bytes between 8-row groups of the activation tile
+constexpr int kTmConv = 256;              // converter threads (8 warps)
+constexpr int kTmThreads = kTmConv + 64;  // + the warp that issues the MMAs + the warp that copies activation tiles
+constexpr int kTmMaxStages = 4;
+constexpr int kTmACols = kTcKS / 2;       // tensor-memory columns of one step's weight tile (fp16 pairs)
+constexpr int kTmUnit = 48;               // raw bytes of one activation unit (three 16-byte copies)
+constexpr int kTmCtl = 2048;              // bytes of the control block at the start of shared memory
+constexpr int kTmPStride = kTmRows + 4;   // floats per token of a partial tile (split K)
+constexpr int kTmMaxSplit = 8;            // CTAs of a cluster that split K
 
-struct TcSmem {
-    union {
-        struct {
-            uint8_t a[kTcStages][kTcTileA];
-            uint8_t b[kTcStages][kTcTileB];
-            uint8_t raw_a[kTcRaw][kTcBM][kTcKS];  // each thread's own activation row, step by step
-            uint8_t raw_b[kTcRaw][kTcBN][16];     // each thread's own packed weight row
-        } in;
-        float part[kTcBM][kTcPStride];  // after the K loop: this CTA's partial tile (split K)
-    };
-    uint64_t full[kTcStages];      // the converters have written the stage (kTcConv arrivals)
-    uint64_t mma_done[kTcStages];  // the MMAs reading the stage are done (tcgen05.commit)
-    float xs[kTcBM];               // activation scales of the tile's tokens
+// Two ways to the activation tile.  PRE: converted once per call by
+// t158_act_tiles_kernel into a workspace, one bulk copy per stage; else
+// converted by the converter warps from the int8 codes at every step.
+// Stages (operand tiles) and raw stages (copies ahead) of each:
+__host__ __device__ constexpr int tm_stages(bool pre) { return pre ? 4 : 3; }
+__host__ __device__ constexpr int tm_raws(bool pre) { return pre ? 4 : 3; }
+
+struct TmCtl {
+    uint64_t full[kTmMaxStages];      // the stage is filled (converter arrivals, + the copy with PRE)
+    uint64_t mma_done[kTmMaxStages];  // the MMAs reading the stage are done (tcgen05.commit)
+    float xs[kTmMaxTok];              // activation scales of the tile's tokens
     uint32_t tmem;
     int abort;
+    int issued;  // steps whose MMAs were issued
 };
+static_assert(sizeof(TmCtl) <= kTmCtl, "control block");
+
+// Dynamic shared memory for T tokens: control block, the activation tiles of
+// the stages, raw activation stages (2 T units; in-kernel conversion only),
+// raw weight stages (8 bytes per converter); after the K loop the partial
+// tile (split K) reuses the space behind the control block.
+__host__ __device__ constexpr int tm_b_bytes(int T) { return T / 8 * kTcSBO; }
+__host__ __device__ constexpr int tm_raw_a_off(int T, bool pre) { return kTmCtl + tm_stages(pre) * tm_b_bytes(T); }
+__host__ __device__ constexpr int tm_raw_w_off(int T, bool pre) {
+    return tm_raw_a_off(T, pre) + (pre ? 0 : tm_raws(pre) * 2 * T * kTmUnit);
+}
+__host__ __device__ constexpr int tm_smem_bytes(int T, bool pre) {
+    return tm_raw_w_off(T, pre) + tm_raws(pre) * kTmConv * 8 > kTmCtl + T * kTmPStride * 4
+               ? tm_raw_w_off(T, pre) + tm_raws(pre) * kTmConv * 8
+               : kTmCtl + T * kTmPStride * 4;
+}
+// Tensor-memory columns: T accumulator columns, then the stages' weight
+// tiles; a power of two from 32 (the allocation unit).
+__host__ __device__ inline uint32_t tm_cols(int T, bool pre) {
+    uint32_t c = 32;
+    while ((int)c < T + tm_stages(pre) * kTmACols) c <<= 1;
+    return c;
+}
+static_assert(tm_smem_bytes(kTmMaxTok, false) <= 227 * 1024 && tm_smem_bytes(kTmMaxTok, true) <= 227 * 1024,
+              "shared memory of the largest tile");
 
 // Shared-memory matrix descriptor of the MMA: K-major, no swizzle, leading
 // byte offset 128 (next core matrix along K), stride byte offset kTcSBO (next
@@ -75,20 +117,22 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
-// K-major, N = kTcBN, M = kTcBM.  Both tiles use the descriptor above (the same
-// K step, so the same stride between 8-row groups).
-constexpr uint32_t kTcIdesc =
-    (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kTcBN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
+// K-major, N = T tokens, M = kTmRows weight rows.
+__device__ __forceinline__ uint32_t tm_idesc(int T) {
+    return (1u << 4) | ((uint32_t)(T >> 3) << 17) | ((uint32_t)(kTmRows >> 4) << 24);
+}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
+// D (tensor memory) (+)= A (tensor memory) x B (shared memory)
+__device__ __forceinline__ void tm_mma(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(kTcIdesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -97,20 +141,25 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// 32 consecutive accumulator columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// four consecutive 32-bit columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tm_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 16 consecutive accumulator columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tm_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Byte offset of 16-byte chunk kc of row r in an operand tile.
+// Byte offset of 16-byte chunk kc of row r in an activation tile.
 __device__ __forceinline__ int tc_off(int r, int kc) { return (r >> 3) * kTcSBO + kc * 128 + (r & 7) * 16; }
 
 // Two int8 bytes (already xor 0x80, i.e. v + 128) -> fp16x2 of the two values:
@@ -127,45 +176,57 @@ __device__ __forceinline__ uint32_t h2sub(uint32_t bits, uint32_t cbits) {
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// 80 activation bytes of one row (words in[], byte v + 128 of each value v,
-// i.e. already xor 0x80) into row r of the A tile, K' order, fp16.
-__device__ __forceinline__ void tc_put_a(uint8_t *tile, const uint32_t (&in)[20], int r) {
+// Activation unit H of token row r: in[] holds bytes 32 H .. 32 H + 47 of the
+// step (v + 128 for each value v); it fills chunks kc = 2 i + H (K' 16 i + 8 H
+// .. + 7, i.e. packed-byte columns j = 8 H .. 8 H + 7 of digit i) of row r.
+template <int H>
+__device__ __forceinline__ void tm_put_act(uint8_t *tile, const uint32_t (&in)[12], int r) {
 #pragma unroll
-    for (int kc = 0; kc < kTcChunks; kc++) {
+    for (int i = 0; i < 5; i++) {
         uint32_t h[4];
 #pragma unroll
         for (int p = 0; p < 4; p++) {
-            const int kp = 8 * kc + 2 * p;           // K' of the low half
-            const int i = kp >> 4, j = kp & 15;      // digit, packed byte
-            const int e0 = 5 * j + i, e1 = e0 + 5;   // element offsets within the step
+            // K' = 16 i + 8 H + 2 p is element 5 (8 H + 2 p) + i, byte 8 H + 10 p + i of the unit
+            const int e0 = 8 * H + 10 * p + i, e1 = e0 + 5;
             h[p] = h2sub(i8pair_bits(in[e0 >> 2], in[e1 >> 2], e0 & 3, e1 & 3), 0x64806480u);
         }
-        *reinterpret_cast<uint4 *>(tile + tc_off(r, kc)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(tile + tc_off(r, 2 * i + H)) = make_uint4(h[0], h[1], h[2], h[3]);
     }
 }
 
-// 16 packed bytes of one weight row into row r of the B tile, K' order, fp16 trits.
-__device__ __forceinline__ void tc_put_b(uint8_t *tile, const uint4 v, int r) {
-    uint32_t D[4][5];
-    t158_planes(v.x, D[0]);
-    t158_planes(v.y, D[1]);
-    t158_planes(v.z, D[2]);
-    t158_planes(v.w, D[3]);
+// Eight packed bytes (v.x, v.y: packed-byte columns 8 hw .. 8 hw + 7 of the
+// step) of this thread's weight row -> fp16 trits into its tensor-memory lane:
+// chunk kc = 2 i + hw is the four columns 4 kc .. 4 kc + 3 from `ta`.
+__device__ __forceinline__ void tm_put_w(uint32_t ta, uint2 v, int hw) {
+    uint32_t D0[5], D1[5];
+    t158_planes(v.x, D0);
+    t158_planes(v.y, D1);
 #pragma unroll
-    for (int kc = 0; kc < kTcChunks; kc++) {
-        const int i = kc >> 1, wa = 2 * (kc & 1);
+    for (int i = 0; i < 5; i++) {
         // digits d in 0..2: fp16 (1024 + d) - 1025 = d - 1
-        const uint32_t h0 = h2sub(__byte_perm(D[wa][i], 0x6464u, 0x5140u), 0x64016401u);
-        const uint32_t h1 = h2sub(__byte_perm(D[wa][i], 0x6464u, 0x5342u), 0x64016401u);
-        const uint32_t h2 = h2sub(__byte_perm(D[wa + 1][i], 0x6464u, 0x5140u), 0x64016401u);
-        const uint32_t h3 = h2sub(__byte_perm(D[wa + 1][i], 0x6464u, 0x5342u), 0x64016401u);
-        *reinterpret_cast<uint4 *>(tile + tc_off(r, kc)) = make_uint4(h0, h1, h2, h3);
+        const uint32_t h0 = h2sub(__byte_perm(D0[i], 0x6464u, 0x5140u), 0x64016401u);
+        const uint32_t h1 = h2sub(__byte_perm(D0[i], 0x6464u, 0x5342u), 0x64016401u);
+        const uint32_t h2 = h2sub(__byte_perm(D1[i], 0x6464u, 0x5140u), 0x64016401u);
+        const uint32_t h3 = h2sub(__byte_perm(D1[i], 0x6464u, 0x5342u), 0x64016401u);
+        tm_st4(ta + (uint32_t)(4 * (2 * i + hw)), h0, h1, h2, h3);
     }
 }
 
-// 16 bytes global -> shared, the bytes past src_bytes (0..16) zero.
+// 16 (8) bytes global -> shared, the bytes past src_bytes zero.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async8(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+// 1-D bulk copy global -> shared completing on `bar`; bytes and both addresses
+// multiples of 16.
+__device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -174,40 +235,22 @@ __device__ __forceinline__ void cp_async_wait_pending() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Activation row m (token) of step s into the A tile, K' order, fp16, loaded
-// directly (any alignment).
-__device__ __forceinline__ void tc_fill_a(uint8_t *tile, const int8_t *__restrict__ xq, int M, int K, int m, int r,
-                                          int s, bool vec) {
-    const int k0 = s * kTcKS;
-    uint32_t in[20];
-    if (m >= M) {
+// Unit h of token m at step s loaded directly (any alignment; zero past K and
+// for m >= M), as bytes v + 128.
+__device__ __forceinline__ void tm_load_act(uint32_t (&in)[12], const int8_t *__restrict__ xq, int M, int K, int m,
+                                            int s, int h) {
+    const int k0 = s * kTcKS + 32 * h;
 #pragma unroll
-        for (int i = 0; i < 20; i++) in[i] = 0x80808080u;  // bytes v + 128 of v = 0
-    } else if (vec && k0 + kTcKS <= K) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(xq + (int64_t)m * K + k0);
+    for (int i = 0; i < 12; i++) {
+        uint32_t v = 0;
 #pragma unroll
-        for (int i = 0; i < 5; i++) {
-            const uint4 v = __ldg(src + i);
-            in[4 * i] = v.x ^ 0x80808080u;
-            in[4 * i + 1] = v.y ^ 0x80808080u;
-            in[4 * i + 2] = v.z ^ 0x80808080u;
-            in[4 * i + 3] = v.w ^ 0x80808080u;
+        for (int b = 0; b < 4; b++) {
+            const int k = k0 + 4 * i + b;
+            const uint32_t byte = (m < M && k < K) ? (uint32_t)(uint8_t)xq[(int64_t)m * K + k] : 0u;
+            v |= byte << (8 * b);
         }
-    } else {
-        const int8_t *row = xq + (int64_t)m * K;
-#pragma unroll
-        for (int i = 0; i < 20; i++) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                const int k = k0 + 4 * i + b;
-                const uint32_t byte = k < K ? (uint32_t)(uint8_t)row[k] : 0u;
-                v |= byte << (8 * b);
-            }
-            in[i] = v ^ 0x80808080u;
-        }
+        in[i] = v ^ 0x80808080u;
     }
-    tc_put_a(tile, in, r);
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -228,235 +271,362 @@ __device__ __forceinline__ float4 ld_peer_f4(const void *local, uint32_t rank) {
     return v;
 }
 
-// Grid: (N tiles, M tiles, split); a cluster is the `split` CTAs of one tile,
-// each over its own range of K steps.  split == 1: no cluster reduction.
-__global__ void __launch_bounds__(kTcThreads, 1) t158_tc_kernel(const int8_t *__restrict__ xq,
-                                                               const float *__restrict__ xs,
-                                                               const uint8_t *__restrict__ w, int64_t pitch, float ws_arg,
-                                                               const float *__restrict__ ws_ptr,
-                                                               float *__restrict__ y, int32_t *__restrict__ acc_out,
-                                                               int M, int N, int K, int split) {
+// One token row of one step into an activation tile: in[] holds the 80 bytes
+// (v + 128 for each value v); chunk kc of row r is K' 8 kc .. 8 kc + 7.
+__device__ __forceinline__ void tm_put_row(uint8_t *tile, const uint32_t (&in)[20], int r) {
+#pragma unroll
+    for (int kc = 0; kc < kTcChunks; kc++) {
+        uint32_t h[4];
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            const int kp = 8 * kc + 2 * p;          // K' of the low half
+            const int e0 = 5 * (kp & 15) + (kp >> 4), e1 = e0 + 5;  // elements 5 j + i
+            h[p] = h2sub(i8pair_bits(in[e0 >> 2], in[e1 >> 2], e0 & 3, e1 & 3), 0x64806480u);
+        }
+        *reinterpret_cast<uint4 *>(tile + tc_off(r, kc)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
+// Activation tiles for the PRE path, converted once per call: the image of
+// the shared-memory activation tile of token tile tt at step s (tokens
+// tt T .. + T - 1, elements 80 s .. + 79, zero past M and K) at
+// out + (tt nsteps + s) tm_b_bytes(T).  One thread per token row and step;
+// a warp's 32 rows make 4 runs of 128 contiguous bytes per store.
+__global__ void __launch_bounds__(256) t158_act_tiles_kernel(const int8_t *__restrict__ xq, int M, int K, int T,
+                                                             int tiles_m, int nsteps, uint8_t *__restrict__ out) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)tiles_m * T * nsteps) return;
+    const int r = (int)(idx % T);
+    const int64_t rest = idx / T;
+    const int tt = (int)(rest % tiles_m), s = (int)(rest / tiles_m);
+    const int m = tt * T + r, k0 = s * kTcKS;
+    uint32_t in[20];
+    if (m >= M) {
+#pragma unroll
+        for (int i = 0; i < 20; i++) in[i] = 0x80808080u;  // bytes v + 128 of v = 0
+    } else if ((reinterpret_cast<uintptr_t>(xq) & 15) == 0 && K % 16 == 0) {
+        const int8_t *row = xq + (int64_t)m * K;
+#pragma unroll
+        for (int c = 0; c < 5; c++) {
+            // K % 16 == 0: a 16-byte chunk is wholly inside K or wholly past it
+            const uint4 v = k0 + 16 * c < K ? __ldg(reinterpret_cast<const uint4 *>(row + k0 + 16 * c))
+                                            : make_uint4(0, 0, 0, 0);
+            in[4 * c] = v.x ^ 0x80808080u;
+            in[4 * c + 1] = v.y ^ 0x80808080u;
+            in[4 * c + 2] = v.z ^ 0x80808080u;
+            in[4 * c + 3] = v.w ^ 0x80808080u;
+        }
+    } else {
+        const int8_t *row = xq + (int64_t)m * K;
+#pragma unroll
+        for (int i = 0; i < 20; i++) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int b = 0; b < 4; b++) {
+                const int k = k0 + 4 * i + b;
+                v |= (k < K ? (uint32_t)(uint8_t)row[k] : 0u) << (8 * b);
+            }
+            in[i] = v ^ 0x80808080u;
+        }
+    }
+    tm_put_row(out + ((int64_t)tt * nsteps + s) * tm_b_bytes(T), in, r);
+}
+
+// Grid: (weight-row tiles, token tiles, split); a cluster is the `split` CTAs
+// of one tile, each over its own range of K steps.  split == 1: no cluster
+// reduction.  T: tokens per tile (a multiple of 32, at most kTmMaxTok).
+// PRE: `tiles` holds the activation tiles written by t158_act_tiles_kernel.
+template <bool PRE>
+__global__ void __launch_bounds__(kTmThreads, 1)
+    t158_tm_kernel(const int8_t *__restrict__ xq, const uint8_t *__restrict__ tiles, const float *__restrict__ xs,
+                   const uint8_t *__restrict__ w, int64_t pitch, float ws_arg, const float *__restrict__ ws_ptr,
+                   float *__restrict__ y, int32_t *__restrict__ acc_out, int M, int N, int K, int T, int split) {
+    constexpr int S = tm_stages(PRE), R = tm_raws(PRE);
     const float ws = ws_ptr ? __ldg(ws_ptr) : ws_arg;  // the weight scale, from device memory when given
-    extern __shared__ __align__(128) uint8_t tc_smem_raw[];
-    TcSmem &S = *reinterpret_cast<TcSmem *>(tc_smem_raw);
+    extern __shared__ __align__(128) uint8_t tm_smem[];
+    TmCtl &C = *reinterpret_cast<TmCtl *>(tm_smem);
+    uint8_t *const btile = tm_smem + kTmCtl;
+    uint8_t *const raw_a = tm_smem + tm_raw_a_off(T, PRE);
+    uint8_t *const raw_w = tm_smem + tm_raw_w_off(T, PRE);
+    const int bstage = tm_b_bytes(T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * kTcBN, m0 = blockIdx.y * kTcBM;
+    const int n0 = blockIdx.x * kTmRows, m0 = blockIdx.y * T;
     const int nsteps = (K + kTcKS - 1) / kTcKS;
     const int z = split > 1 ? (int)cluster_rank() : 0;
     const int s_lo = (int)((int64_t)nsteps * z / split), s_hi = (int)((int64_t)nsteps * (z + 1) / split);
+    const int nst = s_hi - s_lo;  // steps of this CTA
+    const int units = 2 * T;      // activation units per step (in-kernel conversion)
+    // converter roles: weight rows 32 q .. + 31, packed bytes 8 hw .. + 7 of each step
+    const int q = warp & 3, hw = (warp >> 2) & 1;
+    const int wrow = 32 * q + lane;
+    const bool a_async = !PRE && (reinterpret_cast<uintptr_t>(xq) & 15) == 0 && K % 16 == 0;
 
-    // Converters.  Raw bytes of each thread's own row run kTcRaw - 1
-    // steps ahead through cp.async (16-byte copies, zero-filled past K, M
-    // and N: such products are zero or land outside the output); a thread
-    // reads back only what it copied, so its own wait_group is enough.
-    // Activations that are not 16-byte aligned are loaded directly.
-    const bool a_async = (reinterpret_cast<uintptr_t>(xq) & 15) == 0 && K % 16 == 0;
-    const bool is_a = tid < kTcBM;
-    const int r_own = is_a ? tid : tid - kTcBM;
+    // Raw bytes of each converter's own work run R - 1 steps ahead (zero-filled
+    // past K, M and N: such products are zero or land outside the output); a
+    // thread reads back only what it copied, so its own wait_group is enough.
+    // Unaligned activations are loaded directly.
     auto fetch = [&](int s) {
         if (s < s_hi) {
-            const int rs = (s - s_lo) % kTcRaw;
-            if (is_a) {
-                if (a_async) {
-                    const int m = m0 + r_own, k0 = s * kTcKS;
-                    const int8_t *row = xq + (int64_t)(m < M ? m : 0) * K;
+            const int rs = (s - s_lo) % R;
+            const int n = n0 + wrow;
+            cp_async8(raw_w + (rs * kTmConv + tid) * 8, w + (int64_t)(n < N ? n : 0) * pitch + (int64_t)s * 16 + 8 * hw,
+                      n < N ? 8 : 0);
+            if (a_async) {
 #pragma unroll
-                    for (int c = 0; c < kTcKS / 16; c++) {
-                        const int kb = k0 + 16 * c;
-                        const int nb = m < M ? max(0, min(16, K - kb)) : 0;
-                        cp_async16(S.in.raw_a[rs][r_own] + 16 * c, nb > 0 ? row + kb : row, nb);
+                for (int k = 0; k < 2; k++) {
+                    const int u = tid + kTmConv * k;
+                    if (u < units) {
+                        const int h = u >= T, m = m0 + (h ? u - T : u);
+                        const int8_t *row = xq + (int64_t)(m < M ? m : 0) * K;
+#pragma unroll
+                        for (int c = 0; c < 3; c++) {
+                            const int kb = s * kTcKS + 32 * h + 16 * c;
+                            const int nb = m < M ? max(0, min(16, K - kb)) : 0;
+                            cp_async16(raw_a + (rs * units + u) * kTmUnit + 16 * c, nb > 0 ? row + kb : row, nb);
+                        }
                     }
                 }
-            } else {
-                const int n = n0 + r_own;
-                cp_async16(S.in.raw_b[rs][r_own], w + (int64_t)(n < N ? n : 0) * pitch + (int64_t)s * 16,
-                           n < N ? 16 : 0);
             }
         }
         cp_async_commit();
     };
     // the first copies go out before anything else
-    if (tid < kTcConv) {
+    if (tid < kTmConv) {
 #pragma unroll
-        for (int s = 0; s < kTcRaw - 1; s++) fetch(s_lo + s);
+        for (int s = 0; s < R - 1; s++) fetch(s_lo + s);
     }
-    for (int i = tid; i < kTcBM; i += kTcThreads) S.xs[i] = m0 + i < M ? xs[m0 + i] : 0.0f;
+    for (int i = tid; i < T; i += kTmThreads) C.xs[i] = m0 + i < M ? xs[m0 + i] : 0.0f;
+    const uint32_t ncols = tm_cols(T, PRE);
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&S.tmem)),
-                     "r"(kTcCols)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&C.tmem)),
+                     "r"(ncols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 32) {
-        for (int i = 0; i < kTcStages; i++) {
-            mbar_init(&S.full[i], kTcConv);
-            mbar_init(&S.mma_done[i], 1);
+        for (int i = 0; i < S; i++) {
+            mbar_init(&C.full[i], kTmConv + (PRE ? 1 : 0));
+            mbar_init(&C.mma_done[i], 1);
         }
-        S.abort = 0;
+        C.abort = 0;
+        C.issued = 0;
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = S.tmem;
-    volatile int *abort = &S.abort;
-    const int nst = s_hi - s_lo;  // steps of this CTA
+    const uint32_t tmem = C.tmem;
+    volatile int *abort = &C.abort;
 
-    if (warp == kTcConv / 32) {
-        // ---- MMA warp: lane 0 issues each step's five MMAs once the converters
-        // have filled the stage, and commits them to the stage's mma_done
+    if (warp == kTmConv / 32) {
+        // ---- MMA warp: lane 0 issues each step's five MMAs once the stage is
+        // filled, and commits them to the stage's mma_done
         if (lane == 0) {
+            const uint32_t idesc = tm_idesc(T);
             for (int i = 0; i < nst && !*abort; i++) {
-                const int st = i & 1;
-                if (!mbar_wait(&S.full[st], (i >> 1) & 1)) {
+                const int st = i % S;
+                if (!mbar_wait(&C.full[st], (uint32_t)(i / S) & 1u)) {
                     *abort = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = smem_addr(S.in.a[st]), b0 = smem_addr(S.in.b[st]);
+                const uint32_t b0 = smem_addr(btile + st * bstage);
+                const uint32_t a0 = tmem + (uint32_t)(T + kTmACols * st);
 #pragma unroll
-                for (int u = 0; u < kTcKS / 16; u++)  // K = 16: two core-matrix columns (256 bytes)
-                    tc_mma(tmem, tc_desc(a0 + 256u * u), tc_desc(b0 + 256u * u), (i > 0 || u > 0) ? 1u : 0u);
-                tc_commit(&S.mma_done[st]);
+                for (int u = 0; u < kTcKS / 16; u++)  // K = 16: 8 weight columns, 2 activation core matrices
+                    tm_mma(tmem, a0 + 8u * u, tc_desc(b0 + 256u * u), idesc, (i > 0 || u > 0) ? 1u : 0u);
+                tc_commit(&C.mma_done[st]);
+                *reinterpret_cast<volatile int *>(&C.issued) = i + 1;
+            }
+        }
+    } else if (warp == kTmConv / 32 + 1) {
+        // ---- copy warp (PRE): lane 0 brings each step's activation tile in
+        // with one bulk copy once the MMAs that read the stage before are done
+        if (PRE && lane == 0) {
+            const uint8_t *src = tiles + ((int64_t)blockIdx.y * nsteps + s_lo) * bstage;
+            for (int i = 0; i < nst && !*abort; i++) {
+                const int st = i % S;
+                if (i >= S && !mbar_wait(&C.mma_done[st], (uint32_t)(i / S - 1) & 1u)) {
+                    *abort = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&C.full[st], (uint32_t)bstage);
+                bulk_g2s_plain(btile + st * bstage, src + (int64_t)i * bstage, (uint32_t)bstage, &C.full[st]);
             }
         }
     } else {
-        // ---- converters
-        for (int i = 0; i < nst && !*abort; i++) {
-            const int s = s_lo + i, st = i & 1;
-            fetch(s + kTcRaw - 1);
-            cp_async_wait_pending<kTcRaw - 1>();  // this thread's copies of step s have landed
-            // the MMAs of step i-2 read this stage: wait until they are done
-            if (i >= 2 && !mbar_wait(&S.mma_done[st], ((i >> 1) - 1) & 1)) {
+        // ---- converters (whole warps: the tensor-memory stores are warp-wide)
+        const uint32_t ta_row = tmem + ((uint32_t)(32 * q) << 16);
+        for (int i = 0; i < nst; i++) {
+            if (__any_sync(0xffffffffu, *abort != 0)) break;
+            const int s = s_lo + i, st = i % S, rs = i % R;
+            fetch(s + R - 1);
+            cp_async_wait_pending<R - 1>();  // this thread's copies of step s have landed
+            // the MMAs of step i - S read this stage: wait until they are done
+            bool ok = true;
+            if (i >= S) ok = mbar_wait(&C.mma_done[st], (uint32_t)(i / S - 1) & 1u);
+            if (!__all_sync(0xffffffffu, ok)) {
                 *abort = 1;
                 break;
             }
-            if (is_a) {
-                if (a_async) {
-                    uint32_t in[20];
-                    const uint4 *src = reinterpret_cast<const uint4 *>(S.in.raw_a[i % kTcRaw][r_own]);
+            tc_fence_after();
+            tm_put_w(ta_row + (uint32_t)(T + kTmACols * st),
+                     *reinterpret_cast<const uint2 *>(raw_w + (rs * kTmConv + tid) * 8), hw);
+            if (!PRE) {
+                uint8_t *const bt = btile + st * bstage;
 #pragma unroll
-                    for (int q = 0; q < 5; q++) {
-                        const uint4 v = src[q];
-                        in[4 * q] = v.x ^ 0x80808080u;
-                        in[4 * q + 1] = v.y ^ 0x80808080u;
-                        in[4 * q + 2] = v.z ^ 0x80808080u;
-                        in[4 * q + 3] = v.w ^ 0x80808080u;
+                for (int k = 0; k < 2; k++) {
+                    const int u = tid + kTmConv * k;
+                    if (u < units) {  // whole warps: T is a multiple of 32
+                        const int h = u >= T, r = h ? u - T : u;
+                        uint32_t in[12];
+                        if (a_async) {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(raw_a + (rs * units + u) * kTmUnit);
+#pragma unroll
+                            for (int c = 0; c < 3; c++) {
+                                const uint4 v = src[c];
+                                in[4 * c] = v.x ^ 0x80808080u;
+                                in[4 * c + 1] = v.y ^ 0x80808080u;
+                                in[4 * c + 2] = v.z ^ 0x80808080u;
+                                in[4 * c + 3] = v.w ^ 0x80808080u;
+                            }
+                        } else {
+                            tm_load_act(in, xq, M, K, m0 + r, s, h);
+                        }
+                        if (h)
+                            tm_put_act<1>(bt, in, r);
+                        else
+                            tm_put_act<0>(bt, in, r);
                     }
-                    tc_put_a(S.in.a[st], in, r_own);
-                } else {
-                    tc_fill_a(S.in.a[st], xq, M, K, m0 + r_own, r_own, s, false);
                 }
-            } else {
-                tc_put_b(S.in.b[st], *reinterpret_cast<const uint4 *>(S.in.raw_b[i % kTcRaw][r_own]), r_own);
             }
+            tm_wait_st();
             // the generic-proxy writes above, visible to the tensor core (async proxy)
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&S.full[st]);
+            if (!PRE) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(&C.full[st]);
         }
         cp_async_wait_pending<0>();
     }
     // the last commit covers every MMA issued before it
-    bool ok = true;
-    if (nst > 0 && !*abort) {
-        const int i = nst - 1;
-        if (!mbar_wait(&S.mma_done[i & 1], (i >> 1) & 1)) *abort = 1;
+    __syncthreads();
+    const int issued = C.issued;
+    if (issued > 0) {
+        const int i = issued - 1;
+        if (!mbar_wait(&C.mma_done[i % S], (uint32_t)(i / S) & 1u)) *abort = 1;
     }
     __syncthreads();
-    ok = !*abort;
+    const bool ok = !*abort && issued == nst;
     tc_fence_after();
 
     const float nanv = ok ? 0.0f : __int_as_float(0x7fc00000);  // a wait that gave up: the tile reads NaN
-    const bool vec_out = y && (reinterpret_cast<uintptr_t>(y) & 15) == 0 && N % 4 == 0;
-    // the accumulator into shared memory (warps 0..7: lanes 32 (w % 4) .. + 31,
-    // columns 128 (w / 4) .. + 127), so that the output rows are written coalesced
-    if (warp < 8) {
-        const int q = warp & 3, cg = warp >> 2;
-        const int row = 32 * q + lane;
-#pragma unroll 1
-        for (int c = 0; c < 4; c++) {
-            const int col = 128 * cg + 32 * c;
-            uint32_t r[32];
-            tc_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
-            float4 *dst = reinterpret_cast<float4 *>(&S.part[row][col]);
+    float *const part = reinterpret_cast<float *>(tm_smem + kTmCtl);
+    if (warp < kTmConv / 32) {
+        // warp w: weight rows 32 (w % 4) .. + 31 (its lanes), tokens T/2 (w / 4) .. + T/2 - 1
+        const int n = n0 + wrow;
+        const int tb = (warp >> 2) * (T / 2);
+        for (int t0 = tb; t0 < tb + T / 2; t0 += 16) {
+            uint32_t r[16];
+            tm_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)t0, r);
+            if (split == 1) {
+                if (n < N) {
 #pragma unroll
-            for (int j = 0; j < 8; j++)
-                dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    for (int j = 0; j < 16; j++) {
+                        const int m = m0 + t0 + j;
+                        if (m >= M) break;
+                        const float v = __uint_as_float(r[j]);
+                        if (acc_out) acc_out[(int64_t)m * N + n] = __float2int_rz(v);
+                        if (y) y[(int64_t)m * N + n] = __fadd_rn(__fmul_rn(__fmul_rn(v, ws), C.xs[t0 + j]), nanv);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++) part[(t0 + j) * kTmPStride + wrow] = __uint_as_float(r[j]);
+            }
         }
     }
-    // split K: CTA z adds rows [128 z / split, 128 (z+1) / split) over the
-    // cluster in rank order (integers below 2^24: exact); split 1: all rows
-    if (split > 1)
+    if (split > 1) {
+        // CTA z adds tokens [T z / split, T (z+1) / split) over the cluster in
+        // rank order (integers below 2^24: exact)
         cluster_sync();
-    else
-        __syncthreads();
-    const int r0 = kTcBM * z / split, r1 = kTcBM * (z + 1) / split;
-#pragma unroll 4
-    for (int e = tid; e < (r1 - r0) * (kTcBN / 4); e += kTcThreads) {
-        const int row = r0 + e / (kTcBN / 4), c4 = e % (kTcBN / 4);
-        float4 v;
-        if (split == 1) {
-            v = *reinterpret_cast<const float4 *>(&S.part[row][4 * c4]);
-        } else {
-            float4 u[kTcMaxSplit];
+        const int t_lo = T * z / split, t_hi = T * (z + 1) / split;
+        const bool vec_y = y && (reinterpret_cast<uintptr_t>(y) & 15) == 0 && N % 4 == 0;
+        const bool vec_acc = acc_out && (reinterpret_cast<uintptr_t>(acc_out) & 15) == 0 && N % 4 == 0;
+#pragma unroll 2
+        for (int e = tid; e < (t_hi - t_lo) * (kTmRows / 4); e += kTmThreads) {
+            const int t = t_lo + e / (kTmRows / 4), c4 = e % (kTmRows / 4);
+            const int m = m0 + t, nb = n0 + 4 * c4;
+            if (m >= M || nb >= N) continue;
+            float4 u[kTmMaxSplit];
 #pragma unroll
-            for (int qq = 0; qq < kTcMaxSplit; qq++)
-                if (qq < split) u[qq] = ld_peer_f4(&S.part[row][4 * c4], (uint32_t)qq);
-            v = u[0];
+            for (int qq = 0; qq < kTmMaxSplit; qq++)
+                if (qq < split) u[qq] = ld_peer_f4(&part[t * kTmPStride + 4 * c4], (uint32_t)qq);
+            float4 v = u[0];
 #pragma unroll
-            for (int qq = 1; qq < kTcMaxSplit; qq++)
+            for (int qq = 1; qq < kTmMaxSplit; qq++)
                 if (qq < split) {
                     v.x = __fadd_rn(v.x, u[qq].x);
                     v.y = __fadd_rn(v.y, u[qq].y);
                     v.z = __fadd_rn(v.z, u[qq].z);
                     v.w = __fadd_rn(v.w, u[qq].w);
                 }
-        }
-        const int m = m0 + row, nb = n0 + 4 * c4;
-        if (m >= M || nb >= N) continue;
-        const float xsm = S.xs[row];
-        const float vv[4] = {v.x, v.y, v.z, v.w};
-        if (acc_out) {
-            if ((reinterpret_cast<uintptr_t>(acc_out) & 15) == 0 && N % 4 == 0 && nb + 4 <= N) {
-                *reinterpret_cast<int4 *>(acc_out + (int64_t)m * N + nb) =
-                    make_int4(__float2int_rz(vv[0]), __float2int_rz(vv[1]), __float2int_rz(vv[2]), __float2int_rz(vv[3]));
-            } else {
-                for (int j = 0; j < 4; j++)
-                    if (nb + j < N) acc_out[(int64_t)m * N + nb + j] = __float2int_rz(vv[j]);
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+            const float xsm = C.xs[t];
+            if (acc_out) {
+                if (vec_acc && nb + 4 <= N) {
+                    *reinterpret_cast<int4 *>(acc_out + (int64_t)m * N + nb) = make_int4(
+                        __float2int_rz(vv[0]), __float2int_rz(vv[1]), __float2int_rz(vv[2]), __float2int_rz(vv[3]));
+                } else {
+                    for (int j = 0; j < 4; j++)
+                        if (nb + j < N) acc_out[(int64_t)m * N + nb + j] = __float2int_rz(vv[j]);
+                }
+            }
+            if (y) {
+                float o[4];
+#pragma unroll
+                for (int j = 0; j < 4; j++) o[j] = __fadd_rn(__fmul_rn(__fmul_rn(vv[j], ws), xsm), nanv);
+                if (vec_y && nb + 4 <= N) {
+                    *reinterpret_cast<float4 *>(y + (int64_t)m * N + nb) = make_float4(o[0], o[1], o[2], o[3]);
+                } else {
+                    for (int j = 0; j < 4; j++)
+                        if (nb + j < N) y[(int64_t)m * N + nb + j] = o[j];
+                }
             }
         }
-        if (y) {
-            if (vec_out && nb + 4 <= N) {
-                *reinterpret_cast<float4 *>(y + (int64_t)m * N + nb) =
-                    make_float4(__fadd_rn(__fmul_rn(__fmul_rn(vv[0], ws), xsm), nanv),
-                                __fadd_rn(__fmul_rn(__fmul_rn(vv[1], ws), xsm), nanv),
-                                __fadd_rn(__fmul_rn(__fmul_rn(vv[2], ws), xsm), nanv),
-                                __fadd_rn(__fmul_rn(__fmul_rn(vv[3], ws), xsm), nanv));
-            } else {
-                for (int j = 0; j < 4; j++)
-                    if (nb + j < N) y[(int64_t)m * N + nb + j] = __fadd_rn(__fmul_rn(__fmul_rn(vv[j], ws), xsm), nanv);
-            }
-        }
+        cluster_sync();  // no CTA leaves while another still reads its shared memory
     }
-    if (split > 1) cluster_sync();  // no CTA leaves while another still reads its shared memory
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols) : "memory");
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
 }
 
-// Clusters of `c` CTAs of this kernel that can be resident at once (cached).
-static int tc_resident_clusters(int c, size_t smem) {
+// Token tiling of M tokens: the fewest tiles of at most kTmMaxTok tokens,
+// T rounded up to a multiple of 32.
+static void tm_token_tiles(int M, int &tiles_m, int &T) {
+    tiles_m = (M + kTmMaxTok - 1) / kTmMaxTok;
+    T = ((M + tiles_m - 1) / tiles_m + 31) / 32 * 32;
+}
+
+size_t t158_tc_workspace_bytes(int M, int K) {
+    int tiles_m = 0, T = 0;
+    tm_token_tiles(M, tiles_m, T);
+    return (size_t)tiles_m * (size_t)((K + kTcKS - 1) / kTcKS) * (size_t)tm_b_bytes(T);
+}
+
+// Clusters of `c` CTAs of this kernel with `smem` bytes each that can be
+// resident at once (cached).
+template <bool PRE>
+static int tm_resident_clusters(int c, size_t smem) {
     static std::mutex mu;
-    static std::map<std::pair<int, int>, int> cache;
+    static std::map<std::tuple<int, int, size_t>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     std::lock_guard<std::mutex> lk(mu);
-    auto it = cache.find({dev, c});
+    auto it = cache.find({dev, c, smem});
     if (it != cache.end()) return it->second;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, (unsigned)c);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(kTmThreads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -466,36 +636,72 @@ static int tc_resident_clusters(int c, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, t158_tc_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, t158_tm_kernel<PRE>, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         n = 0;
     }
-    cache[{dev, c}] = n;
+    cache[{dev, c, smem}] = n;
     return n;
 }
 
-qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
-                                     const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K,
-                                     cudaStream_t st) {
-    const size_t smem = sizeof(TcSmem);
+// Dynamic shared memory of a launch with T tokens per tile (cached per
+// device).  No more CTAs may share an SM than their tensor-memory allocations
+// fit in (512 columns): a CTA beyond that would block in tcgen05.alloc, and
+// with split-K clusters waiting on one another that wait might never end.
+// Shared memory enforces it: each CTA takes more than 1/(fit+1) of the SM's,
+// checked against the occupancy the runtime reports.
+template <bool PRE>
+static qlin_status tm_launch_smem(int T, size_t *out) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, size_t> cache;
+    int dev = 0;
+    QLIN_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find({dev, T});
+    if (it != cache.end()) {
+        *out = it->second;
+        return QLIN_OK;
+    }
+    const int fit = (int)(512u / tm_cols(T, PRE));
+    size_t smem = (size_t)tm_smem_bytes(T, PRE);
+    int sm_smem = 0, reserved = 0;
+    QLIN_CUDA(cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+    QLIN_CUDA(cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev));
+    const size_t floor_smem = (size_t)(sm_smem / (fit + 1) - reserved + 16) / 16 * 16 + 16;
+    if (smem < floor_smem) smem = floor_smem;
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "qlin_t158_i8: tensor-core tile does not fit");
-    blocks_per_sm((const void *)t158_tc_kernel, smem);  // raises the dynamic shared-memory limit
-    const int tiles_n = (N + kTcBN - 1) / kTcBN, tiles_m = (M + kTcBM - 1) / kTcBM;
+    blocks_per_sm((const void *)t158_tm_kernel<PRE>, smem);  // raises the dynamic shared-memory limit
+    int resident = 0;
+    QLIN_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, t158_tm_kernel<PRE>, kTmThreads, smem));
+    QLIN_REQUIRE(resident >= 1 && resident <= fit, QLIN_ERR_UNSUPPORTED,
+                 "qlin_t158_i8: %d CTAs per SM would exceed tensor memory (%d fit)", resident, fit);
+    cache[{dev, T}] = smem;
+    *out = smem;
+    return QLIN_OK;
+}
+
+template <bool PRE>
+static qlin_status launch_tm(const int8_t *xq, const uint8_t *tiles, const float *xs, const uint8_t *w, int64_t pitch,
+                             float ws, const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, int tiles_m,
+                             int T, cudaStream_t st) {
+    size_t smem = 0;
+    if (qlin_status e = tm_launch_smem<PRE>(T, &smem)) return e;
+    const int tiles_n = (N + kTmRows - 1) / kTmRows;
     const int nsteps = (K + kTcKS - 1) / kTcKS;
     // split K over a cluster when the tiles alone leave SMs idle: the largest
     // split whose clusters (they must fit within a GPC) are all resident at once
-    const int tiles = tiles_n * tiles_m;
+    const int ntiles = tiles_n * tiles_m;
     int split = 1;
-    for (int c = kTcMaxSplit; c >= 2; c--) {
-        if (c > nsteps || tiles * c > 2 * sm_count()) continue;
-        if (tc_resident_clusters(c, smem) >= tiles) {
+    for (int c = kTmMaxSplit; c >= 2; c--) {
+        if (c > nsteps || ntiles * c > 2 * sm_count()) continue;
+        if (tm_resident_clusters<PRE>(c, smem) >= ntiles) {
             split = c;
             break;
         }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)tiles_n, (unsigned)tiles_m, (unsigned)split);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(kTmThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -505,9 +711,31 @@ qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const ui
     attr[0].val.clusterDim.z = (unsigned)split;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tc_kernel, xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, split));
-    QLIN_LAUNCHED("t158_tc_kernel");
+    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tm_kernel<PRE>, xq, tiles, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, T,
+                                 split));
+    QLIN_LAUNCHED("t158_tm_kernel");
     return QLIN_OK;
+}
+
+// work: device scratch of at least t158_tc_workspace_bytes(M, K) bytes,
+// 16-byte aligned, or null (then the converter warps convert the activations
+// at every step of every tile).  convert: write the activation tiles of xq
+// into work first; false when an earlier call with the same xq, M and K on
+// this stream already did.
+qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
+                                     const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st,
+                                     void *work, bool convert) {
+    int tiles_m = 0, T = 0;
+    tm_token_tiles(M, tiles_m, T);
+    if (!work) return launch_tm<false>(xq, nullptr, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, tiles_m, T, st);
+    if (convert) {
+        const int nsteps = (K + kTcKS - 1) / kTcKS;
+        const int64_t threads = (int64_t)tiles_m * T * nsteps;
+        t158_act_tiles_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(xq, M, K, T, tiles_m, nsteps,
+                                                                                 (uint8_t *)work);
+        QLIN_LAUNCHED("t158_act_tiles_kernel");
+    }
+    return launch_tm<true>(xq, (const uint8_t *)work, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, tiles_m, T, st);
 }
 
 }  // namespace qlin

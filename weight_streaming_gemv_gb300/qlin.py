@@ -65,6 +65,8 @@ SIGNATURES = {
     "qlin_w8_quantize": ([_P, _I64, _I64, _P, _I64, _P, _P], _ST),
     "qlin_quant_i8": ([_P, _P, _P, _I, _I, _P], _ST),
     "qlin_t158_i8": ([_P, _P, _P, _I64, _F, _P, _P, _I, _I, _I, _P], _ST),
+    "qlin_t158_i8_workspace_size": ([_I, _I], _SZ),
+    "qlin_t158_i8_ws": ([_P, _P, _P, _I64, _F, _P, _P, _I, _I, _I, _P, _SZ, _P], _ST),
     "qlin_w8_f32": ([_P, _P, _I64, _F, _P, _I, _I, _I, _P], _ST),
     "qlin_w8g_quantize": ([_P, _I64, _I64, _I, _P, _I64, _P, _I64, _P], _ST),
     "qlin_w8g_f32": ([_P, _P, _I64, _P, _I64, _I, _P, _I, _I, _I, _P], _ST),
@@ -187,6 +189,17 @@ def qlin_quant_i8(x, xq, x_scale, M, K, stream=None):
 def qlin_t158_i8(xq, x_scale, w_packed, w_pitch, w_scale, y, acc, M, N, K, stream=None):
     _check("qlin_t158_i8", lib().qlin_t158_i8(_ptr(xq), _ptr(x_scale), _ptr(w_packed), w_pitch, float(w_scale),
                                               _ptr(y), _ptr(acc), M, N, K, _stream(stream)))
+
+
+def qlin_t158_i8_workspace_size(M, K):
+    return int(lib().qlin_t158_i8_workspace_size(M, K))
+
+
+def qlin_t158_i8_ws(xq, x_scale, w_packed, w_pitch, w_scale, y, acc, M, N, K, workspace, workspace_bytes,
+                    stream=None):
+    _check("qlin_t158_i8_ws", lib().qlin_t158_i8_ws(_ptr(xq), _ptr(x_scale), _ptr(w_packed), w_pitch,
+                                                    float(w_scale), _ptr(y), _ptr(acc), M, N, K, _ptr(workspace),
+                                                    workspace_bytes, _stream(stream)))
 
 
 def qlin_w8_f32(x, w8, w_pitch, w_scale, y, M, N, K, stream=None):
