@@ -30,6 +30,7 @@ qlin_status t158_linear_dev_scale(const int8_t *xq, const float *xs, const uint8
                                   const float *ws_ptr, float *y, int M, int N, int K, cudaStream_t st, void *work,
                                   bool convert);
 size_t t158_workspace_bytes(int M, int K);
+qlin_status quant_i8_tiles(const float *x, int8_t *xq, float *xs, int M, int K, void *work, cudaStream_t st);
 
 namespace {
 
@@ -258,15 +259,18 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     for (int j = 0; j < T158_NMAT; j++) W[j] = m->w[j];
     const int rows[T158_NMAT] = {qd, kvd, kvd, d, f, f, d};
     const int cols[T158_NMAT] = {d, d, d, qd, d, d, f};
-    // linear j of layer l on the quantised activations in w.xq / w.xs; the
-    // first linear after each quantisation converts them to tensor-core tiles
-    // once (convert), the ones sharing its input (k, v; up) reuse the tiles
+    // linear j of layer l on the quantised activations in w.xq / w.xs (and,
+    // on the tensor-core path, the tiles the quantiser wrote into w.tiles)
     auto lin = [&](int l, int j, float *out, bool convert) -> qlin_status {
         return t158_linear_dev_scale(w.xq, w.xs, W[j] + (int64_t)l * rows[j] * m->pitch[j], m->pitch[j],
                                      m->scales + (int64_t)l * T158_NMAT + j, out, M, rows[j], cols[j], s, w.tiles,
                                      convert);
     };
-    auto quant = [&](const float *x, int K) { return qlin_quant_i8(x, w.xq, w.xs, M, K, stream); };
+    // the quantiser also writes the tensor-core tiles when the linears take that path
+    const bool tiles = t158_workspace_bytes(M, d) > 0;
+    auto quant = [&](const float *x, int K) {
+        return tiles ? quant_i8_tiles(x, w.xq, w.xs, M, K, w.tiles, s) : qlin_quant_i8(x, w.xq, w.xs, M, K, stream);
+    };
     const int add_blocks = std::max(1, std::min(4 * sm_count(), (int)(((int64_t)M * d + 255) / 256)));
     const size_t attn_smem = (size_t)2 * 32 * hd * sizeof(float);
     const int attn_threads = kAttnGroupThreads * std::min(kAttnMaxGroups, nh / nkv);
@@ -277,7 +281,7 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     for (int l = 0; l < L; l++) {
         if ((st = qlin_rmsnorm(w.h, m->g_attn + (int64_t)l * d, w.xn, M, d, m->eps, stream))) return st;
         if ((st = quant(w.xn, d))) return st;
-        if ((st = lin(l, 0, w.q, true)) || (st = lin(l, 1, w.k, false)) || (st = lin(l, 2, w.v, false))) return st;
+        if ((st = lin(l, 0, w.q, false)) || (st = lin(l, 1, w.k, false)) || (st = lin(l, 2, w.v, false))) return st;
         lanes_rope_kv_kernel<<<M, 256, (size_t)kvd * sizeof(float), s>>>(
             w.q, w.k, w.v, kv_caches, positions, seqs, n_seqs, l, L, m->max_pos, m->rope_cos, m->rope_sin, nh, nkv,
             hd, w.status);
@@ -289,14 +293,14 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
         lanes_attn_merge_kernel<<<dim3(nh, M), 256, (size_t)next_pow2(ncmax) * sizeof(float), s>>>(
             w.attn, ncmax, positions, seqs, n_seqs, m->max_pos, nh, hd, w.att);
         QLIN_LAUNCHED("lanes_attn_merge_kernel");
-        if ((st = quant(w.att, qd)) || (st = lin(l, 3, w.y, true))) return st;
+        if ((st = quant(w.att, qd)) || (st = lin(l, 3, w.y, false))) return st;
         lanes_add_kernel<<<add_blocks, 256, 0, s>>>(w.h, w.y, (int64_t)M * d);
         QLIN_LAUNCHED("lanes_add_kernel");
         if ((st = qlin_rmsnorm(w.h, m->g_ffn + (int64_t)l * d, w.xn, M, d, m->eps, stream))) return st;
         if ((st = quant(w.xn, d))) return st;
-        if ((st = lin(l, 4, w.g, true)) || (st = lin(l, 5, w.u, false))) return st;
+        if ((st = lin(l, 4, w.g, false)) || (st = lin(l, 5, w.u, false))) return st;
         if ((st = qlin_geglu(w.g, w.u, w.g, M * f, stream))) return st;
-        if ((st = quant(w.g, f)) || (st = lin(l, 6, w.y, true))) return st;
+        if ((st = quant(w.g, f)) || (st = lin(l, 6, w.y, false))) return st;
         lanes_add_kernel<<<add_blocks, 256, 0, s>>>(w.h, w.y, (int64_t)M * d);
         QLIN_LAUNCHED("lanes_add_kernel");
     }
@@ -309,11 +313,10 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
 int decode_lanes_t158_launches(const t158_model *m, int n_lanes) {
     qlin::clear_error();
     if (check_lanes_model(m) || n_lanes < 1) return -1;
-    // embed; per layer 2 norms, 4 quantisations, 7 linears, rope/append, 2 attention, 2 adds, geglu
-    // (+ 4 activation-tile conversions when the linears run on the tensor cores); final norm; the
-    // lanes' output layer (a split and a table pass per 64 lanes)
-    const int tiles = t158_workspace_bytes(n_lanes, m->dim) > 0 ? 4 : 0;
-    return 1 + m->n_layers * (19 + tiles) + 1 + 2 * ((n_lanes + 63) / 64);
+    // embed; per layer 2 norms, 4 quantisations (with the tensor-core tiles from 8 lanes), 7 linears,
+    // rope/append, 2 attention, 2 adds, geglu; final norm; the lanes' output layer (a split and a
+    // table pass per 64 lanes)
+    return 1 + m->n_layers * 19 + 1 + 2 * ((n_lanes + 63) / 64);
 }
 
 qlin_status decode_lanes_t158_status(void *workspace, qlin_stream_t stream) {

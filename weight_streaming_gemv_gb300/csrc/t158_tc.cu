@@ -332,6 +332,61 @@ __global__ void __launch_bounds__(256) t158_act_tiles_kernel(const int8_t *__res
     tm_put_row(out + ((int64_t)tt * nsteps + s) * tm_b_bytes(T), in, r);
 }
 
+// The activation quantiser (absmax per token, as quant_i8_kernel) fused with
+// the tile conversion of t158_act_tiles_kernel: block m quantises token m and
+// writes its codes to xq and, as fp16 in K' order, into its row of every
+// step's tile image; blocks M .. tiles_m T - 1 zero the padding rows.  One
+// thread per 16-byte chunk (eight K' values of one step); every input is read
+// by exactly one chunk.
+__global__ void __launch_bounds__(256) t158_quant_tiles_kernel(const float *__restrict__ x, int8_t *__restrict__ xq,
+                                                               float *__restrict__ xs, int M, int K, int T,
+                                                               int tiles_m, int nsteps, uint8_t *__restrict__ out) {
+    __shared__ float red[32];
+    const int m = blockIdx.x;
+    const int tt = m / T, r = m % T;
+    const bool real = m < M;
+    const float *row = x + (int64_t)(real ? m : 0) * K;
+    float sc = 0.0f, rinv = 0.0f;
+    if (real) {
+        float a = 0.0f;
+        for (int k = threadIdx.x; k < K; k += blockDim.x) a = fmaxf(a, fabsf(row[k]));
+        a = warp_max(a);
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+            v = warp_max(v);
+            if (threadIdx.x == 0) red[0] = v;
+        }
+        __syncthreads();
+        sc = quant_scale(red[0]);
+        rinv = __fdiv_rn(1.0f, sc);
+        if (threadIdx.x == 0) xs[m] = sc;
+    }
+    for (int c = threadIdx.x; c < nsteps * kTcChunks; c += blockDim.x) {
+        const int s = c / kTcChunks, kc = c % kTcChunks;
+        const int i = kc >> 1, jb = 8 * (kc & 1);  // digit i of packed-byte columns jb .. jb + 7
+        uint32_t h[4];
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            int q2[2];
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const int k = s * kTcKS + 5 * (jb + 2 * p + e) + i;
+                q2[e] = 0;
+                if (real && k < K) {
+                    q2[e] = quant_code_r(row[k], sc, rinv);
+                    xq[(int64_t)m * K + k] = (int8_t)q2[e];
+                }
+            }
+            const __half2 hv = __halves2half2(__int2half_rn(q2[0]), __int2half_rn(q2[1]));
+            h[p] = *reinterpret_cast<const uint32_t *>(&hv);
+        }
+        *reinterpret_cast<uint4 *>(out + ((int64_t)tt * nsteps + s) * tm_b_bytes(T) + tc_off(r, kc)) =
+            make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
 // Grid: (weight-row tiles, token tiles, split); a cluster is the `split` CTAs
 // of one tile, each over its own range of K steps.  split == 1: no cluster
 // reduction.  T: tokens per tile (a multiple of 32, at most kTmMaxTok).
@@ -736,6 +791,19 @@ qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const ui
         QLIN_LAUNCHED("t158_act_tiles_kernel");
     }
     return launch_tm<true>(xq, (const uint8_t *)work, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, tiles_m, T, st);
+}
+
+// qlin_quant_i8 (same xq and xs) that also writes the activation tiles of
+// t158_linear_tensor_cores into work (t158_tc_workspace_bytes(M, K) bytes),
+// so that the linears on this input run with convert = false.
+qlin_status quant_i8_tiles(const float *x, int8_t *xq, float *xs, int M, int K, void *work, cudaStream_t st) {
+    int tiles_m = 0, T = 0;
+    tm_token_tiles(M, tiles_m, T);
+    const int nsteps = (K + kTcKS - 1) / kTcKS;
+    t158_quant_tiles_kernel<<<(unsigned)(tiles_m * T), 256, 0, st>>>(x, xq, xs, M, K, T, tiles_m, nsteps,
+                                                                     (uint8_t *)work);
+    QLIN_LAUNCHED("t158_quant_tiles_kernel");
+    return QLIN_OK;
 }
 
 }  // namespace qlin
