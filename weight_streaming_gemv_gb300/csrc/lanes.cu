@@ -94,12 +94,23 @@ __device__ __forceinline__ LaneAttnWs lane_attn_ws(float *base, int lane, int nc
     return w;
 }
 
+// 16 bytes global -> shared without a register round trip; every copy of a
+// thread stays in flight until its wait.
+__device__ __forceinline__ void lanes_cp16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void lanes_cp_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 constexpr int kAttnGroupThreads = 128;  // threads per query head in the chunk kernel
 constexpr int kAttnMaxGroups = 8;        // query heads served at once (1024 threads)
 
 // grid (ncmax, nkv, lanes), block hpar * 128 threads: chunk c of KV head g of
 // lane i for every query head of the group.  The chunk's k and v rows are
-// read once into shared memory (16-byte loads); hpar heads then run at once,
+// read once into shared memory (16-byte asynchronous copies, all of them in
+// flight together); hpar heads then run at once,
 // each on its own 128 threads and hardware barrier.  Chunks past the lane's
 // position exit.
 __global__ void __launch_bounds__(kAttnGroupThreads * kAttnMaxGroups)
@@ -121,9 +132,10 @@ __global__ void __launch_bounds__(kAttnGroupThreads * kAttnMaxGroups)
     const int hd4 = hd / 4;
     for (int e = threadIdx.x; e < nt * hd4; e += blockDim.x) {
         const int t = e / hd4, dd = e - t * hd4;
-        reinterpret_cast<float4 *>(Ks)[e] = *reinterpret_cast<const float4 *>(kc + (int64_t)t * ld + 4 * dd);
-        reinterpret_cast<float4 *>(Vs)[e] = *reinterpret_cast<const float4 *>(vc + (int64_t)t * ld + 4 * dd);
+        lanes_cp16(Ks + 4 * e, kc + (int64_t)t * ld + 4 * dd);
+        lanes_cp16(Vs + 4 * e, vc + (int64_t)t * ld + 4 * dd);
     }
+    lanes_cp_wait_all();  // this thread's copies have landed; the barrier below publishes them
     LaneAttnWs w = lane_attn_ws(ws, i, ncmax, nh, hd);
     const int grp = nh / nkv, hpar = blockDim.x / kAttnGroupThreads;
     const int gi = threadIdx.x / kAttnGroupThreads;
@@ -139,6 +151,164 @@ __global__ void __launch_bounds__(kAttnGroupThreads * kAttnMaxGroups)
             attention_chunk(qs[gi], Ks, Vs, hd, nt, hd, w.m + h * ncmax + c, w.S + h * ncmax + c,
                             w.U + ((int64_t)h * ncmax + c) * hd, sc[gi], g);
     }
+}
+
+// Persistent attention over lanes: the chunk partials of lanes_attn_chunk_kernel
+// (the same arithmetic, term for term, so the same bits), with each CTA
+// streaming a range of units (lane, KV head, chunk) through kAttnBufs
+// shared-memory buffers that asynchronous copies fill ahead of use.  Units are
+// numbered chunk fastest, so a CTA's consecutive units share a lane and KV head
+// and its q rows stay in registers; units past a lane's position are skipped.
+// Per unit: each warp scores positions warp and warp + 16 against every query
+// head of the group (one k row read serves them all), one warp per head takes
+// the softmax, and all threads form the weighted value sums.
+constexpr int kAttnThreads = 512;
+constexpr int kAttnBufs = 3;
+
+template <int HD, int GRP>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    lanes_attn_kernel(const float *__restrict__ q, const float *__restrict__ kv, const int32_t *pos,
+                      const int32_t *seq, int n_seqs, int layer, int L, int max_pos, int nh, int nkv, int M,
+                      float *ws, int ncmax) {
+    constexpr int S = HD / 32;   // dims per lane in the scores
+    constexpr int CH = 32 * HD;  // floats of a chunk's k (or v) rows
+    extern __shared__ __align__(16) float abuf[];  // [kAttnBufs][2][32][HD]
+    __shared__ float sc[GRP][32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int grp = nh / nkv;  // query heads per KV head, <= GRP
+    const int ld = nkv * HD;
+    const int64_t per_lane = (int64_t)nkv * ncmax;
+    const int64_t units = (int64_t)M * per_lane;
+    const int64_t u_hi = units * (blockIdx.x + 1) / gridDim.x;
+    int64_t next = units * blockIdx.x / gridDim.x;
+    const float div = __fsqrt_rn((float)HD);
+
+    // the next unit of this CTA with work, or -1 (every thread computes the same)
+    auto advance = [&]() -> int64_t {
+        for (; next < u_hi; next++) {
+            const int i = (int)(next / per_lane), c = (int)(next % ncmax);
+            if (lane_ok(pos[i], seq[i], max_pos, n_seqs) && c * 32 <= pos[i]) return next++;
+        }
+        return -1;
+    };
+    auto issue = [&](int64_t u, int b) {
+        const int i = (int)(u / per_lane), g = (int)((u / ncmax) % nkv), c = (int)(u % ncmax);
+        const int p = pos[i], s = seq[i];
+        const int t0 = c * 32, nt = min(32, p + 1 - t0);
+        const float *kc = kv + (((int64_t)s * L + layer) * 2 + 0) * max_pos * ld + (int64_t)t0 * ld + g * HD;
+        const float *vc = kc + (int64_t)max_pos * ld;
+        float *Kb = abuf + (size_t)b * 2 * CH, *Vb = Kb + CH;
+        for (int e = tid; e < nt * (HD / 4); e += kAttnThreads) {
+            const int t = e / (HD / 4), dd = e - t * (HD / 4);
+            lanes_cp16(Kb + 4 * e, kc + (int64_t)t * ld + 4 * dd);
+            lanes_cp16(Vb + 4 * e, vc + (int64_t)t * ld + 4 * dd);
+        }
+    };
+
+    int64_t slot[kAttnBufs];
+#pragma unroll
+    for (int b = 0; b < kAttnBufs; b++) {
+        slot[b] = advance();
+        if (slot[b] >= 0) issue(slot[b], b);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    float qr[GRP][S];
+    int64_t cur = -1;  // lane * nkv + KV head whose q rows are in qr
+    for (int k = 0;; k++) {
+        const int b = k % kAttnBufs;
+        int64_t u = -1;
+#pragma unroll
+        for (int j = 0; j < kAttnBufs; j++)
+            if (j == b) u = slot[j];
+        if (u < 0) break;
+        asm volatile("cp.async.wait_group %0;" ::"n"(kAttnBufs - 1) : "memory");
+        __syncthreads();  // unit u's k and v rows are in buffer b (every thread's copies)
+        const int i = (int)(u / per_lane), g = (int)((u / ncmax) % nkv), c = (int)(u % ncmax);
+        const int p = pos[i];
+        const int t0 = c * 32, nt = min(32, p + 1 - t0);
+        const float *Kb = abuf + (size_t)b * 2 * CH, *Vb = Kb + CH;
+        LaneAttnWs w = lane_attn_ws(ws, i, ncmax, nh, HD);
+        if ((int64_t)i * nkv + g != cur) {
+            cur = (int64_t)i * nkv + g;
+#pragma unroll
+            for (int h = 0; h < GRP; h++)
+#pragma unroll
+                for (int e = 0; e < S; e++)
+                    qr[h][e] = h < grp ? q[((int64_t)i * nh + g * grp + h) * HD + lane * S + e] : 0.0f;
+        }
+        // scores: lane owns dims [lane S, lane S + S), a tree over them, then across lanes
+        for (int t = warp; t < 32; t += kAttnThreads / 32) {
+            float kr[S];
+            if (t < nt) {
+                const float *kt = Kb + t * HD;
+                if constexpr (S == 8) {
+                    // two 16-byte loads; lanes 4..7 of each phase read their upper half first
+                    const float4 *k4 = reinterpret_cast<const float4 *>(kt + lane * S);
+                    const int sw = (lane >> 2) & 1;
+                    const float4 f = k4[sw], s2 = k4[sw ^ 1];
+                    const float4 lo = sw ? s2 : f, hi = sw ? f : s2;
+                    kr[0] = lo.x, kr[1] = lo.y, kr[2] = lo.z, kr[3] = lo.w;
+                    kr[4] = hi.x, kr[5] = hi.y, kr[6] = hi.z, kr[7] = hi.w;
+                } else if constexpr (S == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(kt + lane * 4);
+                    kr[0] = v.x, kr[1] = v.y, kr[2] = v.z, kr[3] = v.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < S; e++) kr[e] = kt[lane * S + e];
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < GRP; h++) {
+                float part = 0.0f;
+                if (t < nt) {
+                    float pp[S];
+#pragma unroll
+                    for (int e = 0; e < S; e++) pp[e] = __fmul_rn(qr[h][e], kr[e]);
+#pragma unroll
+                    for (int st = 1; st < S; st <<= 1)
+#pragma unroll
+                        for (int e = 0; e < S; e += 2 * st) pp[e] = __fadd_rn(pp[e], pp[e + st]);
+                    part = pp[0];
+                }
+                const float sv = warp_psum(part);
+                if (lane == 0) sc[h][t] = (t < nt) ? __fdiv_rn(sv, div) : 0.0f;
+            }
+        }
+        __syncthreads();
+        if (warp < grp) {  // softmax of head `warp` over the chunk
+            const int h = warp, t = lane;
+            const float m = warp_max(t < nt ? sc[h][t] : -__int_as_float(0x7f800000));
+            const float e = (t < nt) ? exp32(__fsub_rn(sc[h][t], m)) : 0.0f;
+            __syncwarp();
+            sc[h][t] = e;
+            const float Ssum = warp_psum(e);
+            if (t == 0) {
+                const int hg = g * grp + h;
+                w.m[hg * ncmax + c] = m;
+                w.S[hg * ncmax + c] = Ssum;
+            }
+        }
+        __syncthreads();
+        for (int o = tid; o < grp * HD; o += kAttnThreads) {
+            const int h = o / HD, d = o - h * HD;
+            float pp[32];
+#pragma unroll
+            for (int t = 0; t < 32; t++) pp[t] = (t < nt) ? __fmul_rn(sc[h][t], Vb[t * HD + d]) : 0.0f;
+#pragma unroll
+            for (int st = 1; st < 32; st <<= 1)
+#pragma unroll
+                for (int t = 0; t < 32; t += 2 * st) pp[t] = __fadd_rn(pp[t], pp[t + st]);
+            w.U[((int64_t)(g * grp + h) * ncmax + c) * HD + d] = pp[0];
+        }
+        __syncthreads();  // buffer b and sc are free again
+        const int64_t un = advance();
+#pragma unroll
+        for (int j = 0; j < kAttnBufs; j++)
+            if (j == b) slot[j] = un;
+        if (un >= 0) issue(un, b);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // grid (nh, lanes): merge the lane's chunks of head h
@@ -201,6 +371,27 @@ LanesWs carve_lanes(const t158_model *m, int max_lanes, char *base) {
     w.tiles = take(t158_workspace_bytes(max_lanes, (int)big));
     w.bytes = off;
     return w;
+}
+
+// The persistent attention kernel for head_dim 64..256 and up to 8 query
+// heads per KV head (one CTA per SM over every lane's units); null otherwise.
+template <int HD>
+const void *attn_kernel_for(int grp) {
+    switch (grp <= 1 ? 1 : grp <= 2 ? 2 : grp <= 4 ? 4 : grp <= 8 ? 8 : 0) {
+        case 1: return (const void *)lanes_attn_kernel<HD, 1>;
+        case 2: return (const void *)lanes_attn_kernel<HD, 2>;
+        case 4: return (const void *)lanes_attn_kernel<HD, 4>;
+        case 8: return (const void *)lanes_attn_kernel<HD, 8>;
+        default: return nullptr;
+    }
+}
+const void *attn_kernel(int hd, int grp) {
+    switch (hd) {
+        case 64: return attn_kernel_for<64>(grp);
+        case 128: return attn_kernel_for<128>(grp);
+        case 256: return attn_kernel_for<256>(grp);
+        default: return nullptr;
+    }
 }
 
 qlin_status check_lanes_model(const t158_model *m) {
@@ -275,6 +466,15 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     const size_t attn_smem = (size_t)2 * 32 * hd * sizeof(float);
     const int attn_threads = kAttnGroupThreads * std::min(kAttnMaxGroups, nh / nkv);
     if (attn_smem > 48 * 1024) blocks_per_sm((const void *)lanes_attn_chunk_kernel, attn_smem);  // raises the limit once
+    // persistent attention: one CTA per SM (or per unit when there are fewer)
+    const void *attn_k = attn_kernel(hd, nh / nkv);
+    const size_t attn_k_smem = (size_t)kAttnBufs * 2 * 32 * hd * sizeof(float);
+    const int64_t attn_units = (int64_t)M * nkv * ncmax;
+    const int attn_grid = (int)std::min<int64_t>(sm_count(), attn_units);
+    if (attn_k) {
+        QLIN_REQUIRE((int)attn_k_smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "decode_lanes_t158: attention buffers");
+        blocks_per_sm(attn_k, attn_k_smem);  // raises the dynamic shared-memory limit
+    }
 
     lanes_embed_kernel<<<M, 256, 0, s>>>(m->emb, m->vocab, d, tokens, w.h, w.status);
     QLIN_LAUNCHED("lanes_embed_kernel");
@@ -286,10 +486,18 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
             w.q, w.k, w.v, kv_caches, positions, seqs, n_seqs, l, L, m->max_pos, m->rope_cos, m->rope_sin, nh, nkv,
             hd, w.status);
         QLIN_LAUNCHED("lanes_rope_kv_kernel");
-        lanes_attn_chunk_kernel<<<dim3(ncmax, nkv, M), attn_threads, attn_smem, s>>>(w.q, kv_caches, positions, seqs, n_seqs,
-                                                                             l, L, m->max_pos, nh, nkv, hd, w.attn,
-                                                                             ncmax);
-        QLIN_LAUNCHED("lanes_attn_chunk_kernel");
+        if (attn_k) {
+            void *args[] = {(void *)&w.q, (void *)&kv_caches, (void *)&positions, (void *)&seqs, (void *)&n_seqs,
+                            (void *)&l, (void *)&L, (void *)&m->max_pos, (void *)&m->n_heads, (void *)&m->n_kv_heads,
+                            (void *)&M, (void *)&w.attn, (void *)&ncmax};
+            QLIN_CUDA(cudaLaunchKernel(attn_k, dim3(attn_grid), dim3(kAttnThreads), args, attn_k_smem, s));
+            QLIN_LAUNCHED("lanes_attn_kernel");
+        } else {
+            lanes_attn_chunk_kernel<<<dim3(ncmax, nkv, M), attn_threads, attn_smem, s>>>(w.q, kv_caches, positions, seqs, n_seqs,
+                                                                                 l, L, m->max_pos, nh, nkv, hd, w.attn,
+                                                                                 ncmax);
+            QLIN_LAUNCHED("lanes_attn_chunk_kernel");
+        }
         lanes_attn_merge_kernel<<<dim3(nh, M), 256, (size_t)next_pow2(ncmax) * sizeof(float), s>>>(
             w.attn, ncmax, positions, seqs, n_seqs, m->max_pos, nh, hd, w.att);
         QLIN_LAUNCHED("lanes_attn_merge_kernel");
