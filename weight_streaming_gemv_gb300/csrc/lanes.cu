@@ -31,6 +31,10 @@ qlin_status t158_linear_dev_scale(const int8_t *xq, const float *xs, const uint8
                                   bool convert);
 size_t t158_workspace_bytes(int M, int K);
 qlin_status quant_i8_tiles(const float *x, int8_t *xq, float *xs, int M, int K, void *work, cudaStream_t st);
+qlin_status norm_quant_tiles(float *h, const float *y, const float *gain, float eps, int8_t *xq, float *xs, int M,
+                             int K, void *work, cudaStream_t st);
+qlin_status geglu_quant_tiles(const float *gate, const float *up, int8_t *xq, float *xs, int M, int K, void *work,
+                              cudaStream_t st);
 
 namespace {
 
@@ -457,11 +461,8 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
                                      m->scales + (int64_t)l * T158_NMAT + j, out, M, rows[j], cols[j], s, w.tiles,
                                      convert);
     };
-    // the quantiser also writes the tensor-core tiles when the linears take that path
-    const bool tiles = t158_workspace_bytes(M, d) > 0;
-    auto quant = [&](const float *x, int K) {
-        return tiles ? quant_i8_tiles(x, w.xq, w.xs, M, K, w.tiles, s) : qlin_quant_i8(x, w.xq, w.xs, M, K, stream);
-    };
+    // the quantisers also write the tensor-core tiles when the linears take that path
+    void *const tiles = t158_workspace_bytes(M, d) > 0 ? w.tiles : nullptr;
     const int add_blocks = std::max(1, std::min(4 * sm_count(), (int)(((int64_t)M * d + 255) / 256)));
     const size_t attn_smem = (size_t)2 * 32 * hd * sizeof(float);
     const int attn_threads = kAttnGroupThreads * std::min(kAttnMaxGroups, nh / nkv);
@@ -479,8 +480,10 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     lanes_embed_kernel<<<M, 256, 0, s>>>(m->emb, m->vocab, d, tokens, w.h, w.status);
     QLIN_LAUNCHED("lanes_embed_kernel");
     for (int l = 0; l < L; l++) {
-        if ((st = qlin_rmsnorm(w.h, m->g_attn + (int64_t)l * d, w.xn, M, d, m->eps, stream))) return st;
-        if ((st = quant(w.xn, d))) return st;
+        // (the previous layer's FFN output joins the residual stream here)
+        if ((st = norm_quant_tiles(w.h, l > 0 ? w.y : nullptr, m->g_attn + (int64_t)l * d, m->eps, w.xq, w.xs, M, d,
+                                   tiles, s)))
+            return st;
         if ((st = lin(l, 0, w.q, false)) || (st = lin(l, 1, w.k, false)) || (st = lin(l, 2, w.v, false))) return st;
         lanes_rope_kv_kernel<<<M, 256, (size_t)kvd * sizeof(float), s>>>(
             w.q, w.k, w.v, kv_caches, positions, seqs, n_seqs, l, L, m->max_pos, m->rope_cos, m->rope_sin, nh, nkv,
@@ -501,17 +504,13 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
         lanes_attn_merge_kernel<<<dim3(nh, M), 256, (size_t)next_pow2(ncmax) * sizeof(float), s>>>(
             w.attn, ncmax, positions, seqs, n_seqs, m->max_pos, nh, hd, w.att);
         QLIN_LAUNCHED("lanes_attn_merge_kernel");
-        if ((st = quant(w.att, qd)) || (st = lin(l, 3, w.y, false))) return st;
-        lanes_add_kernel<<<add_blocks, 256, 0, s>>>(w.h, w.y, (int64_t)M * d);
-        QLIN_LAUNCHED("lanes_add_kernel");
-        if ((st = qlin_rmsnorm(w.h, m->g_ffn + (int64_t)l * d, w.xn, M, d, m->eps, stream))) return st;
-        if ((st = quant(w.xn, d))) return st;
+        if ((st = quant_i8_tiles(w.att, w.xq, w.xs, M, qd, tiles, s)) || (st = lin(l, 3, w.y, false))) return st;
+        if ((st = norm_quant_tiles(w.h, w.y, m->g_ffn + (int64_t)l * d, m->eps, w.xq, w.xs, M, d, tiles, s))) return st;
         if ((st = lin(l, 4, w.g, false)) || (st = lin(l, 5, w.u, false))) return st;
-        if ((st = qlin_geglu(w.g, w.u, w.g, M * f, stream))) return st;
-        if ((st = quant(w.g, f)) || (st = lin(l, 6, w.y, false))) return st;
-        lanes_add_kernel<<<add_blocks, 256, 0, s>>>(w.h, w.y, (int64_t)M * d);
-        QLIN_LAUNCHED("lanes_add_kernel");
+        if ((st = geglu_quant_tiles(w.g, w.u, w.xq, w.xs, M, f, tiles, s)) || (st = lin(l, 6, w.y, false))) return st;
     }
+    lanes_add_kernel<<<add_blocks, 256, 0, s>>>(w.h, w.y, (int64_t)M * d);  // the last layer's FFN output
+    QLIN_LAUNCHED("lanes_add_kernel");
     if ((st = qlin_rmsnorm(w.h, m->g_final, w.xn, M, d, m->eps, stream))) return st;
     // the output layer for all lanes in one pass over the table (tensor cores)
     if ((st = qlin_lm_head_lanes(m->emb, w.xn, m->vocab, d, M, logits, next, w.lm, w.lm_bytes, stream))) return st;
@@ -521,10 +520,10 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
 int decode_lanes_t158_launches(const t158_model *m, int n_lanes) {
     qlin::clear_error();
     if (check_lanes_model(m) || n_lanes < 1) return -1;
-    // embed; per layer 2 norms, 4 quantisations (with the tensor-core tiles from 8 lanes), 7 linears,
-    // rope/append, 2 attention, 2 adds, geglu; final norm; the lanes' output layer (a split and a
-    // table pass per 64 lanes)
-    return 1 + m->n_layers * 19 + 1 + 2 * ((n_lanes + 63) / 64);
+    // embed; per layer 4 quantisations (two behind the residual add and RMSNorm, one behind the GeGLU
+    // product), 7 linears, rope/append, 2 attention; the last residual add and the final norm; the
+    // lanes' output layer (a split and a table pass per 64 lanes)
+    return 1 + m->n_layers * 14 + 2 + 2 * ((n_lanes + 63) / 64);
 }
 
 qlin_status decode_lanes_t158_status(void *workspace, qlin_stream_t stream) {

@@ -46,6 +46,7 @@
 #include <tuple>
 
 #include "common.cuh"
+#include "decode_ops.cuh"
 #include "stream.cuh"
 
 namespace qlin {
@@ -332,26 +333,69 @@ __global__ void __launch_bounds__(256) t158_act_tiles_kernel(const int8_t *__res
     tm_put_row(out + ((int64_t)tt * nsteps + s) * tm_b_bytes(T), in, r);
 }
 
-// The activation quantiser (absmax per token, as quant_i8_kernel) fused with
-// the tile conversion of t158_act_tiles_kernel: block m quantises token m and
-// writes its codes to xq and, as fp16 in K' order, into its row of every
-// step's tile image; blocks M .. tiles_m T - 1 zero the padding rows.  One
-// thread per 16-byte chunk (eight K' values of one step); every input is read
-// by exactly one chunk.
-__global__ void __launch_bounds__(256) t158_quant_tiles_kernel(const float *__restrict__ x, int8_t *__restrict__ xq,
-                                                               float *__restrict__ xs, int M, int K, int T,
-                                                               int tiles_m, int nsteps, uint8_t *__restrict__ out) {
+// Where the row a quantiser block quantises comes from.
+enum QtMode : int {
+    kQtRow = 0,   // x[m] as it is
+    kQtNorm = 1,  // h[m] (+= y[m] first, written back, when y is given), then RMSNorm with gain g
+    kQtGeglu = 2  // gelu(x[m]) * u[m], elementwise
+};
+struct QtArgs {
+    const float *x;  // kQtRow, kQtGeglu: the row (gate); kQtNorm: unused
+    float *h;        // kQtNorm: the residual stream
+    const float *y;  // kQtNorm: added to h first, or null
+    const float *g;  // kQtNorm: the RMSNorm gain
+    const float *u;  // kQtGeglu: the up projection
+    float eps;
+    int8_t *xq;
+    float *xs;
+    uint8_t *tiles;  // activation tiles (t158_tc_workspace_bytes(M, K)), or null
+    int M, K, T, tiles_m, nsteps;
+};
+
+// The activation quantiser (absmax per token, as quant_i8_kernel) with the
+// tile conversion of t158_act_tiles_kernel, behind an optional row prologue
+// (the residual add and RMSNorm of rmsnorm_kernel, or the GeGLU product of
+// geglu_kernel, the same operations in the same order): block m builds its
+// row (in shared memory for the prologues), quantises it to xq and, as fp16
+// in K' order, into its row of every step's tile image; blocks M ..
+// tiles_m T - 1 zero the padding rows.  One thread per 16-byte chunk (eight
+// K' values of one step); every input is read by exactly one chunk.
+constexpr int kQtThreads = 1024;  // a whole row per block: wide blocks keep a few tokens fast
+
+template <int MODE>
+__global__ void __launch_bounds__(kQtThreads) t158_quant_tiles_kernel(QtArgs a) {
+    extern __shared__ float qt_row[];  // prologues: [K] the row, then [next_pow2(K)] scratch (kQtNorm)
     __shared__ float red[32];
-    const int m = blockIdx.x;
-    const int tt = m / T, r = m % T;
-    const bool real = m < M;
-    const float *row = x + (int64_t)(real ? m : 0) * K;
+    const int m = blockIdx.x, K = a.K;
+    const bool real = m < a.M;
+    const float *row = nullptr;
+    if (real) {
+        if (MODE == kQtRow) {
+            row = a.x + (int64_t)m * K;
+        } else if (MODE == kQtGeglu) {
+            const float *gr = a.x + (int64_t)m * K, *ur = a.u + (int64_t)m * K;
+            for (int k = threadIdx.x; k < K; k += blockDim.x) qt_row[k] = __fmul_rn(gelu32(gr[k]), ur[k]);
+            __syncthreads();
+            row = qt_row;
+        } else {
+            float *hr = a.h + (int64_t)m * K;
+            if (a.y) {
+                const float *yr = a.y + (int64_t)m * K;
+                for (int k = threadIdx.x; k < K; k += blockDim.x) hr[k] = __fadd_rn(hr[k], yr[k]);
+            }
+            // each thread reads back only the elements it wrote; rmsnorm_row syncs before the sum
+            rmsnorm_row(hr, a.g, qt_row, K, a.eps, qt_row + K, red, whole_block());
+            __syncthreads();
+            row = qt_row;
+        }
+    }
     float sc = 0.0f, rinv = 0.0f;
     if (real) {
-        float a = 0.0f;
-        for (int k = threadIdx.x; k < K; k += blockDim.x) a = fmaxf(a, fabsf(row[k]));
-        a = warp_max(a);
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+        float am = 0.0f;
+        for (int k = threadIdx.x; k < K; k += blockDim.x) am = fmaxf(am, fabsf(row[k]));
+        am = warp_max(am);
+        __syncthreads();  // red is free (the prologue's sums are done with it)
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = am;
         __syncthreads();
         if (threadIdx.x < 32) {
             float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
@@ -361,12 +405,18 @@ __global__ void __launch_bounds__(256) t158_quant_tiles_kernel(const float *__re
         __syncthreads();
         sc = quant_scale(red[0]);
         rinv = __fdiv_rn(1.0f, sc);
-        if (threadIdx.x == 0) xs[m] = sc;
+        if (threadIdx.x == 0) a.xs[m] = sc;
     }
-    for (int c = threadIdx.x; c < nsteps * kTcChunks; c += blockDim.x) {
+    if (!a.tiles) {  // codes only
+        if (real)
+            for (int k = threadIdx.x; k < K; k += blockDim.x) a.xq[(int64_t)m * K + k] = (int8_t)quant_code_r(row[k], sc, rinv);
+        return;
+    }
+    const int tt = m / a.T, r = m % a.T;
+    for (int c = threadIdx.x; c < a.nsteps * kTcChunks; c += blockDim.x) {
         const int s = c / kTcChunks, kc = c % kTcChunks;
         const int i = kc >> 1, jb = 8 * (kc & 1);  // digit i of packed-byte columns jb .. jb + 7
-        uint32_t h[4];
+        uint32_t hh[4];
 #pragma unroll
         for (int p = 0; p < 4; p++) {
             int q2[2];
@@ -376,14 +426,14 @@ __global__ void __launch_bounds__(256) t158_quant_tiles_kernel(const float *__re
                 q2[e] = 0;
                 if (real && k < K) {
                     q2[e] = quant_code_r(row[k], sc, rinv);
-                    xq[(int64_t)m * K + k] = (int8_t)q2[e];
+                    a.xq[(int64_t)m * K + k] = (int8_t)q2[e];
                 }
             }
             const __half2 hv = __halves2half2(__int2half_rn(q2[0]), __int2half_rn(q2[1]));
-            h[p] = *reinterpret_cast<const uint32_t *>(&hv);
+            hh[p] = *reinterpret_cast<const uint32_t *>(&hv);
         }
-        *reinterpret_cast<uint4 *>(out + ((int64_t)tt * nsteps + s) * tm_b_bytes(T) + tc_off(r, kc)) =
-            make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(a.tiles + ((int64_t)tt * a.nsteps + s) * tm_b_bytes(a.T) + tc_off(r, kc)) =
+            make_uint4(hh[0], hh[1], hh[2], hh[3]);
     }
 }
 
@@ -793,17 +843,53 @@ qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const ui
     return launch_tm<true>(xq, (const uint8_t *)work, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, tiles_m, T, st);
 }
 
-// qlin_quant_i8 (same xq and xs) that also writes the activation tiles of
-// t158_linear_tensor_cores into work (t158_tc_workspace_bytes(M, K) bytes),
-// so that the linears on this input run with convert = false.
-qlin_status quant_i8_tiles(const float *x, int8_t *xq, float *xs, int M, int K, void *work, cudaStream_t st) {
+// The quantiser kernels' launch: one block per token (per padded token row
+// when tiles are written), with the row prologue's shared memory.
+template <int MODE>
+static qlin_status launch_qt(QtArgs a, void *work, cudaStream_t st) {
     int tiles_m = 0, T = 0;
-    tm_token_tiles(M, tiles_m, T);
-    const int nsteps = (K + kTcKS - 1) / kTcKS;
-    t158_quant_tiles_kernel<<<(unsigned)(tiles_m * T), 256, 0, st>>>(x, xq, xs, M, K, T, tiles_m, nsteps,
-                                                                     (uint8_t *)work);
+    tm_token_tiles(a.M, tiles_m, T);
+    a.T = T;
+    a.tiles_m = tiles_m;
+    a.nsteps = (a.K + kTcKS - 1) / kTcKS;
+    a.tiles = (uint8_t *)work;
+    const size_t smem = MODE == kQtRow     ? 0
+                        : MODE == kQtGeglu ? (size_t)a.K * sizeof(float)
+                                           : (size_t)(a.K + next_pow2(a.K)) * sizeof(float);
+    QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "quantiser: row of %d too long", a.K);
+    if (smem > 48 * 1024) blocks_per_sm((const void *)t158_quant_tiles_kernel<MODE>, smem);
+    const unsigned grid = (unsigned)(work ? tiles_m * T : a.M);
+    t158_quant_tiles_kernel<MODE><<<grid, kQtThreads, smem, st>>>(a);
     QLIN_LAUNCHED("t158_quant_tiles_kernel");
     return QLIN_OK;
+}
+
+// qlin_quant_i8 (the same xq and xs) that also writes the activation tiles of
+// t158_linear_tensor_cores into work (t158_tc_workspace_bytes(M, K) bytes;
+// null: codes only), so that the linears on this input run with convert =
+// false.
+qlin_status quant_i8_tiles(const float *x, int8_t *xq, float *xs, int M, int K, void *work, cudaStream_t st) {
+    QtArgs a{};
+    a.x = x, a.xq = xq, a.xs = xs, a.M = M, a.K = K;
+    return launch_qt<kQtRow>(a, work, st);
+}
+
+// h[m] += y[m] (y may be null), then the quantiser on RMSNorm(h[m]) * gain:
+// rmsnorm_kernel and quant_i8_tiles in one launch, the same values.
+qlin_status norm_quant_tiles(float *h, const float *y, const float *gain, float eps, int8_t *xq, float *xs, int M,
+                             int K, void *work, cudaStream_t st) {
+    QtArgs a{};
+    a.h = h, a.y = y, a.g = gain, a.eps = eps, a.xq = xq, a.xs = xs, a.M = M, a.K = K;
+    return launch_qt<kQtNorm>(a, work, st);
+}
+
+// The quantiser on gelu(gate) * up: geglu_kernel and quant_i8_tiles in one
+// launch, the same values (the product itself is not stored).
+qlin_status geglu_quant_tiles(const float *gate, const float *up, int8_t *xq, float *xs, int M, int K, void *work,
+                              cudaStream_t st) {
+    QtArgs a{};
+    a.x = gate, a.u = up, a.xq = xq, a.xs = xs, a.M = M, a.K = K;
+    return launch_qt<kQtGeglu>(a, work, st);
 }
 
 }  // namespace qlin
