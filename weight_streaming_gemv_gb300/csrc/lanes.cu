@@ -329,6 +329,52 @@ __global__ void __launch_bounds__(256) lanes_attn_merge_kernel(const float *ws, 
                     out + ((int64_t)i * nh + h) * hd, wbuf, red, whole_block());
 }
 
+// grid (nh, lanes): lanes_attn_merge_kernel with the lane's partials of head h
+// staged in shared memory first (4-byte asynchronous copies, all in flight
+// together), then the same maximum, weights, pairwise sums and division.
+// Shared memory: [ncmax hd] U, [ncmax] m, [ncmax] S, [next_pow2(ncmax)]
+// weights, [hd] outputs.
+__global__ void __launch_bounds__(256) lanes_attn_merge_smem_kernel(const float *ws, int ncmax, const int32_t *pos,
+                                                                    const int32_t *seq, int n_seqs, int max_pos,
+                                                                    int nh, int hd, float *out) {
+    extern __shared__ __align__(16) float msm[];
+    __shared__ float red[32];
+    const int h = blockIdx.x, i = blockIdx.y;
+    const int p = pos[i];
+    if (!lane_ok(p, seq[i], max_pos, n_seqs)) return;
+    const int nc = p / 32 + 1, P = next_pow2(nc);
+    LaneAttnWs w = lane_attn_ws(const_cast<float *>(ws), i, ncmax, nh, hd);
+    const float *pU = w.U + (int64_t)h * ncmax * hd, *pm = w.m + h * ncmax, *pS = w.S + h * ncmax;
+    float *U = msm, *Mc = U + (size_t)ncmax * hd, *Sc = Mc + ncmax, *wb = Sc + ncmax, *o = wb + next_pow2(ncmax);
+    for (int e = threadIdx.x; e < nc * hd; e += blockDim.x)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(U + e)),
+                     "l"(pU + e)
+                     : "memory");
+    for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(Mc + c)),
+                     "l"(pm + c)
+                     : "memory");
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(Sc + c)),
+                     "l"(pS + c)
+                     : "memory");
+    }
+    lanes_cp_wait_all();
+    __syncthreads();
+    float m = Mc[0];
+    for (int c = 1; c < nc; c++) m = fmaxf(m, Mc[c]);
+    for (int c = threadIdx.x; c < P; c += blockDim.x) wb[c] = (c < nc) ? exp32(__fsub_rn(Mc[c], m)) : 0.0f;
+    __syncthreads();
+    for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+        PairwiseStream<16> ps;
+        for (int c = 0; c < nc; c++) ps.push(__fmul_rn(U[(size_t)c * hd + d], wb[c]));
+        o[d] = ps.result();
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < P; c += blockDim.x) wb[c] = (c < nc) ? __fmul_rn(Sc[c], wb[c]) : 0.0f;
+    const float S = block_psum(wb, P, red, whole_block());
+    for (int d = threadIdx.x; d < hd; d += blockDim.x) out[((int64_t)i * nh + h) * hd + d] = __fdiv_rn(o[d], S);
+}
+
 __global__ void lanes_add_kernel(float *h, const float *y, int64_t n) {
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x)
         h[e] = __fadd_rn(h[e], y[e]);
@@ -467,6 +513,10 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     const size_t attn_smem = (size_t)2 * 32 * hd * sizeof(float);
     const int attn_threads = kAttnGroupThreads * std::min(kAttnMaxGroups, nh / nkv);
     if (attn_smem > 48 * 1024) blocks_per_sm((const void *)lanes_attn_chunk_kernel, attn_smem);  // raises the limit once
+    // the merge stages a head's partials in shared memory when they fit in 64 KB
+    size_t merge_smem = ((size_t)ncmax * hd + 2 * ncmax + next_pow2(ncmax) + hd) * sizeof(float);
+    if (merge_smem > 64 * 1024) merge_smem = 0;
+    else if (merge_smem > 48 * 1024) blocks_per_sm((const void *)lanes_attn_merge_smem_kernel, merge_smem);
     // persistent attention: one CTA per SM (or per unit when there are fewer)
     const void *attn_k = attn_kernel(hd, nh / nkv);
     const size_t attn_k_smem = (size_t)kAttnBufs * 2 * 32 * hd * sizeof(float);
@@ -501,9 +551,15 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
                                                                                  ncmax);
             QLIN_LAUNCHED("lanes_attn_chunk_kernel");
         }
-        lanes_attn_merge_kernel<<<dim3(nh, M), 256, (size_t)next_pow2(ncmax) * sizeof(float), s>>>(
-            w.attn, ncmax, positions, seqs, n_seqs, m->max_pos, nh, hd, w.att);
-        QLIN_LAUNCHED("lanes_attn_merge_kernel");
+        if (merge_smem) {
+            lanes_attn_merge_smem_kernel<<<dim3(nh, M), 256, merge_smem, s>>>(w.attn, ncmax, positions, seqs, n_seqs,
+                                                                            m->max_pos, nh, hd, w.att);
+            QLIN_LAUNCHED("lanes_attn_merge_smem_kernel");
+        } else {
+            lanes_attn_merge_kernel<<<dim3(nh, M), 256, (size_t)next_pow2(ncmax) * sizeof(float), s>>>(
+                w.attn, ncmax, positions, seqs, n_seqs, m->max_pos, nh, hd, w.att);
+            QLIN_LAUNCHED("lanes_attn_merge_kernel");
+        }
         if ((st = quant_i8_tiles(w.att, w.xq, w.xs, M, qd, tiles, s)) || (st = lin(l, 3, w.y, false))) return st;
         if ((st = norm_quant_tiles(w.h, w.y, m->g_ffn + (int64_t)l * d, m->eps, w.xq, w.xs, M, d, tiles, s))) return st;
         if ((st = lin(l, 4, w.g, false)) || (st = lin(l, 5, w.u, false))) return st;
