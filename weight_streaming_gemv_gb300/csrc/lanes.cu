@@ -30,7 +30,11 @@ qlin_status t158_linear_dev_scale(const int8_t *xq, const float *xs, const uint8
                                   const float *ws_ptr, float *y, int M, int N, int K, cudaStream_t st, void *work,
                                   bool convert);
 size_t t158_workspace_bytes(int M, int K);
+size_t t158_tc_workspace_bytes(int M, int K);
 qlin_status quant_i8_tiles(const float *x, int8_t *xq, float *xs, int M, int K, void *work, cudaStream_t st);
+qlin_status t158_linear_tiles_multi(const float *xs, int count, const uint8_t *const *w, const int64_t *pitch,
+                                    const float *const *ws_ptr, float *const *y, const int *N, int M, int K,
+                                    void *work, cudaStream_t st);
 qlin_status norm_quant_tiles(float *h, const float *y, const float *gain, float eps, int8_t *xq, float *xs, int M,
                              int K, void *work, cudaStream_t st);
 qlin_status geglu_quant_tiles(const float *gate, const float *up, int8_t *xq, float *xs, int M, int K, void *work,
@@ -39,6 +43,10 @@ qlin_status geglu_quant_tiles(const float *gate, const float *up, int8_t *xq, fl
 namespace {
 
 constexpr int kLaneStatusBad = 1;  // a lane's token, position or sequence slot out of range
+// Lanes from which every linear runs on the tensor cores (on activation tiles
+// the quantisers write, the linears sharing an input in one launch); below it
+// the CUDA-core kernels, one launch per linear.
+constexpr int kLanesTensorMin = 2;
 
 __device__ __forceinline__ bool lane_ok(int pos, int seq, int max_pos, int n_seqs) {
     return pos >= 0 && pos < max_pos && seq >= 0 && seq < n_seqs;
@@ -418,7 +426,7 @@ LanesWs carve_lanes(const t158_model *m, int max_lanes, char *base) {
     w.attn = (float *)take(4 * M * m->n_heads * (size_t)attn_chunks(m->max_pos) * (2 + m->head_dim));
     w.lm_bytes = qlin_lm_head_lanes_workspace_size(m->vocab, m->dim);
     w.lm = take(w.lm_bytes);
-    w.tiles = take(t158_workspace_bytes(max_lanes, (int)big));
+    w.tiles = take(max_lanes >= kLanesTensorMin ? t158_tc_workspace_bytes(max_lanes, (int)big) : 0);
     w.bytes = off;
     return w;
 }
@@ -508,7 +516,27 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
                                      convert);
     };
     // the quantisers also write the tensor-core tiles when the linears take that path
-    void *const tiles = t158_workspace_bytes(M, d) > 0 ? w.tiles : nullptr;
+    void *const tiles = M >= kLanesTensorMin ? w.tiles : nullptr;
+    // linears j0 .. j0 + n - 1 of layer l (same input): one tensor-core launch on the tiles, else one each
+    auto lin_group = [&](int l, int j0, int n, float *const *out) -> qlin_status {
+        if (!tiles) {
+            for (int k = 0; k < n; k++)
+                if (qlin_status e = lin(l, j0 + k, out[k], false)) return e;
+            return QLIN_OK;
+        }
+        const uint8_t *wj[3];
+        int64_t pj[3];
+        const float *sj[3];
+        int nj[3];
+        for (int k = 0; k < n; k++) {
+            const int j = j0 + k;
+            wj[k] = W[j] + (int64_t)l * rows[j] * m->pitch[j];
+            pj[k] = m->pitch[j];
+            sj[k] = m->scales + (int64_t)l * T158_NMAT + j;
+            nj[k] = rows[j];
+        }
+        return t158_linear_tiles_multi(w.xs, n, wj, pj, sj, out, nj, M, cols[j0], tiles, s);
+    };
     const int add_blocks = std::max(1, std::min(4 * sm_count(), (int)(((int64_t)M * d + 255) / 256)));
     const size_t attn_smem = (size_t)2 * 32 * hd * sizeof(float);
     const int attn_threads = kAttnGroupThreads * std::min(kAttnMaxGroups, nh / nkv);
@@ -534,7 +562,10 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
         if ((st = norm_quant_tiles(w.h, l > 0 ? w.y : nullptr, m->g_attn + (int64_t)l * d, m->eps, w.xq, w.xs, M, d,
                                    tiles, s)))
             return st;
-        if ((st = lin(l, 0, w.q, false)) || (st = lin(l, 1, w.k, false)) || (st = lin(l, 2, w.v, false))) return st;
+        {
+            float *const qkv[3] = {w.q, w.k, w.v};
+            if ((st = lin_group(l, 0, 3, qkv))) return st;
+        }
         lanes_rope_kv_kernel<<<M, 256, (size_t)kvd * sizeof(float), s>>>(
             w.q, w.k, w.v, kv_caches, positions, seqs, n_seqs, l, L, m->max_pos, m->rope_cos, m->rope_sin, nh, nkv,
             hd, w.status);
@@ -560,10 +591,13 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
                 w.attn, ncmax, positions, seqs, n_seqs, m->max_pos, nh, hd, w.att);
             QLIN_LAUNCHED("lanes_attn_merge_kernel");
         }
-        if ((st = quant_i8_tiles(w.att, w.xq, w.xs, M, qd, tiles, s)) || (st = lin(l, 3, w.y, false))) return st;
+        if ((st = quant_i8_tiles(w.att, w.xq, w.xs, M, qd, tiles, s)) || (st = lin_group(l, 3, 1, &w.y))) return st;
         if ((st = norm_quant_tiles(w.h, w.y, m->g_ffn + (int64_t)l * d, m->eps, w.xq, w.xs, M, d, tiles, s))) return st;
-        if ((st = lin(l, 4, w.g, false)) || (st = lin(l, 5, w.u, false))) return st;
-        if ((st = geglu_quant_tiles(w.g, w.u, w.xq, w.xs, M, f, tiles, s)) || (st = lin(l, 6, w.y, false))) return st;
+        {
+            float *const gu[2] = {w.g, w.u};
+            if ((st = lin_group(l, 4, 2, gu))) return st;
+        }
+        if ((st = geglu_quant_tiles(w.g, w.u, w.xq, w.xs, M, f, tiles, s)) || (st = lin_group(l, 6, 1, &w.y))) return st;
     }
     lanes_add_kernel<<<add_blocks, 256, 0, s>>>(w.h, w.y, (int64_t)M * d);  // the last layer's FFN output
     QLIN_LAUNCHED("lanes_add_kernel");
@@ -577,9 +611,11 @@ int decode_lanes_t158_launches(const t158_model *m, int n_lanes) {
     qlin::clear_error();
     if (check_lanes_model(m) || n_lanes < 1) return -1;
     // embed; per layer 4 quantisations (two behind the residual add and RMSNorm, one behind the GeGLU
-    // product), 7 linears, rope/append, 2 attention; the last residual add and the final norm; the
-    // lanes' output layer (a split and a table pass per 64 lanes)
-    return 1 + m->n_layers * 14 + 2 + 2 * ((n_lanes + 63) / 64);
+    // product), 7 linears (3 launches on the tensor cores: q k v, o, gate up, down as 4), rope/append,
+    // 2 attention; the last residual add and the final norm; the lanes' output layer (a split and a
+    // table pass per 64 lanes)
+    const int lin_launches = n_lanes >= kLanesTensorMin ? 4 : 7;
+    return 1 + m->n_layers * (7 + lin_launches) + 2 + 2 * ((n_lanes + 63) / 64);
 }
 
 qlin_status decode_lanes_t158_status(void *workspace, qlin_stream_t stream) {

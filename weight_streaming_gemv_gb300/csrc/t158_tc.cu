@@ -437,6 +437,21 @@ __global__ void __launch_bounds__(kQtThreads) t158_quant_tiles_kernel(QtArgs a) 
     }
 }
 
+// Up to three weight matrices that share the input (and K): one launch runs
+// them all, tiles 0 .. of matrix 0 first (blockIdx.x from tile0[j] on is
+// matrix j).
+constexpr int kTmMaxMats = 3;
+struct TmMats {
+    const uint8_t *w[kTmMaxMats];
+    int64_t pitch[kTmMaxMats];
+    const float *ws_ptr[kTmMaxMats];  // weight scale in device memory, or null (then ws_arg)
+    float *y[kTmMaxMats];
+    int32_t *acc[kTmMaxMats];
+    int N[kTmMaxMats];
+    int tile0[kTmMaxMats + 1];
+    int count;
+};
+
 // Grid: (weight-row tiles, token tiles, split); a cluster is the `split` CTAs
 // of one tile, each over its own range of K steps.  split == 1: no cluster
 // reduction.  T: tokens per tile (a multiple of 32, at most kTmMaxTok).
@@ -444,10 +459,16 @@ __global__ void __launch_bounds__(kQtThreads) t158_quant_tiles_kernel(QtArgs a) 
 template <bool PRE>
 __global__ void __launch_bounds__(kTmThreads, 1)
     t158_tm_kernel(const int8_t *__restrict__ xq, const uint8_t *__restrict__ tiles, const float *__restrict__ xs,
-                   const uint8_t *__restrict__ w, int64_t pitch, float ws_arg, const float *__restrict__ ws_ptr,
-                   float *__restrict__ y, int32_t *__restrict__ acc_out, int M, int N, int K, int T, int split) {
+                   const TmMats mats, float ws_arg, int M, int K, int T, int split) {
     constexpr int S = tm_stages(PRE), R = tm_raws(PRE);
-    const float ws = ws_ptr ? __ldg(ws_ptr) : ws_arg;  // the weight scale, from device memory when given
+    int mj = 0;  // this CTA's matrix
+    while (mj + 1 < mats.count && (int)blockIdx.x >= mats.tile0[mj + 1]) mj++;
+    const uint8_t *__restrict__ w = mats.w[mj];
+    const int64_t pitch = mats.pitch[mj];
+    float *__restrict__ y = mats.y[mj];
+    int32_t *__restrict__ acc_out = mats.acc[mj];
+    const int N = mats.N[mj];
+    const float ws = mats.ws_ptr[mj] ? __ldg(mats.ws_ptr[mj]) : ws_arg;  // the weight scale, from device memory when given
     extern __shared__ __align__(128) uint8_t tm_smem[];
     TmCtl &C = *reinterpret_cast<TmCtl *>(tm_smem);
     uint8_t *const btile = tm_smem + kTmCtl;
@@ -455,7 +476,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     uint8_t *const raw_w = tm_smem + tm_raw_w_off(T, PRE);
     const int bstage = tm_b_bytes(T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * kTmRows, m0 = blockIdx.y * T;
+    const int n0 = ((int)blockIdx.x - mats.tile0[mj]) * kTmRows, m0 = blockIdx.y * T;
     const int nsteps = (K + kTcKS - 1) / kTcKS;
     const int z = split > 1 ? (int)cluster_rank() : 0;
     const int s_lo = (int)((int64_t)nsteps * z / split), s_hi = (int)((int64_t)nsteps * (z + 1) / split);
@@ -786,12 +807,14 @@ static qlin_status tm_launch_smem(int T, size_t *out) {
 }
 
 template <bool PRE>
-static qlin_status launch_tm(const int8_t *xq, const uint8_t *tiles, const float *xs, const uint8_t *w, int64_t pitch,
-                             float ws, const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, int tiles_m,
-                             int T, cudaStream_t st) {
+static qlin_status launch_tm(const int8_t *xq, const uint8_t *tiles, const float *xs, TmMats mats, float ws,
+                             int M, int K, int tiles_m, int T, cudaStream_t st) {
     size_t smem = 0;
     if (qlin_status e = tm_launch_smem<PRE>(T, &smem)) return e;
-    const int tiles_n = (N + kTmRows - 1) / kTmRows;
+    mats.tile0[0] = 0;
+    for (int j = 0; j < mats.count; j++) mats.tile0[j + 1] = mats.tile0[j] + (mats.N[j] + kTmRows - 1) / kTmRows;
+    for (int j = mats.count + 1; j <= kTmMaxMats; j++) mats.tile0[j] = mats.tile0[mats.count];
+    const int tiles_n = mats.tile0[mats.count];
     const int nsteps = (K + kTcKS - 1) / kTcKS;
     // split K over a cluster when the tiles alone leave SMs idle: the largest
     // split whose clusters (they must fit within a GPC) are all resident at once
@@ -816,8 +839,7 @@ static qlin_status launch_tm(const int8_t *xq, const uint8_t *tiles, const float
     attr[0].val.clusterDim.z = (unsigned)split;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tm_kernel<PRE>, xq, tiles, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, T,
-                                 split));
+    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tm_kernel<PRE>, xq, tiles, xs, mats, ws, M, K, T, split));
     QLIN_LAUNCHED("t158_tm_kernel");
     return QLIN_OK;
 }
@@ -832,7 +854,10 @@ qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const ui
                                      void *work, bool convert) {
     int tiles_m = 0, T = 0;
     tm_token_tiles(M, tiles_m, T);
-    if (!work) return launch_tm<false>(xq, nullptr, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, tiles_m, T, st);
+    TmMats mats{};
+    mats.w[0] = w, mats.pitch[0] = pitch, mats.ws_ptr[0] = ws_ptr, mats.y[0] = y, mats.acc[0] = acc, mats.N[0] = N;
+    mats.count = 1;
+    if (!work) return launch_tm<false>(xq, nullptr, xs, mats, ws, M, K, tiles_m, T, st);
     if (convert) {
         const int nsteps = (K + kTcKS - 1) / kTcKS;
         const int64_t threads = (int64_t)tiles_m * T * nsteps;
@@ -840,7 +865,24 @@ qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const ui
                                                                                  (uint8_t *)work);
         QLIN_LAUNCHED("t158_act_tiles_kernel");
     }
-    return launch_tm<true>(xq, (const uint8_t *)work, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, tiles_m, T, st);
+    return launch_tm<true>(xq, (const uint8_t *)work, xs, mats, ws, M, K, tiles_m, T, st);
+}
+
+// Linears j = 0 .. count - 1 on one set of activation tiles (already in work,
+// written by the quantiser for this xq, M and K): w[j] [N[j]][pitch[j]],
+// weight scale in device memory at ws_ptr[j], output y[j] [M][N[j]], all in
+// one launch.
+qlin_status t158_linear_tiles_multi(const float *xs, int count, const uint8_t *const *w, const int64_t *pitch,
+                                    const float *const *ws_ptr, float *const *y, const int *N, int M, int K,
+                                    void *work, cudaStream_t st) {
+    QLIN_REQUIRE(count >= 1 && count <= kTmMaxMats && work, QLIN_ERR_INVALID_ARG, "t158_linear_tiles_multi: %d", count);
+    int tiles_m = 0, T = 0;
+    tm_token_tiles(M, tiles_m, T);
+    TmMats mats{};
+    for (int j = 0; j < count; j++)
+        mats.w[j] = w[j], mats.pitch[j] = pitch[j], mats.ws_ptr[j] = ws_ptr[j], mats.y[j] = y[j], mats.N[j] = N[j];
+    mats.count = count;
+    return launch_tm<true>(nullptr, (const uint8_t *)work, xs, mats, 0.0f, M, K, tiles_m, T, st);
 }
 
 // The quantiser kernels' launch: one block per token (per padded token row
