@@ -23,6 +23,7 @@
 
 #include "common.cuh"
 #include "decode_ops.cuh"
+#include "stream.cuh"
 
 namespace qlin {
 
@@ -42,7 +43,8 @@ qlin_status geglu_quant_tiles(const float *gate, const float *up, int8_t *xq, fl
 
 namespace {
 
-constexpr int kLaneStatusBad = 1;  // a lane's token, position or sequence slot out of range
+constexpr int kLaneStatusBad = 1;      // a lane's token, position or sequence slot out of range
+constexpr int kLaneStatusTimeout = 2;  // a bounded wait inside the attention kernel gave up
 // Lanes from which every linear runs on the tensor cores (on activation tiles
 // the quantisers write, the linears sharing an input in one launch); below it
 // the CUDA-core kernels, one launch per linear.
@@ -181,62 +183,98 @@ template <int HD, int GRP>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     lanes_attn_kernel(const float *__restrict__ q, const float *__restrict__ kv, const int32_t *pos,
                       const int32_t *seq, int n_seqs, int layer, int L, int max_pos, int nh, int nkv, int M,
-                      float *ws, int ncmax) {
+                      float *ws, int ncmax, int32_t *status) {
     constexpr int S = HD / 32;   // dims per lane in the scores
     constexpr int CH = 32 * HD;  // floats of a chunk's k (or v) rows
     extern __shared__ __align__(16) float abuf[];  // [kAttnBufs][2][32][HD]
-    __shared__ float sc[GRP][32];
+    __shared__ __align__(16) float sc[GRP][32];
+    __shared__ uint64_t full[kAttnBufs];  // buffer b's rows have landed (one arrival + the bytes)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = nh / nkv;  // query heads per KV head, <= GRP
+    if (tid == 0) {
+        for (int b = 0; b < kAttnBufs; b++) mbar_init(&full[b], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const uint64_t pol = l2_evict_first();  // every KV row is read once per step
     const int ld = nkv * HD;
-    const int64_t per_lane = (int64_t)nkv * ncmax;
-    const int64_t units = (int64_t)M * per_lane;
-    const int64_t u_hi = units * (blockIdx.x + 1) / gridDim.x;
-    int64_t next = units * blockIdx.x / gridDim.x;
+    const int64_t units = (int64_t)M * nkv * ncmax;
+    const int64_t u_lo = units * blockIdx.x / gridDim.x;
+    int64_t left = units * (blockIdx.x + 1) / gridDim.x - u_lo;  // units of this CTA not yet walked
+    // unit counters, chunk fastest: lane ai, KV head ag, chunk ac
+    int ac = (int)(u_lo % ncmax), ag = (int)((u_lo / ncmax) % nkv), ai = (int)(u_lo / ((int64_t)ncmax * nkv));
     const float div = __fsqrt_rn((float)HD);
 
-    // the next unit of this CTA with work, or -1 (every thread computes the same)
-    auto advance = [&]() -> int64_t {
-        for (; next < u_hi; next++) {
-            const int i = (int)(next / per_lane), c = (int)(next % ncmax);
-            if (lane_ok(pos[i], seq[i], max_pos, n_seqs) && c * 32 <= pos[i]) return next++;
+    // the position and sequence slot of lane ci, loaded once per lane (units
+    // of one lane are consecutive)
+    int ci = -1, cpos = 0, cseq = 0;
+    auto lane_info = [&](int li) {
+        if (li != ci) {
+            ci = li;
+            cpos = pos[li];
+            cseq = seq[li];
         }
-        return -1;
     };
-    auto issue = [&](int64_t u, int b) {
-        const int i = (int)(u / per_lane), g = (int)((u / ncmax) % nkv), c = (int)(u % ncmax);
-        const int p = pos[i], s = seq[i];
+    // the next unit of this CTA with work as {lane, KV head, chunk, position},
+    // lane -1 when none is left (every thread computes the same)
+    auto advance = [&]() -> int4 {
+        while (left > 0) {
+            const int li = ai, g = ag, c = ac;
+            left--;
+            if (++ac == ncmax) {
+                ac = 0;
+                if (++ag == nkv) ag = 0, ai++;
+            }
+            lane_info(li);
+            if (lane_ok(cpos, cseq, max_pos, n_seqs) && c * 32 <= cpos) return make_int4(li, g, c, cpos);
+        }
+        return make_int4(-1, 0, 0, 0);
+    };
+    auto issue = [&](int4 un, int b) {  // un's lane is the one advance() just found
+        const int g = un.y, c = un.z, p = un.w, s = cseq;
         const int t0 = c * 32, nt = min(32, p + 1 - t0);
         const float *kc = kv + (((int64_t)s * L + layer) * 2 + 0) * max_pos * ld + (int64_t)t0 * ld + g * HD;
         const float *vc = kc + (int64_t)max_pos * ld;
         float *Kb = abuf + (size_t)b * 2 * CH, *Vb = Kb + CH;
-        for (int e = tid; e < nt * (HD / 4); e += kAttnThreads) {
-            const int t = e / (HD / 4), dd = e - t * (HD / 4);
-            lanes_cp16(Kb + 4 * e, kc + (int64_t)t * ld + 4 * dd);
-            lanes_cp16(Vb + 4 * e, vc + (int64_t)t * ld + 4 * dd);
+        constexpr uint32_t rowb = HD * sizeof(float);
+        if (ld == HD) {  // one KV head: the chunk's k rows are contiguous, and so are its v rows
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&full[b], 2u * (uint32_t)nt * rowb);
+                bulk_g2s(Kb, kc, (uint32_t)nt * rowb, &full[b], pol);
+                bulk_g2s(Vb, vc, (uint32_t)nt * rowb, &full[b], pol);
+            }
+        } else if (warp == 0) {  // one bulk copy per k row and per v row, lane t: row t
+            if (lane == 0) mbar_arrive_expect_tx(&full[b], 2u * (uint32_t)nt * rowb);
+            __syncwarp();
+            if (lane < nt) {
+                bulk_g2s(Kb + lane * HD, kc + (int64_t)lane * ld, rowb, &full[b], pol);
+                bulk_g2s(Vb + lane * HD, vc + (int64_t)lane * ld, rowb, &full[b], pol);
+            }
         }
     };
 
-    int64_t slot[kAttnBufs];
+    int4 slot[kAttnBufs];
 #pragma unroll
     for (int b = 0; b < kAttnBufs; b++) {
         slot[b] = advance();
-        if (slot[b] >= 0) issue(slot[b], b);
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (slot[b].x >= 0) issue(slot[b], b);
     }
     float qr[GRP][S];
     int64_t cur = -1;  // lane * nkv + KV head whose q rows are in qr
     for (int k = 0;; k++) {
         const int b = k % kAttnBufs;
-        int64_t u = -1;
+        int4 un = slot[0];
 #pragma unroll
-        for (int j = 0; j < kAttnBufs; j++)
-            if (j == b) u = slot[j];
-        if (u < 0) break;
-        asm volatile("cp.async.wait_group %0;" ::"n"(kAttnBufs - 1) : "memory");
-        __syncthreads();  // unit u's k and v rows are in buffer b (every thread's copies)
-        const int i = (int)(u / per_lane), g = (int)((u / ncmax) % nkv), c = (int)(u % ncmax);
-        const int p = pos[i];
+        for (int j = 1; j < kAttnBufs; j++)
+            if (j == b) un = slot[j];
+        if (un.x < 0) break;
+        // unit un's k and v rows are in buffer b (its (k / kAttnBufs)-th fill)
+        const bool landed = mbar_wait(&full[b], (uint32_t)(k / kAttnBufs) & 1u);
+        if (__syncthreads_or(!landed)) {
+            if (tid == 0) atomicOr(status, kLaneStatusTimeout);
+            return;
+        }
+        const int i = un.x, g = un.y, c = un.z, p = un.w;
         const int t0 = c * 32, nt = min(32, p + 1 - t0);
         const float *Kb = abuf + (size_t)b * 2 * CH, *Vb = Kb + CH;
         LaneAttnWs w = lane_attn_ws(ws, i, ncmax, nh, HD);
@@ -269,9 +307,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int e = 0; e < S; e++) kr[e] = kt[lane * S + e];
                 }
             }
+            // every head's lane tree, then the warp sums level by level across
+            // heads (the sums of warp_psum, interleaved)
+            float part[GRP];
 #pragma unroll
             for (int h = 0; h < GRP; h++) {
-                float part = 0.0f;
+                part[h] = 0.0f;
                 if (t < nt) {
                     float pp[S];
 #pragma unroll
@@ -280,10 +321,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int st = 1; st < S; st <<= 1)
 #pragma unroll
                         for (int e = 0; e < S; e += 2 * st) pp[e] = __fadd_rn(pp[e], pp[e + st]);
-                    part = pp[0];
+                    part[h] = pp[0];
                 }
-                const float sv = warp_psum(part);
-                if (lane == 0) sc[h][t] = (t < nt) ? __fdiv_rn(sv, div) : 0.0f;
+            }
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1)
+#pragma unroll
+                for (int h = 0; h < GRP; h++) part[h] = __fadd_rn(part[h], __shfl_xor_sync(0xffffffffu, part[h], off));
+            if (lane < GRP) {  // lane h stores head h
+                float sv = part[0];
+#pragma unroll
+                for (int h = 1; h < GRP; h++)
+                    if (lane == h) sv = part[h];
+                sc[lane][t] = (t < nt) ? __fdiv_rn(sv, div) : 0.0f;
             }
         }
         __syncthreads();
@@ -301,26 +351,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
         }
         __syncthreads();
-        for (int o = tid; o < grp * HD; o += kAttnThreads) {
-            const int h = o / HD, d = o - h * HD;
-            float pp[32];
+        {
+            // thread: dim d, heads hb, hb + HG, ... (HG = threads / HD), two at a
+            // time sharing each value load
+            constexpr int HG = kAttnThreads / HD;
+            const int d = tid % HD, hb = tid / HD;
+            for (int h0 = hb; h0 < grp; h0 += 2 * HG) {
+                const int h1 = h0 + HG;
+                const bool two = h1 < grp;
+                // running pairwise stacks over the 32 positions: pushing t merges
+                // the completed subtrees below it, so after 32 pushes level 5 holds
+                // the balanced tree (left + right at every node)
+                float sa[6], sb[6];
+                float4 wa = make_float4(0.f, 0.f, 0.f, 0.f), wb = wa;
 #pragma unroll
-            for (int t = 0; t < 32; t++) pp[t] = (t < nt) ? __fmul_rn(sc[h][t], Vb[t * HD + d]) : 0.0f;
+                for (int t = 0; t < 32; t++) {
+                    if ((t & 3) == 0) {  // the weights of positions t .. t + 3, one load per head
+                        wa = *reinterpret_cast<const float4 *>(&sc[h0][t]);
+                        if (two) wb = *reinterpret_cast<const float4 *>(&sc[h1][t]);
+                    }
+                    const float ea = (t & 3) == 0 ? wa.x : (t & 3) == 1 ? wa.y : (t & 3) == 2 ? wa.z : wa.w;
+                    const float eb = (t & 3) == 0 ? wb.x : (t & 3) == 1 ? wb.y : (t & 3) == 2 ? wb.z : wb.w;
+                    const float v = (t < nt) ? Vb[t * HD + d] : 0.0f;
+                    float xa = (t < nt) ? __fmul_rn(ea, v) : 0.0f;
+                    float xb = (t < nt && two) ? __fmul_rn(eb, v) : 0.0f;
+                    int k = 0;
 #pragma unroll
-            for (int st = 1; st < 32; st <<= 1)
-#pragma unroll
-                for (int t = 0; t < 32; t += 2 * st) pp[t] = __fadd_rn(pp[t], pp[t + st]);
-            w.U[((int64_t)(g * grp + h) * ncmax + c) * HD + d] = pp[0];
+                    for (int jj = t; jj & 1; jj >>= 1, k++) {
+                        xa = __fadd_rn(sa[k], xa);
+                        xb = __fadd_rn(sb[k], xb);
+                    }
+                    sa[k] = xa;
+                    sb[k] = xb;
+                }
+                w.U[((int64_t)(g * grp + h0) * ncmax + c) * HD + d] = sa[5];
+                if (two) w.U[((int64_t)(g * grp + h1) * ncmax + c) * HD + d] = sb[5];
+            }
         }
         __syncthreads();  // buffer b and sc are free again
-        const int64_t un = advance();
+        const int4 nx = advance();
 #pragma unroll
         for (int j = 0; j < kAttnBufs; j++)
-            if (j == b) slot[j] = un;
-        if (un >= 0) issue(un, b);
-        asm volatile("cp.async.commit_group;" ::: "memory");
+            if (j == b) slot[j] = nx;
+        if (nx.x >= 0) issue(nx, b);
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // grid (nh, lanes): merge the lane's chunks of head h
@@ -573,7 +647,7 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
         if (attn_k) {
             void *args[] = {(void *)&w.q, (void *)&kv_caches, (void *)&positions, (void *)&seqs, (void *)&n_seqs,
                             (void *)&l, (void *)&L, (void *)&m->max_pos, (void *)&m->n_heads, (void *)&m->n_kv_heads,
-                            (void *)&M, (void *)&w.attn, (void *)&ncmax};
+                            (void *)&M, (void *)&w.attn, (void *)&ncmax, (void *)&w.status};
             QLIN_CUDA(cudaLaunchKernel(attn_k, dim3(attn_grid), dim3(kAttnThreads), args, attn_k_smem, s));
             QLIN_LAUNCHED("lanes_attn_kernel");
         } else {
@@ -627,6 +701,8 @@ qlin_status decode_lanes_t158_status(void *workspace, qlin_stream_t stream) {
     QLIN_CUDA(cudaMemset(workspace, 0, sizeof stw));
     QLIN_REQUIRE(!(stw[0] & kLaneStatusBad), QLIN_ERR_INVALID_ARG,
                  "decode_lanes_t158: a lane's token, position or sequence slot was out of range");
+    QLIN_REQUIRE(!(stw[0] & kLaneStatusTimeout), QLIN_ERR_TIMEOUT,
+                 "decode_lanes_t158: a bounded wait in the attention kernel gave up");
     return QLIN_OK;
 }
 
