@@ -45,7 +45,7 @@ struct LlSmem {
         } in;
         float d[kLlRows][kLlDStride];  // after the K loop: the accumulator
     };
-    uint64_t full[kLlStages];      // the loaders' copies of the stage have landed (kLlLoaders arrivals)
+    uint64_t full[kLlStages];      // the stage has landed (kLlLoaders arrivals + the lanes operand's bytes)
     uint64_t mma_done[kLlStages];  // the MMAs reading the stage are done (tcgen05.commit)
     float bv[8][kLlMaxLanes];      // epilogue: each warp's best per lane
     int bi[8][kLlMaxLanes];
@@ -109,25 +109,38 @@ __device__ __forceinline__ int ll_off(int r, int kc) { return (r >> 3) * kLlSBO 
 
 __device__ __forceinline__ bool ll_better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
-// x [U][K] fp32 -> xs [3][Up][K] bf16 (hi, mid, lo; zero rows for lanes U..Up-1)
-__global__ void lm_lanes_split_kernel(const float *__restrict__ x, int U, int Up, int K, uint16_t *__restrict__ xs) {
-    const int u = blockIdx.x;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-        const float v = u < U ? x[(int64_t)u * K + k] : 0.0f;
+// x [U][K] fp32 -> the lanes' operand of every K step as the image of its
+// shared-memory stage: N = 3 Up rows (row t Up + u: term t of lane u, the terms
+// hi, mid, lo), step s at xs + s N 64 elements in the K-major core-matrix
+// layout; zero for lanes U..Up-1 and past K.
+__global__ void lm_lanes_split_kernel(const float *__restrict__ x, int U, int Up, int K, int nsteps,
+                                      uint16_t *__restrict__ xs) {
+    const int u = blockIdx.x, N = 3 * Up;
+    for (int k = threadIdx.x; k < nsteps * kLlKS; k += blockDim.x) {
+        const float v = (u < U && k < K) ? x[(int64_t)u * K + k] : 0.0f;
         const __nv_bfloat16 hi = __float2bfloat16_rn(v);
         const float r1 = __fsub_rn(v, __bfloat162float(hi));
         const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
         const float r2 = __fsub_rn(r1, __bfloat162float(mid));
         const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
-        xs[((int64_t)0 * Up + u) * K + k] = __bfloat16_as_ushort(hi);
-        xs[((int64_t)1 * Up + u) * K + k] = __bfloat16_as_ushort(mid);
-        xs[((int64_t)2 * Up + u) * K + k] = __bfloat16_as_ushort(lo);
+        const int st = k / kLlKS, kc = (k % kLlKS) / 8, e = k % 8;
+        uint16_t *img = xs + (int64_t)st * N * kLlKS;
+        img[(ll_off(0 * Up + u, kc) >> 1) + e] = __bfloat16_as_ushort(hi);
+        img[(ll_off(1 * Up + u, kc) >> 1) + e] = __bfloat16_as_ushort(mid);
+        img[(ll_off(2 * Up + u, kc) >> 1) + e] = __bfloat16_as_ushort(lo);
     }
+}
+
+// L2 policy for data every CTA reads again: keep it.
+__device__ __forceinline__ uint64_t ll_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
 struct LlArgs {
     const uint16_t *emb;  // [V][K]
-    const uint16_t *xs;   // [3][Up][K]
+    const uint16_t *xs;   // the split kernel's step images, [ceil(K/64)][3 Up x 64]
     int V, K, U, Up;
     float *logits;        // [U][V] or null
     int32_t *next;        // [U]
@@ -144,7 +157,18 @@ __global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
     const int K = A.K, N = 3 * A.Up;
     const int nsteps = (K + kLlKS - 1) / kLlKS;
 
-    // copies of step t into its stage: 1024 table chunks and N * 8 lane chunks
+    const uint32_t bbytes = (uint32_t)N * kLlKS * 2;  // the lanes' operand of one step
+    const uint64_t keep = ll_evict_last();
+    // step t's lanes operand: one bulk copy of its image (thread 0; the stage's
+    // barrier is initialised), completing on the stage's full barrier
+    auto fetch_b = [&](int t) {
+        if (t < nsteps) {
+            const int st = t % kLlStages;
+            mbar_arrive_expect_tx(&S.full[st], bbytes);
+            bulk_g2s(S.in.b[st], A.xs + (int64_t)t * N * kLlKS, bbytes, &S.full[st], keep);
+        }
+    };
+    // step t's table rows into its stage: 1024 chunks of 16 bytes over the loaders
     auto fetch = [&](int t) {
         if (t < nsteps) {
             const int st = t % kLlStages, k0 = t * kLlKS;
@@ -154,17 +178,23 @@ __global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
                 const bool ok = row < A.V && k < K;
                 ll_cp16(S.in.a[st] + ll_off(r, kc), A.emb + (ok ? (int64_t)row * K + k : 0), ok ? 16 : 0);
             }
-            for (int idx = tid; idx < N * kLlChunks; idx += kLlLoaders) {
-                const int n = idx / kLlChunks, kc = idx % kLlChunks;
-                const int k = k0 + 8 * kc;
-                const bool ok = k < K;
-                ll_cp16(S.in.b[st] + ll_off(n, kc), A.xs + (ok ? (int64_t)n * K + k : 0), ok ? 16 : 0);
-            }
+            if (tid == 0) fetch_b(t);
         }
         ll_commit_group();
     };
     if (tid < kLlLoaders)
-        for (int t = 0; t < kLlStages - 1; t++) fetch(t);
+        for (int t = 0; t < kLlStages - 1; t++) {  // table rows only: the barriers are not yet initialised
+            if (t < nsteps) {
+                const int st = t % kLlStages, k0 = t * kLlKS;
+                for (int idx = tid; idx < kLlRows * kLlChunks; idx += kLlLoaders) {
+                    const int r = idx / kLlChunks, kc = idx % kLlChunks;
+                    const int row = row0 + r, k = k0 + 8 * kc;
+                    const bool ok = row < A.V && k < K;
+                    ll_cp16(S.in.a[st] + ll_off(r, kc), A.emb + (ok ? (int64_t)row * K + k : 0), ok ? 16 : 0);
+                }
+            }
+            ll_commit_group();
+        }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&S.tmem)),
                      "r"(kLlCols)
@@ -173,7 +203,7 @@ __global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
     }
     if (tid == kLlLoaders) {
         for (int i = 0; i < kLlStages; i++) {
-            mbar_init(&S.full[i], kLlLoaders);
+            mbar_init(&S.full[i], kLlLoaders + 1);  // the loaders, and thread 0's byte-counted arrival
             mbar_init(&S.mma_done[i], 1);
         }
         S.abort = 0;
@@ -184,6 +214,8 @@ __global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = S.tmem;
     volatile int *abort = &S.abort;
+    if (tid == 0)
+        for (int t = 0; t < kLlStages - 1; t++) fetch_b(t);
 
     if (warp == kLlLoaders / 32) {
         if (lane == 0) {  // the MMAs of each step once its stage is full
@@ -329,7 +361,7 @@ LlWs carve_ll(int vocab, int dim, char *base) {
     };
     w.status = (int32_t *)take(16);
     w.ticket = (unsigned *)take(4);
-    w.xs = (uint16_t *)take((size_t)3 * kLlMaxLanes * dim * 2);
+    w.xs = (uint16_t *)take((size_t)(dim + kLlKS - 1) / kLlKS * kLlKS * 3 * kLlMaxLanes * 2);
     w.part = (float2 *)take(sizeof(float2) * (size_t)((vocab + kLlRows - 1) / kLlRows) * kLlMaxLanes);
     w.bytes = off;
     return w;
@@ -367,7 +399,8 @@ qlin_status qlin_lm_head_lanes(const uint16_t *emb, const float *x, int vocab, i
     for (int u0 = 0; u0 < n_lanes; u0 += kLlMaxLanes) {  // up to 64 lanes per pass over the table
         const int U = std::min(kLlMaxLanes, n_lanes - u0);
         const int Up = (U + 15) / 16 * 16;
-        lm_lanes_split_kernel<<<Up, 256, 0, st>>>(x + (int64_t)u0 * dim, U, Up, dim, w.xs);
+        lm_lanes_split_kernel<<<Up, 256, 0, st>>>(x + (int64_t)u0 * dim, U, Up, dim, (dim + kLlKS - 1) / kLlKS,
+                                                  w.xs);
         QLIN_LAUNCHED("lm_lanes_split_kernel");
         LlArgs a{};
         a.emb = emb;
