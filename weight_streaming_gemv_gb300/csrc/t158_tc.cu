@@ -521,7 +521,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 #pragma unroll
         for (int s = 0; s < R - 1; s++) fetch(s_lo + s);
     }
-    for (int i = tid; i < T; i += kTmThreads) C.xs[i] = m0 + i < M ? xs[m0 + i] : 0.0f;
+    // the tile's activation scales: loaded now, stored for the epilogue after the K loop
+    const float xs_own = (tid < T && m0 + tid < M) ? xs[m0 + tid] : 0.0f;
     const uint32_t ncols = tm_cols(T, PRE);
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&C.tmem)),
@@ -556,11 +557,11 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t b0 = smem_addr(btile + st * bstage);
+                const uint64_t bd = tc_desc(smem_addr(btile + st * bstage));
                 const uint32_t a0 = tmem + (uint32_t)(T + kTmACols * st);
 #pragma unroll
-                for (int u = 0; u < kTcKS / 16; u++)  // K = 16: 8 weight columns, 2 activation core matrices
-                    tm_mma(tmem, a0 + 8u * u, tc_desc(b0 + 256u * u), idesc, (i > 0 || u > 0) ? 1u : 0u);
+                for (int u = 0; u < kTcKS / 16; u++)  // K = 16: 8 weight columns, 2 activation core matrices (256 bytes)
+                    tm_mma(tmem, a0 + 8u * u, bd + (uint64_t)(16 * u), idesc, (i > 0 || u > 0) ? 1u : 0u);
                 tc_commit(&C.mma_done[st]);
                 *reinterpret_cast<volatile int *>(&C.issued) = i + 1;
             }
@@ -634,6 +635,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         }
         cp_async_wait_pending<0>();
     }
+    if (tid < T) C.xs[tid] = xs_own;  // read after the barriers below
     // the last commit covers every MMA issued before it
     __syncthreads();
     const int issued = C.issued;
