@@ -428,10 +428,16 @@ __global__ void __launch_bounds__(256) lanes_attn_merge_smem_kernel(const float 
     LaneAttnWs w = lane_attn_ws(const_cast<float *>(ws), i, ncmax, nh, hd);
     const float *pU = w.U + (int64_t)h * ncmax * hd, *pm = w.m + h * ncmax, *pS = w.S + h * ncmax;
     float *U = msm, *Mc = U + (size_t)ncmax * hd, *Sc = Mc + ncmax, *wb = Sc + ncmax, *o = wb + next_pow2(ncmax);
-    for (int e = threadIdx.x; e < nc * hd; e += blockDim.x)
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(U + e)),
-                     "l"(pU + e)
-                     : "memory");
+    // a lane's U rows start 16-byte aligned when nh ncmax is even (hd is a
+    // multiple of 4 and the workspace base is aligned): 16-byte copies then
+    if (((nh * ncmax) & 1) == 0) {
+        for (int e = threadIdx.x; e < nc * hd / 4; e += blockDim.x) lanes_cp16(U + 4 * e, pU + 4 * e);
+    } else {
+        for (int e = threadIdx.x; e < nc * hd; e += blockDim.x)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(U + e)),
+                         "l"(pU + e)
+                         : "memory");
+    }
     for (int c = threadIdx.x; c < nc; c += blockDim.x) {
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(Mc + c)),
                      "l"(pm + c)
@@ -589,8 +595,10 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
                                      m->scales + (int64_t)l * T158_NMAT + j, out, M, rows[j], cols[j], s, w.tiles,
                                      convert);
     };
-    // the quantisers also write the tensor-core tiles when the linears take that path
+    // the quantisers write the tensor-core tiles when the linears take that path
+    // (and then no int8 codes: nothing reads them), else the codes
     void *const tiles = M >= kLanesTensorMin ? w.tiles : nullptr;
+    int8_t *const codes = tiles ? nullptr : w.xq;
     // linears j0 .. j0 + n - 1 of layer l (same input): one tensor-core launch on the tiles, else one each
     auto lin_group = [&](int l, int j0, int n, float *const *out) -> qlin_status {
         if (!tiles) {
@@ -633,7 +641,7 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     QLIN_LAUNCHED("lanes_embed_kernel");
     for (int l = 0; l < L; l++) {
         // (the previous layer's FFN output joins the residual stream here)
-        if ((st = norm_quant_tiles(w.h, l > 0 ? w.y : nullptr, m->g_attn + (int64_t)l * d, m->eps, w.xq, w.xs, M, d,
+        if ((st = norm_quant_tiles(w.h, l > 0 ? w.y : nullptr, m->g_attn + (int64_t)l * d, m->eps, codes, w.xs, M, d,
                                    tiles, s)))
             return st;
         {
@@ -665,13 +673,13 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
                 w.attn, ncmax, positions, seqs, n_seqs, m->max_pos, nh, hd, w.att);
             QLIN_LAUNCHED("lanes_attn_merge_kernel");
         }
-        if ((st = quant_i8_tiles(w.att, w.xq, w.xs, M, qd, tiles, s)) || (st = lin_group(l, 3, 1, &w.y))) return st;
-        if ((st = norm_quant_tiles(w.h, w.y, m->g_ffn + (int64_t)l * d, m->eps, w.xq, w.xs, M, d, tiles, s))) return st;
+        if ((st = quant_i8_tiles(w.att, codes, w.xs, M, qd, tiles, s)) || (st = lin_group(l, 3, 1, &w.y))) return st;
+        if ((st = norm_quant_tiles(w.h, w.y, m->g_ffn + (int64_t)l * d, m->eps, codes, w.xs, M, d, tiles, s))) return st;
         {
             float *const gu[2] = {w.g, w.u};
             if ((st = lin_group(l, 4, 2, gu))) return st;
         }
-        if ((st = geglu_quant_tiles(w.g, w.u, w.xq, w.xs, M, f, tiles, s)) || (st = lin_group(l, 6, 1, &w.y))) return st;
+        if ((st = geglu_quant_tiles(w.g, w.u, codes, w.xs, M, f, tiles, s)) || (st = lin_group(l, 6, 1, &w.y))) return st;
     }
     lanes_add_kernel<<<add_blocks, 256, 0, s>>>(w.h, w.y, (int64_t)M * d);  // the last layer's FFN output
     QLIN_LAUNCHED("lanes_add_kernel");

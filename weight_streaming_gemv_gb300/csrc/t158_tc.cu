@@ -346,9 +346,9 @@ struct QtArgs {
     const float *g;  // kQtNorm: the RMSNorm gain
     const float *u;  // kQtGeglu: the up projection
     float eps;
-    int8_t *xq;
+    int8_t *xq;      // the codes [M][K], or null when only the tiles are wanted
     float *xs;
-    uint8_t *tiles;  // activation tiles (t158_tc_workspace_bytes(M, K)), or null
+    uint8_t *tiles;  // activation tiles (t158_tc_workspace_bytes(M, K)), or null (then xq is required)
     int M, K, T, tiles_m, nsteps;
 };
 
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kQtThreads) t158_quant_tiles_kernel(QtArgs a) 
                 q2[e] = 0;
                 if (real && k < K) {
                     q2[e] = quant_code_r(row[k], sc, rinv);
-                    a.xq[(int64_t)m * K + k] = (int8_t)q2[e];
+                    if (a.xq) a.xq[(int64_t)m * K + k] = (int8_t)q2[e];
                 }
             }
             const __half2 hv = __halves2half2(__int2half_rn(q2[0]), __int2half_rn(q2[1]));
@@ -901,6 +901,7 @@ static qlin_status launch_qt(QtArgs a, void *work, cudaStream_t st) {
                         : MODE == kQtGeglu ? (size_t)a.K * sizeof(float)
                                            : (size_t)(a.K + next_pow2(a.K)) * sizeof(float);
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "quantiser: row of %d too long", a.K);
+    QLIN_REQUIRE(a.xq || work, QLIN_ERR_INVALID_ARG, "quantiser: neither codes nor tiles requested");
     if (smem > 48 * 1024) blocks_per_sm((const void *)t158_quant_tiles_kernel<MODE>, smem);
     const unsigned grid = (unsigned)(work ? tiles_m * T : a.M);
     t158_quant_tiles_kernel<MODE><<<grid, kQtThreads, smem, st>>>(a);
