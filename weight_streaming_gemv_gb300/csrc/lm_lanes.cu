@@ -237,7 +237,13 @@ __global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
         }
     } else {
         for (int t = 0; t < nsteps && !*abort; t++) {
-            // stage (t - 1) % S is refilled with step t + S - 1 once the MMAs of step t - 1 are done
+            // step t is signalled as soon as this thread's copies of it have landed
+            // (one group per step; steps t + 1 and t + 2 may still be in flight) ...
+            ll_wait_group<kLlStages - 2>();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&S.full[t % kLlStages]);
+            // ... then stage (t - 1) % S is refilled with step t + S - 1 once the
+            // MMAs of step t - 1 are done
             if (t >= 1 && t + kLlStages - 1 < nsteps &&
                 !mbar_wait(&S.mma_done[(t - 1) % kLlStages], ((t - 1) / kLlStages) & 1)) {
                 *abort = 1;
@@ -245,9 +251,6 @@ __global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
                 break;
             }
             fetch(t + kLlStages - 1);
-            ll_wait_group<kLlStages - 1>();  // this thread's copies of step t have landed
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&S.full[t % kLlStages]);
         }
         ll_wait_group<0>();
     }
@@ -280,31 +283,40 @@ __global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
     // each lane's logits, its best row in this tile
     const int Up = A.Up;
     if (warp < 8) {
-        for (int u = warp; u < A.U; u += 8) {
-            float bv = -__int_as_float(0x7f800000);
-            int bi = 0x7fffffff;
-            for (int r = lane; r < kLlRows; r += 32) {
-                const int row = row0 + r;
-                if (row >= A.V) break;
-                const float v = ok ? __fadd_rn(__fadd_rn(S.d[r][u], S.d[r][Up + u]), S.d[r][2 * Up + u])
-                                   : __int_as_float(0x7fc00000);
-                if (A.logits) A.logits[(int64_t)u * A.V + row] = v;
-                if (ll_better(v, row, bv, bi)) {
-                    bv = v;
-                    bi = row;
-                }
-            }
+        // warp w: lanes w, w + 8, ... together (the (value, row) order is total,
+        // so the reduction order does not matter)
+        constexpr int LPW = kLlMaxLanes / 8;
+        float bv[LPW];
+        int bi[LPW];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (ll_better(ov, oi, bv, bi)) {
-                    bv = ov;
-                    bi = oi;
+        for (int j = 0; j < LPW; j++) bv[j] = -__int_as_float(0x7f800000), bi[j] = 0x7fffffff;
+        for (int r = lane; r < kLlRows; r += 32) {
+            const int row = row0 + r;
+            if (row >= A.V) break;
+#pragma unroll
+            for (int j = 0; j < LPW; j++) {
+                const int u = warp + 8 * j;
+                if (u < A.U) {
+                    const float v = ok ? __fadd_rn(__fadd_rn(S.d[r][u], S.d[r][Up + u]), S.d[r][2 * Up + u])
+                                       : __int_as_float(0x7fc00000);
+                    if (A.logits) A.logits[(int64_t)u * A.V + row] = v;
+                    if (ll_better(v, row, bv[j], bi[j])) bv[j] = v, bi[j] = row;
                 }
             }
-            if (lane == 0) A.part[(int64_t)blockIdx.x * kLlMaxLanes + u] = make_float2(bv, __int_as_float(bi));
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int j = 0; j < LPW; j++) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv[j], off);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi[j], off);
+                if (ll_better(ov, oi, bv[j], bi[j])) bv[j] = ov, bi[j] = oi;
+            }
+        if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < LPW; j++)
+                if (warp + 8 * j < A.U)
+                    A.part[(int64_t)blockIdx.x * kLlMaxLanes + warp + 8 * j] = make_float2(bv[j], __int_as_float(bi[j]));
     }
     __syncthreads();
     if (tid == 0) {
