@@ -324,17 +324,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     part[h] = pp[0];
                 }
             }
+            // Reduce-scatter over the heads, then a butterfly: at level off = 1,
+            // 2, .. < GRP a lane keeps the half of its heads picked by lane bit
+            // off, sends the other half and adds the partner's copy of the half
+            // it keeps (the partner sent exactly those); once one head is left
+            // (hk, from the lane's low bits) the remaining levels are those of
+            // warp_psum.  Every head's sum is the same adjacent-lanes-first tree.
+            int hk = 0;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1)
+            for (int off = 1, n = GRP; off < GRP; off <<= 1, n >>= 1) {
+                const bool up = (lane & off) != 0;
 #pragma unroll
-                for (int h = 0; h < GRP; h++) part[h] = __fadd_rn(part[h], __shfl_xor_sync(0xffffffffu, part[h], off));
-            if (lane < GRP) {  // lane h stores head h
-                float sv = part[0];
-#pragma unroll
-                for (int h = 1; h < GRP; h++)
-                    if (lane == h) sv = part[h];
-                sc[lane][t] = (t < nt) ? __fdiv_rn(sv, div) : 0.0f;
+                for (int i = 0; i < n / 2; i++) {
+                    const float keep = up ? part[n / 2 + i] : part[i];
+                    const float send = up ? part[i] : part[n / 2 + i];
+                    part[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, off));
+                }
+                if (up) hk += n / 2;
             }
+            float sv = part[0];
+#pragma unroll
+            for (int off = GRP; off < 32; off <<= 1) sv = __fadd_rn(sv, __shfl_xor_sync(0xffffffffu, sv, off));
+            if (lane < GRP) sc[hk][t] = (t < nt) ? __fdiv_rn(sv, div) : 0.0f;  // lanes 0 .. GRP-1 hold every head once
         }
         __syncthreads();
         if (warp < grp) {  // softmax of head `warp` over the chunk
