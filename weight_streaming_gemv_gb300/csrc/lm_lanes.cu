@@ -9,15 +9,20 @@
 // three bf16 terms, x = hi + mid + lo with hi = bf16(x), mid = bf16(x - hi),
 // lo = bf16(x - hi - mid) (each difference exact in fp32), so the three
 // partial logits carry x to 24 bits and their fp32 sum (hi + mid) + lo is
-// within fp32 rounding of the fp32 dot product.  K advances 64 elements a
-// step through four shared-memory stages filled by cp.async (256 loader
-// threads, 16-byte copies into the no-swizzle K-major core-matrix layout); one
-// thread issues the step's four MMAs.  The accumulator goes to shared memory,
-// each lane's logits are formed, written (if asked for) and reduced to the
-// CTA's best row; the last CTA reduces the CTAs' bests per lane.
+// within fp32 rounding of the fp32 dot product.  One persistent CTA per SM
+// walks its row tiles: K advances 64 elements a step through four
+// shared-memory stages (table rows by cp.async from 256 loader threads into
+// the no-swizzle K-major core-matrix layout; the lanes' operand as one bulk
+// copy of the image the split kernel prepared), one thread issues each step's
+// four MMAs, and two accumulators alternate between tiles so that four
+// epilogue warps reduce one tile (each lane's logits, its best row) while the
+// next is multiplied.  The last CTA reduces the CTAs' bests per lane.
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "stream.cuh"
@@ -29,30 +34,51 @@ constexpr int kLlRows = 128;              // table rows per CTA (MMA M)
 constexpr int kLlKS = 64;                 // K elements per step
 constexpr int kLlChunks = kLlKS / 8;      // 16-byte core-matrix columns per row and step
 constexpr int kLlSBO = kLlChunks * 128;   // bytes between 8-row groups
-constexpr int kLlStages = 4;
-constexpr int kLlLoaders = 256;
-constexpr int kLlThreads = kLlLoaders + 32;  // + the warp that issues the MMAs
+constexpr int kLlStages = 5;
+constexpr int kLlEpiWarps = 4;  // read a finished tile's accumulator (one per tensor-memory lane quarter)
+constexpr int kLlThreads = 64 + 32 * kLlEpiWarps;  // the copy warp, the MMA warp, the epilogue warps
 constexpr int kLlMaxLanes = 64;              // lanes per pass: 3 x 64 = 192 accumulator columns
 constexpr int kLlMaxN = 3 * kLlMaxLanes;
-constexpr uint32_t kLlCols = 256;            // tensor-memory columns allocated
-constexpr int kLlDStride = kLlMaxN + 1;      // floats per accumulator row in shared memory
+constexpr uint32_t kLlCols = 512;            // tensor-memory columns: two accumulators, at 0 and 256
+constexpr int kLlAccStride = 256;
+constexpr int kLlATile = kLlRows * kLlKS * 2;     // 16 KB: 128 table rows x 64 inputs, 128-byte swizzled
+constexpr int kLlBTile = kLlMaxN / 8 * kLlSBO;    // 24 KB: the lanes' operand of a step
 
-struct LlSmem {
-    union {
-        struct {
-            uint8_t a[kLlStages][kLlRows / 8 * kLlSBO];  // table rows of a step
-            uint8_t b[kLlStages][kLlMaxN / 8 * kLlSBO];  // the lanes' split x of a step
-        } in;
-        float d[kLlRows][kLlDStride];  // after the K loop: the accumulator
-    };
-    uint64_t full[kLlStages];      // the stage has landed (kLlLoaders arrivals + the lanes operand's bytes)
-    uint64_t mma_done[kLlStages];  // the MMAs reading the stage are done (tcgen05.commit)
-    float bv[8][kLlMaxLanes];      // epilogue: each warp's best per lane
-    int bi[8][kLlMaxLanes];
+struct LlSmem {  // 1024-byte aligned (the swizzled table tiles)
+    uint8_t a[kLlStages][kLlATile];  // table rows of a step, as the tensor copy writes them
+    uint8_t b[kLlStages][kLlBTile];  // the lanes' split x of a step
+    uint64_t full[kLlStages];        // the stage has landed (one arrival + the bytes of both copies)
+    uint64_t mma_done[kLlStages];    // the MMAs reading the stage are done (tcgen05.commit)
+    uint64_t acc_full[2];            // accumulator b holds a finished tile (tcgen05.commit)
+    uint64_t acc_empty[2];           // the epilogue warps have read accumulator b
+    float2 wbest[kLlEpiWarps][kLlMaxLanes];  // a tile's best (value, row) per lane from each epilogue warp
+    float2 cbest[kLlMaxLanes];               // this CTA's best per lane over its tiles so far
     uint32_t tmem;
     int abort;
     int last;
 };
+
+// Descriptor of a table tile: K-major, 128-byte swizzle (the layout of the
+// tensor copy with CU_TENSOR_MAP_SWIZZLE_128B: row r at 128 r, its 16-byte
+// chunk c at chunk c ^ (r % 8)), 8-row groups 1024 bytes apart; the start
+// advances 32 bytes per 16 inputs inside the swizzle atom.
+__device__ __forceinline__ uint64_t ll_desc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;                         // leading byte offset (unused for this layout)
+    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;  // next 8-row group
+    d |= (uint64_t)1 << 46;                         // descriptor version
+    d |= (uint64_t)2 << 61;                         // 128-byte swizzle
+    return d;
+}
+
+// 2-D tensor copy (tile mode; out-of-range rows read as zeros) completing on bar
+__device__ __forceinline__ void ll_tma_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
 
 __device__ __forceinline__ uint64_t ll_desc(uint32_t saddr) {
     uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
@@ -82,27 +108,11 @@ __device__ __forceinline__ void ll_commit(uint64_t *bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void ll_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// 16-byte cp.async; nbytes < 16 zero-fills the rest
-__device__ __forceinline__ void ll_cp16(void *dst, const void *src, int nbytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(nbytes)
-                 : "memory");
-}
-__device__ __forceinline__ void ll_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void ll_wait_group() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// 8 consecutive accumulator columns of this thread's tensor-memory lane (no wait)
+__device__ __forceinline__ void ll_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
 }
 
 __device__ __forceinline__ int ll_off(int r, int kc) { return (r >> 3) * kLlSBO + kc * 128 + (r & 7) * 16; }
@@ -149,175 +159,176 @@ struct LlArgs {
     int32_t *status;
 };
 
-__global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
-    extern __shared__ __align__(128) uint8_t ll_smem_raw[];
-    LlSmem &S = *reinterpret_cast<LlSmem *>(ll_smem_raw);
+// Persistent: CTA c takes row tiles c, c + gridDim.x, ... (128 rows each).  The
+// K steps of all its tiles form one sequence g = tile * nsteps + step through
+// the stage ring, so the copies of the next tile start while the current one
+// is multiplied.  Two accumulators alternate between tiles: the epilogue warps
+// read tile i's (each lane's logits, its best row) while the MMAs of tile i + 1
+// run.  Each lane's best over the CTA's tiles stays in shared memory; the last
+// CTA to finish takes every lane's best over the CTAs (ties to the lower row).
+__global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(const __grid_constant__ CUtensorMap tmap, LlArgs A) {
+    extern __shared__ uint8_t ll_smem_raw[];
+    // the swizzled table tiles want a 1024-byte aligned base (the launch adds 1 KB)
+    uint8_t *const ll_base = ll_smem_raw + ((1024u - (smem_addr(ll_smem_raw) & 1023u)) & 1023u);
+    LlSmem &S = *reinterpret_cast<LlSmem *>(ll_base);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row0 = blockIdx.x * kLlRows;
-    const int K = A.K, N = 3 * A.Up;
+    const int K = A.K, Up = A.Up, N = 3 * Up;
     const int nsteps = (K + kLlKS - 1) / kLlKS;
-
+    const int ntiles = (A.V + kLlRows - 1) / kLlRows;
+    const int my_tiles = ntiles > (int)blockIdx.x ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = my_tiles * nsteps;  // steps of this CTA
+    auto tile_row0 = [&](int i) { return ((int)blockIdx.x + i * (int)gridDim.x) * kLlRows; };
     const uint32_t bbytes = (uint32_t)N * kLlKS * 2;  // the lanes' operand of one step
-    const uint64_t keep = ll_evict_last();
-    // step t's lanes operand: one bulk copy of its image (thread 0; the stage's
-    // barrier is initialised), completing on the stage's full barrier
-    auto fetch_b = [&](int t) {
-        if (t < nsteps) {
-            const int st = t % kLlStages;
-            mbar_arrive_expect_tx(&S.full[st], bbytes);
-            bulk_g2s(S.in.b[st], A.xs + (int64_t)t * N * kLlKS, bbytes, &S.full[st], keep);
-        }
-    };
-    // step t's table rows into its stage: 1024 chunks of 16 bytes over the loaders
-    auto fetch = [&](int t) {
-        if (t < nsteps) {
-            const int st = t % kLlStages, k0 = t * kLlKS;
-            for (int idx = tid; idx < kLlRows * kLlChunks; idx += kLlLoaders) {
-                const int r = idx / kLlChunks, kc = idx % kLlChunks;
-                const int row = row0 + r, k = k0 + 8 * kc;
-                const bool ok = row < A.V && k < K;
-                ll_cp16(S.in.a[st] + ll_off(r, kc), A.emb + (ok ? (int64_t)row * K + k : 0), ok ? 16 : 0);
-            }
-            if (tid == 0) fetch_b(t);
-        }
-        ll_commit_group();
-    };
-    if (tid < kLlLoaders)
-        for (int t = 0; t < kLlStages - 1; t++) {  // table rows only: the barriers are not yet initialised
-            if (t < nsteps) {
-                const int st = t % kLlStages, k0 = t * kLlKS;
-                for (int idx = tid; idx < kLlRows * kLlChunks; idx += kLlLoaders) {
-                    const int r = idx / kLlChunks, kc = idx % kLlChunks;
-                    const int row = row0 + r, k = k0 + 8 * kc;
-                    const bool ok = row < A.V && k < K;
-                    ll_cp16(S.in.a[st] + ll_off(r, kc), A.emb + (ok ? (int64_t)row * K + k : 0), ok ? 16 : 0);
-                }
-            }
-            ll_commit_group();
-        }
+
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&S.tmem)),
                      "r"(kLlCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (tid == kLlLoaders) {
+    if (tid == 32) {
         for (int i = 0; i < kLlStages; i++) {
-            mbar_init(&S.full[i], kLlLoaders + 1);  // the loaders, and thread 0's byte-counted arrival
+            mbar_init(&S.full[i], 1);
             mbar_init(&S.mma_done[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&S.acc_full[i], 1);
+            mbar_init(&S.acc_empty[i], 32 * kLlEpiWarps);
         }
         S.abort = 0;
         fence_mbar_init();
     }
+    if (tid < kLlMaxLanes) S.cbest[tid] = make_float2(-__int_as_float(0x7f800000), __int_as_float(0x7fffffff));
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = S.tmem;
     volatile int *abort = &S.abort;
-    if (tid == 0)
-        for (int t = 0; t < kLlStages - 1; t++) fetch_b(t);
 
-    if (warp == kLlLoaders / 32) {
-        if (lane == 0) {  // the MMAs of each step once its stage is full
+    if (warp == 0) {
+        // ---- copies: step g's table tile (one tensor copy) and lanes operand
+        // (one bulk copy) into stage g % S once the MMAs of step g - S are done
+        if (lane == 0) {
+            const uint64_t keep = ll_evict_last();
+            for (int g = 0; g < total && !*abort; g++) {
+                const int st = g % kLlStages;
+                if (g >= kLlStages && !mbar_wait(&S.mma_done[st], (uint32_t)(g / kLlStages - 1) & 1u)) {
+                    *abort = 1;
+                    raise_status(A.status, kStatusTimeout);
+                    break;
+                }
+                mbar_arrive_expect_tx(&S.full[st], (uint32_t)kLlATile + bbytes);
+                ll_tma_2d(S.a[st], &tmap, (g % nsteps) * kLlKS, tile_row0(g / nsteps), &S.full[st]);
+                bulk_g2s(S.b[st], A.xs + (int64_t)(g % nsteps) * N * kLlKS, bbytes, &S.full[st], keep);
+            }
+        }
+    } else if (warp == 1) {
+        // ---- lane 0 issues each step's four MMAs into the tile's accumulator
+        if (lane == 0) {
             const uint32_t idesc = ll_idesc(N);
-            for (int t = 0; t < nsteps && !*abort; t++) {
-                const int st = t % kLlStages;
-                if (!mbar_wait(&S.full[st], (t / kLlStages) & 1)) {
+            for (int g = 0; g < total && !*abort; g++) {
+                const int ti = g / nsteps, t = g % nsteps, buf = ti & 1;
+                // the accumulator of tile ti - 2 must have been read out
+                if (t == 0 && ti >= 2 && !mbar_wait(&S.acc_empty[buf], (uint32_t)((ti >> 1) - 1) & 1u)) {
+                    *abort = 1;
+                    raise_status(A.status, kStatusTimeout);
+                    break;
+                }
+                const int st = g % kLlStages;
+                if (!mbar_wait(&S.full[st], (uint32_t)(g / kLlStages) & 1u)) {
                     *abort = 1;
                     raise_status(A.status, kStatusTimeout);
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a0 = smem_addr(S.in.a[st]), b0 = smem_addr(S.in.b[st]);
+                const uint32_t a0 = smem_addr(S.a[st]), b0 = smem_addr(S.b[st]);
+                const uint32_t dacc = tmem + (uint32_t)(buf * kLlAccStride);
 #pragma unroll
-                for (int kk = 0; kk < kLlKS / 16; kk++)  // K = 16: two core-matrix columns (256 bytes)
-                    ll_mma(tmem, ll_desc(a0 + 256u * kk), ll_desc(b0 + 256u * kk), idesc, (t > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kLlKS / 16; kk++)  // K = 16: 32 bytes of a table row, 2 core-matrix columns of x
+                    ll_mma(dacc, ll_desc_sw128(a0 + 32u * kk), ll_desc(b0 + 256u * kk), idesc,
+                           (t > 0 || kk > 0) ? 1u : 0u);
                 ll_commit(&S.mma_done[st]);
+                if (t == nsteps - 1) ll_commit(&S.acc_full[buf]);
             }
         }
     } else {
-        for (int t = 0; t < nsteps && !*abort; t++) {
-            // step t is signalled as soon as this thread's copies of it have landed
-            // (one group per step; steps t + 1 and t + 2 may still be in flight) ...
-            ll_wait_group<kLlStages - 2>();
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&S.full[t % kLlStages]);
-            // ... then stage (t - 1) % S is refilled with step t + S - 1 once the
-            // MMAs of step t - 1 are done
-            if (t >= 1 && t + kLlStages - 1 < nsteps &&
-                !mbar_wait(&S.mma_done[(t - 1) % kLlStages], ((t - 1) / kLlStages) & 1)) {
+        // ---- epilogue warps: warp w reads tensor-memory lanes 32 (w % 4) .. + 31,
+        // i.e. those rows of each finished tile
+        const int ew = warp - 2;
+        const int q = warp & 3;
+        for (int ti = 0; ti < my_tiles; ti++) {
+            const int buf = ti & 1;
+            uint32_t fail = *abort != 0;
+            if (!fail && !mbar_wait(&S.acc_full[buf], (uint32_t)(ti >> 1) & 1u)) {
+                fail = 1;
                 *abort = 1;
                 raise_status(A.status, kStatusTimeout);
-                break;
             }
-            fetch(t + kLlStages - 1);
-        }
-        ll_wait_group<0>();
-    }
-    // the last commit covers every MMA issued before it
-    if (nsteps > 0 && !*abort) {
-        const int t = nsteps - 1;
-        if (!mbar_wait(&S.mma_done[t % kLlStages], (t / kLlStages) & 1)) {
-            *abort = 1;
-            raise_status(A.status, kStatusTimeout);
-        }
-    }
-    __syncthreads();
-    const bool ok = !*abort;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    // the accumulator into shared memory: warp w (< 4) reads lanes 32 w .. + 31
-    if (warp < 4 && ok) {
-        const int row = 32 * warp + lane;
-        for (int col = 0; col < N; col += 32) {
-            uint32_t r[32];
-            ll_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)col, r);
+            // one decision for all epilogue warps (they meet at named barriers below)
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                : "=r"(fail)
+                : "r"(fail), "n"(32 * kLlEpiWarps)
+                : "memory");
+            if (fail) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int row = tile_row0(ti) + 32 * q + lane;
+            const bool row_ok = row < A.V;
+            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kLlAccStride);
+            for (int u0 = 0; u0 < Up; u0 += 8) {
+                uint32_t hi[8], mid[8], lo[8];
+                ll_ld8(tb + (uint32_t)u0, hi);
+                ll_ld8(tb + (uint32_t)(Up + u0), mid);
+                ll_ld8(tb + (uint32_t)(2 * Up + u0), lo);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                float bv[8];
+                int bi[8];
 #pragma unroll
-            for (int j = 0; j < 32; j++)
-                if (col + j < kLlMaxN) S.d[row][col + j] = __uint_as_float(r[j]);
+                for (int j = 0; j < 8; j++) {
+                    const int u = u0 + j;
+                    const float v = __fadd_rn(__fadd_rn(__uint_as_float(hi[j]), __uint_as_float(mid[j])),
+                                              __uint_as_float(lo[j]));
+                    const bool ok = row_ok && u < A.U;
+                    if (ok && A.logits) A.logits[(int64_t)u * A.V + row] = v;
+                    bv[j] = ok ? v : -__int_as_float(0x7f800000);
+                    bi[j] = ok ? row : 0x7fffffff;
+                }
+                // (value, row) is a total order: the reduction order does not matter
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        const float ov = __shfl_xor_sync(0xffffffffu, bv[j], off);
+                        const int oi = __shfl_xor_sync(0xffffffffu, bi[j], off);
+                        if (ll_better(ov, oi, bv[j], bi[j])) bv[j] = ov, bi[j] = oi;
+                    }
+                if (lane == 0)
+#pragma unroll
+                    for (int j = 0; j < 8; j++) S.wbest[ew][u0 + j] = make_float2(bv[j], __int_as_float(bi[j]));
+            }
+            // the accumulator is read: the MMAs of tile ti + 2 may overwrite it
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            mbar_arrive(&S.acc_empty[buf]);
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kLlEpiWarps) : "memory");
+            if (ew == 0)
+                for (int u = lane; u < A.U; u += 32) {
+                    float2 b = S.cbest[u];
+#pragma unroll
+                    for (int w = 0; w < kLlEpiWarps; w++) {
+                        const float2 c = S.wbest[w][u];
+                        if (ll_better(c.x, __float_as_int(c.y), b.x, __float_as_int(b.y))) b = c;
+                    }
+                    S.cbest[u] = b;
+                }
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kLlEpiWarps) : "memory");  // wbest is free for the next tile
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kLlCols) : "memory");
-    // each lane's logits, its best row in this tile
-    const int Up = A.Up;
-    if (warp < 8) {
-        // warp w: lanes w, w + 8, ... together (the (value, row) order is total,
-        // so the reduction order does not matter)
-        constexpr int LPW = kLlMaxLanes / 8;
-        float bv[LPW];
-        int bi[LPW];
-#pragma unroll
-        for (int j = 0; j < LPW; j++) bv[j] = -__int_as_float(0x7f800000), bi[j] = 0x7fffffff;
-        for (int r = lane; r < kLlRows; r += 32) {
-            const int row = row0 + r;
-            if (row >= A.V) break;
-#pragma unroll
-            for (int j = 0; j < LPW; j++) {
-                const int u = warp + 8 * j;
-                if (u < A.U) {
-                    const float v = ok ? __fadd_rn(__fadd_rn(S.d[r][u], S.d[r][Up + u]), S.d[r][2 * Up + u])
-                                       : __int_as_float(0x7fc00000);
-                    if (A.logits) A.logits[(int64_t)u * A.V + row] = v;
-                    if (ll_better(v, row, bv[j], bi[j])) bv[j] = v, bi[j] = row;
-                }
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-            for (int j = 0; j < LPW; j++) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv[j], off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi[j], off);
-                if (ll_better(ov, oi, bv[j], bi[j])) bv[j] = ov, bi[j] = oi;
-            }
-        if (lane == 0)
-#pragma unroll
-            for (int j = 0; j < LPW; j++)
-                if (warp + 8 * j < A.U)
-                    A.part[(int64_t)blockIdx.x * kLlMaxLanes + warp + 8 * j] = make_float2(bv[j], __int_as_float(bi[j]));
-    }
+    if (tid < A.U) A.part[(int64_t)blockIdx.x * kLlMaxLanes + tid] = S.cbest[tid];
     __syncthreads();
     if (tid == 0) {
         __threadfence();
@@ -327,8 +338,8 @@ __global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
     if (!S.last) return;
     __threadfence();
     // the last CTA: every lane's best over all CTAs (ties to the lower row)
-    if (warp < 8) {
-        for (int u = warp; u < A.U; u += 8) {
+    {
+        for (int u = warp; u < A.U; u += kLlThreads / 32) {
             float bv = -__int_as_float(0x7f800000);
             int bi = 0x7fffffff;
             for (int c = lane; c < (int)gridDim.x; c += 32) {
@@ -354,6 +365,41 @@ __global__ void __launch_bounds__(kLlThreads, 1) lm_lanes_kernel(LlArgs A) {
 }
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+// The table's tensor map: bf16 [vocab][dim], boxes of 64 inputs x 128 rows,
+// 128-byte swizzle, zeros out of range.  Encoded through the driver entry
+// point (no link against the driver library); the last one is kept for the
+// next call with the same table.
+qlin_status table_map(const uint16_t *emb, int vocab, int dim, CUtensorMap *out) {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static CUtensorMap last;
+    static const void *last_emb = nullptr;
+    static int last_v = 0, last_d = 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (last_emb == emb && last_v == vocab && last_d == dim) {
+        *out = last;
+        return QLIN_OK;
+    }
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        QLIN_CUDA(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
+        QLIN_REQUIRE(fn && q == cudaDriverEntryPointSuccess, QLIN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+        encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    const cuuint64_t gdim[2] = {(cuuint64_t)dim, (cuuint64_t)vocab};
+    const cuuint64_t gstride[1] = {(cuuint64_t)dim * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kLlKS, (cuuint32_t)kLlRows};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = encode(&last, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(emb), gdim, gstride, box,
+                              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    QLIN_REQUIRE(r == CUDA_SUCCESS, QLIN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    last_emb = emb, last_v = vocab, last_d = dim;
+    *out = last;
+    return QLIN_OK;
+}
 
 struct LlWs {
     int32_t *status;
@@ -404,10 +450,12 @@ qlin_status qlin_lm_head_lanes(const uint16_t *emb, const float *x, int vocab, i
     QLIN_REQUIRE(workspace_bytes >= w.bytes, QLIN_ERR_INVALID_ARG, "qlin_lm_head_lanes: workspace %zu < %zu bytes",
                  workspace_bytes, w.bytes);
     cudaStream_t st = (cudaStream_t)stream;
-    const size_t smem = sizeof(LlSmem);
+    const size_t smem = sizeof(LlSmem) + 1024;  // + the alignment of the swizzled tiles
+    CUtensorMap tmap;
+    if (qlin_status e = table_map(emb, vocab, dim, &tmap)) return e;
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "qlin_lm_head_lanes: tile does not fit");
     blocks_per_sm((const void *)lm_lanes_kernel, smem);  // raises the dynamic shared-memory limit once
-    const int grid = (vocab + kLlRows - 1) / kLlRows;
+    const int grid = std::min(sm_count(), (vocab + kLlRows - 1) / kLlRows);  // persistent: one CTA per SM
     for (int u0 = 0; u0 < n_lanes; u0 += kLlMaxLanes) {  // up to 64 lanes per pass over the table
         const int U = std::min(kLlMaxLanes, n_lanes - u0);
         const int Up = (U + 15) / 16 * 16;
@@ -426,7 +474,7 @@ qlin_status qlin_lm_head_lanes(const uint16_t *emb, const float *x, int vocab, i
         a.part = w.part;
         a.ticket = w.ticket;
         a.status = w.status;
-        lm_lanes_kernel<<<grid, kLlThreads, smem, st>>>(a);
+        lm_lanes_kernel<<<grid, kLlThreads, smem, st>>>(tmap, a);
         QLIN_LAUNCHED("lm_lanes_kernel");
     }
     return QLIN_OK;
