@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     extern __shared__ __align__(16) float abuf[];  // [kAttnBufs][2][32][HD]
     __shared__ __align__(16) float sc[GRP][32];
     __shared__ uint64_t full[kAttnBufs];  // buffer b's rows have landed (one arrival + the bytes)
+    __shared__ int4 unit[kAttnBufs];      // buffer b's unit {lane, KV head, chunk, position}, lane -1: no more
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = nh / nkv;  // query heads per KV head, <= GRP
     if (tid == 0) {
@@ -237,13 +238,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float *vc = kc + (int64_t)max_pos * ld;
         float *Kb = abuf + (size_t)b * 2 * CH, *Vb = Kb + CH;
         constexpr uint32_t rowb = HD * sizeof(float);
+        // (the issuing warp only)
         if (ld == HD) {  // one KV head: the chunk's k rows are contiguous, and so are its v rows
-            if (tid == 0) {
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&full[b], 2u * (uint32_t)nt * rowb);
                 bulk_g2s(Kb, kc, (uint32_t)nt * rowb, &full[b], pol);
                 bulk_g2s(Vb, vc, (uint32_t)nt * rowb, &full[b], pol);
             }
-        } else if (warp == 0) {  // one bulk copy per k row and per v row, lane t: row t
+        } else {  // one bulk copy per k row and per v row, lane t: row t
             if (lane == 0) mbar_arrive_expect_tx(&full[b], 2u * (uint32_t)nt * rowb);
             __syncwarp();
             if (lane < nt) {
@@ -252,28 +254,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
         }
     };
+    // The last warp walks the units and issues the copies: it publishes buffer
+    // b's unit in unit[b] before the buffer's barrier completes (with the bytes,
+    // or with a plain arrival for the end marker), so the other warps learn
+    // the unit there; it finds the next unit while the others take the softmax.
+    constexpr int kIssWarp = kAttnThreads / 32 - 1;
+    static_assert(kIssWarp >= GRP, "the issuing warp is not a softmax warp");
+    auto publish = [&](int4 un, int b) {
+        if (lane == 0) unit[b] = un;
+        __syncwarp();
+        if (un.x >= 0)
+            issue(un, b);
+        else if (lane == 0)
+            mbar_arrive(&full[b]);
+    };
 
-    int4 slot[kAttnBufs];
-#pragma unroll
-    for (int b = 0; b < kAttnBufs; b++) {
-        slot[b] = advance();
-        if (slot[b].x >= 0) issue(slot[b], b);
-    }
+    if (warp == kIssWarp)
+        for (int b = 0; b < kAttnBufs; b++) publish(advance(), b);
+    int4 nx = make_int4(-1, 0, 0, 0);  // the issuing warp: the unit found during the softmax
     float qr[GRP][S];
     int64_t cur = -1;  // lane * nkv + KV head whose q rows are in qr
     for (int k = 0;; k++) {
         const int b = k % kAttnBufs;
-        int4 un = slot[0];
-#pragma unroll
-        for (int j = 1; j < kAttnBufs; j++)
-            if (j == b) un = slot[j];
-        if (un.x < 0) break;
-        // unit un's k and v rows are in buffer b (its (k / kAttnBufs)-th fill)
+        // buffer b's (k / kAttnBufs)-th fill: unit[b] and, for a unit, its k and v rows
         const bool landed = mbar_wait(&full[b], (uint32_t)(k / kAttnBufs) & 1u);
         if (__syncthreads_or(!landed)) {
             if (tid == 0) atomicOr(status, kLaneStatusTimeout);
             return;
         }
+        const int4 un = unit[b];
+        if (un.x < 0) break;
         const int i = un.x, g = un.y, c = un.z, p = un.w;
         const int t0 = c * 32, nt = min(32, p + 1 - t0);
         const float *Kb = abuf + (size_t)b * 2 * CH, *Vb = Kb + CH;
@@ -348,6 +358,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (lane < GRP) sc[hk][t] = (t < nt) ? __fdiv_rn(sv, div) : 0.0f;  // lanes 0 .. GRP-1 hold every head once
         }
         __syncthreads();
+        if (warp == kIssWarp) nx = advance();  // meanwhile: the unit for buffer b after this one
         if (warp < grp) {  // softmax of head `warp` over the chunk
             const int h = warp, t = lane;
             const float m = warp_max(t < nt ? sc[h][t] : -__int_as_float(0x7f800000));
@@ -399,12 +410,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (two) w.U[((int64_t)(g * grp + h1) * ncmax + c) * HD + d] = sb[5];
             }
         }
-        __syncthreads();  // buffer b and sc are free again
-        const int4 nx = advance();
-#pragma unroll
-        for (int j = 0; j < kAttnBufs; j++)
-            if (j == b) slot[j] = nx;
-        if (nx.x >= 0) issue(nx, b);
+        __syncthreads();  // buffer b, unit[b] and sc are free again
+        if (warp == kIssWarp) publish(nx, b);
     }
 }
 
