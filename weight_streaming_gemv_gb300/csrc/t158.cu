@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(256) t158_gemv_kernel(const int8_t *__restrict
 #pragma unroll
             for (int r = 0; r < R; r++) {
                 const int64_t row = r0 + r * RPS + rsub;
+                // the chunk two iterations ahead toward L2 (more bytes in flight per warp)
+                if (row < N && c + 2 * LPR < C)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(w + row * pitch + (int64_t)(c + 2 * LPR) * 16));
                 wv[r] = (row < N) ? ld_stream_v4(w + row * pitch + (int64_t)c * 16) : make_uint4(0, 0, 0, 0);
             }
             uint32_t D[R][4][5];
