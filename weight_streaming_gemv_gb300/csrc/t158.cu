@@ -11,6 +11,8 @@
 // reordered once per block into matching planes, so every plane is one
 // __dp4a operand.  Digits are unsigned (d = trit + 1); the row result is
 // sum(d * x) - sum(x).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace qlin {
@@ -121,8 +123,8 @@ __global__ void __launch_bounds__(256) t158_gemv_kernel(const int8_t *__restrict
 #pragma unroll
             for (int r = 0; r < R; r++) {
                 const int64_t row = r0 + r * RPS + rsub;
-                // the chunk two iterations ahead toward L2 (more bytes in flight per warp)
-                if (row < N && c + 2 * LPR < C)
+                // wide rows: the chunk two iterations ahead toward L2 (more bytes in flight per warp)
+                if (LPR == 32 && row < N && c + 2 * LPR < C)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(w + row * pitch + (int64_t)(c + 2 * LPR) * 16));
                 wv[r] = (row < N) ? ld_stream_v4(w + row * pitch + (int64_t)c * 16) : make_uint4(0, 0, 0, 0);
             }
@@ -195,7 +197,9 @@ static qlin_status launch_t158(const int8_t *xq, const float *xs, const uint8_t 
     constexpr int ROWS = (32 / LPR) * R;
     const int64_t warps_needed = (N + ROWS - 1) / ROWS;
     int64_t blocks = (warps_needed + 7) / 8;
-    const int64_t cap = (int64_t)sm_count() * per_sm;
+    // each block builds the activation planes once: at most two blocks per SM,
+    // so that they serve more rows each (the grid-stride loop takes the rest)
+    const int64_t cap = (int64_t)sm_count() * std::min(per_sm, 2);
     if (blocks > cap) blocks = cap;
     dim3 grid((unsigned)blocks, (unsigned)((M + MT - 1) / MT));
     kern<<<grid, 256, smem, st>>>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K);
