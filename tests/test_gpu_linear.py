@@ -214,7 +214,7 @@ def test_t158_tensor_core_tiles(dev, M, K, N):
 @pytest.mark.parametrize("M,K,N", [(257, 333, 200), (4096, 160, 129), (40, 6912, 1152), (200, 1152, 140),
                                    (64, 1152, 6912), (480, 240, 384)])
 def test_t158_tensor_core_token_tiles(dev, M, K, N):
-    # token tiles of 32..256 (the MMA's N), one or several per call, with and
+    # token tiles of 32..128 (the MMA's N), one or several per call, with and
     # without split K, against the oracle bit for bit
     _t158_case(dev, M, K, N, seed=13)
 

@@ -9,7 +9,8 @@
 // addition is exact and the accumulator equals the int32 sum.
 //
 // One CTA computes 128 weight rows x T tokens (T a multiple of 32, at most
-// 256) with tcgen05.mma (M = 128 weight rows, N = T tokens, K = 16 per
+// 128, so that two CTAs share an SM's tensor memory and one's output write
+// overlaps the other's products) with tcgen05.mma (M = 128 weight rows, N = T tokens, K = 16 per
 // instruction) into T fp32 accumulator columns of tensor memory.  K advances in
 // steps of 80 elements: 16 packed bytes of every weight row.  Within a step
 // both operands use the same permuted K order, K' = 16 i + j for element
@@ -52,7 +53,7 @@
 namespace qlin {
 
 constexpr int kTmRows = 128;              // weight rows per CTA (MMA M, tensor-memory lanes)
-constexpr int kTmMaxTok = 256;            // tokens per CTA at most (MMA N)
+constexpr int kTmMaxTok = 128;            // tokens per CTA at most (MMA N)
 constexpr int kTcKS = 80;                 // K elements per step (16 packed bytes)
 constexpr int kTcChunks = kTcKS / 8;      // 16-byte core-matrix columns per row and step
 constexpr int kTcSBO = kTcChunks * 128;   // bytes between 8-row groups of the activation tile
@@ -69,7 +70,7 @@ constexpr int kTmMaxSplit = 8;            // CTAs of a cluster that split K
 // t158_act_tiles_kernel into a workspace, one bulk copy per stage; else
 // converted by the converter warps from the int8 codes at every step.
 // Stages (operand tiles) and raw stages (copies ahead) of each:
-__host__ __device__ constexpr int tm_stages(bool pre) { return pre ? 4 : 3; }
+__host__ __device__ constexpr int tm_stages(bool) { return 3; }
 __host__ __device__ constexpr int tm_raws(bool pre) { return pre ? 4 : 3; }
 
 struct TmCtl {
