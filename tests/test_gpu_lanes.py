@@ -2,7 +2,8 @@
 against the oracle's lane step: next tokens equal (or in a near tie of the
 oracle's fp64 logits), logits within max-abs-rel 2e-3, every KV cache bit for
 bit.  Lanes of separate sequences, a prompt chunk listed out of order, one
-lane (CUDA-core linears) and 2 or more (tensor cores), the
+lane (CUDA-core linears) and 2 or more (tensor cores), attention shapes
+(head_dim 64 and 128; 1, 2 and 8 query heads per KV head; two KV heads), the
 Gemma-3-1B-shaped decoder at context 1024 with 16 users, and bad lanes.
 """
 import numpy as np
@@ -69,6 +70,31 @@ def test_tiny_lanes_batches_and_prompt_chunks(dev):
     toks = [30, 31, 32, 33]
     for s in range(4):
         nx = _lane_step(gpu, orc, kvs_o, toks, [2 + s, 2 + s, 11 + s, 9 + s], [0, 1, 2, 3], logit_check=(s == 3))
+        toks = [int(t) for t in nx]
+    np.testing.assert_array_equal(host(gpu.kv_lanes), kvs_o)
+
+
+@pytest.mark.parametrize("shape", [
+    # 8 query heads per KV head, head_dim 64
+    dict(n_layers=2, dim=128, n_heads=8, n_kv_heads=1, head_dim=64, ffn=192, vocab=512, eps=1e-6, rope_base=10000.0),
+    # 2 KV heads (rows of a chunk are not contiguous: one copy per row), 2 query heads each, head_dim 128
+    dict(n_layers=2, dim=128, n_heads=4, n_kv_heads=2, head_dim=128, ffn=160, vocab=512, eps=1e-6, rope_base=10000.0),
+    # one query head per KV head
+    dict(n_layers=1, dim=64, n_heads=2, n_kv_heads=2, head_dim=64, ffn=96, vocab=300, eps=1e-6, rope_base=10000.0),
+])
+def test_lanes_attention_shapes(dev, shape):
+    # the persistent attention kernel's other head widths and groupings, a prompt
+    # chunk across two 32-position chunks, lanes of three sequences at mixed positions
+    cfg = synth.DecoderConfig(max_pos=100, **shape)
+    gpu, orc = _pair(cfg, 6, dev)
+    gpu.prepare_lanes(n_seqs=3, max_lanes=40)
+    kvs_o = np.zeros((3, cfg.n_layers, 2, cfg.max_pos, cfg.kv_dim), np.float32)
+    prompt = synth.prompt_ids(10, 40, cfg.vocab)
+    _lane_step(gpu, orc, kvs_o, prompt[:37], np.arange(37), [0] * 37)
+    _lane_step(gpu, orc, kvs_o, prompt[37:40], [37, 0, 0], [0, 1, 2])
+    toks = [5, 6, 7]
+    for s in range(3):
+        nx = _lane_step(gpu, orc, kvs_o, toks, [38 + s, 1 + s, 1 + s], [0, 1, 2], logit_check=(s == 2))
         toks = [int(t) for t in nx]
     np.testing.assert_array_equal(host(gpu.kv_lanes), kvs_o)
 
