@@ -385,7 +385,7 @@ def lanes_decode(gpu, cfg, stream, single_tok_s):
     = U / step time, against the single-user fused step."""
     import torch
 
-    users = (1, 2, 4, 8, 16, 32, 64)
+    users = (1, 2, 4, 8, 16, 32, 64, 128, 256)
     U_MAX = users[-1]
     gpu.prepare_lanes(n_seqs=U_MAX, max_lanes=U_MAX)
     kv0 = gpu.kv[:, :, :, :].clone()  # the bench's cache: filled to 1024 by the decode run
