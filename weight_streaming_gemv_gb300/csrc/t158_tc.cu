@@ -334,6 +334,51 @@ __global__ void __launch_bounds__(256) t158_act_tiles_kernel(const int8_t *__res
     tm_put_row(out + ((int64_t)tt * nsteps + s) * tm_b_bytes(T), in, r);
 }
 
+// rmsnorm_row (decode_ops.cuh) for a whole block, the same sums: the squares'
+// pairwise tree over next_pow2(n) zero-padded leaves, each of the T threads
+// (T the largest power of two in the block) first reducing its segment of
+// P / T adjacent leaves, then lanes, then warps adjacent first.  The warps'
+// partials are reduced by one warp's butterfly instead of a serial loop (zero
+// padding past the last warp adds exactly nothing, so the tree is the same).
+// buf: shared memory >= next_pow2(n) floats, red: >= 32 floats.
+__device__ __forceinline__ void qt_rmsnorm(const float *x, const float *g, float *out, int n, float eps, float *buf,
+                                           float *red) {
+    const int P = next_pow2(n), tid = threadIdx.x, nth = blockDim.x;
+    for (int i = tid; i < P; i += nth) {
+        const float v = (i < n) ? x[i] : 0.0f;
+        buf[i] = __fmul_rn(v, v);
+    }
+    int T = 32;
+    while (2 * T <= nth) T *= 2;
+    __syncthreads();
+    float v = 0.0f;
+    if (tid < T) {
+        if (P >= T) {
+            const int S = P / T;
+            float *a = buf + tid * S;
+            for (int st = 1; st < S; st <<= 1)
+                for (int i = 0; i < S; i += 2 * st) a[i] = __fadd_rn(a[i], a[i + st]);
+            v = a[0];
+        } else {
+            v = (tid < P) ? buf[tid] : 0.0f;
+        }
+    }
+    v = warp_psum(v);
+    if ((tid & 31) == 0 && tid < T) red[tid >> 5] = v;
+    __syncthreads();
+    if (tid < 32) {
+        float w = tid < (T >> 5) ? red[tid] : 0.0f;
+        w = warp_psum(w);
+        if (tid == 0) red[0] = w;
+    }
+    __syncthreads();
+    float ss = red[0];
+    ss = __fdiv_rn(ss, (float)n);
+    ss = __fadd_rn(ss, eps);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(ss));
+    for (int i = tid; i < n; i += nth) out[i] = __fmul_rn(g[i], __fmul_rn(r, x[i]));
+}
+
 // Where the row a quantiser block quantises comes from.
 enum QtMode : int {
     kQtRow = 0,   // x[m] as it is
@@ -384,8 +429,8 @@ __global__ void __launch_bounds__(kQtThreads) t158_quant_tiles_kernel(QtArgs a) 
                 const float *yr = a.y + (int64_t)m * K;
                 for (int k = threadIdx.x; k < K; k += blockDim.x) hr[k] = __fadd_rn(hr[k], yr[k]);
             }
-            // each thread reads back only the elements it wrote; rmsnorm_row syncs before the sum
-            rmsnorm_row(hr, a.g, qt_row, K, a.eps, qt_row + K, red, whole_block());
+            // each thread reads back only the elements it wrote; the norm syncs before the sum
+            qt_rmsnorm(hr, a.g, qt_row, K, a.eps, qt_row + K, red);
             __syncthreads();
             row = qt_row;
         }
