@@ -429,6 +429,39 @@ __global__ void __launch_bounds__(256) lanes_attn_merge_kernel(const float *ws, 
                     out + ((int64_t)i * nh + h) * hd, wbuf, red, whole_block());
 }
 
+// block_psum (decode_ops.cuh) for a whole block, the same tree: each of the T
+// threads (T the largest power of two in the block) reduces its segment of
+// P / T adjacent terms, then lanes, then warps adjacent first; the warps'
+// partials by one warp's butterfly (zero padding adds exactly nothing).
+__device__ __forceinline__ float merge_psum(float *buf, int P, float *red) {
+    const int tid = threadIdx.x;
+    int T = 32;
+    while (2 * T <= (int)blockDim.x) T *= 2;
+    __syncthreads();
+    float v = 0.0f;
+    if (tid < T) {
+        if (P >= T) {
+            const int S = P / T;
+            float *a = buf + tid * S;
+            for (int st = 1; st < S; st <<= 1)
+                for (int i = 0; i < S; i += 2 * st) a[i] = __fadd_rn(a[i], a[i + st]);
+            v = a[0];
+        } else {
+            v = (tid < P) ? buf[tid] : 0.0f;
+        }
+    }
+    v = warp_psum(v);
+    if ((tid & 31) == 0 && tid < T) red[tid >> 5] = v;
+    __syncthreads();
+    if (tid < 32) {
+        float w = tid < (T >> 5) ? red[tid] : 0.0f;
+        w = warp_psum(w);
+        if (tid == 0) red[0] = w;
+    }
+    __syncthreads();
+    return red[0];
+}
+
 // grid (nh, lanes): lanes_attn_merge_kernel with the lane's partials of head h
 // staged in shared memory first (4-byte asynchronous copies, all in flight
 // together), then the same maximum, weights, pairwise sums and division.
@@ -466,8 +499,10 @@ __global__ void __launch_bounds__(256) lanes_attn_merge_smem_kernel(const float 
     }
     lanes_cp_wait_all();
     __syncthreads();
-    float m = Mc[0];
-    for (int c = 1; c < nc; c++) m = fmaxf(m, Mc[c]);
+    // the largest chunk maximum (exact in any order): lane-strided, then across the warp
+    float m = -__int_as_float(0x7f800000);
+    for (int c = threadIdx.x & 31; c < nc; c += 32) m = fmaxf(m, Mc[c]);
+    m = warp_max(m);
     for (int c = threadIdx.x; c < P; c += blockDim.x) wb[c] = (c < nc) ? exp32(__fsub_rn(Mc[c], m)) : 0.0f;
     __syncthreads();
     for (int d = threadIdx.x; d < hd; d += blockDim.x) {
@@ -477,7 +512,7 @@ __global__ void __launch_bounds__(256) lanes_attn_merge_smem_kernel(const float 
     }
     __syncthreads();
     for (int c = threadIdx.x; c < P; c += blockDim.x) wb[c] = (c < nc) ? __fmul_rn(Sc[c], wb[c]) : 0.0f;
-    const float S = block_psum(wb, P, red, whole_block());
+    const float S = merge_psum(wb, P, red);
     for (int d = threadIdx.x; d < hd; d += blockDim.x) out[((int64_t)i * nh + h) * hd + d] = __fdiv_rn(o[d], S);
 }
 
