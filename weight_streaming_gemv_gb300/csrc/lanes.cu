@@ -30,7 +30,6 @@ namespace qlin {
 qlin_status t158_linear_dev_scale(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch,
                                   const float *ws_ptr, float *y, int M, int N, int K, cudaStream_t st, void *work,
                                   bool convert);
-size_t t158_workspace_bytes(int M, int K);
 size_t t158_tc_workspace_bytes(int M, int K);
 qlin_status quant_i8_tiles(const float *x, int8_t *xq, float *xs, int M, int K, void *work, cudaStream_t st);
 qlin_status t158_linear_tiles_multi(const float *xs, int count, const uint8_t *const *w, const int64_t *pitch,
@@ -641,12 +640,13 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     for (int j = 0; j < T158_NMAT; j++) W[j] = m->w[j];
     const int rows[T158_NMAT] = {qd, kvd, kvd, d, f, f, d};
     const int cols[T158_NMAT] = {d, d, d, qd, d, d, f};
-    // linear j of layer l on the quantised activations in w.xq / w.xs (and,
-    // on the tensor-core path, the tiles the quantiser wrote into w.tiles)
-    auto lin = [&](int l, int j, float *out, bool convert) -> qlin_status {
+    // linear j of layer l on the quantised activations in w.xq / w.xs (one
+    // lane: the CUDA-core kernels; from kLanesTensorMin lanes lin_group below
+    // takes the tensor cores on the tiles the quantisers wrote)
+    auto lin = [&](int l, int j, float *out) -> qlin_status {
         return t158_linear_dev_scale(w.xq, w.xs, W[j] + (int64_t)l * rows[j] * m->pitch[j], m->pitch[j],
-                                     m->scales + (int64_t)l * T158_NMAT + j, out, M, rows[j], cols[j], s, w.tiles,
-                                     convert);
+                                     m->scales + (int64_t)l * T158_NMAT + j, out, M, rows[j], cols[j], s, nullptr,
+                                     false);
     };
     // the quantisers write the tensor-core tiles when the linears take that path
     // (and then no int8 codes: nothing reads them), else the codes
@@ -656,7 +656,7 @@ qlin_status decode_lanes_t158(const t158_model *m, float *kv_caches, int n_seqs,
     auto lin_group = [&](int l, int j0, int n, float *const *out) -> qlin_status {
         if (!tiles) {
             for (int k = 0; k < n; k++)
-                if (qlin_status e = lin(l, j0 + k, out[k], false)) return e;
+                if (qlin_status e = lin(l, j0 + k, out[k])) return e;
             return QLIN_OK;
         }
         const uint8_t *wj[3];
