@@ -4,6 +4,8 @@
 // output rows).  Weights stream with 16-byte loads; each int8 is widened to
 // fp32 exactly with the 2^23 magic-number trick (one byte permute and one
 // subtraction) and accumulated with fp32 FMA.
+#include <algorithm>
+
 #include "common.cuh"
 #include "stream.cuh"
 
@@ -494,9 +496,9 @@ qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float
     if (M == 1 && w_pitch <= 16 * 32 * qlin::kW8Warps * qlin::kW8JMax) {
         const qlin::W8Smem L = qlin::w8_stream_layout(w_pitch, qlin::max_smem_optin());
         if (L.tr >= 1) {
-            qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel<false>, L.total);  // raises the dynamic smem limit
+            const int per_sm = qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel<false>, L.total);
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)qlin::sm_count());
+            cfg.gridDim = dim3((unsigned)(qlin::sm_count() * std::min(per_sm, 2)));
             cfg.blockDim = dim3(32 * (qlin::kW8Warps + 1));
             cfg.dynamicSmemBytes = (size_t)L.total;
             cfg.stream = st;
@@ -552,9 +554,9 @@ qlin_status qlin_w8g_f32(const float *x, const int8_t *w8, int64_t w_pitch, cons
     if (M == 1 && w_pitch <= 16 * 32 * qlin::kW8Warps * qlin::kW8JMax) {
         const qlin::W8Smem L = qlin::w8_stream_layout(w_pitch, qlin::max_smem_optin(), s_pitch);
         if (L.tr >= 1) {
-            qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel<true>, L.total);  // raises the dynamic smem limit
+            const int per_sm = qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel<true>, L.total);
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)qlin::sm_count());
+            cfg.gridDim = dim3((unsigned)(qlin::sm_count() * std::min(per_sm, 2)));
             cfg.blockDim = dim3(32 * (qlin::kW8Warps + 1));
             cfg.dynamicSmemBytes = (size_t)L.total;
             cfg.stream = st;
