@@ -46,7 +46,8 @@ def parse():
     p.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
     p.add_argument("--workload", choices=["decode"], default="decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--kernel", choices=["sketch_head", "decode_steps", "lanes_steps", "t158_linears", "t158_calls"],
+    p.add_argument("--kernel", choices=["sketch_head", "decode_steps", "lanes_steps", "t158_linears", "t158_calls",
+                                        "t158_gemv"],
                    default=None,
                    help="time one kernel alone on its full-size synthetic inputs (for profiling); no JSON bench line")
     return p.parse_args()
@@ -713,6 +714,22 @@ def kernel_only(name):
         stream = torch.cuda.current_stream(dev)
         print(json.dumps({"kernel": name, "prefill_m512": prefill_m512(dev, stream),
                           "lanes_t158": lanes_t158(dev, stream)}))
+        return 0
+    if name == "t158_gemv":
+        # five plain M=1 calls of qlin_t158_i8 per shape (1152->6912, 6912->1152, 16384->16384, in that
+        # order), each shape after one quantiser launch: a short launch list for the profiler
+        for K, N in [(1152, 6912), (6912, 1152), (16384, 16384)]:
+            d = synth.t158_gemv(3, 1, K, N)
+            pitch = qlin.t158_pitch(K)
+            w = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+            xq = torch.empty((1, K), dtype=torch.int8, device=dev)
+            xs = torch.empty(1, dtype=torch.float32, device=dev)
+            qlin.qlin_quant_i8(torch.from_numpy(d["x"]).to(dev), xq, xs, 1, K)
+            y = torch.empty((1, N), dtype=torch.float32, device=dev)
+            for _ in range(5):
+                qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, 1, N, K)
+        torch.cuda.synchronize()
+        print(json.dumps({"kernel": name}))
         return 0
     if name == "t158_calls":
         # five plain calls of qlin_t158_i8_ws per shape (512 and 64 tokens through 1152->6912 and

@@ -186,6 +186,13 @@ def test_t158_ragged_shapes(dev, M, K, N):
     _t158_case(dev, M, K, N, seed=M * 1000 + K)
 
 
+@pytest.mark.parametrize("K,N", [(2051, 16001), (1999, 3001), (1100, 9800), (333, 9800), (77, 20000)])
+def test_t158_m1_row_slot_variants(dev, K, N):
+    # one token through the CUDA-core kernel at row counts that select 4, 2 and 1 row slots per warp
+    # for each chunk width on a 152-SM GPU; 2051 x 16001 also takes a second grid-stride pass
+    _t158_case(dev, 1, K, N, seed=K + N)
+
+
 def test_t158_adversarial_extremes(dev):
     # all +1 trits against all +127 activations: acc = 127 K at K = 6912, the largest in use
     K, N = 6912, 64

@@ -44,41 +44,68 @@ __global__ void __launch_bounds__(256) quant_i8_kernel(const float *__restrict__
 // ---------------------------------------------------------------- activation planes
 // xr[c*5 + i] (uint4) holds, in word w / byte b, the activation of trit
 // 5*(16c + 4w + b) + i: digit i of byte 4w + b of chunk c.  Zero past K.
-__device__ __forceinline__ void build_planes(const int8_t *__restrict__ x, int K, int C, uint4 *xr) {
-    uint32_t *xw = reinterpret_cast<uint32_t *>(xr);
-    const int nwords = C * 20;
-    for (int idx = threadIdx.x; idx < nwords; idx += blockDim.x) {
-        const int c = idx / 20, r = idx % 20, i = r / 4, w = r % 4;
-        const int byte0 = 16 * c + 4 * w;
-        uint32_t v = 0;
-#pragma unroll
-        for (int b = 0; b < 4; b++) {
-            const int k = 5 * (byte0 + b) + i;
-            const uint32_t xb = (k < K) ? (uint32_t)(uint8_t)x[k] : 0u;
-            v |= xb << (8 * b);
-        }
-        xw[idx] = v;
-    }
+//
+// The planes are built from a copy of the row in shared memory: the row is
+// fetched with 16-byte loads (the bytes before the first and after the last
+// 16-byte boundary one by one), so a block pays one L2 round trip for it.
+// stage[off0 + k] = x[k] for k < K and 0 up to 80*C, where off0 = x mod 16
+// keeps the 16-byte stores aligned; stage holds 80*C + 32 bytes.
+__device__ __forceinline__ void stage_row(const int8_t *__restrict__ x, int K, int C, uint8_t *stage) {
+    const int off0 = (int)((uintptr_t)x & 15);
+    const uint8_t *base = reinterpret_cast<const uint8_t *>(x) - off0;  // 16-byte aligned
+    const int j0 = off0 ? 1 : 0;            // first 16-byte block lying wholly inside the row
+    const int j1 = max((off0 + K) >> 4, j0);  // one past the last such block
+    for (int j = j0 + (int)threadIdx.x; j < j1; j += blockDim.x)
+        reinterpret_cast<uint4 *>(stage)[j] = ld_stream_v4(base + 16 * (size_t)j);
+    const int head = min(K, 16 * j0 - off0);  // bytes k < head precede the blocks
+    const int tail = max(16 * j1 - off0, head);  // bytes k >= tail follow them
+    for (int k = threadIdx.x; k < head; k += blockDim.x) stage[off0 + k] = (uint8_t)x[k];
+    for (int k = tail + (int)threadIdx.x; k < K; k += blockDim.x) stage[off0 + k] = (uint8_t)x[k];
+    for (int k = K + (int)threadIdx.x; k < 80 * C; k += blockDim.x) stage[off0 + k] = 0;
 }
 
-// Row sum of the int8 activations (exact).
-__device__ __forceinline__ int block_isum(const int8_t *__restrict__ x, int K, int *red) {
-    int s = 0;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) s += x[k];
+// One span is the 20 activations of the four packed bytes 4w..4w+3 of chunk c
+// (s = 4c + w); plane i of the span takes its bytes i, i+5, i+10, i+15.
+// Returns this thread's part of the row's byte sum (exact, signed).
+__device__ __forceinline__ int planes_from_stage(const uint8_t *stage, int off0, int C, uint4 *xr) {
+    uint32_t *xw = reinterpret_cast<uint32_t *>(xr);
+    const uint32_t *sw = reinterpret_cast<const uint32_t *>(stage);
+    const uint32_t sh = 8u * (uint32_t)(off0 & 3);
+    int sum = 0;
+    for (int sp = threadIdx.x; sp < 4 * C; sp += blockDim.x) {
+        const int b0 = off0 + 20 * sp;  // stage index of the span's first byte
+        const int q = b0 >> 2;
+        uint32_t u[6], v[5];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
-    __syncthreads();
-    int t = 0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); i++) t += red[i];
-    __syncthreads();
-    return t;
+        for (int t = 0; t < 6; t++) u[t] = sw[q + t];
+#pragma unroll
+        for (int t = 0; t < 5; t++) v[t] = __funnelshift_r(u[t], u[t + 1], sh);  // bytes 4t..4t+3 of the span
+        // plane i = span bytes {i, i+5, i+10, i+15}
+        const uint32_t p0 = __byte_perm(__byte_perm(v[0], v[1], 0x0050), __byte_perm(v[2], v[3], 0x0072), 0x5410);
+        const uint32_t p1 = __byte_perm(__byte_perm(v[0], v[1], 0x0061), __byte_perm(v[2], v[4], 0x0043), 0x5410);
+        const uint32_t p2 = __byte_perm(__byte_perm(v[0], v[1], 0x0072), __byte_perm(v[3], v[4], 0x0050), 0x5410);
+        const uint32_t p3 = __byte_perm(__byte_perm(v[0], v[2], 0x0043), __byte_perm(v[3], v[4], 0x0061), 0x5410);
+        const uint32_t p4 = __byte_perm(__byte_perm(v[1], v[2], 0x0050), __byte_perm(v[3], v[4], 0x0072), 0x5410);
+        const int c = sp >> 2, w = sp & 3;
+        uint32_t *o = xw + (size_t)c * 20 + w;
+        o[0] = p0;
+        o[4] = p1;
+        o[8] = p2;
+        o[12] = p3;
+        o[16] = p4;
+#pragma unroll
+        for (int t = 0; t < 5; t++) sum = dp4a(v[t], 0x01010101u, sum);
+    }
+    return sum;
 }
 
 // ---------------------------------------------------------------- S4 / S6 GEMV
 // LPR lanes share one packed row (chunk c = lane % LPR + LPR*j); 32/LPR rows
 // per slot, R slots per warp pass.  MT tokens per block (grid.y tiles M).
+// The weight chunks are double-buffered in registers: the next chunk's loads
+// are in flight while the current one is decoded, and the first chunk of a
+// warp's first rows is requested before the activation planes are built, so
+// that its DRAM latency overlaps the plane build.
 template <int LPR, int R, int MT>
 __global__ void __launch_bounds__(256) t158_gemv_kernel(const int8_t *__restrict__ xq, const float *__restrict__ xs,
                                                         const uint8_t *__restrict__ w, int64_t pitch, float ws,
@@ -86,30 +113,51 @@ __global__ void __launch_bounds__(256) t158_gemv_kernel(const int8_t *__restrict
                                                         int M, int N, int K) {
     extern __shared__ uint4 smem[];
     const int C = (int)(pitch / 16);
-    uint4 *xr = smem;                                            // [MT][C*5]
-    int *sumx = reinterpret_cast<int *>(smem + (size_t)MT * C * 5);  // [MT] then 32 scratch
+    uint4 *xr = smem;                                                    // [MT][C*5]
+    uint8_t *stage = reinterpret_cast<uint8_t *>(smem + (size_t)MT * C * 5);  // 80*C + 32 bytes
+    int *sumx = reinterpret_cast<int *>(stage + 80 * (size_t)C + 32);     // [MT]
+    int *red = sumx + MT;                                                // [MT][8] warp partial sums
     const int m0 = blockIdx.y * MT;
-    const float wsv = ws_ptr ? *ws_ptr : ws;
-    for (int mm = 0; mm < MT; mm++) {
-        const int m = m0 + mm;
-        if (m < M) {
-            build_planes(xq + (int64_t)m * K, K, C, xr + (size_t)mm * C * 5);
-            const int s = block_isum(xq + (int64_t)m * K, K, sumx + MT);
-            if (threadIdx.x == 0) sumx[mm] = s;
-        } else {
-            for (int idx = threadIdx.x; idx < C * 5; idx += blockDim.x) xr[(size_t)mm * C * 5 + idx] = make_uint4(0, 0, 0, 0);
-            if (threadIdx.x == 0) sumx[mm] = 0;
-        }
-    }
-    __syncthreads();
 
     constexpr int RPS = 32 / LPR;
+    constexpr int ROWS = RPS * R;
     const int lane = threadIdx.x & 31;
     const int sub = lane % LPR, rsub = lane / LPR;
     const int warps = blockDim.x >> 5;
     const int64_t gwarp = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * warps;
-    constexpr int ROWS = RPS * R;
+    uint4 nxt[R];  // the next chunk of each of the warp's R row slots
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        const int64_t row = gwarp * ROWS + r * RPS + rsub;
+        nxt[r] = (row < N && sub < C) ? ld_stream_v4(w + row * pitch + (int64_t)sub * 16) : make_uint4(0, 0, 0, 0);
+    }
+
+    const float wsv = ws_ptr ? *ws_ptr : ws;
+    for (int mm = 0; mm < MT; mm++) {
+        const int m = m0 + mm;
+        int part = 0;
+        if (m < M) {
+            const int8_t *xrow = xq + (int64_t)m * K;
+            if (mm > 0) __syncthreads();  // the previous token's planes have been read from the stage
+            stage_row(xrow, K, C, stage);
+            __syncthreads();
+            part = planes_from_stage(stage, (int)((uintptr_t)xrow & 15), C, xr + (size_t)mm * C * 5);
+        } else {
+            for (int idx = threadIdx.x; idx < C * 5; idx += blockDim.x) xr[(size_t)mm * C * 5 + idx] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) red[mm * 8 + (threadIdx.x >> 5)] = part;
+    }
+    __syncthreads();
+    if (threadIdx.x < MT) {
+        int t = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) t += red[threadIdx.x * 8 + i];
+        sumx[threadIdx.x] = t;
+    }
+    __syncthreads();
 
     for (int64_t r0 = gwarp * ROWS; r0 < N; r0 += nwarps * ROWS) {
         int acc[R][MT];
@@ -117,6 +165,13 @@ __global__ void __launch_bounds__(256) t158_gemv_kernel(const int8_t *__restrict
         for (int r = 0; r < R; r++)
 #pragma unroll
             for (int mm = 0; mm < MT; mm++) acc[r][mm] = 0;
+        if (r0 != gwarp * ROWS) {
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                const int64_t row = r0 + r * RPS + rsub;
+                nxt[r] = (row < N && sub < C) ? ld_stream_v4(w + row * pitch + (int64_t)sub * 16) : make_uint4(0, 0, 0, 0);
+            }
+        }
 
         for (int c = sub; c < C; c += LPR) {
             uint4 wv[R];
@@ -126,7 +181,9 @@ __global__ void __launch_bounds__(256) t158_gemv_kernel(const int8_t *__restrict
                 // wide rows: the chunk two iterations ahead toward L2 (more bytes in flight per warp)
                 if (LPR == 32 && row < N && c + 2 * LPR < C)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(w + row * pitch + (int64_t)(c + 2 * LPR) * 16));
-                wv[r] = (row < N) ? ld_stream_v4(w + row * pitch + (int64_t)c * 16) : make_uint4(0, 0, 0, 0);
+                wv[r] = nxt[r];
+                nxt[r] = (row < N && c + LPR < C) ? ld_stream_v4(w + row * pitch + (int64_t)(c + LPR) * 16)
+                                                  : make_uint4(0, 0, 0, 0);
             }
             uint32_t D[R][4][5];
 #pragma unroll
@@ -190,16 +247,17 @@ static qlin_status launch_t158(const int8_t *xq, const float *xs, const uint8_t 
                                const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st) {
     auto kern = t158_gemv_kernel<LPR, R, MT>;
     const int C = (int)(pitch / 16);
-    const size_t smem = (size_t)MT * C * 5 * sizeof(uint4) + (MT + 32) * sizeof(int);
+    const size_t smem = (size_t)MT * C * 5 * sizeof(uint4) + 80 * (size_t)C + 32 + (size_t)MT * 9 * sizeof(int);
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "qlin_t158_i8: K=%d needs %zu B of shared memory",
                  K, smem);
     const int per_sm = blocks_per_sm((const void *)kern, smem);
     constexpr int ROWS = (32 / LPR) * R;
     const int64_t warps_needed = (N + ROWS - 1) / ROWS;
     int64_t blocks = (warps_needed + 7) / 8;
-    // each block builds the activation planes once: at most two blocks per SM,
-    // so that they serve more rows each (the grid-stride loop takes the rest)
-    const int64_t cap = (int64_t)sm_count() * std::min(per_sm, 2);
+    // each block builds the activation planes once: at most three blocks per
+    // SM for one token (two for several), so that they serve more rows each
+    // (the grid-stride loop takes the rest)
+    const int64_t cap = (int64_t)sm_count() * std::min(per_sm, MT == 1 ? 3 : 2);
     if (blocks > cap) blocks = cap;
     dim3 grid((unsigned)blocks, (unsigned)((M + MT - 1) / MT));
     kern<<<grid, 256, smem, st>>>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K);
@@ -210,7 +268,13 @@ static qlin_status launch_t158(const int8_t *xq, const float *xs, const uint8_t 
 template <int LPR>
 static qlin_status dispatch_mt(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
                                const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st) {
-    if (M == 1) return launch_t158<LPR, 4, 1>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+    if (M == 1) {
+        // row slots per warp: the most that still give every SM a block
+        const int64_t blocks_r1 = ((int64_t)N + (32 / LPR) * 8 - 1) / ((32 / LPR) * 8);
+        if (blocks_r1 >= 4LL * sm_count()) return launch_t158<LPR, 4, 1>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+        if (blocks_r1 >= 2LL * sm_count()) return launch_t158<LPR, 2, 1>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+        return launch_t158<LPR, 1, 1>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+    }
     if (M == 2) return launch_t158<LPR, 4, 2>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
     if (M <= 4) return launch_t158<LPR, 2, 4>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
     if (M <= 8) return launch_t158<LPR, 2, 8>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
