@@ -6,9 +6,10 @@
 // one byte holding the four trits t[n][4g .. 4g+3] in base 3, and a group's
 // bytes for all rows are contiguous.  Every CTA lists the token's nonzero
 // groups (a ballot over the int8 codes), then takes its share of that list
-// for its 1024 rows: per group one 32-bit load gives four rows' bytes, a
-// shared-memory table turns a byte into its four trits (int8 x 4) and one
-// dp4a with the group's four codes adds the group to a row.  A zero group's
+// for its 1024 rows: per group one 32-bit load gives four rows' bytes (the
+// loads of 32 groups in flight per thread), a shared-memory table turns a
+// byte into its four trits (int8 x 4) and one dp4a with the group's four
+// codes adds the group to a row.  A zero group's
 // weight bytes are never read.  Partial sums go to the workspace per group
 // share; the last CTA of a row block adds them in share order (integers:
 // exact) and writes acc and y = ((float)acc * w_scale) * x_scale.
@@ -24,8 +25,10 @@ constexpr int kSkThreads = 256;
 constexpr int kSkRows = 4 * kSkThreads;  // rows per CTA: four per thread
 constexpr int kSkMaxGroups = 16384;      // K <= 65536
 constexpr int kSkMaxShares = 16;
+constexpr int kSkBatch = 32;             // weight loads in flight per thread
+constexpr int kSkListLoads = 16;         // code words per thread and round of the list (4096 groups)
 
-__global__ void __launch_bounds__(kSkThreads) t158_skip_kernel(const int8_t *__restrict__ xq,
+__global__ void __launch_bounds__(kSkThreads, 2) t158_skip_kernel(const int8_t *__restrict__ xq,
                                                               const float *__restrict__ xs,
                                                               const uint8_t *__restrict__ wg, int64_t gpitch,
                                                               float w_scale, int N, int K, int32_t *part,
@@ -50,10 +53,10 @@ __global__ void __launch_bounds__(kSkThreads) t158_skip_kernel(const int8_t *__r
     __shared__ unsigned wsum[kSkThreads / 32 + 1];
     const int lane = tid & 31, warp = tid >> 5;
     unsigned base = 0;
-    for (int g0 = 0; g0 < G; g0 += 8 * kSkThreads) {
-        uint32_t x4[8];
+    for (int g0 = 0; g0 < G; g0 += kSkListLoads * kSkThreads) {
+        uint32_t x4[kSkListLoads];
 #pragma unroll
-        for (int u = 0; u < 8; u++) {  // every load of the round in flight
+        for (int u = 0; u < kSkListLoads; u++) {  // every load of the round in flight
             const int g = g0 + u * kSkThreads + tid;
             uint32_t v = 0u;
             if (g < G) {
@@ -67,7 +70,7 @@ __global__ void __launch_bounds__(kSkThreads) t158_skip_kernel(const int8_t *__r
         }
         unsigned c = 0;
 #pragma unroll
-        for (int u = 0; u < 8; u++) c += x4[u] != 0u;
+        for (int u = 0; u < kSkListLoads; u++) c += x4[u] != 0u;
         unsigned inc = c;  // inclusive scan over the threads
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(kSkThreads) t158_skip_kernel(const int8_t *__r
         __syncthreads();
         unsigned p = base + wsum[warp] + inc - c;
 #pragma unroll
-        for (int u = 0; u < 8; u++)
+        for (int u = 0; u < kSkListLoads; u++)
             if (x4[u] != 0u) {
                 list[p] = (uint16_t)(g0 + u * kSkThreads + tid);
                 xg[p] = x4[u];
@@ -105,27 +108,21 @@ __global__ void __launch_bounds__(kSkThreads) t158_skip_kernel(const int8_t *__r
     int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
     if (rows_in) {
         const uint8_t *col = wg + n0;
-        int j = j0;
-        for (; j + 8 <= j1; j += 8) {
-            uint32_t w[8];
+        // batches of kSkBatch groups, every load of a batch in flight at once; a
+        // slot past the share adds nothing (its codes are zero)
+        for (int j = j0; j < j1; j += kSkBatch) {
+            uint32_t w[kSkBatch];
 #pragma unroll
-            for (int u = 0; u < 8; u++) w[u] = __ldg(reinterpret_cast<const uint32_t *>(col + (int64_t)list[j + u] * gpitch));
+            for (int u = 0; u < kSkBatch; u++)  // a slot past the share reloads the share's last group
+                w[u] = __ldg(reinterpret_cast<const uint32_t *>(col + (int64_t)list[min(j + u, j1 - 1)] * gpitch));
 #pragma unroll
-            for (int u = 0; u < 8; u++) {
-                const uint32_t x4 = xg[j + u];
+            for (int u = 0; u < kSkBatch; u++) {
+                const uint32_t x4 = j + u < j1 ? xg[min(j + u, j1 - 1)] : 0u;
                 a0 = __dp4a((int)tab[w[u] & 0xffu], (int)x4, a0);
                 a1 = __dp4a((int)tab[(w[u] >> 8) & 0xffu], (int)x4, a1);
                 a2 = __dp4a((int)tab[(w[u] >> 16) & 0xffu], (int)x4, a2);
                 a3 = __dp4a((int)tab[w[u] >> 24], (int)x4, a3);
             }
-        }
-        for (; j < j1; j++) {
-            const uint32_t wv = __ldg(reinterpret_cast<const uint32_t *>(col + (int64_t)list[j] * gpitch));
-            const uint32_t x4 = xg[j];
-            a0 = __dp4a((int)tab[wv & 0xffu], (int)x4, a0);
-            a1 = __dp4a((int)tab[(wv >> 8) & 0xffu], (int)x4, a1);
-            a2 = __dp4a((int)tab[(wv >> 16) & 0xffu], (int)x4, a2);
-            a3 = __dp4a((int)tab[wv >> 24], (int)x4, a3);
         }
         *reinterpret_cast<int4 *>(part + (int64_t)share * Np + n0) = make_int4(a0, a1, a2, a3);
     }
