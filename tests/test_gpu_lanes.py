@@ -59,14 +59,14 @@ def test_tiny_lanes_batches_and_prompt_chunks(dev):
     # a prompt chunk of 9 tokens for sequence 2, listed out of order (9 lanes: tensor-core linears)
     order = np.array([8, 0, 7, 1, 6, 2, 5, 3, 4])
     _lane_step(gpu, orc, kvs_o, prompt[order], order, [2] * 9)
-    # single tokens for sequences 0, 1 (2 lanes: tensor cores) and 3 (1 lane: CUDA-core linears)
+    # single tokens for sequences 0, 1 (2 lanes) and 3 (1 lane): CUDA-core linears at two tokens and one
     _lane_step(gpu, orc, kvs_o, [3, 4], [0, 0], [0, 1])
     _lane_step(gpu, orc, kvs_o, [5], [0], [3])
     # a mixed step: sequence 2 continues at 9 and 10, the others at 1, plus a new
     # sequence-3 chunk: 12 lanes
     _lane_step(gpu, orc, kvs_o, [11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22],
                [9, 10, 1, 1, 1, 2, 3, 4, 5, 6, 7, 8], [2, 2, 0, 1, 3, 3, 3, 3, 3, 3, 3, 3])
-    # greedy continuation of four users for a few steps, tokens fed back
+    # greedy continuation of four users for a few steps, tokens fed back (4 lanes: tensor-core linears)
     toks = [30, 31, 32, 33]
     for s in range(4):
         nx = _lane_step(gpu, orc, kvs_o, toks, [2 + s, 2 + s, 11 + s, 9 + s], [0, 1, 2, 3], logit_check=(s == 3))

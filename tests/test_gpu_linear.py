@@ -193,6 +193,14 @@ def test_t158_m1_row_slot_variants(dev, K, N):
     _t158_case(dev, 1, K, N, seed=K + N)
 
 
+@pytest.mark.parametrize("M,K,N", [(2, 6912, 1152), (2, 1999, 3001), (2, 2051, 5000), (4, 6912, 1152),
+                                   (4, 1999, 3001), (6, 1100, 9800), (3, 333, 9800), (7, 77, 20000)])
+def test_t158_few_tokens_row_slot_variants(dev, M, K, N):
+    # 2..7 tokens through the CUDA-core kernel at row counts that select 4 (two tokens only), 2 and 1
+    # row slots per warp on a 152-SM GPU
+    _t158_case(dev, M, K, N, seed=100 * M + K)
+
+
 def test_t158_adversarial_extremes(dev):
     # all +1 trits against all +127 activations: acc = 127 K at K = 6912, the largest in use
     K, N = 6912, 64

@@ -13,9 +13,6 @@
 
 namespace qlin {
 
-qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
-                                   const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st);
-
 // ---------------------------------------------------------------- S8
 __global__ void embed_kernel(const uint16_t *__restrict__ emb, int vocab, int dim, const int32_t *__restrict__ token,
                              float *__restrict__ h, int32_t *status) {

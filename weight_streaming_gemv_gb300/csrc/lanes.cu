@@ -47,7 +47,7 @@ constexpr int kLaneStatusTimeout = 2;  // a bounded wait inside the attention ke
 // Lanes from which every linear runs on the tensor cores (on activation tiles
 // the quantisers write, the linears sharing an input in one launch); below it
 // the CUDA-core kernels, one launch per linear.
-constexpr int kLanesTensorMin = 2;
+constexpr int kLanesTensorMin = 3;
 
 __device__ __forceinline__ bool lane_ok(int pos, int seq, int max_pos, int n_seqs) {
     return pos >= 0 && pos < max_pos && seq >= 0 && seq < n_seqs;

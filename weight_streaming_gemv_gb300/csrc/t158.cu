@@ -265,20 +265,26 @@ static qlin_status launch_t158(const int8_t *xq, const float *xs, const uint8_t 
     return QLIN_OK;
 }
 
+// Row slots per warp: the most (up to RMAX) that still give every SM a block.
+template <int LPR, int MT, int RMAX>
+static qlin_status launch_slots(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
+                                const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st) {
+    const int64_t blocks_r1 = ((int64_t)N + (32 / LPR) * 8 - 1) / ((32 / LPR) * 8);
+    if constexpr (RMAX >= 4)
+        if (blocks_r1 >= 4LL * sm_count()) return launch_t158<LPR, 4, MT>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+    if (blocks_r1 >= 2LL * sm_count()) return launch_t158<LPR, 2, MT>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+    return launch_t158<LPR, 1, MT>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+}
+
+// Tokens per block: 1, 2, 4, then 8 (grid.y takes the rest; the public entry
+// points send 8 tokens and more to the tensor cores).
 template <int LPR>
 static qlin_status dispatch_mt(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
                                const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st) {
-    if (M == 1) {
-        // row slots per warp: the most that still give every SM a block
-        const int64_t blocks_r1 = ((int64_t)N + (32 / LPR) * 8 - 1) / ((32 / LPR) * 8);
-        if (blocks_r1 >= 4LL * sm_count()) return launch_t158<LPR, 4, 1>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
-        if (blocks_r1 >= 2LL * sm_count()) return launch_t158<LPR, 2, 1>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
-        return launch_t158<LPR, 1, 1>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
-    }
-    if (M == 2) return launch_t158<LPR, 4, 2>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
-    if (M <= 4) return launch_t158<LPR, 2, 4>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
-    if (M <= 8) return launch_t158<LPR, 2, 8>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
-    return launch_t158<LPR, 2, 16>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+    if (M == 1) return launch_slots<LPR, 1, 4>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+    if (M == 2) return launch_slots<LPR, 2, 4>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+    if (M <= 4) return launch_slots<LPR, 4, 2>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
+    return launch_slots<LPR, 8, 2>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
 }
 
 // Tokens from which the tensor-core kernel (a 128-token tile) takes over: its
