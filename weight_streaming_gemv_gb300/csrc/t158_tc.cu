@@ -334,6 +334,8 @@ __global__ void __launch_bounds__(256) t158_act_tiles_kernel(const int8_t *__res
     tm_put_row(out + ((int64_t)tt * nsteps + s) * tm_b_bytes(T), in, r);
 }
 
+constexpr int kQtNormLoads = 4;  // elements per thread and round of the norm prologue (n <= 4096: one round)
+
 // rmsnorm_row (decode_ops.cuh) for a whole block, the same sums: the squares'
 // pairwise tree over next_pow2(n) zero-padded leaves, each of the T threads
 // (T the largest power of two in the block) first reducing its segment of
@@ -344,9 +346,18 @@ __global__ void __launch_bounds__(256) t158_act_tiles_kernel(const int8_t *__res
 __device__ __forceinline__ void qt_rmsnorm(const float *x, const float *g, float *out, int n, float eps, float *buf,
                                            float *red) {
     const int P = next_pow2(n), tid = threadIdx.x, nth = blockDim.x;
-    for (int i = tid; i < P; i += nth) {
-        const float v = (i < n) ? x[i] : 0.0f;
-        buf[i] = __fmul_rn(v, v);
+    for (int i0 = tid; i0 < P; i0 += kQtNormLoads * nth) {  // every load of a round in flight
+        float v[kQtNormLoads];
+#pragma unroll
+        for (int j = 0; j < kQtNormLoads; j++) {
+            const int i = i0 + j * nth;
+            v[j] = (i < n) ? x[i] : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kQtNormLoads; j++) {
+            const int i = i0 + j * nth;
+            if (i < P) buf[i] = __fmul_rn(v[j], v[j]);
+        }
     }
     int T = 32;
     while (2 * T <= nth) T *= 2;
@@ -376,7 +387,20 @@ __device__ __forceinline__ void qt_rmsnorm(const float *x, const float *g, float
     ss = __fdiv_rn(ss, (float)n);
     ss = __fadd_rn(ss, eps);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(ss));
-    for (int i = tid; i < n; i += nth) out[i] = __fmul_rn(g[i], __fmul_rn(r, x[i]));
+    for (int i0 = tid; i0 < n; i0 += kQtNormLoads * nth) {
+        float gv[kQtNormLoads], xv[kQtNormLoads];
+#pragma unroll
+        for (int j = 0; j < kQtNormLoads; j++) {
+            const int i = i0 + j * nth;
+            gv[j] = i < n ? g[i] : 0.0f;
+            xv[j] = i < n ? x[i] : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kQtNormLoads; j++) {
+            const int i = i0 + j * nth;
+            if (i < n) out[i] = __fmul_rn(gv[j], __fmul_rn(r, xv[j]));
+        }
+    }
 }
 
 // Where the row a quantiser block quantises comes from.
@@ -407,6 +431,7 @@ struct QtArgs {
 // tiles_m T - 1 zero the padding rows.  One thread per 16-byte chunk (eight
 // K' values of one step); every input is read by exactly one chunk.
 constexpr int kQtThreads = 1024;  // a whole row per block: wide blocks keep a few tokens fast
+constexpr int kQtGegluLoads = 8;  // gate and up elements per thread and round of the GeGLU prologue
 
 template <int MODE>
 __global__ void __launch_bounds__(kQtThreads) t158_quant_tiles_kernel(QtArgs a) {
@@ -419,15 +444,43 @@ __global__ void __launch_bounds__(kQtThreads) t158_quant_tiles_kernel(QtArgs a) 
         if (MODE == kQtRow) {
             row = a.x + (int64_t)m * K;
         } else if (MODE == kQtGeglu) {
+            // rounds of kQtGegluLoads elements per thread (K <= 8192: one round), every
+            // load of a round in flight before the products
             const float *gr = a.x + (int64_t)m * K, *ur = a.u + (int64_t)m * K;
-            for (int k = threadIdx.x; k < K; k += blockDim.x) qt_row[k] = __fmul_rn(gelu32(gr[k]), ur[k]);
+            for (int k0 = threadIdx.x; k0 < K; k0 += kQtGegluLoads * blockDim.x) {
+                float gv[kQtGegluLoads], uv[kQtGegluLoads];
+#pragma unroll
+                for (int j = 0; j < kQtGegluLoads; j++) {
+                    const int k = k0 + j * blockDim.x;
+                    gv[j] = k < K ? gr[k] : 0.0f;
+                    uv[j] = k < K ? ur[k] : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < kQtGegluLoads; j++) {
+                    const int k = k0 + j * blockDim.x;
+                    if (k < K) qt_row[k] = __fmul_rn(gelu32(gv[j]), uv[j]);
+                }
+            }
             __syncthreads();
             row = qt_row;
         } else {
             float *hr = a.h + (int64_t)m * K;
             if (a.y) {
                 const float *yr = a.y + (int64_t)m * K;
-                for (int k = threadIdx.x; k < K; k += blockDim.x) hr[k] = __fadd_rn(hr[k], yr[k]);
+                for (int k0 = threadIdx.x; k0 < K; k0 += kQtNormLoads * blockDim.x) {
+                    float hv[kQtNormLoads], yv[kQtNormLoads];
+#pragma unroll
+                    for (int j = 0; j < kQtNormLoads; j++) {
+                        const int k = k0 + j * blockDim.x;
+                        hv[j] = k < K ? hr[k] : 0.0f;
+                        yv[j] = k < K ? yr[k] : 0.0f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < kQtNormLoads; j++) {
+                        const int k = k0 + j * blockDim.x;
+                        if (k < K) hr[k] = __fadd_rn(hv[j], yv[j]);
+                    }
+                }
             }
             // each thread reads back only the elements it wrote; the norm syncs before the sum
             qt_rmsnorm(hr, a.g, qt_row, K, a.eps, qt_row + K, red);
