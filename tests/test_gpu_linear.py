@@ -201,6 +201,13 @@ def test_t158_few_tokens_row_slot_variants(dev, M, K, N):
     _t158_case(dev, M, K, N, seed=100 * M + K)
 
 
+@pytest.mark.parametrize("M,N", [(1, 64), (3, 33), (7, 40)])
+def test_t158_longest_rows(dev, M, N):
+    # K = 131071, the largest the entry points accept: a few tokens' activation planes no longer fit in
+    # shared memory, so the tensor-core kernel takes the call (the same acc and y, bit for bit)
+    _t158_case(dev, M, 131071, N, seed=M + N)
+
+
 def test_t158_adversarial_extremes(dev):
     # all +1 trits against all +127 activations: acc = 127 K at K = 6912, the largest in use
     K, N = 6912, 64

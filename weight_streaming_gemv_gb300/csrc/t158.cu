@@ -302,6 +302,12 @@ size_t t158_tc_workspace_bytes(int M, int K);
 qlin_status t158_linear_cuda_cores(const int8_t *xq, const float *xs, const uint8_t *w, int64_t pitch, float ws,
                                    const float *ws_ptr, float *y, int32_t *acc, int M, int N, int K, cudaStream_t st) {
     const int C = (int)(pitch / 16);
+    // the activation planes of a block's tokens and the staged row must fit in
+    // shared memory; past that (very long rows) the tensor-core kernel, which
+    // streams K in steps, takes the call: the same acc and y
+    const int MT = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
+    if ((size_t)MT * C * 80 + 80 * (size_t)C + 32 + (size_t)MT * 9 * sizeof(int) > (size_t)max_smem_optin())
+        return t158_linear_tensor_cores(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st, nullptr, true);
     if (C <= 8) return dispatch_mt<8>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
     if (C <= 16) return dispatch_mt<16>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
     return dispatch_mt<32>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K, st);
