@@ -109,7 +109,9 @@ qlin_status qlin_quant_i8(const float *x, int8_t *xq, float *x_scale, int M, int
  * each matrix in one pass) the products run on the tensor cores as an fp16
  * matrix product with fp32 accumulation, exact for these operands (int8
  * codes and trits are fp16 integers and every partial sum stays below
- * 127 K < 2^24): the same acc and y, bit for bit.
+ * 127 K < 2^24): the same acc and y, bit for bit.  Below 8 tokens the
+ * CUDA-core kernel runs, except for rows too long for its activation planes
+ * in shared memory, which take the tensor-core path as well.
  * ====================================================================== */
 qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *w_packed, int64_t w_pitch,
                          float w_scale, float *y, int32_t *acc, int M, int N, int K, qlin_stream_t stream);
