@@ -105,8 +105,8 @@ qlin_status qlin_quant_i8(const float *x, int8_t *xq, float *x_scale, int M, int
  * Bytes above 242 in w_packed give unspecified but memory-safe results.
  * M: 1..4096.  K: 1..131071 (so that |acc| stays below 2^24 and the fp32
  * epilogue is exact).  UNSUPPORTED outside these ranges.
- * From M = 8 tokens (prefill and batched decode, [citric] "Step 4": all prompt tokens through
- * each matrix in one pass) the products run on the tensor cores as an fp16
+ * From M = 8 tokens (prefill and batched decode, [citric] "Step 1: a kernel for 1.6-bit
+ * weights": all prompt tokens through each matrix in one pass) the products run on the tensor cores as an fp16
  * matrix product with fp32 accumulation, exact for these operands (int8
  * codes and trits are fp16 integers and every partial sum stays below
  * 127 K < 2^24): the same acc and y, bit for bit.  Below 8 tokens the
@@ -158,10 +158,17 @@ qlin_status qlin_t158_i8_skip(const int8_t *xq, const float *x_scale, const uint
  * M: 1..64.  Accuracy: within 1e-5 of max|y| (max-abs-rel against the exact
  * dot product) on the parity inputs.
  * One token (M = 1, K <= 16384): the weights stream through shared memory by
- * bulk copies and the dot products are integer: each 16-element slice of x a
- * lane owns is held as 22-bit fixed point on a power-of-two scale from that
- * slice's largest |x| (three int8 limbs, dp4a), i.e. x is rounded to within
- * 2^-23 of the slice maximum.  A NaN or an infinity in x makes every y NaN.
+ * bulk copies and the dot products are integer: the slice of x a lane owns
+ * (at most four 16-element chunks) is held as 22-bit fixed point on a
+ * power-of-two scale 2^e from that slice's largest |x| (largest |x| < 2^e;
+ * three int8 limbs, dp4a), i.e. every x is rounded to within 2^(e-23).  So
+ * |y[n] - exact| <= w_scale * sum_k 2^(e(k)-23) |w8[n][k]| plus fp32 rounding
+ * of at most 2^-19 w_scale sum_k |x[k] w8[n][k]|, e(k) the exponent of k's
+ * slice.  That is within 1e-5 of max|y| when the magnitudes inside a slice
+ * are alike (N(0,1) inputs, or outliers whose weights are not zero); an
+ * input with a large outlier beside small values whose weights cancel the
+ * outlier's row sums can exceed it, up to the bound.  A NaN or an infinity
+ * in x makes every y NaN.
  * The kernel is launched with programmatic stream serialisation: it may start
  * while the previous kernel on the stream finishes, and waits for that
  * kernel's completion before it reads x or w8 or writes y.
@@ -252,7 +259,10 @@ qlin_status qlin_attention_decode(const float *q, const float *k_cache, const fl
  *    QLIN_ERR_UNSUPPORTED and launch nothing.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is cached per device ordinal
+ *    and belongs to the device's primary context: after cudaDeviceReset, or
+ *    from a context other than the primary one, the cached address is no
+ *    longer valid, so such callers must not use this entry point.
  *  - All calls share the one array and it keeps the last call's contents
  *    (nothing in it needs to start at zero): calls whose kernels overlap on
  *    the GPU, e.g. on two streams, race on it and give wrong results.

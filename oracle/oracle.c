@@ -23,8 +23,8 @@
  * fp64 and round once.  Everything that feeds an activation quantiser in the
  * decode step is defined in fp32 with a fixed operation order (pairwise sums,
  * a Cody-Waite exponential), because a one-ulp change in front of an int8
- * rounding changes a code and then every later token; see the readings in
- * the design notes.  Compile with -ffp-contract=off.
+ * rounding changes a code and then every later token.  Compile with
+ * -ffp-contract=off.
  *
  * Parity pins: every function here is pinned by tests under tests/ against
  * closed forms, hand-worked vectors, brute force or fp64 references.

@@ -40,10 +40,15 @@ def _lane_step(gpu, orc, kvs_o, tokens, positions, seqs, logit_check=True):
     nx_o, lg_o = orc.lanes(kvs_o, tokens, positions, seqs, want_logits=True)
     gpu.check_lanes_status()
     nx_g = host(gpu.lane_next)[:M]
+    # The lanes' hidden states are the oracle's bit for bit (the KV checks below);
+    # only the output layer's fp32 accumulation differs from the oracle's fp64
+    # sums, by about 1e-6 of the largest logit.  A token may differ only in a
+    # tie that close: the runner-up within 2e-5 of the largest |logit|, and the
+    # GPU's token must be that runner-up.
     for i in range(M):
         if nx_g[i] != nx_o[i]:
-            top = np.sort(lg_o[i])[-2:]
-            assert top[1] - top[0] <= 2e-3 * np.abs(lg_o[i]).max(), f"lane {i}: {nx_g[i]} != {nx_o[i]}"
+            tol = 2e-5 * np.abs(lg_o[i]).max()
+            assert lg_o[i][nx_o[i]] - lg_o[i][nx_g[i]] <= tol, f"lane {i}: {nx_g[i]} != {nx_o[i]}"
     if logit_check:
         for i in range(M):
             assert max_abs_rel(host(lg)[i], lg_o[i]) <= 2e-3

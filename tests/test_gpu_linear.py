@@ -121,6 +121,42 @@ def test_w8_m1_unaligned_x_tiny_values_and_nonfinite(dev):
         assert np.isnan(host(y)).all()
 
 
+def test_w8_m1_outliers_beside_small_values(dev):
+    """The one-token W8 path holds each lane's slice of x as fixed point on the
+    scale of the slice's largest |x|.  One outlier (1e4, then 1e6) in every
+    16-element chunk of N(0,1) values: with the outliers' weights as drawn the
+    result stays within 1e-5 of max|y|; with the outliers' weight columns set
+    to zero (the outliers add nothing, the small values carry the sum) every
+    row stays within the error bound the entry point states:
+    w_scale * sum_k 2^(e(k) - 23) |w8[n][k]| + 2^-19 w_scale sum_k |x[k] w8[n][k]|,
+    2^e(k) above the largest |x| of k's slice (here every slice holds an
+    outlier, so e is the outlier's exponent)."""
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    K, N = 4096, 1024
+    d = synth.w8_gemv(9, 1, K, N)
+    q_o, s_o = oracle.w8_quantize(d["w"])
+    for big in (1e4, 1e6):
+        x = d["x"].copy()
+        x[0, 7::16] = np.float32(big)
+        for zero_cols in (False, True):
+            q = q_o.copy()
+            if zero_cols:
+                q[:, 7::16] = 0
+            w8d = to_dev(np.ascontiguousarray(q), dev)
+            y = _empty((1, N), torch.float32, dev)
+            qlin.qlin_w8_f32(to_dev(x, dev), w8d, K, float(s_o), y, 1, N, K)
+            got = host(y)[0].astype(np.float64)
+            ref = oracle.w8_linear(x, q, s_o)[0].astype(np.float64)
+            if not zero_cols:
+                assert max_abs_rel(got, ref) <= 1e-5
+            e = np.floor(np.log2(np.float64(big))) + 1  # big < 2^e
+            qa = np.abs(q.astype(np.float64))
+            bound = float(s_o) * (2.0 ** (e - 23)) * qa.sum(1) + 2.0 ** -19 * float(s_o) * (qa @ np.abs(x[0].astype(np.float64)))
+            assert (np.abs(got - ref) <= bound).all()
+
+
 # ---------------------------------------------------------------- S1 W8 quantisation
 @pytest.mark.parametrize("N,K", [(768, 288), (4096, 4096), (1, 1), (3, 17)])
 def test_w8_quantize_bit_exact(dev, N, K):

@@ -5,13 +5,16 @@ plugin inside an application that owns all device memory, a real-time loop
 that cannot risk an allocation, a process that reserved its memory up front):
 it keeps its chunk partials in a fixed 256 KiB array inside the library
 instead of a caller workspace.  These checks call it through the C ABI and
-compare it with qlin_attention_decode, which takes a workspace, bit for bit
-(the tolerance the attention parity tests use), on two calls in a row; the
-second call runs on the array the first one left behind.
+compare it, bit for bit (the tolerance of the attention parity tests), with
+the oracle's decode attention and with qlin_attention_decode, which takes a
+workspace, on two calls in a row: the second call runs on the array the
+first one left behind.  The largest call that fits the array is checked the
+same way.
 """
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from gpu_util import device, host, to_dev
 
@@ -28,19 +31,33 @@ def _with_workspace(qlin, q, kc, vc, pos, nh, nkv, hd, dev):
     return host(out)
 
 
-def test_noalloc_matches_workspace_version_two_calls_in_a_row():
+def _inputs(i, pos, nh, nkv, hd):
+    q = synth.normal_f32(70, i, (nh * hd,), 0.0, 0.5)
+    kc = synth.normal_f32(71, i, (pos + 1, nkv * hd))
+    vc = synth.normal_f32(72, i, (pos + 1, nkv * hd))
+    return q, kc, vc
+
+
+def _check(qlin, dev, i, pos, nh, nkv, hd):
     import torch
+
+    q, kc, vc = _inputs(i, pos, nh, nkv, hd)
+    ref = oracle.attention(q, kc, vc, pos, nh, nkv, hd)
+    qd, kd, vd = to_dev(q, dev), to_dev(kc, dev), to_dev(vc, dev)
+    out = torch.full((nh * hd,), float("nan"), dtype=torch.float32, device=dev)
+    qlin.qlin_attention_decode_noalloc(qd, kd, vd, pos, nh, nkv, hd, out)
+    got = host(out)
+    np.testing.assert_array_equal(got, ref)
+    np.testing.assert_array_equal(got, _with_workspace(qlin, qd, kd, vd, pos, nh, nkv, hd, dev))
+
+
+def test_noalloc_matches_oracle_two_calls_in_a_row():
     from weight_streaming_gemv_gb300 import qlin
 
     dev = device()
-    cases = [(1087, 4, 1, 256), (40, 4, 2, 16)]  # the Gemma-3-1B shape at context 1088, then a small GQA case
-    for i, (pos, nh, nkv, hd) in enumerate(cases):
-        q = to_dev(synth.normal_f32(70, i, (nh * hd,), 0.0, 0.5), dev)
-        kc = to_dev(synth.normal_f32(71, i, (pos + 1, nkv * hd)), dev)
-        vc = to_dev(synth.normal_f32(72, i, (pos + 1, nkv * hd)), dev)
-        out = torch.full((nh * hd,), float("nan"), dtype=torch.float32, device=dev)
-        qlin.qlin_attention_decode_noalloc(q, kc, vc, pos, nh, nkv, hd, out)
-        np.testing.assert_array_equal(host(out), _with_workspace(qlin, q, kc, vc, pos, nh, nkv, hd, dev))
+    # the Gemma-3-1B shape at context 1088, then a small GQA case on what the first call left
+    for i, (pos, nh, nkv, hd) in enumerate([(1087, 4, 1, 256), (40, 4, 2, 16)]):
+        _check(qlin, dev, i, pos, nh, nkv, hd)
 
 
 def test_noalloc_rejects_calls_beyond_its_array():
@@ -58,6 +75,6 @@ def test_noalloc_rejects_calls_beyond_its_array():
         qlin.qlin_attention_decode_noalloc(q, kc, kc, pos, nh, nkv, hd, out)
     assert e.value.status == 2 and "scratch" in str(e.value)
     assert (host(out) == 7.0).all()  # nothing was launched
-    # the largest call that fits still works
-    qlin.qlin_attention_decode_noalloc(q, kc, kc, pos - 1, nh, nkv, hd, out)
-    torch.cuda.synchronize()
+    # the largest call that fits (nearly the whole array) is still exact
+    assert qlin.qlin_attention_workspace_size(pos, nh, hd) <= qlin.ATTENTION_NOALLOC_SCRATCH_BYTES
+    _check(qlin, dev, 2, pos - 1, nh, nkv, hd)

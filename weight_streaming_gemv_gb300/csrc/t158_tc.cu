@@ -1,12 +1,13 @@
 // T158 linear for many tokens (prefill, batched decode) on the fifth-generation
 // tensor cores.
 //
-// All tokens go through each weight matrix in one pass (citric, "Step 4":
-// batched prompt processing).  The integer dot products of "Step 1" run as an
-// fp16 matrix product with fp32 accumulation, which is exact here: int8 codes
-// (|x| <= 127) and trits are fp16 integers, every product is an integer of
-// magnitude <= 127 and every partial sum stays below 127 K < 2^24, so each fp32
-// addition is exact and the accumulator equals the int32 sum.
+// All tokens go through each weight matrix in one pass (citric, "Step 1: a
+// kernel for 1.6-bit weights": batched prompt processing).  The integer dot
+// products of that step run as an fp16 matrix product with fp32 accumulation,
+// which is exact here: int8 codes (|x| <= 127) and trits are fp16 integers,
+// every product is an integer of magnitude <= 127 and every partial sum stays
+// below 127 K < 2^24, so each fp32 addition is exact and the accumulator
+// equals the int32 sum.
 //
 // One CTA computes 128 weight rows x T tokens (T a multiple of 32, at most
 // 128, so that two CTAs share an SM's tensor memory and one's output write
