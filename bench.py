@@ -257,6 +257,7 @@ def run_decode(args, rank, local, world):
     sketch = sketch_decode(gpu, cfg, args, stream, lm_ms, peak)
     lanes = lanes_decode(gpu, cfg, stream, tok_s)
     gemv = gemv_m1(dev, stream)
+    gemv_cfg = gemv_configs(dev, stream, peak)
     prefill = prefill_m512(dev, stream)
     lanes_gemm = lanes_t158(dev, stream)
     step_gbs = step_bytes * args.steps / (ms / 1e3) / 1e9
@@ -294,6 +295,7 @@ def run_decode(args, rank, local, world):
         "sketch_head": sketch,
         "lanes_decode": lanes,
         "gemv_m1": gemv,
+        "gemv_configs": gemv_cfg,
         "prefill_m512": prefill,
         "lanes_t158": lanes_gemm,
         # the step is one launch of the fused kernel: its algorithmic bytes over
@@ -436,6 +438,114 @@ def qlin_launches(gpu, U):
     from weight_streaming_gemv_gb300 import qlin
 
     return qlin.decode_lanes_t158_launches(gpu.model, U)
+
+
+def _single_launch_us(fn, stream, n=25):
+    """One call alone: an L2 flush (a 256 MB write), then CUDA events around the call on the
+    launching stream; the median of n such calls, in microseconds."""
+    import torch
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=torch.device("cuda", torch.cuda.current_device()))
+    for _ in range(3):
+        fn()
+    ts = []
+    for it in range(n):
+        flush.fill_(it & 255)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        fn()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a0.elapsed_time(a1) * 1e3)
+    del flush
+    return float(np.median(ts))
+
+
+def _oracle_us(fn, budget_s=1.5, max_calls=200):
+    """The oracle's call timed on the host cores: calls until `budget_s` or `max_calls`."""
+    fn()
+    n, t0 = 0, time.perf_counter()
+    while n < max_calls and (n == 0 or time.perf_counter() - t0 < budget_s):
+        fn()
+        n += 1
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dt / n * 1e6, n, int(os.environ.get("OMP_NUM_THREADS", cores))
+
+
+def gemv_configs(dev, stream, peak):
+    """The GEMV configurations the metric is quoted on, each with weight GB/s over rotating
+    weight copies (>= 4x L2, CUDA graph), the fraction of the measured HBM peak, the oracle's
+    time for the same call on the host cores, and (configs 1 and 2) the single-launch time:
+    * W8 M=1, K=288, N=768 (stories15M FFN w1), seed 0;
+    * T158 M=1, K=1152, N=6912 (Gemma-3-1B gate/up), seed 1;
+    * W8 at Llama-2-7B shapes (4096->11008, 11008->4096, 4096->4096) x M in {1, 4, 16}, seed 3."""
+    import torch
+
+    import oracle
+    import synth
+    from weight_streaming_gemv_gb300 import qlin
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    out = {}
+
+    def w8_point(seed, M, K, N, single):
+        d = synth.w8_gemv(seed, M, K, N)
+        q_o, s_o = oracle.w8_quantize(d["w"])
+        pitch = (K + 15) // 16 * 16
+        w8 = np.zeros((N, pitch), np.int8)
+        w8[:, :K] = q_o
+        w1 = torch.from_numpy(w8).to(dev)
+        R = int(np.ceil(4 * l2 / w1.numel()))
+        wr = w1.repeat(R, 1)
+        x = torch.from_numpy(d["x"]).to(dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        alg = N * K + 4 * M * K + 4 * M * N
+        r = _time_rotating(lambda i: qlin.qlin_w8_f32(x, wr[i * N], pitch, float(s_o), y, M, N, K), R, alg, stream)
+        r["frac"] = round(r["gbs"] / peak, 4)
+        if single:
+            us1 = _single_launch_us(lambda: qlin.qlin_w8_f32(x, w1, pitch, float(s_o), y, M, N, K), stream)
+            r["single_launch_us"] = round(us1, 2)
+            r["single_launch_gbs"] = round(alg / (us1 * 1e-6) / 1e9, 1)
+        o_us, o_n, o_thr = _oracle_us(lambda: oracle.w8_linear(d["x"], w8, s_o, K))
+        r["cpu_baseline"] = {"us_per_call": round(o_us, 1), "gbs": round(alg / (o_us * 1e-6) / 1e9, 3),
+                             "calls": o_n, "cores": o_thr, "kind": "oracle"}
+        del w1, wr
+        return r
+
+    out["cfg1_w8_m1_k288_n768"] = w8_point(0, 1, 288, 768, True)
+    # T158 M=1 (config 2)
+    K, N = 1152, 6912
+    d = synth.t158_gemv(1, 1, K, N)
+    pitch = qlin.t158_pitch(K)
+    w1 = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+    R = int(np.ceil(4 * l2 / w1.numel()))
+    wr = w1.repeat(R, 1)
+    x = torch.from_numpy(d["x"]).to(dev)
+    xq = torch.empty((1, K), dtype=torch.int8, device=dev)
+    xs = torch.empty(1, dtype=torch.float32, device=dev)
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    qlin.qlin_quant_i8(x, xq, xs, 1, K)
+    alg = N * ((K + 4) // 5) + K + 4 + N * 4
+    r = _time_rotating(lambda i: qlin.qlin_t158_i8(xq, xs, wr[i * N], pitch, d["w_scale"], y, None, 1, N, K), R, alg,
+                       stream)
+    r["frac"] = round(r["gbs"] / peak, 4)
+    us1 = _single_launch_us(lambda: qlin.qlin_t158_i8(xq, xs, w1, pitch, d["w_scale"], y, None, 1, N, K), stream)
+    r["single_launch_us"] = round(us1, 2)
+    r["single_launch_gbs"] = round(alg / (us1 * 1e-6) / 1e9, 1)
+    xq_o, xs_o = oracle.quant_i8(d["x"])
+    pk_o = oracle.t158_pack(d["trits"])
+    o_us, o_n, o_thr = _oracle_us(lambda: oracle.t158_linear(xq_o, xs_o, pk_o, d["w_scale"], K))
+    r["cpu_baseline"] = {"us_per_call": round(o_us, 1), "gbs": round(alg / (o_us * 1e-6) / 1e9, 3), "calls": o_n,
+                         "cores": o_thr, "kind": "oracle"}
+    out["cfg2_t158_m1_k1152_n6912"] = r
+    del w1, wr
+    for K, N in ((4096, 11008), (11008, 4096), (4096, 4096)):
+        for M in (1, 4, 16):
+            out[f"cfg4_w8_m{M}_k{K}_n{N}"] = w8_point(3, M, K, N, False)
+    torch.cuda.empty_cache()
+    return out
 
 
 def gemv_m1(dev, stream):

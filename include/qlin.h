@@ -401,8 +401,24 @@ qlin_status decode_step_t158(const t158_model *m, float *kv_cache, void *workspa
 int decode_step_t158_launches(const t158_model *m);
 
 /* Reads (synchronously, after synchronising `stream`) and clears the status
- * word of a decode workspace. */
+ * word of a decode workspace.  After QLIN_ERR_TIMEOUT the workspace must be
+ * zero-filled again before the next step, and that step's KV rows at pos
+ * rewritten (the step that gave up may have left them half written). */
 qlin_status decode_step_t158_status(void *workspace, qlin_stream_t stream);
+
+/* The longest a step's CTAs wait for one another or for a copy before they
+ * give up and the status word reports QLIN_ERR_TIMEOUT (process-wide, for
+ * steps launched afterwards; 0 restores the default of 2 s).  A correct step
+ * waits microseconds; a limit below about 1 ms can make a slow but correct
+ * step give up. */
+void decode_step_t158_set_wait_limit(uint64_t ns);
+
+/* Test hook (process-wide, for steps launched afterwards): layer >= 0 makes
+ * the CTA that owns residual row 0 skip publishing its residual rows after
+ * the attention block of that layer, so every CTA's wait for them runs out
+ * and the step reports QLIN_ERR_TIMEOUT; -1 (the default) turns it off.  It
+ * exists so a test can exercise the bounded waits without faulting the GPU. */
+void decode_step_t158_test_withhold(int layer);
 
 /* The decode step with the sketch head as its output layer ([citric] "Step 3:
  * the output layer became the bottleneck"): decode_step_t158 up to the final

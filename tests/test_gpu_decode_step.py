@@ -174,3 +174,45 @@ def test_decode_step_rejects_bad_arguments(dev):
         gpu.step(8)  # pos == max_pos
     with pytest.raises(qlin.QlinError):
         qlin.decode_step_t158(gpu.model, gpu.kv, gpu.workspace, gpu.ws_bytes - 1, gpu.token, 0, None, gpu.token)
+
+
+def test_bounded_wait_runs_out_and_the_next_step_recovers(dev):
+    """Every wait of a CTA on another CTA's words is bounded.  With a 1 ms limit
+    and the test hook that makes the CTA owning residual row 0 withhold its
+    rows in layer 1,
+    every other CTA's wait for them runs out: the status word reports
+    QLIN_ERR_TIMEOUT and the kernel ends (nothing faults, the context stays
+    usable).  With the hook off, the default limit back, a re-zeroed
+    workspace and the step's KV rows rewritten by a rerun, the step matches
+    the oracle again."""
+    import time
+
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    cfg = synth.DecoderConfig(max_pos=16, **synth.TINY)
+    gpu, orc = _pair(cfg, 5, dev)
+    kv_o = orc.new_cache()
+    token = 3
+    nx_o, _ = orc.step(kv_o, token, 0)
+    qlin.decode_step_t158_set_wait_limit(1_000_000)
+    qlin.decode_step_t158_test_withhold(1)
+    try:
+        gpu.token.fill_(token)
+        t0 = time.perf_counter()
+        gpu.step(0, logits=False)
+        torch.cuda.synchronize()
+        assert time.perf_counter() - t0 < 10.0
+        with pytest.raises(qlin.QlinError) as e:
+            gpu.check_status()
+        assert e.value.status == 5  # QLIN_ERR_TIMEOUT
+    finally:
+        qlin.decode_step_t158_test_withhold(-1)
+        qlin.decode_step_t158_set_wait_limit(0)
+    gpu.workspace.zero_()
+    gpu.token.fill_(token)
+    gpu.step(0)
+    torch.cuda.synchronize()
+    gpu.check_status()
+    assert int(gpu.token.item()) == nx_o
+    np.testing.assert_array_equal(host(gpu.kv)[:, :, 0], kv_o[:, :, 0])

@@ -349,6 +349,7 @@ static qlin_status launch_lm_head(const uint16_t *emb, const float *x, int vocab
 // The step runs as one persistent kernel (decode_fused.cu).
 qlin_status launch_decode_fused(const FusedArgs &args, cudaStream_t st);
 size_t fused_smem_bytes(const t158_model *m, int G);
+int fused_lpt(const t158_model &m, int G);
 
 static size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
@@ -357,10 +358,15 @@ struct DecodeWs {
     unsigned *seq;
     unsigned *lm_ticket;
     float2 *lm_part;
-    uint64_t *hT, *qkvT, *attT, *aT, *pmT, *pST, *pUT;
+    uint64_t *hT, *qkvT, *attT, *aT, *pmT, *pST, *pUT, *amaxT, *hAcc;
     int ncmax;
     size_t bytes;
 };
+
+// Host-side settings of the fused step (process-wide): the longest wait on
+// another CTA or on a copy, and the test hook that withholds one CTA's words.
+static uint64_t g_decode_wait_ns = 0;  // 0: the 2 s default
+static int g_decode_withhold = -1;
 
 // Workspace layout; every word is zero in a fresh (zero-filled) workspace,
 // and a zero tagged word never matches the tag of any phase.
@@ -376,7 +382,7 @@ static DecodeWs carve(const t158_model *m, char *base) {
     w.ncmax = att_chunks(m->max_pos);
     w.status = (int32_t *)take(16);  // must stay first: decode_step_t158_status reads offset 0
     w.seq = (unsigned *)take(8);
-    w.lm_ticket = (unsigned *)take(4);
+    w.lm_ticket = (unsigned *)take(32);
     w.lm_part = (float2 *)take(sizeof(float2) * (size_t)sm_count());
     w.hT = (uint64_t *)take(8 * (size_t)d);
     w.qkvT = (uint64_t *)take(8 * (size_t)(qd + 2 * kvd));
@@ -385,6 +391,8 @@ static DecodeWs carve(const t158_model *m, char *base) {
     w.pmT = (uint64_t *)take(8 * (size_t)m->n_heads * w.ncmax);
     w.pST = (uint64_t *)take(8 * (size_t)m->n_heads * w.ncmax);
     w.pUT = (uint64_t *)take(8 * (size_t)m->n_heads * w.ncmax * m->head_dim);
+    w.amaxT = (uint64_t *)take(8 * (size_t)sm_count());
+    w.hAcc = (uint64_t *)take(8 * 2 * (size_t)m->n_layers * d);
     w.bytes = off;
     return w;
 }
@@ -402,14 +410,22 @@ static qlin_status check_model(const t158_model *m) {
         QLIN_REQUIRE(m->w[j] && aligned16(m->w[j]), QLIN_ERR_INVALID_ARG, "decode_step_t158: weight %d null/misaligned", j);
         QLIN_REQUIRE(m->pitch[j] % 16 == 0 && m->pitch[j] >= (ins[j] + 4) / 5, QLIN_ERR_INVALID_ARG,
                      "decode_step_t158: pitch[%d]=%lld", j, (long long)m->pitch[j]);
-        QLIN_REQUIRE(m->pitch[j] <= kFSlot, QLIN_ERR_UNSUPPORTED, "decode_step_t158: pitch[%d]=%lld above %d", j,
-                     (long long)m->pitch[j], kFSlot);
+        QLIN_REQUIRE(m->pitch[j] <= kItemMax, QLIN_ERR_UNSUPPORTED, "decode_step_t158: pitch[%d]=%lld above %d", j,
+                     (long long)m->pitch[j], kItemMax);
     }
     QLIN_REQUIRE(m->pitch[4] == m->pitch[5], QLIN_ERR_UNSUPPORTED,
                  "decode_step_t158: gate and up rows must have the same pitch (%lld, %lld)", (long long)m->pitch[4],
                  (long long)m->pitch[5]);
-    QLIN_REQUIRE(32 * kvd * 4 <= kFSlot && d * 2 <= kFSlot, QLIN_ERR_UNSUPPORTED,
+    QLIN_REQUIRE(32 * kvd * 4 <= kItemMax && d * 2 <= kItemMax, QLIN_ERR_UNSUPPORTED,
                  "decode_step_t158: kv width %d or dim %d too large for the weight ring", kvd, d);
+    {
+        // the down projection's tile of one CTA: its output rows and input chunks
+        const int G = sm_count(), KG = down_kgroups(G), NG = G / KG;
+        const int rows = (d + NG - 1) / NG, chunks = ((int)(m->pitch[6] / 16) + KG - 1) / KG;
+        QLIN_REQUIRE(rows <= kFMaxRows && rows * chunks * 16 <= kItemMax && 80 * chunks <= m->ffn + 80,
+                     QLIN_ERR_UNSUPPORTED, "decode_step_t158: down projection tile %d x %d chunks too large", rows,
+                     chunks);
+    }
     QLIN_REQUIRE(m->max_pos <= 4096, QLIN_ERR_UNSUPPORTED, "decode_step_t158: max_pos %d above 4096", m->max_pos);
     QLIN_REQUIRE(m->ffn % 4 == 0, QLIN_ERR_UNSUPPORTED, "decode_step_t158: ffn %d not a multiple of 4", m->ffn);
     QLIN_REQUIRE(m->n_layers <= 127, QLIN_ERR_UNSUPPORTED, "decode_step_t158: %d layers above 127", m->n_layers);
@@ -418,6 +434,9 @@ static qlin_status check_model(const t158_model *m) {
                  "decode_step_t158: dim %d needs more than four packed bytes per thread", m->dim);
     QLIN_REQUIRE(m->scales && m->g_attn && m->g_ffn && m->g_final && m->emb && m->rope_cos && m->rope_sin,
                  QLIN_ERR_INVALID_ARG, "decode_step_t158: null model tensor");
+    QLIN_REQUIRE(aligned16(m->g_attn) && aligned16(m->g_ffn) && aligned16(m->g_final), QLIN_ERR_INVALID_ARG,
+                 "decode_step_t158: norm gains not 16-byte aligned");
+    QLIN_REQUIRE(fused_lpt(*m, sm_count()) > 0, QLIN_ERR_UNSUPPORTED, "decode_step_t158: model too wide");
     QLIN_REQUIRE(aligned16(m->emb), QLIN_ERR_INVALID_ARG, "decode_step_t158: emb not 16-byte aligned");
     return QLIN_OK;
 }
@@ -550,11 +569,15 @@ qlin_status decode_step_t158(const t158_model *m, float *kv_cache, void *workspa
     a.pmT = w.pmT;
     a.pST = w.pST;
     a.pUT = w.pUT;
+    a.amaxT = w.amaxT;
+    a.hAcc = w.hAcc;
     a.ncmax = w.ncmax;
     a.lm_part = w.lm_part;
     a.lm_ticket = w.lm_ticket;
     a.seq = w.seq;
     a.status = w.status;
+    a.wait_ns = qlin::g_decode_wait_ns;
+    a.withhold = qlin::g_decode_withhold;
     return qlin::launch_decode_fused(a, (cudaStream_t)stream);
 }
 
@@ -635,11 +658,15 @@ qlin_status decode_step_t158_sketch(const t158_model *m, const t158_sketch *s, f
     a.pmT = w.pmT;
     a.pST = w.pST;
     a.pUT = w.pUT;
+    a.amaxT = w.amaxT;
+    a.hAcc = w.hAcc;
     a.ncmax = w.ncmax;
     a.lm_part = w.lm_part;
     a.lm_ticket = w.lm_ticket;
     a.seq = w.seq;
     a.status = w.status;
+    a.wait_ns = qlin::g_decode_wait_ns;
+    a.withhold = qlin::g_decode_withhold;
     if ((st = qlin::launch_decode_fused(a, (cudaStream_t)stream))) return st;
     return qlin_sketch_head(m->emb, s->emb_t, s->signs, s->perm, s->c_e, m->vocab, m->dim, sw.final_x, s->k, s->n_cand,
                             nullptr, sw.cand, sw.cand_logits, next_token, sw.sketch, sw.sketch_bytes, stream);
@@ -661,6 +688,10 @@ int decode_step_t158_launches(const t158_model *m) {
     if (qlin::check_model(m)) return -1;
     return 1;  // one persistent kernel per step
 }
+
+void decode_step_t158_set_wait_limit(uint64_t ns) { qlin::g_decode_wait_ns = ns; }
+
+void decode_step_t158_test_withhold(int layer) { qlin::g_decode_withhold = layer; }
 
 qlin_status decode_step_t158_status(void *workspace, qlin_stream_t stream) {
     qlin::clear_error();

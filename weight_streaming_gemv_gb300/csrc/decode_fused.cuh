@@ -1,7 +1,8 @@
-// Pieces of the fused decode step: the per-CTA schedule of weight slices
-// (shared by the TMA producer and the consumer warps, so both walk the same
-// items in the same order), quantise-into-planes, T158 rows from a shared
-// memory slot, and the bounded grid barrier.
+// Pieces of the fused decode step: the byte ring that streams each CTA's
+// weights and cached K/V rows into shared memory (the TMA producer and the
+// consumer warps walk the same items in the same order), the words CTAs hand
+// to one another (tagged values, counted integer sums), quantise-into-planes,
+// and T158 rows from shared memory.
 #pragma once
 
 #include "decode_ops.cuh"
@@ -9,11 +10,12 @@
 
 namespace qlin {
 
-constexpr int kFStages = 4;
-constexpr int kFSlot = 36864;  // bytes per ring slot (16 bf16 rows of 1152)
+constexpr int kRingBytes = 147456;  // byte ring of variable-size items
+constexpr int kRingBars = 32;       // items in flight at most (one full and one empty barrier each)
+constexpr int kItemMax = 36864;     // largest item (16 bf16 rows of 1152, 36 rows of 1024 B)
 constexpr int kFConsumerWarps = 11;  // + 1 producer warp = 12 warps: 3 per SM sub-partition, up to 168 registers
 constexpr int kFThreads = 32 * (kFConsumerWarps + 1);
-constexpr int kFMaxRows = 512;  // rows of a T158 piece (their integer sums wait in shared memory)
+constexpr int kFMaxRows = 160;  // rows of a T158 item: a warp collects at most 32 rounds of row sums
 
 struct FusedArgs {
     t158_model m;
@@ -25,11 +27,15 @@ struct FusedArgs {
     float *final_x;  // non-null: stop after the final norm and write it here (no lm_head, next untouched)
     // workspace: vectors passed between CTAs as tagged words (value | tag << 32)
     uint64_t *hT, *qkvT, *attT, *aT, *pmT, *pST, *pUT;
+    uint64_t *amaxT;  // [G] each CTA's largest |GeGLU output| (tagged)
+    uint64_t *hAcc;   // [2][n_layers][dim] counted integer sums of the down projection (by launch parity)
     int ncmax;
     float2 *lm_part;
-    unsigned *lm_ticket;
+    unsigned *lm_ticket;  // [8]: the lm_head ticket, then the counters of the six hand-offs of a layer
     unsigned *seq;  // launch sequence number, advanced by the last CTA of every launch
     int32_t *status;
+    uint64_t wait_ns;  // longest wait on another CTA or on a copy before the step gives up
+    int withhold;      // test hook: >= 0 makes the CTA owning residual row 0 skip its words of that layer
 };
 
 // ---------------------------------------------------------------- tagged words
@@ -50,6 +56,30 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t *p) {
 __device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t tag) {
     const uint64_t w = (uint64_t)__float_as_uint(v) | ((uint64_t)tag << 32);
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+// The wait limit of the current launch (set once per CTA from FusedArgs).
+__device__ __forceinline__ uint64_t &wait_limit_ns() {
+    __shared__ uint64_t lim;
+    return lim;
+}
+
+// One poll round found words still missing: true when the caller should stop
+// waiting (its limit ran out, or another CTA already gave up and raised the
+// timeout bit in the status word, which this CTA then sees within 64 rounds).
+__device__ __forceinline__ bool wait_gives_up(int pass, uint64_t &t0, volatile int *abort, int32_t *status) {
+    if (*abort) return true;
+    if (pass == 0) t0 = global_ns();
+    if ((pass & 63) == 63 && (*reinterpret_cast<volatile int32_t *>(status) & kStatusTimeout)) {
+        *abort = 1;
+        return true;
+    }
+    if (global_ns() - t0 > wait_limit_ns()) {
+        raise_status(status, kStatusTimeout);
+        *abort = 1;
+        return true;
+    }
+    return false;
 }
 
 // out[j] = value of the tagged word at ptr(j) for every j whose bit is set in
@@ -74,17 +104,73 @@ __device__ __forceinline__ void fetch_tagged_at(Ptr &&ptr, uint32_t mask, uint32
 #pragma unroll
         for (int j = 0; j < N; j++)
             if ((pending & (1u << j)) && (uint32_t)(w[j] >> 32) == tag) pending &= ~(1u << j);
-        if (!pending || *abort) break;
-        if (pass == 0) t0 = global_ns();
-        if (global_ns() - t0 > kWaitLimitNs) {
-            raise_status(status, kStatusTimeout);
-            *abort = 1;
-            break;
-        }
+        if (!pending || wait_gives_up(pass, t0, abort, status)) break;
         __nanosleep(32);
     }
 #pragma unroll
     for (int j = 0; j < N; j++) out[j] = (mask & (1u << j)) ? __uint_as_float((uint32_t)w[j]) : 0.0f;
+}
+
+// ---------------------------------------------------------------- hand-off counters
+// An all-to-all hand-off (every CTA publishes words, every CTA reads all of
+// them) also counts arrivals: after publishing, each CTA adds one to the
+// hand-off's counter (relaxed: the words carry their own tags, so their
+// visibility need not be ordered with the count), and a reader polls that one
+// word with one thread until every CTA has arrived, then reads the words once
+// (re-polling only a word whose tag is still stale).  One polled word per CTA
+// instead of every word keeps the poll traffic off the words being written.
+__device__ __forceinline__ void hop_arrive(unsigned *c) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
+}
+
+__device__ __forceinline__ void hop_wait(const unsigned *c, unsigned want, volatile int *abort, int32_t *status) {
+    uint64_t t0 = 0;
+    for (int pass = 0;; pass++) {
+        unsigned v;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+        if ((int)(v - want) >= 0 || wait_gives_up(pass, t0, abort, status)) return;
+        __nanosleep(20);
+    }
+}
+
+// ---------------------------------------------------------------- counted integer sums
+// An exact int32 sum assembled from several CTAs' partial sums: each
+// contributor adds 2^48 + (its partial, as a two's-complement 64-bit value)
+// to one 8-byte word with a relaxed atomic.  The low 48 bits then hold the
+// running sum (|sum| < 2^47) and the high bits the number of contributions,
+// so a reader knows the sum is complete when the count reaches the number of
+// contributors; integer addition makes the result independent of their order.
+__device__ __forceinline__ void counted_add(uint64_t *p, int partial) {
+    const uint64_t v = (1ull << 48) + (uint64_t)(int64_t)partial;
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ int64_t counted_sum(uint64_t w) { return ((int64_t)(w << 16)) >> 16; }
+__device__ __forceinline__ uint32_t counted_count(uint64_t w) { return (uint32_t)((w - (uint64_t)counted_sum(w)) >> 48); }
+
+// out[j] = the complete sum of word ptr(j) for every j whose bit is set in
+// mask (0 for the others), once `want` contributions have arrived (bounded
+// wait, as fetch_tagged_at).
+template <int N, class Ptr>
+__device__ __forceinline__ void fetch_counted_at(Ptr &&ptr, uint32_t mask, uint32_t want, int (&out)[N],
+                                                 volatile int *abort, int32_t *status) {
+    uint64_t w[N];
+#pragma unroll
+    for (int j = 0; j < N; j++) w[j] = 0;
+    uint32_t pending = mask;
+    uint64_t t0 = 0;
+    for (int pass = 0;; pass++) {
+#pragma unroll
+        for (int j = 0; j < N; j++)
+            if (pending & (1u << j)) w[j] = ld_relaxed_u64(ptr(j));
+#pragma unroll
+        for (int j = 0; j < N; j++)
+            if ((pending & (1u << j)) && counted_count(w[j]) >= want) pending &= ~(1u << j);
+        if (!pending || wait_gives_up(pass, t0, abort, status)) break;
+        __nanosleep(32);
+    }
+#pragma unroll
+    for (int j = 0; j < N; j++) out[j] = (mask & (1u << j)) ? (int)counted_sum(w[j]) : 0;
 }
 
 // src[first + j * stride] for j < count (count <= N)
@@ -101,40 +187,114 @@ __device__ __forceinline__ void share(int n, int b, int G, int &lo, int &hi) {
     hi = (int)((int64_t)n * (b + 1) / G);
 }
 
-// A piece: up to slot-sized run of consecutive rows of one matrix.
-struct Piece {
-    const uint8_t *src;
-    int rows, pitch, row0, mat;
+// ---------------------------------------------------------------- the byte ring
+// Every CTA streams its share of the step's data (weight rows, cached K/V
+// rows, lm_head rows) through one ring of kRingBytes of shared memory, as a
+// sequence of items of any size up to kItemMax.  Item i occupies the next
+// bytes of the ring (an item that would cross the end starts at 0 instead)
+// and uses barrier pair i % kRingBars: full (one producer arrival plus the
+// copied bytes) and empty (one arrival per consumer warp when the warp is done
+// with it).  Every consumer warp waits for an item by itself, so warps that
+// work on different rows of one item never wait for one another.  Consumers release items in order, so the producer may reuse bytes as
+// soon as the oldest items holding them are released: small items no longer
+// waste a whole slot, and the producer runs as far ahead as the bytes allow.
+struct ByteRing {
+    uint64_t full[kRingBars];
+    uint64_t empty[kRingBars];
+
+    __device__ __forceinline__ void init() {
+        for (int s = 0; s < kRingBars; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kFConsumerWarps);
+        }
+        fence_mbar_init();
+    }
 };
 
-// Calls f(piece) for every slot-sized piece of rows [lo, hi) of matrix `mat`.
+// Placement of the items: both sides walk the same sizes, so they agree on
+// every item's offset without communicating.
+struct RingCursor {
+    uint32_t v = 0;  // virtual offset of the next item (bytes streamed so far, with skipped tails)
+    int i = 0;       // index of the next item
+    __device__ __forceinline__ uint32_t place(uint32_t alloc, uint32_t &vstart) {
+        uint32_t off = v % kRingBytes;
+        if (off + alloc > (uint32_t)kRingBytes) {
+            v += kRingBytes - off;
+            off = 0;
+        }
+        vstart = v;
+        v += alloc;
+        i++;
+        return off;
+    }
+};
+
+// An item: `rows` rows of row_bytes copied from src (row r at src + r *
+// src_stride; one bulk copy when the rows are contiguous), with room for
+// alloc_rows rows in the ring.
+struct Item {
+    const uint8_t *src;
+    int64_t src_stride;
+    int rows, alloc_rows, row_bytes, row0, mat;
+};
+
+__device__ __forceinline__ Item make_item(const uint8_t *src, int rows, int row_bytes, int row0, int mat) {
+    Item it;
+    it.src = src;
+    it.src_stride = row_bytes;
+    it.rows = rows;
+    it.alloc_rows = rows;
+    it.row_bytes = row_bytes;
+    it.row0 = row0;
+    it.mat = mat;
+    return it;
+}
+
+// Calls f(item) for every item-sized run of rows [lo, hi) of matrix `mat`.
 template <class F>
 __device__ __forceinline__ void pieces(const uint8_t *base, int64_t pitch, int lo, int hi, int mat, F &&f,
                                        int max_rows = 1 << 30) {
-    int per = (int)(kFSlot / pitch) > 0 ? (int)(kFSlot / pitch) : 1;
+    int per = (int)(kItemMax / pitch) > 0 ? (int)(kItemMax / pitch) : 1;
     per = per < max_rows ? per : max_rows;
-    for (int r = lo; r < hi; r += per) {
-        Piece p;
-        p.rows = min(per, hi - r);
-        p.pitch = (int)pitch;
-        p.row0 = r;
-        p.mat = mat;
-        p.src = base + (int64_t)r * pitch;
-        f(p);
-    }
+    for (int r = lo; r < hi; r += per) f(make_item(base + (int64_t)r * pitch, min(per, hi - r), (int)pitch, r, mat));
 }
 
-// The items of layer l for CTA b, in consumption order.  QKV rows are the
-// concatenation q | k | v; Wo and down share the residual rows this CTA owns;
-// gate and up share the GeGLU rows; attention item e = chunk * n_heads + head
-// (chunk = 32 positions) belongs to CTA e mod G and needs the cached rows of
-// its chunk below `pos`, K then V.
+// The down projection of a layer is split over the grid in two dimensions:
+// KG groups of its input (16-byte chunks of the packed rows: 80 inputs each)
+// times NG groups of its output rows, CTA b taking input group b % KG and
+// row group b / KG.  Each output row then gets KG partial integer sums.
+__host__ __device__ __forceinline__ int down_kgroups(int G) { return G % 8 == 0 ? 8 : G % 4 == 0 ? 4 : G % 2 == 0 ? 2 : 1; }
+
+struct DownTile {
+    int c0, c1;  // 16-byte chunks [c0, c1) of a packed row
+    int r0, r1;  // output rows
+};
+
+__device__ __forceinline__ DownTile down_tile(const t158_model &m, int b, int G) {
+    const int KG = down_kgroups(G), NG = G / KG;
+    const int kg = b % KG, ng = b / KG;
+    const int C = (int)(m.pitch[6] / 16);
+    DownTile t;
+    t.c0 = C * kg / KG;
+    t.c1 = C * (kg + 1) / KG;
+    t.r0 = m.dim * ng / NG;
+    t.r1 = m.dim * (ng + 1) / NG;
+    return t;
+}
+
+// The items of layer l for CTA b, in consumption order (layer_items calls
+// the five generators below in turn; the consumers call each one at its
+// phase).  QKV rows are the concatenation q | k | v; attention item e = chunk
+// * n_heads + head (chunk = 32 positions) belongs to CTA e mod G and needs
+// the cached rows of its chunk below `pos`, K then V (with room for the
+// current position's row when the chunk holds it); Wo rows are the residual
+// rows this CTA owns; gate and up share the GeGLU rows; the down projection
+// is this CTA's tile (its output rows x its input chunks: one copy per row).
 template <class F>
-__device__ __forceinline__ void layer_items(const FusedArgs &A, int l, int b, int G, F &&f) {
+__device__ __forceinline__ void qkv_items(const FusedArgs &A, int l, int b, int G, F &&f) {
     const t158_model &m = A.m;
-    const int d = m.dim, qd = m.n_heads * m.head_dim, kvd = m.n_kv_heads * m.head_dim, ff = m.ffn;
-    const int rows[T158_NMAT] = {qd, kvd, kvd, d, ff, ff, d};
-    // Q K V
+    const int qd = m.n_heads * m.head_dim, kvd = m.n_kv_heads * m.head_dim;
+    const int rows[3] = {qd, kvd, kvd};
     int lo, hi;
     share(qd + 2 * kvd, b, G, lo, hi);
     int base = 0;
@@ -145,39 +305,77 @@ __device__ __forceinline__ void layer_items(const FusedArgs &A, int l, int b, in
             pieces(m.w[j] + (int64_t)l * rows[j] * m.pitch[j], m.pitch[j], a0 - base, a1 - base, j, f, kFMaxRows);
         base += rows[j];
     }
-    // attention K/V prefetch (rows strictly below pos) for this CTA's (chunk, head) items
-    const int nc = A.pos / 32 + 1;
+}
+
+// the K and V items of attention item e (none when the chunk has no cached rows)
+template <class F>
+__device__ __forceinline__ void attn_items(const FusedArgs &A, int l, int e, F &&f) {
+    const t158_model &m = A.m;
+    const int kvd = m.n_kv_heads * m.head_dim;
+    const int c = e / m.n_heads;
+    const int t0 = 32 * c, npre = min(t0 + 32, A.pos) - t0;
+    const int nt = min(32, A.pos + 1 - t0);
+    if (npre <= 0) return;
     const float *kc = A.kv + (int64_t)(2 * l) * m.max_pos * kvd;
     const float *vc = A.kv + (int64_t)(2 * l + 1) * m.max_pos * kvd;
-    for (int e = b; e < nc * m.n_heads; e += G) {
-        const int c = e / m.n_heads;
-        const int t0 = 32 * c, npre = min(t0 + 32, A.pos) - t0;
-        if (npre > 0) {
-            Piece p;
-            p.rows = npre;
-            p.pitch = kvd * 4;
-            p.row0 = t0;
-            p.mat = 7;
-            p.src = reinterpret_cast<const uint8_t *>(kc + (int64_t)t0 * kvd);
-            f(p);
-            p.mat = 8;
-            p.src = reinterpret_cast<const uint8_t *>(vc + (int64_t)t0 * kvd);
-            f(p);
-        }
-    }
-    share(d, b, G, lo, hi);
-    pieces(m.w[3] + (int64_t)l * rows[3] * m.pitch[3], m.pitch[3], lo, hi, 3, f, kFMaxRows);
+    Item it = make_item(reinterpret_cast<const uint8_t *>(kc + (int64_t)t0 * kvd), npre, kvd * 4, t0, 7);
+    it.alloc_rows = nt;
+    f(it);
+    it.src = reinterpret_cast<const uint8_t *>(vc + (int64_t)t0 * kvd);
+    it.mat = 8;
+    f(it);
+}
+
+template <class F>
+__device__ __forceinline__ void wo_items(const FusedArgs &A, int l, int b, int G, F &&f) {
+    const t158_model &m = A.m;
+    int lo, hi;
+    share(m.dim, b, G, lo, hi);
+    pieces(m.w[3] + (int64_t)l * m.dim * m.pitch[3], m.pitch[3], lo, hi, 3, f, kFMaxRows);
+}
+
+// gate and up in pairs over the same rows (one pass computes both): f(gate item, up item)
+template <class F>
+__device__ __forceinline__ void gateup_items(const FusedArgs &A, int l, int b, int G, F &&f) {
+    const t158_model &m = A.m;
     int g0, g1;
-    share(ff, b, G, g0, g1);
-    // gate and up in pairs over the same rows (one pass computes both)
-    pieces(m.w[4] + (int64_t)l * rows[4] * m.pitch[4], m.pitch[4], g0, g1, 4, [&](const Piece &p) {
-        f(p);
-        Piece u = p;
+    share(m.ffn, b, G, g0, g1);
+    pieces(m.w[4] + (int64_t)l * m.ffn * m.pitch[4], m.pitch[4], g0, g1, 4, [&](const Item &p) {
+        Item u = p;
         u.mat = 5;
-        u.src = m.w[5] + (int64_t)l * rows[5] * m.pitch[5] + (int64_t)p.row0 * m.pitch[5];
-        f(u);
+        u.src = m.w[5] + (int64_t)l * m.ffn * m.pitch[5] + (int64_t)p.row0 * m.pitch[5];
+        f(p, u);
     }, kFMaxRows);
-    pieces(m.w[6] + (int64_t)l * rows[6] * m.pitch[6], m.pitch[6], lo, hi, 6, f, kFMaxRows);
+}
+
+// the down tile: rows [r0, r1), bytes [16 c0, 16 c1) of each (always one item, maybe empty)
+__device__ __forceinline__ Item down_item(const FusedArgs &A, int l, int b, int G) {
+    const t158_model &m = A.m;
+    const DownTile dt = down_tile(m, b, G);
+    Item it = make_item(m.w[6] + (int64_t)l * m.dim * m.pitch[6] + (int64_t)dt.r0 * m.pitch[6] + 16 * dt.c0,
+                        dt.c1 > dt.c0 ? dt.r1 - dt.r0 : 0, 16 * (dt.c1 - dt.c0), dt.r0, 6);
+    it.src_stride = m.pitch[6];
+    return it;
+}
+
+// a vector of norm gains (one row of dim floats)
+__device__ __forceinline__ Item gain_item(const float *gam, int dim) {
+    return make_item(reinterpret_cast<const uint8_t *>(gam), 1, dim * 4, 0, 10);
+}
+
+template <class F>
+__device__ __forceinline__ void layer_items(const FusedArgs &A, int l, int b, int G, F &&f) {
+    f(gain_item(A.m.g_attn + (int64_t)l * A.m.dim, A.m.dim));
+    qkv_items(A, l, b, G, f);
+    const int nc = A.pos / 32 + 1;
+    for (int e = b; e < nc * A.m.n_heads; e += G) attn_items(A, l, e, f);
+    wo_items(A, l, b, G, f);
+    f(gain_item(A.m.g_ffn + (int64_t)l * A.m.dim, A.m.dim));
+    gateup_items(A, l, b, G, [&](const Item &p, const Item &u) {
+        f(p);
+        f(u);
+    });
+    f(down_item(A, l, b, G));
 }
 
 // lm_head tiles of CTA b
@@ -190,192 +388,142 @@ __device__ __forceinline__ void lm_items(const FusedArgs &A, int b, int G, F &&f
     pieces(reinterpret_cast<const uint8_t *>(A.m.emb), (int64_t)dim * 2, lo, hi, 9, f, 2 * kFConsumerWarps);
 }
 
-// ---------------------------------------------------------------- quantise into digit-plane order
-// Codes of v (shared memory, K elements) for step `scale` into the plane
-// layout, one plane word per thread and round: word c*20 + 4i + w holds, in
-// byte b, the code of element 5(16c + 4w + b) + i (0 past K).  The sum of the
-// codes is added into *isum (shared memory, zeroed by the caller before the
-// last group barrier).  No group barrier inside: the caller syncs once after.
-__device__ __forceinline__ void planes_words(const float *v, int K, float scale, int C, uint4 *xr, int *isum, Grp g) {
-    uint32_t *xw = reinterpret_cast<uint32_t *>(xr);
+// ---------------------------------------------------------------- vectors held in registers
+// Every vector of the step that feeds a quantiser (h, h', the attention
+// output, a slice of the GeGLU output) is held LPT elements per consumer
+// thread: thread t owns elements [LPT t, LPT t + LPT).  LPT is 4 for vectors
+// of up to 4 x 352 = 1408 elements and 16 above.
+
+// The plane byte of element k of a quantised vector: word c*20 + 4i + w holds,
+// in byte b, the code of element 5(16c + 4w + b) + i (c = k / 80).
+__device__ __forceinline__ int plane_byte(int k) {
+    const int c = k / 80, q = k - 80 * c;
+    const int j = q / 5, i = q - 5 * j;
+    return (c * 20 + 4 * i + (j >> 2)) * 4 + (j & 3);
+}
+
+// Codes of this thread's elements (k = k0 + j < K; zero for K <= k < Kpad)
+// for step `scale` written into the planes; returns the sum of the codes.
+template <int LPT>
+__device__ __forceinline__ int codes_to_planes(const float (&v)[LPT], int k0, int K, int Kpad, float scale,
+                                               int8_t *planes) {
     const float rinv = __fdiv_rn(1.0f, scale);
-    const int nwords = C * 20;
     int s = 0;
-    for (int wi = g.tid; wi < nwords; wi += g.n) {
-        const int c = wi / 20, r = wi - 20 * c;
-        const int base = 5 * (16 * c + 4 * (r & 3)) + (r >> 2);
-        uint32_t word = 0;
 #pragma unroll
-        for (int bb = 0; bb < 4; bb++) {
-            const int k = base + 5 * bb;
-            const int q = k < K ? quant_code_r(v[k], scale, rinv) : 0;
+    for (int j = 0; j < LPT; j++) {
+        const int k = k0 + j;
+        if (k < Kpad) {
+            const int q = k < K ? quant_code_r(v[j], scale, rinv) : 0;
+            planes[plane_byte(k)] = (int8_t)q;
             s += q;
-            word |= (uint32_t)(q & 0xff) << (8 * bb);
         }
-        xw[wi] = word;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (g.lane() == 0) atomicAdd(isum, s);
+    return s;
 }
 
-// Sum of squares of x[0..d) (d <= 4096) as the pairwise tree over
-// next_pow2(d) zero-padded leaves.  The 32-leaf segment s of x (elements
-// 32s .. 32s+31) is held by warp s mod nw, one element per lane, so the loads
-// are coalesced; the warp sums the squares of a segment with the adjacent-lane
-// tree (its lower five levels) and seg[s] keeps the result.  With srcT the
-// vector comes from tagged words (waited for by tag) and is staged into xs;
-// without, xs already holds it.  The caller syncs the group, then calls
-// seg_total.
-__device__ __forceinline__ void stage_segments(const uint64_t *srcT, uint32_t tag, float *xs, int d, float *seg,
-                                               Grp g, volatile int *abort, int32_t *status) {
-    constexpr int N = 8;
-    const int nw = g.n >> 5, lane = g.lane(), w = g.warp();
-    const int nseg = (d + 31) >> 5;
-    for (int s0 = 0; s0 < nseg; s0 += N * nw) {
-        uint32_t mask = 0;
-#pragma unroll
-        for (int j = 0; j < N; j++) {
-            const int k = 32 * (s0 + w + j * nw) + lane;
-            if (k < d) mask |= 1u << j;
-        }
-        float v[N];
-        if (srcT) {
-            fetch_tagged_at<N>([&](int j) { return srcT + 32 * (s0 + w + j * nw) + lane; }, mask, tag, v, abort,
-                               status);
-#pragma unroll
-            for (int j = 0; j < N; j++)
-                if (mask & (1u << j)) xs[32 * (s0 + w + j * nw) + lane] = v[j];
-        } else {
-#pragma unroll
-            for (int j = 0; j < N; j++) v[j] = (mask & (1u << j)) ? xs[32 * (s0 + w + j * nw) + lane] : 0.0f;
-        }
-#pragma unroll
-        for (int j = 0; j < N; j++) {
-            const int sg = s0 + w + j * nw;  // uniform across the warp
-            if (sg < nseg) {
-                const float sq = warp_psum(__fmul_rn(v[j], v[j]));
-                if (lane == 0) seg[sg] = sq;
-            }
-        }
-    }
+__device__ __forceinline__ int warp_isum(int v) { return __reduce_add_sync(0xffffffffu, v); }
+
+// Largest of a warp's non-negative floats (their bit patterns order as unsigned integers).
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
 
-// The upper levels of the tree of stage_segments: every warp sums the
-// segment sums (zero past the last segment of x) and returns the total.
-__device__ __forceinline__ float seg_total(const float *seg, int d, Grp g) {
-    const int nseg = (d + 31) >> 5;
-    const int ns = next_pow2(d) >> 5;  // segments of the padded tree (>= 1)
-    const int L = ns > 32 ? ns / 32 : 1;  // 1, 2 or 4 per lane
-    const int lane = g.lane();
-    float a[4];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int idx = lane * L + i;
-        a[i] = (i < L && idx < nseg) ? seg[idx] : 0.0f;
-    }
-    float t = a[0];
-    if (L == 2) t = __fadd_rn(a[0], a[1]);
-    if (L == 4) t = __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
-    return warp_psum(t);
+// Largest of a warp's floats (any sign, no NaN): the bits mapped to a signed key
+// that orders as the floats do.
+__device__ __forceinline__ float warp_max_any(float v) {
+    const int b = __float_as_int(v);
+    const int k = __reduce_max_sync(0xffffffffu, b ^ ((b >> 31) & 0x7fffffff));
+    return __int_as_float(k ^ ((k >> 31) & 0x7fffffff));
 }
 
-// RMSNorm + absmax quantisation of a d-vector (d <= 4096) into the planes,
-// with three group barriers.  The vector comes from tagged words srcT (other
-// CTAs' output, waited for by tag, staged into xs) or, when srcT is null, is
-// already in xs (shared memory).  Sum of squares as stage_segments/seg_total;
-// each thread normalises the elements k = t, t + n, ... into xn, with its
-// gains (global memory, read-only) read into registers before the vector
-// arrives; the group takes the absmax, and the codes are written one plane
-// word per thread (planes_words).  Returns the step; *sumx gets the sum of
-// the codes.  The arithmetic is that of rmsnorm_row and the
-// absmax quantiser.
-__device__ __forceinline__ float norm_quant(const uint64_t *srcT, uint32_t tag, float *xs, const float *gam, int d,
-                                            float eps, float *xn, uint4 *xr, int C, float *red, float *seg, int *isum,
-                                            int *sumx, Grp g, volatile int *abort, int32_t *status) {
-    const int t = g.tid;
-    constexpr int MAXE = 20;  // elements per thread (d <= 20 * group size)
-    float gv[MAXE];
+// Scratch of the register-vector helpers (shared memory, per CTA).
+struct VecScratch {
+    float wsum[32];  // warp subtree sums of a norm
+    float wmax[32];  // warp maxima
+    int wisum[32];   // warp code sums
+};
+
+// Sum of squares of the vector (d elements) as the pairwise tree over
+// next_pow2(d) zero-padded leaves: each thread's LPT leaves in place, then the
+// warp's 32 lanes by xor shuffles (adjacent subtrees first), then every thread
+// adds the warp subtrees (32 LPT leaves each) in a balanced tree.  One group
+// barrier.
+template <int LPT>
+__device__ __forceinline__ float sumsq_tree(const float (&v)[LPT], int d, VecScratch *S, Grp g) {
+    float a[LPT];
 #pragma unroll
-    for (int e = 0; e < MAXE; e++) {
-        const int k = t + e * g.n;
-        gv[e] = k < d ? __ldg(gam + k) : 0.0f;
-    }
-    stage_segments(srcT, tag, xs, d, seg, g, abort, status);
-    g.sync();  // 1: segment sums and the staged vector are visible
-    float ss = seg_total(seg, d, g);
-    ss = __fdiv_rn(ss, (float)d);
-    ss = __fadd_rn(ss, eps);
-    const float r = __fdiv_rn(1.0f, __fsqrt_rn(ss));
-    float amax = 0.0f;
+    for (int j = 0; j < LPT; j++) a[j] = __fmul_rn(v[j], v[j]);
 #pragma unroll
-    for (int e = 0; e < MAXE; e++) {
-        const int k = t + e * g.n;
-        if (k < d) {
-            const float val = __fmul_rn(gv[e], __fmul_rn(r, xs[k]));
-            xn[k] = val;
-            amax = fmaxf(amax, fabsf(val));
-        }
-    }
-    amax = warp_max(amax);
-    if (g.lane() == 0) red[8 + g.warp()] = amax;
-    if (t == 0) *isum = 0;
-    g.sync();  // 2: the normalised vector and the absmax parts
-    float m = red[8];
-    for (int w = 1; w < (g.n >> 5); w++) m = fmaxf(m, red[8 + w]);
+    for (int st = 1; st < LPT; st <<= 1)
+#pragma unroll
+        for (int j = 0; j < LPT; j += 2 * st) a[j] = __fadd_rn(a[j], a[j + st]);
+    const float w = warp_psum(a[0]);
+    if (g.lane() == 0) S->wsum[g.warp()] = w;
+    g.sync();
+    const int P = next_pow2(d), W = 32 * LPT, nw = g.n >> 5;
+    const int nsub = P > W ? P / W : 1;  // <= 16 for the supported sizes
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) t[i] = (i < nsub && i < nw) ? S->wsum[i] : 0.0f;
+#pragma unroll
+    for (int st = 1; st < 16; st <<= 1)
+#pragma unroll
+        for (int i = 0; i < 16; i += 2 * st)
+            if (i + st < nsub) t[i] = __fadd_rn(t[i], t[i + st]);
+    return t[0];
+}
+
+// Absmax quantisation of this thread's elements (values v, K elements, the
+// vector's largest |value| at least amax_in) into the planes (bytes up to
+// Kpad).  Returns the step; sumx gets the sum of the codes.  Two group
+// barriers.
+template <int LPT>
+__device__ __forceinline__ float quant_regs(const float (&v)[LPT], int K, float amax_in, int Kpad, int8_t *planes,
+                                            VecScratch *S, int &sumx, Grp g) {
+    const int k0 = LPT * g.tid;
+    float amax = amax_in;
+#pragma unroll
+    for (int j = 0; j < LPT; j++)
+        if (k0 + j < K) amax = fmaxf(amax, fabsf(v[j]));
+    amax = warp_max_nonneg(amax);
+    if (g.lane() == 0) S->wmax[g.warp()] = amax;
+    g.sync();
+    const int nw = g.n >> 5;
+    float m = S->wmax[0];
+    for (int w = 1; w < nw; w++) m = fmaxf(m, S->wmax[w]);
     const float scale = quant_scale(m);
-    planes_words(xn, d, scale, C, xr, isum, g);
-    g.sync();  // 3: planes and the code sum
-    *sumx = *isum;
+    const int s = warp_isum(codes_to_planes<LPT>(v, k0, K, Kpad, scale, planes));
+    if (g.lane() == 0) S->wisum[g.warp()] = s;
+    g.sync();
+    int t = 0;
+    for (int w = 0; w < nw; w++) t += S->wisum[w];
+    sumx = t;
     return scale;
 }
 
-// Absmax quantisation of a K-vector of tagged words (other CTAs' output, waited
-// for by tag) into the planes, with two group barriers: the vector is staged
-// in v (shared memory) while each thread tracks its maximum.
-__device__ __forceinline__ float quant_from_tagged(const uint64_t *srcT, uint32_t tag, int K, float *v, uint4 *xr, int C,
-                                                   float *red, int *isum, int *sumx, Grp g, volatile int *abort,
-                                                   int32_t *status) {
-    float amax = 0.0f;
-    for (int k0 = 0; k0 < K; k0 += 32 * g.n) {
-        const int first = k0 + g.tid;
-        const int cnt = first < K ? min(32, (K - first + g.n - 1) / g.n) : 0;
-        float val[32];
-        fetch_tagged<32>(srcT, first < K ? first : 0, g.n, cnt, tag, val, abort, status);
-#pragma unroll
-        for (int j = 0; j < 32; j++)
-            if (j < cnt) {
-                v[first + j * g.n] = val[j];
-                amax = fmaxf(amax, fabsf(val[j]));
-            }
-    }
-    amax = warp_max(amax);
-    if (g.lane() == 0) red[g.warp()] = amax;
-    if (g.tid == 0) *isum = 0;
-    g.sync();
-    float m = red[0];
-    for (int w = 1; w < (g.n >> 5); w++) m = fmaxf(m, red[w]);
-    const float scale = quant_scale(m);
-    planes_words(v, K, scale, C, xr, isum, g);
-    g.sync();
-    *sumx = *isum;
-    return scale;
-}
-
-// RMSNorm of the d-vector of tagged words srcT (waited for by tag) into xn
-// (shared memory), staging x in xs; gains gam in global memory.  Same tree as
-// rmsnorm_row.
-__device__ __forceinline__ void rmsnorm_from_tagged(const uint64_t *srcT, uint32_t tag, const float *gam, float *xs,
-                                                    float *xn, int d, float eps, float *seg, Grp g,
-                                                    volatile int *abort, int32_t *status) {
-    stage_segments(srcT, tag, xs, d, seg, g, abort, status);
-    g.sync();
-    float ss = seg_total(seg, d, g);
+// RMSNorm of this thread's elements of x (d elements, gains gam in shared
+// memory), as rmsnorm_row: ss = pairwise sum of x^2, ss = ss/d + eps,
+// r = 1/sqrtf(ss), o = g*(r*x).  One group barrier.
+template <int LPT>
+__device__ __forceinline__ void rmsnorm_regs(const float (&x)[LPT], const float *gam, int d, float eps, float (&o)[LPT],
+                                             VecScratch *S, Grp g) {
+    float ss = sumsq_tree<LPT>(x, d, S, g);
     ss = __fdiv_rn(ss, (float)d);
     ss = __fadd_rn(ss, eps);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(ss));
-    for (int i = g.tid; i < d; i += g.n) xn[i] = __fmul_rn(__ldg(gam + i), __fmul_rn(r, xs[i]));
-    g.sync();
+    const int k0 = LPT * g.tid;
+#pragma unroll
+    for (int j = 0; j < LPT; j++) o[j] = (k0 + j < d) ? __fmul_rn(gam[k0 + j], __fmul_rn(r, x[j])) : 0.0f;
+}
+
+// RMSNorm, then absmax quantisation into the planes: the step; sumx the sum
+// of the codes.  Three group barriers.
+template <int LPT>
+__device__ __forceinline__ float norm_quant_regs(const float (&x)[LPT], const float *gam, int d, float eps, int Kpad,
+                                                 int8_t *planes, VecScratch *S, int &sumx, Grp g) {
+    float o[LPT];
+    rmsnorm_regs<LPT>(x, gam, d, eps, o, S, g);
+    return quant_regs<LPT>(o, d, 0.0f, Kpad, planes, S, sumx, g);
 }
 
 // attention_merge_one on tagged partials (pm/pS [chunk], pU [chunk][hd] of
@@ -437,49 +585,24 @@ __device__ __forceinline__ int chunk_dot(const uint4 wv, const uint4 *X, int acc
     t158_planes(wv.y, D[1]);
     t158_planes(wv.z, D[2]);
     t158_planes(wv.w, D[3]);
+    // four independent accumulator chains (integer sums: exact in any order)
+    int a0 = acc, a1 = 0, a2 = 0, a3 = 0;
 #pragma unroll
     for (int i = 0; i < 5; i++) {
         const uint4 xv = X[i];
-        acc = dp4a(D[0][i], xv.x, acc);
-        acc = dp4a(D[1][i], xv.y, acc);
-        acc = dp4a(D[2][i], xv.z, acc);
-        acc = dp4a(D[3][i], xv.w, acc);
+        a0 = dp4a(D[0][i], xv.x, a0);
+        a1 = dp4a(D[1][i], xv.y, a1);
+        a2 = dp4a(D[2][i], xv.z, a2);
+        a3 = dp4a(D[3][i], xv.w, a3);
     }
-    return acc;
+    return (a0 + a1) + (a2 + a3);
 }
 
-// Integer row sums of `rows` packed rows (pitch bytes each) at `slot` against
-// the planes xr, added into racc[row] (shared memory, zero on entry); with
-// slot2, rows rows1.. come from slot2 (two matrices of one input in one pass).  The
-// rows x C chunk dot products are spread over the whole group in units of U
-// chunks of one row (U <= 4, so that nearly every thread has work and keeps
-// several independent chunks in flight); unit k of a row takes chunks k,
-// k + upr, ... so consecutive lanes read consecutive chunks.  Partial sums
-// meet through shared-memory atomics: integer addition, exact in any order.
-__device__ __forceinline__ void t158_rows(const uint8_t *slot, int rows, int pitch, const uint4 *xr, int *racc, Grp g,
-                                          const uint8_t *slot2 = nullptr, int rows1 = 1 << 30) {
-    const int C = pitch / 16;
-    int U = (rows * C + g.n - 1) / g.n;
-    U = U < 1 ? 1 : U > 4 ? 4 : U;
-    const int upr = (C + U - 1) / U;
-    const int units = rows * upr;
-    for (int u = g.tid; u < units; u += g.n) {
-        const int r = u / upr, k = u - r * upr;
-        const uint8_t *wr = r < rows1 ? slot + (size_t)r * pitch : slot2 + (size_t)(r - rows1) * pitch;
-        int a0 = 0, a1 = 0;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int c = k + j * upr;
-            if (j < U && c < C) {
-                const int t = chunk_dot(lds128(wr + (size_t)c * 16), xr + (size_t)c * 5, 0);
-                if (j & 1)
-                    a1 += t;
-                else
-                    a0 += t;
-            }
-        }
-        atomicAdd(&racc[r], a0 + a1);
-    }
+// Sums over the two 16-lane halves of a warp (integer: exact in any order);
+// every lane of the warp must call it.  lo: the low half's sum, hi: the high half's.
+__device__ __forceinline__ void half_isums(int v, int lane, int &lo, int &hi) {
+    lo = __reduce_add_sync(0xffffffffu, lane < 16 ? v : 0);
+    hi = __reduce_add_sync(0xffffffffu, lane < 16 ? 0 : v);
 }
 
 }  // namespace qlin

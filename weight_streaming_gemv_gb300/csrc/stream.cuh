@@ -69,6 +69,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return false;
 }
 
+// The same wait with a caller-given limit.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 26); i++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && global_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+}
+
 // L2 policy for data read once (weights): evict first.
 __device__ __forceinline__ uint64_t l2_evict_first() {
     uint64_t p;

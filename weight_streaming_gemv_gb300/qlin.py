@@ -90,6 +90,8 @@ SIGNATURES = {
     "decode_step_t158": ([ctypes.POINTER(T158ModelC), _P, _P, _SZ, _P, ctypes.c_int32, _P, _P, _P], _ST),
     "decode_step_t158_launches": ([ctypes.POINTER(T158ModelC)], _I),
     "decode_step_t158_status": ([_P, _P], _ST),
+    "decode_step_t158_set_wait_limit": ([ctypes.c_uint64], None),
+    "decode_step_t158_test_withhold": ([ctypes.c_int], None),
     "decode_step_t158_sketch_workspace_size": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(T158SketchC),
                                                 ctypes.POINTER(_SZ)], _ST),
     "decode_step_t158_sketch": ([ctypes.POINTER(T158ModelC), ctypes.POINTER(T158SketchC), _P, _P, _SZ, _P,
@@ -321,6 +323,14 @@ def decode_step_t158_launches(model: T158ModelC) -> int:
 
 def decode_step_t158_status(workspace, stream=None):
     _check("decode_step_t158_status", lib().decode_step_t158_status(_ptr(workspace), _stream(stream)))
+
+
+def decode_step_t158_set_wait_limit(ns: int):
+    lib().decode_step_t158_set_wait_limit(int(ns))
+
+
+def decode_step_t158_test_withhold(layer: int):
+    lib().decode_step_t158_test_withhold(int(layer))
 
 
 def decode_step_t158_sketch_workspace_size(model: T158ModelC, sk: T158SketchC) -> int:
