@@ -502,10 +502,22 @@ def gemv_configs(dev, stream, peak):
         x = torch.from_numpy(d["x"]).to(dev)
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
         alg = N * K + 4 * M * K + 4 * M * N
-        r = _time_rotating(lambda i: qlin.qlin_w8_f32(x, wr[i * N], pitch, float(s_o), y, M, N, K), R, alg, stream)
+        # M > 1: the workspace entry point (activation terms once per call), its scratch
+        # allocated once outside the timed calls
+        nb = qlin.qlin_w8_f32_workspace_size(M, K)
+        work = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+
+        def call(wt):
+            if M == 1:
+                qlin.qlin_w8_f32(x, wt, pitch, float(s_o), y, M, N, K)
+            else:
+                qlin.qlin_w8_f32_ws(x, wt, pitch, float(s_o), y, M, N, K, work, nb)
+
+        r = _time_rotating(lambda i: call(wr[i * N]), R, alg, stream)
+        r["api"] = "qlin_w8_f32" if M == 1 else "qlin_w8_f32_ws"
         r["frac"] = round(r["gbs"] / peak, 4)
         if single:
-            us1 = _single_launch_us(lambda: qlin.qlin_w8_f32(x, w1, pitch, float(s_o), y, M, N, K), stream)
+            us1 = _single_launch_us(lambda: call(w1), stream)
             r["single_launch_us"] = round(us1, 2)
             r["single_launch_gbs"] = round(alg / (us1 * 1e-6) / 1e9, 1)
         o_us, o_n, o_thr = _oracle_us(lambda: oracle.w8_linear(d["x"], w8, s_o, K))
@@ -543,7 +555,7 @@ def gemv_configs(dev, stream, peak):
     del w1, wr
     for K, N in ((4096, 11008), (11008, 4096), (4096, 4096)):
         for M in (1, 4, 16):
-            out[f"cfg4_w8_m{M}_k{K}_n{N}"] = w8_point(3, M, K, N, False)
+            out[f"cfg4_w8_m{M}_k{K}_n{N}"] = w8_point(3, M, K, N, True)
     torch.cuda.empty_cache()
     return out
 

@@ -169,12 +169,42 @@ qlin_status qlin_t158_i8_skip(const int8_t *xq, const float *x_scale, const uint
  * input with a large outlier beside small values whose weights cancel the
  * outlier's row sums can exceed it, up to the bound.  A NaN or an infinity
  * in x makes every y NaN.
- * The kernel is launched with programmatic stream serialisation: it may start
- * while the previous kernel on the stream finishes, and waits for that
- * kernel's completion before it reads x or w8 or writes y.
+ * Two to 64 tokens run on the tensor cores (tcgen05.mma, fp32 accumulator
+ * in tensor memory): each int8 weight is a bf16 value exactly and each x
+ * enters as three bf16 terms hi + mid + lo that hold all of its 24
+ * significant bits, so every product is exact and the error is the fp32
+ * accumulation's: |y[n] - exact| <= about K 2^-24 w_scale sum_k |x[k]
+ * w8[n][k]| in the worst case, far less on random signs.  A NaN or an
+ * infinity in x, or |x| above the largest bf16 (about 3.39e38), makes the
+ * outputs of its token NaN.
+ * The kernels are launched with programmatic stream serialisation: they may
+ * start while the previous kernel on the stream finishes.  The weights are
+ * taken to be read-only inputs: the M >= 2 kernels start their weight copies
+ * at once, and wait for the previous kernel's completion before they read x
+ * or write y (the one-token kernel waits before it reads anything).
  * ====================================================================== */
 qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float w_scale, float *y, int M, int N,
                         int K, qlin_stream_t stream);
+
+/* qlin_w8_f32 with caller scratch for 2 <= M <= 64: the activations are
+ * turned into the tensor cores' operand once per call (one small launch per
+ * token) instead of inside the product for every 128 weight rows, and the
+ * weights enter the product as fp16.  fp16's exponent range is narrow, so
+ * each token's x is scaled by a power of two, x' = x 2^(14-e) with max|x| <
+ * 2^e, split into three fp16 terms (exact down to fp16's subnormal step,
+ * i.e. every x to within 2^(e-39)), and the output is multiplied back by
+ * 2^(e-14): the error is the fp32 accumulation's, as for qlin_w8_f32.  A
+ * NaN or an infinity in x makes its token's outputs NaN.
+ * workspace: device, 16-byte aligned, at least qlin_w8_f32_workspace_size(M,
+ * K) bytes (0 for M = 1, where NULL is accepted and the call is
+ * qlin_w8_f32's), owned by the caller and overwritten; calls sharing a
+ * workspace must not overlap on the GPU (calls on one stream do not).  A
+ * smaller or misaligned workspace is QLIN_ERR_INVALID_ARG.  Other arguments
+ * and ranges as qlin_w8_f32.  qlin_w8_f32_workspace_size returns 0 for M
+ * outside 2..64 or K < 1. */
+size_t qlin_w8_f32_workspace_size(int M, int K);
+qlin_status qlin_w8_f32_ws(const float *x, const int8_t *w8, int64_t w_pitch, float w_scale, float *y, int M, int N,
+                           int K, void *workspace, size_t workspace_bytes, qlin_stream_t stream);
 
 /* ========================================================================
  * W8 with one scale per group of G weights ([gemma.cpp tour] "The compression

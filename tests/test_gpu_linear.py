@@ -364,6 +364,103 @@ def test_w8_linear(dev, M, K, N):
     assert max_abs_rel(host(y), y_o) <= 1e-5
 
 
+@pytest.mark.parametrize("M,K,N,x_offset,w_pitch", [
+    (2, 4096, 4096, 0, None),      # token capacity 4 (MMA N = 16)
+    (5, 1000, 300, 0, None),       # capacity 8, K and N ragged against the 128 x 128 weight box
+    (8, 11008, 4096, 0, None),     # split K over a cluster of 8
+    (13, 4096, 11008, 0, None),    # capacity 16, split K over a cluster of 3
+    (17, 2048, 640, 0, None),      # two token tiles
+    (33, 129, 257, 0, None),       # three token tiles, one element past a stage, one row past a tile
+    (6, 301, 77, 1, None),         # x at an odd float offset, K % 4 != 0: element-wise copies
+    (4, 512, 200, 3, 1024),        # x unaligned, row pitch far past K
+])
+def test_w8_tensor_core_shapes(dev, M, K, N, x_offset, w_pitch):
+    """The tensor-core path (2 <= M <= 64): token tiles of capacity 4, 8 and 16,
+    split K, ragged K and N, unaligned activations and a wide row pitch."""
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    d = synth.w8_gemv(31, M, K, N)
+    q_o, s_o = oracle.w8_quantize(d["w"])
+    y_o = oracle.w8_linear(d["x"], q_o, s_o)
+    pitch = w_pitch or (K + 15) // 16 * 16
+    w8 = np.full((N, pitch), 0x55, np.int8)  # bytes past K are not read as weights
+    w8[:, :K] = q_o
+    buf = torch.zeros(M * K + x_offset, dtype=torch.float32, device=dev)
+    buf[x_offset:] = to_dev(d["x"].reshape(-1), dev)
+    w8d = to_dev(w8, dev)
+    y = _empty((M, N), torch.float32, dev)
+    qlin.qlin_w8_f32(buf[x_offset:], w8d, pitch, float(s_o), y, M, N, K)
+    assert max_abs_rel(host(y), y_o) <= 1e-5
+    # the same call again: split-K sums in rank order, so the result repeats bit for bit
+    y2 = _empty((M, N), torch.float32, dev)
+    qlin.qlin_w8_f32(buf[x_offset:], w8d, pitch, float(s_o), y2, M, N, K)
+    np.testing.assert_array_equal(host(y2), host(y))
+    # the workspace path (activation terms once per call, fp16 operands), twice on one workspace
+    nb = qlin.qlin_w8_f32_workspace_size(M, K)
+    assert nb > 0
+    work = _empty((nb,), torch.uint8, dev)
+    y3 = _empty((M, N), torch.float32, dev)
+    for _ in range(2):
+        qlin.qlin_w8_f32_ws(buf[x_offset:], w8d, pitch, float(s_o), y3, M, N, K, work, nb)
+    assert max_abs_rel(host(y3), y_o) <= 1e-5
+
+
+def test_w8_tensor_core_exact_terms(dev):
+    """x values of 24 significant bits over a wide exponent range: the three
+    bf16 terms carry them exactly, so with small-integer weights every
+    product is exact and the result stays at fp32 accumulation error."""
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    M, K, N = 16, 2048, 256
+    rng = np.random.default_rng(5)
+    mant = rng.integers(1 << 23, 1 << 24, size=(M, K)).astype(np.float64)
+    expo = rng.integers(-30, 10, size=(M, K))
+    sign = rng.choice([-1.0, 1.0], size=(M, K))
+    x = (sign * mant * np.exp2(expo - 23)).astype(np.float32)
+    q = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    xd, qd = to_dev(x, dev), to_dev(q, dev)
+    exact = x.astype(np.float64) @ q.astype(np.float64).T
+    bound = 2.0 ** -22 * (np.abs(x).astype(np.float64) @ np.abs(q).astype(np.float64).T) + 1e-30
+    y = _empty((M, N), torch.float32, dev)
+    qlin.qlin_w8_f32(xd, qd, K, 1.0, y, M, N, K)
+    assert (np.abs(host(y) - exact) <= bound).all()
+    nb = qlin.qlin_w8_f32_workspace_size(M, K)
+    work = _empty((nb,), torch.uint8, dev)
+    qlin.qlin_w8_f32_ws(xd, qd, K, 1.0, y, M, N, K, work, nb)
+    assert (np.abs(host(y) - exact) <= bound).all()
+
+
+@pytest.mark.parametrize("ws", [False, True])
+def test_w8_tensor_core_nonfinite_token(dev, ws):
+    """An infinity or a NaN in one token's x makes that token's outputs NaN and
+    leaves the other tokens' outputs as they are."""
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    M, K, N = 5, 700, 300
+    d = synth.w8_gemv(33, M, K, N)
+    q_o, s_o = oracle.w8_quantize(d["w"])
+    pitch = (K + 15) // 16 * 16
+    w8 = np.zeros((N, pitch), np.int8)
+    w8[:, :K] = q_o
+    x = d["x"].copy()
+    x[1, 17] = np.inf
+    x[3, 650] = np.nan
+    y_o = oracle.w8_linear(np.where(np.isfinite(x), x, 0.0).astype(np.float32), q_o, s_o)
+    y = _empty((M, N), torch.float32, dev)
+    if ws:
+        nb = qlin.qlin_w8_f32_workspace_size(M, K)
+        qlin.qlin_w8_f32_ws(to_dev(x, dev), to_dev(w8, dev), pitch, float(s_o), y, M, N, K, _empty((nb,), torch.uint8, dev), nb)
+    else:
+        qlin.qlin_w8_f32(to_dev(x, dev), to_dev(w8, dev), pitch, float(s_o), y, M, N, K)
+    yh = host(y)
+    assert np.isnan(yh[[1, 3]]).all()
+    ok = [0, 2, 4]
+    assert max_abs_rel(yh[ok], y_o[ok]) <= 1e-5
+
+
 # ---------------------------------------------------------------- W8 with group scales
 def _w8g_case(dev, M, K, N, G, seed, x_offset=0, w_pitch=None):
     import torch

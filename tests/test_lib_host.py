@@ -98,6 +98,14 @@ def test_device_calls_validate_before_launch():
     assert L.qlin_t158_i8(8, 16, 32, 32, 1.0, 64, None, 5000, 8, 100, None) == 2  # M too large
     assert L.qlin_w8_f32(16, 32, 8, 1.0, 64, 1, 1, 16, None) == 1  # pitch < K
     assert L.qlin_w8_f32(16, 32, 16, 1.0, 64, 65, 1, 16, None) == 2  # M > 64
+    # the workspace variant: sizes and the workspace checks come before any GPU work
+    assert L.qlin_w8_f32_workspace_size(1, 4096) == 0
+    assert L.qlin_w8_f32_workspace_size(65, 4096) == 0
+    assert L.qlin_w8_f32_workspace_size(16, 4096) >= 16 * 4096 * 6
+    nb = L.qlin_w8_f32_workspace_size(4, 300)
+    assert L.qlin_w8_f32_ws(16, 32, 16, 1.0, 64, 4, 1, 16, None, nb, None) == 1  # no workspace
+    assert L.qlin_w8_f32_ws(16, 32, 16, 1.0, 64, 4, 1, 16, 48, 0, None) == 1  # too small
+    assert L.qlin_w8_f32_ws(16, 32, 16, 1.0, 64, 65, 1, 16, 48, 1 << 20, None) == 2  # M > 64
     assert L.qlin_quant_i8(None, 16, 16, 1, 1, None) == 1
     assert L.qlin_attention_decode(16, 16, 16, 0, 4, 1, 24, 16, 16, 1 << 20, None) == 2  # head_dim not pow2
     assert "head_dim" in qlin.lib().qlin_last_error().decode()

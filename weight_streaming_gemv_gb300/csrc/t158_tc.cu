@@ -50,6 +50,7 @@
 #include "common.cuh"
 #include "decode_ops.cuh"
 #include "stream.cuh"
+#include "tcgen05.cuh"
 
 namespace qlin {
 
@@ -125,42 +126,10 @@ __device__ __forceinline__ uint32_t tm_idesc(int T) {
     return (1u << 4) | ((uint32_t)(T >> 3) << 17) | ((uint32_t)(kTmRows >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D (tensor memory) (+)= A (tensor memory) x B (shared memory)
-__device__ __forceinline__ void tm_mma(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
 
-// four consecutive 32-bit columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tm_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
-                 "r"(c), "r"(d)
-                 : "memory");
-}
-__device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 16 consecutive accumulator columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tm_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 
 // Byte offset of 16-byte chunk kc of row r in an activation tile.
 __device__ __forceinline__ int tc_off(int r, int kc) { return (r >> 3) * kTcSBO + kc * 128 + (r & 7) * 16; }
@@ -215,15 +184,6 @@ __device__ __forceinline__ void tm_put_w(uint32_t ta, uint2 v, int hw) {
     }
 }
 
-// 16 (8) bytes global -> shared, the bytes past src_bytes zero.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async8(void *dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
 // 1-D bulk copy global -> shared completing on `bar`; bytes and both addresses
 // multiples of 16.
 __device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -231,11 +191,6 @@ __device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint3
                      smem_addr(dst)),
                  "l"(src), "r"(bytes), "r"(smem_addr(bar))
                  : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_pending() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Unit h of token m at step s loaded directly (any alignment; zero past K and
@@ -256,23 +211,6 @@ __device__ __forceinline__ void tm_load_act(uint32_t (&in)[12], const int8_t *__
     }
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// float4 at a shared address of CTA `rank` of this cluster
-__device__ __forceinline__ float4 ld_peer_f4(const void *local, uint32_t rank) {
-    uint32_t a;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(local)), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a)
-                 : "memory");
-    return v;
-}
 
 // One token row of one step into an activation tile: in[] holds the 80 bytes
 // (v + 128 for each value v); chunk kc of row r is K' 8 kc .. 8 kc + 7.

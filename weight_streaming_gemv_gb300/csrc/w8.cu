@@ -438,6 +438,14 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
     }
 }
 
+// the tensor-core paths for 2 <= M <= 64 (w8_tc.cu): activations split in
+// the product kernel, or once per call into a workspace
+qlin_status w8_linear_tensor_cores(const float *x, const int8_t *w8, int64_t pitch, float s, float *y, int M, int N,
+                                   int K, cudaStream_t st);
+size_t w8_tc_workspace_bytes(int M, int K);
+qlin_status w8_linear_tensor_cores_ws(const float *x, const int8_t *w8, int64_t pitch, float s, float *y, int M,
+                                      int N, int K, void *work, cudaStream_t st);
+
 template <int R, int MT>
 static qlin_status launch_w8(const float *x, const int8_t *w, int64_t pitch, float s, float *y, int M, int N, int K,
                              cudaStream_t st, const float *scales = nullptr, int64_t s_pitch = 0, int G = 0) {
@@ -492,7 +500,6 @@ qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float
                  "qlin_w8_f32: misaligned pointer");
     QLIN_REQUIRE(M <= 64, QLIN_ERR_UNSUPPORTED, "qlin_w8_f32: M=%d > 64", M);
     cudaStream_t st = (cudaStream_t)stream;
-    const size_t tile8_smem = (size_t)8 * ((K + 15) / 16) * 16 * sizeof(float);
     if (M == 1 && w_pitch <= 16 * 32 * qlin::kW8Warps * qlin::kW8JMax) {
         const qlin::W8Smem L = qlin::w8_stream_layout(w_pitch, qlin::max_smem_optin());
         if (L.tr >= 1) {
@@ -514,9 +521,26 @@ qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float
         }
     }
     if (M == 1) return qlin::launch_w8<4, 1>(x, w8, w_pitch, w_scale, y, M, N, K, st);
-    if (M <= 4 || (int)tile8_smem > qlin::max_smem_optin())
-        return qlin::launch_w8<2, 4>(x, w8, w_pitch, w_scale, y, M, N, K, st);
-    return qlin::launch_w8<2, 8>(x, w8, w_pitch, w_scale, y, M, N, K, st);
+    return qlin::w8_linear_tensor_cores(x, w8, w_pitch, w_scale, y, M, N, K, st);
+}
+
+size_t qlin_w8_f32_workspace_size(int M, int K) { return qlin::w8_tc_workspace_bytes(M, K); }
+
+qlin_status qlin_w8_f32_ws(const float *x, const int8_t *w8, int64_t w_pitch, float w_scale, float *y, int M, int N,
+                           int K, void *workspace, size_t workspace_bytes, qlin_stream_t stream) {
+    qlin::clear_error();
+    QLIN_REQUIRE(x && w8 && y, QLIN_ERR_INVALID_ARG, "qlin_w8_f32_ws: null pointer");
+    QLIN_REQUIRE(M >= 1 && N >= 1 && K >= 1, QLIN_ERR_INVALID_ARG, "qlin_w8_f32_ws: M=%d N=%d K=%d", M, N, K);
+    QLIN_REQUIRE(w_pitch >= K && w_pitch % 16 == 0, QLIN_ERR_INVALID_ARG, "qlin_w8_f32_ws: w_pitch %lld",
+                 (long long)w_pitch);
+    QLIN_REQUIRE(qlin::aligned16(w8) && qlin::aligned4(x) && qlin::aligned4(y), QLIN_ERR_INVALID_ARG,
+                 "qlin_w8_f32_ws: misaligned pointer");
+    QLIN_REQUIRE(M <= 64, QLIN_ERR_UNSUPPORTED, "qlin_w8_f32_ws: M=%d > 64", M);
+    if (M == 1) return qlin_w8_f32(x, w8, w_pitch, w_scale, y, M, N, K, stream);
+    const size_t need = qlin::w8_tc_workspace_bytes(M, K);
+    QLIN_REQUIRE(workspace_bytes >= need && workspace && qlin::aligned16(workspace), QLIN_ERR_INVALID_ARG,
+                 "qlin_w8_f32_ws: workspace %zu < %zu bytes, null or not 16-byte aligned", workspace_bytes, need);
+    return qlin::w8_linear_tensor_cores_ws(x, w8, w_pitch, w_scale, y, M, N, K, workspace, (cudaStream_t)stream);
 }
 
 qlin_status qlin_w8g_quantize(const float *w, int64_t N, int64_t K, int G, int8_t *w8, int64_t w_pitch, float *scales,

@@ -68,6 +68,8 @@ SIGNATURES = {
     "qlin_t158_i8_workspace_size": ([_I, _I], _SZ),
     "qlin_t158_i8_ws": ([_P, _P, _P, _I64, _F, _P, _P, _I, _I, _I, _P, _SZ, _P], _ST),
     "qlin_w8_f32": ([_P, _P, _I64, _F, _P, _I, _I, _I, _P], _ST),
+    "qlin_w8_f32_workspace_size": ([_I, _I], _SZ),
+    "qlin_w8_f32_ws": ([_P, _P, _I64, _F, _P, _I, _I, _I, _P, _SZ, _P], _ST),
     "qlin_w8g_quantize": ([_P, _I64, _I64, _I, _P, _I64, _P, _I64, _P], _ST),
     "qlin_w8g_f32": ([_P, _P, _I64, _P, _I64, _I, _P, _I, _I, _I, _P], _ST),
     "qlin_embed_bf16": ([_P, _I, _I, _P, _P, _P, _P], _ST),
@@ -207,6 +209,15 @@ def qlin_t158_i8_ws(xq, x_scale, w_packed, w_pitch, w_scale, y, acc, M, N, K, wo
 def qlin_w8_f32(x, w8, w_pitch, w_scale, y, M, N, K, stream=None):
     _check("qlin_w8_f32", lib().qlin_w8_f32(_ptr(x), _ptr(w8), w_pitch, float(w_scale), _ptr(y), M, N, K,
                                             _stream(stream)))
+
+
+def qlin_w8_f32_workspace_size(M, K):
+    return int(lib().qlin_w8_f32_workspace_size(M, K))
+
+
+def qlin_w8_f32_ws(x, w8, w_pitch, w_scale, y, M, N, K, workspace, workspace_bytes, stream=None):
+    _check("qlin_w8_f32_ws", lib().qlin_w8_f32_ws(_ptr(x), _ptr(w8), w_pitch, float(w_scale), _ptr(y), M, N, K,
+                                                  _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def qlin_w8g_quantize(w, N, K, G, w8, w_pitch, scales, s_pitch, stream=None):
