@@ -442,7 +442,9 @@ def qlin_launches(gpu, U):
 
 def _single_launch_us(fn, stream, n=25):
     """One call alone: an L2 flush (a 256 MB write), then CUDA events around the call on the
-    launching stream; the median of n such calls, in microseconds."""
+    launching stream; the median of n such calls, in microseconds.  A device-side sleep after
+    the flush keeps the stream busy while the host queues the events and the call, so the
+    interval holds the call's device time, not the host's launch latency."""
     import torch
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=torch.device("cuda", torch.cuda.current_device()))
@@ -451,6 +453,7 @@ def _single_launch_us(fn, stream, n=25):
     ts = []
     for it in range(n):
         flush.fill_(it & 255)
+        torch.cuda._sleep(200000)  # about 0.1 ms at 2 GHz
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
         fn()

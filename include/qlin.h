@@ -111,7 +111,12 @@ qlin_status qlin_quant_i8(const float *x, int8_t *xq, float *x_scale, int M, int
  * codes and trits are fp16 integers and every partial sum stays below
  * 127 K < 2^24): the same acc and y, bit for bit.  Below 8 tokens the
  * CUDA-core kernel runs, except for rows too long for its activation planes
- * in shared memory, which take the tensor-core path as well.
+ * in shared memory, which take the tensor-core path as well.  The CUDA-core
+ * kernel is launched with programmatic stream serialisation: it may start
+ * while the previous kernel on the stream finishes, requests its first
+ * weight chunks at once (the packed weights are taken to be read-only
+ * inputs) and waits for that kernel's completion before it reads xq,
+ * x_scale or the weight scale or writes y and acc.
  * ====================================================================== */
 qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *w_packed, int64_t w_pitch,
                          float w_scale, float *y, int32_t *acc, int M, int N, int K, qlin_stream_t stream);
@@ -179,9 +184,9 @@ qlin_status qlin_t158_i8_skip(const int8_t *xq, const float *x_scale, const uint
  * outputs of its token NaN.
  * The kernels are launched with programmatic stream serialisation: they may
  * start while the previous kernel on the stream finishes.  The weights are
- * taken to be read-only inputs: the M >= 2 kernels start their weight copies
- * at once, and wait for the previous kernel's completion before they read x
- * or write y (the one-token kernel waits before it reads anything).
+ * taken to be read-only inputs: the kernels start their weight copies at
+ * once, and wait for the previous kernel's completion before they read x or
+ * write y.
  * ====================================================================== */
 qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float w_scale, float *y, int M, int N,
                         int K, qlin_stream_t stream);

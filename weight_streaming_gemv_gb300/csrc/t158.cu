@@ -126,12 +126,19 @@ __global__ void __launch_bounds__(256) t158_gemv_kernel(const int8_t *__restrict
     const int warps = blockDim.x >> 5;
     const int64_t gwarp = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * warps;
+    // Programmatic dependent launch: the next kernel on the stream may start
+    // its set-up now.  The packed weights are read-only inputs, so the first
+    // chunks are requested at once; the activations, their scales and the
+    // weight scale are read, and y written, only after the previous kernel
+    // on the stream has completed (griddepcontrol.wait).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     uint4 nxt[R];  // the next chunk of each of the warp's R row slots
 #pragma unroll
     for (int r = 0; r < R; r++) {
         const int64_t row = gwarp * ROWS + r * RPS + rsub;
         nxt[r] = (row < N && sub < C) ? ld_stream_v4(w + row * pitch + (int64_t)sub * 16) : make_uint4(0, 0, 0, 0);
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const float wsv = ws_ptr ? *ws_ptr : ws;
     for (int mm = 0; mm < MT; mm++) {
@@ -259,8 +266,17 @@ static qlin_status launch_t158(const int8_t *xq, const float *xs, const uint8_t 
     // (the grid-stride loop takes the rest)
     const int64_t cap = (int64_t)sm_count() * std::min(per_sm, MT == 1 ? 3 : 2);
     if (blocks > cap) blocks = cap;
-    dim3 grid((unsigned)blocks, (unsigned)((M + MT - 1) / MT));
-    kern<<<grid, 256, smem, st>>>(xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, (unsigned)((M + MT - 1) / MT));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    QLIN_CUDA(cudaLaunchKernelEx(&cfg, kern, xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K));
     QLIN_LAUNCHED("t158_gemv_kernel");
     return QLIN_OK;
 }

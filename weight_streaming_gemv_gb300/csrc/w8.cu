@@ -243,13 +243,11 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
     const int64_t r0 = (int64_t)N * blockIdx.x / gridDim.x, r1 = (int64_t)N * (blockIdx.x + 1) / gridDim.x;
     const int ntiles = (int)((r1 - r0 + TR - 1) / TR);
     // Programmatic dependent launch: the next kernel on the stream may start its
-    // own set-up now; this one waits for the previous kernel to complete (and its
-    // writes to be visible) before it reads x or the weights or writes y.
+    // own set-up now.  The weights (and group scales) are read-only inputs, so
+    // the first stages of their stream go out at once; this kernel waits for
+    // the previous one to complete (and its writes to be visible) before it
+    // reads x or writes y.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (threadIdx.x == 0) ring->init(kW8Warps);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // the first tile of the weight stream goes out at once, the other stages after
-    // the x loads below (so that those few loads do not queue behind the stream)
     const uint64_t pol = l2_evict_first();
     auto issue = [&](int t) {
         const int st = t % kW8Stages;
@@ -260,9 +258,12 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
         bulk_g2s(slots + (size_t)st * L.slot, w + row * pitch, bytes, &ring->full[st], pol);
         if (GROUPED) bulk_g2s(slots + L.soff + (size_t)st * L.sslot, scales + row * s_pitch, sbytes, &ring->full[st], pol);
     };
-    if (threadIdx.x == 0 && ntiles > 0) issue(0);
-    // consumers: load this lane's x slice first, so that these few loads do not
-    // queue behind the weight stream
+    if (threadIdx.x == 0) {
+        ring->init(kW8Warps);
+        for (int t = 0; t < min(ntiles, kW8Stages); t++) issue(t);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // consumers: this lane's x slice
     const int cw = warp - 1, p = cw % KS, grp = cw / KS;
     const int ca = C * p / KS, cb = C * (p + 1) / KS;
     // the slice straight from global memory, every load in flight at once (16-byte
@@ -294,10 +295,8 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
             }
         }
     }
-    // the loads are in flight; one barrier, then the weight stream starts
+    // the loads are in flight; one barrier (the ring is initialised), then the rest of the stream
     __syncthreads();
-    if (threadIdx.x == 0)
-        for (int t = 1; t < min(ntiles, kW8Stages); t++) issue(t);
 
     if (warp == 0) {
         if (lane != 0) return;
