@@ -76,7 +76,9 @@ constexpr int kWtXHalf = kWtMaxTT * kWtChunks * 16;              // raw activati
 constexpr int kWtXStage = 2 * kWtXHalf;                          // both halves of every unit of a stage
 constexpr int kWtWStage = kWtRows * kWtKS;                       // 16 KB
 constexpr int kWtPStride = kWtRows + 4;                          // floats per token of a partial tile
-constexpr int kWtTermThreads = 512;                              // w8_terms_kernel
+constexpr int kWtTermThreads = 1024;                             // w8_terms_kernel: threads per CTA,
+constexpr int kWtTermChunks = 2;                                 // chunks a thread holds in registers,
+constexpr int kWtTermMaxP = 8;                                   // CTAs per token (a cluster) at most
 constexpr uint32_t kWtCols = 256;   // tensor memory: accumulators at column 0, the A slots from kWtACol
 constexpr uint32_t kWtACol = 64;    // A slot s: columns kWtACol + 64 s .. + 63 (128 16-bit values per lane)
 static_assert(kWtMaxTT * kWtChunks <= kWtUnits * kWtXThreads, "splitter units");
@@ -182,32 +184,85 @@ __device__ __forceinline__ void sts128(void *p, uint32_t a, uint32_t b, uint32_t
                  : "memory");
 }
 
-// One block per token m (workspace path): the largest |x| of the row, the
-// power of two, and the three fp16 terms of every x' into the B images of the
-// token's tile (rows p PS + t of each stage's image, t = m % TT; zeros past
-// K); tscale[m] = 2^(e - 14) as two factors.  A row holding a NaN or an
+// Workspace path: a cluster of P CTAs per token m (cluster rank = the CTA's
+// slice of K, whole 8-activation chunks) finds the largest |x| of the row
+// (each CTA over its slice, then over the cluster through distributed shared
+// memory), takes the power of two and writes the three fp16 terms of every
+// x' into the B images of the token's tile (rows p PS + t of each stage's
+// image, t = m % TT; zeros past K); tscale[m] = 2^(e - 14) as two factors.  A
+// thread holds up to kWtTermChunks chunks in registers between the two
+// steps (longer slices read their chunks again).  A row holding a NaN or an
 // infinity gets NaN terms and a NaN scale.
 template <int PS>
 __global__ void __launch_bounds__(kWtTermThreads) w8_terms_kernel(const float *__restrict__ x, int M, int K, int TT,
                                                                   int nstg, uint8_t *__restrict__ imgs,
                                                                   float2 *__restrict__ tscale) {
     __shared__ uint32_t red[kWtTermThreads / 32];
+    __shared__ uint32_t cta_max;
     constexpr int IMG = wt_img_bytes(PS);
-    const int m = blockIdx.x, tt = m / TT, t = m % TT;
+    const int P = (int)gridDim.x, rank = (int)blockIdx.x;  // the cluster spans x
+    const int m = blockIdx.y, tt = m / TT, t = m % TT;
     const int tid = threadIdx.x;
+    const int nchunks = nstg * kWtChunks;  // up to the end of the last stage (zeros past K)
+    const int c_lo = (int)((int64_t)nchunks * rank / P), c_hi = (int)((int64_t)nchunks * (rank + 1) / P);
     // the product kernel after this one may start its weight copies; the
     // workspace may still be read by the product before this one
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const float *row = x + (int64_t)m * K;
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    auto load = [&](int c, float (&v)[8]) {
+        const int k0 = 8 * c;
+        if (vec && k0 + 8 <= K) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(row + k0));
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(row + k0 + 4));
+            v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; q++) v[q] = k0 + q < K ? row[k0 + q] : 0.0f;
+        }
+    };
+    float v[kWtTermChunks][8];
     uint32_t mb = 0;  // largest magnitude bits (NaN and infinity have all exponent bits set)
-    for (int k = tid; k < K; k += kWtTermThreads) mb = max(mb, __float_as_uint(row[k]) & 0x7fffffffu);
+#pragma unroll
+    for (int j = 0; j < kWtTermChunks; j++) {
+        const int c = c_lo + tid + kWtTermThreads * j;
+        if (c < c_hi) {
+            load(c, v[j]);
+#pragma unroll
+            for (int q = 0; q < 8; q++) mb = max(mb, __float_as_uint(v[j][q]) & 0x7fffffffu);
+        }
+    }
+    for (int c = c_lo + tid + kWtTermThreads * kWtTermChunks; c < c_hi; c += kWtTermThreads) {
+        float u[8];
+        load(c, u);
+#pragma unroll
+        for (int q = 0; q < 8; q++) mb = max(mb, __float_as_uint(u[q]) & 0x7fffffffu);
+    }
     mb = __reduce_max_sync(0xffffffffu, mb);
     if ((tid & 31) == 0) red[tid >> 5] = mb;
     __syncthreads();
-    mb = 0;
+    if (tid == 0) {
+        uint32_t b = 0;
 #pragma unroll
-    for (int w = 0; w < kWtTermThreads / 32; w++) mb = max(mb, red[w]);
+        for (int w = 0; w < kWtTermThreads / 32; w++) b = max(b, red[w]);
+        cta_max = b;
+    }
+    if (P == 1) {
+        __syncthreads();
+        mb = cta_max;
+    } else {
+        cluster_sync();  // every CTA's maximum is written
+        mb = 0;
+        for (int q = 0; q < P; q++) {
+            uint32_t a;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(&cta_max)), "r"(q));
+            uint32_t b;
+            asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(b) : "r"(a) : "memory");
+            mb = max(mb, b);
+        }
+        cluster_sync();  // no CTA leaves while another still reads its maximum
+    }
     const bool finite = mb < 0x7f800000u;
     int e = 0;  // max|x| < 2^e
     if (finite && mb != 0) {
@@ -222,26 +277,15 @@ __global__ void __launch_bounds__(kWtTermThreads) w8_terms_kernel(const float *_
     float u1, u2, d1, d2;
     pow2_pair(14 - e, u1, u2);
     pow2_pair(e - 14, d1, d2);
-    if (tid == 0)
+    if (rank == 0 && tid == 0)
         tscale[m] = finite ? make_float2(d1, d2) : make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
-    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
     uint8_t *const base = imgs + (int64_t)tt * nstg * IMG;
-    for (int c = tid; c < nstg * kWtChunks; c += kWtTermThreads) {
-        const int k0 = 8 * c;
-        float v[8];
-        if (vec && k0 + 8 <= K) {
-            const float4 a = __ldg(reinterpret_cast<const float4 *>(row + k0));
-            const float4 b = __ldg(reinterpret_cast<const float4 *>(row + k0 + 4));
-            v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; q++) v[q] = k0 + q < K ? row[k0 + q] : 0.0f;
-        }
+    auto emit = [&](int c, const float (&u)[8]) {
         uint32_t th[4], tm[4], tl[4];
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             if (finite) {
-                wt_split_f16(__fmul_rn(__fmul_rn(v[2 * q], u1), u2), __fmul_rn(__fmul_rn(v[2 * q + 1], u1), u2), th[q],
+                wt_split_f16(__fmul_rn(__fmul_rn(u[2 * q], u1), u2), __fmul_rn(__fmul_rn(u[2 * q + 1], u1), u2), th[q],
                              tm[q], tl[q]);
             } else {
                 th[q] = tm[q] = tl[q] = 0x7e007e00u;  // fp16 NaN
@@ -252,6 +296,16 @@ __global__ void __launch_bounds__(kWtTermThreads) w8_terms_kernel(const float *_
         *reinterpret_cast<uint4 *>(img + wt_boff(t, kc)) = make_uint4(th[0], th[1], th[2], th[3]);
         *reinterpret_cast<uint4 *>(img + wt_boff(PS + t, kc)) = make_uint4(tm[0], tm[1], tm[2], tm[3]);
         *reinterpret_cast<uint4 *>(img + wt_boff(2 * PS + t, kc)) = make_uint4(tl[0], tl[1], tl[2], tl[3]);
+    };
+#pragma unroll
+    for (int j = 0; j < kWtTermChunks; j++) {
+        const int c = c_lo + tid + kWtTermThreads * j;
+        if (c < c_hi) emit(c, v[j]);
+    }
+    for (int c = c_lo + tid + kWtTermThreads * kWtTermChunks; c < c_hi; c += kWtTermThreads) {
+        float u[8];
+        load(c, u);
+        emit(c, u);
     }
 }
 
@@ -699,15 +753,23 @@ qlin_status launch_wt(const CUtensorMap &map, const float *x, const uint8_t *img
 
 template <int PS>
 qlin_status launch_terms(const float *x, int M, int K, int TT, uint8_t *imgs, float2 *tscale, cudaStream_t st) {
+    // CTAs per token: enough that each thread holds its chunks in registers
+    const int nchunks = (K + kWtKS - 1) / kWtKS * kWtChunks;
+    int P = (nchunks + kWtTermThreads * kWtTermChunks - 1) / (kWtTermThreads * kWtTermChunks);
+    P = P < 1 ? 1 : P > kWtTermMaxP ? kWtTermMaxP : P;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)M);
+    cfg.gridDim = dim3((unsigned)P, (unsigned)M);
     cfg.blockDim = dim3(kWtTermThreads);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)P;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = P > 1 ? 2 : 1;  // one CTA per token (K <= 16384) needs no cluster
     QLIN_CUDA(cudaLaunchKernelEx(&cfg, w8_terms_kernel<PS>, x, M, K, TT, (K + kWtKS - 1) / kWtKS, imgs, tscale));
     QLIN_LAUNCHED("w8_terms_kernel");
     return QLIN_OK;
