@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--workload", choices=["decode"], default="decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--kernel", choices=["sketch_head", "decode_steps", "lanes_steps", "t158_linears", "t158_calls",
-                                        "t158_gemv"],
+                                        "t158_gemv", "w8_calls"],
                    default=None,
                    help="time one kernel alone on its full-size synthetic inputs (for profiling); no JSON bench line")
     return p.parse_args()
@@ -853,6 +853,26 @@ def kernel_only(name):
             y = torch.empty((1, N), dtype=torch.float32, device=dev)
             for _ in range(5):
                 qlin.qlin_t158_i8(xq, xs, w, pitch, d["w_scale"], y, None, 1, N, K)
+        torch.cuda.synchronize()
+        print(json.dumps({"kernel": name}))
+        return 0
+    if name == "w8_calls":
+        # four calls of qlin_w8_f32_ws, then four of qlin_w8_f32, 16 tokens through 4096 -> 11008
+        # (config-4 inputs, quantised on the GPU): a short launch list for the profiler
+        M, K, N = 16, 4096, 11008
+        d = synth.w8_gemv(3, M, K, N)
+        w8 = torch.empty((N, K), dtype=torch.int8, device=dev)
+        sc = torch.empty(1, dtype=torch.float32, device=dev)
+        qlin.qlin_w8_quantize(torch.from_numpy(d["w"]).to(dev), N, K, w8, K, sc)
+        s = float(sc.item())
+        x = torch.from_numpy(d["x"]).to(dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        nb = qlin.qlin_w8_f32_workspace_size(M, K)
+        work = torch.empty(nb, dtype=torch.uint8, device=dev)
+        for _ in range(4):
+            qlin.qlin_w8_f32_ws(x, w8, K, s, y, M, N, K, work, nb)
+        for _ in range(4):
+            qlin.qlin_w8_f32(x, w8, K, s, y, M, N, K)
         torch.cuda.synchronize()
         print(json.dumps({"kernel": name}))
         return 0

@@ -373,6 +373,7 @@ def test_w8_linear(dev, M, K, N):
     (33, 129, 257, 0, None),       # three token tiles, one element past a stage, one row past a tile
     (6, 301, 77, 1, None),         # x at an odd float offset, K % 4 != 0: element-wise copies
     (4, 512, 200, 3, 1024),        # x unaligned, row pitch far past K
+    (3, 20000, 130, 0, None),      # long rows: a cluster of activation-term CTAs per token
 ])
 def test_w8_tensor_core_shapes(dev, M, K, N, x_offset, w_pitch):
     """The tensor-core path (2 <= M <= 64): token tiles of capacity 4, 8 and 16,
