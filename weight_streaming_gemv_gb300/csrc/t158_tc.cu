@@ -67,6 +67,7 @@ constexpr int kTmUnit = 48;               // raw bytes of one activation unit (t
 constexpr int kTmCtl = 2048;              // bytes of the control block at the start of shared memory
 constexpr int kTmPStride = kTmRows + 4;   // floats per token of a partial tile (split K)
 constexpr int kTmMaxSplit = 8;            // CTAs of a cluster that split K
+constexpr int kTmEarlyMaxItems = 16384;   // tile-conversion work items (token rows x steps) behind which the product starts early
 
 // Two ways to the activation tile.  PRE: converted once per call by
 // t158_act_tiles_kernel into a workspace, one bulk copy per stage; else
@@ -235,6 +236,10 @@ __device__ __forceinline__ void tm_put_row(uint8_t *tile, const uint32_t (&in)[2
 // a warp's 32 rows make 4 runs of 128 contiguous bytes per store.
 __global__ void __launch_bounds__(256) t158_act_tiles_kernel(const int8_t *__restrict__ xq, int M, int K, int T,
                                                              int tiles_m, int nsteps, uint8_t *__restrict__ out) {
+    // the product kernel after this one may start its weight decode now; the
+    // codes are read only after the kernel that wrote them has completed
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (int64_t)tiles_m * T * nsteps) return;
     const int r = (int)(idx % T);
@@ -376,6 +381,10 @@ template <int MODE>
 __global__ void __launch_bounds__(kQtThreads) t158_quant_tiles_kernel(QtArgs a) {
     extern __shared__ float qt_row[];  // prologues: [K] the row, then [next_pow2(K)] scratch (kQtNorm)
     __shared__ float red[32];
+    // the product kernel after this one may start its weight decode now; the
+    // inputs are read only after the kernel that wrote them has completed
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int m = blockIdx.x, K = a.K;
     const bool real = m < a.M;
     const float *row = nullptr;
@@ -554,13 +563,24 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         }
         cp_async_commit();
     };
+    // Programmatic dependent launch: the next kernel on the stream may start
+    // its set-up now.  The packed weights and their scale are read-only
+    // inputs, so their copies start at once; the activations (codes, tiles,
+    // scales) are read, and y and acc written, only after the previous kernel
+    // on the stream has completed (griddepcontrol.wait).  With the tile
+    // images (PRE) only the copy warp (which also loads the scales) waits, so
+    // the weight decode of the first steps overlaps the kernel that wrote the
+    // tiles; otherwise the converters read the codes and wait too.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!PRE) asm volatile("griddepcontrol.wait;" ::: "memory");
     // the first copies go out before anything else
     if (tid < kTmConv) {
 #pragma unroll
         for (int s = 0; s < R - 1; s++) fetch(s_lo + s);
     }
-    // the tile's activation scales: loaded now, stored for the epilogue after the K loop
-    const float xs_own = (tid < T && m0 + tid < M) ? xs[m0 + tid] : 0.0f;
+    // the tile's activation scales (without tile images): loaded now, stored for the
+    // epilogue after the K loop; with them the copy warp stores them
+    const float xs_own = (!PRE && tid < T && m0 + tid < M) ? xs[m0 + tid] : 0.0f;
     const uint32_t ncols = tm_cols(T, PRE);
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&C.tmem)),
@@ -607,6 +627,10 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     } else if (warp == kTmConv / 32 + 1) {
         // ---- copy warp (PRE): lane 0 brings each step's activation tile in
         // with one bulk copy once the MMAs that read the stage before are done
+        if (PRE) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");  // the tile images and the scales are written
+            for (int t = lane; t < T; t += 32) C.xs[t] = m0 + t < M ? xs[m0 + t] : 0.0f;  // read after the barriers below
+        }
         if (PRE && lane == 0) {
             const uint8_t *src = tiles + ((int64_t)blockIdx.y * nsteps + s_lo) * bstage;
             for (int i = 0; i < nst && !*abort; i++) {
@@ -673,7 +697,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         }
         cp_async_wait_pending<0>();
     }
-    if (tid < T) C.xs[tid] = xs_own;  // read after the barriers below
+    if (!PRE && tid < T) C.xs[tid] = xs_own;  // read after the barriers below
     // the last commit covers every MMA issued before it
     __syncthreads();
     const int issued = C.issued;
@@ -684,6 +708,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     __syncthreads();
     const bool ok = !*abort && issued == nst;
     tc_fence_after();
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // y and acc may be read by the previous kernel until it ends
 
     const float nanv = ok ? 0.0f : __int_as_float(0x7fc00000);  // a wait that gave up: the tile reads NaN
     float *const part = reinterpret_cast<float *>(tm_smem + kTmCtl);
@@ -846,9 +871,14 @@ static qlin_status tm_launch_smem(int T, size_t *out) {
     return QLIN_OK;
 }
 
+// early: launch with programmatic stream serialisation, so that the weight
+// decode of the first steps overlaps the kernel before (the tile
+// conversion).  Measured on the decoder's shapes: a win except behind a
+// large conversion (512 tokens x 6912 inputs), where the early CTAs slow the
+// conversion down more than they gain.
 template <bool PRE>
 static qlin_status launch_tm(const int8_t *xq, const uint8_t *tiles, const float *xs, TmMats mats, float ws,
-                             int M, int K, int tiles_m, int T, cudaStream_t st) {
+                             int M, int K, int tiles_m, int T, cudaStream_t st, bool early = true) {
     size_t smem = 0;
     if (qlin_status e = tm_launch_smem<PRE>(T, &smem)) return e;
     mats.tile0[0] = 0;
@@ -872,13 +902,15 @@ static qlin_status launch_tm(const int8_t *xq, const uint8_t *tiles, const float
     cfg.blockDim = dim3(kTmThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = (unsigned)split;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = early ? 2 : 1;
     QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tm_kernel<PRE>, xq, tiles, xs, mats, ws, M, K, T, split));
     QLIN_LAUNCHED("t158_tm_kernel");
     return QLIN_OK;
@@ -901,11 +933,17 @@ qlin_status t158_linear_tensor_cores(const int8_t *xq, const float *xs, const ui
     if (convert) {
         const int nsteps = (K + kTcKS - 1) / kTcKS;
         const int64_t threads = (int64_t)tiles_m * T * nsteps;
-        t158_act_tiles_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(xq, M, K, T, tiles_m, nsteps,
-                                                                                 (uint8_t *)work);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
+        cfg.blockDim = dim3(256);
+        cfg.stream = st;
+        // launched after the previous kernel ends; it lets the product start at once
+        QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_act_tiles_kernel, xq, M, K, T, tiles_m, nsteps, (uint8_t *)work));
         QLIN_LAUNCHED("t158_act_tiles_kernel");
     }
-    return launch_tm<true>(xq, (const uint8_t *)work, xs, mats, ws, M, K, tiles_m, T, st);
+    // behind a large tile conversion the product does not start early (see launch_tm)
+    const bool early = !convert || (int64_t)tiles_m * T * ((K + kTcKS - 1) / kTcKS) <= kTmEarlyMaxItems;
+    return launch_tm<true>(xq, (const uint8_t *)work, xs, mats, ws, M, K, tiles_m, T, st, early);
 }
 
 // Linears j = 0 .. count - 1 on one set of activation tiles (already in work,
@@ -942,7 +980,13 @@ static qlin_status launch_qt(QtArgs a, void *work, cudaStream_t st) {
     QLIN_REQUIRE(a.xq || work, QLIN_ERR_INVALID_ARG, "quantiser: neither codes nor tiles requested");
     if (smem > 48 * 1024) blocks_per_sm((const void *)t158_quant_tiles_kernel<MODE>, smem);
     const unsigned grid = (unsigned)(work ? tiles_m * T : a.M);
-    t158_quant_tiles_kernel<MODE><<<grid, kQtThreads, smem, st>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kQtThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    // launched after the previous kernel ends; it lets the product start at once
+    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_quant_tiles_kernel<MODE>, a));
     QLIN_LAUNCHED("t158_quant_tiles_kernel");
     return QLIN_OK;
 }

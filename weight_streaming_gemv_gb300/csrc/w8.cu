@@ -244,9 +244,11 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
     const int ntiles = (int)((r1 - r0 + TR - 1) / TR);
     // Programmatic dependent launch: the next kernel on the stream may start its
     // own set-up now.  The weights (and group scales) are read-only inputs, so
-    // the first stages of their stream go out at once; this kernel waits for
-    // the previous one to complete (and its writes to be visible) before it
-    // reads x or writes y.
+    // the first tile of their stream goes out before this kernel waits for the
+    // previous one to complete (and its writes to be visible); x is read and y
+    // written after the wait.  The other stages go out after the x loads, so
+    // that those few loads do not queue behind the stream (issuing all of
+    // them first measured 6% slower).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint64_t pol = l2_evict_first();
     auto issue = [&](int t) {
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
     };
     if (threadIdx.x == 0) {
         ring->init(kW8Warps);
-        for (int t = 0; t < min(ntiles, kW8Stages); t++) issue(t);
+        if (ntiles > 0) issue(0);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // consumers: this lane's x slice
@@ -297,6 +299,8 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
     }
     // the loads are in flight; one barrier (the ring is initialised), then the rest of the stream
     __syncthreads();
+    if (threadIdx.x == 0)
+        for (int t = 1; t < min(ntiles, kW8Stages); t++) issue(t);
 
     if (warp == 0) {
         if (lane != 0) return;
