@@ -909,8 +909,9 @@ static qlin_status launch_tm(const int8_t *xq, const uint8_t *tiles, const float
     attr[0].val.clusterDim.z = (unsigned)split;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = early ? 2 : 1;
+    // without a K split no cluster is needed: a plain grid launch
+    cfg.attrs = split > 1 ? attr : attr + 1;
+    cfg.numAttrs = (split > 1 ? 1 : 0) + (early ? 1 : 0);
     QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tm_kernel<PRE>, xq, tiles, xs, mats, ws, M, K, T, split));
     QLIN_LAUNCHED("t158_tm_kernel");
     return QLIN_OK;
