@@ -288,6 +288,33 @@ def test_t158_tensor_core_extreme_operands(dev):
     _t158_case(dev, M, K, N, seed=14, trits=t, xq=xq)
 
 
+def test_t158_ws_one_workspace_for_many_calls(dev):
+    """One workspace of the largest size, filled with stale bytes, serves
+    calls of several M and K in a row, twice over, bit for bit against the
+    oracle."""
+    import torch
+    from weight_streaming_gemv_gb300 import qlin
+
+    shapes = [(512, 1152, 6912), (40, 6912, 1152), (8, 1152, 700), (130, 333, 2000)]
+    nb = max(qlin.qlin_t158_i8_workspace_size(M, K) for M, K, _ in shapes)
+    work = torch.full((nb,), 0x7f, dtype=torch.uint8, device=dev)
+    cases = []
+    for i, (M, K, N) in enumerate(shapes):
+        d = synth.t158_gemv(50 + i, M, K, N)
+        xq_o, xs_o = oracle.quant_i8(d["x"])
+        acc_o, y_o = oracle.t158_linear(xq_o, xs_o, oracle.t158_pack(d["trits"]), d["w_scale"], K)
+        pitch = qlin.t158_pitch(K)
+        w = torch.from_numpy(qlin.t158_pack(d["trits"], pitch)).to(dev)
+        cases.append((M, K, N, pitch, w, to_dev(xq_o, dev), to_dev(xs_o, dev), d["w_scale"], acc_o, y_o))
+    for _ in range(2):
+        for M, K, N, pitch, w, xq, xs, ws, acc_o, y_o in cases:
+            y = _empty((M, N), torch.float32, dev)
+            acc = _empty((M, N), torch.int32, dev)
+            qlin.qlin_t158_i8_ws(xq, xs, w, pitch, ws, y, acc, M, N, K, work, nb)
+            np.testing.assert_array_equal(host(acc), acc_o)
+            np.testing.assert_array_equal(host(y), y_o)
+
+
 def test_t158_ws_rejects_small_workspace(dev):
     import torch
     from weight_streaming_gemv_gb300 import qlin
