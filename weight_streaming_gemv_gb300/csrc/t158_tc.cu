@@ -41,11 +41,15 @@
 // outputs of each token.  Split K: a cluster of CTAs over one tile, each over
 // its own K steps, adds the partial tiles through distributed shared memory in
 // rank order.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <type_traits>
 
 #include "common.cuh"
 #include "decode_ops.cuh"
@@ -497,16 +501,27 @@ struct TmMats {
     int N[kTmMaxMats];
     int tile0[kTmMaxMats + 1];
     int count;
+    int y_maps;  // bit j: y[j] is written through ymaps.m[j] (tile staged in shared memory, one tensor store)
+};
+
+// Tensor maps of the outputs y[j]: fp32 [M][N[j]], boxes of kTmRows outputs
+// x T tokens, no swizzle.
+struct alignas(64) TmYMaps {
+    CUtensorMap m[kTmMaxMats];
+};
+struct TmNoMaps {  // the launches that store y directly (a K split) carry no maps
+    int unused;
 };
 
 // Grid: (weight-row tiles, token tiles, split); a cluster is the `split` CTAs
 // of one tile, each over its own range of K steps.  split == 1: no cluster
 // reduction.  T: tokens per tile (a multiple of 32, at most kTmMaxTok).
 // PRE: `tiles` holds the activation tiles written by t158_act_tiles_kernel.
-template <bool PRE>
+template <bool PRE, bool YT>
 __global__ void __launch_bounds__(kTmThreads, 1)
     t158_tm_kernel(const int8_t *__restrict__ xq, const uint8_t *__restrict__ tiles, const float *__restrict__ xs,
-                   const TmMats mats, float ws_arg, int M, int K, int T, int split) {
+                   const TmMats mats, const __grid_constant__ typename std::conditional<YT, TmYMaps, TmNoMaps>::type ymaps,
+                   float ws_arg, int M, int K, int T, int split) {
     constexpr int S = tm_stages(PRE), R = tm_raws(PRE);
     int mj = 0;  // this CTA's matrix
     while (mj + 1 < mats.count && (int)blockIdx.x >= mats.tile0[mj + 1]) mj++;
@@ -712,27 +727,66 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 
     const float nanv = ok ? 0.0f : __int_as_float(0x7fc00000);  // a wait that gave up: the tile reads NaN
     float *const part = reinterpret_cast<float *>(tm_smem + kTmCtl);
+    // Without a K split, y leaves as one tensor store of the tile, staged in
+    // shared memory as [token][row] (the stages' space, free now): one 4-byte
+    // shared store per value instead of a global store with its address.
+    const bool y_tma = YT && split == 1 && y && ((mats.y_maps >> mj) & 1) && (smem_addr(part) & 127u) == 0;
     if (warp < kTmConv / 32) {
         // warp w: weight rows 32 (w % 4) .. + 31 (its lanes), tokens T/2 (w / 4) .. + T/2 - 1
         const int n = n0 + wrow;
         const int tb = (warp >> 2) * (T / 2);
-        for (int t0 = tb; t0 < tb + T / 2; t0 += 16) {
-            uint32_t r[16];
-            tm_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)t0, r);
+        const int nch = T / 32;  // 16-column loads of this warp's T/2 tokens (1..4)
+        // two loads go out before each wait
+#pragma unroll 1
+        for (int k2 = 0; k2 < nch; k2 += 2) {
+        uint32_t r[2][16];
+#pragma unroll
+        for (int k = 0; k < 2; k++)
+            if (k2 + k < nch) tm_ld16_nw(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(tb + 16 * (k2 + k)), r[k]);
+#pragma unroll
+        for (int k = 0; k < 2; k++)
+            if (k2 + k < nch) tm_wait_ld(r[k]);
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+            if (k2 + k >= nch) break;
+            const int t0 = tb + 16 * (k2 + k);
             if (split == 1) {
-                if (n < N) {
+                if (y_tma) {  // rows past N and tokens past M are clipped by the store
+                    // the scales first: a store into the stage may alias them for the
+                    // compiler, which would otherwise wait out each load in turn
+                    float xk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; j++) xk[j] = C.xs[t0 + j];
+#pragma unroll
+                    for (int j = 0; j < 16; j++)
+                        part[(t0 + j) * kTmRows + wrow] =
+                            __fadd_rn(__fmul_rn(__fmul_rn(__uint_as_float(r[k][j]), ws), xk[j]), nanv);
+                }
+                if (n < N && (acc_out || (y && !y_tma))) {
 #pragma unroll
                     for (int j = 0; j < 16; j++) {
                         const int m = m0 + t0 + j;
                         if (m >= M) break;
-                        const float v = __uint_as_float(r[j]);
+                        const float v = __uint_as_float(r[k][j]);
                         if (acc_out) acc_out[(int64_t)m * N + n] = __float2int_rz(v);
-                        if (y) y[(int64_t)m * N + n] = __fadd_rn(__fmul_rn(__fmul_rn(v, ws), C.xs[t0 + j]), nanv);
+                        if (y && !y_tma) y[(int64_t)m * N + n] = __fadd_rn(__fmul_rn(__fmul_rn(v, ws), C.xs[t0 + j]), nanv);
                     }
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 16; j++) part[(t0 + j) * kTmPStride + wrow] = __uint_as_float(r[j]);
+                for (int j = 0; j < 16; j++) part[(t0 + j) * kTmPStride + wrow] = __uint_as_float(r[k][j]);
+            }
+        }
+        }
+        if (y_tma) {
+            fence_proxy_async_smem();  // the staged tile, visible to the tensor store
+            asm volatile("bar.sync 2, %0;" ::"n"(kTmConv) : "memory");
+            if constexpr (YT) {
+                if (tid == 0) {
+                    tma_store_2d(&ymaps.m[mj], part, n0, m0);
+                    bulk_commit_group();
+                    bulk_wait_read_all();  // the shared memory is read before the CTA can leave
+                }
             }
         }
     }
@@ -804,6 +858,45 @@ size_t t158_tc_workspace_bytes(int M, int K) {
     return (size_t)tiles_m * (size_t)((K + kTcKS - 1) / kTcKS) * (size_t)tm_b_bytes(T);
 }
 
+// The tensor map of an output y: fp32 [M][N] (N a multiple of 4, y 16-byte
+// aligned), boxes of kTmRows outputs x T tokens, no swizzle.  Encoded through
+// the driver entry point (no link against the driver library); recent maps
+// are kept for the next call on the same output.
+static qlin_status tm_y_map(float *y, int M, int N, int T, CUtensorMap *out) {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::map<std::tuple<int, const void *, int, int, int>, CUtensorMap> cache;
+    int dev = 0;
+    QLIN_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(mu);
+    const auto key = std::make_tuple(dev, (const void *)y, M, N, T);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *out = it->second;
+        return QLIN_OK;
+    }
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        QLIN_CUDA(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
+        QLIN_REQUIRE(fn && q == cudaDriverEntryPointSuccess, QLIN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+        encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    const cuuint64_t gdim[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    const cuuint64_t gstride[1] = {(cuuint64_t)N * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)kTmRows, (cuuint32_t)T};
+    const cuuint32_t estride[2] = {1, 1};
+    CUtensorMap m;
+    const CUresult r = encode(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, gdim, gstride, box, estride,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    QLIN_REQUIRE(r == CUDA_SUCCESS, QLIN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    if (cache.size() >= 256) cache.clear();
+    cache[key] = m;
+    *out = m;
+    return QLIN_OK;
+}
+
 // Clusters of `c` CTAs of this kernel with `smem` bytes each that can be
 // resident at once (cached).
 template <bool PRE>
@@ -827,7 +920,7 @@ static int tm_resident_clusters(int c, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, t158_tm_kernel<PRE>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, t158_tm_kernel<PRE, false>, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         n = 0;
     }
@@ -861,9 +954,10 @@ static qlin_status tm_launch_smem(int T, size_t *out) {
     const size_t floor_smem = (size_t)(sm_smem / (fit + 1) - reserved + 16) / 16 * 16 + 16;
     if (smem < floor_smem) smem = floor_smem;
     QLIN_REQUIRE((int)smem <= max_smem_optin(), QLIN_ERR_UNSUPPORTED, "qlin_t158_i8: tensor-core tile does not fit");
-    blocks_per_sm((const void *)t158_tm_kernel<PRE>, smem);  // raises the dynamic shared-memory limit
+    blocks_per_sm((const void *)t158_tm_kernel<PRE, false>, smem);  // raises the dynamic shared-memory limit
+    blocks_per_sm((const void *)t158_tm_kernel<PRE, true>, smem);
     int resident = 0;
-    QLIN_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, t158_tm_kernel<PRE>, kTmThreads, smem));
+    QLIN_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, t158_tm_kernel<PRE, false>, kTmThreads, smem));
     QLIN_REQUIRE(resident >= 1 && resident <= fit, QLIN_ERR_UNSUPPORTED,
                  "qlin_t158_i8: %d CTAs per SM would exceed tensor memory (%d fit)", resident, fit);
     cache[{dev, T}] = smem;
@@ -881,6 +975,7 @@ static qlin_status launch_tm(const int8_t *xq, const uint8_t *tiles, const float
                              int M, int K, int tiles_m, int T, cudaStream_t st, bool early = true) {
     size_t smem = 0;
     if (qlin_status e = tm_launch_smem<PRE>(T, &smem)) return e;
+    mats.y_maps = 0;
     mats.tile0[0] = 0;
     for (int j = 0; j < mats.count; j++) mats.tile0[j + 1] = mats.tile0[j] + (mats.N[j] + kTmRows - 1) / kTmRows;
     for (int j = mats.count + 1; j <= kTmMaxMats; j++) mats.tile0[j] = mats.tile0[mats.count];
@@ -912,7 +1007,22 @@ static qlin_status launch_tm(const int8_t *xq, const uint8_t *tiles, const float
     // without a K split no cluster is needed: a plain grid launch
     cfg.attrs = split > 1 ? attr : attr + 1;
     cfg.numAttrs = (split > 1 ? 1 : 0) + (early ? 1 : 0);
-    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tm_kernel<PRE>, xq, tiles, xs, mats, ws, M, K, T, split));
+    if (split == 1) {
+        // y through tensor stores where its layout allows (16-byte rows)
+        TmYMaps ymaps;
+        memset(&ymaps, 0, sizeof(ymaps));
+        for (int j = 0; j < mats.count; j++)
+            if (mats.y[j] && (reinterpret_cast<uintptr_t>(mats.y[j]) & 15) == 0 && mats.N[j] % 4 == 0) {
+                if (qlin_status e = tm_y_map(mats.y[j], M, mats.N[j], T, &ymaps.m[j])) return e;
+                mats.y_maps |= 1 << j;
+            }
+        if (mats.y_maps) {
+            QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tm_kernel<PRE, true>, xq, tiles, xs, mats, ymaps, ws, M, K, T, split));
+            QLIN_LAUNCHED("t158_tm_kernel");
+            return QLIN_OK;
+        }
+    }
+    QLIN_CUDA(cudaLaunchKernelEx(&cfg, t158_tm_kernel<PRE, false>, xq, tiles, xs, mats, TmNoMaps{0}, ws, M, K, T, split));
     QLIN_LAUNCHED("t158_tm_kernel");
     return QLIN_OK;
 }
