@@ -42,9 +42,9 @@ __device__ __forceinline__ void tm_st16(uint32_t taddr, const uint32_t (&v)[16])
         : "memory");
 }
 __device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-// 16 consecutive accumulator columns of this thread's tensor-memory lane
-// The same load without its wait: several loads go out together, then
-// tm_wait_ld before any of their registers is read.
+// 16 consecutive accumulator columns of this thread's tensor-memory lane,
+// without the wait: several loads go out together, then tm_wait_ld before any
+// of their registers is read.
 __device__ __forceinline__ void tm_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -62,6 +62,7 @@ __device__ __forceinline__ void tm_wait_ld(uint32_t (&r)[16]) {
                  :
                  : "memory");
 }
+// the same load followed by its wait
 __device__ __forceinline__ void tm_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
