@@ -111,13 +111,13 @@ qlin_status qlin_quant_i8(const float *x, int8_t *xq, float *x_scale, int M, int
  * codes and trits are fp16 integers and every partial sum stays below
  * 127 K < 2^24): the same acc and y, bit for bit.  Below 8 tokens the
  * CUDA-core kernel runs, except for rows too long for its activation planes
- * in shared memory, which take the tensor-core path as well.  The
- * tensor-core kernel is launched with programmatic stream serialisation
- * (except behind a large activation-tile conversion): it may start while the
- * previous kernel on the stream finishes and decodes its first weight steps
- * at once (the packed weights and their scale are taken to be read-only
- * inputs); it reads the activations and their scales, and writes y and acc,
- * only after that kernel has completed.
+ * in shared memory, which take the tensor-core path as well.  Both kernels
+ * are launched with programmatic stream serialisation (the tensor-core one
+ * except behind a large activation-tile conversion): each may start while the
+ * previous kernel on the stream finishes and begins its weight reads at once
+ * (the packed weights and their scale are taken to be read-only inputs); it
+ * reads the activations and their scales, and writes y and acc, only after
+ * that kernel has completed.
  * ====================================================================== */
 qlin_status qlin_t158_i8(const int8_t *xq, const float *x_scale, const uint8_t *w_packed, int64_t w_pitch,
                          float w_scale, float *y, int32_t *acc, int M, int N, int K, qlin_stream_t stream);

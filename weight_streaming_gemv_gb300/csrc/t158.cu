@@ -126,13 +126,13 @@ __global__ void __launch_bounds__(256) t158_gemv_kernel(const int8_t *__restrict
     const int warps = blockDim.x >> 5;
     const int64_t gwarp = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * warps;
-    // Programmatic dependent launch: a following kernel launched that way may
-    // start its set-up now.  The packed weights are read-only inputs, so the
-    // first chunks are requested before the wait; the activations, their
-    // scales and the weight scale are read, and y written, only after the
-    // previous kernel on the stream has completed (griddepcontrol.wait, which
-    // returns at once for a plain launch).
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Programmatic dependent launch: the packed weights are read-only inputs,
+    // so the first chunks are requested before the wait; the activations,
+    // their scales and the weight scale are read, and y written, only after
+    // the previous kernel on the stream has completed (griddepcontrol.wait).
+    // The next kernel may launch once every CTA has begun its last row pass
+    // (below): launched at the start instead, its early reads slowed these
+    // latency-bound calls down.
     uint4 nxt[R];  // the next chunk of each of the warp's R row slots
 #pragma unroll
     for (int r = 0; r < R; r++) {
@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(256) t158_gemv_kernel(const int8_t *__restrict
     __syncthreads();
 
     for (int64_t r0 = gwarp * ROWS; r0 < N; r0 += nwarps * ROWS) {
+        if (r0 + nwarps * ROWS >= N) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         int acc[R][MT];
 #pragma unroll
         for (int r = 0; r < R; r++)
@@ -272,10 +273,15 @@ static qlin_status launch_t158(const int8_t *xq, const float *xs, const uint8_t 
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    // A plain launch: with programmatic stream serialisation the next call's
-    // early weight reads slowed these latency-bound calls down (6912 -> 1152 at
-    // one token: 3.9 -> 6.3 us).  The kernel still lets a following
-    // programmatic launch start early.
+    // Programmatic stream serialisation: the launch and the first weight reads
+    // overlap the previous kernel's last row passes (6912 -> 1152 at one
+    // token: 3.9 -> 3.4 us per call in a graph of back-to-back calls; with the
+    // kernel's trigger at its start instead: 6.3 us).
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     QLIN_CUDA(cudaLaunchKernelEx(&cfg, kern, xq, xs, w, pitch, ws, ws_ptr, y, acc, M, N, K));
     QLIN_LAUNCHED("t158_gemv_kernel");
     return QLIN_OK;

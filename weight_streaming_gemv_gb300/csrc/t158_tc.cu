@@ -506,7 +506,7 @@ struct TmMats {
 
 // Tensor maps of the outputs y[j]: fp32 [M][N[j]], boxes of kTmRows outputs
 // x T tokens, no swizzle.
-struct alignas(64) TmYMaps {
+struct TmYMaps {
     CUtensorMap m[kTmMaxMats];
 };
 struct TmNoMaps {  // the launches that store y directly (a K split) carry no maps
