@@ -166,7 +166,10 @@ __global__ void __launch_bounds__(256) w8_gemv_kernel(const float *__restrict__ 
 // ---------------------------------------------------------------- S5 GEMV, one token, TMA streaming
 // One CTA per SM over a contiguous run of rows.  Lane 0 of warp 0 streams the
 // run as tiles of TR whole rows (one bulk copy each: rows are contiguous)
-// through a ring of kW8Stages shared-memory slots; an mbarrier per slot counts
+// through a ring of S shared-memory slots (3 or 4: the count that keeps the
+// more bytes in flight within half an SM's shared memory, for the row length;
+// five slots of 22 KB measured slower than four);
+// an mbarrier per slot counts
 // the bytes in, another counts the consumer warps out.
 //
 // The consumers never widen a weight.  Each lane holds its slice of x (at most
@@ -185,42 +188,55 @@ __global__ void __launch_bounds__(256) w8_gemv_kernel(const float *__restrict__ 
 // consumers meet at a named barrier and one warp adds the KS partials of each
 // row in a fixed order, so the result does not depend on timing.
 constexpr int kW8Warps = 8;    // consumer warps
-constexpr int kW8Stages = 3;  // 3 slots of <= 32 KB: two CTAs fit on an SM, so the next call's can wait there
+constexpr int kW8MinStages = 3, kW8MaxStages = 4;  // slots of <= 32 KB within half an SM: two CTAs fit on an SM
 constexpr int kW8JMax = 4;     // chunks per lane: C <= 32 * 8 * 4 (K <= 16384)
 constexpr int kW8MaxTR = 32;   // rows per tile
 
 struct W8Smem {
     int slot, tr, ks, xoff, total;  // slots at 0, then (at xoff) the ring and the partials
+    int stages;                     // slots in the ring
     int sslot, soff;                // group scales: a slot of sslot bytes per stage at soff (0 without groups)
 };
 
 // s_pitch: floats per row of group scales (0: one scale for the tensor)
-__host__ __device__ inline W8Smem w8_stream_layout(int64_t pitch, int smem_optin, int64_t s_pitch = 0) {
+__host__ __device__ inline W8Smem w8_stream_layout_s(int64_t pitch, int smem_optin, int64_t s_pitch, int stages) {
     W8Smem L;
+    L.stages = stages;
     const int C = (int)(pitch / 16);
     L.ks = 1;  // the fewest K parts that leave at most kW8JMax chunks per lane
     while (L.ks < kW8Warps && (C + L.ks * 32 - 1) / (L.ks * 32) > kW8JMax) L.ks *= 2;
     const int rstep = 2 * (kW8Warps / L.ks);  // a tile holds whole row pairs of every group
-    const int fixed = (int)(sizeof(Ring<kW8Stages>) + 2 * kW8MaxTR * kW8Warps * sizeof(float)) + 256;
+    const int fixed = (int)(sizeof(Ring<kW8MaxStages>) + 2 * kW8MaxTR * kW8Warps * sizeof(float)) + 256;
     // weight tiles of up to 32 KB, group scales (4 s_pitch bytes a row) beside
     // them, all within half the shared memory so that two CTAs fit on an SM
     const int budget = smem_optin / 2 - 1024 - fixed;
-    int slot = budget / kW8Stages;
+    int slot = budget / stages;
     slot = slot > 32768 ? 32768 : slot;
     slot = slot / 128 * 128;  // so that the rounded-up tile below stays within it
     int tr = (int)(slot / pitch);
     tr = tr > kW8MaxTR ? kW8MaxTR : tr;
     tr = tr / rstep * rstep;
-    while (tr > 0 && kW8Stages * (((tr * pitch + 127) / 128 + (tr * 4 * s_pitch + 127) / 128) * 128) > budget)
+    while (tr > 0 && stages * (((tr * pitch + 127) / 128 + (tr * 4 * s_pitch + 127) / 128) * 128) > budget)
         tr -= rstep;
     L.tr = tr;
     L.slot = (int)((tr * pitch + 127) / 128 * 128);
     L.sslot = (int)((tr * 4 * s_pitch + 127) / 128 * 128);
-    L.soff = kW8Stages * L.slot;
-    L.xoff = kW8Stages * (L.slot + L.sslot);
+    L.soff = stages * L.slot;
+    L.xoff = stages * (L.slot + L.sslot);
     L.total = L.xoff + fixed;
     if ((C + L.ks * 32 - 1) / (L.ks * 32) > kW8JMax) L.tr = 0;  // K too large for this kernel
     return L;
+}
+
+// The ring with the most bytes in flight (stages x slot) that holds at least
+// one row per tile; ties go to fewer stages.
+inline W8Smem w8_stream_layout(int64_t pitch, int smem_optin, int64_t s_pitch = 0) {
+    W8Smem best = w8_stream_layout_s(pitch, smem_optin, s_pitch, kW8MinStages);
+    for (int st = kW8MinStages + 1; st <= kW8MaxStages; st++) {
+        const W8Smem L = w8_stream_layout_s(pitch, smem_optin, s_pitch, st);
+        if (L.tr >= 1 && (best.tr < 1 || (int64_t)st * L.slot > (int64_t)best.stages * best.slot)) best = L;
+    }
+    return best;
 }
 
 // 2^e for -126 <= e <= 127
@@ -228,7 +244,7 @@ __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) 
 
 // GROUPED: group scales `scales` [N][s_pitch], one per G weights of a row;
 // otherwise one scale s of the whole tensor (scales unused)
-template <bool GROUPED>
+template <bool GROUPED, int S>
 __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const float *__restrict__ x,
                                                                          const int8_t *__restrict__ w, int64_t pitch,
                                                                          float s, float *__restrict__ y, int N, int K,
@@ -236,8 +252,8 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
                                                                          int64_t s_pitch, int G) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *slots = smem;
-    Ring<kW8Stages> *ring = reinterpret_cast<Ring<kW8Stages> *>(smem + L.xoff);
-    float *part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ring) + sizeof(Ring<kW8Stages>));
+    Ring<S> *ring = reinterpret_cast<Ring<S> *>(smem + L.xoff);  // within the fixed part sized for kW8MaxStages
+    float *part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ring) + sizeof(Ring<S>));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = (int)(pitch / 16), TR = L.tr, KS = L.ks;
     const int64_t r0 = (int64_t)N * blockIdx.x / gridDim.x, r1 = (int64_t)N * (blockIdx.x + 1) / gridDim.x;
@@ -252,7 +268,7 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint64_t pol = l2_evict_first();
     auto issue = [&](int t) {
-        const int st = t % kW8Stages;
+        const int st = t % S;
         const int64_t row = r0 + (int64_t)t * TR;
         const int64_t nr = min((int64_t)TR, r1 - row);
         const uint32_t bytes = (uint32_t)(nr * pitch), sbytes = GROUPED ? (uint32_t)(nr * 4 * s_pitch) : 0u;
@@ -300,17 +316,17 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
     // the loads are in flight; one barrier (the ring is initialised), then the rest of the stream
     __syncthreads();
     if (threadIdx.x == 0)
-        for (int t = 1; t < min(ntiles, kW8Stages); t++) issue(t);
+        for (int t = 1; t < min(ntiles, S); t++) issue(t);
 
     if (warp == 0) {
         if (lane != 0) return;
-        int t = min(ntiles, kW8Stages);
+        int t = min(ntiles, S);
         for (; t < ntiles; t++) {
-            if (!mbar_wait(&ring->empty[t % kW8Stages], ((t / kW8Stages) - 1) & 1)) break;
+            if (!mbar_wait(&ring->empty[t % S], ((t / S) - 1) & 1)) break;
             issue(t);
         }
         // every copy issued must have landed before the CTA leaves
-        for (int u = max(0, t - kW8Stages); u < t; u++) mbar_wait(&ring->full[u % kW8Stages], (u / kW8Stages) & 1);
+        for (int u = max(0, t - S); u < t; u++) mbar_wait(&ring->full[u % S], (u / S) & 1);
         return;
     }
 
@@ -368,8 +384,8 @@ __global__ void __launch_bounds__(32 * (kW8Warps + 1), 2) w8_stream_kernel(const
 
     bool ok = true;
     for (int t = 0; t < ntiles; t++) {
-        const int st = t % kW8Stages;
-        if (ok && !__all_sync(0xffffffffu, mbar_wait(&ring->full[st], (t / kW8Stages) & 1))) ok = false;
+        const int st = t % S;
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(&ring->full[st], (t / S) & 1))) ok = false;
         const int64_t row0 = r0 + (int64_t)t * TR;
         const int rows = (int)min((int64_t)TR, r1 - row0);
         float *pt = part + (size_t)(t & 1) * kW8MaxTR * kW8Warps;
@@ -449,6 +465,34 @@ size_t w8_tc_workspace_bytes(int M, int K);
 qlin_status w8_linear_tensor_cores_ws(const float *x, const int8_t *w8, int64_t pitch, float s, float *y, int M,
                                       int N, int K, void *work, cudaStream_t st);
 
+// The one-token stream kernel for layout L (its ring depth picks the
+// instantiation), launched with programmatic stream serialisation.
+template <bool GROUPED, int S>
+static qlin_status launch_stream_s(const float *x, const int8_t *w, int64_t pitch, float s, float *y, int N, int K,
+                                   const W8Smem &L, const float *scales, int64_t s_pitch, int G, cudaStream_t st) {
+    const int per_sm = blocks_per_sm((const void *)w8_stream_kernel<GROUPED, S>, L.total);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sm_count() * std::min(per_sm, 2)));
+    cfg.blockDim = dim3(32 * (kW8Warps + 1));
+    cfg.dynamicSmemBytes = (size_t)L.total;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    QLIN_CUDA(cudaLaunchKernelEx(&cfg, w8_stream_kernel<GROUPED, S>, x, w, pitch, s, y, N, K, L, scales, s_pitch, G));
+    QLIN_LAUNCHED("w8_stream_kernel");
+    return QLIN_OK;
+}
+template <bool GROUPED>
+static qlin_status launch_stream(const float *x, const int8_t *w, int64_t pitch, float s, float *y, int N, int K,
+                                 const W8Smem &L, const float *scales, int64_t s_pitch, int G, cudaStream_t st) {
+    static_assert(kW8MinStages == 3 && kW8MaxStages == 4, "instantiations");
+    if (L.stages == 4) return launch_stream_s<GROUPED, 4>(x, w, pitch, s, y, N, K, L, scales, s_pitch, G, st);
+    return launch_stream_s<GROUPED, 3>(x, w, pitch, s, y, N, K, L, scales, s_pitch, G, st);
+}
+
 template <int R, int MT>
 static qlin_status launch_w8(const float *x, const int8_t *w, int64_t pitch, float s, float *y, int M, int N, int K,
                              cudaStream_t st, const float *scales = nullptr, int64_t s_pitch = 0, int G = 0) {
@@ -505,23 +549,9 @@ qlin_status qlin_w8_f32(const float *x, const int8_t *w8, int64_t w_pitch, float
     cudaStream_t st = (cudaStream_t)stream;
     if (M == 1 && w_pitch <= 16 * 32 * qlin::kW8Warps * qlin::kW8JMax) {
         const qlin::W8Smem L = qlin::w8_stream_layout(w_pitch, qlin::max_smem_optin());
-        if (L.tr >= 1) {
-            const int per_sm = qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel<false>, L.total);
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)(qlin::sm_count() * std::min(per_sm, 2)));
-            cfg.blockDim = dim3(32 * (qlin::kW8Warps + 1));
-            cfg.dynamicSmemBytes = (size_t)L.total;
-            cfg.stream = st;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            QLIN_CUDA(cudaLaunchKernelEx(&cfg, qlin::w8_stream_kernel<false>, x, w8, w_pitch, w_scale, y, N, K, L,
-                                         (const float *)nullptr, (int64_t)0, 0));
-            QLIN_LAUNCHED("w8_stream_kernel");
-            return QLIN_OK;
-        }
+        if (L.tr >= 1)
+            return qlin::launch_stream<false>(x, w8, w_pitch, w_scale, y, N, K, L, (const float *)nullptr, (int64_t)0, 0,
+                                              st);
     }
     if (M == 1) return qlin::launch_w8<4, 1>(x, w8, w_pitch, w_scale, y, M, N, K, st);
     return qlin::w8_linear_tensor_cores(x, w8, w_pitch, w_scale, y, M, N, K, st);
@@ -580,23 +610,7 @@ qlin_status qlin_w8g_f32(const float *x, const int8_t *w8, int64_t w_pitch, cons
     cudaStream_t st = (cudaStream_t)stream;
     if (M == 1 && w_pitch <= 16 * 32 * qlin::kW8Warps * qlin::kW8JMax) {
         const qlin::W8Smem L = qlin::w8_stream_layout(w_pitch, qlin::max_smem_optin(), s_pitch);
-        if (L.tr >= 1) {
-            const int per_sm = qlin::blocks_per_sm((const void *)qlin::w8_stream_kernel<true>, L.total);
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)(qlin::sm_count() * std::min(per_sm, 2)));
-            cfg.blockDim = dim3(32 * (qlin::kW8Warps + 1));
-            cfg.dynamicSmemBytes = (size_t)L.total;
-            cfg.stream = st;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            QLIN_CUDA(cudaLaunchKernelEx(&cfg, qlin::w8_stream_kernel<true>, x, w8, w_pitch, 1.0f, y, N, K, L, scales,
-                                         s_pitch, G));
-            QLIN_LAUNCHED("w8_stream_kernel");
-            return QLIN_OK;
-        }
+        if (L.tr >= 1) return qlin::launch_stream<true>(x, w8, w_pitch, 1.0f, y, N, K, L, scales, s_pitch, G, st);
     }
     const size_t tile8_smem = (size_t)8 * ((K + 15) / 16) * 16 * sizeof(float);
     if (M == 1) return qlin::launch_w8<4, 1>(x, w8, w_pitch, 1.0f, y, M, N, K, st, scales, s_pitch, G);
