@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedA
     const int nc = A.pos / 32 + 1;
     const int cpos = A.pos / 32;
     int Q0, Q1;  // rows of the concatenation q | k | v owned by this CTA
-    share(qd + 2 * kvd, b, G, Q0, Q1);
+    qkv_share(qd, kvd, b, G, Q0, Q1);
 
     int sumx = 0;
     float xs = 0.0f;

@@ -187,6 +187,32 @@ __device__ __forceinline__ void share(int n, int b, int G, int &lo, int &hi) {
     hi = (int)((int64_t)n * (b + 1) / G);
 }
 
+// rows [lo, hi) of the concatenation q | k | v owned by CTA b of G: the CTAs
+// are dealt to the three matrices in proportion to their rows, so that no CTA
+// takes rows of two matrices (two items, two passes) and waits the hand-off
+// for the others (every matrix gets a CTA; with fewer CTAs, a plain split)
+__device__ __forceinline__ void qkv_share(int qd, int kvd, int b, int G, int &lo, int &hi) {
+    const int total = qd + 2 * kvd;
+    const int gq = (int)(((int64_t)G * qd + total / 2) / total), gk = (int)(((int64_t)G * kvd + total / 2) / total);
+    const int gv = G - gq - gk;
+    if (gq < 1 || gk < 1 || gv < 1) {
+        share(total, b, G, lo, hi);
+        return;
+    }
+    int base = 0;
+    if (b < gq) {
+        share(qd, b, gq, lo, hi);
+    } else if (b < gq + gk) {
+        share(kvd, b - gq, gk, lo, hi);
+        base = qd;
+    } else {
+        share(kvd, b - gq - gk, gv, lo, hi);
+        base = qd + kvd;
+    }
+    lo += base;
+    hi += base;
+}
+
 // ---------------------------------------------------------------- the byte ring
 // Every CTA streams its share of the step's data (weight rows, cached K/V
 // rows, lm_head rows) through one ring of kRingBytes of shared memory, as a
@@ -296,7 +322,7 @@ __device__ __forceinline__ void qkv_items(const FusedArgs &A, int l, int b, int 
     const int qd = m.n_heads * m.head_dim, kvd = m.n_kv_heads * m.head_dim;
     const int rows[3] = {qd, kvd, kvd};
     int lo, hi;
-    share(qd + 2 * kvd, b, G, lo, hi);
+    qkv_share(qd, kvd, b, G, lo, hi);
     int base = 0;
 #pragma unroll
     for (int j = 0; j < 3; j++) {
