@@ -57,7 +57,7 @@ def parse():
 # dram__bytes_write.sum from one ncu capture at context `pos`), valid only for
 # the kernel sources it was taken on: any change to them reports null.
 FUSED_SOURCES = ['decode_fused.cu', 'decode_fused.cuh', 'decode_ops.cuh', 'stream.cuh', 'common.cuh']
-FUSED_TRAFFIC = {"sha256": "65c78b27edad3cb6cdfa22700fa503ec99ddd7a2f8fe4d47a43a6364b0fb2a21", "bytes": 808675072, "pos": 1024}
+FUSED_TRAFFIC = {"sha256": "e1e4bf77c2f314a446fe017f44eca2c0419a5ed3b7c768b6b4b5678a0aa53be8", "bytes": 808881408, "pos": 1024}
 
 
 def fused_traffic():
